@@ -1,0 +1,437 @@
+"""Throughput of the fused lattice-Boltzmann step on GB300, in MLUPS.
+
+One benchmark step is one submission of the hot path: ``--lbm-steps`` time steps of the
+fused AA collide-and-stream kernel (alternating even and odd forms) followed by the
+diagnostics reduction (mass, momentum, solid force, wall heat flux) read back to the
+host.  MLUPS = cells x time steps / seconds / 1e6, counting every lattice cell (the
+MLUPS metric of the multi-GPU thermal LBM page; "cell updates per second" of the
+streaming-layout page).
+
+Legs, all printed on one JSON line by rank 0:
+  value         device-resident state, K timed steps between CUDA events (max over ranks)
+  roofline      the step kernel's achieved algorithmic bandwidth (bytes per cell update
+                x cells / average launch time) against the measured HBM copy bandwidth
+  e2e           the same metric through the C ABI with page-locked HOST fields: each
+                step uploads rho, u (T), initialises, steps, and writes rho, u (T) back
+  cpu_baseline  the fp64 oracle on the host cores on a bounded sample of the workload
+  secondary     the other workloads of the target (thermal cavities, 128^3) briefly
+
+``--impl reference`` times the oracle instead (the reference arm: a slow, plain CPU
+program on this machine's host cores), one bounded sample step per benchmark step.
+Multi-GPU runs (torchrun) are independent replicas, one per GPU ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLUPS at 1 GB300 (D3Q19 MRT fp32, AA) and % of HBM bandwidth roofline"
+UNIT = "MLUPS"
+
+# Algorithmic bytes per cell update: populations read once and written once, fp32.
+BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112}
+
+# DRAM bytes per cell update of the step kernel measured with ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum per launch / cells), with a hash of the kernel sources they were
+# taken on; reported as "traffic" only while the sources are unchanged.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lattice_boltzmann_cfd_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def make_workload(name: str):
+    from lattice_boltzmann_cfd_gb300 import workloads as W
+    table = {
+        "d3q19_mrt_periodic_512": lambda: W.random_periodic(n=512, seed=2),
+        "d3q19_mrt_periodic_128": lambda: W.random_periodic(n=128, seed=2),
+        "taylor_green_32": lambda: W.taylor_green(),
+        "channel_sphere_128": lambda: W.channel_sphere(),
+        "cavity2d_4096": lambda: W.cavity2d(),
+        "cavity3d_512": lambda: W.cavity3d(),
+    }
+    return table[name]()
+
+
+def workload_label(name, w=None) -> str:
+    return {
+        "d3q19_mrt_periodic_512": "D3Q19 MRT periodic 512^3, seeded rho=1+N(0,1e-3), "
+                                  "u~U(-0.02,0.02), nu=0.01, other rates 1.2",
+        "d3q19_mrt_periodic_128": "D3Q19 MRT periodic 128^3, seeded rho=1+N(0,1e-3), "
+                                  "u~U(-0.02,0.02), nu=0.01, other rates 1.2",
+    }.get(name, w.name if w is not None else name)
+
+
+# ------------------------------------------------------------------ clocks ---------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi clock samples every 200 ms while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3])
+                          if v.lower().startswith("active")})
+        sm = [r[0] for r in rows]
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# ------------------------------------------------------------------ GPU legs -------
+
+def upload(w, device, pinned=False):
+    import torch
+    arrs = [w.rho0, w.u0] + ([w.T_init] if w.thermal else [])
+    out = []
+    for a in arrs:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        out.append(t.pin_memory() if pinned else t.to(device))
+    if not w.thermal:
+        out.append(None)
+    return out
+
+
+def timed_device_leg(sim, w, steps, warmup, lbm_steps, dist_ctx):
+    """K submissions on a device-resident state; returns (seconds, kernel_ms, clocks)."""
+    import torch
+    for _ in range(warmup):
+        sim.step(lbm_steps)
+        sim.diagnostics(allow_nonfinite=True)
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        t0.record()
+        for k in range(steps):
+            ev[k][0].record()
+            sim.step(lbm_steps)
+            ev[k][1].record()
+            sim.diagnostics(allow_nonfinite=True)
+        t1.record()
+        torch.cuda.synchronize()
+    dist_ctx.barrier()
+    secs = t0.elapsed_time(t1) / 1e3
+    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / (steps * lbm_steps)
+    return secs, kernel_ms, clk.summary()
+
+
+def timed_e2e_leg(sim, w, steps, warmup, lbm_steps, dist_ctx):
+    """K submissions through the C ABI with page-locked host fields."""
+    import torch
+    rho_h, u_h, T_h = upload(w, None, pinned=True)
+    out_rho = torch.empty_like(rho_h).pin_memory()
+    out_u = torch.empty_like(u_h).pin_memory()
+    out_T = torch.empty_like(T_h).pin_memory() if T_h is not None else None
+
+    def one():
+        sim.init_equilibrium(rho_h, u_h, T_h)
+        sim.step(lbm_steps)
+        sim.macroscopic(out_rho, out_u, out_T)
+        sim.diagnostics(allow_nonfinite=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        one()
+    t1.record()
+    torch.cuda.synchronize()
+    dist_ctx.barrier()
+    secs = t0.elapsed_time(t1) / 1e3
+    h2d = sum(t.numel() * t.element_size() for t in (rho_h, u_h, T_h) if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in (out_rho, out_u, out_T) if t is not None)
+    d2h += 15 * 8   # diagnostics read-back
+    return secs, h2d, d2h
+
+
+# --------------------------------------------------------------- CPU baseline ------
+
+def oracle_sample(name: str):
+    """A bounded sample of the workload for the CPU oracle: the same generator and
+    physics on a smaller grid (periodic sub-box / reduced cavity)."""
+    from lattice_boltzmann_cfd_gb300 import workloads as W
+    if name.startswith("d3q19_mrt_periodic"):
+        return W.random_periodic(shape=(256, 256, 64), seed=2), "periodic 256x256x64 sub-box"
+    if name == "cavity3d_512":
+        return W.cavity3d(shape=(256, 256, 64)), "cavity 256x256x64"
+    if name == "cavity2d_4096":
+        return W.cavity2d(shape=(2048, 2048, 1)), "cavity 2048^2"
+    if name == "channel_sphere_128":
+        return W.channel_sphere(), "full 128^3"
+    return W.taylor_green(), "full 32^3"
+
+
+def time_oracle(name: str, steps: int):
+    import oracle
+    oracle.build()
+    w, label = oracle_sample(name)
+    p = oracle.Problem(w)
+    f, g = oracle.init_equilibrium(p, w.rho0, w.u0, w.T_init)
+    oracle.run(p, f, g, 1)   # first touch
+    t = time.perf_counter()
+    oracle.run(p, f, g, steps)
+    dt = time.perf_counter() - t
+    mlups = w.cells * steps / dt / 1e6
+    return mlups, dt, w.cells, label, oracle.max_threads()
+
+
+def cpu_baseline(name: str) -> dict:
+    mlups, dt, cells, label, cores = time_oracle(name, 4)
+    return {"value": round(mlups, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{label} of the same workload, 4 fp64 two-buffer steps "
+                      f"({cells * 4 / 1e6:.0f} M cell updates, {dt:.1f} s)"}
+
+
+# ----------------------------------------------------------------- helpers --------
+
+class DistCtx:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def done(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def run_secondary(name, lbm_steps, reps):
+    import torch
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = make_workload(name)
+    sim = Simulation(w)
+    sim.init_equilibrium(*upload(w, sim.device))
+    sim.step(lbm_steps)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        sim.step(lbm_steps)
+    b.record()
+    torch.cuda.synchronize()
+    kernel_s = a.elapsed_time(b) / 1e3 / (reps * lbm_steps)
+    bpc = BYTES_PER_CELL[(w.lattice, w.thermal)]
+    peak, _ = measured_peak()
+    achieved = bpc * w.cells / kernel_s / 1e9
+    sim.close()
+    del sim
+    torch.cuda.empty_cache()
+    return {"workload": workload_label(name, w), "mlups": round(w.cells / kernel_s / 1e6, 1),
+            "bytes_per_cell": bpc, "achieved_gbs": round(achieved, 1),
+            "frac": round(achieved / peak, 4)}
+
+
+# --------------------------------------------------------------------- main --------
+
+def run_gpu(args, dctx):
+    import torch
+    from lattice_boltzmann_cfd_gb300 import Simulation, capi
+    torch.cuda.set_device(dctx.local)
+    dctx.init("nccl")
+    capi.load()
+    w = make_workload(args.workload)
+    sim = Simulation(w)
+    sim.init_equilibrium(*upload(w, sim.device))
+    secs, kernel_ms, clocks = timed_device_leg(sim, w, args.steps, args.warmup,
+                                               args.lbm_steps, dctx)
+    secs = dctx.max(secs)
+    kernel_ms = dctx.max(kernel_ms)
+    updates = w.cells * args.lbm_steps * args.steps * dctx.world
+    value = updates / secs / 1e6
+    e2e_secs, h2d, d2h = timed_e2e_leg(sim, w, args.steps, min(args.warmup, 2),
+                                       args.lbm_steps, dctx)
+    e2e_secs = dctx.max(e2e_secs)
+    e2e_value = updates / e2e_secs / 1e6
+    sim.close()
+    del sim
+    torch.cuda.empty_cache()
+    if dctx.rank != 0:
+        return None
+    bpc = BYTES_PER_CELL[(w.lattice, w.thermal)]
+    peak, peak_kind = measured_peak()
+    achieved = bpc * w.cells / (kernel_ms / 1e3) / 1e9
+    src = kernel_source_hash()
+    tr = NCU_TRAFFIC.get(args.workload)
+    traffic = (round(tr["bytes_per_cell"] * w.cells) if tr and tr["src_hash"] == src else None)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dctx.world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_label(args.workload, w),
+                   "grid": list(w.shape), "cells": w.cells,
+                   "lbm_steps_per_step": args.lbm_steps,
+                   "step": f"{args.lbm_steps} fused AA collide-and-stream launches + "
+                           "diagnostics reduction read back",
+                   "layout": "AA in-place, one fp32 SoA population buffer",
+                   "l2": "state far larger than the 129 MB L2 (no flush needed)",
+                   "parallelism": f"replicas x{dctx.world}" if dctx.world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "step_kernel (even/odd AA forms)",
+                     "kernel_ms": round(kernel_ms, 4), "bytes_per_cell": bpc,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)"},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "path": "page-locked host rho,u in -> lbm_init_equilibrium -> lbm_step -> "
+                        "lbm_macroscopic into page-locked host -> lbm_diagnostics"},
+        "gpu_launches": args.steps * (args.lbm_steps + 2),
+        "clocks": clocks,
+    }
+    if not args.no_secondary:
+        line["secondary"] = [run_secondary(n, args.lbm_steps, 4)
+                             for n in ("cavity3d_512", "cavity2d_4096", "d3q19_mrt_periodic_128")]
+    line["cpu_baseline"] = cpu_baseline(args.workload)
+    return line
+
+
+def run_reference(args, dctx):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if dctx.rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w, label = oracle_sample(args.workload)
+    p = oracle.Problem(w)
+    f, g = oracle.init_equilibrium(p, w.rho0, w.u0, w.T_init)
+    for _ in range(args.warmup):
+        oracle.run(p, f, g, 1)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(p, f, g, 1)
+    dt = time.perf_counter() - t
+    value = w.cells * args.steps / dt / 1e6
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": dctx.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_label(args.workload),
+                   "sample": label, "lbm_steps_per_step": 1},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{label}: one fp64 two-buffer step per benchmark step"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default="d3q19_mrt_periodic_512")
+    ap.add_argument("--lbm-steps", type=int, default=50,
+                    help="time steps per benchmark step (one submission)")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="do not measure the other workloads after the main one")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dctx = DistCtx()
+    line = run_reference(args, dctx) if args.impl == "reference" else run_gpu(args, dctx)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    dctx.done()
+
+
+if __name__ == "__main__":
+    main()

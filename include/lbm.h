@@ -1,0 +1,184 @@
+/*
+ * lbm.h -- C ABI of the GB300 (sm_103a) lattice-Boltzmann collide-and-stream library.
+ *
+ * One library call advances a lattice-Boltzmann flow (D3Q19 or D2Q9 populations, BGK or
+ * MRT collision, Guo forcing with Boussinesq buoyancy, optional D3Q7 / D2Q5 thermal
+ * populations) by n time steps, one fused kernel launch per step, populations streamed in
+ * place with the AA pattern in a single fp32 structure-of-arrays buffer.
+ *
+ * Sources (the method each call implements):
+ *   [TLBM] "Multi-GPU thermal lattice Boltzmann simulations using OpenACC and MPI",
+ *          Sec. 2: Eq. 5 (MRT evolution of f, forcing F' = M^-1 (I - S/2) M F~),
+ *          rho = sum f_i, u = (sum e_i f_i + F/2) / rho, F = rho g beta_T (T - T0) along
+ *          the vertical axis, half-way bounce-back f_ibar(x, t+1) = f_i+(x, t); Eq. 7
+ *          (MRT evolution of g), T = sum g_i, half-way anti-bounce-back
+ *          g_ibar(x, t+1) = -g_i+(x, t) + omega T_w with omega = (4 + a_T)/10 (D2Q5) or
+ *          (6 + a_T)/21 (D3Q7), adiabatic walls by half-way bounce-back;
+ *          Sec. 3: SoA index x + Nx y + Nx Ny z + Nx Ny Nz i; the MLUPS metric.
+ *   [AA]   "GPU lattice Boltzmann: streaming layout and performance": the in-place AA
+ *          pattern (even steps read (q, x) and write (opposite(q), x); odd steps read
+ *          (opposite(q), x - c_q) and write (q, x + c_q)), 152 bytes per D3Q19 update,
+ *          momentum exchange read back from the last step of a submission.
+ *   [KFS]  "GPU Optimization for High-Quality Kinetic Fluid Simulation", Sec. 3.1,
+ *          Eq. 1-5 (lattice Boltzmann equation, moments, pull streaming, MRT collision
+ *          Omega = -M^-1 D (m - m_eq)); Sec. 4 (SoA layout, bounce-back at solid nodes).
+ *
+ * Conventions shared by every call:
+ *   - Memory.  The caller owns all device memory: it allocates one device workspace of
+ *     lbm_workspace_bytes() bytes and passes it to lbm_create(); the library carves the
+ *     populations, the link mask and the reduction scratch out of it and never calls
+ *     cudaMalloc or cudaFree.  The library owns only the small host-side context.
+ *   - Fields.  fp32, structure of arrays, x fastest: a scalar field is nx*ny*nz floats
+ *     (index x + nx*(y + ny*z)); the velocity is dim such planes, component-major
+ *     (u_x plane, then u_y, then u_z in 3-D).  Populations in get/set are Q planes
+ *     (q-major) of nx*ny*nz floats, in the lattice order given below.  Solid cells read
+ *     out as rho = u = T = 0 and populations 0.
+ *   - Field pointers may be device memory or page-locked host memory (cudaHostAlloc /
+ *     cudaHostRegister; the kernel then reads or writes it over the host link).  Pageable
+ *     host memory is accepted only where the device reports pageable-memory access.
+ *   - Ordering.  All device work is enqueued on the stream given to lbm_create(), in call
+ *     order, and returns without waiting, except lbm_solid_force() and lbm_diagnostics(),
+ *     which wait for that stream.
+ *   - Errors.  Every call returns an lbm_status.  Argument errors are found on the host
+ *     before anything is enqueued.  A CUDA error is returned as LBM_ERR_CUDA; its text is
+ *     available from lbm_last_error().  No call aborts, traps or throws across the ABI.
+ *
+ * Lattice orders (c_q):
+ *   D3Q19: 0 rest; 1 +x, 2 -x, 3 +y, 4 -y, 5 +z, 6 -z; 7 (+,+,0), 8 (-,+,0), 9 (+,-,0),
+ *          10 (-,-,0); 11 (+,0,+), 12 (-,0,+), 13 (+,0,-), 14 (-,0,-); 15 (0,+,+),
+ *          16 (0,-,+), 17 (0,+,-), 18 (0,-,-).
+ *   D2Q9:  0 rest; 1 +x, 2 +y, 3 -x, 4 -y, 5 (+,+), 6 (-,+), 7 (-,-), 8 (+,-).
+ *   D3Q7:  0 rest; 1 +x, 2 -x, 3 +y, 4 -y, 5 +z, 6 -z.   D2Q5: 0 rest; 1 +x, 2 +y, 3 -x, 4 -y.
+ * Moment rows (index of s[] / s_T[]):
+ *   D3Q19 (d'Humieres basis): 0 rho, 1 e, 2 eps, 3 jx, 4 qx, 5 jy, 6 qy, 7 jz, 8 qz,
+ *          9 3pxx, 10 3pixx, 11 pww, 12 piww, 13 pxy, 14 pyz, 15 pxz, 16 mx, 17 my, 18 mz.
+ *   D2Q9 (Lallemand-Luo basis): 0 rho, 1 e, 2 eps, 3 jx, 4 qx, 5 jy, 6 qy, 7 pxx, 8 pxy.
+ *   D3Q7: 0 T, 1-3 jx..jz, 4 e (rest weight -6), 5 (0,2,2,-1,-1,-1,-1), 6 (0,0,0,1,1,-1,-1).
+ *   D2Q5: 0 T, 1 jx, 2 jy, 3 e (rest weight -4), 4 (0,1,-1,1,-1).
+ *   Rates of conserved rows (rho, j; T) are ignored.  Viscosity nu = (1/s_nu - 1/2)/3 on
+ *   the stress rows; thermal diffusivity kappa = omega (1/s_kappa - 1/2) on the j rows.
+ */
+#ifndef LBM_GB300_H
+#define LBM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct lbm_ctx lbm_ctx; /* opaque, host side */
+
+typedef enum {
+    LBM_OK = 0,
+    LBM_ERR_ARG = 1,         /* bad argument (null pointer, size, range)            */
+    LBM_ERR_UNSUPPORTED = 2, /* valid but not supported combination                 */
+    LBM_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned          */
+    LBM_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed         */
+    LBM_ERR_NONFINITE = 5,   /* diagnostics found a non-finite rho or T             */
+    LBM_ERR_STATE = 6        /* call out of order (e.g. stepping before any init)   */
+} lbm_status;
+
+enum { LBM_D2Q9 = 9, LBM_D3Q19 = 19 };
+enum { LBM_THERMAL_NONE = 0, LBM_D2Q5 = 5, LBM_D3Q7 = 7 };
+enum { LBM_BGK = 0, LBM_MRT = 1 };
+enum { LBM_FACE_PERIODIC = 0, LBM_FACE_WALL = 1 };        /* flow: half-way bounce-back */
+enum { LBM_TFACE_ADIABATIC = 0, LBM_TFACE_DIRICHLET = 1 }; /* thermal, on WALL faces   */
+
+/* Problem description ([TLBM] Sec. 2; [KFS] Sec. 3.1).  Face order: -x, +x, -y, +y, -z, +z.
+ * Both faces of an axis must have the same flow kind.  A link is a wall link when its
+ * far end lies outside the domain through a WALL face or is a solid cell; wall links
+ * bounce back f, and bounce back g (adiabatic face or solid) or anti-bounce-back g
+ * (DIRICHLET face, wall temperature T_wall[face]). */
+typedef struct {
+    int nx, ny, nz;       /* cells; nz == 1 for D2Q9; nx*ny*nz < 2^31                  */
+    int lattice;          /* LBM_D3Q19 or LBM_D2Q9                                     */
+    int thermal;          /* LBM_THERMAL_NONE, LBM_D3Q7 (with D3Q19), LBM_D2Q5 (D2Q9)  */
+    int collision;        /* LBM_BGK or LBM_MRT (momentum populations)                 */
+    double tau;           /* BGK relaxation time, > 1/2                                */
+    double s[19];         /* MRT rate of each moment row, in [0, 2)                    */
+    double s_T[7];        /* thermal MRT rate of each row, in [0, 2)                   */
+    double a_T;           /* thermal energy-moment constant (e_eq = a_T T), in (-Q_T+1, 1) */
+    double g_body[3];     /* body acceleration: F += rho g_body                        */
+    double gbeta, T0;     /* buoyancy: F += rho gbeta (T - T0) e_up (thermal only)      */
+    int up_axis;          /* 0, 1, 2 = x, y, z (2-D: 0 or 1)                           */
+    int face_flow[6];     /* LBM_FACE_PERIODIC or LBM_FACE_WALL                        */
+    int face_T[6];        /* LBM_TFACE_ADIABATIC or LBM_TFACE_DIRICHLET (WALL faces)    */
+    double T_wall[6];     /* wall temperature of DIRICHLET faces                       */
+    const uint8_t *solid_mask; /* HOST pointer, nx*ny*nz bytes, x fastest, nonzero =
+                                  solid; NULL = no solid cells.  Copied by lbm_create. */
+} lbm_config;
+
+/* Diagnostics of the current state (see lbm_diagnostics). */
+typedef struct {
+    double mass;          /* sum over fluid cells of rho                                  */
+    double momentum[3];   /* sum over fluid cells of sum_q c_q f_q (no force shift)        */
+    double force[3];      /* momentum exchanged with solid cells in the last step          */
+    double heat[6];       /* per face: sum over fluid cells next to a DIRICHLET face of
+                             2 (T_w - T), the wall-normal gradient over the half cell     */
+    double nu_hot;        /* Nusselt number of the hottest / coldest DIRICHLET face:       */
+    double nu_cold;       /*   |heat| * H / (dT * A), H = cells across, A = face cells     */
+    long long fluid_cells;
+    long long steps;      /* time steps taken since the last init / set                   */
+    int finite;           /* 1 if every fluid rho (and T) is finite                        */
+} lbm_diag;
+
+/* Bytes of device workspace lbm_create() needs for this configuration (validates it). */
+lbm_status lbm_workspace_bytes(const lbm_config *cfg, size_t *bytes);
+
+/* Validate cfg, carve the workspace (device memory, >= lbm_workspace_bytes bytes,
+ * 256-byte aligned), copy the solid mask and build the per-cell link mask on
+ * cuda_stream (a cudaStream_t; NULL = the legacy default stream).  *out receives the
+ * context.  The context holds no state until lbm_init_equilibrium or lbm_set_populations. */
+lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace_bytes,
+                      void *cuda_stream, lbm_ctx **out);
+
+/* f = f_eq(rho, u) ([KFS] Eq. 2 inverted by the quadratic equilibrium), g = g_eq(T, u)
+ * (equilibrium moments T, u T, a_T T, 0...), at every fluid cell; resets parity and the
+ * step count.  rho: N floats, u: dim*N, T: N (NULL allowed only without thermal).  u is
+ * used as given (no F/2 shift). */
+lbm_status lbm_init_equilibrium(lbm_ctx *ctx, const float *rho, const float *u, const float *T);
+
+/* Advance n >= 0 time steps ([TLBM] Eq. 5 and Eq. 7 fused with streaming, [AA]): one
+ * kernel launch per step, alternating the even and odd AA forms. */
+lbm_status lbm_step(lbm_ctx *ctx, int n);
+
+/* rho = sum f, u = (sum c f + F/2)/rho, T = sum g of the current state ([TLBM] Sec. 2).
+ * Any of the three pointers may be NULL to skip that field. */
+lbm_status lbm_macroscopic(lbm_ctx *ctx, float *rho, float *u, float *T);
+
+/* Momentum exchanged with solid cells in the last step taken: the sum over links from a
+ * fluid cell x into a solid cell of 2 f_q+(x) c_q ([AA]: read back from the step whose
+ * forces are wanted).  Domain-face walls are not included.  Waits for the stream. */
+lbm_status lbm_solid_force(lbm_ctx *ctx, double F_out[3]);
+
+/* Mass, momentum, solid force, wall heat flux and Nusselt numbers, fp64 reductions.
+ * Waits for the stream.  Returns LBM_ERR_NONFINITE (with *out filled) if a fluid rho or
+ * T is not finite. */
+lbm_status lbm_diagnostics(lbm_ctx *ctx, lbm_diag *out);
+
+/* Copy the logical populations (parity resolved, f unshifted) out to / in from Q planes
+ * (q-major, N floats each).  g may be NULL without a thermal lattice.  set resets the
+ * step count but keeps the parity; get of a solid cell yields 0. */
+lbm_status lbm_get_populations(lbm_ctx *ctx, float *f, float *g);
+lbm_status lbm_set_populations(lbm_ctx *ctx, const float *f, const float *g);
+
+/* Copy the per-cell link mask (N uint32): bit q (1..Q-1) = link q is a wall link,
+ * bit 19+k (k = 1..Q_T-1) = thermal link k ends on a DIRICHLET face, bit 31 = solid cell.
+ * Device or page-locked host destination. */
+lbm_status lbm_get_link_mask(lbm_ctx *ctx, uint32_t *mask);
+
+/* Enqueue later work on another stream (a cudaStream_t). */
+lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);
+
+int lbm_parity(const lbm_ctx *ctx);                 /* steps taken mod 2, -1 if ctx NULL */
+long long lbm_steps_taken(const lbm_ctx *ctx);      /* -1 if ctx NULL                    */
+const char *lbm_last_error(const lbm_ctx *ctx);     /* ctx NULL: last create-time error */
+const char *lbm_version(void);
+void lbm_destroy(lbm_ctx *ctx);                     /* frees the host context only       */
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,1 +1,22 @@
-"""GB300-native lattice-Boltzmann collide-and-stream step (placeholder; filled below)."""
+"""GB300-native (sm_103a) lattice-Boltzmann collide-and-stream step.
+
+The compute lives in ``liblbm_gb300.so`` (CUDA, C ABI declared in ``include/lbm.h``):
+D3Q19 / D2Q9 populations with BGK or MRT collision, Guo forcing with Boussinesq
+buoyancy, fused D3Q7 / D2Q5 thermal populations, half-way bounce-back and
+anti-bounce-back walls through a per-cell link mask, momentum exchange on solids, all
+streamed in place with the AA pattern in one fp32 structure-of-arrays buffer.
+
+* ``capi``      -- one Python function per C entry point (same names).
+* ``solver``    -- ``make_config`` and the ``Simulation`` handle.
+* ``workloads`` -- seeded synthetic problems.
+"""
+from . import capi, workloads  # noqa: F401
+from .solver import Simulation, make_config  # noqa: F401
+
+__all__ = ["capi", "workloads", "Simulation", "make_config", "build"]
+
+
+def build(force: bool = False) -> str:
+    """Compile liblbm_gb300.so (sm_103a) in-tree and return its path."""
+    from . import _build
+    return _build.build(force=force)

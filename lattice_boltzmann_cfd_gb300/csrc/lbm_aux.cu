@@ -1,0 +1,137 @@
+// Launchers of the auxiliary kernels (initialisation, mask, read-out, diagnostics) for
+// both lattices.
+#include "lbm_internal.h"
+
+namespace lbm {
+namespace {
+
+template <class F3, class F2>
+cudaError_t by_lattice(int lattice, int thermal, F3 &&f3, F2 &&f2)
+{
+    if (lattice == 19) {
+        if (thermal == 7) return f3(D3Q7{});
+        return f3(NoThermal{});
+    }
+    if (thermal == 5) return f2(D2Q5{});
+    return f2(NoThermal{});
+}
+
+Shape shape_of(const Params &P) { return cell_shape(P.nx, P.ny, P.nz); }
+
+}  // namespace
+
+cudaError_t launch_init(int lattice, int thermal, const Params &P, const float *rho,
+                        const float *u, const float *T, cudaStream_t s)
+{
+    const Shape sh = shape_of(P);
+    return by_lattice(
+        lattice, thermal,
+        [&](auto tl) {
+            init_kernel<D3Q19, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+            return cudaGetLastError();
+        },
+        [&](auto tl) {
+            init_kernel<D2Q9, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+            return cudaGetLastError();
+        });
+}
+
+cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t *solid,
+                        uint32_t *mask, cudaStream_t s)
+{
+    const Shape sh = shape_of(P);
+    return by_lattice(
+        lattice, thermal,
+        [&](auto tl) {
+            mask_kernel<D3Q19, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, solid, mask);
+            return cudaGetLastError();
+        },
+        [&](auto tl) {
+            mask_kernel<D2Q9, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, solid, mask);
+            return cudaGetLastError();
+        });
+}
+
+namespace {
+template <class L, class TL>
+cudaError_t macro_go(bool masked, bool odd, const Params &P, float *rho, float *u, float *T,
+                     cudaStream_t s)
+{
+    const Shape sh = shape_of(P);
+    if (masked) {
+        if (odd) macro_kernel<L, TL, true, true><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+        else macro_kernel<L, TL, true, false><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+    } else {
+        if (odd) macro_kernel<L, TL, false, true><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+        else macro_kernel<L, TL, false, false><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+    }
+    return cudaGetLastError();
+}
+
+template <class L, class TL, bool SET>
+cudaError_t pop_go(bool masked, bool odd, const Params &P, float *f, float *g, cudaStream_t s)
+{
+    const Shape sh = shape_of(P);
+    if (masked) {
+        if (odd) pop_kernel<L, TL, true, true, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
+        else pop_kernel<L, TL, true, false, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
+    } else {
+        if (odd) pop_kernel<L, TL, false, true, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
+        else pop_kernel<L, TL, false, false, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
+    }
+    return cudaGetLastError();
+}
+
+template <class L, class TL>
+cudaError_t diag_go(bool masked, bool odd, const Params &P, double *partial, double *out,
+                    cudaStream_t s)
+{
+    const dim3 g(DIAG_BLOCKS), b(DIAG_THREADS);
+    if (masked) {
+        if (odd) diag_kernel<L, TL, true, true><<<g, b, 0, s>>>(P, partial);
+        else diag_kernel<L, TL, true, false><<<g, b, 0, s>>>(P, partial);
+    } else {
+        if (odd) diag_kernel<L, TL, false, true><<<g, b, 0, s>>>(P, partial);
+        else diag_kernel<L, TL, false, false><<<g, b, 0, s>>>(P, partial);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    diag_finalize<<<1, DIAG_THREADS, 0, s>>>(partial, DIAG_BLOCKS, out);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_macro(int lattice, int thermal, bool masked, bool odd, const Params &P,
+                         float *rho, float *u, float *T, cudaStream_t s)
+{
+    return by_lattice(
+        lattice, thermal,
+        [&](auto tl) { return macro_go<D3Q19, decltype(tl)>(masked, odd, P, rho, u, T, s); },
+        [&](auto tl) { return macro_go<D2Q9, decltype(tl)>(masked, odd, P, rho, u, T, s); });
+}
+
+cudaError_t launch_pop(int lattice, int thermal, bool masked, bool odd, bool set,
+                       const Params &P, float *f, float *g, cudaStream_t s)
+{
+    return by_lattice(
+        lattice, thermal,
+        [&](auto tl) {
+            return set ? pop_go<D3Q19, decltype(tl), true>(masked, odd, P, f, g, s)
+                       : pop_go<D3Q19, decltype(tl), false>(masked, odd, P, f, g, s);
+        },
+        [&](auto tl) {
+            return set ? pop_go<D2Q9, decltype(tl), true>(masked, odd, P, f, g, s)
+                       : pop_go<D2Q9, decltype(tl), false>(masked, odd, P, f, g, s);
+        });
+}
+
+cudaError_t launch_diag(int lattice, int thermal, bool masked, bool odd, const Params &P,
+                        double *partial, double *out, cudaStream_t s)
+{
+    return by_lattice(
+        lattice, thermal,
+        [&](auto tl) { return diag_go<D3Q19, decltype(tl)>(masked, odd, P, partial, out, s); },
+        [&](auto tl) { return diag_go<D2Q9, decltype(tl)>(masked, odd, P, partial, out, s); });
+}
+
+}  // namespace lbm

@@ -1,0 +1,358 @@
+// C ABI of the GB300 lattice-Boltzmann library (declared in include/lbm.h): argument
+// validation, workspace layout, parity bookkeeping, launches and error status.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "../../include/lbm.h"
+#include "lbm_internal.h"
+#include "lbm_setup.h"
+
+using lbm_setup::Layout;
+using lbm_setup::ALIGN;
+
+namespace {
+
+thread_local std::string g_error;  // errors without a context (create, workspace_bytes)
+
+struct DeviceGuard {
+    int prev = -1;
+    bool changed = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+            changed = cudaSetDevice(dev) == cudaSuccess;
+        }
+    }
+    ~DeviceGuard()
+    {
+        if (changed) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct lbm_ctx {
+    lbm_config cfg{};
+    Layout L;
+    lbm::Params P{};
+    char *ws = nullptr;
+    uint8_t *solid = nullptr;
+    double *partial = nullptr, *result = nullptr;
+    cudaStream_t stream = nullptr;
+    int device = 0;
+    int parity = 0;
+    long long steps = 0;
+    bool initialized = false;
+    std::string err;
+};
+
+namespace {
+
+lbm_status fail(lbm_ctx *c, lbm_status s, const std::string &msg)
+{
+    if (c) c->err = msg;
+    else g_error = msg;
+    return s;
+}
+
+lbm_status cuda_fail(lbm_ctx *c, cudaError_t e, const char *where)
+{
+    std::string m = std::string(where) + ": " + cudaGetErrorName(e) + " (" +
+                    cudaGetErrorString(e) + ")";
+    return fail(c, LBM_ERR_CUDA, m);
+}
+
+// Resolve a caller's field pointer to an address a kernel can use.
+lbm_status device_address(lbm_ctx *c, const void *p, const char *what, void **out)
+{
+    cudaPointerAttributes a;
+    cudaError_t e = cudaPointerGetAttributes(&a, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, LBM_ERR_ARG, std::string(what) + ": not a valid pointer");
+    }
+    switch (a.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged:
+        if (a.device != c->device)
+            return fail(c, LBM_ERR_ARG, std::string(what) + ": memory of another device");
+        *out = const_cast<void *>(p);
+        return LBM_OK;
+    case cudaMemoryTypeHost:
+        *out = a.devicePointer ? a.devicePointer : const_cast<void *>(p);
+        return LBM_OK;
+    default: {
+        int pageable = 0;
+        cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccess, c->device);
+        if (!pageable)
+            return fail(c, LBM_ERR_ARG,
+                        std::string(what) +
+                            ": pageable host memory; pass device or page-locked memory");
+        *out = const_cast<void *>(p);
+        return LBM_OK;
+    }
+    }
+}
+
+bool is_odd(const lbm_ctx *c) { return c->parity != 0; }
+
+}  // namespace
+
+extern "C" {
+
+lbm_status lbm_workspace_bytes(const lbm_config *cfg, size_t *bytes)
+{
+    if (!bytes) return fail(nullptr, LBM_ERR_ARG, "bytes is NULL");
+    Layout L;
+    std::string why;
+    lbm_status s = lbm_setup::validate(cfg, &L, &why);
+    if (s != LBM_OK) return fail(nullptr, s, why);
+    *bytes = L.bytes;
+    return LBM_OK;
+}
+
+lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace_bytes,
+                      void *cuda_stream, lbm_ctx **out)
+{
+    if (!out) return fail(nullptr, LBM_ERR_ARG, "out is NULL");
+    *out = nullptr;
+    Layout L;
+    std::string why;
+    lbm_status s = lbm_setup::validate(cfg, &L, &why);
+    if (s != LBM_OK) return fail(nullptr, s, why);
+    if (!d_workspace) return fail(nullptr, LBM_ERR_WORKSPACE, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(d_workspace) % ALIGN)
+        return fail(nullptr, LBM_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (workspace_bytes < L.bytes)
+        return fail(nullptr, LBM_ERR_WORKSPACE,
+                    "workspace too small: need " + std::to_string(L.bytes) + " bytes");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+    cudaPointerAttributes a;
+    e = cudaPointerGetAttributes(&a, d_workspace);
+    if (e != cudaSuccess || a.type != cudaMemoryTypeDevice || a.device != dev) {
+        cudaGetLastError();
+        return fail(nullptr, LBM_ERR_WORKSPACE,
+                    "workspace must be device memory of the current device");
+    }
+    lbm_ctx *c = new (std::nothrow) lbm_ctx();
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "out of host memory");
+    c->cfg = *cfg;
+    c->cfg.solid_mask = nullptr;
+    c->L = L;
+    c->ws = static_cast<char *>(d_workspace);
+    c->stream = static_cast<cudaStream_t>(cuda_stream);
+    c->device = dev;
+    c->partial = reinterpret_cast<double *>(c->ws + L.off_partial);
+    c->result = reinterpret_cast<double *>(c->ws + L.off_result);
+    lbm_setup::fill_params(c->cfg, c->L, c->ws, c->P);
+    if (L.masked) {
+        uint8_t *solid = nullptr;
+        if (L.has_solid) {
+            solid = reinterpret_cast<uint8_t *>(c->ws + L.off_solid);
+            e = cudaMemcpyAsync(solid, cfg->solid_mask, (size_t)L.N, cudaMemcpyHostToDevice,
+                                c->stream);
+            if (e != cudaSuccess) {
+                lbm_status r = cuda_fail(nullptr, e, "copy of solid_mask");
+                delete c;
+                return r;
+            }
+        }
+        e = lbm::launch_mask(cfg->lattice, cfg->thermal, c->P, solid,
+                             const_cast<uint32_t *>(c->P.mask), c->stream);
+        if (e != cudaSuccess) {
+            lbm_status r = cuda_fail(nullptr, e, "mask kernel");
+            delete c;
+            return r;
+        }
+    }
+    *out = c;
+    return LBM_OK;
+}
+
+lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, const float *T)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!rho || !u) return fail(c, LBM_ERR_ARG, "rho and u are required");
+    if (c->L.QT && !T) return fail(c, LBM_ERR_ARG, "T is required with a thermal lattice");
+    DeviceGuard guard(c->device);
+    void *dr, *du, *dT = nullptr;
+    lbm_status s = device_address(c, rho, "rho", &dr);
+    if (s == LBM_OK) s = device_address(c, u, "u", &du);
+    if (s == LBM_OK && c->L.QT) s = device_address(c, T, "T", &dT);
+    if (s != LBM_OK) return s;
+    cudaError_t e = lbm::launch_init(c->cfg.lattice, c->cfg.thermal, c->P, (const float *)dr,
+                                     (const float *)du, (const float *)dT, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "init kernel");
+    c->parity = 0;
+    c->steps = 0;
+    c->initialized = true;
+    return LBM_OK;
+}
+
+lbm_status lbm_step(lbm_ctx *c, int n)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (n < 0) return fail(c, LBM_ERR_ARG, "n must be >= 0");
+    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    DeviceGuard guard(c->device);
+    const lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
+    for (int i = 0; i < n; ++i) {
+        const bool odd = is_odd(c);
+        cudaError_t e = (c->cfg.lattice == LBM_D3Q19)
+                            ? lbm::launch_step_d3q19(c->cfg.thermal, c->cfg.collision,
+                                                     c->L.masked, odd, c->P, sh, c->stream)
+                            : lbm::launch_step_d2q9(c->cfg.thermal, c->cfg.collision,
+                                                    c->L.masked, odd, c->P, sh, c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "step kernel");
+        c->parity ^= 1;
+        ++c->steps;
+    }
+    return LBM_OK;
+}
+
+lbm_status lbm_macroscopic(lbm_ctx *c, float *rho, float *u, float *T)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    DeviceGuard guard(c->device);
+    void *dr = nullptr, *du = nullptr, *dT = nullptr;
+    lbm_status s = LBM_OK;
+    if (rho) s = device_address(c, rho, "rho", &dr);
+    if (s == LBM_OK && u) s = device_address(c, u, "u", &du);
+    if (s == LBM_OK && T && c->L.QT) s = device_address(c, T, "T", &dT);
+    if (s != LBM_OK) return s;
+    cudaError_t e = lbm::launch_macro(c->cfg.lattice, c->cfg.thermal, c->L.masked, is_odd(c),
+                                      c->P, (float *)dr, (float *)du, (float *)dT, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "macroscopic kernel");
+    return LBM_OK;
+}
+
+lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!out) return fail(c, LBM_ERR_ARG, "out is NULL");
+    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    DeviceGuard guard(c->device);
+    cudaError_t e = lbm::launch_diag(c->cfg.lattice, c->cfg.thermal, c->L.masked, is_odd(c),
+                                     c->P, c->partial, c->result, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "diagnostics kernel");
+    double r[lbm::DIAG_N] = {0};
+    e = cudaMemcpyAsync(r, c->result, sizeof(double) * 15, cudaMemcpyDeviceToHost, c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "diagnostics read-back");
+    std::memset(out, 0, sizeof(*out));
+    out->fluid_cells = (long long)std::llround(r[14]);
+    out->mass = (double)out->fluid_cells + r[0];
+    for (int a = 0; a < 3; ++a) {
+        out->momentum[a] = r[1 + a];
+        out->force[a] = r[4 + a];
+    }
+    for (int i = 0; i < 6; ++i) out->heat[i] = r[7 + i];
+    out->steps = c->steps;
+    out->finite = r[13] == 0.0 && std::isfinite(r[0]);
+    // Nusselt numbers of the hottest and coldest Dirichlet faces
+    const lbm::Params &P = c->P;
+    int hot = -1, cold = -1;
+    for (int i = 0; i < 6; ++i) {
+        if (!P.face_dir[i]) continue;
+        if (hot < 0 || c->cfg.T_wall[i] > c->cfg.T_wall[hot]) hot = i;
+        if (cold < 0 || c->cfg.T_wall[i] < c->cfg.T_wall[cold]) cold = i;
+    }
+    if (hot >= 0 && cold >= 0 && c->cfg.T_wall[hot] > c->cfg.T_wall[cold]) {
+        const double dT = c->cfg.T_wall[hot] - c->cfg.T_wall[cold];
+        const int n[3] = {c->cfg.nx, c->cfg.ny, c->cfg.nz};
+        auto nusselt = [&](int face) {
+            const int a = face / 2;
+            const double area = (double)n[0] * n[1] * n[2] / n[a];
+            return std::fabs(out->heat[face]) * n[a] / (dT * area);
+        };
+        out->nu_hot = nusselt(hot);
+        out->nu_cold = nusselt(cold);
+    }
+    if (!out->finite) return fail(c, LBM_ERR_NONFINITE, "non-finite rho or T in the state");
+    return LBM_OK;
+}
+
+lbm_status lbm_solid_force(lbm_ctx *c, double F_out[3])
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!F_out) return fail(c, LBM_ERR_ARG, "F_out is NULL");
+    lbm_diag d;
+    lbm_status s = lbm_diagnostics(c, &d);
+    if (s != LBM_OK && s != LBM_ERR_NONFINITE) return s;
+    for (int a = 0; a < 3; ++a) F_out[a] = d.force[a];
+    return s;
+}
+
+static lbm_status populations(lbm_ctx *c, float *f, float *g, bool set)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!f) return fail(c, LBM_ERR_ARG, "f is NULL");
+    if (c->L.QT && !g && set) return fail(c, LBM_ERR_ARG, "g is required with a thermal lattice");
+    if (!set && !c->initialized) return fail(c, LBM_ERR_STATE, "no state to read");
+    DeviceGuard guard(c->device);
+    void *df, *dg = nullptr;
+    lbm_status s = device_address(c, f, "f", &df);
+    if (s == LBM_OK && g && c->L.QT) s = device_address(c, g, "g", &dg);
+    if (s != LBM_OK) return s;
+    cudaError_t e = lbm::launch_pop(c->cfg.lattice, c->cfg.thermal, c->L.masked, is_odd(c), set,
+                                    c->P, (float *)df, (float *)dg, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, set ? "set kernel" : "get kernel");
+    if (set) {
+        c->initialized = true;
+        c->steps = 0;
+    }
+    return LBM_OK;
+}
+
+lbm_status lbm_get_populations(lbm_ctx *c, float *f, float *g)
+{
+    return populations(c, f, g, false);
+}
+
+lbm_status lbm_set_populations(lbm_ctx *c, const float *f, const float *g)
+{
+    return populations(c, const_cast<float *>(f), const_cast<float *>(g), true);
+}
+
+lbm_status lbm_get_link_mask(lbm_ctx *c, uint32_t *mask)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!mask) return fail(c, LBM_ERR_ARG, "mask is NULL");
+    DeviceGuard guard(c->device);
+    void *dm;
+    lbm_status s = device_address(c, mask, "mask", &dm);
+    if (s != LBM_OK) return s;
+    cudaError_t e;
+    if (c->L.masked)
+        e = cudaMemcpyAsync(dm, c->P.mask, sizeof(uint32_t) * (size_t)c->L.N,
+                            cudaMemcpyDefault, c->stream);
+    else
+        e = cudaMemsetAsync(dm, 0, sizeof(uint32_t) * (size_t)c->L.N, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "mask copy");
+    return LBM_OK;
+}
+
+lbm_status lbm_set_stream(lbm_ctx *c, void *cuda_stream)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    c->stream = static_cast<cudaStream_t>(cuda_stream);
+    return LBM_OK;
+}
+
+int lbm_parity(const lbm_ctx *c) { return c ? c->parity : -1; }
+
+long long lbm_steps_taken(const lbm_ctx *c) { return c ? c->steps : -1; }
+
+const char *lbm_last_error(const lbm_ctx *c) { return c ? c->err.c_str() : g_error.c_str(); }
+
+const char *lbm_version(void) { return "lbm-gb300 0.1 (sm_103a, AA in-place, fp32)"; }
+
+void lbm_destroy(lbm_ctx *c) { delete c; }
+
+}  // extern "C"

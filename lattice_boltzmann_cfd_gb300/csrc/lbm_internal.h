@@ -1,0 +1,45 @@
+// Host-side launch interface between the C ABI (lbm_capi.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "lbm_kernels.cuh"
+
+namespace lbm {
+
+struct Shape {
+    dim3 grid, block;
+};
+
+// One thread per cell, blocks of `threads` along x (rows of a block stacked in y when a
+// row is shorter than the block).
+inline Shape cell_shape(int nx, int ny, int nz, int threads = 256)
+{
+    int bx = ((nx + 31) / 32) * 32;
+    if (bx > threads) bx = threads;
+    int by = threads / bx;
+    if (by < 1) by = 1;
+    Shape s;
+    s.block = dim3(bx, by, 1);
+    s.grid = dim3((nx + bx - 1) / bx, (ny + by - 1) / by, nz);
+    return s;
+}
+
+constexpr int DIAG_BLOCKS = 1024;
+
+// Each returns the launch error (cudaGetLastError) of what it enqueued.
+cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, const Params &P,
+                              const Shape &sh, cudaStream_t s);
+cudaError_t launch_step_d2q9(int thermal, int coll, bool masked, bool odd, const Params &P,
+                             const Shape &sh, cudaStream_t s);
+cudaError_t launch_init(int lattice, int thermal, const Params &P, const float *rho,
+                        const float *u, const float *T, cudaStream_t s);
+cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t *solid,
+                        uint32_t *mask, cudaStream_t s);
+cudaError_t launch_macro(int lattice, int thermal, bool masked, bool odd, const Params &P,
+                         float *rho, float *u, float *T, cudaStream_t s);
+cudaError_t launch_pop(int lattice, int thermal, bool masked, bool odd, bool set,
+                       const Params &P, float *f, float *g, cudaStream_t s);
+cudaError_t launch_diag(int lattice, int thermal, bool masked, bool odd, const Params &P,
+                        double *partial, double *out, cudaStream_t s);
+
+}  // namespace lbm

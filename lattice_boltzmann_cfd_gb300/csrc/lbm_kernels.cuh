@@ -1,0 +1,509 @@
+// Kernels of the CUDA path: the fused AA collide-and-stream step (even and odd forms)
+// and the auxiliary kernels (equilibrium initialisation, link-mask build, parity-aware
+// read-out of macroscopic fields and populations, diagnostics reduction).
+//
+// Storage ("Multi-GPU thermal lattice Boltzmann simulations using OpenACC and MPI",
+// Sec. 3, SoA index x + Nx y + Nx Ny z + Nx Ny Nz i): population q of cell idx lives at
+// f[q * S + idx], S = plane stride (cells rounded up to 64, so that every plane starts
+// on a 256-byte boundary); f holds f_q - w_q (see lbm_collide.cuh), g holds g_q.
+//
+// AA pattern ("GPU lattice Boltzmann: streaming layout and performance"): one buffer.
+//   even step: read (q, x); collide; write f+_q to (opp q, x).
+//   odd step:  read (opp q, x - c_q); collide; write f+_q to (q, x + c_q).
+// Wall links fold into the odd step through the per-cell link mask (bit q: the link
+// from x along c_q ends on a wall or a solid cell): the read of q redirects to the own
+// slot (q, x) when link opp q is a wall, the write of q redirects to (opp q, x) when
+// link q is a wall.  Both hit the same slot, so every cell writes exactly the slots it
+// read and no cells race.  This realises the half-way bounce-back f_qbar(x, t+1) =
+// f_q+(x, t) and, for Dirichlet thermal links, the anti-bounce-back g_qbar(x, t+1) =
+// -g_q+(x, t) + omega T_w (multi-GPU thermal LBM page, Sec. 2): the sign flip and the
+// omega T_w term are applied where the odd step writes, or reads, the redirected slot.
+// Even steps need no wall handling.  After an odd number of steps the logical state is
+// read with the odd step's read pattern.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include "lbm_collide.cuh"
+
+namespace lbm {
+
+struct Params {
+    float *f;              // Q planes of S floats (shifted populations)
+    float *g;              // Q_T planes (thermal), may be null
+    const uint32_t *mask;  // link mask, null when there are no walls or solids
+    size_t S;              // plane stride in elements
+    int nx, ny, nz;
+    CollideParams c;
+    float abbT[7];         // per thermal direction k: omega * T_wall of the face k leaves by
+    int face_wall[6];      // per face: 1 = wall (flow)
+    int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
+    float T_wall[6];
+};
+
+// Neighbour offsets with periodic wrap by compare and add.
+struct Offs {
+    int xp, xm, yp, ym, zp, zm;
+};
+
+LBM_HD Offs make_offs(int x, int y, int z, const Params &P)
+{
+    Offs o;
+    const int sy = P.nx, sz = P.nx * P.ny;
+    o.xp = (x == P.nx - 1) ? 1 - P.nx : 1;
+    o.xm = (x == 0) ? P.nx - 1 : -1;
+    o.yp = (y == P.ny - 1) ? (1 - P.ny) * sy : sy;
+    o.ym = (y == 0) ? (P.ny - 1) * sy : -sy;
+    o.zp = (z == P.nz - 1) ? (1 - P.nz) * sz : sz;
+    o.zm = (z == 0) ? (P.nz - 1) * sz : -sz;
+    return o;
+}
+
+// Offset of the cell at x + (cx, cy, cz) (constants after unrolling).
+LBM_HD int nb(const Offs &o, int cx, int cy, int cz)
+{
+    return (cx > 0 ? o.xp : cx < 0 ? o.xm : 0) + (cy > 0 ? o.yp : cy < 0 ? o.ym : 0) +
+           (cz > 0 ? o.zp : cz < 0 ? o.zm : 0);
+}
+
+LBM_HD bool bit(uint32_t m, int b) { return (m >> b) & 1u; }
+
+// ---------------------------------------------------------------- cell access ---------
+
+// Load the logical populations of a fluid cell.  ODD = the odd step's read pattern.
+template <class L, class TL, bool MASKED, bool ODD>
+LBM_HD void load_cell(const Params &P, int idx, const Offs &o, uint32_t m,
+                                          float (&f)[L::Q], float (&g)[TL::QA])
+{
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) {
+        const float *p;
+        if (!ODD || q == 0) {
+            p = P.f + (q * P.S + idx);
+        } else {
+            const int oq = L::opp(q);
+            const bool wall_in = MASKED && bit(m, oq);
+            p = wall_in ? P.f + (q * P.S + idx)
+                        : P.f + (oq * P.S + (idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q))));
+        }
+        f[q] = *p;
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) {
+            if (!ODD || k == 0) {
+                g[k] = P.g[k * P.S + idx];
+            } else {
+                const int ok = L::opp(k);
+                const bool wall_in = MASKED && bit(m, ok);
+                if (wall_in) {
+                    const float raw = P.g[k * P.S + idx];
+                    g[k] = bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - raw : raw;
+                } else {
+                    g[k] = P.g[ok * P.S + (idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))];
+                }
+            }
+        }
+    }
+}
+
+// Store post-collision populations.  Even: swapped into (opp q, x).  Odd: to (q, x + c_q)
+// or, for a wall link, to (opp q, x) with bounce-back / anti-bounce-back applied.
+template <class L, class TL, bool MASKED, bool ODD>
+LBM_HD void store_cell(const Params &P, int idx, const Offs &o, uint32_t m,
+                                           const float (&f)[L::Q], const float (&g)[TL::QA])
+{
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) {
+        const int oq = L::opp(q);
+        float *p;
+        if (!ODD) {
+            p = P.f + (oq * P.S + idx);
+        } else if (q == 0) {
+            p = P.f + idx;
+        } else {
+            const bool wall_out = MASKED && bit(m, q);
+            p = wall_out ? P.f + (oq * P.S + idx)
+                         : P.f + (q * P.S + (idx + nb(o, L::cx(q), L::cy(q), L::cz(q))));
+        }
+        *p = f[q];
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) {
+            const int ok = L::opp(k);
+            if (!ODD) {
+                P.g[ok * P.S + idx] = g[k];
+            } else if (k == 0) {
+                P.g[idx] = g[0];
+            } else {
+                const bool wall_out = MASKED && bit(m, k);
+                if (wall_out) {
+                    P.g[ok * P.S + idx] =
+                        bit(m, DIRICHLET_SHIFT + k) ? P.abbT[k] - g[k] : g[k];
+                } else {
+                    P.g[k * P.S + (idx + nb(o, L::cx(k), L::cy(k), L::cz(k)))] = g[k];
+                }
+            }
+        }
+    }
+}
+
+// Store logical populations so that load_cell<..., ODD> reads them back (used by
+// set_populations; the inverse of load_cell).
+template <class L, class TL, bool MASKED, bool ODD>
+LBM_HD void store_logical(const Params &P, int idx, const Offs &o,
+                                              uint32_t m, const float (&f)[L::Q],
+                                              const float (&g)[TL::QA])
+{
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) {
+        float *p;
+        if (!ODD || q == 0) {
+            p = P.f + (q * P.S + idx);
+        } else {
+            const int oq = L::opp(q);
+            const bool wall_in = MASKED && bit(m, oq);
+            p = wall_in ? P.f + (q * P.S + idx)
+                        : P.f + (oq * P.S + (idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q))));
+        }
+        *p = f[q];
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) {
+            if (!ODD || k == 0) {
+                P.g[k * P.S + idx] = g[k];
+            } else {
+                const int ok = L::opp(k);
+                if (MASKED && bit(m, ok)) {
+                    P.g[k * P.S + idx] =
+                        bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - g[k] : g[k];
+                } else {
+                    P.g[ok * P.S + (idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))] = g[k];
+                }
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the step ----------
+
+// One time step: one thread per cell, blocks along x (x fastest for coalescing).
+template <class L, class TL, int COLL, bool MASKED, bool ODD>
+__global__ void __launch_bounds__(256) step_kernel(const Params P)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    const int idx = x + P.nx * (y + P.ny * z);
+    uint32_t m = 0;
+    if (MASKED) {
+        m = P.mask[idx];
+        if (m & SOLID_BIT) return;
+    }
+    Offs o{};
+    if (ODD) o = make_offs(x, y, z, P);
+    float f[L::Q], g[TL::QA];
+    load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+    collide<L, TL, COLL>(f, g, P.c);
+    store_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+}
+
+// ------------------------------------------------------------ auxiliary kernels -------
+
+// f = f_eq(rho, u) - w, g = g_eq(T, u) into the natural slots (parity 0) of one cell.
+template <class L, class TL>
+LBM_HD void init_cell(const Params &P, int idx, const float *rho, const float *u,
+                      const float *T)
+{
+    const size_t N = (size_t)P.nx * P.ny * P.nz;
+    const bool solid = P.mask && (P.mask[idx] & SOLID_BIT);
+    float f[L::Q], g[TL::QA];
+    if (solid) {
+#pragma unroll
+        for (int q = 0; q < L::Q; ++q) f[q] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < TL::QA; ++k) g[k] = 0.0f;
+    } else {
+        const float r = rho[idx];
+        const float dr = r - 1.0f;
+        const float ux = u[idx], uy = u[N + idx], uz = (L::DIM == 3) ? u[2 * N + idx] : 0.0f;
+        const float u15 = 1.5f * (ux * ux + uy * uy + uz * uz);
+#pragma unroll
+        for (int q = 0; q < L::Q; ++q) {
+            const float cu = L::cx(q) * ux + L::cy(q) * uy + L::cz(q) * uz;
+            f[q] = L::w(q) * (dr + r * (3.0f * cu + 4.5f * cu * cu - u15));
+        }
+        if constexpr (TL::Q == 7) d3q7_equilibrium(g, P.c.a_T, T[idx], ux, uy, uz);
+        if constexpr (TL::Q == 5) d2q5_equilibrium(g, P.c.a_T, T[idx], ux, uy);
+    }
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) P.f[q * P.S + idx] = f[q];
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) P.g[k * P.S + idx] = g[k];
+    }
+}
+
+template <class L, class TL>
+__global__ void init_kernel(const Params P, const float *__restrict__ rho,
+                            const float *__restrict__ u, const float *__restrict__ T)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    init_cell<L, TL>(P, x + P.nx * (y + P.ny * z), rho, u, T);
+}
+
+// Link mask of cell (x, y, z): bit q (1..Q-1) when the link x -> x + c_q leaves the
+// domain through a WALL face or ends in a solid cell; bit 19 + k when thermal link k
+// leaves through a Dirichlet face; bit 31 for a solid cell.
+template <class L, class TL>
+LBM_HD uint32_t cell_mask(const Params &P, const uint8_t *solid, int x, int y, int z)
+{
+    const int idx = x + P.nx * (y + P.ny * z);
+    if (solid && solid[idx]) return SOLID_BIT;
+    uint32_t m = 0;
+    const int n[3] = {P.nx, P.ny, P.nz};
+    const int c0[3] = {x, y, z};
+#pragma unroll
+    for (int q = 1; q < L::Q; ++q) {
+        const int c[3] = {L::cx(q), L::cy(q), L::cz(q)};
+        int s[3];
+        bool wall = false;
+        int face = -1;
+        for (int a = 0; a < 3; ++a) {
+            s[a] = c0[a] + c[a];
+            if (s[a] < 0) {
+                if (P.face_wall[2 * a]) { wall = true; face = 2 * a; }
+                else s[a] += n[a];
+            } else if (s[a] >= n[a]) {
+                if (P.face_wall[2 * a + 1]) { wall = true; face = 2 * a + 1; }
+                else s[a] -= n[a];
+            }
+        }
+        if (!wall && solid && solid[s[0] + P.nx * (s[1] + P.ny * s[2])]) wall = true;
+        if (wall) m |= 1u << q;
+        if (TL::Q > 0 && q < TL::Q && face >= 0 && P.face_dir[face])
+            m |= 1u << (DIRICHLET_SHIFT + q);
+    }
+    return m;
+}
+
+template <class L, class TL>
+__global__ void mask_kernel(const Params P, const uint8_t *__restrict__ solid,
+                            uint32_t *__restrict__ mask)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    mask[x + P.nx * (y + P.ny * z)] = cell_mask<L, TL>(P, solid, x, y, z);
+}
+
+// Macroscopic fields of the logical state: rho, u = (j + F/2)/rho, T.
+template <class L, class TL, bool MASKED, bool ODD>
+__global__ void macro_kernel(const Params P, float *__restrict__ rho, float *__restrict__ u,
+                             float *__restrict__ T)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    const int idx = x + P.nx * (y + P.ny * z);
+    const size_t N = (size_t)P.nx * P.ny * P.nz;
+    uint32_t m = 0;
+    if (MASKED) m = P.mask[idx];
+    if (m & SOLID_BIT) {
+        if (rho) rho[idx] = 0.0f;
+        if (u) {
+            for (int a = 0; a < L::DIM; ++a) u[a * N + idx] = 0.0f;
+        }
+        if (T) T[idx] = 0.0f;
+        return;
+    }
+    Offs o{};
+    if (ODD) o = make_offs(x, y, z, P);
+    float f[L::Q], g[TL::QA];
+    load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+    float dr = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f, t = 0.0f;
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) {
+        dr += f[q];
+        jx += L::cx(q) * f[q];
+        jy += L::cy(q) * f[q];
+        jz += L::cz(q) * f[q];
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) t += g[k];
+    }
+    const float r = 1.0f + dr;
+    float Fx, Fy, Fz, ux, uy, uz;
+    force_velocity<(TL::Q > 0)>(P.c, r, t, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz);
+    if (rho) rho[idx] = r;
+    if (u) {
+        u[idx] = ux;
+        u[N + idx] = uy;
+        if (L::DIM == 3) u[2 * N + idx] = uz;
+    }
+    if (T) T[idx] = t;
+}
+
+// Logical populations out (f unshifted), or in (SET).
+template <class L, class TL, bool MASKED, bool ODD, bool SET>
+__global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__restrict__ go)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    const int idx = x + P.nx * (y + P.ny * z);
+    const size_t N = (size_t)P.nx * P.ny * P.nz;
+    uint32_t m = 0;
+    if (MASKED) m = P.mask[idx];
+    if (m & SOLID_BIT) {
+        if (!SET) {
+            for (int q = 0; q < L::Q; ++q) fo[q * N + idx] = 0.0f;
+            if (TL::Q > 0 && go)
+                for (int k = 0; k < TL::Q; ++k) go[k * N + idx] = 0.0f;
+        }
+        return;
+    }
+    Offs o{};
+    if (ODD) o = make_offs(x, y, z, P);
+    float f[L::Q], g[TL::QA];
+    if (SET) {
+#pragma unroll
+        for (int q = 0; q < L::Q; ++q) f[q] = fo[q * N + idx] - L::w(q);
+        if constexpr (TL::Q > 0) {
+#pragma unroll
+            for (int k = 0; k < TL::Q; ++k) g[k] = go[k * N + idx];
+        }
+        store_logical<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+    } else {
+        load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+#pragma unroll
+        for (int q = 0; q < L::Q; ++q) fo[q * N + idx] = f[q] + L::w(q);
+        if constexpr (TL::Q > 0) {
+            if (go) {
+#pragma unroll
+                for (int k = 0; k < TL::Q; ++k) go[k * N + idx] = g[k];
+            }
+        }
+    }
+}
+
+// Diagnostics: per-block fp64 partial sums of
+//   [0] sum (rho - 1), [1..3] sum j, [4..6] momentum exchange with solid cells,
+//   [7..12] wall heat flux per Dirichlet face, [13] non-finite cells, [14] fluid cells.
+constexpr int DIAG_N = 16;
+constexpr int DIAG_THREADS = 256;
+
+template <class L, class TL, bool MASKED, bool ODD>
+__global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, double *partial)
+{
+    double acc[15];
+#pragma unroll
+    for (int i = 0; i < 15; ++i) acc[i] = 0.0;
+    const long long N = (long long)P.nx * P.ny * P.nz;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < N;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int idx = (int)i;
+        const int x = idx % P.nx;
+        const int y = (idx / P.nx) % P.ny;
+        const int z = idx / (P.nx * P.ny);
+        uint32_t m = 0;
+        if (MASKED) m = P.mask[idx];
+        if (m & SOLID_BIT) continue;
+        Offs o{};
+        if (ODD) o = make_offs(x, y, z, P);
+        float f[L::Q], g[TL::QA];
+        load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+        double dr = 0.0, t = 0.0;
+#pragma unroll
+        for (int q = 0; q < L::Q; ++q) {
+            dr += f[q];
+            acc[1] += L::cx(q) * (double)f[q];
+            acc[2] += L::cy(q) * (double)f[q];
+            acc[3] += L::cz(q) * (double)f[q];
+        }
+        acc[0] += dr;
+        if constexpr (TL::Q > 0) {
+#pragma unroll
+            for (int k = 0; k < TL::Q; ++k) t += g[k];
+        }
+        if (!isfinite(dr) || !isfinite(t)) acc[13] += 1.0;
+        acc[14] += 1.0;
+        if (MASKED) {
+            // links into solid cells: the bounced-back population of the last step is the
+            // logical f_opp(q)(x) now; exchange 2 f+_q c_q
+            const int c0[3] = {x, y, z};
+            const int n[3] = {P.nx, P.ny, P.nz};
+#pragma unroll
+            for (int q = 1; q < L::Q; ++q) {
+                if (!bit(m, q)) continue;
+                const int c[3] = {L::cx(q), L::cy(q), L::cz(q)};
+                bool face = false;
+                for (int a = 0; a < 3; ++a) {
+                    const int s = c0[a] + c[a];
+                    if ((s < 0 && P.face_wall[2 * a]) || (s >= n[a] && P.face_wall[2 * a + 1]))
+                        face = true;
+                }
+                if (face) continue;
+                const double fp = (double)f[L::opp(q)] + (double)L::w(q);
+                acc[4] += 2.0 * fp * c[0];
+                acc[5] += 2.0 * fp * c[1];
+                acc[6] += 2.0 * fp * c[2];
+            }
+        }
+        if constexpr (TL::Q > 0) {
+            const int c0[3] = {x, y, z};
+            const int n[3] = {P.nx, P.ny, P.nz};
+            for (int a = 0; a < L::DIM; ++a) {
+                if (c0[a] == 0 && P.face_dir[2 * a]) acc[7 + 2 * a] += 2.0 * (P.T_wall[2 * a] - t);
+                if (c0[a] == n[a] - 1 && P.face_dir[2 * a + 1])
+                    acc[8 + 2 * a] += 2.0 * (P.T_wall[2 * a + 1] - t);
+            }
+        }
+    }
+    // block reduction in a fixed order: warp shuffles, then warps in order
+    __shared__ double sh[DIAG_THREADS / 32][15];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < 15; ++i) {
+        double v = acc[i];
+        for (int s = 16; s > 0; s >>= 1) v += __shfl_down_sync(0xffffffffu, v, s);
+        if (lane == 0) sh[warp][i] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 15) {
+        double v = 0.0;
+        for (int w = 0; w < DIAG_THREADS / 32; ++w) v += sh[w][threadIdx.x];
+        partial[blockIdx.x * DIAG_N + threadIdx.x] = v;
+    }
+}
+
+// Sum the per-block partials in a fixed order into out[0..14].
+static __global__ void __launch_bounds__(DIAG_THREADS) diag_finalize(const double *partial, int nblocks,
+                                                               double *out)
+{
+    __shared__ double sh[DIAG_THREADS][15];
+    double acc[15];
+    for (int i = 0; i < 15; ++i) acc[i] = 0.0;
+    for (int b = threadIdx.x; b < nblocks; b += DIAG_THREADS)
+        for (int i = 0; i < 15; ++i) acc[i] += partial[b * DIAG_N + i];
+    for (int i = 0; i < 15; ++i) sh[threadIdx.x][i] = acc[i];
+    __syncthreads();
+    for (int s = DIAG_THREADS / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s)
+            for (int i = 0; i < 15; ++i) sh[threadIdx.x][i] += sh[threadIdx.x + s][i];
+        __syncthreads();
+    }
+    if (threadIdx.x < 15) out[threadIdx.x] = sh[0][threadIdx.x];
+}
+
+}  // namespace lbm

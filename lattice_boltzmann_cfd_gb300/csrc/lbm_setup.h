@@ -1,0 +1,176 @@
+// Host-side set-up shared by the C ABI: validation of an lbm_config, the workspace
+// layout, and the kernel parameters (rates scaled by the moment-row norms, anti-bounce-
+// back weights, face flags).
+#pragma once
+#include <cmath>
+#include <cstdint>
+#include <string>
+
+#include "../../include/lbm.h"
+#include "lbm_internal.h"
+
+namespace lbm_setup {
+
+constexpr size_t ALIGN = 256;
+inline size_t align_up(size_t v) { return (v + ALIGN - 1) / ALIGN * ALIGN; }
+
+// Norms |row|^2 of the moment bases (rows as listed in include/lbm.h).
+constexpr double NORM_D3Q19[19] = {19, 2394, 252, 10, 40, 10, 40, 10, 40, 36,
+                               72, 12,   24,  4,  4,  4,  8,  8,  8};
+constexpr double NORM_D2Q9[9] = {9, 36, 36, 6, 12, 6, 12, 4, 4};
+constexpr double NORM_D3Q7[7] = {7, 2, 2, 2, 42, 12, 4};
+constexpr double NORM_D2Q5[5] = {5, 2, 2, 20, 4};
+
+inline bool conserved_row(int lattice, int k)
+{
+    return k == 0 || k == 3 || k == 5 || (lattice == 19 && k == 7);
+}
+
+struct Layout {
+    int Q = 0, QT = 0, dim = 0;
+    long long N = 0;
+    size_t S = 0;
+    bool masked = false, has_solid = false;
+    size_t off_f = 0, off_g = 0, off_mask = 0, off_solid = 0, off_partial = 0, off_result = 0;
+    size_t bytes = 0;
+};
+
+inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
+{
+    auto bad = [&](lbm_status s, const char *msg) {
+        *why = msg;
+        return s;
+    };
+    if (!c) return bad(LBM_ERR_ARG, "config is NULL");
+    if (c->lattice != LBM_D3Q19 && c->lattice != LBM_D2Q9)
+        return bad(LBM_ERR_ARG, "lattice must be LBM_D3Q19 or LBM_D2Q9");
+    if (c->thermal != LBM_THERMAL_NONE && c->thermal != LBM_D3Q7 && c->thermal != LBM_D2Q5)
+        return bad(LBM_ERR_ARG, "thermal must be NONE, LBM_D3Q7 or LBM_D2Q5");
+    if ((c->thermal == LBM_D3Q7 && c->lattice != LBM_D3Q19) ||
+        (c->thermal == LBM_D2Q5 && c->lattice != LBM_D2Q9))
+        return bad(LBM_ERR_UNSUPPORTED, "thermal lattice must match: D3Q19+D3Q7 or D2Q9+D2Q5");
+    if (c->collision != LBM_BGK && c->collision != LBM_MRT)
+        return bad(LBM_ERR_ARG, "collision must be LBM_BGK or LBM_MRT");
+    if (c->nx < 1 || c->ny < 1 || c->nz < 1) return bad(LBM_ERR_ARG, "grid sizes must be >= 1");
+    if (c->lattice == LBM_D2Q9 && c->nz != 1) return bad(LBM_ERR_ARG, "D2Q9 needs nz == 1");
+    const long long N = (long long)c->nx * c->ny * c->nz;
+    if (N >= (1LL << 31)) return bad(LBM_ERR_ARG, "nx*ny*nz must be < 2^31");
+    if (c->nz > 65535) return bad(LBM_ERR_UNSUPPORTED, "nz must be <= 65535");
+    if (c->ny > 65535 * 8) return bad(LBM_ERR_UNSUPPORTED, "ny too large");
+    if (c->collision == LBM_BGK && !(std::isfinite(c->tau) && c->tau > 0.5))
+        return bad(LBM_ERR_ARG, "BGK tau must be finite and > 1/2");
+    const int Q = c->lattice;
+    if (c->collision == LBM_MRT)
+        for (int k = 0; k < Q; ++k)
+            if (!conserved_row(Q, k) && !(c->s[k] >= 0.0 && c->s[k] < 2.0))
+                return bad(LBM_ERR_ARG, "MRT rates of non-conserved rows must lie in [0, 2)");
+    const int QT = c->thermal;
+    if (QT) {
+        for (int k = 1; k < QT; ++k)
+            if (!(c->s_T[k] >= 0.0 && c->s_T[k] < 2.0))
+                return bad(LBM_ERR_ARG, "thermal rates must lie in [0, 2)");
+        if (!(c->a_T > -(QT - 1) && c->a_T < 1.0))
+            return bad(LBM_ERR_ARG, "a_T must lie in (-(Q_T - 1), 1)");
+    } else if (c->gbeta != 0.0) {
+        return bad(LBM_ERR_ARG, "buoyancy (gbeta != 0) needs a thermal lattice");
+    }
+    const int dim = (Q == LBM_D3Q19) ? 3 : 2;
+    if (c->up_axis < 0 || c->up_axis >= dim) return bad(LBM_ERR_ARG, "up_axis out of range");
+    if (dim == 2 && c->g_body[2] != 0.0) return bad(LBM_ERR_ARG, "g_body[2] must be 0 in 2-D");
+    for (int a = 0; a < 3; ++a)
+        if (!std::isfinite(c->g_body[a])) return bad(LBM_ERR_ARG, "g_body must be finite");
+    if (!std::isfinite(c->gbeta) || !std::isfinite(c->T0))
+        return bad(LBM_ERR_ARG, "gbeta and T0 must be finite");
+    bool any_wall = false;
+    for (int i = 0; i < 2 * dim; ++i) {
+        if (c->face_flow[i] != LBM_FACE_PERIODIC && c->face_flow[i] != LBM_FACE_WALL)
+            return bad(LBM_ERR_ARG, "face_flow entries must be PERIODIC or WALL");
+        if (c->face_T[i] != LBM_TFACE_ADIABATIC && c->face_T[i] != LBM_TFACE_DIRICHLET)
+            return bad(LBM_ERR_ARG, "face_T entries must be ADIABATIC or DIRICHLET");
+        if (!std::isfinite(c->T_wall[i])) return bad(LBM_ERR_ARG, "T_wall must be finite");
+        any_wall |= c->face_flow[i] == LBM_FACE_WALL;
+    }
+    for (int a = 0; a < dim; ++a)
+        if (c->face_flow[2 * a] != c->face_flow[2 * a + 1])
+            return bad(LBM_ERR_UNSUPPORTED,
+                       "both faces of an axis must have the same flow kind (AA addressing)");
+
+    L->Q = Q;
+    L->QT = QT;
+    L->dim = dim;
+    L->N = N;
+    L->S = ((size_t)N + 63) / 64 * 64;
+    L->has_solid = c->solid_mask != nullptr;
+    L->masked = any_wall || L->has_solid;
+    size_t off = 0;
+    L->off_f = off;
+    off = align_up(off + (size_t)Q * L->S * sizeof(float));
+    L->off_g = off;
+    off = align_up(off + (size_t)QT * L->S * sizeof(float));
+    L->off_mask = off;
+    if (L->masked) off = align_up(off + L->S * sizeof(uint32_t));
+    L->off_solid = off;
+    if (L->has_solid) off = align_up(off + L->S);
+    L->off_partial = off;
+    off = align_up(off + (size_t)lbm::DIAG_BLOCKS * lbm::DIAG_N * sizeof(double));
+    L->off_result = off;
+    off = align_up(off + lbm::DIAG_N * sizeof(double));
+    L->bytes = off;
+    return LBM_OK;
+}
+
+inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Params &P)
+{
+    P.f = reinterpret_cast<float *>(ws + L.off_f);
+    P.g = L.QT ? reinterpret_cast<float *>(ws + L.off_g) : nullptr;
+    P.mask = L.masked ? reinterpret_cast<const uint32_t *>(ws + L.off_mask) : nullptr;
+    P.S = L.S;
+    P.nx = g.nx;
+    P.ny = g.ny;
+    P.nz = g.nz;
+    lbm::CollideParams &C = P.c;
+    C.omega = (float)(1.0 / g.tau);
+    C.fcoef = (float)(1.0 - 0.5 / g.tau);
+    const double *norm = (g.lattice == LBM_D3Q19) ? NORM_D3Q19 : NORM_D2Q9;
+    for (int k = 0; k < 19; ++k) {
+        C.mA[k] = 0.0f;
+        C.mB[k] = 0.0f;
+    }
+    for (int k = 0; k < g.lattice; ++k) {
+        if (k == 0) continue;
+        if (conserved_row(g.lattice, k)) {
+            C.mB[k] = (float)(1.0 / norm[k]);
+        } else if (g.collision == LBM_MRT) {
+            C.mA[k] = (float)(g.s[k] / norm[k]);
+            C.mB[k] = (float)((1.0 - 0.5 * g.s[k]) / norm[k]);
+        }
+    }
+    for (int k = 0; k < 7; ++k) C.tA[k] = 0.0f;
+    const double *tnorm = (g.thermal == LBM_D3Q7) ? NORM_D3Q7 : NORM_D2Q5;
+    for (int k = 1; k < g.thermal; ++k) C.tA[k] = (float)(g.s_T[k] / tnorm[k]);
+    C.a_T = (float)g.a_T;
+    C.gx = (float)g.g_body[0];
+    C.gy = (float)g.g_body[1];
+    C.gz = (float)g.g_body[2];
+    C.gbeta = (float)g.gbeta;
+    C.T0 = (float)g.T0;
+    C.up_axis = g.up_axis;
+    const int dim = L.dim;
+    for (int i = 0; i < 6; ++i) {
+        const bool active = i < 2 * dim;
+        P.face_wall[i] = active && g.face_flow[i] == LBM_FACE_WALL;
+        P.face_dir[i] = P.face_wall[i] && g.thermal && g.face_T[i] == LBM_TFACE_DIRICHLET;
+        P.T_wall[i] = (float)g.T_wall[i];
+    }
+    // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)
+    const double omega = (g.thermal == LBM_D2Q5) ? (4.0 + g.a_T) / 10.0 : (6.0 + g.a_T) / 21.0;
+    for (int k = 0; k < 7; ++k) P.abbT[k] = 0.0f;
+    for (int k = 1; k < g.thermal; ++k) {
+        const int cx = (g.lattice == 19) ? lbm::D3Q19::cx(k) : lbm::D2Q9::cx(k);
+        const int cy = (g.lattice == 19) ? lbm::D3Q19::cy(k) : lbm::D2Q9::cy(k);
+        const int cz = (g.lattice == 19) ? lbm::D3Q19::cz(k) : lbm::D2Q9::cz(k);
+        P.abbT[k] = (float)(omega * g.T_wall[lbm::axis_face(cx, cy, cz)]);
+    }
+}
+
+}  // namespace lbm_setup

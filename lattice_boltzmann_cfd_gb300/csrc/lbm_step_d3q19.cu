@@ -1,0 +1,37 @@
+// D3Q19 (optionally + D3Q7) instantiations of the fused AA step kernel.
+#include "lbm_internal.h"
+
+namespace lbm {
+namespace {
+
+template <class TL, int C, bool M, bool O>
+cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s)
+{
+    step_kernel<D3Q19, TL, C, M, O><<<sh.grid, sh.block, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
+using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
+
+template <class TL>
+cudaError_t dispatch(int coll, bool masked, bool odd, const Params &P, const Shape &sh,
+                     cudaStream_t s)
+{
+    static const Fn table[2][2][2] = {
+        {{go<TL, 0, false, false>, go<TL, 0, false, true>},
+         {go<TL, 0, true, false>, go<TL, 0, true, true>}},
+        {{go<TL, 1, false, false>, go<TL, 1, false, true>},
+         {go<TL, 1, true, false>, go<TL, 1, true, true>}}};
+    return table[coll ? 1 : 0][masked ? 1 : 0][odd ? 1 : 0](P, sh, s);
+}
+
+}  // namespace
+
+cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, const Params &P,
+                              const Shape &sh, cudaStream_t s)
+{
+    if (thermal == 7) return dispatch<D3Q7>(coll, masked, odd, P, sh, s);
+    return dispatch<NoThermal>(coll, masked, odd, P, sh, s);
+}
+
+}  // namespace lbm

@@ -132,7 +132,7 @@ def random_periodic(n: int = 128, seed: int = 2, nu: float = 0.01, shape=None,
     name = f"D{dim}Q{lattice} {collision.upper()} periodic {nx}x{ny}x{nz} random"
     return Workload(name=name, lattice=lattice, thermal=0, collision=collision,
                     shape=(nx, ny, nz), nu=nu, rates=_momentum_rates(lattice), rho0=rho,
-                    u0=u, steps=1000)
+                    u0=u, up_axis=dim - 1, steps=1000)
 
 
 def sphere_mask(shape, center, radius) -> np.ndarray:

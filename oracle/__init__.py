@@ -38,12 +38,12 @@ BGK, MRT = 0, 1
 
 
 def build(force: bool = False) -> str:
-    """Compile liblbm_oracle.so next to its source (gcc, OpenMP, -O2)."""
+    """Compile liblbm_oracle.so next to its source (gcc, OpenMP, -O3)."""
     stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < max(
         os.path.getmtime(_SRC), os.path.getmtime(os.path.join(_HERE, "lbm_oracle.h")))
     if force or stale:
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-std=c11", "-shared", "-fPIC",
+        subprocess.check_call(["gcc", "-O3", "-fopenmp", "-std=c11", "-shared", "-fPIC",
                                "-o", tmp, _SRC, "-lm"], cwd=_HERE)
         os.replace(tmp, _LIB)
     return _LIB

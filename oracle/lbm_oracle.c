@@ -452,66 +452,67 @@ int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, do
         for (int q = 0; q < QT; ++q) gpost[q * W + n] = go[q];
     }
 
-    /* 2. pull streaming back into the state buffer, one z-plane per task; the momentum
-     *    exchange of each plane is summed in plane order afterwards. */
-    double *plane_force = (double *)calloc((size_t)wz * 3, sizeof(double));
-    if (!plane_force) return -40;
+    /* 2. pull streaming back into the state buffer, one x-row per task; the momentum
+     *    exchange of each row is summed in row order afterwards. */
+    const long rows = (long)wy * wz;
+    double *row_force = (double *)calloc((size_t)rows * 3, sizeof(double));
+    if (!row_force) return -40;
 #pragma omp parallel for schedule(static)
-    for (int k = 0; k < wz; ++k) {
+    for (long r = 0; r < rows; ++r) {
+        const int j = (int)(r % wy), k = (int)(r / wy);
         double pf[3] = {0, 0, 0};
-        for (int j = 0; j < wy; ++j)
-            for (int i = 0; i < wx; ++i) {
-                const long n = i + (long)wx * (j + (long)wy * k);
-                if (is_solid(&C, n)) {
-                    for (int q = 0; q < Q; ++q) f[q * W + n] = 0.0;
-                    for (int q = 0; q < QT; ++q) g[q * W + n] = 0.0;
-                    continue;
-                }
-                for (int q = 0; q < Q; ++q) {
-                    long ns = 0;
-                    int face = -1;
-                    const int kind = pull_source(&C, i, j, k, C.F.c[q], &ns, &face);
-                    const int o = C.F.opp[q];
-                    if (kind == SRC_CELL) {
-                        f[q * W + n] = fpost[q * W + ns];
-                    } else if (kind == SRC_UNKNOWN) {
-                        f[q * W + n] = NAN;
-                    } else {
-                        /* half-way bounce-back: f_q(x, t+1) = f+_opp(q)(x, t) */
-                        const double v = fpost[o * W + n];
-                        f[q * W + n] = v;
-                        if (kind == SRC_SOLID)
-                            for (int a = 0; a < 3; ++a) pf[a] += 2.0 * v * C.F.c[o][a];
-                    }
-                }
-                for (int q = 0; q < QT; ++q) {
-                    long ns = 0;
-                    int face = -1;
-                    const int kind = pull_source(&C, i, j, k, C.G.c[q], &ns, &face);
-                    const int o = C.G.opp[q];
-                    if (kind == SRC_CELL) {
-                        g[q * W + n] = gpost[q * W + ns];
-                    } else if (kind == SRC_UNKNOWN) {
-                        g[q * W + n] = NAN;
-                    } else if (kind == SRC_FACE_WALL && p->face_T[face] == ORC_DIRICHLET) {
-                        /* half-way anti-bounce-back: g_q = -g+_opp(q) + omega T_w */
-                        g[q * W + n] = -gpost[o * W + n] + C.omega * p->T_wall[face];
-                    } else {
-                        /* adiabatic wall or solid: half-way bounce-back */
-                        g[q * W + n] = gpost[o * W + n];
-                    }
+        for (int i = 0; i < wx; ++i) {
+            const long n = i + (long)wx * (j + (long)wy * k);
+            if (is_solid(&C, n)) {
+                for (int q = 0; q < Q; ++q) f[q * W + n] = 0.0;
+                for (int q = 0; q < QT; ++q) g[q * W + n] = 0.0;
+                continue;
+            }
+            for (int q = 0; q < Q; ++q) {
+                long ns = 0;
+                int face = -1;
+                const int kind = pull_source(&C, i, j, k, C.F.c[q], &ns, &face);
+                const int o = C.F.opp[q];
+                if (kind == SRC_CELL) {
+                    f[q * W + n] = fpost[q * W + ns];
+                } else if (kind == SRC_UNKNOWN) {
+                    f[q * W + n] = NAN;
+                } else {
+                    /* half-way bounce-back: f_q(x, t+1) = f+_opp(q)(x, t) */
+                    const double v = fpost[o * W + n];
+                    f[q * W + n] = v;
+                    if (kind == SRC_SOLID)
+                        for (int a = 0; a < 3; ++a) pf[a] += 2.0 * v * C.F.c[o][a];
                 }
             }
-        plane_force[3 * k + 0] = pf[0];
-        plane_force[3 * k + 1] = pf[1];
-        plane_force[3 * k + 2] = pf[2];
+            for (int q = 0; q < QT; ++q) {
+                long ns = 0;
+                int face = -1;
+                const int kind = pull_source(&C, i, j, k, C.G.c[q], &ns, &face);
+                const int o = C.G.opp[q];
+                if (kind == SRC_CELL) {
+                    g[q * W + n] = gpost[q * W + ns];
+                } else if (kind == SRC_UNKNOWN) {
+                    g[q * W + n] = NAN;
+                } else if (kind == SRC_FACE_WALL && p->face_T[face] == ORC_DIRICHLET) {
+                    /* half-way anti-bounce-back: g_q = -g+_opp(q) + omega T_w */
+                    g[q * W + n] = -gpost[o * W + n] + C.omega * p->T_wall[face];
+                } else {
+                    /* adiabatic wall or solid: half-way bounce-back */
+                    g[q * W + n] = gpost[o * W + n];
+                }
+            }
+        }
+        row_force[3 * r + 0] = pf[0];
+        row_force[3 * r + 1] = pf[1];
+        row_force[3 * r + 2] = pf[2];
     }
     if (force) {
         force[0] = force[1] = force[2] = 0.0;
-        for (int k = 0; k < wz; ++k)
-            for (int a = 0; a < 3; ++a) force[a] += plane_force[3 * k + a];
+        for (long r = 0; r < rows; ++r)
+            for (int a = 0; a < 3; ++a) force[a] += row_force[3 * r + a];
     }
-    free(plane_force);
+    free(row_force);
     return 0;
 }
 

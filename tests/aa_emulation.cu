@@ -1,0 +1,168 @@
+// Host emulation of the CUDA path's AA step, for tests only (built by tests/conftest.py).
+//
+// Runs the library's own per-cell functions (cell_mask, init_cell, load_cell, collide,
+// store_cell) on the CPU, one cell at a time, but writes every step into a second buffer
+// filled with NaN beforehand.  If a cell read a slot that another cell writes in the
+// same step, or two cells wrote one slot, or a slot of a fluid cell were left unwritten,
+// the stale or NaN value would reach the results; tests compare them with the oracle.
+// The read-out uses the parity-aware logical load, as lbm_get_populations does.
+#include <cmath>
+#include <cstring>
+#include <limits>
+#include <vector>
+
+#include "lbm_setup.h"
+
+using namespace lbm;
+
+namespace {
+
+template <class L, class TL, int C, bool M, bool O>
+void step_all(const Params &Pr, const Params &Pw)
+{
+    for (int z = 0; z < Pr.nz; ++z)
+        for (int y = 0; y < Pr.ny; ++y)
+            for (int x = 0; x < Pr.nx; ++x) {
+                const int idx = x + Pr.nx * (y + Pr.ny * z);
+                uint32_t m = 0;
+                if (M) {
+                    m = Pr.mask[idx];
+                    if (m & SOLID_BIT) continue;
+                }
+                Offs o{};
+                if (O) o = make_offs(x, y, z, Pr);
+                float f[L::Q], g[TL::QA];
+                load_cell<L, TL, M, O>(Pr, idx, o, m, f, g);
+                collide<L, TL, C>(f, g, Pr.c);
+                store_cell<L, TL, M, O>(Pw, idx, o, m, f, g);
+            }
+}
+
+template <class L, class TL, bool M, bool O>
+void read_all(const Params &P, float *fout, float *gout)
+{
+    const size_t N = (size_t)P.nx * P.ny * P.nz;
+    for (int z = 0; z < P.nz; ++z)
+        for (int y = 0; y < P.ny; ++y)
+            for (int x = 0; x < P.nx; ++x) {
+                const int idx = x + P.nx * (y + P.ny * z);
+                uint32_t m = M ? P.mask[idx] : 0u;
+                float f[L::Q], g[TL::QA];
+                if (m & SOLID_BIT) {
+                    for (int q = 0; q < L::Q; ++q) fout[q * N + idx] = 0.0f;
+                    for (int k = 0; k < TL::Q; ++k) gout[k * N + idx] = 0.0f;
+                    continue;
+                }
+                Offs o{};
+                if (O) o = make_offs(x, y, z, P);
+                load_cell<L, TL, M, O>(P, idx, o, m, f, g);
+                for (int q = 0; q < L::Q; ++q) fout[q * N + idx] = f[q] + L::w(q);
+                for (int k = 0; k < TL::Q; ++k) gout[k * N + idx] = g[k];
+            }
+}
+
+template <class L, class TL, int C>
+int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, const float *u,
+        const float *T, int steps, float *fout, float *gout, uint32_t *mask_out)
+{
+    const float nan = std::numeric_limits<float>::quiet_NaN();
+    const size_t S = Lay.S;
+    std::vector<float> f(Lay.Q * S, nan), fn(Lay.Q * S, nan);
+    std::vector<float> g((Lay.QT ? Lay.QT : 1) * S, nan), gn((Lay.QT ? Lay.QT : 1) * S, nan);
+    std::vector<uint32_t> mask(S, 0u);
+    std::vector<char> ws(Lay.bytes + 256);
+    Params P{};
+    lbm_setup::fill_params(cfg, Lay, ws.data(), P);
+    P.f = f.data();
+    P.g = Lay.QT ? g.data() : nullptr;
+    P.mask = Lay.masked ? mask.data() : nullptr;
+    if (Lay.masked)
+        for (int z = 0; z < cfg.nz; ++z)
+            for (int y = 0; y < cfg.ny; ++y)
+                for (int x = 0; x < cfg.nx; ++x)
+                    mask[x + cfg.nx * (y + cfg.ny * z)] =
+                        cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
+    for (long long i = 0; i < Lay.N; ++i) init_cell<L, TL>(P, (int)i, rho, u, T);
+    int parity = 0;
+    for (int s = 0; s < steps; ++s) {
+        std::fill(fn.begin(), fn.end(), nan);
+        std::fill(gn.begin(), gn.end(), nan);
+        Params Pw = P;
+        Pw.f = fn.data();
+        Pw.g = Lay.QT ? gn.data() : nullptr;
+        if (Lay.masked) {
+            if (parity) step_all<L, TL, C, true, true>(P, Pw);
+            else step_all<L, TL, C, true, false>(P, Pw);
+        } else {
+            if (parity) step_all<L, TL, C, false, true>(P, Pw);
+            else step_all<L, TL, C, false, false>(P, Pw);
+        }
+        f.swap(fn);
+        g.swap(gn);
+        P.f = f.data();
+        P.g = Lay.QT ? g.data() : nullptr;
+        parity ^= 1;
+    }
+    if (Lay.masked) {
+        if (parity) read_all<L, TL, true, true>(P, fout, gout);
+        else read_all<L, TL, true, false>(P, fout, gout);
+    } else {
+        if (parity) read_all<L, TL, false, true>(P, fout, gout);
+        else read_all<L, TL, false, false>(P, fout, gout);
+    }
+    if (mask_out) std::memcpy(mask_out, mask.data(), sizeof(uint32_t) * (size_t)Lay.N);
+    return 0;
+}
+
+}  // namespace
+
+extern "C" int emu_run(const lbm_config *cfg, const float *rho, const float *u, const float *T,
+                       int steps, float *fout, float *gout, uint32_t *mask_out)
+{
+    lbm_setup::Layout Lay;
+    std::string why;
+    if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
+    const bool mrt = cfg->collision == LBM_MRT;
+    if (cfg->lattice == 19) {
+        if (cfg->thermal == 7)
+            return mrt ? run<D3Q19, D3Q7, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                       : run<D3Q19, D3Q7, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+        return mrt ? run<D3Q19, NoThermal, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                   : run<D3Q19, NoThermal, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+    }
+    if (cfg->thermal == 5)
+        return mrt ? run<D2Q9, D2Q5, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                   : run<D2Q9, D2Q5, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+    return mrt ? run<D2Q9, NoThermal, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+               : run<D2Q9, NoThermal, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+}
+
+// Every neighbour index the odd-step access pattern forms (idx + offset of +-c_q for each
+// direction, with the periodic wrap) must name a cell of the grid: returns the number of
+// out-of-range indices over all cells (0 expected).
+extern "C" long long emu_count_bad_indices(int lattice, int nx, int ny, int nz)
+{
+    Params P{};
+    P.nx = nx;
+    P.ny = ny;
+    P.nz = nz;
+    const long long N = (long long)nx * ny * nz;
+    long long bad = 0;
+    for (int z = 0; z < nz; ++z)
+        for (int y = 0; y < ny; ++y)
+            for (int x = 0; x < nx; ++x) {
+                const long long idx = x + (long long)nx * (y + (long long)ny * z);
+                const Offs o = make_offs(x, y, z, P);
+                const int Q = lattice;
+                for (int q = 0; q < Q; ++q) {
+                    const int cx = lattice == 19 ? D3Q19::cx(q) : D2Q9::cx(q);
+                    const int cy = lattice == 19 ? D3Q19::cy(q) : D2Q9::cy(q);
+                    const int cz = lattice == 19 ? D3Q19::cz(q) : D2Q9::cz(q);
+                    for (int sgn = -1; sgn <= 1; sgn += 2) {
+                        const long long j = idx + nb(o, sgn * cx, sgn * cy, sgn * cz);
+                        if (j < 0 || j >= N) ++bad;
+                    }
+                }
+            }
+    return bad;
+}

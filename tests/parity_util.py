@@ -1,0 +1,167 @@
+"""Helpers shared by the parity tests: run a workload through the oracle, through the
+CUDA library (GPU) or through the host emulation of its kernels, and compare."""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import numpy as np
+
+from lattice_boltzmann_cfd_gb300 import workloads as W
+from lattice_boltzmann_cfd_gb300.solver import make_config
+
+# the benchmark spec tolerances: fp32 GPU vs fp64 oracle after 200 steps
+TOL_FIELDS = 2e-5      # max-abs on rho, u, T
+TOL_FORCE_REL = 1e-4   # relative on the solid force
+
+
+def fluid_of(w):
+    return np.ones(w.grid, bool) if w.solid is None else (w.solid == 0)
+
+
+def oracle_states(oracle, w, checkpoints, window=None):
+    """{steps: dict(f, g, rho, u, T, force, diag)} from the fp64 oracle."""
+    p = oracle.Problem(w, window)
+    f, g = oracle.init_equilibrium(p, w.rho0, w.u0, w.T_init)
+    out, done = {}, 0
+    for n in sorted(checkpoints):
+        force = oracle.run(p, f, g, n - done)
+        done = n
+        rho, u, T = oracle.macroscopic(p, f, g)
+        out[n] = dict(f=f.copy(), g=g.copy(), rho=rho, u=u, T=T, force=force,
+                      diag=oracle.diagnostics(p, f, g) if window is None else None)
+    return out
+
+
+def mask_brute_force(w) -> np.ndarray:
+    """The link mask from its definition (numpy, independent of the library): bit q when
+    the neighbour along c_q is outside through a WALL face or solid; bit 19+k when thermal
+    axis link k leaves through a Dirichlet face; bit 31 for a solid cell."""
+    c = {19: [(0, 0, 0), (1, 0, 0), (-1, 0, 0), (0, 1, 0), (0, -1, 0), (0, 0, 1), (0, 0, -1),
+              (1, 1, 0), (-1, 1, 0), (1, -1, 0), (-1, -1, 0), (1, 0, 1), (-1, 0, 1), (1, 0, -1),
+              (-1, 0, -1), (0, 1, 1), (0, -1, 1), (0, 1, -1), (0, -1, -1)],
+         9: [(0, 0, 0), (1, 0, 0), (0, 1, 0), (-1, 0, 0), (0, -1, 0), (1, 1, 0), (-1, 1, 0),
+             (-1, -1, 0), (1, -1, 0)]}[w.lattice]
+    nz, ny, nx = w.grid
+    solid = np.zeros(w.grid, bool) if w.solid is None else w.solid.astype(bool)
+    z, y, x = np.meshgrid(np.arange(nz), np.arange(ny), np.arange(nx), indexing="ij")
+    m = np.zeros(w.grid, np.uint64)
+    wall_face = [k == "wall" for k in w.face_flow]
+    dirichlet = [bool(w.face_flow[i] == "wall" and w.face_T[i] == "dirichlet" and w.thermal)
+                 for i in range(6)]
+    for q in range(1, w.lattice):
+        cx, cy, cz = c[q]
+        wall = np.zeros(w.grid, bool)
+        dir_hit = np.zeros(w.grid, bool)
+        coords = []
+        for a, (pos, d, n) in enumerate(((x, cx, nx), (y, cy, ny), (z, cz, nz))):
+            s = pos + d
+            lo, hi = s < 0, s >= n
+            if wall_face[2 * a]:
+                wall |= lo
+                dir_hit |= lo & dirichlet[2 * a]
+            if wall_face[2 * a + 1]:
+                wall |= hi
+                dir_hit |= hi & dirichlet[2 * a + 1]
+            coords.append(np.mod(s, n))
+        wall |= ~wall & solid[coords[2], coords[1], coords[0]]
+        m |= wall.astype(np.uint64) << np.uint64(q)
+        if w.thermal and q < w.thermal:
+            m |= dir_hit.astype(np.uint64) << np.uint64(19 + q)
+    m = np.where(solid, np.uint64(1 << 31), m)
+    return m.astype(np.uint32)
+
+
+def emulate(emu_lib, w, steps):
+    """(f, g, mask) after ``steps`` steps of the host emulation of the CUDA kernels."""
+    cfg, keep = make_config(w)
+    N = w.cells
+    fo = np.zeros((w.lattice, N), np.float32)
+    go = np.zeros((max(w.thermal, 1), N), np.float32)
+    mo = np.zeros(N, np.uint32)
+    rho = np.ascontiguousarray(w.rho0, np.float32)
+    u = np.ascontiguousarray(w.u0, np.float32)
+    T = np.ascontiguousarray(w.T_init, np.float32) if w.thermal else None
+    vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = emu_lib.emu_run(ctypes.byref(cfg), vp(rho), vp(u), vp(T), int(steps), vp(fo), vp(go),
+                         vp(mo))
+    assert rc == 0
+    return (fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid),
+            mo.reshape(w.grid))
+
+
+def small_cases():
+    """Small problems covering every lattice, collision, boundary kind and forcing."""
+    cases = [W.random_periodic(shape=(6, 5, 4), seed=1),
+             W.random_periodic(shape=(6, 5, 4), seed=1, collision="bgk"),
+             W.random_periodic(shape=(7, 5, 1), seed=2, lattice=9),
+             W.taylor_green(n=8)]
+    cs = W.perturbed(W.channel_sphere(shape=(12, 10, 9), center=(5, 4, 4), radius=2.5), seed=3)
+    cases.append(dataclasses.replace(cs, g_body=(1e-4, 2e-5, -1e-5)))
+    c3 = W.perturbed(W.cavity3d(shape=(9, 7, 6)), seed=4)
+    sol = np.zeros(c3.grid, np.uint8)
+    sol[2:4, 3:5, 4:6] = 1
+    cases.append(dataclasses.replace(c3, solid=sol, gbeta=0.01))
+    cases.append(dataclasses.replace(c3, collision="bgk", gbeta=0.02, up_axis=0))
+    c2 = dataclasses.replace(W.perturbed(W.cavity2d(shape=(10, 8, 1)), seed=5), gbeta=0.01)
+    cases.append(c2)
+    cases.append(dataclasses.replace(
+        c2, face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"),
+        face_T=("adiabatic", "adiabatic", "dirichlet", "dirichlet", "adiabatic", "adiabatic"),
+        T_wall=(0.0, 0.0, 0.3, -0.2, 0.0, 0.0)))
+    return cases
+
+
+def split_steps(n):
+    """Uneven chunks so that parity is carried across lbm_step calls (97 + 103 = 200)."""
+    out = []
+    while n > 0:
+        c = min(n, 97 if not out else 103)
+        out.append(c)
+        n -= c
+    return out
+
+
+def gpu_states(w, checkpoints, window_fn=None, edit=None):
+    """{steps: dict} of the CUDA path's results (numpy), stepping in uneven chunks."""
+    import torch
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    sim = Simulation(w, edit=edit)
+    dev = sim.device
+    T = torch.from_numpy(np.ascontiguousarray(w.T_init)).to(dev) if w.thermal else None
+    sim.init_equilibrium(torch.from_numpy(np.ascontiguousarray(w.rho0)).to(dev),
+                         torch.from_numpy(np.ascontiguousarray(w.u0)).to(dev), T)
+    out, done = {}, 0
+    for n in sorted(checkpoints):
+        for c in split_steps(n - done):
+            sim.step(c)
+        done = n
+        rho, u, Tt = sim.macroscopic()
+        f, g = sim.populations()
+        r = dict(rho=rho, u=u, T=Tt, f=f, g=g)
+        if window_fn is None:
+            r = {k: (None if v is None else v.cpu().numpy()) for k, v in r.items()}
+            r["diag"] = sim.diagnostics(allow_nonfinite=True)
+        else:
+            r = window_fn(r)
+        r["parity"] = sim.parity
+        out[n] = r
+    torch.cuda.synchronize()
+    sim.close()
+    return out
+
+
+def compare_fields(w, got, ref, tol=TOL_FIELDS, pop_tol=None):
+    """Max-abs differences over fluid cells; asserts within tolerance."""
+    fluid = fluid_of(w)
+    errs = {"rho": np.abs(got["rho"] - ref["rho"])[fluid].max(),
+            "u": np.abs(got["u"] - ref["u"])[:, fluid].max(),
+            "f": np.abs(got["f"] - ref["f"])[:, fluid].max()}
+    if w.thermal:
+        errs["T"] = np.abs(got["T"] - ref["T"])[fluid].max()
+        errs["g"] = np.abs(got["g"] - ref["g"])[:, fluid].max()
+    pop_tol = tol if pop_tol is None else pop_tol
+    for k, e in errs.items():
+        lim = pop_tol if k in ("f", "g") else tol
+        assert e <= lim, f"{w.name}: {k} max-abs {e:.3e} > {lim:.1e}"
+    return errs

@@ -1,0 +1,357 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, on the GPU.
+
+Tolerances: max-abs 2e-5 on rho, u, T (and on the populations) and 1e-4 relative on the
+solid force after 200 steps, as the target states for fp32 against fp64; the link mask is
+compared bit for bit.  Every comparison runs at both AA parities (odd and even step
+counts) with lbm_step called in uneven chunks.
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+
+from lattice_boltzmann_cfd_gb300 import workloads as W
+from parity_util import (TOL_FIELDS, TOL_FORCE_REL, compare_fields, fluid_of, gpu_states,
+                         mask_brute_force, oracle_states, small_cases)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CASES = small_cases()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from lattice_boltzmann_cfd_gb300 import capi
+    capi.load()
+
+
+# ----------------------------------------------------------------- small grids ----
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_small_grids_few_steps(oracle_mod, w):
+    """Every lattice / collision / boundary kind on tiny grids after 1, 2, 5, 6 steps."""
+    ref = oracle_states(oracle_mod, w, [1, 2, 5, 6])
+    got = gpu_states(w, [1, 2, 5, 6])
+    for n in ref:
+        compare_fields(w, got[n], ref[n], tol=1e-6)
+        assert got[n]["parity"] == n % 2
+
+
+# --------------------------------------------------- 200 / 201 steps, all configs ---
+
+def _reduced_configs():
+    """The five workloads' physics on grids the oracle finishes in seconds, shaped to span
+    several thread blocks along x with ragged tails (blocks are 256 cells wide)."""
+    cfg1 = W.taylor_green()                                          # full size, 32^3
+    cfg2 = W.random_periodic(shape=(300, 20, 14), seed=2)
+    cfg3 = W.channel_sphere(shape=(300, 24, 20), center=(40, 12, 10), radius=6, gx=1e-5)
+    cfg3p = dataclasses.replace(W.perturbed(cfg3, seed=21), name=cfg3.name + " perturbed")
+    cfg4 = W.cavity2d(shape=(300, 180, 1))
+    cfg4p = W.perturbed(cfg4, seed=22)
+    cfg5 = W.cavity3d(shape=(70, 40, 36))
+    cfg5p = W.perturbed(cfg5, seed=23)
+    return [cfg1, cfg2, cfg3, cfg3p, cfg4, cfg4p, cfg5, cfg5p]
+
+
+REDUCED = _reduced_configs()
+
+
+@pytest.mark.parametrize("w", REDUCED, ids=[c.name for c in REDUCED])
+def test_configs_200_and_201_steps(oracle_mod, w):
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    got = gpu_states(w, [200, 201])
+    for n in (200, 201):
+        compare_fields(w, got[n], ref[n])
+        if w.solid is not None:
+            F, Fr = np.array(got[n]["diag"]["force"]), ref[n]["force"]
+            assert np.linalg.norm(F - Fr) <= TOL_FORCE_REL * np.linalg.norm(Fr), (F, Fr)
+        d, dr = got[n]["diag"], ref[n]["diag"]
+        assert math.isclose(d["mass"], dr["mass"], rel_tol=1e-6)
+        assert np.allclose(d["momentum"], dr["momentum"], rtol=1e-4, atol=1e-6 * dr["mass"])
+        if w.thermal:
+            assert np.allclose(d["heat"], dr["heat"], rtol=1e-4, atol=1e-3)
+
+
+@pytest.mark.parametrize("name", ["random_periodic", "channel_sphere"])
+def test_full_size_128_cubed_200_201(oracle_mod, name):
+    """Configs 2 and 3 at their full 128^3 size, whole domain, 200 and 201 steps."""
+    w = W.by_name(name)
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    got = gpu_states(w, [200, 201])
+    for n in (200, 201):
+        compare_fields(w, got[n], ref[n])
+        if w.solid is not None:
+            F, Fr = np.array(got[n]["diag"]["force"]), ref[n]["force"]
+            assert np.linalg.norm(F - Fr) <= TOL_FORCE_REL * np.linalg.norm(Fr), (F, Fr)
+
+
+# --------------------------------------------------- full sizes: sampled windows ----
+
+def _windows(shape, size, steps, rng, extra=6):
+    """Corner, edge, face-centre, centre and random windows of a grid."""
+    dims = [s for s in shape]
+    spans = []
+    for a, n in enumerate(dims):
+        sz = min(size, n)
+        spans.append([0, (n - sz) // 2, n - sz])
+    out = set()
+    import itertools
+    for combo in itertools.product(*spans):
+        out.add(tuple(combo))
+    for _ in range(extra):
+        out.add(tuple(int(rng.integers(0, max(1, n - min(size, n) + 1))) for n in dims))
+    return [(o, tuple(min(size, n) for n in dims)) for o in sorted(out)]
+
+
+@pytest.mark.parametrize("name,perturb", [("cavity3d", False), ("cavity3d", True),
+                                          ("cavity2d", False), ("cavity2d", True),
+                                          ("random_periodic_512", True)])
+def test_full_size_sampled_windows(oracle_mod, name, perturb):
+    """At the full 512^3 / 4096^2 sizes, in the launch configuration the benchmark uses:
+    after 1, 2 and 3 steps every cell of sampled windows (corners, edges, faces, centre,
+    random) matches the oracle run on that window (cells the window's cut faces can
+    reach are unknown to the oracle and skipped)."""
+    if name == "random_periodic_512":
+        w = W.random_periodic(n=512, seed=2)
+    else:
+        w = W.by_name(name)
+    if perturb and name != "random_periodic_512":
+        w = W.perturbed(w, seed=31)
+    nz, ny, nx = w.grid
+    rng = np.random.default_rng(5)
+    wins = _windows((nx, ny, nz) if w.dim == 3 else (nx, ny, 1), 14, 3, rng)
+
+    def take(r):
+        res = {}
+        for i, ((x0, y0, z0), (wx, wy, wz)) in enumerate(wins):
+            sl = (slice(z0, z0 + wz), slice(y0, y0 + wy), slice(x0, x0 + wx))
+            res[i] = dict(rho=r["rho"][sl].cpu().numpy(), u=r["u"][(slice(None),) + sl].cpu().numpy(),
+                          f=r["f"][(slice(None),) + sl].cpu().numpy(),
+                          T=None if r["T"] is None else r["T"][sl].cpu().numpy(),
+                          g=None if r["g"] is None else r["g"][(slice(None),) + sl].cpu().numpy())
+        return res
+
+    got = gpu_states(w, [1, 2, 3], window_fn=take)
+    compared = 0
+    for i, win in enumerate(wins):
+        ref = oracle_states(oracle_mod, w, [1, 2, 3], window=win)
+        for n in (1, 2, 3):
+            r, g_ = ref[n], got[n][i]
+            known = ~np.isnan(r["rho"])
+            assert known.sum() > 0
+            (x0, y0, z0), (wx, wy, wz) = win
+            fluid = known if w.solid is None else known & (
+                w.solid[z0:z0 + wz, y0:y0 + wy, x0:x0 + wx] == 0)
+            assert np.abs(g_["rho"] - r["rho"])[fluid].max() <= TOL_FIELDS
+            assert np.abs(g_["u"] - r["u"])[:, fluid].max() <= TOL_FIELDS
+            assert np.abs(g_["f"] - r["f"])[:, fluid].max() <= 1e-6
+            if w.thermal:
+                assert np.abs(g_["T"] - r["T"])[fluid].max() <= TOL_FIELDS
+                assert np.abs(g_["g"] - r["g"])[:, fluid].max() <= 1e-6
+            compared += int(fluid.sum())
+    assert compared > 1000
+
+
+# ------------------------------------------------------------------- link mask -----
+
+@pytest.mark.parametrize("name,kw", [("channel_sphere", {}), ("cavity2d", {}),
+                                     ("cavity3d", {"n": 256})],
+                         ids=["channel_sphere_128", "cavity2d_4096", "cavity3d_256"])
+def test_link_mask_bit_exact_full_size(name, kw):
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.by_name(name, **kw)
+    sim = Simulation(w)
+    m = sim.link_mask().cpu().numpy().view(np.uint32)
+    sim.close()
+    assert np.array_equal(m, mask_brute_force(w))
+
+
+# ------------------------------------------------------------ state and errors -----
+
+def test_checkpoint_resume(oracle_mod):
+    """get at step 100 or 101, set into a fresh context, then the remaining steps: the
+    same state as 201 straight steps within fp32 rounding (the read-out adds the rest
+    weights back in fp32, which rounds by at most one ulp of w_q)."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.perturbed(W.cavity3d(shape=(40, 20, 18)), seed=41)
+    dev = torch.device("cuda")
+
+    def start():
+        s = Simulation(w)
+        s.init_equilibrium(torch.from_numpy(w.rho0).to(dev), torch.from_numpy(w.u0).to(dev),
+                           torch.from_numpy(w.T_init).to(dev))
+        return s
+
+    a = start()
+    a.step(201)
+    fa, ga = a.populations()
+    for k in (100, 101):
+        b = start()
+        b.step(k)
+        fb, gb = b.populations()
+        c = Simulation(w)
+        c.set_populations(fb, gb)
+        assert c.parity == 0
+        c.step(201 - k)
+        fc, gc = c.populations()
+        assert (fa - fc).abs().max().item() < 1e-6
+        assert (ga - gc).abs().max().item() < 1e-6
+        b.close()
+        c.close()
+    a.close()
+
+
+@pytest.mark.parametrize("parity", [0, 1])
+def test_set_get_roundtrip(parity):
+    """set then get returns the populations bit for bit at either parity (values within
+    a factor 2 of w_q subtract and re-add exactly)."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.perturbed(W.channel_sphere(shape=(40, 16, 14), center=(10, 8, 7), radius=3), seed=3)
+    sim = Simulation(w)
+    dev = sim.device
+    sim.init_equilibrium(torch.from_numpy(w.rho0).to(dev), torch.from_numpy(w.u0).to(dev))
+    sim.step(parity)
+    f, _ = sim.populations()
+    f2 = f + 1e-3 * torch.rand_like(f)
+    solid = torch.from_numpy(w.solid.astype(bool)).to(dev)
+    f2[:, solid] = 0
+    sim.set_populations(f2)
+    assert sim.parity == parity
+    f3, _ = sim.populations()
+    assert torch.equal(f3, f2)
+    sim.close()
+
+
+def test_pure_streaming_is_exact_permutation():
+    """All rates 0 and no force: a step only streams; after 1 and 2 steps (both AA forms)
+    the populations are exactly the np.roll of the initial ones."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+
+    def zero_rates(cfg):
+        for k in range(19):
+            cfg.s[k] = 0.0
+
+    w = W.random_periodic(shape=(37, 6, 5), seed=7)
+    sim = Simulation(w, edit=zero_rates)
+    rng = np.random.default_rng(0)
+    f0 = (1.0 / 19 + 1e-3 * rng.standard_normal((19,) + w.grid)).astype(np.float32)
+    sim.set_populations(torch.from_numpy(f0).cuda())
+    c = [(0, 0, 0), (1, 0, 0), (-1, 0, 0), (0, 1, 0), (0, -1, 0), (0, 0, 1), (0, 0, -1),
+         (1, 1, 0), (-1, 1, 0), (1, -1, 0), (-1, -1, 0), (1, 0, 1), (-1, 0, 1), (1, 0, -1),
+         (-1, 0, -1), (0, 1, 1), (0, -1, 1), (0, 1, -1), (0, -1, -1)]
+    w_q = np.array([1 / 3] + [1 / 18] * 6 + [1 / 36] * 12, np.float32)
+    for n in (1, 2, 3):
+        sim.step(1)
+        f, _ = sim.populations()
+        f = f.cpu().numpy()
+        for q in range(19):
+            want = np.roll(f0[q], shift=(n * c[q][2], n * c[q][1], n * c[q][0]), axis=(0, 1, 2))
+            # stored shifted by w_q in fp32: (v - w) + w may round, so allow 1 ulp of w
+            assert np.abs(f[q] - want).max() <= 2 * np.spacing(np.float32(w_q[q])), (n, q)
+    sim.close()
+
+
+def test_nonfinite_state_is_reported():
+    from lattice_boltzmann_cfd_gb300 import Simulation, capi
+    w = W.random_periodic(shape=(16, 8, 8), seed=1)
+    rho = w.rho0.copy()
+    rho[3, 4, 5] = np.nan
+    sim = Simulation(w)
+    sim.init_equilibrium(torch.from_numpy(rho).cuda(), torch.from_numpy(w.u0).cuda())
+    sim.step(3)
+    with pytest.raises(capi.LbmError) as e:
+        sim.diagnostics()
+    assert e.value.status == capi.LBM_ERR_NONFINITE
+    d = sim.diagnostics(allow_nonfinite=True)
+    assert not d["finite"]
+    sim.close()
+
+
+def test_state_errors_and_zero_steps():
+    from lattice_boltzmann_cfd_gb300 import Simulation, capi
+    w = W.random_periodic(shape=(16, 8, 8), seed=1)
+    sim = Simulation(w)
+    with pytest.raises(capi.LbmError) as e:
+        sim.step(1)
+    assert e.value.status == capi.LBM_ERR_STATE
+    sim.init_equilibrium(torch.from_numpy(w.rho0).cuda(), torch.from_numpy(w.u0).cuda())
+    f0, _ = sim.populations()
+    sim.step(0)
+    f1, _ = sim.populations()
+    assert torch.equal(f0, f1) and sim.steps_taken == 0
+    with pytest.raises(capi.LbmError):
+        sim.step(-1)
+    sim.close()
+
+
+def test_page_locked_host_buffers_match_device():
+    """Fields given in page-locked host memory (read and written by the kernels over the
+    host link) give the same state and read-out as device tensors."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.perturbed(W.cavity3d(shape=(48, 20, 16)), seed=9)
+    outs = []
+    for host in (False, True):
+        sim = Simulation(w)
+        if host:
+            args = [torch.from_numpy(a).pin_memory() for a in (w.rho0, w.u0, w.T_init)]
+        else:
+            args = [torch.from_numpy(a).cuda() for a in (w.rho0, w.u0, w.T_init)]
+        sim.init_equilibrium(*args)
+        sim.step(7)
+        if host:
+            rho = torch.empty(w.grid).pin_memory()
+            u = torch.empty((3,) + w.grid).pin_memory()
+            T = torch.empty(w.grid).pin_memory()
+            sim.macroscopic(rho, u, T)
+            torch.cuda.synchronize()
+        else:
+            rho, u, T = (t.cpu() for t in sim.macroscopic())
+        outs.append((rho.clone(), u.clone(), T.clone()))
+        sim.close()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------- physics on the GPU ----
+
+def test_gpu_taylor_green_decay_rate():
+    """Config 1 on the GPU: fitted decay rate over t in [50, 200] within 1% of 3 nu k^2."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.taylor_green()
+    sim = Simulation(w)
+    sim.init_equilibrium(torch.from_numpy(w.rho0).cuda(), torch.from_numpy(w.u0).cuda())
+    n, k = 32, 2 * math.pi / 32
+    z, y, x = np.meshgrid(np.arange(n), np.arange(n), np.arange(n), indexing="ij")
+    mode = np.sin(k * x) * np.cos(k * y) * np.cos(k * z)
+    sim.step(50)
+    ts, amps = [], []
+    for t in range(50, 201, 25):
+        if t > 50:
+            sim.step(25)
+        u = sim.macroscopic()[1].cpu().numpy().astype(np.float64)
+        ts.append(t)
+        amps.append((u[0] * mode).sum() / (mode * mode).sum())
+    rate = -np.polyfit(ts, np.log(amps), 1)[0]
+    assert abs(rate / (3 * w.nu * k * k) - 1) < 0.01
+    sim.close()
+
+
+def test_gpu_poiseuille_profile():
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    H, nu, gx = 32, 0.1, 1e-5
+    w = W.Workload(name="poiseuille", lattice=19, thermal=0, collision="mrt", shape=(4, H, 2),
+                   nu=nu, rates={"e": 1.2, "eps": 1.2, "q": 1.2, "pi": 1.2, "m": 1.2},
+                   g_body=(gx, 0, 0),
+                   face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"))
+    sim = Simulation(w)
+    sim.init_equilibrium(torch.ones(w.grid).cuda(), torch.zeros((3,) + w.grid).cuda())
+    sim.step(int(8 * H * H / nu))
+    ux = sim.macroscopic()[1][0, 0, :, 0].cpu().numpy().astype(np.float64)
+    y = np.arange(H)
+    exact = gx * (y + 0.5) * (H - 0.5 - y) / (2 * nu)
+    assert np.max(np.abs(ux - exact)) < 0.005 * exact.max()
+    sim.close()
