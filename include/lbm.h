@@ -172,6 +172,28 @@ lbm_status lbm_get_link_mask(lbm_ctx *ctx, uint32_t *mask);
 /* Enqueue later work on another stream (a cudaStream_t). */
 lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);
 
+/* Sum mass, momentum and thermal energy of populations held in caller memory, without
+ * allocating anything.  No page describes this call: it is a service for callers that
+ * cannot call cudaMalloc (code running inside another framework's memory pool, or in a
+ * loop where an allocation is not allowed) and so cannot provide a workspace.
+ *   f: Q planes (q-major) of nx*ny*nz fp32 populations, unshifted, in the lattice order
+ *      above (as lbm_get_populations writes them); g: Q_T planes or NULL without thermal.
+ *   out: 6 doubles written in stream order on cuda_stream (a cudaStream_t; NULL = legacy
+ *      default stream): sum f, sum c_x f, sum c_y f, sum c_z f, sum g, and the number of
+ *      cells whose sum f or sum g is not finite.  Nothing waits for the stream.
+ *   f, g, out: device memory of the current device or page-locked host memory.
+ * Limit: nx*ny*nz <= 2^28 (268435456) cells; larger grids are rejected with LBM_ERR_ARG.
+ * The reduction's scratch is one file-scope static device array of 2 MiB, which every
+ * device that loads the library keeps until the process exits.  The first call on a
+ * device looks up that array's device address (once per device, with the device
+ * current), so make a first call before capturing the stream into a CUDA graph.  Every
+ * call reuses the same array: calls that overlap on the GPU (other streams, or threads
+ * without ordering between them) race on it and must be serialised by the caller.
+ * Errors are reported through lbm_last_error(NULL). */
+lbm_status lbm_reduce_populations_static(int lattice, int thermal, int nx, int ny, int nz,
+                                         const float *f, const float *g, double *out,
+                                         void *cuda_stream);
+
 int lbm_parity(const lbm_ctx *ctx);                 /* steps taken mod 2, -1 if ctx NULL */
 long long lbm_steps_taken(const lbm_ctx *ctx);      /* -1 if ctx NULL                    */
 const char *lbm_last_error(const lbm_ctx *ctx);     /* ctx NULL: last create-time error */

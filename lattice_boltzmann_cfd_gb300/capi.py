@@ -69,6 +69,9 @@ SIGNATURES = [
     ("lbm_set_populations", ctypes.c_int, [_VP, _VP, _VP]),
     ("lbm_get_link_mask", ctypes.c_int, [_VP, _VP]),
     ("lbm_set_stream", ctypes.c_int, [_VP, _VP]),
+    ("lbm_reduce_populations_static", ctypes.c_int,
+     [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP,
+      _VP]),
     ("lbm_parity", ctypes.c_int, [_VP]),
     ("lbm_steps_taken", ctypes.c_longlong, [_VP]),
     ("lbm_last_error", ctypes.c_char_p, [_VP]),
@@ -118,7 +121,7 @@ def _addr(x):
     if isinstance(x, torch.Tensor):
         if not x.is_contiguous():
             raise ValueError("tensor must be contiguous")
-        if x.dtype not in (torch.float32, torch.int32, torch.uint8):
+        if x.dtype not in (torch.float32, torch.float64, torch.int32, torch.uint8):
             raise ValueError(f"unsupported dtype {x.dtype}")
         return x.data_ptr()
     raise TypeError(f"expected a tensor, an int address or None, got {type(x)}")
@@ -191,6 +194,14 @@ def lbm_get_link_mask(ctx, mask):
 
 def lbm_set_stream(ctx, stream):
     _check(load().lbm_set_stream(ctx, _stream_handle(stream)), ctx)
+
+
+def lbm_reduce_populations_static(lattice, thermal, nx, ny, nz, f, g, out, stream=None):
+    """Allocation-free sums (mass, momentum, thermal energy, non-finite cells) of
+    caller-held populations into ``out`` (6 doubles, device or page-locked host)."""
+    _check(load().lbm_reduce_populations_static(int(lattice), int(thermal), int(nx), int(ny),
+                                                int(nz), _addr(f), _addr(g), _addr(out),
+                                                _stream_handle(stream)))
 
 
 def lbm_parity(ctx) -> int:

@@ -101,6 +101,8 @@ bool is_odd(const lbm_ctx *c) { return c->parity != 0; }
 
 }  // namespace
 
+void lbm_internal_set_error(const char *msg) { g_error = msg ? msg : ""; }
+
 extern "C" {
 
 lbm_status lbm_workspace_bytes(const lbm_config *cfg, size_t *bytes)

@@ -43,3 +43,6 @@ cudaError_t launch_diag(int lattice, int thermal, bool masked, bool odd, const P
                         double *partial, double *out, cudaStream_t s);
 
 }  // namespace lbm
+
+// Record the error text returned by lbm_last_error(NULL) on this thread.
+void lbm_internal_set_error(const char *msg);
