@@ -60,7 +60,9 @@ def make_workload(name: str):
     from lattice_boltzmann_cfd_gb300 import workloads as W
     table = {
         "d3q19_mrt_periodic_512": lambda: W.random_periodic(n=512, seed=2),
+        "d3q19_mrt_periodic_256": lambda: W.random_periodic(n=256, seed=2),
         "d3q19_mrt_periodic_128": lambda: W.random_periodic(n=128, seed=2),
+        "cavity3d_256": lambda: W.cavity3d(n=256),
         "taylor_green_32": lambda: W.taylor_green(),
         "channel_sphere_128": lambda: W.channel_sphere(),
         "cavity2d_4096": lambda: W.cavity2d(),
