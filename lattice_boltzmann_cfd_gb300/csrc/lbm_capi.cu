@@ -203,13 +203,16 @@ lbm_status lbm_step(lbm_ctx *c, int n)
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
     DeviceGuard guard(c->device);
     const lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
+    // 32-bit population indices when the largest index (Q * S - 1) fits
+    const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
     for (int i = 0; i < n; ++i) {
         const bool odd = is_odd(c);
-        cudaError_t e = (c->cfg.lattice == LBM_D3Q19)
-                            ? lbm::launch_step_d3q19(c->cfg.thermal, c->cfg.collision,
-                                                     c->L.masked, odd, c->P, sh, c->stream)
-                            : lbm::launch_step_d2q9(c->cfg.thermal, c->cfg.collision,
-                                                    c->L.masked, odd, c->P, sh, c->stream);
+        cudaError_t e =
+            (c->cfg.lattice == LBM_D3Q19)
+                ? lbm::launch_step_d3q19(c->cfg.thermal, c->cfg.collision, c->L.masked, odd,
+                                         narrow, c->P, sh, c->stream)
+                : lbm::launch_step_d2q9(c->cfg.thermal, c->cfg.collision, c->L.masked, odd,
+                                        narrow, c->P, sh, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "step kernel");
         c->parity ^= 1;
         ++c->steps;

@@ -27,10 +27,11 @@ inline Shape cell_shape(int nx, int ny, int nz, int threads = 256)
 constexpr int DIAG_BLOCKS = 1024;
 
 // Each returns the launch error (cudaGetLastError) of what it enqueued.
-cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, const Params &P,
-                              const Shape &sh, cudaStream_t s);
-cudaError_t launch_step_d2q9(int thermal, int coll, bool masked, bool odd, const Params &P,
-                             const Shape &sh, cudaStream_t s);
+// narrow: every population index fits in 32 bits (see slot()).
+cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, bool narrow,
+                              const Params &P, const Shape &sh, cudaStream_t s);
+cudaError_t launch_step_d2q9(int thermal, int coll, bool masked, bool odd, bool narrow,
+                             const Params &P, const Shape &sh, cudaStream_t s);
 cudaError_t launch_init(int lattice, int thermal, const Params &P, const float *rho,
                         const float *u, const float *T, cudaStream_t s);
 cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t *solid,

@@ -70,37 +70,45 @@ LBM_HD bool bit(uint32_t m, int b) { return (m >> b) & 1u; }
 
 // ---------------------------------------------------------------- cell access ---------
 
+// Element index of slot (q, cell): 32-bit (NARROW) when every index of the population
+// arrays fits in 32 bits, which keeps the address arithmetic of the 19 + 7 accesses in
+// single registers; 64-bit otherwise.
+template <bool NARROW>
+LBM_HD auto slot(const Params &P, int q, int cell)
+{
+    if constexpr (NARROW) return (unsigned)q * (unsigned)P.S + (unsigned)cell;
+    else return (size_t)q * P.S + (size_t)(unsigned)cell;
+}
+
 // Load the logical populations of a fluid cell.  ODD = the odd step's read pattern.
-template <class L, class TL, bool MASKED, bool ODD>
-LBM_HD void load_cell(const Params &P, int idx, const Offs &o, uint32_t m,
-                                          float (&f)[L::Q], float (&g)[TL::QA])
+template <class L, class TL, bool MASKED, bool ODD, bool NARROW = false>
+LBM_HD void load_cell(const Params &P, int idx, const Offs &o, uint32_t m, float (&f)[L::Q],
+                      float (&g)[TL::QA])
 {
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
-        const float *p;
         if (!ODD || q == 0) {
-            p = P.f + (q * P.S + idx);
+            f[q] = P.f[slot<NARROW>(P, q, idx)];
         } else {
             const int oq = L::opp(q);
             const bool wall_in = MASKED && bit(m, oq);
-            p = wall_in ? P.f + (q * P.S + idx)
-                        : P.f + (oq * P.S + (idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q))));
+            f[q] = P.f[wall_in ? slot<NARROW>(P, q, idx)
+                               : slot<NARROW>(P, oq, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))];
         }
-        f[q] = *p;
     }
     if constexpr (TL::Q > 0) {
 #pragma unroll
         for (int k = 0; k < TL::Q; ++k) {
             if (!ODD || k == 0) {
-                g[k] = P.g[k * P.S + idx];
+                g[k] = P.g[slot<NARROW>(P, k, idx)];
             } else {
                 const int ok = L::opp(k);
                 const bool wall_in = MASKED && bit(m, ok);
                 if (wall_in) {
-                    const float raw = P.g[k * P.S + idx];
+                    const float raw = P.g[slot<NARROW>(P, k, idx)];
                     g[k] = bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - raw : raw;
                 } else {
-                    g[k] = P.g[ok * P.S + (idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))];
+                    g[k] = P.g[slot<NARROW>(P, ok, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))];
                 }
             }
         }
@@ -109,40 +117,38 @@ LBM_HD void load_cell(const Params &P, int idx, const Offs &o, uint32_t m,
 
 // Store post-collision populations.  Even: swapped into (opp q, x).  Odd: to (q, x + c_q)
 // or, for a wall link, to (opp q, x) with bounce-back / anti-bounce-back applied.
-template <class L, class TL, bool MASKED, bool ODD>
+template <class L, class TL, bool MASKED, bool ODD, bool NARROW = false>
 LBM_HD void store_cell(const Params &P, int idx, const Offs &o, uint32_t m,
-                                           const float (&f)[L::Q], const float (&g)[TL::QA])
+                       const float (&f)[L::Q], const float (&g)[TL::QA])
 {
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
         const int oq = L::opp(q);
-        float *p;
         if (!ODD) {
-            p = P.f + (oq * P.S + idx);
+            P.f[slot<NARROW>(P, oq, idx)] = f[q];
         } else if (q == 0) {
-            p = P.f + idx;
+            P.f[slot<NARROW>(P, 0, idx)] = f[0];
         } else {
             const bool wall_out = MASKED && bit(m, q);
-            p = wall_out ? P.f + (oq * P.S + idx)
-                         : P.f + (q * P.S + (idx + nb(o, L::cx(q), L::cy(q), L::cz(q))));
+            P.f[wall_out ? slot<NARROW>(P, oq, idx)
+                         : slot<NARROW>(P, q, idx + nb(o, L::cx(q), L::cy(q), L::cz(q)))] = f[q];
         }
-        *p = f[q];
     }
     if constexpr (TL::Q > 0) {
 #pragma unroll
         for (int k = 0; k < TL::Q; ++k) {
             const int ok = L::opp(k);
             if (!ODD) {
-                P.g[ok * P.S + idx] = g[k];
+                P.g[slot<NARROW>(P, ok, idx)] = g[k];
             } else if (k == 0) {
-                P.g[idx] = g[0];
+                P.g[slot<NARROW>(P, 0, idx)] = g[0];
             } else {
                 const bool wall_out = MASKED && bit(m, k);
                 if (wall_out) {
-                    P.g[ok * P.S + idx] =
+                    P.g[slot<NARROW>(P, ok, idx)] =
                         bit(m, DIRICHLET_SHIFT + k) ? P.abbT[k] - g[k] : g[k];
                 } else {
-                    P.g[k * P.S + (idx + nb(o, L::cx(k), L::cy(k), L::cz(k)))] = g[k];
+                    P.g[slot<NARROW>(P, k, idx + nb(o, L::cx(k), L::cy(k), L::cz(k)))] = g[k];
                 }
             }
         }
@@ -152,35 +158,32 @@ LBM_HD void store_cell(const Params &P, int idx, const Offs &o, uint32_t m,
 // Store logical populations so that load_cell<..., ODD> reads them back (used by
 // set_populations; the inverse of load_cell).
 template <class L, class TL, bool MASKED, bool ODD>
-LBM_HD void store_logical(const Params &P, int idx, const Offs &o,
-                                              uint32_t m, const float (&f)[L::Q],
-                                              const float (&g)[TL::QA])
+LBM_HD void store_logical(const Params &P, int idx, const Offs &o, uint32_t m,
+                          const float (&f)[L::Q], const float (&g)[TL::QA])
 {
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
-        float *p;
         if (!ODD || q == 0) {
-            p = P.f + (q * P.S + idx);
+            P.f[slot<false>(P, q, idx)] = f[q];
         } else {
             const int oq = L::opp(q);
             const bool wall_in = MASKED && bit(m, oq);
-            p = wall_in ? P.f + (q * P.S + idx)
-                        : P.f + (oq * P.S + (idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q))));
+            P.f[wall_in ? slot<false>(P, q, idx)
+                        : slot<false>(P, oq, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))] = f[q];
         }
-        *p = f[q];
     }
     if constexpr (TL::Q > 0) {
 #pragma unroll
         for (int k = 0; k < TL::Q; ++k) {
             if (!ODD || k == 0) {
-                P.g[k * P.S + idx] = g[k];
+                P.g[slot<false>(P, k, idx)] = g[k];
             } else {
                 const int ok = L::opp(k);
                 if (MASKED && bit(m, ok)) {
-                    P.g[k * P.S + idx] =
+                    P.g[slot<false>(P, k, idx)] =
                         bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - g[k] : g[k];
                 } else {
-                    P.g[ok * P.S + (idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))] = g[k];
+                    P.g[slot<false>(P, ok, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))] = g[k];
                 }
             }
         }
@@ -190,7 +193,7 @@ LBM_HD void store_logical(const Params &P, int idx, const Offs &o,
 // ------------------------------------------------------------------ the step ----------
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
-template <class L, class TL, int COLL, bool MASKED, bool ODD>
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
@@ -203,12 +206,21 @@ __global__ void __launch_bounds__(256) step_kernel(const Params P)
         m = P.mask[idx];
         if (m & SOLID_BIT) return;
     }
-    Offs o{};
-    if (ODD) o = make_offs(x, y, z, P);
     float f[L::Q], g[TL::QA];
-    load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+    {
+        Offs o{};
+        if (ODD) o = make_offs(x, y, z, P);
+        load_cell<L, TL, MASKED, ODD, NARROW>(P, idx, o, m, f, g);
+    }
     collide<L, TL, COLL>(f, g, P.c);
-    store_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+    // Recompute the store addresses after the collision instead of keeping the load-time
+    // values live through it (the empty asm hides that they are the same).
+    int xs = x, ys = y, zs = z, is = idx;
+    uint32_t ms = m;
+    asm volatile("" : "+r"(xs), "+r"(ys), "+r"(zs), "+r"(is), "+r"(ms));
+    Offs o{};
+    if (ODD) o = make_offs(xs, ys, zs, P);
+    store_cell<L, TL, MASKED, ODD, NARROW>(P, is, o, ms, f, g);
 }
 
 // ------------------------------------------------------------ auxiliary kernels -------
@@ -423,15 +435,19 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
         if (ODD) o = make_offs(x, y, z, P);
         float f[L::Q], g[TL::QA];
         load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
-        double dr = 0.0, t = 0.0;
+        // per-cell sums in fp32 (GB300's fp64 rate is low), running totals in fp64
+        float dr = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f, t = 0.0f;
 #pragma unroll
         for (int q = 0; q < L::Q; ++q) {
             dr += f[q];
-            acc[1] += L::cx(q) * (double)f[q];
-            acc[2] += L::cy(q) * (double)f[q];
-            acc[3] += L::cz(q) * (double)f[q];
+            if (L::cx(q)) jx += L::cx(q) * f[q];
+            if (L::cy(q)) jy += L::cy(q) * f[q];
+            if (L::cz(q)) jz += L::cz(q) * f[q];
         }
         acc[0] += dr;
+        acc[1] += jx;
+        acc[2] += jy;
+        acc[3] += jz;
         if constexpr (TL::Q > 0) {
 #pragma unroll
             for (int k = 0; k < TL::Q; ++k) t += g[k];

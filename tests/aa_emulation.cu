@@ -17,7 +17,7 @@ using namespace lbm;
 
 namespace {
 
-template <class L, class TL, int C, bool M, bool O>
+template <class L, class TL, int C, bool M, bool O, bool NARROW>
 void step_all(const Params &Pr, const Params &Pw)
 {
     for (int z = 0; z < Pr.nz; ++z)
@@ -32,9 +32,9 @@ void step_all(const Params &Pr, const Params &Pw)
                 Offs o{};
                 if (O) o = make_offs(x, y, z, Pr);
                 float f[L::Q], g[TL::QA];
-                load_cell<L, TL, M, O>(Pr, idx, o, m, f, g);
+                load_cell<L, TL, M, O, NARROW>(Pr, idx, o, m, f, g);
                 collide<L, TL, C>(f, g, Pr.c);
-                store_cell<L, TL, M, O>(Pw, idx, o, m, f, g);
+                store_cell<L, TL, M, O, NARROW>(Pw, idx, o, m, f, g);
             }
 }
 
@@ -61,7 +61,7 @@ void read_all(const Params &P, float *fout, float *gout)
             }
 }
 
-template <class L, class TL, int C>
+template <class L, class TL, int C, bool NARROW>
 int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, const float *u,
         const float *T, int steps, float *fout, float *gout, uint32_t *mask_out)
 {
@@ -91,11 +91,11 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
         Pw.f = fn.data();
         Pw.g = Lay.QT ? gn.data() : nullptr;
         if (Lay.masked) {
-            if (parity) step_all<L, TL, C, true, true>(P, Pw);
-            else step_all<L, TL, C, true, false>(P, Pw);
+            if (parity) step_all<L, TL, C, true, true, NARROW>(P, Pw);
+            else step_all<L, TL, C, true, false, NARROW>(P, Pw);
         } else {
-            if (parity) step_all<L, TL, C, false, true>(P, Pw);
-            else step_all<L, TL, C, false, false>(P, Pw);
+            if (parity) step_all<L, TL, C, false, true, NARROW>(P, Pw);
+            else step_all<L, TL, C, false, false, NARROW>(P, Pw);
         }
         f.swap(fn);
         g.swap(gn);
@@ -116,25 +116,36 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
 
 }  // namespace
 
+template <bool NARROW>
+int run_any(const lbm_config *cfg, const lbm_setup::Layout &Lay, const float *rho,
+            const float *u, const float *T, int steps, float *fout, float *gout,
+            uint32_t *mask_out)
+{
+    const bool mrt = cfg->collision == LBM_MRT;
+    if (cfg->lattice == 19) {
+        if (cfg->thermal == 7)
+            return mrt ? run<D3Q19, D3Q7, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                       : run<D3Q19, D3Q7, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+        return mrt ? run<D3Q19, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                   : run<D3Q19, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+    }
+    if (cfg->thermal == 5)
+        return mrt ? run<D2Q9, D2Q5, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                   : run<D2Q9, D2Q5, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+    return mrt ? run<D2Q9, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+               : run<D2Q9, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+}
+
+// narrow != 0: the step uses 32-bit population indices, as the library does whenever
+// every index fits in 32 bits; 0: the 64-bit form used for larger grids.
 extern "C" int emu_run(const lbm_config *cfg, const float *rho, const float *u, const float *T,
-                       int steps, float *fout, float *gout, uint32_t *mask_out)
+                       int steps, float *fout, float *gout, uint32_t *mask_out, int narrow)
 {
     lbm_setup::Layout Lay;
     std::string why;
     if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
-    const bool mrt = cfg->collision == LBM_MRT;
-    if (cfg->lattice == 19) {
-        if (cfg->thermal == 7)
-            return mrt ? run<D3Q19, D3Q7, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                       : run<D3Q19, D3Q7, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
-        return mrt ? run<D3Q19, NoThermal, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                   : run<D3Q19, NoThermal, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
-    }
-    if (cfg->thermal == 5)
-        return mrt ? run<D2Q9, D2Q5, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                   : run<D2Q9, D2Q5, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
-    return mrt ? run<D2Q9, NoThermal, 1>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-               : run<D2Q9, NoThermal, 0>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+    return narrow ? run_any<true>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
+                  : run_any<false>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
 }
 
 // Every neighbour index the odd-step access pattern forms (idx + offset of +-c_q for each

@@ -72,7 +72,7 @@ def mask_brute_force(w) -> np.ndarray:
     return m.astype(np.uint32)
 
 
-def emulate(emu_lib, w, steps):
+def emulate(emu_lib, w, steps, narrow=True):
     """(f, g, mask) after ``steps`` steps of the host emulation of the CUDA kernels."""
     cfg, keep = make_config(w)
     N = w.cells
@@ -84,7 +84,7 @@ def emulate(emu_lib, w, steps):
     T = np.ascontiguousarray(w.T_init, np.float32) if w.thermal else None
     vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     rc = emu_lib.emu_run(ctypes.byref(cfg), vp(rho), vp(u), vp(T), int(steps), vp(fo), vp(go),
-                         vp(mo))
+                         vp(mo), int(bool(narrow)))
     assert rc == 0
     return (fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid),
             mo.reshape(w.grid))

@@ -14,12 +14,13 @@ from parity_util import emulate, fluid_of, mask_brute_force, oracle_states, smal
 CASES = small_cases()
 
 
+@pytest.mark.parametrize("narrow", [True, False], ids=["idx32", "idx64"])
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_emulated_aa_step_matches_oracle(oracle_mod, emu_lib, w):
+def test_emulated_aa_step_matches_oracle(oracle_mod, emu_lib, w, narrow):
     ref = oracle_states(oracle_mod, w, [1, 2, 5, 6])
     fluid = fluid_of(w)
     for n, r in ref.items():
-        f, g, _ = emulate(emu_lib, w, n)
+        f, g, _ = emulate(emu_lib, w, n, narrow)
         assert not np.isnan(f[:, fluid]).any()
         assert np.abs(f - r["f"])[:, fluid].max() < 1e-6, n
         if w.thermal:

@@ -109,17 +109,22 @@ def _windows(shape, size, steps, rng, extra=6):
 
 @pytest.mark.parametrize("name,perturb", [("cavity3d", False), ("cavity3d", True),
                                           ("cavity2d", False), ("cavity2d", True),
-                                          ("random_periodic_512", True)])
+                                          ("random_periodic_512", True),
+                                          ("random_periodic_wide", True)])
 def test_full_size_sampled_windows(oracle_mod, name, perturb):
     """At the full 512^3 / 4096^2 sizes, in the launch configuration the benchmark uses:
     after 1, 2 and 3 steps every cell of sampled windows (corners, edges, faces, centre,
     random) matches the oracle run on that window (cells the window's cut faces can
-    reach are unknown to the oracle and skipped)."""
+    reach are unknown to the oracle and skipped).  The 640x640x568 case has more than 2^32
+    population slots, so its steps take the 64-bit index form."""
     if name == "random_periodic_512":
         w = W.random_periodic(n=512, seed=2)
+    elif name == "random_periodic_wide":
+        w = W.random_periodic(shape=(640, 640, 568), seed=3)
+        assert 19 * ((w.cells + 63) // 64 * 64) > 2 ** 32
     else:
         w = W.by_name(name)
-    if perturb and name != "random_periodic_512":
+    if perturb and not name.startswith("random_periodic"):
         w = W.perturbed(w, seed=31)
     nz, ny, nx = w.grid
     rng = np.random.default_rng(5)
