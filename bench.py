@@ -44,7 +44,10 @@ BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112}
 # DRAM bytes per cell update of the step kernel measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch / cells), with a hash of the kernel sources they were
 # taken on; reported as "traffic" only while the sources are unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # ncu --set full, one even + one odd launch at 256^3 (see profiles/), scaled by cells
+    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.56, "src_hash": "06ae7c62f5807132"},
+}
 
 
 def kernel_source_hash() -> str:
@@ -221,9 +224,9 @@ def oracle_sample(name: str):
     physics on a smaller grid (periodic sub-box / reduced cavity)."""
     from lattice_boltzmann_cfd_gb300 import workloads as W
     if name.startswith("d3q19_mrt_periodic"):
-        return W.random_periodic(shape=(256, 256, 64), seed=2), "periodic 256x256x64 sub-box"
-    if name == "cavity3d_512":
-        return W.cavity3d(shape=(256, 256, 64)), "cavity 256x256x64"
+        return W.random_periodic(shape=(512, 512, 64), seed=2), "periodic 512x512x64 slab"
+    if name.startswith("cavity3d"):
+        return W.cavity3d(shape=(512, 512, 48)), "cavity 512x512x48 slab"
     if name == "cavity2d_4096":
         return W.cavity2d(shape=(2048, 2048, 1)), "cavity 2048^2"
     if name == "channel_sphere_128":
@@ -245,11 +248,11 @@ def time_oracle(name: str, steps: int):
     return mlups, dt, w.cells, label, oracle.max_threads()
 
 
-def cpu_baseline(name: str) -> dict:
-    mlups, dt, cells, label, cores = time_oracle(name, 4)
+def cpu_baseline(name: str, steps: int = 16) -> dict:
+    mlups, dt, cells, label, cores = time_oracle(name, steps)
     return {"value": round(mlups, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{label} of the same workload, 4 fp64 two-buffer steps "
-                      f"({cells * 4 / 1e6:.0f} M cell updates, {dt:.1f} s)"}
+            "sample": f"{label} of the same workload, {steps} fp64 two-buffer steps "
+                      f"({cells * steps / 1e6:.0f} M cell updates, {dt:.1f} s)"}
 
 
 # ----------------------------------------------------------------- helpers --------
