@@ -536,3 +536,48 @@ def test_window_run_matches_full_run(oracle_mod):
     assert np.array_equal(fw[sl_w], f[sl_f])
     assert np.array_equal(gw[sl_w], g[sl_f])
     assert np.isnan(fw).any()
+
+
+@pytest.mark.parametrize("lattice,walls", [(19, "y"), (19, "z"), (9, "y")])
+def test_poiseuille_exact_in_two_rate_limit(oracle_mod, lattice, walls):
+    """With every odd non-conserved moment (q, m) relaxed at s_odd and every even one at
+    s_nu, half-way bounce-back Poiseuille flow is exact when
+    Lambda = (1/s_nu - 1/2)(1/s_odd - 1/2) = 3/16 (Ginzburg and d'Humieres' two-relaxation-
+    time result; not on the pages).  Exactness to 1e-9 pins which rows each rate acts on,
+    the half-way wall position and the forcing."""
+    H, nu, gx = 16, 0.1, 1e-6
+    s_nu = 1.0 / (3 * nu + 0.5)
+    s_odd = 1.0 / ((3.0 / 16.0) / (1.0 / s_nu - 0.5) + 0.5)
+    rates = ({"e": s_nu, "eps": s_nu, "q": s_odd, "pi": s_nu, "m": s_odd} if lattice == 19
+             else {"e": s_nu, "eps": s_nu, "q": s_odd})
+    if walls == "y":
+        shape, faces = (1, H, 1), ("periodic", "periodic", "wall", "wall", "periodic", "periodic")
+    else:
+        shape, faces = (1, 1, H), ("periodic", "periodic", "periodic", "periodic", "wall", "wall")
+    w = _spec(lattice=lattice, shape=shape, nu=nu, g_body=(gx, 0, 0), rates=rates,
+              face_flow=faces)
+    p, f, g = _start(oracle_mod, w)
+    oracle_mod.run(p, f, g, int(20 * H * H / nu))
+    ux = oracle_mod.macroscopic(p, f, g)[1][0].ravel()
+    y = np.arange(H)
+    exact = gx * (y + 0.5) * (H - 0.5 - y) / (2 * nu)
+    assert np.max(np.abs(ux - exact)) < 1e-9 * exact.max()
+
+
+def test_buoyancy_momentum_increment(oracle_mod):
+    """Periodic domain with a random temperature field: per step the momentum along the
+    vertical axis grows by exactly sum rho g beta (T - T0) (Boussinesq force of the thermal
+    multi-GPU page, taken at the pre-collision state), the other components not at all."""
+    base = W.perturbed(W.cavity3d(shape=(6, 5, 4)), seed=1)
+    for up in (0, 1, 2):
+        w = dataclasses.replace(base, face_flow=("periodic",) * 6, gbeta=0.05, T0=0.1,
+                                up_axis=up)
+        p, f, g = _start(oracle_mod, w)
+        for _ in range(2):
+            d0 = oracle_mod.diagnostics(p, f, g)
+            rho, _, T = oracle_mod.macroscopic(p, f, g)
+            oracle_mod.run(p, f, g, 1)
+            d1 = oracle_mod.diagnostics(p, f, g)
+            want = np.zeros(3)
+            want[up] = (rho * w.gbeta * (T - w.T0)).sum()
+            assert np.allclose(d1["momentum"] - d0["momentum"], want, rtol=1e-10, atol=1e-14)
