@@ -85,6 +85,11 @@ enum { LBM_THERMAL_NONE = 0, LBM_D2Q5 = 5, LBM_D3Q7 = 7 };
 enum { LBM_BGK = 0, LBM_MRT = 1 };
 enum { LBM_FACE_PERIODIC = 0, LBM_FACE_WALL = 1 };        /* flow: half-way bounce-back */
 enum { LBM_TFACE_ADIABATIC = 0, LBM_TFACE_DIRICHLET = 1 }; /* thermal, on WALL faces   */
+/* Population layout ([AA] Options::streaming): AA = one buffer streamed in place (152 B
+ * per D3Q19 update); PULL = two buffers, one fused pull-collide kernel per step (152 B,
+ * twice the memory); SPLIT = two buffers, collide in place then pull into the other
+ * buffer, two kernels per step (304 B). */
+enum { LBM_STREAM_AA = 0, LBM_STREAM_PULL = 1, LBM_STREAM_SPLIT = 2 };
 
 /* Problem description ([TLBM] Sec. 2; [KFS] Sec. 3.1).  Face order: -x, +x, -y, +y, -z, +z.
  * Both faces of an axis must have the same flow kind.  A link is a wall link when its
@@ -108,6 +113,7 @@ typedef struct {
     double T_wall[6];     /* wall temperature of DIRICHLET faces                       */
     const uint8_t *solid_mask; /* HOST pointer, nx*ny*nz bytes, x fastest, nonzero =
                                   solid; NULL = no solid cells.  Copied by lbm_create. */
+    int streaming;        /* LBM_STREAM_AA (default 0), LBM_STREAM_PULL or LBM_STREAM_SPLIT */
 } lbm_config;
 
 /* Diagnostics of the current state (see lbm_diagnostics). */

@@ -23,6 +23,8 @@ LBM_THERMAL_NONE, LBM_D2Q5, LBM_D3Q7 = 0, 5, 7
 LBM_BGK, LBM_MRT = 0, 1
 LBM_FACE_PERIODIC, LBM_FACE_WALL = 0, 1
 LBM_TFACE_ADIABATIC, LBM_TFACE_DIRICHLET = 0, 1
+LBM_STREAM_AA, LBM_STREAM_PULL, LBM_STREAM_SPLIT = 0, 1, 2
+STREAMING = {"aa": LBM_STREAM_AA, "pull": LBM_STREAM_PULL, "split": LBM_STREAM_SPLIT}
 
 
 class LbmError(RuntimeError):
@@ -40,6 +42,7 @@ class lbm_config(ctypes.Structure):
         ("gbeta", ctypes.c_double), ("T0", ctypes.c_double), ("up_axis", ctypes.c_int),
         ("face_flow", ctypes.c_int * 6), ("face_T", ctypes.c_int * 6),
         ("T_wall", ctypes.c_double * 6), ("solid_mask", ctypes.POINTER(ctypes.c_uint8)),
+        ("streaming", ctypes.c_int),
     ]
 
 

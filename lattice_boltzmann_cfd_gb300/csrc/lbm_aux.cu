@@ -1,5 +1,7 @@
 // Launchers of the auxiliary kernels (initialisation, mask, read-out, diagnostics) for
 // both lattices.
+#include <type_traits>
+
 #include "lbm_internal.h"
 
 namespace lbm {
@@ -20,20 +22,25 @@ Shape shape_of(const Params &P) { return cell_shape(P.nx, P.ny, P.nz); }
 
 }  // namespace
 
-cudaError_t launch_init(int lattice, int thermal, const Params &P, const float *rho,
-                        const float *u, const float *T, cudaStream_t s)
+namespace {
+template <class L, class TL>
+cudaError_t init_go(int pat, const Params &P, const float *rho, const float *u, const float *T,
+                    cudaStream_t s)
 {
     const Shape sh = shape_of(P);
+    if (pat == PULL) init_kernel<L, TL, PULL><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+    else init_kernel<L, TL, NATURAL><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_init(int lattice, int thermal, int pat, const Params &P, const float *rho,
+                        const float *u, const float *T, cudaStream_t s)
+{
     return by_lattice(
         lattice, thermal,
-        [&](auto tl) {
-            init_kernel<D3Q19, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
-            return cudaGetLastError();
-        },
-        [&](auto tl) {
-            init_kernel<D2Q9, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
-            return cudaGetLastError();
-        });
+        [&](auto tl) { return init_go<D3Q19, decltype(tl)>(pat, P, rho, u, T, s); },
+        [&](auto tl) { return init_go<D2Q9, decltype(tl)>(pat, P, rho, u, T, s); });
 }
 
 cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t *solid,
@@ -53,47 +60,50 @@ cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t
 }
 
 namespace {
+// Call fn with compile-time (MASKED, PAT).
+template <class Fn>
+void with_pattern(bool masked, int pat, Fn &&fn)
+{
+    auto by_pat = [&](auto m) {
+        if (pat == AA_ODD) fn(m, std::integral_constant<int, AA_ODD>{});
+        else if (pat == PULL) fn(m, std::integral_constant<int, PULL>{});
+        else fn(m, std::integral_constant<int, NATURAL>{});
+    };
+    if (masked) by_pat(std::true_type{});
+    else by_pat(std::false_type{});
+}
+
 template <class L, class TL>
-cudaError_t macro_go(bool masked, bool odd, const Params &P, float *rho, float *u, float *T,
+cudaError_t macro_go(bool masked, int pat, const Params &P, float *rho, float *u, float *T,
                      cudaStream_t s)
 {
     const Shape sh = shape_of(P);
-    if (masked) {
-        if (odd) macro_kernel<L, TL, true, true><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
-        else macro_kernel<L, TL, true, false><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
-    } else {
-        if (odd) macro_kernel<L, TL, false, true><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
-        else macro_kernel<L, TL, false, false><<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
-    }
+    with_pattern(masked, pat, [&](auto m, auto p) {
+        macro_kernel<L, TL, decltype(m)::value, decltype(p)::value>
+            <<<sh.grid, sh.block, 0, s>>>(P, rho, u, T);
+    });
     return cudaGetLastError();
 }
 
 template <class L, class TL, bool SET>
-cudaError_t pop_go(bool masked, bool odd, const Params &P, float *f, float *g, cudaStream_t s)
+cudaError_t pop_go(bool masked, int pat, const Params &P, float *f, float *g, cudaStream_t s)
 {
     const Shape sh = shape_of(P);
-    if (masked) {
-        if (odd) pop_kernel<L, TL, true, true, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
-        else pop_kernel<L, TL, true, false, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
-    } else {
-        if (odd) pop_kernel<L, TL, false, true, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
-        else pop_kernel<L, TL, false, false, SET><<<sh.grid, sh.block, 0, s>>>(P, f, g);
-    }
+    with_pattern(masked, pat, [&](auto m, auto p) {
+        pop_kernel<L, TL, decltype(m)::value, decltype(p)::value, SET>
+            <<<sh.grid, sh.block, 0, s>>>(P, f, g);
+    });
     return cudaGetLastError();
 }
 
 template <class L, class TL>
-cudaError_t diag_go(bool masked, bool odd, const Params &P, double *partial, double *out,
+cudaError_t diag_go(bool masked, int pat, const Params &P, double *partial, double *out,
                     cudaStream_t s)
 {
     const dim3 g(DIAG_BLOCKS), b(DIAG_THREADS);
-    if (masked) {
-        if (odd) diag_kernel<L, TL, true, true><<<g, b, 0, s>>>(P, partial);
-        else diag_kernel<L, TL, true, false><<<g, b, 0, s>>>(P, partial);
-    } else {
-        if (odd) diag_kernel<L, TL, false, true><<<g, b, 0, s>>>(P, partial);
-        else diag_kernel<L, TL, false, false><<<g, b, 0, s>>>(P, partial);
-    }
+    with_pattern(masked, pat, [&](auto m, auto p) {
+        diag_kernel<L, TL, decltype(m)::value, decltype(p)::value><<<g, b, 0, s>>>(P, partial);
+    });
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     diag_finalize<<<1, DIAG_THREADS, 0, s>>>(partial, DIAG_BLOCKS, out);
@@ -101,37 +111,37 @@ cudaError_t diag_go(bool masked, bool odd, const Params &P, double *partial, dou
 }
 }  // namespace
 
-cudaError_t launch_macro(int lattice, int thermal, bool masked, bool odd, const Params &P,
+cudaError_t launch_macro(int lattice, int thermal, bool masked, int pat, const Params &P,
                          float *rho, float *u, float *T, cudaStream_t s)
 {
     return by_lattice(
         lattice, thermal,
-        [&](auto tl) { return macro_go<D3Q19, decltype(tl)>(masked, odd, P, rho, u, T, s); },
-        [&](auto tl) { return macro_go<D2Q9, decltype(tl)>(masked, odd, P, rho, u, T, s); });
+        [&](auto tl) { return macro_go<D3Q19, decltype(tl)>(masked, pat, P, rho, u, T, s); },
+        [&](auto tl) { return macro_go<D2Q9, decltype(tl)>(masked, pat, P, rho, u, T, s); });
 }
 
-cudaError_t launch_pop(int lattice, int thermal, bool masked, bool odd, bool set,
+cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
                        const Params &P, float *f, float *g, cudaStream_t s)
 {
     return by_lattice(
         lattice, thermal,
         [&](auto tl) {
-            return set ? pop_go<D3Q19, decltype(tl), true>(masked, odd, P, f, g, s)
-                       : pop_go<D3Q19, decltype(tl), false>(masked, odd, P, f, g, s);
+            return set ? pop_go<D3Q19, decltype(tl), true>(masked, pat, P, f, g, s)
+                       : pop_go<D3Q19, decltype(tl), false>(masked, pat, P, f, g, s);
         },
         [&](auto tl) {
-            return set ? pop_go<D2Q9, decltype(tl), true>(masked, odd, P, f, g, s)
-                       : pop_go<D2Q9, decltype(tl), false>(masked, odd, P, f, g, s);
+            return set ? pop_go<D2Q9, decltype(tl), true>(masked, pat, P, f, g, s)
+                       : pop_go<D2Q9, decltype(tl), false>(masked, pat, P, f, g, s);
         });
 }
 
-cudaError_t launch_diag(int lattice, int thermal, bool masked, bool odd, const Params &P,
+cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s)
 {
     return by_lattice(
         lattice, thermal,
-        [&](auto tl) { return diag_go<D3Q19, decltype(tl)>(masked, odd, P, partial, out, s); },
-        [&](auto tl) { return diag_go<D2Q9, decltype(tl)>(masked, odd, P, partial, out, s); });
+        [&](auto tl) { return diag_go<D3Q19, decltype(tl)>(masked, pat, P, partial, out, s); },
+        [&](auto tl) { return diag_go<D2Q9, decltype(tl)>(masked, pat, P, partial, out, s); });
 }
 
 }  // namespace lbm

@@ -5,6 +5,7 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <utility>
 
 #include "../../include/lbm.h"
 #include "lbm_internal.h"
@@ -97,7 +98,13 @@ lbm_status device_address(lbm_ctx *c, const void *p, const char *what, void **ou
     }
 }
 
-bool is_odd(const lbm_ctx *c) { return c->parity != 0; }
+// Read pattern of the stored logical state.
+int pattern(const lbm_ctx *c)
+{
+    if (c->L.streaming == LBM_STREAM_PULL) return lbm::PULL;
+    if (c->L.streaming == LBM_STREAM_SPLIT) return lbm::NATURAL;
+    return c->parity ? lbm::AA_ODD : lbm::NATURAL;
+}
 
 }  // namespace
 
@@ -187,8 +194,13 @@ lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, co
     if (s == LBM_OK) s = device_address(c, u, "u", &du);
     if (s == LBM_OK && c->L.QT) s = device_address(c, T, "T", &dT);
     if (s != LBM_OK) return s;
-    cudaError_t e = lbm::launch_init(c->cfg.lattice, c->cfg.thermal, c->P, (const float *)dr,
-                                     (const float *)du, (const float *)dT, c->stream);
+    // the AA state starts at parity 0 (natural slots); SPLIT stores the natural state;
+    // PULL stores a post-collision state read with the pull pattern
+    c->parity = 0;
+    const int pat = (c->L.streaming == LBM_STREAM_PULL) ? lbm::PULL : lbm::NATURAL;
+    cudaError_t e = lbm::launch_init(c->cfg.lattice, c->cfg.thermal, pat, c->P,
+                                     (const float *)dr, (const float *)du, (const float *)dT,
+                                     c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "init kernel");
     c->parity = 0;
     c->steps = 0;
@@ -205,15 +217,31 @@ lbm_status lbm_step(lbm_ctx *c, int n)
     const lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
     // 32-bit population indices when the largest index (Q * S - 1) fits
     const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
+    const bool d3 = c->cfg.lattice == LBM_D3Q19;
+    const int th = c->cfg.thermal, coll = c->cfg.collision;
+    const bool masked = c->L.masked;
     for (int i = 0; i < n; ++i) {
-        const bool odd = is_odd(c);
-        cudaError_t e =
-            (c->cfg.lattice == LBM_D3Q19)
-                ? lbm::launch_step_d3q19(c->cfg.thermal, c->cfg.collision, c->L.masked, odd,
-                                         narrow, c->P, sh, c->stream)
-                : lbm::launch_step_d2q9(c->cfg.thermal, c->cfg.collision, c->L.masked, odd,
-                                        narrow, c->P, sh, c->stream);
+        cudaError_t e;
+        switch (c->L.streaming) {
+        case LBM_STREAM_PULL:
+            e = d3 ? lbm::launch_pull_d3q19(th, coll, masked, narrow, c->P, sh, c->stream)
+                   : lbm::launch_pull_d2q9(th, coll, masked, narrow, c->P, sh, c->stream);
+            break;
+        case LBM_STREAM_SPLIT:
+            e = d3 ? lbm::launch_split_d3q19(th, coll, masked, narrow, c->P, sh, c->stream)
+                   : lbm::launch_split_d2q9(th, coll, masked, narrow, c->P, sh, c->stream);
+            break;
+        default: {
+            const bool odd = c->parity != 0;
+            e = d3 ? lbm::launch_step_d3q19(th, coll, masked, odd, narrow, c->P, sh, c->stream)
+                   : lbm::launch_step_d2q9(th, coll, masked, odd, narrow, c->P, sh, c->stream);
+        }
+        }
         if (e != cudaSuccess) return cuda_fail(c, e, "step kernel");
+        if (c->L.streaming != LBM_STREAM_AA) {
+            std::swap(c->P.f, c->P.fo);
+            std::swap(c->P.g, c->P.go);
+        }
         c->parity ^= 1;
         ++c->steps;
     }
@@ -231,7 +259,7 @@ lbm_status lbm_macroscopic(lbm_ctx *c, float *rho, float *u, float *T)
     if (s == LBM_OK && u) s = device_address(c, u, "u", &du);
     if (s == LBM_OK && T && c->L.QT) s = device_address(c, T, "T", &dT);
     if (s != LBM_OK) return s;
-    cudaError_t e = lbm::launch_macro(c->cfg.lattice, c->cfg.thermal, c->L.masked, is_odd(c),
+    cudaError_t e = lbm::launch_macro(c->cfg.lattice, c->cfg.thermal, c->L.masked, pattern(c),
                                       c->P, (float *)dr, (float *)du, (float *)dT, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "macroscopic kernel");
     return LBM_OK;
@@ -243,7 +271,7 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
     if (!out) return fail(c, LBM_ERR_ARG, "out is NULL");
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
     DeviceGuard guard(c->device);
-    cudaError_t e = lbm::launch_diag(c->cfg.lattice, c->cfg.thermal, c->L.masked, is_odd(c),
+    cudaError_t e = lbm::launch_diag(c->cfg.lattice, c->cfg.thermal, c->L.masked, pattern(c),
                                      c->P, c->partial, c->result, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "diagnostics kernel");
     double r[lbm::DIAG_N] = {0};
@@ -305,7 +333,7 @@ static lbm_status populations(lbm_ctx *c, float *f, float *g, bool set)
     lbm_status s = device_address(c, f, "f", &df);
     if (s == LBM_OK && g && c->L.QT) s = device_address(c, g, "g", &dg);
     if (s != LBM_OK) return s;
-    cudaError_t e = lbm::launch_pop(c->cfg.lattice, c->cfg.thermal, c->L.masked, is_odd(c), set,
+    cudaError_t e = lbm::launch_pop(c->cfg.lattice, c->cfg.thermal, c->L.masked, pattern(c), set,
                                     c->P, (float *)df, (float *)dg, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, set ? "set kernel" : "get kernel");
     if (set) {

@@ -32,15 +32,26 @@ cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, bool
                               const Params &P, const Shape &sh, cudaStream_t s);
 cudaError_t launch_step_d2q9(int thermal, int coll, bool masked, bool odd, bool narrow,
                              const Params &P, const Shape &sh, cudaStream_t s);
-cudaError_t launch_init(int lattice, int thermal, const Params &P, const float *rho,
+// Two-buffer modes: one PULL step, or one SPLIT step (collide + stream), from P.f/P.g
+// into P.fo/P.go.
+cudaError_t launch_pull_d3q19(int thermal, int coll, bool masked, bool narrow, const Params &P,
+                              const Shape &sh, cudaStream_t s);
+cudaError_t launch_pull_d2q9(int thermal, int coll, bool masked, bool narrow, const Params &P,
+                             const Shape &sh, cudaStream_t s);
+cudaError_t launch_split_d3q19(int thermal, int coll, bool masked, bool narrow, const Params &P,
+                               const Shape &sh, cudaStream_t s);
+cudaError_t launch_split_d2q9(int thermal, int coll, bool masked, bool narrow, const Params &P,
+                              const Shape &sh, cudaStream_t s);
+// pat: read pattern of the logical state (NATURAL, AA_ODD or PULL).
+cudaError_t launch_init(int lattice, int thermal, int pat, const Params &P, const float *rho,
                         const float *u, const float *T, cudaStream_t s);
 cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t *solid,
                         uint32_t *mask, cudaStream_t s);
-cudaError_t launch_macro(int lattice, int thermal, bool masked, bool odd, const Params &P,
+cudaError_t launch_macro(int lattice, int thermal, bool masked, int pat, const Params &P,
                          float *rho, float *u, float *T, cudaStream_t s);
-cudaError_t launch_pop(int lattice, int thermal, bool masked, bool odd, bool set,
+cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
                        const Params &P, float *f, float *g, cudaStream_t s);
-cudaError_t launch_diag(int lattice, int thermal, bool masked, bool odd, const Params &P,
+cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s);
 
 }  // namespace lbm

@@ -20,6 +20,13 @@
 // omega T_w term are applied where the odd step writes, or reads, the redirected slot.
 // Even steps need no wall handling.  After an odd number of steps the logical state is
 // read with the odd step's read pattern.
+//
+// Two-buffer modes (that page's A-B layout, for comparison): PULL fuses the step into one
+// kernel that pulls f_q(x - c_q) (bounce-back f_opp(x) on wall links) from the current
+// buffer, collides and writes (q, x) of the other buffer, so the stored state is the
+// post-collision one and is read with the pull pattern; SPLIT collides in place (natural
+// slots), then a second kernel pulls into the other buffer, so the stored state is the
+// natural pre-collision one (304 B per D3Q19 update instead of 152).
 #pragma once
 #include <cstddef>
 #include <cstdint>
@@ -29,8 +36,9 @@
 namespace lbm {
 
 struct Params {
-    float *f;              // Q planes of S floats (shifted populations)
+    float *f;              // Q planes of S floats (shifted populations), current buffer
     float *g;              // Q_T planes (thermal), may be null
+    float *fo, *go;        // the other buffer of the two-buffer modes (null for AA)
     const uint32_t *mask;  // link mask, null when there are no walls or solids
     size_t S;              // plane stride in elements
     int nx, ny, nz;
@@ -80,38 +88,91 @@ LBM_HD auto slot(const Params &P, int q, int cell)
     else return (size_t)q * P.S + (size_t)(unsigned)cell;
 }
 
-// Load the logical populations of a fluid cell.  ODD = the odd step's read pattern.
-template <class L, class TL, bool MASKED, bool ODD, bool NARROW = false>
+// Read patterns of the logical state (population q of cell x at the current time):
+//   NATURAL  (q, x): after an even number of AA steps; the SPLIT mode.
+//   AA_ODD   (opp q, x - c_q), or (q, x) on a wall link: after an odd number of AA steps.
+//   PULL     (q, x - c_q), or (opp q, x) on a wall link: the PULL mode (post-collision state).
+// On a wall link (the link x -> x - c_q, i.e. mask bit opp q) the stored value is the cell's
+// own post-collision f_opp(q); for a Dirichlet thermal link it is turned into the
+// anti-bounce-back value omega T_w - g.
+enum { NATURAL = 0, AA_ODD = 1, PULL = 2 };
+
+// Load the logical populations of a fluid cell with read pattern PAT.
+template <class L, class TL, bool MASKED, int PAT, bool NARROW = false>
 LBM_HD void load_cell(const Params &P, int idx, const Offs &o, uint32_t m, float (&f)[L::Q],
                       float (&g)[TL::QA])
 {
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
-        if (!ODD || q == 0) {
+        if (PAT == NATURAL || q == 0) {
             f[q] = P.f[slot<NARROW>(P, q, idx)];
         } else {
             const int oq = L::opp(q);
             const bool wall_in = MASKED && bit(m, oq);
-            f[q] = P.f[wall_in ? slot<NARROW>(P, q, idx)
-                               : slot<NARROW>(P, oq, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))];
+            const int own = PAT == AA_ODD ? q : oq, far = PAT == AA_ODD ? oq : q;
+            f[q] = P.f[wall_in ? slot<NARROW>(P, own, idx)
+                               : slot<NARROW>(P, far, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))];
         }
     }
     if constexpr (TL::Q > 0) {
 #pragma unroll
         for (int k = 0; k < TL::Q; ++k) {
-            if (!ODD || k == 0) {
+            if (PAT == NATURAL || k == 0) {
                 g[k] = P.g[slot<NARROW>(P, k, idx)];
             } else {
                 const int ok = L::opp(k);
                 const bool wall_in = MASKED && bit(m, ok);
+                const int own = PAT == AA_ODD ? k : ok, far = PAT == AA_ODD ? ok : k;
                 if (wall_in) {
-                    const float raw = P.g[slot<NARROW>(P, k, idx)];
+                    const float raw = P.g[slot<NARROW>(P, own, idx)];
                     g[k] = bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - raw : raw;
                 } else {
-                    g[k] = P.g[slot<NARROW>(P, ok, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))];
+                    g[k] = P.g[slot<NARROW>(P, far, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))];
                 }
             }
         }
+    }
+}
+
+// After load_cell<..., MASKED=false, PAT> loaded every population as if no link were a
+// wall (so that all loads issue without waiting for the mask), replace the ones whose
+// link is a wall by the cell's own slot.  Only cells next to a wall or a solid take this
+// branch; the speculative loads they discard read valid slots of other cells.
+template <class L, class TL, int PAT, bool NARROW>
+LBM_HD void fix_wall_loads(const Params &P, int idx, uint32_t m, float (&f)[L::Q],
+                           float (&g)[TL::QA])
+{
+    static_assert(PAT != NATURAL, "natural reads have no wall redirect");
+#pragma unroll
+    for (int q = 1; q < L::Q; ++q) {
+        const int oq = L::opp(q);
+        if (bit(m, oq)) f[q] = P.f[slot<NARROW>(P, PAT == AA_ODD ? q : oq, idx)];
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 1; k < TL::Q; ++k) {
+            const int ok = L::opp(k);
+            if (bit(m, ok)) {
+                const float raw = P.g[slot<NARROW>(P, PAT == AA_ODD ? k : ok, idx)];
+                g[k] = bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - raw : raw;
+            }
+        }
+    }
+}
+
+template <class L>
+LBM_HD constexpr uint32_t wall_bits() { return (1u << L::Q) - 2u; }
+
+// Store populations into the natural slots (q, x) of the given arrays.
+template <class L, class TL, bool NARROW>
+LBM_HD void store_natural(const Params &P, float *F, float *G, int idx, const float (&f)[L::Q],
+                          const float (&g)[TL::QA])
+{
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) F[slot<NARROW>(P, q, idx)] = f[q];
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) G[slot<NARROW>(P, k, idx)] = g[k];
     }
 }
 
@@ -155,35 +216,37 @@ LBM_HD void store_cell(const Params &P, int idx, const Offs &o, uint32_t m,
     }
 }
 
-// Store logical populations so that load_cell<..., ODD> reads them back (used by
-// set_populations; the inverse of load_cell).
-template <class L, class TL, bool MASKED, bool ODD>
+// Store logical populations so that load_cell<..., PAT> reads them back (initialisation
+// and set_populations; the inverse of load_cell).
+template <class L, class TL, bool MASKED, int PAT>
 LBM_HD void store_logical(const Params &P, int idx, const Offs &o, uint32_t m,
                           const float (&f)[L::Q], const float (&g)[TL::QA])
 {
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
-        if (!ODD || q == 0) {
+        if (PAT == NATURAL || q == 0) {
             P.f[slot<false>(P, q, idx)] = f[q];
         } else {
             const int oq = L::opp(q);
             const bool wall_in = MASKED && bit(m, oq);
-            P.f[wall_in ? slot<false>(P, q, idx)
-                        : slot<false>(P, oq, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))] = f[q];
+            const int own = PAT == AA_ODD ? q : oq, far = PAT == AA_ODD ? oq : q;
+            P.f[wall_in ? slot<false>(P, own, idx)
+                        : slot<false>(P, far, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))] = f[q];
         }
     }
     if constexpr (TL::Q > 0) {
 #pragma unroll
         for (int k = 0; k < TL::Q; ++k) {
-            if (!ODD || k == 0) {
+            if (PAT == NATURAL || k == 0) {
                 P.g[slot<false>(P, k, idx)] = g[k];
             } else {
                 const int ok = L::opp(k);
+                const int own = PAT == AA_ODD ? k : ok, far = PAT == AA_ODD ? ok : k;
                 if (MASKED && bit(m, ok)) {
-                    P.g[slot<false>(P, k, idx)] =
+                    P.g[slot<false>(P, own, idx)] =
                         bit(m, DIRICHLET_SHIFT + ok) ? P.abbT[ok] - g[k] : g[k];
                 } else {
-                    P.g[slot<false>(P, ok, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))] = g[k];
+                    P.g[slot<false>(P, far, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))] = g[k];
                 }
             }
         }
@@ -193,8 +256,99 @@ LBM_HD void store_logical(const Params &P, int idx, const Offs &o, uint32_t m,
 // ------------------------------------------------------------------ the step ----------
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
+// One AA step of cell (x, y, z): loads through Pr, stores through Pw (the same buffer in
+// the kernel; a separate one in the host emulation of the tests).
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW>
+LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
+{
+    const int idx = x + Pr.nx * (y + Pr.ny * z);
+    // The mask load and the population loads are issued together: the populations are
+    // loaded as if no link were a wall, and wall links are fixed once the mask is in.
+    const uint32_t m = MASKED ? Pr.mask[idx] : 0u;
+    float f[L::Q], g[TL::QA];
+    {
+        Offs o{};
+        if (ODD) o = make_offs(x, y, z, Pr);
+        load_cell<L, TL, false, ODD ? AA_ODD : NATURAL, NARROW>(Pr, idx, o, 0u, f, g);
+    }
+    if (MASKED) {
+        if (m & SOLID_BIT) return;
+        if (ODD && (m & wall_bits<L>())) fix_wall_loads<L, TL, AA_ODD, NARROW>(Pr, idx, m, f, g);
+    }
+    collide<L, TL, COLL>(f, g, Pr.c);
+    // Recompute the store addresses after the collision instead of keeping the load-time
+    // values live through it (the empty asm hides that they are the same).
+    int xs = x, ys = y, zs = z, is = idx;
+    uint32_t ms = m;
+    asm volatile("" : "+r"(xs), "+r"(ys), "+r"(zs), "+r"(is), "+r"(ms));
+    Offs o{};
+    if (ODD) o = make_offs(xs, ys, zs, Pw);
+    store_cell<L, TL, MASKED, ODD, NARROW>(Pw, is, o, ms, f, g);
+}
+
+// One time step: one thread per cell, blocks along x (x fastest for coalescing).
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW>(P, P, x, y, z);
+}
+
+// Two-buffer PULL step: pull from the current buffer, collide, write the other buffer's
+// natural slots.  No slot is read and written in the same launch.
+template <class L, class TL, int COLL, bool MASKED, bool NARROW>
+LBM_HD void pull_step_cell(const Params &P, float *Wf, float *Wg, int x, int y, int z)
+{
+    const int idx = x + P.nx * (y + P.ny * z);
+    const uint32_t m = MASKED ? P.mask[idx] : 0u;
+    float f[L::Q], g[TL::QA];
+    {
+        const Offs o = make_offs(x, y, z, P);
+        load_cell<L, TL, false, PULL, NARROW>(P, idx, o, 0u, f, g);
+    }
+    if (MASKED) {
+        if (m & SOLID_BIT) return;
+        if (m & wall_bits<L>()) fix_wall_loads<L, TL, PULL, NARROW>(P, idx, m, f, g);
+    }
+    collide<L, TL, COLL>(f, g, P.c);
+    int is = idx;
+    asm volatile("" : "+r"(is));
+    store_natural<L, TL, NARROW>(P, Wf, Wg, is, f, g);
+}
+
+template <class L, class TL, int COLL, bool MASKED, bool NARROW>
+__global__ void __launch_bounds__(256) pull_kernel(const Params P)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    pull_step_cell<L, TL, COLL, MASKED, NARROW>(P, P.fo, P.go, x, y, z);
+}
+
+// SPLIT mode, pass 1: collide in place in the natural slots.
+template <class L, class TL, int COLL, bool MASKED, bool NARROW>
+__global__ void __launch_bounds__(256) collide_kernel(const Params P)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    const int idx = x + P.nx * (y + P.ny * z);
+    if (MASKED && (P.mask[idx] & SOLID_BIT)) return;
+    float f[L::Q], g[TL::QA];
+    const Offs o{};
+    load_cell<L, TL, false, NATURAL, NARROW>(P, idx, o, 0u, f, g);
+    collide<L, TL, COLL>(f, g, P.c);
+    store_natural<L, TL, NARROW>(P, P.f, P.g, idx, f, g);
+}
+
+// SPLIT mode, pass 2: pull the post-collision populations into the other buffer.
+template <class L, class TL, bool MASKED, bool NARROW>
+__global__ void __launch_bounds__(256) stream_kernel(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
@@ -207,28 +361,18 @@ __global__ void __launch_bounds__(256) step_kernel(const Params P)
         if (m & SOLID_BIT) return;
     }
     float f[L::Q], g[TL::QA];
-    {
-        Offs o{};
-        if (ODD) o = make_offs(x, y, z, P);
-        load_cell<L, TL, MASKED, ODD, NARROW>(P, idx, o, m, f, g);
-    }
-    collide<L, TL, COLL>(f, g, P.c);
-    // Recompute the store addresses after the collision instead of keeping the load-time
-    // values live through it (the empty asm hides that they are the same).
-    int xs = x, ys = y, zs = z, is = idx;
-    uint32_t ms = m;
-    asm volatile("" : "+r"(xs), "+r"(ys), "+r"(zs), "+r"(is), "+r"(ms));
-    Offs o{};
-    if (ODD) o = make_offs(xs, ys, zs, P);
-    store_cell<L, TL, MASKED, ODD, NARROW>(P, is, o, ms, f, g);
+    const Offs o = make_offs(x, y, z, P);
+    load_cell<L, TL, MASKED, PULL, NARROW>(P, idx, o, m, f, g);
+    store_natural<L, TL, NARROW>(P, P.fo, P.go, idx, f, g);
 }
 
 // ------------------------------------------------------------ auxiliary kernels -------
 
-// f = f_eq(rho, u) - w, g = g_eq(T, u) into the natural slots (parity 0) of one cell.
-template <class L, class TL>
+// f = f_eq(rho, u) - w, g = g_eq(T, u) as the logical state of one cell, stored for read
+// pattern PAT (NATURAL for AA and SPLIT, PULL for the PULL mode).
+template <class L, class TL, int PAT = NATURAL>
 LBM_HD void init_cell(const Params &P, int idx, const float *rho, const float *u,
-                      const float *T)
+                      const float *T, int x = 0, int y = 0, int z = 0)
 {
     const size_t N = (size_t)P.nx * P.ny * P.nz;
     const bool solid = P.mask && (P.mask[idx] & SOLID_BIT);
@@ -251,15 +395,17 @@ LBM_HD void init_cell(const Params &P, int idx, const float *rho, const float *u
         if constexpr (TL::Q == 7) d3q7_equilibrium(g, P.c.a_T, T[idx], ux, uy, uz);
         if constexpr (TL::Q == 5) d2q5_equilibrium(g, P.c.a_T, T[idx], ux, uy);
     }
-#pragma unroll
-    for (int q = 0; q < L::Q; ++q) P.f[q * P.S + idx] = f[q];
-    if constexpr (TL::Q > 0) {
-#pragma unroll
-        for (int k = 0; k < TL::Q; ++k) P.g[k * P.S + idx] = g[k];
+    if constexpr (PAT == NATURAL) {
+        store_natural<L, TL, false>(P, P.f, P.g, idx, f, g);
+    } else {
+        if (solid) return;   // a solid cell's slots are never read
+        const uint32_t m = P.mask ? P.mask[idx] : 0u;
+        const Offs o = make_offs(x, y, z, P);
+        store_logical<L, TL, true, PAT>(P, idx, o, m, f, g);
     }
 }
 
-template <class L, class TL>
+template <class L, class TL, int PAT>
 __global__ void init_kernel(const Params P, const float *__restrict__ rho,
                             const float *__restrict__ u, const float *__restrict__ T)
 {
@@ -267,7 +413,7 @@ __global__ void init_kernel(const Params P, const float *__restrict__ rho,
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
     if (x >= P.nx || y >= P.ny) return;
-    init_cell<L, TL>(P, x + P.nx * (y + P.ny * z), rho, u, T);
+    init_cell<L, TL, PAT>(P, x + P.nx * (y + P.ny * z), rho, u, T, x, y, z);
 }
 
 // Link mask of cell (x, y, z): bit q (1..Q-1) when the link x -> x + c_q leaves the
@@ -317,7 +463,7 @@ __global__ void mask_kernel(const Params P, const uint8_t *__restrict__ solid,
 }
 
 // Macroscopic fields of the logical state: rho, u = (j + F/2)/rho, T.
-template <class L, class TL, bool MASKED, bool ODD>
+template <class L, class TL, bool MASKED, int PAT>
 __global__ void macro_kernel(const Params P, float *__restrict__ rho, float *__restrict__ u,
                              float *__restrict__ T)
 {
@@ -338,9 +484,9 @@ __global__ void macro_kernel(const Params P, float *__restrict__ rho, float *__r
         return;
     }
     Offs o{};
-    if (ODD) o = make_offs(x, y, z, P);
+    if (PAT != NATURAL) o = make_offs(x, y, z, P);
     float f[L::Q], g[TL::QA];
-    load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+    load_cell<L, TL, MASKED, PAT>(P, idx, o, m, f, g);
     float dr = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f, t = 0.0f;
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
@@ -366,7 +512,7 @@ __global__ void macro_kernel(const Params P, float *__restrict__ rho, float *__r
 }
 
 // Logical populations out (f unshifted), or in (SET).
-template <class L, class TL, bool MASKED, bool ODD, bool SET>
+template <class L, class TL, bool MASKED, int PAT, bool SET>
 __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__restrict__ go)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
@@ -386,7 +532,7 @@ __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__rest
         return;
     }
     Offs o{};
-    if (ODD) o = make_offs(x, y, z, P);
+    if (PAT != NATURAL) o = make_offs(x, y, z, P);
     float f[L::Q], g[TL::QA];
     if (SET) {
 #pragma unroll
@@ -395,9 +541,9 @@ __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__rest
 #pragma unroll
             for (int k = 0; k < TL::Q; ++k) g[k] = go[k * N + idx];
         }
-        store_logical<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+        store_logical<L, TL, MASKED, PAT>(P, idx, o, m, f, g);
     } else {
-        load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+        load_cell<L, TL, MASKED, PAT>(P, idx, o, m, f, g);
 #pragma unroll
         for (int q = 0; q < L::Q; ++q) fo[q * N + idx] = f[q] + L::w(q);
         if constexpr (TL::Q > 0) {
@@ -415,7 +561,7 @@ __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__rest
 constexpr int DIAG_N = 16;
 constexpr int DIAG_THREADS = 256;
 
-template <class L, class TL, bool MASKED, bool ODD>
+template <class L, class TL, bool MASKED, int PAT>
 __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, double *partial)
 {
     double acc[15];
@@ -432,9 +578,9 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
         if (MASKED) m = P.mask[idx];
         if (m & SOLID_BIT) continue;
         Offs o{};
-        if (ODD) o = make_offs(x, y, z, P);
+        if (PAT != NATURAL) o = make_offs(x, y, z, P);
         float f[L::Q], g[TL::QA];
-        load_cell<L, TL, MASKED, ODD>(P, idx, o, m, f, g);
+        load_cell<L, TL, MASKED, PAT>(P, idx, o, m, f, g);
         // per-cell sums in fp32 (GB300's fp64 rate is low), running totals in fp64
         float dr = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f, t = 0.0f;
 #pragma unroll

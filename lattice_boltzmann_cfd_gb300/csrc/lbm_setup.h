@@ -31,7 +31,9 @@ struct Layout {
     long long N = 0;
     size_t S = 0;
     bool masked = false, has_solid = false;
-    size_t off_f = 0, off_g = 0, off_mask = 0, off_solid = 0, off_partial = 0, off_result = 0;
+    int streaming = LBM_STREAM_AA;
+    size_t off_f = 0, off_g = 0, off_f2 = 0, off_g2 = 0, off_mask = 0, off_solid = 0;
+    size_t off_partial = 0, off_result = 0;
     size_t bytes = 0;
 };
 
@@ -90,6 +92,9 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
         if (!std::isfinite(c->T_wall[i])) return bad(LBM_ERR_ARG, "T_wall must be finite");
         any_wall |= c->face_flow[i] == LBM_FACE_WALL;
     }
+    if (c->streaming != LBM_STREAM_AA && c->streaming != LBM_STREAM_PULL &&
+        c->streaming != LBM_STREAM_SPLIT)
+        return bad(LBM_ERR_ARG, "streaming must be LBM_STREAM_AA, _PULL or _SPLIT");
     for (int a = 0; a < dim; ++a)
         if (c->face_flow[2 * a] != c->face_flow[2 * a + 1])
             return bad(LBM_ERR_UNSUPPORTED,
@@ -107,6 +112,13 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     off = align_up(off + (size_t)Q * L->S * sizeof(float));
     L->off_g = off;
     off = align_up(off + (size_t)QT * L->S * sizeof(float));
+    L->streaming = c->streaming;
+    L->off_f2 = L->off_g2 = off;
+    if (c->streaming != LBM_STREAM_AA) {
+        off = align_up(off + (size_t)Q * L->S * sizeof(float));
+        L->off_g2 = off;
+        off = align_up(off + (size_t)QT * L->S * sizeof(float));
+    }
     L->off_mask = off;
     if (L->masked) off = align_up(off + L->S * sizeof(uint32_t));
     L->off_solid = off;
@@ -123,6 +135,9 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
 {
     P.f = reinterpret_cast<float *>(ws + L.off_f);
     P.g = L.QT ? reinterpret_cast<float *>(ws + L.off_g) : nullptr;
+    const bool two = L.streaming != LBM_STREAM_AA;
+    P.fo = two ? reinterpret_cast<float *>(ws + L.off_f2) : nullptr;
+    P.go = (two && L.QT) ? reinterpret_cast<float *>(ws + L.off_g2) : nullptr;
     P.mask = L.masked ? reinterpret_cast<const uint32_t *>(ws + L.off_mask) : nullptr;
     P.S = L.S;
     P.nx = g.nx;

@@ -33,9 +33,11 @@ def anti_bounce_back_weight(thermal: int, a_T: float) -> float:
     return (4.0 + a_T) / 10.0 if thermal == 5 else (6.0 + a_T) / 21.0
 
 
-def make_config(w):
-    """lbm_config for a problem description; returns (cfg, keep-alive objects)."""
+def make_config(w, streaming: str = "aa"):
+    """lbm_config for a problem description; returns (cfg, keep-alive objects).
+    ``streaming``: "aa" (in place), "pull" or "split" (two buffers)."""
     cfg = capi.lbm_config()
+    cfg.streaming = capi.STREAMING[streaming]
     cfg.nx, cfg.ny, cfg.nz = (int(v) for v in w.shape)
     cfg.lattice = int(w.lattice)
     cfg.thermal = int(w.thermal)
@@ -79,12 +81,12 @@ class Simulation:
     populations (Q, nz, ny, nx); they may live on the device or in page-locked host
     memory."""
 
-    def __init__(self, w, device=None, stream=None, edit=None):
+    def __init__(self, w, device=None, stream=None, edit=None, streaming: str = "aa"):
         """``edit``, if given, is called with the ``lbm_config`` before it is used (to set
-        raw fields such as individual rates)."""
+        raw fields such as individual rates).  ``streaming``: "aa", "pull" or "split"."""
         import torch
         self.device = torch.device(device if device is not None else "cuda")
-        self.cfg, self._keep = make_config(w)
+        self.cfg, self._keep = make_config(w, streaming)
         if edit is not None:
             edit(self.cfg)
         self.nbytes = capi.lbm_workspace_bytes(self.cfg)

@@ -1,7 +1,7 @@
 // Host emulation of the CUDA path's AA step, for tests only (built by tests/conftest.py).
 //
-// Runs the library's own per-cell functions (cell_mask, init_cell, load_cell, collide,
-// store_cell) on the CPU, one cell at a time, but writes every step into a second buffer
+// Runs the library's own per-cell functions (cell_mask, init_cell, aa_step_cell,
+// pull_step_cell, load_cell, collide, store_natural) on the CPU, one cell at a time, but writes every step into a second buffer
 // filled with NaN beforehand.  If a cell read a slot that another cell writes in the
 // same step, or two cells wrote one slot, or a slot of a fluid cell were left unwritten,
 // the stale or NaN value would reach the results; tests compare them with the oracle.
@@ -22,23 +22,44 @@ void step_all(const Params &Pr, const Params &Pw)
 {
     for (int z = 0; z < Pr.nz; ++z)
         for (int y = 0; y < Pr.ny; ++y)
-            for (int x = 0; x < Pr.nx; ++x) {
-                const int idx = x + Pr.nx * (y + Pr.ny * z);
-                uint32_t m = 0;
-                if (M) {
-                    m = Pr.mask[idx];
-                    if (m & SOLID_BIT) continue;
-                }
-                Offs o{};
-                if (O) o = make_offs(x, y, z, Pr);
+            for (int x = 0; x < Pr.nx; ++x) aa_step_cell<L, TL, C, M, O, NARROW>(Pr, Pw, x, y, z);
+}
+
+// Two-buffer PULL step: pull from P.f, collide, natural store into W.
+template <class L, class TL, int C, bool M, bool NARROW>
+void pull_all(const Params &P, float *Wf, float *Wg)
+{
+    for (int z = 0; z < P.nz; ++z)
+        for (int y = 0; y < P.ny; ++y)
+            for (int x = 0; x < P.nx; ++x) pull_step_cell<L, TL, C, M, NARROW>(P, Wf, Wg, x, y, z);
+}
+
+// SPLIT step: collide in place, then pull from P.f into W.
+template <class L, class TL, int C, bool M, bool NARROW>
+void split_all(const Params &P, float *Wf, float *Wg)
+{
+    const Offs none{};
+    for (int i = 0; i < P.nx * P.ny * P.nz; ++i) {
+        if (M && (P.mask[i] & SOLID_BIT)) continue;
+        float f[L::Q], g[TL::QA];
+        load_cell<L, TL, false, NATURAL, NARROW>(P, i, none, 0u, f, g);
+        collide<L, TL, C>(f, g, P.c);
+        store_natural<L, TL, NARROW>(P, P.f, P.g, i, f, g);
+    }
+    for (int z = 0; z < P.nz; ++z)
+        for (int y = 0; y < P.ny; ++y)
+            for (int x = 0; x < P.nx; ++x) {
+                const int idx = x + P.nx * (y + P.ny * z);
+                const uint32_t m = M ? P.mask[idx] : 0u;
+                if (m & SOLID_BIT) continue;
+                const Offs o = make_offs(x, y, z, P);
                 float f[L::Q], g[TL::QA];
-                load_cell<L, TL, M, O, NARROW>(Pr, idx, o, m, f, g);
-                collide<L, TL, C>(f, g, Pr.c);
-                store_cell<L, TL, M, O, NARROW>(Pw, idx, o, m, f, g);
+                load_cell<L, TL, M, PULL, NARROW>(P, idx, o, m, f, g);
+                store_natural<L, TL, NARROW>(P, Wf, Wg, idx, f, g);
             }
 }
 
-template <class L, class TL, bool M, bool O>
+template <class L, class TL, bool M, int O>
 void read_all(const Params &P, float *fout, float *gout)
 {
     const size_t N = (size_t)P.nx * P.ny * P.nz;
@@ -54,7 +75,7 @@ void read_all(const Params &P, float *fout, float *gout)
                     continue;
                 }
                 Offs o{};
-                if (O) o = make_offs(x, y, z, P);
+                if (O != NATURAL) o = make_offs(x, y, z, P);
                 load_cell<L, TL, M, O>(P, idx, o, m, f, g);
                 for (int q = 0; q < L::Q; ++q) fout[q * N + idx] = f[q] + L::w(q);
                 for (int k = 0; k < TL::Q; ++k) gout[k * N + idx] = g[k];
@@ -65,6 +86,7 @@ template <class L, class TL, int C, bool NARROW>
 int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, const float *u,
         const float *T, int steps, float *fout, float *gout, uint32_t *mask_out)
 {
+    const int mode = cfg.streaming;
     const float nan = std::numeric_limits<float>::quiet_NaN();
     const size_t S = Lay.S;
     std::vector<float> f(Lay.Q * S, nan), fn(Lay.Q * S, nan);
@@ -82,7 +104,13 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
                 for (int x = 0; x < cfg.nx; ++x)
                     mask[x + cfg.nx * (y + cfg.ny * z)] =
                         cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
-    for (long long i = 0; i < Lay.N; ++i) init_cell<L, TL>(P, (int)i, rho, u, T);
+    for (int z = 0; z < cfg.nz; ++z)
+        for (int y = 0; y < cfg.ny; ++y)
+            for (int x = 0; x < cfg.nx; ++x) {
+                const int i = x + cfg.nx * (y + cfg.ny * z);
+                if (mode == LBM_STREAM_PULL) init_cell<L, TL, PULL>(P, i, rho, u, T, x, y, z);
+                else init_cell<L, TL, NATURAL>(P, i, rho, u, T, x, y, z);
+            }
     int parity = 0;
     for (int s = 0; s < steps; ++s) {
         std::fill(fn.begin(), fn.end(), nan);
@@ -90,7 +118,14 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
         Params Pw = P;
         Pw.f = fn.data();
         Pw.g = Lay.QT ? gn.data() : nullptr;
-        if (Lay.masked) {
+        float *wg = Lay.QT ? gn.data() : nullptr;
+        if (mode == LBM_STREAM_PULL) {
+            if (Lay.masked) pull_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
+            else pull_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
+        } else if (mode == LBM_STREAM_SPLIT) {
+            if (Lay.masked) split_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
+            else split_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
+        } else if (Lay.masked) {
             if (parity) step_all<L, TL, C, true, true, NARROW>(P, Pw);
             else step_all<L, TL, C, true, false, NARROW>(P, Pw);
         } else {
@@ -103,12 +138,16 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
         P.g = Lay.QT ? g.data() : nullptr;
         parity ^= 1;
     }
+    const int pat = mode == LBM_STREAM_PULL ? PULL
+                    : (mode == LBM_STREAM_AA && parity) ? AA_ODD : NATURAL;
     if (Lay.masked) {
-        if (parity) read_all<L, TL, true, true>(P, fout, gout);
-        else read_all<L, TL, true, false>(P, fout, gout);
+        if (pat == PULL) read_all<L, TL, true, PULL>(P, fout, gout);
+        else if (pat == AA_ODD) read_all<L, TL, true, AA_ODD>(P, fout, gout);
+        else read_all<L, TL, true, NATURAL>(P, fout, gout);
     } else {
-        if (parity) read_all<L, TL, false, true>(P, fout, gout);
-        else read_all<L, TL, false, false>(P, fout, gout);
+        if (pat == PULL) read_all<L, TL, false, PULL>(P, fout, gout);
+        else if (pat == AA_ODD) read_all<L, TL, false, AA_ODD>(P, fout, gout);
+        else read_all<L, TL, false, NATURAL>(P, fout, gout);
     }
     if (mask_out) std::memcpy(mask_out, mask.data(), sizeof(uint32_t) * (size_t)Lay.N);
     return 0;

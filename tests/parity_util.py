@@ -72,9 +72,9 @@ def mask_brute_force(w) -> np.ndarray:
     return m.astype(np.uint32)
 
 
-def emulate(emu_lib, w, steps, narrow=True):
+def emulate(emu_lib, w, steps, narrow=True, streaming="aa"):
     """(f, g, mask) after ``steps`` steps of the host emulation of the CUDA kernels."""
-    cfg, keep = make_config(w)
+    cfg, keep = make_config(w, streaming)
     N = w.cells
     fo = np.zeros((w.lattice, N), np.float32)
     go = np.zeros((max(w.thermal, 1), N), np.float32)
@@ -122,11 +122,11 @@ def split_steps(n):
     return out
 
 
-def gpu_states(w, checkpoints, window_fn=None, edit=None):
+def gpu_states(w, checkpoints, window_fn=None, edit=None, streaming="aa"):
     """{steps: dict} of the CUDA path's results (numpy), stepping in uneven chunks."""
     import torch
     from lattice_boltzmann_cfd_gb300 import Simulation
-    sim = Simulation(w, edit=edit)
+    sim = Simulation(w, edit=edit, streaming=streaming)
     dev = sim.device
     T = torch.from_numpy(np.ascontiguousarray(w.T_init)).to(dev) if w.thermal else None
     sim.init_equilibrium(torch.from_numpy(np.ascontiguousarray(w.rho0)).to(dev),

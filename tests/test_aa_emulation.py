@@ -1,4 +1,5 @@
-"""Host emulation of the CUDA path's in-place AA step against the oracle (CPU).
+"""Host emulation of the CUDA path's steps (in-place AA, two-buffer PULL and SPLIT)
+against the oracle (CPU).
 
 The library's own per-cell functions run on the CPU with each step written into a
 NaN-filled second buffer, so a slot read after another cell overwrote it, a slot written
@@ -14,13 +15,15 @@ from parity_util import emulate, fluid_of, mask_brute_force, oracle_states, smal
 CASES = small_cases()
 
 
-@pytest.mark.parametrize("narrow", [True, False], ids=["idx32", "idx64"])
+@pytest.mark.parametrize("mode,narrow", [("aa", True), ("aa", False), ("pull", True),
+                                         ("pull", False), ("split", True)],
+                         ids=["aa-idx32", "aa-idx64", "pull-idx32", "pull-idx64", "split-idx32"])
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_emulated_aa_step_matches_oracle(oracle_mod, emu_lib, w, narrow):
+def test_emulated_step_matches_oracle(oracle_mod, emu_lib, w, mode, narrow):
     ref = oracle_states(oracle_mod, w, [1, 2, 5, 6])
     fluid = fluid_of(w)
     for n, r in ref.items():
-        f, g, _ = emulate(emu_lib, w, n, narrow)
+        f, g, _ = emulate(emu_lib, w, n, narrow, mode)
         assert not np.isnan(f[:, fluid]).any()
         assert np.abs(f - r["f"])[:, fluid].max() < 1e-6, n
         if w.thermal:

@@ -31,11 +31,13 @@ def _cuda():
 
 # ----------------------------------------------------------------- small grids ----
 
+@pytest.mark.parametrize("streaming", ["aa", "pull", "split"])
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_small_grids_few_steps(oracle_mod, w):
-    """Every lattice / collision / boundary kind on tiny grids after 1, 2, 5, 6 steps."""
+def test_small_grids_few_steps(oracle_mod, w, streaming):
+    """Every lattice / collision / boundary kind on tiny grids after 1, 2, 5, 6 steps, in
+    each population layout."""
     ref = oracle_states(oracle_mod, w, [1, 2, 5, 6])
-    got = gpu_states(w, [1, 2, 5, 6])
+    got = gpu_states(w, [1, 2, 5, 6], streaming=streaming)
     for n in ref:
         compare_fields(w, got[n], ref[n], tol=1e-6)
         assert got[n]["parity"] == n % 2
@@ -74,6 +76,46 @@ def test_configs_200_and_201_steps(oracle_mod, w):
         assert np.allclose(d["momentum"], dr["momentum"], rtol=1e-4, atol=1e-6 * dr["mass"])
         if w.thermal:
             assert np.allclose(d["heat"], dr["heat"], rtol=1e-4, atol=1e-3)
+
+
+TWO_BUFFER = [REDUCED[i] for i in (0, 1, 3, 5, 7)]   # TG, periodic, and the perturbed ones
+
+
+@pytest.mark.parametrize("streaming", ["pull", "split"])
+@pytest.mark.parametrize("w", TWO_BUFFER, ids=[c.name for c in TWO_BUFFER])
+def test_two_buffer_modes_200_and_201_steps(oracle_mod, w, streaming):
+    """The two-buffer layouts against the oracle after 200 and 201 steps."""
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    got = gpu_states(w, [200, 201], streaming=streaming)
+    for n in (200, 201):
+        compare_fields(w, got[n], ref[n])
+        if w.solid is not None:
+            F, Fr = np.array(got[n]["diag"]["force"]), ref[n]["force"]
+            assert np.linalg.norm(F - Fr) <= TOL_FORCE_REL * np.linalg.norm(Fr), (F, Fr)
+
+
+def test_layouts_continue_each_others_state():
+    """A state saved from the AA layout and restored into a PULL and a SPLIT context
+    continues on the same trajectory (fp32 rounding only)."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.perturbed(W.cavity3d(shape=(40, 20, 18)), seed=12)
+    dev = torch.device("cuda")
+    a = Simulation(w)
+    a.init_equilibrium(torch.from_numpy(w.rho0).to(dev), torch.from_numpy(w.u0).to(dev),
+                       torch.from_numpy(w.T_init).to(dev))
+    a.step(31)
+    f0, g0 = a.populations()
+    a.step(40)
+    fa, ga = a.populations()
+    for mode in ("pull", "split"):
+        b = Simulation(w, streaming=mode)
+        b.set_populations(f0, g0)
+        b.step(40)
+        fb, gb = b.populations()
+        assert (fa - fb).abs().max().item() < 1e-6
+        assert (ga - gb).abs().max().item() < 1e-6
+        b.close()
+    a.close()
 
 
 @pytest.mark.parametrize("name", ["random_periodic", "channel_sphere"])
@@ -210,13 +252,13 @@ def test_checkpoint_resume(oracle_mod):
     a.close()
 
 
-@pytest.mark.parametrize("parity", [0, 1])
-def test_set_get_roundtrip(parity):
-    """set then get returns the populations bit for bit at either parity (values within
-    a factor 2 of w_q subtract and re-add exactly)."""
+@pytest.mark.parametrize("parity,streaming", [(0, "aa"), (1, "aa"), (1, "pull"), (1, "split")])
+def test_set_get_roundtrip(parity, streaming):
+    """set then get returns the populations bit for bit at either parity and in every
+    layout (values within a factor 2 of w_q subtract and re-add exactly)."""
     from lattice_boltzmann_cfd_gb300 import Simulation
     w = W.perturbed(W.channel_sphere(shape=(40, 16, 14), center=(10, 8, 7), radius=3), seed=3)
-    sim = Simulation(w)
+    sim = Simulation(w, streaming=streaming)
     dev = sim.device
     sim.init_equilibrium(torch.from_numpy(w.rho0).to(dev), torch.from_numpy(w.u0).to(dev))
     sim.step(parity)
