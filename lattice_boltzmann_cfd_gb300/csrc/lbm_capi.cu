@@ -48,6 +48,17 @@ struct lbm_ctx {
     long long steps = 0;
     bool initialized = false;
     std::string err;
+    // CUDA graphs of GRAPH_STEPS steps, one per start parity, built on first use for
+    // grids small enough that launch overhead matters; captured on a private stream.
+    cudaGraphExec_t graph[2] = {nullptr, nullptr};
+    cudaStream_t capture_stream = nullptr;
+    bool graphs_disabled = false;
+    ~lbm_ctx()
+    {
+        for (auto &g : graph)
+            if (g) cudaGraphExecDestroy(g);
+        if (capture_stream) cudaStreamDestroy(capture_stream);
+    }
 };
 
 namespace {
@@ -195,8 +206,10 @@ lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, co
     if (s == LBM_OK && c->L.QT) s = device_address(c, T, "T", &dT);
     if (s != LBM_OK) return s;
     // the AA state starts at parity 0 (natural slots); SPLIT stores the natural state;
-    // PULL stores a post-collision state read with the pull pattern
+    // PULL stores a post-collision state read with the pull pattern.  Parity 0 always
+    // means the first population buffer is current (the step graphs rely on it).
     c->parity = 0;
+    lbm_setup::fill_params(c->cfg, c->L, c->ws, c->P);
     const int pat = (c->L.streaming == LBM_STREAM_PULL) ? lbm::PULL : lbm::NATURAL;
     cudaError_t e = lbm::launch_init(c->cfg.lattice, c->cfg.thermal, pat, c->P,
                                      (const float *)dr, (const float *)du, (const float *)dT,
@@ -208,41 +221,97 @@ lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, co
     return LBM_OK;
 }
 
-lbm_status lbm_step(lbm_ctx *c, int n)
+namespace {
+
+constexpr int GRAPH_STEPS = 64;                    // even: parity and buffers come back
+constexpr long long GRAPH_MAX_CELLS = 1LL << 22;   // launch-bound below ~4 M cells
+
+// Enqueue one step on `stream` from the state (P, parity) and advance them.
+cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStream_t stream)
 {
-    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
-    if (n < 0) return fail(c, LBM_ERR_ARG, "n must be >= 0");
-    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
-    DeviceGuard guard(c->device);
     const lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
     // 32-bit population indices when the largest index (Q * S - 1) fits
     const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
     const bool d3 = c->cfg.lattice == LBM_D3Q19;
     const int th = c->cfg.thermal, coll = c->cfg.collision;
     const bool masked = c->L.masked;
+    cudaError_t e;
+    switch (c->L.streaming) {
+    case LBM_STREAM_PULL:
+        e = d3 ? lbm::launch_pull_d3q19(th, coll, masked, narrow, P, sh, stream)
+               : lbm::launch_pull_d2q9(th, coll, masked, narrow, P, sh, stream);
+        break;
+    case LBM_STREAM_SPLIT:
+        e = d3 ? lbm::launch_split_d3q19(th, coll, masked, narrow, P, sh, stream)
+               : lbm::launch_split_d2q9(th, coll, masked, narrow, P, sh, stream);
+        break;
+    default:
+        e = d3 ? lbm::launch_step_d3q19(th, coll, masked, parity != 0, narrow, P, sh, stream)
+               : lbm::launch_step_d2q9(th, coll, masked, parity != 0, narrow, P, sh, stream);
+    }
+    if (c->L.streaming != LBM_STREAM_AA) {
+        std::swap(P.f, P.fo);
+        std::swap(P.g, P.go);
+    }
+    parity ^= 1;
+    return e;
+}
+
+// The graph of GRAPH_STEPS steps starting at the context's parity (built on first use).
+// Returns nullptr (and stops trying) if capture is not possible.
+cudaGraphExec_t step_graph(lbm_ctx *c)
+{
+    if (c->graphs_disabled) return nullptr;
+    cudaGraphExec_t &exec = c->graph[c->parity];
+    if (exec) return exec;
+    if (!c->capture_stream &&
+        cudaStreamCreateWithFlags(&c->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        c->graphs_disabled = true;
+        return nullptr;
+    }
+    cudaGraph_t graph = nullptr;
+    bool ok = cudaStreamBeginCapture(c->capture_stream, cudaStreamCaptureModeRelaxed) ==
+              cudaSuccess;
+    lbm::Params P = c->P;
+    int parity = c->parity;
+    for (int i = 0; ok && i < GRAPH_STEPS; ++i)
+        ok = enqueue_step(c, P, parity, c->capture_stream) == cudaSuccess;
+    const cudaError_t end = cudaStreamEndCapture(c->capture_stream, &graph);
+    ok = ok && end == cudaSuccess && graph &&
+         cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+    if (graph) cudaGraphDestroy(graph);
+    if (!ok) {
+        cudaGetLastError();
+        exec = nullptr;
+        c->graphs_disabled = true;
+    }
+    return exec;
+}
+
+}  // namespace
+
+lbm_status lbm_step(lbm_ctx *c, int n)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (n < 0) return fail(c, LBM_ERR_ARG, "n must be >= 0");
+    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    DeviceGuard guard(c->device);
+    // Small grids: replay a captured graph of GRAPH_STEPS steps (it leaves the parity and
+    // the buffers as it found them), then launch the remainder one by one.
+    if (c->L.N <= GRAPH_MAX_CELLS && n >= GRAPH_STEPS) {
+        while (n >= GRAPH_STEPS) {
+            cudaGraphExec_t exec = step_graph(c);
+            if (!exec) break;
+            cudaError_t e = cudaGraphLaunch(exec, c->stream);
+            if (e != cudaSuccess) return cuda_fail(c, e, "step graph");
+            c->steps += GRAPH_STEPS;
+            n -= GRAPH_STEPS;
+        }
+    }
     for (int i = 0; i < n; ++i) {
-        cudaError_t e;
-        switch (c->L.streaming) {
-        case LBM_STREAM_PULL:
-            e = d3 ? lbm::launch_pull_d3q19(th, coll, masked, narrow, c->P, sh, c->stream)
-                   : lbm::launch_pull_d2q9(th, coll, masked, narrow, c->P, sh, c->stream);
-            break;
-        case LBM_STREAM_SPLIT:
-            e = d3 ? lbm::launch_split_d3q19(th, coll, masked, narrow, c->P, sh, c->stream)
-                   : lbm::launch_split_d2q9(th, coll, masked, narrow, c->P, sh, c->stream);
-            break;
-        default: {
-            const bool odd = c->parity != 0;
-            e = d3 ? lbm::launch_step_d3q19(th, coll, masked, odd, narrow, c->P, sh, c->stream)
-                   : lbm::launch_step_d2q9(th, coll, masked, odd, narrow, c->P, sh, c->stream);
-        }
-        }
+        cudaError_t e = enqueue_step(c, c->P, c->parity, c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "step kernel");
-        if (c->L.streaming != LBM_STREAM_AA) {
-            std::swap(c->P.f, c->P.fo);
-            std::swap(c->P.g, c->P.go);
-        }
-        c->parity ^= 1;
         ++c->steps;
     }
     return LBM_OK;
