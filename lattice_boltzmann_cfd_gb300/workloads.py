@@ -67,6 +67,11 @@ class Workload:
     u0: Optional[np.ndarray] = None
     T_init: Optional[np.ndarray] = None
     steps: int = 0
+    # immersed-boundary samples: positions (n, 3) in cell units (cell centres at integers),
+    # boundary velocities (n, 3), weights (n,); all float32
+    ib_x: Optional[np.ndarray] = None
+    ib_ub: Optional[np.ndarray] = None
+    ib_w: Optional[np.ndarray] = None
 
     @property
     def dim(self) -> int:
@@ -155,6 +160,32 @@ def channel_sphere(n: int = 128, radius: float = 16, center=(40, 64, 64), gx: fl
         g_body=(gx, 0.0, 0.0),
         face_flow=("periodic", "periodic", "wall", "wall", "wall", "wall"),
         solid=sphere_mask(shape, center, radius), rho0=rho, u0=u, steps=2000)
+
+
+def sphere_samples(center, radius: float, n: int, seed: int = 0) -> np.ndarray:
+    """n points spread evenly over a sphere (Fibonacci lattice, randomly rotated by a seeded
+    rotation), float32 (n, 3).  A stand-in for Poisson-disk surface sampling."""
+    k = np.arange(n) + 0.5
+    phi = np.arccos(1.0 - 2.0 * k / n)
+    theta = math.pi * (1.0 + 5.0 ** 0.5) * k
+    pts = np.stack([np.cos(theta) * np.sin(phi), np.sin(theta) * np.sin(phi), np.cos(phi)], 1)
+    q, _ = np.linalg.qr(np.random.default_rng(seed).standard_normal((3, 3)))
+    return (np.asarray(center, np.float64) + radius * pts @ q.T).astype(np.float32)
+
+
+def channel_ib_sphere(n: int = 128, radius: float = 16, center=(40, 64, 64),
+                      gx: float = 1e-6, nu: float = 0.02, samples_per_area: float = 4.0,
+                      shape=None) -> Workload:
+    """Config 3's channel with the sphere represented by immersed-boundary samples instead
+    of bounce-back cells: samples_per_area samples per unit area, each weighted by the area
+    it represents, at rest."""
+    w = channel_sphere(n=n, radius=radius, center=center, gx=gx, nu=nu, shape=shape)
+    area = 4.0 * math.pi * radius * radius
+    ns = max(4, int(round(samples_per_area * area)))
+    x = sphere_samples(center, radius, ns)
+    return dataclasses.replace(
+        w, name=w.name.replace("+ sphere", "+ IB sphere") + f" ({ns} samples)", solid=None,
+        ib_x=x, ib_ub=np.zeros_like(x), ib_w=np.full(ns, area / ns, np.float32))
 
 
 def cavity_parameters(H: float, Ra: float, Pr: float, Uff: float, dT: float = 1.0):

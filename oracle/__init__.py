@@ -60,6 +60,8 @@ class _Problem(ctypes.Structure):
         ("x0", ctypes.c_int), ("y0", ctypes.c_int), ("z0", ctypes.c_int),
         ("wx", ctypes.c_int), ("wy", ctypes.c_int), ("wz", ctypes.c_int),
         ("solid", ctypes.POINTER(ctypes.c_ubyte)),
+        ("ib_n", ctypes.c_int), ("ib_x", ctypes.POINTER(ctypes.c_double)),
+        ("ib_ub", ctypes.POINTER(ctypes.c_double)), ("ib_w", ctypes.POINTER(ctypes.c_double)),
     ]
 
 
@@ -72,8 +74,9 @@ def _load():
             D = ctypes.POINTER(ctypes.c_double)
             lib.oracle_check.argtypes = [P]
             lib.oracle_init_equilibrium.argtypes = [P, D, D, D, D, D]
-            lib.oracle_step.argtypes = [P, D, D, D, D, D]
-            lib.oracle_run.argtypes = [P, D, D, ctypes.c_int, D]
+            lib.oracle_step.argtypes = [P, D, D, D, D, D, D]
+            lib.oracle_run.argtypes = [P, D, D, ctypes.c_int, D, D]
+            lib.oracle_ib_forces.argtypes = [P, D, D, D, D]
             lib.oracle_macroscopic.argtypes = [P, D, D, D, D, D]
             lib.oracle_diagnostics.argtypes = [P, D, D, D]
             lib.oracle_lattice.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
@@ -81,7 +84,7 @@ def _load():
             lib.oracle_max_threads.argtypes = []
             for fn in ("oracle_check", "oracle_init_equilibrium", "oracle_step", "oracle_run",
                        "oracle_macroscopic", "oracle_diagnostics", "oracle_lattice",
-                       "oracle_max_threads"):
+                       "oracle_max_threads", "oracle_ib_forces"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -161,6 +164,20 @@ class Problem:
                 spec.solid[z0:z0 + wz, y0:y0 + wy, x0:x0 + wx], dtype=np.uint8)
             self._solid = sol
             p.solid = sol.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+        self._ib = []
+        ib_x = getattr(spec, "ib_x", None)
+        if ib_x is not None and len(ib_x):
+            x = np.ascontiguousarray(ib_x, dtype=np.float64).reshape(-1, 3)
+            n = x.shape[0]
+            ub = getattr(spec, "ib_ub", None)
+            ub = (np.zeros((n, 3)) if ub is None else
+                  np.ascontiguousarray(ub, dtype=np.float64).reshape(n, 3))
+            wt = getattr(spec, "ib_w", None)
+            wt = np.ones(n) if wt is None else np.ascontiguousarray(wt, dtype=np.float64)
+            self._ib = [x, ub, wt]
+            p.ib_n = n
+            p.ib_x, p.ib_ub, p.ib_w = (_dptr(a) for a in self._ib)
+        self.last_ib = np.zeros(6)
         self.p = p
         self.Q = spec.lattice
         self.QT = spec.thermal
@@ -204,11 +221,23 @@ def init_equilibrium(prob: Problem, rho, u, T=None):
 
 
 def run(prob: Problem, f, g, steps: int):
-    """Advance (f, g) in place by ``steps`` steps; returns the last step's solid force."""
+    """Advance (f, g) in place by ``steps`` steps; returns the last step's solid force
+    (the immersed boundary's reaction force and torque go to ``prob.last_ib``)."""
     force = np.zeros(3)
+    ib = np.zeros(6)
     _check(_load().oracle_run(ctypes.byref(prob.p), _dptr(f), _dptr(g), int(steps),
-                              _dptr(force)), "run")
+                              _dptr(force), _dptr(ib)), "run")
+    prob.last_ib = ib
     return force
+
+
+def ib_forces(prob: Problem, f, g):
+    """(per-cell immersed-boundary force (3, wz, wy, wx), ib[6]) of the state (f, g)."""
+    F = np.zeros((3,) + prob.wshape)
+    ib = np.zeros(6)
+    _check(_load().oracle_ib_forces(ctypes.byref(prob.p), _dptr(f), _dptr(g), _dptr(F),
+                                    _dptr(ib)), "ib_forces")
+    return F, ib
 
 
 def macroscopic(prob: Problem, f, g):

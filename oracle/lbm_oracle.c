@@ -216,6 +216,7 @@ int oracle_check(const oracle_problem *p)
         return -8;
     if (p->collision == ORC_BGK && !(p->tau > 0.5)) return -9;
     if (p->up_axis < 0 || p->up_axis > 2) return -10;
+    if (p->ib_n < 0 || (p->ib_n > 0 && !p->ib_x)) return -12;
     for (int i = 0; i < 6; ++i)
         if ((p->face_flow[i] != ORC_PERIODIC && p->face_flow[i] != ORC_WALL) ||
             (p->face_T[i] != ORC_ADIABATIC && p->face_T[i] != ORC_DIRICHLET))
@@ -296,9 +297,10 @@ static void guo_source(const lattice_t *L, const double u[3], const double F[3],
     }
 }
 
-/* Collide one fluid cell: fin/gin -> fout/gout (post-collision). */
+/* Collide one fluid cell: fin/gin -> fout/gout (post-collision).  Fext: additional force
+ * on the cell (the immersed boundary's), added to the body force. */
 static void collide_cell(const ctx_t *C, const double *fin, const double *gin, double *fout,
-                         double *gout)
+                         double *gout, const double *Fext)
 {
     const lattice_t *L = &C->F;
     const int Q = L->Q;
@@ -313,6 +315,7 @@ static void collide_cell(const ctx_t *C, const double *fin, const double *gin, d
     /* force and velocity */
     double F[3], u[3];
     body_force(C, rho, T, F);
+    for (int a = 0; a < 3; ++a) F[a] += Fext[a];
     for (int a = 0; a < 3; ++a) u[a] = (j[a] + 0.5 * F[a]) / rho;
     /* equilibrium and source */
     double feq[QMAX], Ft[QMAX];
@@ -396,6 +399,109 @@ static int pull_source(const ctx_t *C, int i, int j, int k, const int *c, long *
     return is_solid(C, *n_src) ? SRC_SOLID : SRC_CELL;
 }
 
+/* ------------------------------------------------------------ immersed boundary -- */
+
+/* Window index of the stencil node base + d (d in {0,1}^3) of a sample, or -1 if it is
+ * outside the window (unknown), -2 if it leaves the domain through a wall face. */
+static long stencil_node(const ctx_t *C, const int base[3], const int d[3])
+{
+    const oracle_problem *p = C->p;
+    const int ext[3] = {p->nx, p->ny, p->nz};
+    const int org[3] = {p->x0, p->y0, p->z0};
+    const int win[3] = {p->wx, p->wy, p->wz};
+    int s[3];
+    for (int a = 0; a < 3; ++a) {
+        s[a] = base[a] + d[a];
+        if (s[a] < 0 || s[a] >= ext[a]) {
+            if (p->face_flow[2 * a + (s[a] >= ext[a])] == ORC_WALL) return -2;
+            s[a] = (s[a] % ext[a] + ext[a]) % ext[a];
+        }
+        s[a] -= org[a];
+        if (s[a] < 0 || s[a] >= win[a]) return -1;
+    }
+    return s[0] + (long)p->wx * (s[1] + (long)p->wy * s[2]);
+}
+
+/* Immersed-boundary force per cell (Fib, 3 planes of W), from the state f, g at time t:
+ * interpolate rho and u = (j + F_body/2)/rho to each sample with the trilinear kernel
+ * (Eq. 6), penalty g_s = w rho (u_b - u) (Eq. 7), spread with the same kernel (Eq. 8).
+ * Solid cells contribute rho = 1, u = 0 and receive nothing.  Unknown stencil nodes make
+ * the sample's force NaN.  ib[6] gets -sum g_s and -sum (x_s - centroid) x g_s. */
+static int ib_forces(const ctx_t *C, const double *f, const double *g, double *Fib, double ib[6])
+{
+    const oracle_problem *p = C->p;
+    const long W = C->W;
+    const int dim = (p->lattice == 19) ? 3 : 2;
+    for (long n = 0; n < 3 * W; ++n) Fib[n] = 0.0;
+    double total[3] = {0, 0, 0}, torque[3] = {0, 0, 0}, centre[3] = {0, 0, 0};
+    for (int s = 0; s < p->ib_n; ++s)
+        for (int a = 0; a < 3; ++a) centre[a] += p->ib_x[3 * s + a] / p->ib_n;
+    for (int s = 0; s < p->ib_n; ++s) {
+        const double *xs = p->ib_x + 3 * s;
+        int base[3] = {0, 0, 0};
+        double fr[3] = {0, 0, 0};
+        for (int a = 0; a < dim; ++a) {
+            base[a] = (int)floor(xs[a]);
+            fr[a] = xs[a] - base[a];
+        }
+        long node[8];
+        double K[8];
+        int nn = 0;
+        double rho = 0.0, u[3] = {0, 0, 0};
+        for (int dz = 0; dz <= (dim == 3); ++dz)
+            for (int dy = 0; dy <= 1; ++dy)
+                for (int dx = 0; dx <= 1; ++dx) {
+                    const int d[3] = {dx, dy, dz};
+                    double k = 1.0;
+                    for (int a = 0; a < dim; ++a) k *= d[a] ? fr[a] : 1.0 - fr[a];
+                    const long nidx = stencil_node(C, base, d);
+                    if (nidx == -2) return -60;
+                    node[nn] = nidx;
+                    K[nn++] = k;
+                    if (nidx < 0) {
+                        rho = NAN;
+                        continue;
+                    }
+                    double r = 1.0, v[3] = {0, 0, 0};
+                    if (!is_solid(C, nidx)) {
+                        double j[3] = {0, 0, 0}, T = 0.0, F[3];
+                        r = 0.0;
+                        for (int q = 0; q < C->F.Q; ++q) {
+                            r += f[q * W + nidx];
+                            for (int a = 0; a < 3; ++a) j[a] += C->F.c[q][a] * f[q * W + nidx];
+                        }
+                        for (int q = 0; q < C->G.Q; ++q) T += g[q * W + nidx];
+                        body_force(C, r, T, F);
+                        for (int a = 0; a < 3; ++a) v[a] = (j[a] + 0.5 * F[a]) / r;
+                    }
+                    rho += k * r;
+                    for (int a = 0; a < 3; ++a) u[a] += k * v[a];
+                }
+        const double w = p->ib_w ? p->ib_w[s] : 1.0;
+        double gs[3];
+        for (int a = 0; a < 3; ++a) {
+            const double ub = p->ib_ub ? p->ib_ub[3 * s + a] : 0.0;
+            gs[a] = (a < dim) ? w * rho * (ub - u[a]) : 0.0;
+            total[a] -= gs[a];
+        }
+        const double r[3] = {xs[0] - centre[0], xs[1] - centre[1], xs[2] - centre[2]};
+        torque[0] -= r[1] * gs[2] - r[2] * gs[1];
+        torque[1] -= r[2] * gs[0] - r[0] * gs[2];
+        torque[2] -= r[0] * gs[1] - r[1] * gs[0];
+        for (int i = 0; i < nn; ++i) {
+            if (node[i] < 0 || is_solid(C, node[i])) continue;
+            for (int a = 0; a < 3; ++a) Fib[a * W + node[i]] += K[i] * gs[a];
+        }
+    }
+    if (ib) {
+        for (int a = 0; a < 3; ++a) {
+            ib[a] = total[a];
+            ib[3 + a] = torque[a];
+        }
+    }
+    return 0;
+}
+
 /* --------------------------------------------------------------------- the API -- */
 
 int oracle_init_equilibrium(const oracle_problem *p, const double *rho, const double *u,
@@ -426,7 +532,7 @@ int oracle_init_equilibrium(const oracle_problem *p, const double *rho, const do
 }
 
 int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, double *gpost,
-                double force[3])
+                double force[3], double ib[6])
 {
     ctx_t C;
     int rc = make_ctx(p, &C);
@@ -434,6 +540,20 @@ int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, do
     const long W = C.W;
     const int Q = C.F.Q, QT = C.G.Q;
     const int wx = p->wx, wy = p->wy, wz = p->wz;
+
+    /* 0. immersed-boundary force of this step, from the state at t */
+    double *Fib = NULL;
+    if (p->ib_n > 0) {
+        Fib = (double *)malloc(sizeof(double) * 3 * (size_t)W);
+        if (!Fib) return -40;
+        rc = ib_forces(&C, f, g, Fib, ib);
+        if (rc) {
+            free(Fib);
+            return rc;
+        }
+    } else if (ib) {
+        for (int a = 0; a < 6; ++a) ib[a] = 0.0;
+    }
 
     /* 1. collide every fluid cell into the second buffer; solid cells hold NaN there so
      *    that a read of them would show up in the results. */
@@ -447,7 +567,9 @@ int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, do
         }
         for (int q = 0; q < Q; ++q) fin[q] = f[q * W + n];
         for (int q = 0; q < QT; ++q) gin[q] = g[q * W + n];
-        collide_cell(&C, fin, gin, fo, go);
+        const double Fext[3] = {Fib ? Fib[n] : 0.0, Fib ? Fib[W + n] : 0.0,
+                                Fib ? Fib[2 * W + n] : 0.0};
+        collide_cell(&C, fin, gin, fo, go, Fext);
         for (int q = 0; q < Q; ++q) fpost[q * W + n] = fo[q];
         for (int q = 0; q < QT; ++q) gpost[q * W + n] = go[q];
     }
@@ -456,7 +578,10 @@ int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, do
      *    exchange of each row is summed in row order afterwards. */
     const long rows = (long)wy * wz;
     double *row_force = (double *)calloc((size_t)rows * 3, sizeof(double));
-    if (!row_force) return -40;
+    if (!row_force) {
+        free(Fib);
+        return -40;
+    }
 #pragma omp parallel for schedule(static)
     for (long r = 0; r < rows; ++r) {
         const int j = (int)(r % wy), k = (int)(r / wy);
@@ -513,10 +638,12 @@ int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, do
             for (int a = 0; a < 3; ++a) force[a] += row_force[3 * r + a];
     }
     free(row_force);
+    free(Fib);
     return 0;
 }
 
-int oracle_run(const oracle_problem *p, double *f, double *g, int steps, double force[3])
+int oracle_run(const oracle_problem *p, double *f, double *g, int steps, double force[3],
+               double ib[6])
 {
     ctx_t C;
     int rc = make_ctx(p, &C);
@@ -530,7 +657,9 @@ int oracle_run(const oracle_problem *p, double *f, double *g, int steps, double 
         return -40;
     }
     if (force) force[0] = force[1] = force[2] = 0.0;
-    for (int t = 0; t < steps && rc == 0; ++t) rc = oracle_step(p, f, g, fpost, gpost, force);
+    if (ib)
+        for (int a = 0; a < 6; ++a) ib[a] = 0.0;
+    for (int t = 0; t < steps && rc == 0; ++t) rc = oracle_step(p, f, g, fpost, gpost, force, ib);
     free(fpost);
     free(gpost);
     return rc;
@@ -614,6 +743,15 @@ int oracle_lattice(int kind, int *Q, int *c, double *w, double *M)
     for (int k = 0; k < L.Q; ++k)
         for (int q = 0; q < L.Q; ++q) M[k * L.Q + q] = L.M[k][q];
     return 0;
+}
+
+int oracle_ib_forces(const oracle_problem *p, const double *f, const double *g, double *Fib,
+                     double ib[6])
+{
+    ctx_t C;
+    int rc = make_ctx(p, &C);
+    if (rc) return rc;
+    return ib_forces(&C, f, g, Fib, ib);
 }
 
 int oracle_max_threads(void)

@@ -53,6 +53,15 @@ typedef struct {
     int x0, y0, z0;       /* window origin in the domain */
     int wx, wy, wz;       /* window extent */
     const unsigned char *solid;   /* wx*wy*wz flags, 1 = solid cell; NULL = no solid */
+    /* immersed boundary ("GPU Optimization for High-Quality Kinetic Fluid Simulation",
+     * Sec. 3.1, Eq. 6-8): ib_n samples at ib_x (3 per sample, domain coordinates, cell
+     * centres at integers) with boundary velocity ib_ub (3 per sample, NULL = 0) and weight
+     * ib_w (NULL = 1).  Each step: trilinear (bilinear in 2-D) interpolation of rho and
+     * u = (j + F_body/2)/rho at the samples from the pre-collision state, penalty
+     * g = w rho (u_b - u), spread with the same kernel into a per-cell force added to the
+     * body force of that step's collision. */
+    int ib_n;
+    const double *ib_x, *ib_ub, *ib_w;
 } oracle_problem;
 
 /* 0 on success, negative on a bad problem description. */
@@ -65,12 +74,20 @@ int oracle_init_equilibrium(const oracle_problem *p, const double *rho, const do
 
 /* One step.  f, g hold the state at t on entry and at t+1 on return.  fpost, gpost are
  * scratch buffers of the same size (post-collision values).  force[3] receives the
- * momentum exchanged with solid-mask cells during this step (may be NULL). */
+ * momentum exchanged with solid-mask cells during this step (may be NULL); ib[6] the
+ * immersed boundary's reaction force -sum g and its torque about the samples' centroid
+ * (may be NULL). */
 int oracle_step(const oracle_problem *p, double *f, double *g, double *fpost, double *gpost,
-                double force[3]);
+                double force[3], double ib[6]);
 
-/* steps repeated oracle_step calls; allocates its own scratch. force: last step's. */
-int oracle_run(const oracle_problem *p, double *f, double *g, int steps, double force[3]);
+/* steps repeated oracle_step calls; allocates its own scratch. force, ib: last step's. */
+int oracle_run(const oracle_problem *p, double *f, double *g, int steps, double force[3],
+               double ib[6]);
+
+/* The immersed-boundary force per cell (3 planes of W) the next step would add, and
+ * ib[6] as in oracle_step (for tests of the interpolation and spreading). */
+int oracle_ib_forces(const oracle_problem *p, const double *f, const double *g, double *Fib,
+                     double ib[6]);
 
 /* rho = sum f, u = (sum c f + F/2) / rho, T = sum g; solid cells read as 0. */
 int oracle_macroscopic(const oracle_problem *p, const double *f, const double *g, double *rho,
