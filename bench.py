@@ -74,7 +74,9 @@ def make_workload(name: str):
         "cavity3d_256": lambda: W.cavity3d(n=256),
         "taylor_green_32": lambda: W.taylor_green(),
         "channel_sphere_128": lambda: W.channel_sphere(),
+        "channel_ib_sphere_128": lambda: W.channel_ib_sphere(),
         "cavity2d_4096": lambda: W.cavity2d(),
+        "cavity2d_2048": lambda: W.cavity2d(n=2048),
         "cavity3d_512": lambda: W.cavity3d(),
     }
     return table[name]()
@@ -399,7 +401,8 @@ def run_gpu(args, dctx):
     }
     if not args.no_secondary:
         _WORKLOAD_CACHE[args.workload] = w
-        runs = [("cavity3d_512", "aa"), ("cavity2d_4096", "aa"), ("taylor_green_32", "aa")]
+        runs = [("cavity3d_512", "aa"), ("cavity2d_4096", "aa"), ("taylor_green_32", "aa"),
+                ("channel_ib_sphere_128", "aa")]
         # the streaming-layout page's comparison: in place vs two buffers
         for n in ("d3q19_mrt_periodic_128", "channel_sphere_128", args.workload):
             runs += [(n, "aa"), (n, "pull"), (n, "split")]

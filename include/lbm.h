@@ -114,6 +114,9 @@ typedef struct {
     const uint8_t *solid_mask; /* HOST pointer, nx*ny*nz bytes, x fastest, nonzero =
                                   solid; NULL = no solid cells.  Copied by lbm_create. */
     int streaming;        /* LBM_STREAM_AA (default 0), LBM_STREAM_PULL or LBM_STREAM_SPLIT */
+    int ib_max_samples;   /* capacity for immersed-boundary samples (0 = none); see
+                             lbm_set_ib_samples                                          */
+    int ib_block;         /* edge l (cells) of the blocks samples are ordered by; 0 = 4    */
 } lbm_config;
 
 /* Diagnostics of the current state (see lbm_diagnostics). */
@@ -128,6 +131,9 @@ typedef struct {
     long long fluid_cells;
     long long steps;      /* time steps taken since the last init / set                   */
     int finite;           /* 1 if every fluid rho (and T) is finite                        */
+    int ib_samples;       /* immersed-boundary samples in use                              */
+    double ib_force[3];   /* their reaction force -sum g_s in the last step               */
+    double ib_torque[3];  /* -sum (x_s - centroid) x g_s about the samples' centroid      */
 } lbm_diag;
 
 /* Bytes of device workspace lbm_create() needs for this configuration (validates it). */
@@ -174,6 +180,23 @@ lbm_status lbm_set_populations(lbm_ctx *ctx, const float *f, const float *g);
  * bit 19+k (k = 1..Q_T-1) = thermal link k ends on a DIRICHLET face, bit 31 = solid cell.
  * Device or page-locked host destination. */
 lbm_status lbm_get_link_mask(lbm_ctx *ctx, uint32_t *mask);
+
+/* Immersed boundary ([KFS] Sec. 3.1, Eq. 6-8; sample order of its Sec. 4, Fig. 7).
+ * Replace the solid samples: n <= cfg.ib_max_samples points xyz (HOST, 3n floats, cell
+ * units: cell centres at integer coordinates), boundary velocities ub (HOST, 3n, NULL = 0)
+ * and weights (HOST, n, NULL = 1).  Each later step, before the collision, interpolates
+ * rho and u = (j + F_body/2)/rho at every sample from its 2x2x2 (2x2 in 2-D) stencil with
+ * the trilinear kernel (Eq. 6), forms the penalty g = w rho (u_b - u) (Eq. 7) and
+ * scatters it with the same kernel (Eq. 8, one thread per sample, atomic additions) into
+ * a per-cell force added to that step's collision.  Solid stencil cells count as rho = 1,
+ * u = 0 and take no force.  Positions on periodic axes are wrapped into the domain; on
+ * wall axes they must satisfy 0 <= x < n - 1 so that the stencil stays inside
+ * (LBM_ERR_ARG otherwise).  Samples are stored sorted by l x l x l block (x fastest) and
+ * by Morton code inside a block, so that one warp's samples touch nearby cells.  n = 0
+ * removes the boundary.  Enqueued on the context's stream; the host arrays may be freed on
+ * return. */
+lbm_status lbm_set_ib_samples(lbm_ctx *ctx, int n, const float *xyz, const float *ub,
+                              const float *weight);
 
 /* Enqueue later work on another stream (a cudaStream_t). */
 lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);

@@ -42,7 +42,8 @@ class lbm_config(ctypes.Structure):
         ("gbeta", ctypes.c_double), ("T0", ctypes.c_double), ("up_axis", ctypes.c_int),
         ("face_flow", ctypes.c_int * 6), ("face_T", ctypes.c_int * 6),
         ("T_wall", ctypes.c_double * 6), ("solid_mask", ctypes.POINTER(ctypes.c_uint8)),
-        ("streaming", ctypes.c_int),
+        ("streaming", ctypes.c_int), ("ib_max_samples", ctypes.c_int),
+        ("ib_block", ctypes.c_int),
     ]
 
 
@@ -52,7 +53,8 @@ class lbm_diag(ctypes.Structure):
         ("force", ctypes.c_double * 3), ("heat", ctypes.c_double * 6),
         ("nu_hot", ctypes.c_double), ("nu_cold", ctypes.c_double),
         ("fluid_cells", ctypes.c_longlong), ("steps", ctypes.c_longlong),
-        ("finite", ctypes.c_int),
+        ("finite", ctypes.c_int), ("ib_samples", ctypes.c_int),
+        ("ib_force", ctypes.c_double * 3), ("ib_torque", ctypes.c_double * 3),
     ]
 
 
@@ -71,6 +73,7 @@ SIGNATURES = [
     ("lbm_get_populations", ctypes.c_int, [_VP, _VP, _VP]),
     ("lbm_set_populations", ctypes.c_int, [_VP, _VP, _VP]),
     ("lbm_get_link_mask", ctypes.c_int, [_VP, _VP]),
+    ("lbm_set_ib_samples", ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP, _VP]),
     ("lbm_set_stream", ctypes.c_int, [_VP, _VP]),
     ("lbm_reduce_populations_static", ctypes.c_int,
      [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP,
@@ -180,7 +183,8 @@ def lbm_diagnostics(ctx, allow_nonfinite: bool = False) -> dict:
     return {"mass": d.mass, "momentum": list(d.momentum), "force": list(d.force),
             "heat": list(d.heat), "nu_hot": d.nu_hot, "nu_cold": d.nu_cold,
             "fluid_cells": d.fluid_cells, "steps": d.steps, "finite": bool(d.finite),
-            "status": st}
+            "ib_samples": d.ib_samples, "ib_force": list(d.ib_force),
+            "ib_torque": list(d.ib_torque), "status": st}
 
 
 def lbm_get_populations(ctx, f, g=None):
@@ -193,6 +197,17 @@ def lbm_set_populations(ctx, f, g=None):
 
 def lbm_get_link_mask(ctx, mask):
     _check(load().lbm_get_link_mask(ctx, _addr(mask)), ctx)
+
+
+def lbm_set_ib_samples(ctx, xyz, ub=None, weight=None):
+    """Immersed-boundary samples from host arrays: xyz (n, 3), ub (n, 3), weight (n,)."""
+    import numpy as np
+    x = np.ascontiguousarray(xyz, dtype=np.float32).reshape(-1, 3)
+    n = x.shape[0]
+    u = None if ub is None else np.ascontiguousarray(ub, dtype=np.float32).reshape(n, 3)
+    w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float32).reshape(n)
+    ptr = lambda a: None if a is None else a.ctypes.data
+    _check(load().lbm_set_ib_samples(ctx, n, ptr(x), ptr(u), ptr(w)), ctx)
 
 
 def lbm_set_stream(ctx, stream):

@@ -59,6 +59,37 @@ cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t
         });
 }
 
+cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s)
+{
+    if (P.ib_n <= 0) return cudaSuccess;
+    const int corners = lattice == 19 ? 8 : 4;
+    const long long threads = (long long)P.ib_n * corners;
+    const dim3 b(128), g((unsigned)((threads + 127) / 128));
+    auto go = [&](auto l, auto tl) {
+        using L = decltype(l);
+        using TL = decltype(tl);
+        if (pat == AA_ODD) ib_kernel<L, TL, AA_ODD><<<g, b, 0, s>>>(P);
+        else if (pat == PULL) ib_kernel<L, TL, PULL><<<g, b, 0, s>>>(P);
+        else ib_kernel<L, TL, NATURAL><<<g, b, 0, s>>>(P);
+        return cudaGetLastError();
+    };
+    return by_lattice(
+        lattice, thermal, [&](auto tl) { return go(D3Q19{}, tl); },
+        [&](auto tl) { return go(D2Q9{}, tl); });
+}
+
+cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
+                           cudaStream_t s)
+{
+    ib_clear_kernel<<<1024, 256, 0, s>>>(mask, cells);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || P.ib_n <= 0) return e;
+    const dim3 b(128), g((P.ib_n + 127) / 128);
+    if (lattice == 19) ib_mark_kernel<D3Q19><<<g, b, 0, s>>>(P, mask);
+    else ib_mark_kernel<D2Q9><<<g, b, 0, s>>>(P, mask);
+    return cudaGetLastError();
+}
+
 namespace {
 // Call fn with compile-time (MASKED, PAT).
 template <class Fn>

@@ -6,6 +6,8 @@
 #include <new>
 #include <string>
 #include <utility>
+#include <algorithm>
+#include <vector>
 
 #include "../../include/lbm.h"
 #include "lbm_internal.h"
@@ -53,10 +55,17 @@ struct lbm_ctx {
     cudaGraphExec_t graph[2] = {nullptr, nullptr};
     cudaStream_t capture_stream = nullptr;
     bool graphs_disabled = false;
-    ~lbm_ctx()
+    // immersed-boundary samples as stored on the device (sorted), for the torque
+    std::vector<float> ib_x;
+    void drop_graphs()
     {
         for (auto &g : graph)
             if (g) cudaGraphExecDestroy(g);
+        graph[0] = graph[1] = nullptr;
+    }
+    ~lbm_ctx()
+    {
+        drop_graphs();
         if (capture_stream) cudaStreamDestroy(capture_stream);
     }
 };
@@ -170,6 +179,14 @@ lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace
     c->partial = reinterpret_cast<double *>(c->ws + L.off_partial);
     c->result = reinterpret_cast<double *>(c->ws + L.off_result);
     lbm_setup::fill_params(c->cfg, c->L, c->ws, c->P);
+    if (L.ib_cap > 0) {
+        e = cudaMemsetAsync(c->P.fib, 0, 3 * L.S * sizeof(float), c->stream);
+        if (e != cudaSuccess) {
+            lbm_status r = cuda_fail(nullptr, e, "clearing the immersed-boundary force");
+            delete c;
+            return r;
+        }
+    }
     if (L.masked) {
         uint8_t *solid = nullptr;
         if (L.has_solid) {
@@ -209,7 +226,9 @@ lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, co
     // PULL stores a post-collision state read with the pull pattern.  Parity 0 always
     // means the first population buffer is current (the step graphs rely on it).
     c->parity = 0;
+    const int ib_n = c->P.ib_n;
     lbm_setup::fill_params(c->cfg, c->L, c->ws, c->P);
+    c->P.ib_n = ib_n;
     const int pat = (c->L.streaming == LBM_STREAM_PULL) ? lbm::PULL : lbm::NATURAL;
     cudaError_t e = lbm::launch_init(c->cfg.lattice, c->cfg.thermal, pat, c->P,
                                      (const float *)dr, (const float *)du, (const float *)dT,
@@ -234,8 +253,16 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
     const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
     const bool d3 = c->cfg.lattice == LBM_D3Q19;
     const int th = c->cfg.thermal, coll = c->cfg.collision;
-    const bool masked = c->L.masked;
+    const int masked = !c->L.masked ? 0 : (c->L.ib_cap > 0 ? 2 : 1);
     cudaError_t e;
+    if (P.ib_n > 0) {
+        const int pat = c->L.streaming == LBM_STREAM_PULL    ? lbm::PULL
+                        : c->L.streaming == LBM_STREAM_SPLIT ? lbm::NATURAL
+                        : parity                             ? lbm::AA_ODD
+                                                             : lbm::NATURAL;
+        e = lbm::launch_ib(c->cfg.lattice, th, pat, P, stream);
+        if (e != cudaSuccess) return e;
+    }
     switch (c->L.streaming) {
     case LBM_STREAM_PULL:
         e = d3 ? lbm::launch_pull_d3q19(th, coll, masked, narrow, P, sh, stream)
@@ -376,6 +403,29 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
         out->nu_hot = nusselt(hot);
         out->nu_cold = nusselt(cold);
     }
+    out->ib_samples = c->P.ib_n;
+    if (c->P.ib_n > 0) {
+        // reaction force and torque of the last step's penalties (fp64 on the host)
+        const int n = c->P.ib_n;
+        const size_t cap = c->L.ib_cap;
+        std::vector<float> gs(3 * cap);
+        e = cudaMemcpyAsync(gs.data(), c->P.ibg, sizeof(float) * gs.size(),
+                            cudaMemcpyDeviceToHost, c->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+        if (e != cudaSuccess) return cuda_fail(c, e, "immersed-boundary read-back");
+        double centre[3] = {0, 0, 0};
+        for (int s = 0; s < n; ++s)
+            for (int a = 0; a < 3; ++a) centre[a] += (double)c->ib_x[3 * s + a] / n;
+        for (int s = 0; s < n; ++s) {
+            const double g[3] = {gs[s], gs[cap + s], gs[2 * cap + s]};
+            const double r[3] = {c->ib_x[3 * s] - centre[0], c->ib_x[3 * s + 1] - centre[1],
+                                 c->ib_x[3 * s + 2] - centre[2]};
+            for (int a = 0; a < 3; ++a) out->ib_force[a] -= g[a];
+            out->ib_torque[0] -= r[1] * g[2] - r[2] * g[1];
+            out->ib_torque[1] -= r[2] * g[0] - r[0] * g[2];
+            out->ib_torque[2] -= r[0] * g[1] - r[1] * g[0];
+        }
+    }
     if (!out->finite) return fail(c, LBM_ERR_NONFINITE, "non-finite rho or T in the state");
     return LBM_OK;
 }
@@ -437,6 +487,91 @@ lbm_status lbm_get_link_mask(lbm_ctx *c, uint32_t *mask)
     else
         e = cudaMemsetAsync(dm, 0, sizeof(uint32_t) * (size_t)c->L.N, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "mask copy");
+    return LBM_OK;
+}
+
+namespace {
+
+// Spread the low 10 bits of v to every third bit (Morton interleave).
+uint32_t spread3(uint32_t v)
+{
+    v &= 0x3ffu;
+    v = (v | (v << 16)) & 0x030000ffu;
+    v = (v | (v << 8)) & 0x0300f00fu;
+    v = (v | (v << 4)) & 0x030c30c3u;
+    v = (v | (v << 2)) & 0x09249249u;
+    return v;
+}
+
+}  // namespace
+
+lbm_status lbm_set_ib_samples(lbm_ctx *c, int n, const float *xyz, const float *ub,
+                              const float *weight)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (c->L.ib_cap <= 0) return fail(c, LBM_ERR_STATE, "created with ib_max_samples = 0");
+    if (n < 0 || n > c->L.ib_cap)
+        return fail(c, LBM_ERR_ARG, "n must lie in [0, ib_max_samples]");
+    if (n > 0 && !xyz) return fail(c, LBM_ERR_ARG, "xyz is required");
+    DeviceGuard guard(c->device);
+    const int dim = c->L.dim;
+    const int ext[3] = {c->cfg.nx, c->cfg.ny, c->cfg.nz};
+    const int l = c->cfg.ib_block > 0 ? c->cfg.ib_block : 4;
+    // positions: wrap periodic axes, check wall axes
+    std::vector<float> x(3 * (size_t)n);
+    for (int s = 0; s < n; ++s)
+        for (int a = 0; a < 3; ++a) {
+            float v = (a < dim) ? xyz[3 * s + a] : 0.0f;
+            if (!std::isfinite(v)) return fail(c, LBM_ERR_ARG, "non-finite sample position");
+            if (a < dim && !c->P.face_wall[2 * a]) {
+                v = std::fmod(v, (float)ext[a]);
+                if (v < 0.0f) v += (float)ext[a];
+                if (v >= (float)ext[a]) v = 0.0f;
+            } else if (a < dim && !(v >= 0.0f && v < (float)(ext[a] - 1))) {
+                return fail(c, LBM_ERR_ARG,
+                            "sample " + std::to_string(s) +
+                                ": its stencil would leave the domain through a wall face");
+            }
+            x[3 * s + a] = v;
+        }
+    // order: l x l x l blocks in x-y-z order, Morton code of the position inside a block
+    const long long nbx = (ext[0] + l - 1) / l, nby = (ext[1] + l - 1) / l;
+    std::vector<std::pair<unsigned long long, int>> key(n);
+    for (int s = 0; s < n; ++s) {
+        long long b[3] = {0, 0, 0};
+        uint32_t m = 0;
+        for (int a = 0; a < dim; ++a) {
+            const float v = x[3 * s + a];
+            b[a] = (long long)(v / l);
+            const float in = v - (float)(b[a] * l);
+            m |= spread3((uint32_t)std::min(1023.0f, in * (1024.0f / l))) << a;
+        }
+        const unsigned long long block = b[0] + nbx * (b[1] + nby * b[2]);
+        key[s] = {(block << 30) | m, s};
+    }
+    std::stable_sort(key.begin(), key.end());
+    const size_t cap = c->L.ib_cap;
+    std::vector<float> host(10 * cap, 0.0f);   // planes: x, y, z, ub x3, w, g x3
+    c->ib_x.assign(3 * (size_t)n, 0.0f);
+    for (int i = 0; i < n; ++i) {
+        const int s = key[i].second;
+        for (int a = 0; a < 3; ++a) {
+            host[a * cap + i] = x[3 * s + a];
+            host[(3 + a) * cap + i] = (ub && a < dim) ? ub[3 * s + a] : 0.0f;
+            c->ib_x[3 * i + a] = x[3 * s + a];
+        }
+        host[6 * cap + i] = weight ? weight[s] : 1.0f;
+    }
+    cudaError_t e = cudaMemcpyAsync(const_cast<float *>(c->P.ibx), host.data(),
+                                    sizeof(float) * host.size(), cudaMemcpyHostToDevice,
+                                    c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);   // host buffer lifetime
+    if (e != cudaSuccess) return cuda_fail(c, e, "copy of the samples");
+    c->P.ib_n = n;
+    c->drop_graphs();   // captured steps hold the sample count
+    e = lbm::launch_ib_mark(c->cfg.lattice, c->P, const_cast<uint32_t *>(c->P.mask), c->L.N,
+                            c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "marking the samples' stencils");
     return LBM_OK;
 }
 

@@ -39,15 +39,21 @@ struct CollideParams {
     int up_axis;
 };
 
-// Body force and force-shifted velocity ([TLBM] Sec. 2).
+// Body force and force-shifted velocity ([TLBM] Sec. 2).  ext: an additional force on the
+// cell (the immersed boundary's), or null.
 template <bool THERMAL>
 LBM_HD void force_velocity(const CollideParams &P, float rho, float T, float jx, float jy,
                            float jz, float &Fx, float &Fy, float &Fz, float &ux, float &uy,
-                           float &uz)
+                           float &uz, const float *ext = nullptr)
 {
     Fx = rho * P.gx;
     Fy = rho * P.gy;
     Fz = rho * P.gz;
+    if (ext) {
+        Fx += ext[0];
+        Fy += ext[1];
+        Fz += ext[2];
+    }
     if (THERMAL) {
         const float b = rho * P.gbeta * (T - P.T0);
         if (P.up_axis == 0) Fx += b;
@@ -130,7 +136,8 @@ LBM_HD void d2q5_equilibrium(float (&g)[5], float a_T, float T, float ux, float 
 // cy^2-cz^2, 12 piww = (3c^2-5)(cy^2-cz^2), 13 pxy, 14 pyz, 15 pxz, 16-18 m.
 // Norms 19, 2394, 252, 10, 40, 10, 40, 10, 40, 36, 72, 12, 24, 4, 4, 4, 8, 8, 8.
 template <bool THERMAL, class TL>
-LBM_HD void collide_d3q19_mrt(float (&f)[19], float (&g)[TL::QA], const CollideParams &P)
+LBM_HD void collide_d3q19_mrt(float (&f)[19], float (&g)[TL::QA], const CollideParams &P,
+                              const float *ext)
 {
     // sums and differences of opposite pairs
     const float sx = f[1] + f[2], dx = f[1] - f[2];
@@ -157,7 +164,7 @@ LBM_HD void collide_d3q19_mrt(float (&f)[19], float (&g)[TL::QA], const CollideP
     }
     const float rho = 1.0f + drho;
     float Fx, Fy, Fz, ux, uy, uz;
-    force_velocity<THERMAL>(P, rho, T, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz);
+    force_velocity<THERMAL>(P, rho, T, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz, ext);
 
     // non-conserved moments of fbar
     const float m1 = -30.0f * f[0] - 11.0f * A + 8.0f * E;
@@ -238,7 +245,8 @@ LBM_HD void collide_d3q19_mrt(float (&f)[19], float (&g)[TL::QA], const CollideP
 // Lallemand-Luo basis: 0 rho, 1 e = 3c^2-4, 2 eps = (9c^4-21c^2+8)/2, 3 jx, 4 qx =
 // (3c^2-5)cx, 5 jy, 6 qy, 7 pxx = cx^2-cy^2, 8 pxy.  Norms 9, 36, 36, 6, 12, 6, 12, 4, 4.
 template <bool THERMAL, class TL>
-LBM_HD void collide_d2q9_mrt(float (&f)[9], float (&g)[TL::QA], const CollideParams &P)
+LBM_HD void collide_d2q9_mrt(float (&f)[9], float (&g)[TL::QA], const CollideParams &P,
+                             const float *ext)
 {
     const float sx = f[1] + f[3], dx = f[1] - f[3];
     const float sy = f[2] + f[4], dy = f[2] - f[4];
@@ -254,7 +262,7 @@ LBM_HD void collide_d2q9_mrt(float (&f)[9], float (&g)[TL::QA], const CollidePar
     }
     const float rho = 1.0f + drho;
     float Fx, Fy, Fz, ux, uy, uz;
-    force_velocity<THERMAL>(P, rho, T, jx, jy, 0.0f, Fx, Fy, Fz, ux, uy, uz);
+    force_velocity<THERMAL>(P, rho, T, jx, jy, 0.0f, Fx, Fy, Fz, ux, uy, uz, ext);
 
     const float m1 = -4.0f * f[0] - A + 2.0f * Dg;
     const float m2 = 4.0f * f[0] - 2.0f * A + Dg;
@@ -293,7 +301,8 @@ LBM_HD void collide_d2q9_mrt(float (&f)[9], float (&g)[TL::QA], const CollidePar
 // ------------------------------------------------------------------------ BGK ---------
 
 template <class L, bool THERMAL, class TL>
-LBM_HD void collide_bgk(float (&f)[L::Q], float (&g)[TL::QA], const CollideParams &P)
+LBM_HD void collide_bgk(float (&f)[L::Q], float (&g)[TL::QA], const CollideParams &P,
+                        const float *ext)
 {
     float drho = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f;
 #pragma unroll
@@ -310,7 +319,7 @@ LBM_HD void collide_bgk(float (&f)[L::Q], float (&g)[TL::QA], const CollideParam
     }
     const float rho = 1.0f + drho;
     float Fx, Fy, Fz, ux, uy, uz;
-    force_velocity<THERMAL>(P, rho, T, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz);
+    force_velocity<THERMAL>(P, rho, T, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz, ext);
     const float u15 = 1.5f * (ux * ux + uy * uy + uz * uz);
     const float uF3 = 3.0f * (ux * Fx + uy * Fy + uz * Fz);
 #pragma unroll
@@ -327,17 +336,18 @@ LBM_HD void collide_bgk(float (&f)[L::Q], float (&g)[TL::QA], const CollideParam
     }
 }
 
-// Dispatch on the collision model.
+// Dispatch on the collision model.  ext: additional force on the cell, or null.
 template <class L, class TL, int COLL>
-LBM_HD void collide(float (&f)[L::Q], float (&g)[TL::QA], const CollideParams &P)
+LBM_HD void collide(float (&f)[L::Q], float (&g)[TL::QA], const CollideParams &P,
+                    const float *ext = nullptr)
 {
     constexpr bool TH = TL::Q > 0;
     if (COLL == 0) {
-        collide_bgk<L, TH, TL>(f, g, P);
+        collide_bgk<L, TH, TL>(f, g, P, ext);
     } else if constexpr (L::Q == 19) {
-        collide_d3q19_mrt<TH, TL>(f, g, P);
+        collide_d3q19_mrt<TH, TL>(f, g, P, ext);
     } else {
-        collide_d2q9_mrt<TH, TL>(f, g, P);
+        collide_d2q9_mrt<TH, TL>(f, g, P, ext);
     }
 }
 

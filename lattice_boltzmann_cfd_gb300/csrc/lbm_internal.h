@@ -27,20 +27,21 @@ inline Shape cell_shape(int nx, int ny, int nz, int threads = 256)
 constexpr int DIAG_BLOCKS = 1024;
 
 // Each returns the launch error (cudaGetLastError) of what it enqueued.
-// narrow: every population index fits in 32 bits (see slot()).
-cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, bool narrow,
+// narrow: every population index fits in 32 bits (see slot()).  masked: 0 = no link
+// mask, 1 = link mask, 2 = link mask and immersed-boundary forces.
+cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
                               const Params &P, const Shape &sh, cudaStream_t s);
-cudaError_t launch_step_d2q9(int thermal, int coll, bool masked, bool odd, bool narrow,
+cudaError_t launch_step_d2q9(int thermal, int coll, int masked, bool odd, bool narrow,
                              const Params &P, const Shape &sh, cudaStream_t s);
 // Two-buffer modes: one PULL step, or one SPLIT step (collide + stream), from P.f/P.g
 // into P.fo/P.go.
-cudaError_t launch_pull_d3q19(int thermal, int coll, bool masked, bool narrow, const Params &P,
+cudaError_t launch_pull_d3q19(int thermal, int coll, int masked, bool narrow, const Params &P,
                               const Shape &sh, cudaStream_t s);
-cudaError_t launch_pull_d2q9(int thermal, int coll, bool masked, bool narrow, const Params &P,
+cudaError_t launch_pull_d2q9(int thermal, int coll, int masked, bool narrow, const Params &P,
                              const Shape &sh, cudaStream_t s);
-cudaError_t launch_split_d3q19(int thermal, int coll, bool masked, bool narrow, const Params &P,
+cudaError_t launch_split_d3q19(int thermal, int coll, int masked, bool narrow, const Params &P,
                                const Shape &sh, cudaStream_t s);
-cudaError_t launch_split_d2q9(int thermal, int coll, bool masked, bool narrow, const Params &P,
+cudaError_t launch_split_d2q9(int thermal, int coll, int masked, bool narrow, const Params &P,
                               const Shape &sh, cudaStream_t s);
 // pat: read pattern of the logical state (NATURAL, AA_ODD or PULL).
 cudaError_t launch_init(int lattice, int thermal, int pat, const Params &P, const float *rho,
@@ -51,6 +52,11 @@ cudaError_t launch_macro(int lattice, int thermal, bool masked, int pat, const P
                          float *rho, float *u, float *T, cudaStream_t s);
 cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
                        const Params &P, float *f, float *g, cudaStream_t s);
+// Immersed boundary: penalty + spreading for every sample (read pattern pat), and the
+// IB_BIT marking of the samples' stencil cells.
+cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s);
+cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
+                           cudaStream_t s);
 cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s);
 

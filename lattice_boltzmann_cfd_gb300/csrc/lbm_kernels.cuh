@@ -47,6 +47,12 @@ struct Params {
     int face_wall[6];      // per face: 1 = wall (flow)
     int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
     float T_wall[6];
+    // immersed boundary: per-cell force (3 planes of S, consumed and zeroed by the step),
+    // samples as planes of ib_cap: position (3), boundary velocity (3), weight, penalty (3)
+    float *fib;
+    const float *ibx, *ibub, *ibw;
+    float *ibg;
+    int ib_n, ib_cap;
 };
 
 // Neighbour offsets with periodic wrap by compare and add.
@@ -256,9 +262,22 @@ LBM_HD void store_logical(const Params &P, int idx, const Offs &o, uint32_t m,
 // ------------------------------------------------------------------ the step ----------
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
+// Read the immersed-boundary force of a cell and zero it for the next step.
+LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
+{
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        float *p = P.fib + ((size_t)a * P.S + (unsigned)idx);
+        ext[a] = *p;
+        *p = 0.0f;
+    }
+}
+
 // One AA step of cell (x, y, z): loads through Pr, stores through Pw (the same buffer in
 // the kernel; a separate one in the host emulation of the tests).
-template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW>
+// IB: the context has immersed-boundary samples (cells with IB_BIT take a per-cell force);
+// kernels without it carry no trace of that path.
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB = false>
 LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
 {
     const int idx = x + Pr.nx * (y + Pr.ny * z);
@@ -271,11 +290,19 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
         if (ODD) o = make_offs(x, y, z, Pr);
         load_cell<L, TL, false, ODD ? AA_ODD : NATURAL, NARROW>(Pr, idx, o, 0u, f, g);
     }
+    float ext[3];
     if (MASKED) {
         if (m & SOLID_BIT) return;
         if (ODD && (m & wall_bits<L>())) fix_wall_loads<L, TL, AA_ODD, NARROW>(Pr, idx, m, f, g);
     }
-    collide<L, TL, COLL>(f, g, Pr.c);
+    if constexpr (IB) {
+        const bool forced = m & IB_BIT;
+        if (forced) take_ib_force(Pr, idx, ext);
+        collide<L, TL, COLL>(f, g, Pr.c, forced ? ext : nullptr);
+    } else {
+        (void)ext;
+        collide<L, TL, COLL>(f, g, Pr.c);
+    }
     // Recompute the store addresses after the collision instead of keeping the load-time
     // values live through it (the empty asm hides that they are the same).
     int xs = x, ys = y, zs = z, is = idx;
@@ -287,19 +314,19 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
 }
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
-template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW>
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
     if (x >= P.nx || y >= P.ny) return;
-    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW>(P, P, x, y, z);
+    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB>(P, P, x, y, z);
 }
 
 // Two-buffer PULL step: pull from the current buffer, collide, write the other buffer's
 // natural slots.  No slot is read and written in the same launch.
-template <class L, class TL, int COLL, bool MASKED, bool NARROW>
+template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB = false>
 LBM_HD void pull_step_cell(const Params &P, float *Wf, float *Wg, int x, int y, int z)
 {
     const int idx = x + P.nx * (y + P.ny * z);
@@ -309,51 +336,68 @@ LBM_HD void pull_step_cell(const Params &P, float *Wf, float *Wg, int x, int y, 
         const Offs o = make_offs(x, y, z, P);
         load_cell<L, TL, false, PULL, NARROW>(P, idx, o, 0u, f, g);
     }
+    float ext[3];
     if (MASKED) {
         if (m & SOLID_BIT) return;
         if (m & wall_bits<L>()) fix_wall_loads<L, TL, PULL, NARROW>(P, idx, m, f, g);
     }
-    collide<L, TL, COLL>(f, g, P.c);
+    if constexpr (IB) {
+        const bool forced = m & IB_BIT;
+        if (forced) take_ib_force(P, idx, ext);
+        collide<L, TL, COLL>(f, g, P.c, forced ? ext : nullptr);
+    } else {
+        (void)ext;
+        collide<L, TL, COLL>(f, g, P.c);
+    }
     int is = idx;
     asm volatile("" : "+r"(is));
     store_natural<L, TL, NARROW>(P, Wf, Wg, is, f, g);
 }
 
-template <class L, class TL, int COLL, bool MASKED, bool NARROW>
+template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB>
 __global__ void __launch_bounds__(256) pull_kernel(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
     if (x >= P.nx || y >= P.ny) return;
-    pull_step_cell<L, TL, COLL, MASKED, NARROW>(P, P.fo, P.go, x, y, z);
+    pull_step_cell<L, TL, COLL, MASKED, NARROW, IB>(P, P.fo, P.go, x, y, z);
 }
 
-// SPLIT mode, pass 1: collide in place in the natural slots.
-template <class L, class TL, int COLL, bool MASKED, bool NARROW>
+// SPLIT mode, pass 1: collide cell idx in place in the natural slots.
+template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB = false>
+LBM_HD void collide_in_place_cell(const Params &P, int idx)
+{
+    const uint32_t m = MASKED ? P.mask[idx] : 0u;
+    if (m & SOLID_BIT) return;
+    float f[L::Q], g[TL::QA], ext[3];
+    const Offs o{};
+    load_cell<L, TL, false, NATURAL, NARROW>(P, idx, o, 0u, f, g);
+    if constexpr (IB) {
+        const bool forced = m & IB_BIT;
+        if (forced) take_ib_force(P, idx, ext);
+        collide<L, TL, COLL>(f, g, P.c, forced ? ext : nullptr);
+    } else {
+        (void)ext;
+        collide<L, TL, COLL>(f, g, P.c);
+    }
+    store_natural<L, TL, NARROW>(P, P.f, P.g, idx, f, g);
+}
+
+template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB>
 __global__ void __launch_bounds__(256) collide_kernel(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
     if (x >= P.nx || y >= P.ny) return;
-    const int idx = x + P.nx * (y + P.ny * z);
-    if (MASKED && (P.mask[idx] & SOLID_BIT)) return;
-    float f[L::Q], g[TL::QA];
-    const Offs o{};
-    load_cell<L, TL, false, NATURAL, NARROW>(P, idx, o, 0u, f, g);
-    collide<L, TL, COLL>(f, g, P.c);
-    store_natural<L, TL, NARROW>(P, P.f, P.g, idx, f, g);
+    collide_in_place_cell<L, TL, COLL, MASKED, NARROW, IB>(P, x + P.nx * (y + P.ny * z));
 }
 
-// SPLIT mode, pass 2: pull the post-collision populations into the other buffer.
+// SPLIT mode, pass 2: pull the post-collision populations of cell (x, y, z) into W.
 template <class L, class TL, bool MASKED, bool NARROW>
-__global__ void __launch_bounds__(256) stream_kernel(const Params P)
+LBM_HD void stream_cell(const Params &P, float *Wf, float *Wg, int x, int y, int z)
 {
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
-    if (x >= P.nx || y >= P.ny) return;
     const int idx = x + P.nx * (y + P.ny * z);
     uint32_t m = 0;
     if (MASKED) {
@@ -363,7 +407,153 @@ __global__ void __launch_bounds__(256) stream_kernel(const Params P)
     float f[L::Q], g[TL::QA];
     const Offs o = make_offs(x, y, z, P);
     load_cell<L, TL, MASKED, PULL, NARROW>(P, idx, o, m, f, g);
-    store_natural<L, TL, NARROW>(P, P.fo, P.go, idx, f, g);
+    store_natural<L, TL, NARROW>(P, Wf, Wg, idx, f, g);
+}
+
+template <class L, class TL, bool MASKED, bool NARROW>
+__global__ void __launch_bounds__(256) stream_kernel(const Params P)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    stream_cell<L, TL, MASKED, NARROW>(P, P.fo, P.go, x, y, z);
+}
+
+// -------------------------------------------------------------- immersed boundary -----
+
+// Immersed boundary ("GPU Optimization for High-Quality Kinetic Fluid Simulation", Sec. 3.1,
+// Eq. 6-8).  Corner c (0 .. 2^dim - 1) of sample s's stencil: its cell, its trilinear weight
+// K, and K rho, K u with rho and u = (j + F_body/2)/rho of the logical state (read with
+// pattern PAT).  A solid stencil cell counts as rho = 1, u = 0.  Sample positions were
+// checked on the host: stencils never leave through a wall face.
+template <class L, class TL, int PAT>
+LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float (&Ku)[3])
+{
+    const int dim = L::DIM;
+    const int n[3] = {P.nx, P.ny, P.nz};
+    int q[3] = {0, 0, 0};
+    float k = 1.0f;
+    for (int a = 0; a < dim; ++a) {
+        const float xa = P.ibx[a * P.ib_cap + s];
+        const int base = (int)floorf(xa);
+        const float fr = xa - (float)base;
+        const int d = (c >> a) & 1;
+        q[a] = base + d;
+        if (q[a] >= n[a]) q[a] -= n[a];
+        k *= d ? fr : 1.0f - fr;
+    }
+    const int idx = q[0] + P.nx * (q[1] + P.ny * q[2]);
+    K = k;
+    const uint32_t m = P.mask ? P.mask[idx] : 0u;
+    if (m & SOLID_BIT) {
+        Krho = k;
+        Ku[0] = Ku[1] = Ku[2] = 0.0f;
+        return idx;
+    }
+    Offs o{};
+    if (PAT != NATURAL) o = make_offs(q[0], q[1], q[2], P);
+    float f[L::Q], g[TL::QA];
+    load_cell<L, TL, true, PAT>(P, idx, o, m, f, g);
+    float dr = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f, t = 0.0f;
+    for (int i = 0; i < L::Q; ++i) {
+        dr += f[i];
+        jx += L::cx(i) * f[i];
+        jy += L::cy(i) * f[i];
+        jz += L::cz(i) * f[i];
+    }
+    if constexpr (TL::Q > 0) {
+        for (int i = 0; i < TL::Q; ++i) t += g[i];
+    }
+    const float r = 1.0f + dr;
+    float Fx, Fy, Fz, ux, uy, uz;
+    force_velocity<(TL::Q > 0)>(P.c, r, t, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz);
+    Krho = k * r;
+    Ku[0] = k * ux;
+    Ku[1] = k * uy;
+    Ku[2] = k * uz;
+    return idx;
+}
+
+// Penalty of sample s from its interpolated rho and u: g = w rho (u_b - u).
+template <class L>
+LBM_HD void ib_penalty(const Params &P, int s, float rho, const float (&u)[3], float (&gs)[3])
+{
+    const float w = P.ibw[s];
+    for (int a = 0; a < 3; ++a)
+        gs[a] = (a < L::DIM) ? w * rho * (P.ibub[a * P.ib_cap + s] - u[a]) : 0.0f;
+}
+
+// Whole sample s, corner by corner (the host emulation's form of the kernel below).
+template <class L, class TL, int PAT>
+LBM_HD int ib_sample(const Params &P, int s, int (&node)[8], float (&K)[8], float (&gs)[3])
+{
+    const int corners = 1 << L::DIM;
+    float rho = 0.0f, u[3] = {0.0f, 0.0f, 0.0f};
+    for (int c = 0; c < corners; ++c) {
+        float kr, ku[3];
+        node[c] = ib_corner<L, TL, PAT>(P, s, c, K[c], kr, ku);
+        rho += kr;
+        for (int a = 0; a < 3; ++a) u[a] += ku[a];
+    }
+    ib_penalty<L>(P, s, rho, u, gs);
+    return corners;
+}
+
+// One thread per stencil corner (2^dim threads per sample, adjacent lanes): each loads its
+// cell, the group sums K rho and K u with shuffles, every thread forms the penalty and
+// spreads its share K g into its cell with atomic additions (cells are shared between
+// samples); corner 0 keeps the penalty for the diagnostics.
+template <class L, class TL, int PAT>
+__global__ void __launch_bounds__(128) ib_kernel(const Params P)
+{
+    constexpr int CORNERS = 1 << L::DIM;
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const int s = t / CORNERS, c = t % CORNERS;
+    const bool active = s < P.ib_n;
+    float K = 0.0f, kr = 0.0f, ku[3] = {0.0f, 0.0f, 0.0f};
+    int idx = 0;
+    if (active) idx = ib_corner<L, TL, PAT>(P, s, c, K, kr, ku);
+#pragma unroll
+    for (int off = 1; off < CORNERS; off <<= 1) {
+        kr += __shfl_xor_sync(0xffffffffu, kr, off, CORNERS);
+        for (int a = 0; a < 3; ++a) ku[a] += __shfl_xor_sync(0xffffffffu, ku[a], off, CORNERS);
+    }
+    if (!active) return;
+    float gs[3];
+    ib_penalty<L>(P, s, kr, ku, gs);
+    if (c == 0)
+        for (int a = 0; a < 3; ++a) P.ibg[a * P.ib_cap + s] = gs[a];
+    if (P.mask[idx] & SOLID_BIT) return;
+    for (int a = 0; a < L::DIM; ++a)
+        atomicAdd(P.fib + ((size_t)a * P.S + (unsigned)idx), K * gs[a]);
+}
+
+// Mark the stencil cells of every sample with IB_BIT (after ib_clear_kernel).
+template <class L>
+__global__ void ib_mark_kernel(const Params P, uint32_t *mask)
+{
+    const int s = blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= P.ib_n) return;
+    const int dim = L::DIM;
+    const int n[3] = {P.nx, P.ny, P.nz};
+    int base[3] = {0, 0, 0};
+    for (int a = 0; a < dim; ++a) base[a] = (int)floorf(P.ibx[a * P.ib_cap + s]);
+    for (int c = 0; c < (1 << dim); ++c) {
+        int q[3] = {base[0], base[1], base[2]};
+        for (int a = 0; a < dim; ++a) {
+            q[a] += (c >> a) & 1;
+            if (q[a] >= n[a]) q[a] -= n[a];
+        }
+        atomicOr(mask + (q[0] + P.nx * (q[1] + P.ny * q[2])), IB_BIT);
+    }
+}
+
+static __global__ void ib_clear_kernel(uint32_t *mask, long long N)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < N;
+         i += (long long)gridDim.x * blockDim.x)
+        mask[i] &= ~IB_BIT;
 }
 
 // ------------------------------------------------------------ auxiliary kernels -------

@@ -73,6 +73,7 @@ LBM_HD constexpr int axis_face(int cx, int cy, int cz) {
 
 // Per-cell link mask bits.
 constexpr unsigned SOLID_BIT = 1u << 31;
+constexpr unsigned IB_BIT = 1u << 30;   // the cell receives immersed-boundary force
 constexpr int DIRICHLET_SHIFT = 19;   // bit 19 + k: thermal link k ends on a Dirichlet face
 
 }  // namespace lbm

@@ -33,7 +33,8 @@ struct Layout {
     bool masked = false, has_solid = false;
     int streaming = LBM_STREAM_AA;
     size_t off_f = 0, off_g = 0, off_f2 = 0, off_g2 = 0, off_mask = 0, off_solid = 0;
-    size_t off_partial = 0, off_result = 0;
+    size_t off_partial = 0, off_result = 0, off_fib = 0, off_ib = 0;
+    int ib_cap = 0;
     size_t bytes = 0;
 };
 
@@ -92,6 +93,9 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
         if (!std::isfinite(c->T_wall[i])) return bad(LBM_ERR_ARG, "T_wall must be finite");
         any_wall |= c->face_flow[i] == LBM_FACE_WALL;
     }
+    if (c->ib_max_samples < 0 || c->ib_max_samples > (1 << 24))
+        return bad(LBM_ERR_ARG, "ib_max_samples must lie in [0, 2^24]");
+    if (c->ib_block < 0 || c->ib_block > 1024) return bad(LBM_ERR_ARG, "ib_block out of range");
     if (c->streaming != LBM_STREAM_AA && c->streaming != LBM_STREAM_PULL &&
         c->streaming != LBM_STREAM_SPLIT)
         return bad(LBM_ERR_ARG, "streaming must be LBM_STREAM_AA, _PULL or _SPLIT");
@@ -106,7 +110,8 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     L->N = N;
     L->S = ((size_t)N + 63) / 64 * 64;
     L->has_solid = c->solid_mask != nullptr;
-    L->masked = any_wall || L->has_solid;
+    L->ib_cap = c->ib_max_samples;
+    L->masked = any_wall || L->has_solid || L->ib_cap > 0;
     size_t off = 0;
     L->off_f = off;
     off = align_up(off + (size_t)Q * L->S * sizeof(float));
@@ -123,6 +128,12 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     if (L->masked) off = align_up(off + L->S * sizeof(uint32_t));
     L->off_solid = off;
     if (L->has_solid) off = align_up(off + L->S);
+    L->off_fib = L->off_ib = off;
+    if (L->ib_cap > 0) {
+        off = align_up(off + 3 * L->S * sizeof(float));   // per-cell force
+        L->off_ib = off;
+        off = align_up(off + (size_t)10 * L->ib_cap * sizeof(float));   // x3 ub3 w g3
+    }
     L->off_partial = off;
     off = align_up(off + (size_t)lbm::DIAG_BLOCKS * lbm::DIAG_N * sizeof(double));
     L->off_result = off;
@@ -135,6 +146,14 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
 {
     P.f = reinterpret_cast<float *>(ws + L.off_f);
     P.g = L.QT ? reinterpret_cast<float *>(ws + L.off_g) : nullptr;
+    P.fib = L.ib_cap ? reinterpret_cast<float *>(ws + L.off_fib) : nullptr;
+    float *ib = L.ib_cap ? reinterpret_cast<float *>(ws + L.off_ib) : nullptr;
+    P.ib_cap = L.ib_cap;
+    P.ib_n = 0;
+    P.ibx = ib;
+    P.ibub = ib ? ib + 3 * (size_t)L.ib_cap : nullptr;
+    P.ibw = ib ? ib + 6 * (size_t)L.ib_cap : nullptr;
+    P.ibg = ib ? ib + 7 * (size_t)L.ib_cap : nullptr;
     const bool two = L.streaming != LBM_STREAM_AA;
     P.fo = two ? reinterpret_cast<float *>(ws + L.off_f2) : nullptr;
     P.go = (two && L.QT) ? reinterpret_cast<float *>(ws + L.off_g2) : nullptr;

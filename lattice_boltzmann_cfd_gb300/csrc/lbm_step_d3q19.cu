@@ -4,29 +4,32 @@
 namespace lbm {
 namespace {
 
-template <class TL, int C, bool M, bool O, bool N>
+template <class TL, int C, bool M, bool O, bool N, bool I>
 cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s)
 {
-    step_kernel<D3Q19, TL, C, M, O, N><<<sh.grid, sh.block, 0, s>>>(P);
+    step_kernel<D3Q19, TL, C, M, O, N, I><<<sh.grid, sh.block, 0, s>>>(P);
     return cudaGetLastError();
 }
 
 using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
 
+// masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces
 template <class TL, bool N>
-cudaError_t dispatch_n(int coll, bool masked, bool odd, const Params &P, const Shape &sh,
+cudaError_t dispatch_n(int coll, int masked, bool odd, const Params &P, const Shape &sh,
                        cudaStream_t s)
 {
-    static const Fn table[2][2][2] = {
-        {{go<TL, 0, false, false, N>, go<TL, 0, false, true, N>},
-         {go<TL, 0, true, false, N>, go<TL, 0, true, true, N>}},
-        {{go<TL, 1, false, false, N>, go<TL, 1, false, true, N>},
-         {go<TL, 1, true, false, N>, go<TL, 1, true, true, N>}}};
-    return table[coll ? 1 : 0][masked ? 1 : 0][odd ? 1 : 0](P, sh, s);
+    static const Fn table[2][3][2] = {
+        {{go<TL, 0, false, false, N, false>, go<TL, 0, false, true, N, false>},
+         {go<TL, 0, true, false, N, false>, go<TL, 0, true, true, N, false>},
+         {go<TL, 0, true, false, N, true>, go<TL, 0, true, true, N, true>}},
+        {{go<TL, 1, false, false, N, false>, go<TL, 1, false, true, N, false>},
+         {go<TL, 1, true, false, N, false>, go<TL, 1, true, true, N, false>},
+         {go<TL, 1, true, false, N, true>, go<TL, 1, true, true, N, true>}}};
+    return table[coll ? 1 : 0][masked][odd ? 1 : 0](P, sh, s);
 }
 
 template <class TL>
-cudaError_t dispatch(int coll, bool masked, bool odd, bool narrow, const Params &P,
+cudaError_t dispatch(int coll, int masked, bool odd, bool narrow, const Params &P,
                      const Shape &sh, cudaStream_t s)
 {
     return narrow ? dispatch_n<TL, true>(coll, masked, odd, P, sh, s)
@@ -35,7 +38,8 @@ cudaError_t dispatch(int coll, bool masked, bool odd, bool narrow, const Params 
 
 }  // namespace
 
-cudaError_t launch_step_d3q19(int thermal, int coll, bool masked, bool odd, bool narrow, const Params &P,
+cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
+                              const Params &P,
                               const Shape &sh, cudaStream_t s)
 {
     if (thermal == 7) return dispatch<D3Q7>(coll, masked, odd, narrow, P, sh, s);

@@ -6,47 +6,52 @@ namespace {
 
 using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
 
-template <class TL, int C, bool M, bool N>
+template <class TL, int C, bool M, bool N, bool I>
 cudaError_t pull(const Params &P, const Shape &sh, cudaStream_t s)
 {
-    pull_kernel<D3Q19, TL, C, M, N><<<sh.grid, sh.block, 0, s>>>(P);
+    pull_kernel<D3Q19, TL, C, M, N, I><<<sh.grid, sh.block, 0, s>>>(P);
     return cudaGetLastError();
 }
 
-template <class TL, int C, bool M, bool N>
+template <class TL, int C, bool M, bool N, bool I>
 cudaError_t split(const Params &P, const Shape &sh, cudaStream_t s)
 {
-    collide_kernel<D3Q19, TL, C, M, N><<<sh.grid, sh.block, 0, s>>>(P);
+    collide_kernel<D3Q19, TL, C, M, N, I><<<sh.grid, sh.block, 0, s>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     stream_kernel<D3Q19, TL, M, N><<<sh.grid, sh.block, 0, s>>>(P);
     return cudaGetLastError();
 }
 
+// masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces
 template <class TL, bool PULL_MODE>
-cudaError_t dispatch(int coll, bool masked, bool narrow, const Params &P, const Shape &sh,
+cudaError_t dispatch(int coll, int masked, bool narrow, const Params &P, const Shape &sh,
                      cudaStream_t s)
 {
-#define LBM_ENTRY(C, M, N) (PULL_MODE ? pull<TL, C, M, N> : split<TL, C, M, N>)
-    static const Fn table[2][2][2] = {
-        {{LBM_ENTRY(0, false, false), LBM_ENTRY(0, false, true)},
-         {LBM_ENTRY(0, true, false), LBM_ENTRY(0, true, true)}},
-        {{LBM_ENTRY(1, false, false), LBM_ENTRY(1, false, true)},
-         {LBM_ENTRY(1, true, false), LBM_ENTRY(1, true, true)}}};
+#define LBM_ENTRY(C, M, N, I) (PULL_MODE ? pull<TL, C, M, N, I> : split<TL, C, M, N, I>)
+    static const Fn table[2][3][2] = {
+        {{LBM_ENTRY(0, false, false, false), LBM_ENTRY(0, false, true, false)},
+         {LBM_ENTRY(0, true, false, false), LBM_ENTRY(0, true, true, false)},
+         {LBM_ENTRY(0, true, false, true), LBM_ENTRY(0, true, true, true)}},
+        {{LBM_ENTRY(1, false, false, false), LBM_ENTRY(1, false, true, false)},
+         {LBM_ENTRY(1, true, false, false), LBM_ENTRY(1, true, true, false)},
+         {LBM_ENTRY(1, true, false, true), LBM_ENTRY(1, true, true, true)}}};
 #undef LBM_ENTRY
-    return table[coll ? 1 : 0][masked ? 1 : 0][narrow ? 1 : 0](P, sh, s);
+    return table[coll ? 1 : 0][masked][narrow ? 1 : 0](P, sh, s);
 }
 
 }  // namespace
 
-cudaError_t launch_pull_d3q19(int thermal, int coll, bool masked, bool narrow, const Params &P,
+cudaError_t launch_pull_d3q19(int thermal, int coll, int masked, bool narrow,
+                              const Params &P,
                               const Shape &sh, cudaStream_t s)
 {
     if (thermal == 7) return dispatch<D3Q7, true>(coll, masked, narrow, P, sh, s);
     return dispatch<NoThermal, true>(coll, masked, narrow, P, sh, s);
 }
 
-cudaError_t launch_split_d3q19(int thermal, int coll, bool masked, bool narrow, const Params &P,
+cudaError_t launch_split_d3q19(int thermal, int coll, int masked, bool narrow,
+                               const Params &P,
                                const Shape &sh, cudaStream_t s)
 {
     if (thermal == 7) return dispatch<D3Q7, false>(coll, masked, narrow, P, sh, s);

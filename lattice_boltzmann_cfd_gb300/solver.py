@@ -67,6 +67,8 @@ def make_config(w, streaming: str = "aa"):
     cfg.face_flow = (ctypes.c_int * 6)(*[_FLOW[k] for k in w.face_flow])
     cfg.face_T = (ctypes.c_int * 6)(*[_TFACE[k] for k in w.face_T])
     cfg.T_wall = (ctypes.c_double * 6)(*[float(v) for v in w.T_wall])
+    ib_x = getattr(w, "ib_x", None)
+    cfg.ib_max_samples = 0 if ib_x is None else int(len(ib_x))
     keep = []
     if w.solid is not None:
         solid = np.ascontiguousarray(w.solid, dtype=np.uint8)
@@ -97,6 +99,8 @@ class Simulation:
         self.Q, self.QT = self.cfg.lattice, self.cfg.thermal
         self.dim = 3 if self.Q == 19 else 2
         self.cells = self.cfg.nx * self.cfg.ny * self.cfg.nz
+        if getattr(w, "ib_x", None) is not None and len(w.ib_x):
+            self.set_ib_samples(w.ib_x, w.ib_ub, w.ib_w)
 
     # -- state ---------------------------------------------------------------------
     def init_equilibrium(self, rho, u, T=None):
@@ -129,6 +133,9 @@ class Simulation:
         m = torch.empty(self.grid, dtype=torch.int32, device=self.device)
         capi.lbm_get_link_mask(self.ctx, m)
         return m
+
+    def set_ib_samples(self, xyz, ub=None, weight=None):
+        capi.lbm_set_ib_samples(self.ctx, xyz, ub, weight)
 
     def diagnostics(self, allow_nonfinite: bool = False) -> dict:
         return capi.lbm_diagnostics(self.ctx, allow_nonfinite)

@@ -1,10 +1,11 @@
-// Host emulation of the CUDA path's AA step, for tests only (built by tests/conftest.py).
+// Host emulation of the CUDA path's steps, for tests only (built by tests/conftest.py).
 //
 // Runs the library's own per-cell functions (cell_mask, init_cell, aa_step_cell,
-// pull_step_cell, load_cell, collide, store_natural) on the CPU, one cell at a time, but writes every step into a second buffer
-// filled with NaN beforehand.  If a cell read a slot that another cell writes in the
-// same step, or two cells wrote one slot, or a slot of a fluid cell were left unwritten,
-// the stale or NaN value would reach the results; tests compare them with the oracle.
+// pull_step_cell, collide_in_place_cell, stream_cell, ib_sample) on the CPU, one cell at a
+// time, but writes every step into a second buffer filled with NaN beforehand.  If a cell
+// read a slot that another cell writes in the same step, or two cells wrote one slot, or a
+// slot of a fluid cell were left unwritten, the stale or NaN value would reach the
+// results; tests compare them with the oracle.
 // The read-out uses the parity-aware logical load, as lbm_get_populations does.
 #include <cmath>
 #include <cstring>
@@ -22,7 +23,7 @@ void step_all(const Params &Pr, const Params &Pw)
 {
     for (int z = 0; z < Pr.nz; ++z)
         for (int y = 0; y < Pr.ny; ++y)
-            for (int x = 0; x < Pr.nx; ++x) aa_step_cell<L, TL, C, M, O, NARROW>(Pr, Pw, x, y, z);
+            for (int x = 0; x < Pr.nx; ++x) aa_step_cell<L, TL, C, M, O, NARROW, M>(Pr, Pw, x, y, z);
 }
 
 // Two-buffer PULL step: pull from P.f, collide, natural store into W.
@@ -31,32 +32,17 @@ void pull_all(const Params &P, float *Wf, float *Wg)
 {
     for (int z = 0; z < P.nz; ++z)
         for (int y = 0; y < P.ny; ++y)
-            for (int x = 0; x < P.nx; ++x) pull_step_cell<L, TL, C, M, NARROW>(P, Wf, Wg, x, y, z);
+            for (int x = 0; x < P.nx; ++x) pull_step_cell<L, TL, C, M, NARROW, M>(P, Wf, Wg, x, y, z);
 }
 
 // SPLIT step: collide in place, then pull from P.f into W.
 template <class L, class TL, int C, bool M, bool NARROW>
 void split_all(const Params &P, float *Wf, float *Wg)
 {
-    const Offs none{};
-    for (int i = 0; i < P.nx * P.ny * P.nz; ++i) {
-        if (M && (P.mask[i] & SOLID_BIT)) continue;
-        float f[L::Q], g[TL::QA];
-        load_cell<L, TL, false, NATURAL, NARROW>(P, i, none, 0u, f, g);
-        collide<L, TL, C>(f, g, P.c);
-        store_natural<L, TL, NARROW>(P, P.f, P.g, i, f, g);
-    }
+    for (int i = 0; i < P.nx * P.ny * P.nz; ++i) collide_in_place_cell<L, TL, C, M, NARROW, M>(P, i);
     for (int z = 0; z < P.nz; ++z)
         for (int y = 0; y < P.ny; ++y)
-            for (int x = 0; x < P.nx; ++x) {
-                const int idx = x + P.nx * (y + P.ny * z);
-                const uint32_t m = M ? P.mask[idx] : 0u;
-                if (m & SOLID_BIT) continue;
-                const Offs o = make_offs(x, y, z, P);
-                float f[L::Q], g[TL::QA];
-                load_cell<L, TL, M, PULL, NARROW>(P, idx, o, m, f, g);
-                store_natural<L, TL, NARROW>(P, Wf, Wg, idx, f, g);
-            }
+            for (int x = 0; x < P.nx; ++x) stream_cell<L, TL, M, NARROW>(P, Wf, Wg, x, y, z);
 }
 
 template <class L, class TL, bool M, int O>
@@ -82,9 +68,36 @@ void read_all(const Params &P, float *fout, float *gout)
             }
 }
 
+// Immersed-boundary pass of one step on the host: the library's per-sample function, then
+// a sequential scatter (the kernel uses atomic additions).
+template <class L, class TL, int PAT>
+void ib_all(const Params &P)
+{
+    for (int s = 0; s < P.ib_n; ++s) {
+        int node[8];
+        float K[8], gs[3];
+        const int nn = ib_sample<L, TL, PAT>(P, s, node, K, gs);
+        for (int a = 0; a < 3; ++a) P.ibg[a * P.ib_cap + s] = gs[a];
+        for (int c = 0; c < nn; ++c) {
+            if (P.mask[node[c]] & SOLID_BIT) continue;
+            for (int a = 0; a < L::DIM; ++a) P.fib[(size_t)a * P.S + node[c]] += K[c] * gs[a];
+        }
+    }
+}
+
+template <class L, class TL>
+void ib_pass(const Params &P, int pat)
+{
+    if (P.ib_n <= 0) return;
+    if (pat == PULL) ib_all<L, TL, PULL>(P);
+    else if (pat == AA_ODD) ib_all<L, TL, AA_ODD>(P);
+    else ib_all<L, TL, NATURAL>(P);
+}
+
 template <class L, class TL, int C, bool NARROW>
 int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, const float *u,
-        const float *T, int steps, float *fout, float *gout, uint32_t *mask_out)
+        const float *T, int steps, float *fout, float *gout, uint32_t *mask_out, int ib_n,
+        const float *ib_x, const float *ib_ub, const float *ib_w)
 {
     const int mode = cfg.streaming;
     const float nan = std::numeric_limits<float>::quiet_NaN();
@@ -104,6 +117,32 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
                 for (int x = 0; x < cfg.nx; ++x)
                     mask[x + cfg.nx * (y + cfg.ny * z)] =
                         cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
+    // immersed-boundary samples (given inside the domain) and their stencils' IB_BIT
+    if (ib_n > 0) {
+        float *planes = const_cast<float *>(P.ibx);
+        const size_t cap = P.ib_cap;
+        for (int s = 0; s < ib_n; ++s) {
+            for (int a = 0; a < 3; ++a) {
+                planes[a * cap + s] = ib_x[3 * s + a];
+                planes[(3 + a) * cap + s] = ib_ub ? ib_ub[3 * s + a] : 0.0f;
+            }
+            planes[6 * cap + s] = ib_w ? ib_w[s] : 1.0f;
+        }
+        P.ib_n = ib_n;
+        const int n[3] = {cfg.nx, cfg.ny, cfg.nz};
+        for (int s = 0; s < ib_n; ++s) {
+            int base[3] = {0, 0, 0};
+            for (int a = 0; a < L::DIM; ++a) base[a] = (int)floorf(P.ibx[a * cap + s]);
+            for (int c = 0; c < (1 << L::DIM); ++c) {
+                int q[3] = {base[0], base[1], base[2]};
+                for (int a = 0; a < L::DIM; ++a) {
+                    q[a] += (c >> a) & 1;
+                    if (q[a] >= n[a]) q[a] -= n[a];
+                }
+                mask[q[0] + cfg.nx * (q[1] + cfg.ny * q[2])] |= IB_BIT;
+            }
+        }
+    }
     for (int z = 0; z < cfg.nz; ++z)
         for (int y = 0; y < cfg.ny; ++y)
             for (int x = 0; x < cfg.nx; ++x) {
@@ -119,6 +158,10 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
         Pw.f = fn.data();
         Pw.g = Lay.QT ? gn.data() : nullptr;
         float *wg = Lay.QT ? gn.data() : nullptr;
+        ib_pass<L, TL>(P, mode == LBM_STREAM_PULL    ? PULL
+                          : mode == LBM_STREAM_SPLIT ? NATURAL
+                          : parity                   ? AA_ODD
+                                                     : NATURAL);
         if (mode == LBM_STREAM_PULL) {
             if (Lay.masked) pull_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
             else pull_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
@@ -158,33 +201,38 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
 template <bool NARROW>
 int run_any(const lbm_config *cfg, const lbm_setup::Layout &Lay, const float *rho,
             const float *u, const float *T, int steps, float *fout, float *gout,
-            uint32_t *mask_out)
+            uint32_t *mask_out, int ib_n, const float *ib_x, const float *ib_ub,
+            const float *ib_w)
 {
     const bool mrt = cfg->collision == LBM_MRT;
     if (cfg->lattice == 19) {
         if (cfg->thermal == 7)
-            return mrt ? run<D3Q19, D3Q7, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                       : run<D3Q19, D3Q7, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
-        return mrt ? run<D3Q19, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                   : run<D3Q19, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+            return mrt ? run<D3Q19, D3Q7, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w)
+                       : run<D3Q19, D3Q7, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w);
+        return mrt ? run<D3Q19, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w)
+                   : run<D3Q19, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w);
     }
     if (cfg->thermal == 5)
-        return mrt ? run<D2Q9, D2Q5, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                   : run<D2Q9, D2Q5, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
-    return mrt ? run<D2Q9, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-               : run<D2Q9, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+        return mrt ? run<D2Q9, D2Q5, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w)
+                   : run<D2Q9, D2Q5, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w);
+    return mrt ? run<D2Q9, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w)
+               : run<D2Q9, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w);
 }
 
 // narrow != 0: the step uses 32-bit population indices, as the library does whenever
 // every index fits in 32 bits; 0: the 64-bit form used for larger grids.
 extern "C" int emu_run(const lbm_config *cfg, const float *rho, const float *u, const float *T,
-                       int steps, float *fout, float *gout, uint32_t *mask_out, int narrow)
+                       int steps, float *fout, float *gout, uint32_t *mask_out, int narrow,
+                       int ib_n, const float *ib_x, const float *ib_ub, const float *ib_w)
 {
     lbm_setup::Layout Lay;
     std::string why;
     if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
-    return narrow ? run_any<true>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out)
-                  : run_any<false>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out);
+    if (ib_n > Lay.ib_cap) return -2;
+    return narrow ? run_any<true>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x,
+                                  ib_ub, ib_w)
+                  : run_any<false>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n,
+                                   ib_x, ib_ub, ib_w);
 }
 
 // Every neighbour index the odd-step access pattern forms (idx + offset of +-c_q for each

@@ -29,6 +29,7 @@ def oracle_states(oracle, w, checkpoints, window=None):
         done = n
         rho, u, T = oracle.macroscopic(p, f, g)
         out[n] = dict(f=f.copy(), g=g.copy(), rho=rho, u=u, T=T, force=force,
+                      ib=p.last_ib.copy(),
                       diag=oracle.diagnostics(p, f, g) if window is None else None)
     return out
 
@@ -68,6 +69,16 @@ def mask_brute_force(w) -> np.ndarray:
         m |= wall.astype(np.uint64) << np.uint64(q)
         if w.thermal and q < w.thermal:
             m |= dir_hit.astype(np.uint64) << np.uint64(19 + q)
+    # bit 30: the cell lies in the 2^dim stencil of an immersed-boundary sample
+    if getattr(w, "ib_x", None) is not None:
+        ext = np.array([nx, ny, nz])
+        for xs in np.asarray(w.ib_x, np.float32):
+            base = np.floor(xs[:w.dim]).astype(int)
+            for corner in range(1 << w.dim):
+                q = [0, 0, 0]
+                for a in range(w.dim):
+                    q[a] = (base[a] + ((corner >> a) & 1)) % ext[a]
+                m[q[2], q[1], q[0]] |= np.uint64(1 << 30)
     m = np.where(solid, np.uint64(1 << 31), m)
     return m.astype(np.uint32)
 
@@ -83,8 +94,14 @@ def emulate(emu_lib, w, steps, narrow=True, streaming="aa"):
     u = np.ascontiguousarray(w.u0, np.float32)
     T = np.ascontiguousarray(w.T_init, np.float32) if w.thermal else None
     vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    ib = [None, None, None]
+    n_ib = 0
+    if getattr(w, "ib_x", None) is not None:
+        n_ib = len(w.ib_x)
+        ib = [np.ascontiguousarray(a, np.float32) if a is not None else None
+              for a in (w.ib_x, w.ib_ub, w.ib_w)]
     rc = emu_lib.emu_run(ctypes.byref(cfg), vp(rho), vp(u), vp(T), int(steps), vp(fo), vp(go),
-                         vp(mo), int(bool(narrow)))
+                         vp(mo), int(bool(narrow)), n_ib, vp(ib[0]), vp(ib[1]), vp(ib[2]))
     assert rc == 0
     return (fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid),
             mo.reshape(w.grid))
@@ -105,6 +122,15 @@ def small_cases():
     cases.append(dataclasses.replace(c3, collision="bgk", gbeta=0.02, up_axis=0))
     c2 = dataclasses.replace(W.perturbed(W.cavity2d(shape=(10, 8, 1)), seed=5), gbeta=0.01)
     cases.append(c2)
+    ibs = W.channel_ib_sphere(shape=(14, 12, 11), center=(6.3, 5.7, 5.2), radius=2.6,
+                              gx=1e-4, samples_per_area=2.0)
+    cases.append(dataclasses.replace(W.perturbed(ibs, seed=6), name=ibs.name + " perturbed"))
+    ib2 = W.perturbed(W.cavity2d(shape=(12, 10, 1)), seed=8)
+    x2 = np.array([[3.3, 4.1, 0.0], [5.7, 2.2, 0.0], [7.1, 6.6, 0.0], [9.4, 5.0, 0.0]],
+                  np.float32)
+    cases.append(dataclasses.replace(ib2, name=ib2.name + " + IB", gbeta=0.01, ib_x=x2,
+                                     ib_ub=np.full((4, 3), 0.01, np.float32),
+                                     ib_w=np.array([1.0, 0.5, 0.8, 1.2], np.float32)))
     cases.append(dataclasses.replace(
         c2, face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"),
         face_T=("adiabatic", "adiabatic", "dirichlet", "dirichlet", "adiabatic", "adiabatic"),

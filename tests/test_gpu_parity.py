@@ -61,6 +61,64 @@ def _reduced_configs():
 
 REDUCED = _reduced_configs()
 
+IB_CASES = [W.channel_ib_sphere(shape=(300, 24, 20), center=(40.3, 11.6, 9.8), radius=6,
+                                gx=1e-5),
+            dataclasses.replace(
+                W.perturbed(W.channel_ib_sphere(shape=(300, 24, 20), center=(40.3, 11.6, 9.8),
+                                                radius=6, gx=1e-5), seed=24),
+                name="IB channel perturbed")]
+
+
+def _compare_ib(got, ref):
+    F, Fr = np.array(got["diag"]["ib_force"]), np.asarray(ref["ib"][:3])
+    assert np.linalg.norm(F - Fr) <= TOL_FORCE_REL * np.linalg.norm(Fr), (F, Fr)
+    Tq, Tr = np.array(got["diag"]["ib_torque"]), np.asarray(ref["ib"][3:])
+    assert np.linalg.norm(Tq - Tr) <= TOL_FORCE_REL * np.linalg.norm(Fr) * 20, (Tq, Tr)
+
+
+@pytest.mark.parametrize("streaming", ["aa", "pull", "split"])
+@pytest.mark.parametrize("w", IB_CASES, ids=["IB sphere rest start", "IB sphere perturbed"])
+def test_immersed_boundary_200_and_201_steps(oracle_mod, w, streaming):
+    """Immersed-boundary sphere in the channel against the oracle: fields after 200 and 201
+    steps, reaction force (1e-4 relative) and torque."""
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    got = gpu_states(w, [200, 201], streaming=streaming)
+    for n in (200, 201):
+        compare_fields(w, got[n], ref[n])
+        _compare_ib(got[n], ref[n])
+
+
+def test_immersed_boundary_sample_order_does_not_matter():
+    """The library sorts samples into l-blocks and Morton order; giving them in a shuffled
+    order gives the same flow (up to the order of the atomic additions)."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.perturbed(W.channel_ib_sphere(shape=(64, 32, 32), center=(20.2, 15.7, 16.1),
+                                        radius=7), seed=4)
+    perm = np.random.default_rng(1).permutation(len(w.ib_x))
+    w2 = dataclasses.replace(w, ib_x=w.ib_x[perm], ib_ub=w.ib_ub[perm], ib_w=w.ib_w[perm])
+    out = []
+    for ww in (w, w2):
+        sim = Simulation(ww)
+        sim.init_equilibrium(torch.from_numpy(ww.rho0).cuda(), torch.from_numpy(ww.u0).cuda())
+        sim.step(50)
+        out.append((sim.populations()[0], sim.diagnostics()["ib_force"]))
+        sim.close()
+    assert (out[0][0] - out[1][0]).abs().max().item() < 1e-6
+    assert np.allclose(out[0][1], out[1][1], rtol=1e-5)
+
+
+def test_immersed_boundary_rejects_stencils_through_walls():
+    from lattice_boltzmann_cfd_gb300 import Simulation, capi
+    w = W.channel_ib_sphere(shape=(32, 16, 16), center=(10, 8, 8), radius=3)
+    sim = Simulation(w)
+    bad = np.array([[5.0, 15.2, 8.0]], np.float32)      # y = 15.2 >= ny - 1 on a wall axis
+    with pytest.raises(capi.LbmError) as e:
+        sim.set_ib_samples(bad)
+    assert e.value.status == capi.LBM_ERR_ARG
+    ok = np.array([[-3.5, 7.2, 8.0]], np.float32)       # periodic x: wrapped
+    sim.set_ib_samples(ok)
+    sim.close()
+
 
 @pytest.mark.parametrize("w", REDUCED, ids=[c.name for c in REDUCED])
 def test_configs_200_and_201_steps(oracle_mod, w):
@@ -118,10 +176,11 @@ def test_layouts_continue_each_others_state():
     a.close()
 
 
-@pytest.mark.parametrize("name", ["random_periodic", "channel_sphere"])
+@pytest.mark.parametrize("name", ["random_periodic", "channel_sphere", "channel_ib_sphere"])
 def test_full_size_128_cubed_200_201(oracle_mod, name):
-    """Configs 2 and 3 at their full 128^3 size, whole domain, 200 and 201 steps."""
-    w = W.by_name(name)
+    """Configs 2 and 3 (and config 3 with an immersed-boundary sphere) at their full 128^3
+    size, whole domain, 200 and 201 steps."""
+    w = W.channel_ib_sphere() if name == "channel_ib_sphere" else W.by_name(name)
     ref = oracle_states(oracle_mod, w, [200, 201])
     got = gpu_states(w, [200, 201])
     for n in (200, 201):
@@ -129,6 +188,8 @@ def test_full_size_128_cubed_200_201(oracle_mod, name):
         if w.solid is not None:
             F, Fr = np.array(got[n]["diag"]["force"]), ref[n]["force"]
             assert np.linalg.norm(F - Fr) <= TOL_FORCE_REL * np.linalg.norm(Fr), (F, Fr)
+        if w.ib_x is not None:
+            _compare_ib(got[n], ref[n])
 
 
 # --------------------------------------------------- full sizes: sampled windows ----
