@@ -46,8 +46,8 @@ BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112}
 # taken on; reported as "traffic" only while the sources are unchanged.
 NCU_TRAFFIC = {
     # ncu --set full, one even + one odd launch at 256^3 (see profiles/), scaled by cells
-    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.58, "src_hash": "3e760443af303491"},
-    "cavity3d_512": {"bytes_per_cell": 208.62, "src_hash": "3e760443af303491"},
+    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.56, "src_hash": "e1c7ee755e8d03c9"},
+    "cavity3d_512": {"bytes_per_cell": 208.65, "src_hash": "e1c7ee755e8d03c9"},
 }
 
 
@@ -341,6 +341,40 @@ def run_secondary(name, lbm_steps, reps, streaming="aa"):
             "frac": round(achieved / peak, 4)}
 
 
+def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None):
+    """MLUPS of a workload run as ``nslabs`` slabs along its outer axis on this GPU, with
+    the halo exchange after every step (a step = one step launch per slab + the exchange's
+    pack and unpack launches)."""
+    import torch
+    from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
+    w = cached_workload(name)
+    dom = SlabDomain(w, nslabs)
+    dom.init_equilibrium()
+    dom.step(4)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        dom.step(lbm_steps)
+    b.record()
+    torch.cuda.synchronize()
+    step_s = a.elapsed_time(b) / 1e3 / (reps * lbm_steps)
+    halo = dom.halo_bytes_per_step()
+    pairs = len(dom.pairs())
+    dom.close()
+    del dom
+    torch.cuda.empty_cache()
+    mlups = w.cells / step_s / 1e6
+    out = {"workload": workload_label(name, w), "layout": "aa", "slabs": nslabs,
+           "decomposition": "slabs along the outer axis, 1 ghost plane per inner face, "
+                            "FILL after even / DRAIN after odd steps, all on this GPU",
+           "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
+           "halo_launches_per_step": 4 * pairs}
+    if single_mlups:
+        out["vs_single_domain"] = round(mlups / single_mlups, 4)
+    return out
+
+
 # --------------------------------------------------------------------- main --------
 
 def run_gpu(args, dctx):
@@ -413,6 +447,12 @@ def run_gpu(args, dctx):
             # the 32^3 case fits in L2 and is launch-bound: long submissions replay graphs
             steps_n = 2048 if n == "taylor_green_32" else args.lbm_steps
             line["secondary"].append(run_secondary(n, steps_n, 4, mode))
+        single = {r["workload"]: r["mlups"] for r in line["secondary"] if r["layout"] == "aa"}
+        single[workload_label(args.workload, w)] = round(value, 1)
+        for n in (args.workload, "cavity3d_512"):
+            lbl = workload_label(n, cached_workload(n))
+            line["secondary"].append(run_slabs_secondary(n, 4, args.lbm_steps, 2,
+                                                         single.get(lbl)))
     line["cpu_baseline"] = cpu_baseline(args.workload)
     return line
 

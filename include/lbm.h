@@ -84,6 +84,12 @@ enum { LBM_D2Q9 = 9, LBM_D3Q19 = 19 };
 enum { LBM_THERMAL_NONE = 0, LBM_D2Q5 = 5, LBM_D3Q7 = 7 };
 enum { LBM_BGK = 0, LBM_MRT = 1 };
 enum { LBM_FACE_PERIODIC = 0, LBM_FACE_WALL = 1 };        /* flow: half-way bounce-back */
+/* A slab face: the context is one slab of a larger domain, split along its outer axis (z
+ * in 3-D, y in 2-D).  The grid then includes one ghost plane at each HALO face (the first /
+ * last plane of that axis); ghost cells are never updated and hold the neighbouring slab's
+ * populations, moved by lbm_halo_pack / lbm_halo_unpack ([TLBM] Sec. 3). */
+enum { LBM_FACE_HALO = 2 };
+enum { LBM_HALO_FILL = 0, LBM_HALO_DRAIN = 1 };
 enum { LBM_TFACE_ADIABATIC = 0, LBM_TFACE_DIRICHLET = 1 }; /* thermal, on WALL faces   */
 /* Population layout ([AA] Options::streaming): AA = one buffer streamed in place (152 B
  * per D3Q19 update); PULL = two buffers, one fused pull-collide kernel per step (152 B,
@@ -177,8 +183,11 @@ lbm_status lbm_get_populations(lbm_ctx *ctx, float *f, float *g);
 lbm_status lbm_set_populations(lbm_ctx *ctx, const float *f, const float *g);
 
 /* Copy the per-cell link mask (N uint32): bit q (1..Q-1) = link q is a wall link,
- * bit 19+k (k = 1..Q_T-1) = thermal link k ends on a DIRICHLET face, bit 31 = solid cell.
- * Device or page-locked host destination. */
+ * bit 19+k (k = 1..Q_T-1) = thermal link k ends on a DIRICHLET face, bit 29 = ghost plane
+ * of a slab, bit 30 = cell in an immersed-boundary sample's stencil, bit 31 = solid cell.
+ * A context with no WALL face, solid mask or sample capacity keeps no mask and yields all
+ * zeros (its ghost planes, if any, are known by their coordinate).  Device or page-locked
+ * host destination. */
 lbm_status lbm_get_link_mask(lbm_ctx *ctx, uint32_t *mask);
 
 /* Immersed boundary ([KFS] Sec. 3.1, Eq. 6-8; sample order of its Sec. 4, Fig. 7).
@@ -197,6 +206,30 @@ lbm_status lbm_get_link_mask(lbm_ctx *ctx, uint32_t *mask);
  * return. */
 lbm_status lbm_set_ib_samples(lbm_ctx *ctx, int n, const float *xyz, const float *ub,
                               const float *weight);
+
+/* Slab halos ([TLBM] Sec. 3: direction-selective exchange of contiguous buffers).  With
+ * the AA pattern only odd steps read or write across a slab face, so a slab driver runs one
+ * exchange after every lbm_step(1) of all its slabs:
+ *   after an even step (parity now 1), FILL: for each HALO side s, lbm_halo_pack(s, FILL)
+ *     here -> buffer -> the neighbour's lbm_halo_unpack(opposite s, FILL).  This supplies
+ *     the ghost slots that the boundary cells read in the odd step, and from which their
+ *     logical state is read (lbm_macroscopic, lbm_diagnostics ...) while the parity is 1;
+ *   after an odd step (parity now 0), DRAIN: the same with phase DRAIN, returning what the
+ *     boundary cells wrote into the ghost plane.  A DRAIN leaves alone a slot whose cell
+ *     bounced that population back itself (the link towards the ghost is a wall link).
+ * Between steps every owned cell then holds exactly what one undivided domain would hold.
+ * Only the populations that cross the face move: 5 of 19 (D3Q19) + 1 of 7 (D3Q7), 3 of 9
+ * (D2Q9) + 1 of 5 (D2Q5), per plane cell.
+ *   side: 0 = low face of the outer axis, 1 = high face; it must be a HALO face.
+ *   buf: device (or page-locked host) memory of lbm_halo_bytes bytes; packed as
+ *        [direction][plane cell] fp32, momentum then thermal, directions in index order.
+ * FILL is allowed at parity 1, DRAIN at parity 0 after at least one step (LBM_ERR_STATE
+ * otherwise).  HALO faces need the AA layout and no immersed-boundary capacity
+ * (LBM_ERR_UNSUPPORTED at create).  Stream-ordered; nothing waits.
+ * lbm_halo_bytes gives 0 for a context without HALO faces. */
+lbm_status lbm_halo_bytes(const lbm_ctx *ctx, size_t *bytes);
+lbm_status lbm_halo_pack(lbm_ctx *ctx, int side, int phase, void *buf);
+lbm_status lbm_halo_unpack(lbm_ctx *ctx, int side, int phase, const void *buf);
 
 /* Enqueue later work on another stream (a cudaStream_t). */
 lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);

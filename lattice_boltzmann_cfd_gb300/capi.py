@@ -21,7 +21,8 @@ STATUS_NAMES = {0: "LBM_OK", 1: "LBM_ERR_ARG", 2: "LBM_ERR_UNSUPPORTED",
 LBM_D2Q9, LBM_D3Q19 = 9, 19
 LBM_THERMAL_NONE, LBM_D2Q5, LBM_D3Q7 = 0, 5, 7
 LBM_BGK, LBM_MRT = 0, 1
-LBM_FACE_PERIODIC, LBM_FACE_WALL = 0, 1
+LBM_FACE_PERIODIC, LBM_FACE_WALL, LBM_FACE_HALO = 0, 1, 2
+LBM_HALO_FILL, LBM_HALO_DRAIN = 0, 1
 LBM_TFACE_ADIABATIC, LBM_TFACE_DIRICHLET = 0, 1
 LBM_STREAM_AA, LBM_STREAM_PULL, LBM_STREAM_SPLIT = 0, 1, 2
 STREAMING = {"aa": LBM_STREAM_AA, "pull": LBM_STREAM_PULL, "split": LBM_STREAM_SPLIT}
@@ -74,6 +75,9 @@ SIGNATURES = [
     ("lbm_set_populations", ctypes.c_int, [_VP, _VP, _VP]),
     ("lbm_get_link_mask", ctypes.c_int, [_VP, _VP]),
     ("lbm_set_ib_samples", ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP, _VP]),
+    ("lbm_halo_bytes", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
+    ("lbm_halo_pack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP]),
+    ("lbm_halo_unpack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_set_stream", ctypes.c_int, [_VP, _VP]),
     ("lbm_reduce_populations_static", ctypes.c_int,
      [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP,
@@ -208,6 +212,20 @@ def lbm_set_ib_samples(ctx, xyz, ub=None, weight=None):
     w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float32).reshape(n)
     ptr = lambda a: None if a is None else a.ctypes.data
     _check(load().lbm_set_ib_samples(ctx, n, ptr(x), ptr(u), ptr(w)), ctx)
+
+
+def lbm_halo_bytes(ctx) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().lbm_halo_bytes(ctx, ctypes.byref(n)), ctx)
+    return n.value
+
+
+def lbm_halo_pack(ctx, side: int, phase: int, buf):
+    _check(load().lbm_halo_pack(ctx, int(side), int(phase), _addr(buf)), ctx)
+
+
+def lbm_halo_unpack(ctx, side: int, phase: int, buf):
+    _check(load().lbm_halo_unpack(ctx, int(side), int(phase), _addr(buf)), ctx)
 
 
 def lbm_set_stream(ctx, stream):

@@ -90,6 +90,23 @@ cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long lo
     return cudaGetLastError();
 }
 
+cudaError_t launch_halo(int lattice, int thermal, const Params &P, int side, int phase,
+                        int unpack, float *buf, cudaStream_t s)
+{
+    const int plane_cells = lattice == 19 ? P.nx * P.ny : P.nx;
+    const dim3 b(256), g((plane_cells + 255) / 256);
+    return by_lattice(
+        lattice, thermal,
+        [&](auto tl) {
+            halo_kernel<D3Q19, decltype(tl)><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+            return cudaGetLastError();
+        },
+        [&](auto tl) {
+            halo_kernel<D2Q9, decltype(tl)><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+            return cudaGetLastError();
+        });
+}
+
 namespace {
 // Call fn with compile-time (MASKED, PAT).
 template <class Fn>

@@ -575,6 +575,64 @@ lbm_status lbm_set_ib_samples(lbm_ctx *c, int n, const float *xyz, const float *
     return LBM_OK;
 }
 
+namespace {
+
+// Populations per plane cell that cross a slab face (momentum + thermal).
+int halo_directions(const lbm_ctx *c)
+{
+    return c->cfg.lattice == LBM_D3Q19 ? 5 + (c->L.QT ? 1 : 0) : 3 + (c->L.QT ? 1 : 0);
+}
+
+size_t halo_plane_cells(const lbm_ctx *c)
+{
+    return c->cfg.lattice == LBM_D3Q19 ? (size_t)c->cfg.nx * c->cfg.ny : (size_t)c->cfg.nx;
+}
+
+lbm_status halo_call(lbm_ctx *c, int side, int phase, int unpack, const void *buf)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!c->L.halo) return fail(c, LBM_ERR_STATE, "no HALO face in this context");
+    if (side != 0 && side != 1) return fail(c, LBM_ERR_ARG, "side must be 0 (low) or 1 (high)");
+    const int face = 2 * (c->L.dim - 1) + side;
+    if (c->cfg.face_flow[face] != LBM_FACE_HALO)
+        return fail(c, LBM_ERR_ARG, "that side is not a HALO face");
+    if (phase != LBM_HALO_FILL && phase != LBM_HALO_DRAIN)
+        return fail(c, LBM_ERR_ARG, "phase must be LBM_HALO_FILL or LBM_HALO_DRAIN");
+    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state");
+    if (phase == LBM_HALO_FILL && c->parity != 1)
+        return fail(c, LBM_ERR_STATE, "FILL belongs before an odd step (parity 1)");
+    if (phase == LBM_HALO_DRAIN && (c->parity != 0 || c->steps == 0))
+        return fail(c, LBM_ERR_STATE, "DRAIN belongs after an odd step (parity 0)");
+    if (!buf) return fail(c, LBM_ERR_ARG, "buf is NULL");
+    DeviceGuard guard(c->device);
+    void *db;
+    lbm_status st = device_address(c, buf, "buf", &db);
+    if (st != LBM_OK) return st;
+    cudaError_t e = lbm::launch_halo(c->cfg.lattice, c->cfg.thermal, c->P, side, phase, unpack,
+                                     static_cast<float *>(db), c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "halo kernel");
+    return LBM_OK;
+}
+
+}  // namespace
+
+lbm_status lbm_halo_bytes(const lbm_ctx *c, size_t *bytes)
+{
+    if (!c || !bytes) return fail(nullptr, LBM_ERR_ARG, "ctx and bytes are required");
+    *bytes = c->L.halo ? sizeof(float) * halo_directions(c) * halo_plane_cells(c) : 0;
+    return LBM_OK;
+}
+
+lbm_status lbm_halo_pack(lbm_ctx *c, int side, int phase, void *buf)
+{
+    return halo_call(c, side, phase, 0, buf);
+}
+
+lbm_status lbm_halo_unpack(lbm_ctx *c, int side, int phase, const void *buf)
+{
+    return halo_call(c, side, phase, 1, buf);
+}
+
 lbm_status lbm_set_stream(lbm_ctx *c, void *cuda_stream)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");

@@ -57,6 +57,9 @@ cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
 cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s);
 cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
                            cudaStream_t s);
+// Slab halo pack (unpack = 0) or unpack (unpack = 1) of one side and phase.
+cudaError_t launch_halo(int lattice, int thermal, const Params &P, int side, int phase,
+                        int unpack, float *buf, cudaStream_t s);
 cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s);
 

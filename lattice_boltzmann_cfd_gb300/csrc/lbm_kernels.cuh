@@ -45,6 +45,8 @@ struct Params {
     CollideParams c;
     float abbT[7];         // per thermal direction k: omega * T_wall of the face k leaves by
     int face_wall[6];      // per face: 1 = wall (flow)
+    int face_halo[6];      // per face: 1 = halo face of a slab (ghost plane, no wrap)
+    int ghost_lo, ghost_hi;  // outer-axis coordinate of a slab's ghost planes, -1 = none
     int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
     float T_wall[6];
     // immersed boundary: per-cell force (3 planes of S, consumed and zeroed by the step),
@@ -81,6 +83,15 @@ LBM_HD int nb(const Offs &o, int cx, int cy, int cz)
 }
 
 LBM_HD bool bit(uint32_t m, int b) { return (m >> b) & 1u; }
+
+// A ghost plane of a slab (outer axis: z in 3-D, y in 2-D).  Masked kernels see GHOST_BIT;
+// unmasked ones (a slab with neither walls nor solids) test the coordinate.
+template <class L>
+LBM_HD bool ghost_plane(const Params &P, int y, int z)
+{
+    const int c = L::DIM == 3 ? z : y;
+    return c == P.ghost_lo || c == P.ghost_hi;
+}
 
 // ---------------------------------------------------------------- cell access ---------
 
@@ -280,6 +291,7 @@ LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB = false>
 LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
 {
+    if (!MASKED && ghost_plane<L>(Pr, y, z)) return;
     const int idx = x + Pr.nx * (y + Pr.ny * z);
     // The mask load and the population loads are issued together: the populations are
     // loaded as if no link were a wall, and wall links are fixed once the mask is in.
@@ -292,7 +304,7 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     }
     float ext[3];
     if (MASKED) {
-        if (m & SOLID_BIT) return;
+        if (m & SKIP_BITS) return;
         if (ODD && (m & wall_bits<L>())) fix_wall_loads<L, TL, AA_ODD, NARROW>(Pr, idx, m, f, g);
     }
     if constexpr (IB) {
@@ -338,7 +350,7 @@ LBM_HD void pull_step_cell(const Params &P, float *Wf, float *Wg, int x, int y, 
     }
     float ext[3];
     if (MASKED) {
-        if (m & SOLID_BIT) return;
+        if (m & SKIP_BITS) return;
         if (m & wall_bits<L>()) fix_wall_loads<L, TL, PULL, NARROW>(P, idx, m, f, g);
     }
     if constexpr (IB) {
@@ -369,7 +381,7 @@ template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB = false
 LBM_HD void collide_in_place_cell(const Params &P, int idx)
 {
     const uint32_t m = MASKED ? P.mask[idx] : 0u;
-    if (m & SOLID_BIT) return;
+    if (m & SKIP_BITS) return;
     float f[L::Q], g[TL::QA], ext[3];
     const Offs o{};
     load_cell<L, TL, false, NATURAL, NARROW>(P, idx, o, 0u, f, g);
@@ -402,7 +414,7 @@ LBM_HD void stream_cell(const Params &P, float *Wf, float *Wg, int x, int y, int
     uint32_t m = 0;
     if (MASKED) {
         m = P.mask[idx];
-        if (m & SOLID_BIT) return;
+        if (m & SKIP_BITS) return;
     }
     float f[L::Q], g[TL::QA];
     const Offs o = make_offs(x, y, z, P);
@@ -613,10 +625,16 @@ template <class L, class TL>
 LBM_HD uint32_t cell_mask(const Params &P, const uint8_t *solid, int x, int y, int z)
 {
     const int idx = x + P.nx * (y + P.ny * z);
-    if (solid && solid[idx]) return SOLID_BIT;
-    uint32_t m = 0;
     const int n[3] = {P.nx, P.ny, P.nz};
     const int c0[3] = {x, y, z};
+    // halo planes of a slab: kept for the neighbours' slots, never updated
+    uint32_t ghost = 0;
+    for (int a = 0; a < 3; ++a)
+        if ((P.face_halo[2 * a] && c0[a] == 0) || (P.face_halo[2 * a + 1] && c0[a] == n[a] - 1))
+            ghost = GHOST_BIT;
+    if (solid && solid[idx]) return SOLID_BIT | ghost;
+    if (ghost) return ghost;
+    uint32_t m = 0;
 #pragma unroll
     for (int q = 1; q < L::Q; ++q) {
         const int c[3] = {L::cx(q), L::cy(q), L::cz(q)};
@@ -626,10 +644,13 @@ LBM_HD uint32_t cell_mask(const Params &P, const uint8_t *solid, int x, int y, i
         for (int a = 0; a < 3; ++a) {
             s[a] = c0[a] + c[a];
             if (s[a] < 0) {
-                if (P.face_wall[2 * a]) { wall = true; face = 2 * a; }
+                if (P.face_wall[2 * a] || P.face_halo[2 * a]) { wall = true; face = 2 * a; }
                 else s[a] += n[a];
             } else if (s[a] >= n[a]) {
-                if (P.face_wall[2 * a + 1]) { wall = true; face = 2 * a + 1; }
+                if (P.face_wall[2 * a + 1] || P.face_halo[2 * a + 1]) {
+                    wall = true;
+                    face = 2 * a + 1;
+                }
                 else s[a] -= n[a];
             }
         }
@@ -665,7 +686,7 @@ __global__ void macro_kernel(const Params P, float *__restrict__ rho, float *__r
     const size_t N = (size_t)P.nx * P.ny * P.nz;
     uint32_t m = 0;
     if (MASKED) m = P.mask[idx];
-    if (m & SOLID_BIT) {
+    if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, y, z))) {
         if (rho) rho[idx] = 0.0f;
         if (u) {
             for (int a = 0; a < L::DIM; ++a) u[a * N + idx] = 0.0f;
@@ -713,7 +734,7 @@ __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__rest
     const size_t N = (size_t)P.nx * P.ny * P.nz;
     uint32_t m = 0;
     if (MASKED) m = P.mask[idx];
-    if (m & SOLID_BIT) {
+    if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, y, z))) {
         if (!SET) {
             for (int q = 0; q < L::Q; ++q) fo[q * N + idx] = 0.0f;
             if (TL::Q > 0 && go)
@@ -766,7 +787,7 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
         const int z = idx / (P.nx * P.ny);
         uint32_t m = 0;
         if (MASKED) m = P.mask[idx];
-        if (m & SOLID_BIT) continue;
+        if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, y, z))) continue;
         Offs o{};
         if (PAT != NATURAL) o = make_offs(x, y, z, P);
         float f[L::Q], g[TL::QA];
@@ -856,6 +877,74 @@ static __global__ void __launch_bounds__(DIAG_THREADS) diag_finalize(const doubl
         __syncthreads();
     }
     if (threadIdx.x < 15) out[threadIdx.x] = sh[0][threadIdx.x];
+}
+
+// ------------------------------------------------------------------ slab halos -------
+
+// Halo exchange of a slab whose outer axis (z in 3-D, y in 2-D) has HALO faces with ghost
+// planes ("Multi-GPU thermal lattice Boltzmann simulations using OpenACC and MPI", Sec. 3:
+// only the populations that cross a face are sent, as contiguous buffers).  Under the AA
+// pattern only the odd step reads and writes across a slab face:
+//   FILL  (before an odd step): the neighbour's boundary plane -> my ghost plane, the
+//         populations pointing out through my face (they are what my boundary cells pull);
+//   DRAIN (after it): my ghost plane -> the neighbour's boundary plane, the same populations
+//         (what my boundary cells pushed into the ghost).
+// A pack of side s / phase FILL reads my boundary plane at s with the populations pointing
+// into my slab; unpack of side s / FILL writes my ghost plane at s with those pointing out;
+// DRAIN swaps the planes' roles.  A DRAIN leaves slot (q, x) alone where the link of x
+// towards the ghost (opposite q) is a wall link: x bounced that population back into the
+// slot itself, and the ghost's copy was never written.  buf: [direction][plane cell],
+// momentum then thermal.
+template <class L, class TL>
+LBM_HD void halo_cell(const Params &P, int side, int phase, int unpack, float *buf, int i)
+{
+    constexpr int outer = L::DIM == 3 ? 2 : 1;
+    const int n_outer = outer == 2 ? P.nz : P.ny;
+    const int plane_cells = outer == 2 ? P.nx * P.ny : P.nx;
+    // ghost plane of the side, or the owned plane next to it
+    const bool ghost_plane = (phase == 0) == (unpack != 0);
+    int plane = side ? n_outer - 1 : 0;
+    if (!ghost_plane) plane += side ? -1 : 1;
+    const int idx = i + plane * plane_cells;
+    // directions pointing out through the side (ghost plane) or into the slab (owned plane)
+    const int out_sign = side ? 1 : -1;
+    const int sign = ghost_plane ? out_sign : -out_sign;
+    // DRAIN into my boundary plane: links that are bounced (or a cell never updated) keep
+    // their own value
+    const bool drain_in = unpack && !ghost_plane;
+    const uint32_t keep = drain_in && P.mask ? P.mask[idx] : 0u;
+    const bool skip_cell = keep & SKIP_BITS;
+    int k = 0;
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) {
+        const int c = outer == 2 ? L::cz(q) : L::cy(q);
+        if (c != sign) continue;
+        float *slot = P.f + ((size_t)q * P.S + (unsigned)idx);
+        float *b = buf + ((size_t)k * plane_cells + i);
+        if (!unpack) *b = *slot;
+        else if (!skip_cell && !bit(keep, L::opp(q))) *slot = *b;
+        ++k;
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int q = 0; q < TL::Q; ++q) {
+            const int c = outer == 2 ? L::cz(q) : L::cy(q);
+            if (c != sign) continue;
+            float *slot = P.g + ((size_t)q * P.S + (unsigned)idx);
+            float *b = buf + ((size_t)k * plane_cells + i);
+            if (!unpack) *b = *slot;
+            else if (!skip_cell && !bit(keep, L::opp(q))) *slot = *b;
+            ++k;
+        }
+    }
+}
+
+template <class L, class TL>
+__global__ void halo_kernel(const Params P, int side, int phase, int unpack, float *buf)
+{
+    const int plane_cells = L::DIM == 3 ? P.nx * P.ny : P.nx;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < plane_cells) halo_cell<L, TL>(P, side, phase, unpack, buf, i);
 }
 
 }  // namespace lbm

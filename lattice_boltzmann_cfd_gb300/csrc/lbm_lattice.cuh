@@ -74,6 +74,8 @@ LBM_HD constexpr int axis_face(int cx, int cy, int cz) {
 // Per-cell link mask bits.
 constexpr unsigned SOLID_BIT = 1u << 31;
 constexpr unsigned IB_BIT = 1u << 30;   // the cell receives immersed-boundary force
+constexpr unsigned GHOST_BIT = 1u << 29;  // halo plane of a slab (holds a neighbour's slots)
+constexpr unsigned SKIP_BITS = SOLID_BIT | GHOST_BIT;   // cells that are never updated
 constexpr int DIRICHLET_SHIFT = 19;   // bit 19 + k: thermal link k ends on a Dirichlet face
 
 }  // namespace lbm

@@ -32,6 +32,7 @@ struct Layout {
     size_t S = 0;
     bool masked = false, has_solid = false;
     int streaming = LBM_STREAM_AA;
+    bool halo = false;
     size_t off_f = 0, off_g = 0, off_f2 = 0, off_g2 = 0, off_mask = 0, off_solid = 0;
     size_t off_partial = 0, off_result = 0, off_fib = 0, off_ib = 0;
     int ib_cap = 0;
@@ -84,26 +85,38 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
         if (!std::isfinite(c->g_body[a])) return bad(LBM_ERR_ARG, "g_body must be finite");
     if (!std::isfinite(c->gbeta) || !std::isfinite(c->T0))
         return bad(LBM_ERR_ARG, "gbeta and T0 must be finite");
-    bool any_wall = false;
+    bool any_wall = false, any_halo = false;
+    const int outer = dim - 1;   // z in 3-D, y in 2-D
     for (int i = 0; i < 2 * dim; ++i) {
-        if (c->face_flow[i] != LBM_FACE_PERIODIC && c->face_flow[i] != LBM_FACE_WALL)
-            return bad(LBM_ERR_ARG, "face_flow entries must be PERIODIC or WALL");
+        const int k = c->face_flow[i];
+        if (k != LBM_FACE_PERIODIC && k != LBM_FACE_WALL && k != LBM_FACE_HALO)
+            return bad(LBM_ERR_ARG, "face_flow entries must be PERIODIC, WALL or HALO");
+        if (k == LBM_FACE_HALO && i / 2 != outer)
+            return bad(LBM_ERR_UNSUPPORTED, "HALO faces only on the outer axis (z in 3-D, y in 2-D)");
         if (c->face_T[i] != LBM_TFACE_ADIABATIC && c->face_T[i] != LBM_TFACE_DIRICHLET)
             return bad(LBM_ERR_ARG, "face_T entries must be ADIABATIC or DIRICHLET");
         if (!std::isfinite(c->T_wall[i])) return bad(LBM_ERR_ARG, "T_wall must be finite");
-        any_wall |= c->face_flow[i] == LBM_FACE_WALL;
+        any_wall |= k == LBM_FACE_WALL;
+        any_halo |= k == LBM_FACE_HALO;
     }
-    if (c->ib_max_samples < 0 || c->ib_max_samples > (1 << 24))
-        return bad(LBM_ERR_ARG, "ib_max_samples must lie in [0, 2^24]");
-    if (c->ib_block < 0 || c->ib_block > 1024) return bad(LBM_ERR_ARG, "ib_block out of range");
-    if (c->streaming != LBM_STREAM_AA && c->streaming != LBM_STREAM_PULL &&
-        c->streaming != LBM_STREAM_SPLIT)
-        return bad(LBM_ERR_ARG, "streaming must be LBM_STREAM_AA, _PULL or _SPLIT");
-    for (int a = 0; a < dim; ++a)
-        if (c->face_flow[2 * a] != c->face_flow[2 * a + 1])
+    for (int a = 0; a < dim; ++a) {
+        const int lo = c->face_flow[2 * a], hi = c->face_flow[2 * a + 1];
+        // a wrap must pair with a wrap; walls and halos mix (no slot is claimed twice)
+        if ((lo == LBM_FACE_PERIODIC) != (hi == LBM_FACE_PERIODIC))
             return bad(LBM_ERR_UNSUPPORTED,
                        "both faces of an axis must have the same flow kind (AA addressing)");
-
+    }
+    if (any_halo) {
+        const int n_outer = dim == 3 ? c->nz : c->ny;
+        const int ghosts = (c->face_flow[2 * outer] == LBM_FACE_HALO) +
+                           (c->face_flow[2 * outer + 1] == LBM_FACE_HALO);
+        if (n_outer < ghosts + 1)
+            return bad(LBM_ERR_ARG, "a slab needs at least one owned plane besides its ghosts");
+        if (c->streaming != LBM_STREAM_AA)
+            return bad(LBM_ERR_UNSUPPORTED, "HALO faces need the AA layout");
+        if (c->ib_max_samples > 0)
+            return bad(LBM_ERR_UNSUPPORTED, "HALO faces with immersed-boundary samples");
+    }
     L->Q = Q;
     L->QT = QT;
     L->dim = dim;
@@ -111,7 +124,9 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     L->S = ((size_t)N + 63) / 64 * 64;
     L->has_solid = c->solid_mask != nullptr;
     L->ib_cap = c->ib_max_samples;
+    // a slab's ghost planes are found by their coordinate: HALO faces need no mask
     L->masked = any_wall || L->has_solid || L->ib_cap > 0;
+    L->halo = any_halo;
     size_t off = 0;
     L->off_f = off;
     off = align_up(off + (size_t)Q * L->S * sizeof(float));
@@ -193,9 +208,13 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
     for (int i = 0; i < 6; ++i) {
         const bool active = i < 2 * dim;
         P.face_wall[i] = active && g.face_flow[i] == LBM_FACE_WALL;
+        P.face_halo[i] = active && g.face_flow[i] == LBM_FACE_HALO;
         P.face_dir[i] = P.face_wall[i] && g.thermal && g.face_T[i] == LBM_TFACE_DIRICHLET;
         P.T_wall[i] = (float)g.T_wall[i];
     }
+    const int outer = dim - 1, n_outer = dim == 3 ? g.nz : g.ny;
+    P.ghost_lo = P.face_halo[2 * outer] ? 0 : -1;
+    P.ghost_hi = P.face_halo[2 * outer + 1] ? n_outer - 1 : -1;
     // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)
     const double omega = (g.thermal == LBM_D2Q5) ? (4.0 + g.a_T) / 10.0 : (6.0 + g.a_T) / 21.0;
     for (int k = 0; k < 7; ++k) P.abbT[k] = 0.0f;

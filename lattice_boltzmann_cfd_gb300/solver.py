@@ -25,7 +25,8 @@ RATE_ROWS = {
     7: {"kappa": [1, 2, 3], "e": [4], "v": [5, 6]},
     5: {"kappa": [1, 2], "e": [3], "v": [4]},
 }
-_FLOW = {"periodic": capi.LBM_FACE_PERIODIC, "wall": capi.LBM_FACE_WALL}
+_FLOW = {"periodic": capi.LBM_FACE_PERIODIC, "wall": capi.LBM_FACE_WALL,
+         "halo": capi.LBM_FACE_HALO}
 _TFACE = {"adiabatic": capi.LBM_TFACE_ADIABATIC, "dirichlet": capi.LBM_TFACE_DIRICHLET}
 
 

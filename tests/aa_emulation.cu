@@ -1,15 +1,17 @@
 // Host emulation of the CUDA path's steps, for tests only (built by tests/conftest.py).
 //
 // Runs the library's own per-cell functions (cell_mask, init_cell, aa_step_cell,
-// pull_step_cell, collide_in_place_cell, stream_cell, ib_sample) on the CPU, one cell at a
+// pull_step_cell, collide_in_place_cell, stream_cell, ib_sample, halo_cell) on the CPU, one cell at a
 // time, but writes every step into a second buffer filled with NaN beforehand.  If a cell
 // read a slot that another cell writes in the same step, or two cells wrote one slot, or a
 // slot of a fluid cell were left unwritten, the stale or NaN value would reach the
 // results; tests compare them with the oracle.
 // The read-out uses the parity-aware logical load, as lbm_get_populations does.
+#include <array>
 #include <cmath>
 #include <cstring>
 #include <limits>
+#include <memory>
 #include <vector>
 
 #include "lbm_setup.h"
@@ -55,7 +57,7 @@ void read_all(const Params &P, float *fout, float *gout)
                 const int idx = x + P.nx * (y + P.ny * z);
                 uint32_t m = M ? P.mask[idx] : 0u;
                 float f[L::Q], g[TL::QA];
-                if (m & SOLID_BIT) {
+                if (m & SKIP_BITS) {
                     for (int q = 0; q < L::Q; ++q) fout[q * N + idx] = 0.0f;
                     for (int k = 0; k < TL::Q; ++k) gout[k * N + idx] = 0.0f;
                     continue;
@@ -94,31 +96,48 @@ void ib_pass(const Params &P, int pat)
     else ib_all<L, TL, NATURAL>(P);
 }
 
+// One domain's state on the host: population buffers (the current one and a NaN-filled one
+// that each step writes), the link mask and the parameter block.
 template <class L, class TL, int C, bool NARROW>
-int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, const float *u,
-        const float *T, int steps, float *fout, float *gout, uint32_t *mask_out, int ib_n,
-        const float *ib_x, const float *ib_ub, const float *ib_w)
-{
-    const int mode = cfg.streaming;
-    const float nan = std::numeric_limits<float>::quiet_NaN();
-    const size_t S = Lay.S;
-    std::vector<float> f(Lay.Q * S, nan), fn(Lay.Q * S, nan);
-    std::vector<float> g((Lay.QT ? Lay.QT : 1) * S, nan), gn((Lay.QT ? Lay.QT : 1) * S, nan);
-    std::vector<uint32_t> mask(S, 0u);
-    std::vector<char> ws(Lay.bytes + 256);
+struct Domain {
+    lbm_config cfg;
+    lbm_setup::Layout Lay;
+    std::vector<float> f, fn, g, gn;
+    std::vector<uint32_t> mask;
+    std::vector<char> ws;
     Params P{};
-    lbm_setup::fill_params(cfg, Lay, ws.data(), P);
-    P.f = f.data();
-    P.g = Lay.QT ? g.data() : nullptr;
-    P.mask = Lay.masked ? mask.data() : nullptr;
-    if (Lay.masked)
-        for (int z = 0; z < cfg.nz; ++z)
-            for (int y = 0; y < cfg.ny; ++y)
-                for (int x = 0; x < cfg.nx; ++x)
-                    mask[x + cfg.nx * (y + cfg.ny * z)] =
-                        cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
+    int parity = 0;
+
+    Domain(const lbm_config &c, const lbm_setup::Layout &lay) : cfg(c), Lay(lay)
+    {
+        const float nan = std::numeric_limits<float>::quiet_NaN();
+        const size_t S = Lay.S;
+        f.assign(Lay.Q * S, nan);
+        fn.assign(Lay.Q * S, nan);
+        g.assign((Lay.QT ? Lay.QT : 1) * S, nan);
+        gn.assign((Lay.QT ? Lay.QT : 1) * S, nan);
+        mask.assign(S, 0u);
+        ws.resize(Lay.bytes + 256);
+        lbm_setup::fill_params(cfg, Lay, ws.data(), P);
+        point();
+        P.mask = Lay.masked ? mask.data() : nullptr;
+        if (Lay.masked)
+            for (int z = 0; z < cfg.nz; ++z)
+                for (int y = 0; y < cfg.ny; ++y)
+                    for (int x = 0; x < cfg.nx; ++x)
+                        mask[x + cfg.nx * (y + cfg.ny * z)] =
+                            cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
+    }
+
+    void point()
+    {
+        P.f = f.data();
+        P.g = Lay.QT ? g.data() : nullptr;
+    }
+
     // immersed-boundary samples (given inside the domain) and their stencils' IB_BIT
-    if (ib_n > 0) {
+    void set_ib(int ib_n, const float *ib_x, const float *ib_ub, const float *ib_w)
+    {
         float *planes = const_cast<float *>(P.ibx);
         const size_t cap = P.ib_cap;
         for (int s = 0; s < ib_n; ++s) {
@@ -143,15 +162,23 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
             }
         }
     }
-    for (int z = 0; z < cfg.nz; ++z)
-        for (int y = 0; y < cfg.ny; ++y)
-            for (int x = 0; x < cfg.nx; ++x) {
-                const int i = x + cfg.nx * (y + cfg.ny * z);
-                if (mode == LBM_STREAM_PULL) init_cell<L, TL, PULL>(P, i, rho, u, T, x, y, z);
-                else init_cell<L, TL, NATURAL>(P, i, rho, u, T, x, y, z);
-            }
-    int parity = 0;
-    for (int s = 0; s < steps; ++s) {
+
+    void init(const float *rho, const float *u, const float *T)
+    {
+        for (int z = 0; z < cfg.nz; ++z)
+            for (int y = 0; y < cfg.ny; ++y)
+                for (int x = 0; x < cfg.nx; ++x) {
+                    const int i = x + cfg.nx * (y + cfg.ny * z);
+                    if (cfg.streaming == LBM_STREAM_PULL)
+                        init_cell<L, TL, PULL>(P, i, rho, u, T, x, y, z);
+                    else init_cell<L, TL, NATURAL>(P, i, rho, u, T, x, y, z);
+                }
+    }
+
+    void step()
+    {
+        const int mode = cfg.streaming;
+        const float nan = std::numeric_limits<float>::quiet_NaN();
         std::fill(fn.begin(), fn.end(), nan);
         std::fill(gn.begin(), gn.end(), nan);
         Params Pw = P;
@@ -177,22 +204,137 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
         }
         f.swap(fn);
         g.swap(gn);
-        P.f = f.data();
-        P.g = Lay.QT ? g.data() : nullptr;
+        point();
         parity ^= 1;
     }
-    const int pat = mode == LBM_STREAM_PULL ? PULL
-                    : (mode == LBM_STREAM_AA && parity) ? AA_ODD : NATURAL;
-    if (Lay.masked) {
-        if (pat == PULL) read_all<L, TL, true, PULL>(P, fout, gout);
-        else if (pat == AA_ODD) read_all<L, TL, true, AA_ODD>(P, fout, gout);
-        else read_all<L, TL, true, NATURAL>(P, fout, gout);
-    } else {
-        if (pat == PULL) read_all<L, TL, false, PULL>(P, fout, gout);
-        else if (pat == AA_ODD) read_all<L, TL, false, AA_ODD>(P, fout, gout);
-        else read_all<L, TL, false, NATURAL>(P, fout, gout);
+
+    // Logical populations (with the weights added back) of every cell.
+    void read(float *fout, float *gout) const
+    {
+        const int pat = cfg.streaming == LBM_STREAM_PULL ? PULL
+                        : (cfg.streaming == LBM_STREAM_AA && parity) ? AA_ODD : NATURAL;
+        if (Lay.masked) {
+            if (pat == PULL) read_all<L, TL, true, PULL>(P, fout, gout);
+            else if (pat == AA_ODD) read_all<L, TL, true, AA_ODD>(P, fout, gout);
+            else read_all<L, TL, true, NATURAL>(P, fout, gout);
+        } else {
+            if (pat == PULL) read_all<L, TL, false, PULL>(P, fout, gout);
+            else if (pat == AA_ODD) read_all<L, TL, false, AA_ODD>(P, fout, gout);
+            else read_all<L, TL, false, NATURAL>(P, fout, gout);
+        }
     }
-    if (mask_out) std::memcpy(mask_out, mask.data(), sizeof(uint32_t) * (size_t)Lay.N);
+
+    // The library's per-cell halo function over one side's plane.
+    void halo(int side, int phase, int unpack, float *buf)
+    {
+        const int plane_cells = L::DIM == 3 ? cfg.nx * cfg.ny : cfg.nx;
+        for (int i = 0; i < plane_cells; ++i) halo_cell<L, TL>(P, side, phase, unpack, buf, i);
+    }
+};
+
+template <class L, class TL, int C, bool NARROW>
+int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, const float *u,
+        const float *T, int steps, float *fout, float *gout, uint32_t *mask_out, int ib_n,
+        const float *ib_x, const float *ib_ub, const float *ib_w)
+{
+    Domain<L, TL, C, NARROW> d(cfg, Lay);
+    if (ib_n > 0) d.set_ib(ib_n, ib_x, ib_ub, ib_w);
+    d.init(rho, u, T);
+    for (int s = 0; s < steps; ++s) d.step();
+    d.read(fout, gout);
+    if (mask_out) std::memcpy(mask_out, d.mask.data(), sizeof(uint32_t) * (size_t)Lay.N);
+    return 0;
+}
+
+// The domain split into slabs along its outer axis at planes edges[0..nslabs] (edges[0] =
+// 0, edges[nslabs] = outer extent), each slab with a ghost plane per inner (or periodic)
+// face, run with one halo exchange after every step (FILL after an even step, DRAIN after
+// an odd one); the owned planes' logical populations are gathered into fout, gout.
+template <class L, class TL, int C, bool NARROW>
+int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const float *T,
+              int steps, int nslabs, const int *edges, float *fout, float *gout)
+{
+    using Dom = Domain<L, TL, C, NARROW>;
+    const int dim = L::DIM, outer = dim - 1;
+    const int n_outer = dim == 3 ? cfg.nz : cfg.ny;
+    const size_t plane = dim == 3 ? (size_t)cfg.nx * cfg.ny : (size_t)cfg.nx;
+    const size_t N = (size_t)cfg.nx * cfg.ny * cfg.nz;
+    const bool periodic = cfg.face_flow[2 * outer] == LBM_FACE_PERIODIC;
+    std::vector<std::unique_ptr<Dom>> doms;
+    std::vector<std::vector<int>> plane_lists;
+    std::vector<std::vector<uint8_t>> solids;
+    std::vector<std::array<bool, 2>> sides;
+    std::vector<std::array<std::vector<float>, 2>> bufs;
+    for (int r = 0; r < nslabs; ++r) {
+        const int lo = edges[r], hi = edges[r + 1];
+        const bool low = periodic || r > 0, high = periodic || r < nslabs - 1;
+        std::vector<int> planes;
+        if (low) planes.push_back((lo - 1 + n_outer) % n_outer);
+        for (int p = lo; p < hi; ++p) planes.push_back(p);
+        if (high) planes.push_back(hi % n_outer);
+        lbm_config lc = cfg;
+        if (dim == 3) lc.nz = (int)planes.size();
+        else lc.ny = (int)planes.size();
+        if (low) lc.face_flow[2 * outer] = LBM_FACE_HALO;
+        if (high) lc.face_flow[2 * outer + 1] = LBM_FACE_HALO;
+        const size_t Nl = plane * planes.size();
+        std::vector<uint8_t> sol;
+        std::vector<float> lr(Nl), lu((size_t)dim * Nl), lT(Nl);
+        if (cfg.solid_mask) sol.resize(Nl);
+        for (size_t k = 0; k < planes.size(); ++k)
+            for (size_t i = 0; i < plane; ++i) {
+                const size_t gi = (size_t)planes[k] * plane + i, li = k * plane + i;
+                if (cfg.solid_mask) sol[li] = cfg.solid_mask[gi];
+                lr[li] = rho[gi];
+                for (int a = 0; a < dim; ++a) lu[a * Nl + li] = u[a * N + gi];
+                if (T) lT[li] = T[gi];
+            }
+        lc.solid_mask = cfg.solid_mask ? sol.data() : nullptr;
+        lbm_setup::Layout Lay;
+        std::string why;
+        if (lbm_setup::validate(&lc, &Lay, &why) != LBM_OK) return -10 - r;
+        auto d = std::make_unique<Dom>(lc, Lay);
+        d->init(lr.data(), lu.data(), T ? lT.data() : nullptr);
+        const int dirs = (L::Q == 19 ? 5 : 3) + (TL::Q ? 1 : 0);
+        std::array<std::vector<float>, 2> b{std::vector<float>(dirs * plane),
+                                            std::vector<float>(dirs * plane)};
+        bufs.push_back(std::move(b));
+        doms.push_back(std::move(d));
+        plane_lists.push_back(planes);
+        solids.push_back(std::move(sol));
+        sides.push_back({low, high});
+    }
+    std::vector<std::pair<int, int>> pairs;
+    for (int r = 0; r + 1 < nslabs; ++r) pairs.push_back({r, r + 1});
+    if (periodic) pairs.push_back({nslabs - 1, 0});
+    for (int s = 0; s < steps; ++s) {
+        for (auto &d : doms) d->step();
+        const int phase = doms[0]->parity == 1 ? LBM_HALO_FILL : LBM_HALO_DRAIN;
+        for (auto [a, b] : pairs) {
+            doms[a]->halo(1, phase, 0, bufs[a][1].data());
+            doms[b]->halo(0, phase, 0, bufs[b][0].data());
+        }
+        for (auto [a, b] : pairs) {
+            doms[a]->halo(1, phase, 1, bufs[b][0].data());
+            doms[b]->halo(0, phase, 1, bufs[a][1].data());
+        }
+    }
+    const int QT = TL::Q;
+    for (int r = 0; r < nslabs; ++r) {
+        const Dom &d = *doms[r];
+        const size_t Nl = d.Lay.N;
+        std::vector<float> lf((size_t)L::Q * Nl), lg((size_t)(QT ? QT : 1) * Nl);
+        d.read(lf.data(), lg.data());
+        const int first = sides[r][0] ? 1 : 0;
+        for (int p = edges[r]; p < edges[r + 1]; ++p) {
+            const size_t k = (size_t)(p - edges[r] + first);
+            for (size_t i = 0; i < plane; ++i) {
+                const size_t gi = (size_t)p * plane + i, li = k * plane + i;
+                for (int q = 0; q < L::Q; ++q) fout[q * N + gi] = lf[q * Nl + li];
+                for (int q = 0; q < QT; ++q) gout[q * N + gi] = lg[q * Nl + li];
+            }
+        }
+    }
     return 0;
 }
 
@@ -233,6 +375,31 @@ extern "C" int emu_run(const lbm_config *cfg, const float *rho, const float *u, 
                                   ib_ub, ib_w)
                   : run_any<false>(cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n,
                                    ib_x, ib_ub, ib_w);
+}
+
+// Slab decomposition of the whole domain cfg (AA layout), see run_slabs; the same
+// population read-out as emu_run.
+extern "C" int emu_run_slabs(const lbm_config *cfg, const float *rho, const float *u,
+                             const float *T, int steps, int nslabs, const int *edges,
+                             float *fout, float *gout)
+{
+    lbm_setup::Layout Lay;
+    std::string why;
+    if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
+    if (cfg->streaming != LBM_STREAM_AA || nslabs < 1) return -2;
+    const bool mrt = cfg->collision == LBM_MRT;
+    if (cfg->lattice == 19) {
+        if (cfg->thermal == 7)
+            return mrt ? run_slabs<D3Q19, D3Q7, 1, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout)
+                       : run_slabs<D3Q19, D3Q7, 0, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
+        return mrt ? run_slabs<D3Q19, NoThermal, 1, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout)
+                   : run_slabs<D3Q19, NoThermal, 0, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
+    }
+    if (cfg->thermal == 5)
+        return mrt ? run_slabs<D2Q9, D2Q5, 1, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout)
+                   : run_slabs<D2Q9, D2Q5, 0, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
+    return mrt ? run_slabs<D2Q9, NoThermal, 1, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout)
+               : run_slabs<D2Q9, NoThermal, 0, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
 }
 
 // Every neighbour index the odd-step access pattern forms (idx + offset of +-c_q for each

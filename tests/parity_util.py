@@ -107,6 +107,62 @@ def emulate(emu_lib, w, steps, narrow=True, streaming="aa"):
             mo.reshape(w.grid))
 
 
+def emulate_slabs(emu_lib, w, steps, nslabs):
+    """(f, g) of the whole domain after ``steps`` steps of the host emulation run as
+    ``nslabs`` slabs along the outer axis with the library's halo exchange."""
+    from lattice_boltzmann_cfd_gb300.slabs import split_ranges
+    cfg, keep = make_config(w, "aa")
+    N = w.cells
+    fo = np.full((w.lattice, N), np.nan, np.float32)
+    go = np.full((max(w.thermal, 1), N), np.nan, np.float32)
+    rho = np.ascontiguousarray(w.rho0, np.float32)
+    u = np.ascontiguousarray(w.u0, np.float32)
+    T = np.ascontiguousarray(w.T_init, np.float32) if w.thermal else None
+    ranges = split_ranges(w.shape[w.dim - 1], nslabs)
+    edges = np.array([r[0] for r in ranges] + [ranges[-1][1]], np.int32)
+    vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = emu_lib.emu_run_slabs(ctypes.byref(cfg), vp(rho), vp(u), vp(T), int(steps),
+                               int(nslabs), vp(edges), vp(fo), vp(go))
+    assert rc == 0, rc
+    return fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid)
+
+
+def slab_cases():
+    """Problems whose outer axis is periodic (the slabs form a ring) or walled, with solid
+    cells and thermal Dirichlet faces on both kinds of axis."""
+    c3 = W.perturbed(W.cavity3d(shape=(9, 7, 13)), seed=31)
+    sol = np.zeros(c3.grid, np.uint8)
+    sol[3:6, 2:5, 3:6] = 1          # straddles the slab faces at z = 4 and z = 5
+    rb = dataclasses.replace(       # heated from below: Dirichlet faces on the outer axis
+        c3, name="D3Q19 MRT + D3Q7 Rayleigh-Benard 9x7x13 perturbed", solid=sol, gbeta=0.01,
+        face_T=("adiabatic",) * 4 + ("dirichlet", "dirichlet"),
+        T_wall=(0.0, 0.0, 0.0, 0.0, 0.4, -0.3))
+    cs = W.perturbed(W.channel_sphere(shape=(10, 9, 12), center=(4, 4, 0), radius=3.0), seed=32)
+    ring = dataclasses.replace(     # periodic z with the sphere across the wrap
+        cs, name="D3Q19 MRT channel periodic-z 10x9x12 + sphere across the wrap",
+        face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"),
+        g_body=(1e-4, 0.0, 2e-5))
+    c2 = dataclasses.replace(W.perturbed(W.cavity2d(shape=(10, 11, 1)), seed=33), gbeta=0.01)
+    c2p = dataclasses.replace(
+        c2, name=c2.name + " periodic-y",
+        face_flow=("wall", "wall", "periodic", "periodic", "periodic", "periodic"))
+    return [W.random_periodic(shape=(7, 6, 11), seed=34),
+            W.random_periodic(shape=(7, 6, 11), seed=35, collision="bgk"),
+            ring, rb, dataclasses.replace(c3, collision="bgk"), c2, c2p,
+            W.random_periodic(shape=(9, 10, 1), seed=36, lattice=9)]
+
+
+def outer_walls_case(shape=(12, 7, 11), seed=37):
+    """Walls and Dirichlet faces only at the ends of the outer axis, periodic elsewhere, no
+    solid: as slabs, the end ones run the masked kernels and the inner ones do not."""
+    c = W.perturbed(W.cavity3d(shape=shape), seed=seed)
+    return dataclasses.replace(
+        c, name=f"D3Q19 MRT + D3Q7 walls on z only {shape[0]}x{shape[1]}x{shape[2]}",
+        face_flow=("periodic",) * 4 + ("wall", "wall"), gbeta=0.01,
+        face_T=("adiabatic",) * 4 + ("dirichlet", "dirichlet"),
+        T_wall=(0.0, 0.0, 0.0, 0.0, 0.4, -0.3))
+
+
 def small_cases():
     """Small problems covering every lattice, collision, boundary kind and forcing."""
     cases = [W.random_periodic(shape=(6, 5, 4), seed=1),

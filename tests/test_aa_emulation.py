@@ -10,7 +10,8 @@ parity-aware.  The link mask is compared bit for bit with a brute-force builder.
 import numpy as np
 import pytest
 
-from parity_util import emulate, fluid_of, mask_brute_force, oracle_states, small_cases
+from parity_util import (emulate, emulate_slabs, fluid_of, mask_brute_force, oracle_states,
+                         outer_walls_case, slab_cases, small_cases)
 
 CASES = small_cases()
 
@@ -47,3 +48,35 @@ def test_neighbour_indices_stay_in_grid(emu_lib, lattice, shape):
     import ctypes
     emu_lib.emu_count_bad_indices.restype = ctypes.c_longlong
     assert emu_lib.emu_count_bad_indices(lattice, *shape) == 0
+
+
+# ------------------------------------------------------------- slab decomposition ---
+
+SLAB_CASES = slab_cases() + [outer_walls_case()]
+
+
+def _slab_counts(w):
+    n = w.shape[w.dim - 1]
+    return sorted({1, 2, 3, n})    # n: one owned plane per slab
+
+
+@pytest.mark.parametrize("w", SLAB_CASES, ids=[c.name for c in SLAB_CASES])
+def test_slabs_match_single_domain_bitwise(oracle_mod, emu_lib, w):
+    """The domain run as slabs along its outer axis, with a FILL exchange after every even
+    step and a DRAIN after every odd one, holds bit for bit the single domain's state at
+    both parities.  Every step writes into a NaN-filled buffer, so a ghost slot the odd step
+    reads but FILL did not supply, or a boundary slot DRAIN did not return, would surface
+    as NaN.  The single domain itself is checked against the oracle."""
+    fluid = fluid_of(w)
+    ref = oracle_states(oracle_mod, w, [5])[5]
+    for n in (1, 2, 5, 6):
+        f1, g1, _ = emulate(emu_lib, w, n)
+        if n == 5:
+            assert np.abs(f1 - ref["f"])[:, fluid].max() < 1e-6
+        for k in _slab_counts(w):
+            fs, gs = emulate_slabs(emu_lib, w, n, k)
+            assert not np.isnan(fs).any(), (n, k)
+            assert np.array_equal(fs, f1), (n, k)
+            if w.thermal:
+                assert not np.isnan(gs).any(), (n, k)
+                assert np.array_equal(gs, g1), (n, k)

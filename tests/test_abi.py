@@ -99,6 +99,33 @@ def test_bad_3d_configs_rejected(capi, overrides, status, text):
     assert text in str(e.value)
 
 
+@pytest.mark.parametrize("lattice,faces,extra,text", [
+    (19, [2, 2, 0, 0, 0, 0], {}, "outer axis"),               # HALO on x
+    (19, [0, 0, 0, 0, 0, 2], {}, "same flow kind"),           # periodic paired with HALO
+    (19, [0, 0, 0, 0, 2, 2], {"streaming": 1}, "AA layout"),  # PULL layout
+    (19, [0, 0, 0, 0, 2, 2], {"ib_max_samples": 4}, "immersed"),
+    (19, [0, 0, 0, 0, 2, 2], {"nz": 2}, "owned plane"),      # ghosts only
+    (9, [1, 1, 2, 1, 0, 0], {"ny": 1}, "owned plane"),
+])
+def test_halo_faces_validated(capi, lattice, faces, extra, text):
+    """HALO faces: outer axis only, never paired with a wrap, AA layout only, no immersed
+    samples, and at least one owned plane besides the ghosts."""
+    w = (W.random_periodic(shape=(8, 6, 5)) if lattice == 19
+         else W.random_periodic(shape=(8, 6, 1), lattice=9))
+    with pytest.raises(capi.LbmError, match=text):
+        _bytes(capi, w, face_flow=faces, **extra)
+
+
+def test_halo_faces_accepted(capi):
+    w = W.random_periodic(shape=(8, 6, 5))
+    assert _bytes(capi, w, face_flow=[0, 0, 0, 0, 2, 2]) > 0
+    assert _bytes(capi, w, face_flow=[1, 1, 0, 0, 1, 2], nz=2) > 0
+    w2 = W.cavity2d(shape=(8, 6, 1))
+    assert _bytes(capi, w2, face_flow=[1, 1, 2, 1, 0, 0]) > 0
+    # the z faces of a 2-D problem are not read, whatever they hold
+    assert _bytes(capi, w2, face_flow=[1, 1, 1, 1, 2, 2]) > 0
+
+
 def test_buoyancy_needs_thermal(capi):
     w = dataclasses.replace(W.random_periodic(shape=(8, 8, 8)), gbeta=1e-3)
     with pytest.raises(capi.LbmError, match="buoyancy"):

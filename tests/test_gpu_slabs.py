@@ -1,0 +1,129 @@
+"""Slab decomposition along the outer axis with the direction-selective halo exchange, on the
+GPU through the C ABI: the slabs together hold bit for bit the state of one domain run with
+the same kernels, at both AA parities, and their summed diagnostics agree with it.
+
+In these cases every slab runs the same kernel family as the undivided domain (masked where
+the domain has walls or solids on its other axes, unmasked where it is periodic and
+all-fluid), so the comparison is between identical per-cell arithmetic and any difference
+is an exchange error.  The undivided domain is in turn held to the oracle by the parity
+tests.  A domain whose only walls close the outer axis mixes the two families (the end
+slabs are masked, the inner ones are not); it is compared within fp32 rounding."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from lattice_boltzmann_cfd_gb300 import capi
+from lattice_boltzmann_cfd_gb300 import workloads as W
+from parity_util import outer_walls_case, slab_cases
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    capi.load()
+
+
+def _single(w, steps):
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    sim = Simulation(w)
+    dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    sim.init_equilibrium(dev(w.rho0), dev(w.u0), dev(w.T_init))
+    sim.step(steps)
+    f, g = sim.populations()
+    out = (f.cpu().numpy(), None if g is None else g.cpu().numpy(), sim.diagnostics())
+    sim.close()
+    return out
+
+
+def _slabs(w, steps, nslabs, chunks=None):
+    from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
+    dom = SlabDomain(w, nslabs)
+    dom.init_equilibrium()
+    for c in chunks or [steps]:
+        dom.step(c)
+    f, g = dom.populations()
+    out = (f.cpu().numpy(), None if g is None else g.cpu().numpy(), dom.diagnostics())
+    dom.close()
+    return out
+
+
+def _large_cases():
+    """Grids spanning several thread blocks along x with ragged tails and uneven slabs."""
+    rp = W.random_periodic(shape=(300, 20, 23), seed=41)
+    cs = W.perturbed(W.channel_sphere(shape=(300, 24, 22), center=(40, 12, 11), radius=6,
+                                      gx=1e-5), seed=42)
+    cs = dataclasses.replace(cs, name=cs.name + " perturbed")
+    c3 = W.perturbed(W.cavity3d(shape=(70, 40, 37)), seed=43)
+    c2 = W.perturbed(W.cavity2d(shape=(300, 181, 1)), seed=44)
+    return [rp, cs, c3, c2]
+
+
+CASES = slab_cases() + _large_cases()
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_slabs_bitwise_equal_single_domain(w):
+    n_outer = w.shape[w.dim - 1]
+    for steps in (7, 8):
+        f1, g1, d1 = _single(w, steps)
+        for k in sorted({2, 3, n_outer if n_outer <= 13 else 5}):
+            fs, gs, ds = _slabs(w, steps, k, chunks=[3, steps - 3])
+            assert np.array_equal(fs, f1), (steps, k)
+            if w.thermal:
+                assert np.array_equal(gs, g1), (steps, k)
+            assert ds["fluid_cells"] == d1["fluid_cells"]
+            assert ds["finite"]
+            assert abs(ds["mass"] - d1["mass"]) <= 1e-9 * abs(d1["mass"])
+            scale = max(1e-30, float(np.abs(d1["momentum"]).max()))
+            assert np.allclose(ds["momentum"], d1["momentum"], rtol=0, atol=1e-9 * scale)
+            fscale = max(1e-30, float(np.abs(d1["force"]).max()))
+            assert np.allclose(ds["force"], d1["force"], rtol=0, atol=1e-5 * fscale)
+            if w.thermal:
+                hscale = max(1e-30, float(np.abs(d1["heat"]).max()))
+                assert np.allclose(ds["heat"], d1["heat"], rtol=0, atol=1e-6 * hscale)
+
+
+def test_walls_only_on_the_outer_axis():
+    """Walls (and Dirichlet faces) only at the ends of the outer axis: the end slabs run
+    the masked kernels, the inner ones the unmasked kernels."""
+    w = outer_walls_case(shape=(64, 20, 24), seed=47)
+    for steps in (8, 9):
+        f1, g1, d1 = _single(w, steps)
+        fs, gs, ds = _slabs(w, steps, 4)
+        assert np.abs(fs - f1).max() < 1e-6
+        assert np.abs(gs - g1).max() < 1e-6
+        assert ds["fluid_cells"] == d1["fluid_cells"]
+        assert np.allclose(ds["heat"], d1["heat"], rtol=1e-5, atol=1e-9)
+
+
+def test_halo_call_order_is_enforced():
+    """FILL only at parity 1, DRAIN only at parity 0 after a step, only on HALO sides."""
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    w = W.random_periodic(shape=(16, 8, 10), seed=46)
+    w = dataclasses.replace(w, face_flow=("periodic",) * 4 + ("wall", "halo"))
+    sim = Simulation(w)
+    nbytes = capi.lbm_halo_bytes(sim.ctx)
+    assert nbytes == 4 * 5 * 16 * 8
+    buf = torch.empty(nbytes // 4, device="cuda")
+    sim.init_equilibrium(*(torch.from_numpy(a).cuda() for a in (w.rho0, w.u0)))
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_pack(sim.ctx, 1, capi.LBM_HALO_DRAIN, buf)   # no step yet
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_pack(sim.ctx, 1, capi.LBM_HALO_FILL, buf)    # parity 0
+    sim.step(1)
+    capi.lbm_halo_pack(sim.ctx, 1, capi.LBM_HALO_FILL, buf)
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_pack(sim.ctx, 0, capi.LBM_HALO_FILL, buf)    # a WALL side
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_pack(sim.ctx, 2, capi.LBM_HALO_FILL, buf)
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_unpack(sim.ctx, 1, capi.LBM_HALO_DRAIN, buf)  # parity 1
+    sim.step(1)
+    capi.lbm_halo_unpack(sim.ctx, 1, capi.LBM_HALO_DRAIN, buf)
+    torch.cuda.synchronize()
+    sim.close()
