@@ -15,6 +15,10 @@ Each move is a pack kernel into a buffer, a buffer copy when the slabs sit on di
 devices, and an unpack kernel, all in stream order; no kernel waits for another.  Between
 steps, the state of every owned cell is therefore what a single domain would hold, bit for
 bit.
+
+Two drivers share the slicing: SlabDomain holds every slab in one process (on one device or
+several); DistSlabDomain is one slab per torch.distributed rank, its buffers moved by
+point-to-point messages (ring_exchange).
 """
 from __future__ import annotations
 
@@ -32,6 +36,89 @@ def split_ranges(n: int, parts: int):
     return [(edges[i], edges[i + 1]) for i in range(parts)]
 
 
+def outer_axis(w):
+    """(axis in (x, y, z), axis in a (nz, ny, nx) field) of the slab direction."""
+    return w.dim - 1, (0 if w.dim == 3 else 1)
+
+
+def slab_part(w, nslabs: int, r: int):
+    """Slab r of ``w`` split into ``nslabs`` along its outer axis: (local workload, (low,
+    high) ghost flags, the domain plane of each local plane).  A periodic outer axis wraps
+    (the slabs form a ring); the end slabs of a walled one keep their faces."""
+    axis, np_axis = outer_axis(w)
+    n_outer = w.shape[axis]
+    lo_face, hi_face = w.face_flow[2 * axis], w.face_flow[2 * axis + 1]
+    periodic = lo_face == "periodic"
+    if not 1 <= nslabs <= n_outer:
+        raise ValueError("nslabs must lie in [1, outer extent]")
+    if getattr(w, "ib_x", None) is not None and len(w.ib_x):
+        raise ValueError("slabs do not take immersed-boundary samples")
+    lo, hi = split_ranges(n_outer, nslabs)[r]
+    low = periodic or r > 0
+    high = periodic or r < nslabs - 1
+    planes = ([(lo - 1) % n_outer] if low else []) + list(range(lo, hi)) + \
+             ([hi % n_outer] if high else [])
+    faces = list(w.face_flow)
+    faces[2 * axis] = "halo" if low else lo_face
+    faces[2 * axis + 1] = "halo" if high else hi_face
+    shape = list(w.shape)
+    shape[axis] = len(planes)
+
+    def take(a, lead=0):
+        if a is None:
+            return None
+        return np.ascontiguousarray(np.take(a, planes, axis=np_axis + lead))
+
+    local = dataclasses.replace(
+        w, shape=tuple(shape), face_flow=tuple(faces), solid=take(w.solid),
+        rho0=take(w.rho0), u0=take(w.u0, 1), T_init=take(w.T_init))
+    return local, (low, high), planes
+
+
+def ring_exchange(rank: int, world: int, periodic: bool, phase: int, pack, unpack, send,
+                  recv, group=None, sync=None):
+    """One halo exchange of slab ``rank`` with its neighbours over torch.distributed.
+
+    pack(side, phase, buf) fills send[side]; unpack(side, phase, buf) consumes a buffer;
+    sync(), if given, runs after the packs and again after the receives (to order device
+    work around the messages).
+    My side-s buffer goes to the neighbour's opposite side.  Messages carry as tag the side
+    they land on, and are posted in one fixed order (sends of sides 0, 1; receives of the
+    neighbours' side 0, then side 1), so that back-ends which match point-to-point messages
+    by order (NCCL) pair them right even when both neighbours are the same rank."""
+    import torch.distributed as dist
+    lo_nb = rank - 1 if rank > 0 else (world - 1 if periodic else None)
+    hi_nb = rank + 1 if rank < world - 1 else (0 if periodic else None)
+    nbs = (lo_nb, hi_nb)
+    for side in (0, 1):
+        if nbs[side] is not None:
+            pack(side, phase, send[side])
+    if sync is not None:
+        sync()
+    if world == 1:
+        if periodic:     # a ring of one slab: its own buffers, crossed
+            unpack(0, phase, send[1])
+            unpack(1, phase, send[0])
+        return
+    ops = []
+    for side in (0, 1):
+        if nbs[side] is not None:
+            ops.append(dist.P2POp(dist.isend, send[side], nbs[side], group, tag=1 - side))
+    # the neighbour's side-0 buffer lands on my side 1, its side-1 buffer on my side 0
+    for their_side in (0, 1):
+        mine = 1 - their_side
+        if nbs[mine] is not None:
+            ops.append(dist.P2POp(dist.irecv, recv[mine], nbs[mine], group, tag=mine))
+    if ops:
+        for req in dist.batch_isend_irecv(ops):
+            req.wait()
+    if sync is not None:
+        sync()
+    for side in (0, 1):
+        if nbs[side] is not None:
+            unpack(side, phase, recv[side])
+
+
 class SlabDomain:
     """The workload ``w`` split into ``nslabs`` slabs along its outer axis, slab r on
     ``devices[r % len(devices)]``.  The outer axis must be periodic (the slabs form a ring)
@@ -39,38 +126,20 @@ class SlabDomain:
 
     def __init__(self, w, nslabs: int, devices=None):
         import torch
-        if getattr(w, "ib_x", None) is not None and len(w.ib_x):
-            raise ValueError("slabs do not take immersed-boundary samples")
         self.w = w
         self.dim = w.dim
-        self.axis = self.dim - 1                  # outer axis in (x, y, z)
-        self.np_axis = 0 if self.dim == 3 else 1  # its axis in a (nz, ny, nx) field
+        self.axis, self.np_axis = outer_axis(w)
         self.n_outer = w.shape[self.axis]
-        lo_face, hi_face = w.face_flow[2 * self.axis], w.face_flow[2 * self.axis + 1]
-        self.periodic = lo_face == "periodic"
-        if not 1 <= nslabs <= self.n_outer:
-            raise ValueError("nslabs must lie in [1, outer extent]")
+        self.periodic = w.face_flow[2 * self.axis] == "periodic"
         devices = list(devices) if devices else [torch.device("cuda")]
-        self.ranges = split_ranges(self.n_outer, nslabs)
+        self.ranges = split_ranges(self.n_outer, nslabs) if 1 <= nslabs <= self.n_outer else []
         self.slabs, self.sides, self.plane_lists, self.buffers = [], [], [], []
-        for r, (lo, hi) in enumerate(self.ranges):
-            low = self.periodic or r > 0          # ghost plane below the owned ones
-            high = self.periodic or r < nslabs - 1
-            planes = ([(lo - 1) % self.n_outer] if low else []) + list(range(lo, hi)) + \
-                     ([hi % self.n_outer] if high else [])
-            faces = list(w.face_flow)
-            faces[2 * self.axis] = "halo" if low else lo_face
-            faces[2 * self.axis + 1] = "halo" if high else hi_face
-            shape = list(w.shape)
-            shape[self.axis] = len(planes)
-            local = dataclasses.replace(
-                w, shape=tuple(shape), face_flow=tuple(faces),
-                solid=self._take(w.solid, planes), rho0=self._take(w.rho0, planes),
-                u0=self._take(w.u0, planes, 1), T_init=self._take(w.T_init, planes))
+        for r in range(nslabs):
+            local, sides, planes = slab_part(w, nslabs, r)
             sim = Simulation(local, device=devices[r % len(devices)])
             nfloat = capi.lbm_halo_bytes(sim.ctx) // 4
             self.slabs.append(sim)
-            self.sides.append((low, high))
+            self.sides.append(sides)
             self.plane_lists.append(planes)
             self.buffers.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
                                  for _ in range(2)])   # [low side, high side]
@@ -174,3 +243,77 @@ class SlabDomain:
     def close(self):
         for sim in self.slabs:
             sim.close()
+
+
+class DistSlabDomain:
+    """Slab ``rank`` of ``w`` split into ``world`` slabs, one per torch.distributed rank
+    (one process per GPU).  Every step is followed by ring_exchange of its halos (FILL after
+    even, DRAIN after odd steps), so between steps the owned planes hold what one undivided
+    domain would hold."""
+
+    def __init__(self, w, rank: int, world: int, device=None, group=None):
+        import torch
+        self.w, self.rank, self.world, self.group = w, rank, world, group
+        self.axis, self.np_axis = outer_axis(w)
+        self.periodic = w.face_flow[2 * self.axis] == "periodic"
+        self.range = split_ranges(w.shape[self.axis], world)[rank]
+        local, self.sides, self.planes = slab_part(w, world, rank)
+        self.local = local
+        self.sim = Simulation(local, device=device)
+        nfloat = capi.lbm_halo_bytes(self.sim.ctx) // 4
+        new = lambda: torch.empty(nfloat, dtype=torch.float32, device=self.sim.device)
+        self.send = [new(), new()]
+        self.recv = [new(), new()]
+
+    @property
+    def parity(self) -> int:
+        return self.sim.parity
+
+    def init_equilibrium(self):
+        import torch
+        dev = lambda a: None if a is None else torch.from_numpy(a).to(self.sim.device)
+        self.sim.init_equilibrium(dev(self.local.rho0), dev(self.local.u0),
+                                  dev(self.local.T_init))
+
+    # The halo kernels run on the context's stream, which need not be torch's current
+    # stream (the one communication back-ends order against): the device is synchronised
+    # after the packs and before the unpacks.
+    def _pack(self, side, phase, buf):
+        capi.lbm_halo_pack(self.sim.ctx, side, phase, buf)
+
+    def _unpack(self, side, phase, buf):
+        capi.lbm_halo_unpack(self.sim.ctx, side, phase, buf)
+
+    def _sync(self):
+        import torch
+        if self.sim.device.type == "cuda":
+            torch.cuda.synchronize(self.sim.device)
+
+    def step(self, n: int = 1):
+        for _ in range(n):
+            self.sim.step(1)
+            phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
+            ring_exchange(self.rank, self.world, self.periodic, phase, self._pack,
+                          self._unpack, self.send, self.recv, self.group, sync=self._sync)
+
+    def owned(self, t, lead=0):
+        """The owned planes of a local field (ghost planes dropped)."""
+        low, high = self.sides
+        idx = [slice(None)] * t.dim()
+        ax = self.np_axis + lead
+        idx[ax] = slice(1 if low else 0, t.shape[ax] - (1 if high else 0))
+        return t[tuple(idx)]
+
+    def populations(self):
+        f, g = self.sim.populations()
+        return self.owned(f, 1), (None if g is None else self.owned(g, 1))
+
+    def macroscopic(self):
+        rho, u, T = self.sim.macroscopic()
+        return self.owned(rho), self.owned(u, 1), (None if T is None else self.owned(T))
+
+    def diagnostics(self) -> dict:
+        return self.sim.diagnostics(allow_nonfinite=True)
+
+    def close(self):
+        self.sim.close()

@@ -33,7 +33,7 @@ def _worker(rank, world, port, out):
 def test_two_gloo_ranks_take_the_max_time():
     import torch.multiprocessing as mp
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert dict(out) == {0: 2.5, 1: 2.5}

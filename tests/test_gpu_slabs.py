@@ -127,3 +127,22 @@ def test_halo_call_order_is_enforced():
     capi.lbm_halo_unpack(sim.ctx, 1, capi.LBM_HALO_DRAIN, buf)
     torch.cuda.synchronize()
     sim.close()
+
+
+@pytest.mark.parametrize("w", [W.random_periodic(shape=(40, 12, 9), seed=48),
+                               W.perturbed(W.cavity2d(shape=(40, 13, 1)), seed=49)],
+                         ids=["periodic ring of one rank", "2-D walled, one rank"])
+def test_per_rank_driver_alone(w):
+    """The one-slab-per-rank driver with a single rank: a periodic axis makes it a ring with
+    itself (its own ghost planes exchanged), a walled one a plain domain."""
+    from lattice_boltzmann_cfd_gb300.slabs import DistSlabDomain
+    for steps in (6, 7):
+        f1, g1, _ = _single(w, steps)
+        d = DistSlabDomain(w, 0, 1)
+        d.init_equilibrium()
+        d.step(steps)
+        f, g = d.populations()
+        assert np.array_equal(f.cpu().numpy(), f1)
+        if w.thermal:
+            assert np.array_equal(g.cpu().numpy(), g1)
+        d.close()
