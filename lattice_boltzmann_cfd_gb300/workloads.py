@@ -75,7 +75,7 @@ class Workload:
 
     @property
     def dim(self) -> int:
-        return 3 if self.lattice == 19 else 2
+        return 2 if self.lattice == 9 else 3
 
     @property
     def cells(self) -> int:
@@ -99,6 +99,8 @@ _OTHER = 1.2   # rate of every non-hydrodynamic moment in the workloads
 
 
 def _momentum_rates(lattice):
+    if lattice == 27:   # central moments: trace of the second order, then orders 3-6
+        return {"bulk": _OTHER, "r3": _OTHER, "r4": _OTHER, "r5": _OTHER, "r6": _OTHER}
     if lattice == 19:
         return {"e": _OTHER, "eps": _OTHER, "q": _OTHER, "pi": _OTHER, "m": _OTHER}
     return {"e": _OTHER, "eps": _OTHER, "q": _OTHER}
@@ -129,8 +131,10 @@ def taylor_green(n: int = 32, u0: float = 0.05, nu: float = 0.1, shape=None) -> 
 
 def random_periodic(n: int = 128, seed: int = 2, nu: float = 0.01, shape=None,
                     collision: str = "mrt", lattice: int = 19) -> Workload:
-    nx, ny, nz = shape or ((n, n, n) if lattice == 19 else (n, n, 1))
-    dim = 3 if lattice == 19 else 2
+    nx, ny, nz = shape or ((n, n, 1) if lattice == 9 else (n, n, n))
+    dim = 2 if lattice == 9 else 3
+    if lattice == 27:
+        collision = "cm"
     rng = np.random.default_rng(seed)
     rho = (1.0 + rng.normal(0.0, 1e-3, size=(nz, ny, nx))).astype(np.float32)
     u = rng.uniform(-0.02, 0.02, size=(dim, nz, ny, nx)).astype(np.float32)
@@ -150,13 +154,17 @@ def sphere_mask(shape, center, radius) -> np.ndarray:
 
 
 def channel_sphere(n: int = 128, radius: float = 16, center=(40, 64, 64), gx: float = 1e-6,
-                   nu: float = 0.02, shape=None) -> Workload:
+                   nu: float = 0.02, shape=None, lattice: int = 19) -> Workload:
+    """Body-force-driven channel (walls in y and z, periodic in x) around a solid sphere;
+    lattice 19 with MRT or 27 with central moments."""
     shape = shape or (n, n, n)
     rho, u = _rest(shape, 3)
     nx, ny, nz = shape
+    coll = "cm" if lattice == 27 else "mrt"
     return Workload(
-        name=f"D3Q19 MRT channel {nx}x{ny}x{nz} + sphere r={radius:g}", lattice=19, thermal=0,
-        collision="mrt", shape=shape, nu=nu, rates=_momentum_rates(19),
+        name=f"D3Q{lattice} {coll.upper()} channel {nx}x{ny}x{nz} + sphere r={radius:g}",
+        lattice=lattice, thermal=0, collision=coll, shape=shape, nu=nu,
+        rates=_momentum_rates(lattice),
         g_body=(gx, 0.0, 0.0),
         face_flow=("periodic", "periodic", "wall", "wall", "wall", "wall"),
         solid=sphere_mask(shape, center, radius), rho0=rho, u0=u, steps=2000)

@@ -34,7 +34,7 @@ _lib = None
 
 PERIODIC, WALL = 0, 1
 ADIABATIC, DIRICHLET = 0, 1
-BGK, MRT = 0, 1
+BGK, MRT, CM = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -53,6 +53,7 @@ class _Problem(ctypes.Structure):
     _fields_ = [
         ("lattice", ctypes.c_int), ("thermal", ctypes.c_int), ("collision", ctypes.c_int),
         ("tau", ctypes.c_double), ("s", ctypes.c_double * 19), ("s_T", ctypes.c_double * 7),
+        ("cm_rates", ctypes.c_double * 5),
         ("a_T", ctypes.c_double), ("g_body", ctypes.c_double * 3), ("gbeta", ctypes.c_double),
         ("T0", ctypes.c_double), ("up_axis", ctypes.c_int), ("face_flow", ctypes.c_int * 6),
         ("face_T", ctypes.c_int * 6), ("T_wall", ctypes.c_double * 6),
@@ -111,6 +112,10 @@ _ROWS = {
     5: {"kappa": [1, 2], "e": [3], "v": [4]},
 }
 
+# D3Q27 central-moment rates by name: trace of the second-order moments, then one per order
+# (the shear rate comes from nu).
+CM_RATE_NAMES = ("bulk", "r3", "r4", "r5", "r6")
+
 
 class Problem:
     """The oracle's view of a workload, optionally restricted to a window of the domain.
@@ -127,14 +132,17 @@ class Problem:
         p = _Problem()
         p.lattice = spec.lattice
         p.thermal = spec.thermal
-        p.collision = {"bgk": BGK, "mrt": MRT}[spec.collision]
+        p.collision = {"bgk": BGK, "mrt": MRT, "cm": CM}[spec.collision]
         p.tau = 3.0 * spec.nu + 0.5
         s = [0.0] * 19
         rates = dict(spec.rates)
         rates["nu"] = 1.0 / (3.0 * spec.nu + 0.5)
-        for name, rows in _ROWS[spec.lattice].items():
-            for k in rows:
-                s[k] = rates[name]
+        if spec.lattice == 27:
+            p.cm_rates = (ctypes.c_double * 5)(*[rates[n] for n in CM_RATE_NAMES])
+        else:
+            for name, rows in _ROWS[spec.lattice].items():
+                for k in rows:
+                    s[k] = rates[name]
         p.s = (ctypes.c_double * 19)(*s)
         sT = [0.0] * 7
         if spec.thermal:
@@ -181,7 +189,7 @@ class Problem:
         self.p = p
         self.Q = spec.lattice
         self.QT = spec.thermal
-        self.dim = 3 if spec.lattice == 19 else 2
+        self.dim = 2 if spec.lattice == 9 else 3
         self.wshape = (wz, wy, wx)
         self.window = window
         _check(_load().oracle_check(ctypes.byref(p)), "check")
@@ -257,15 +265,16 @@ def diagnostics(prob: Problem, f, g):
 
 
 def lattice(kind: int):
-    """(c[Q,3], w[Q] or None, M[Q,Q]) as the oracle builds them for kind 19, 9, 7 or 5."""
+    """(c[Q,3], w[Q] or None, M[Q,Q]) as the oracle builds them for kind 27, 19, 9, 7 or 5
+    (M is zero for 27, whose central-moment matrix depends on u)."""
     Q = ctypes.c_int(0)
-    c = (ctypes.c_int * 57)()
-    w = np.zeros(19)
-    M = np.zeros(19 * 19)
+    c = (ctypes.c_int * 81)()
+    w = np.zeros(27)
+    M = np.zeros(27 * 27)
     _check(_load().oracle_lattice(kind, ctypes.byref(Q), c, _dptr(w), _dptr(M)), "lattice")
     q = Q.value
     cc = np.array(c[:3 * q], dtype=np.int64).reshape(q, 3)
-    return cc, (w[:q].copy() if kind in (9, 19) else None), M[:q * q].reshape(q, q).copy()
+    return cc, (w[:q].copy() if kind in (9, 19, 27) else None), M[:q * q].reshape(q, q).copy()
 
 
 def max_threads() -> int:

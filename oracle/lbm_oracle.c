@@ -26,6 +26,19 @@
  * when its source lies outside the domain through a WALL face or is a solid cell; solid
  * links are adiabatic for g; the momentum exchange is the sum of 2 f_i+ c_i over links
  * from fluid cells into solid cells (domain faces excluded).
+ *
+ * D3Q27 central-moment MRT ("GPU Optimization for High-Quality Kinetic Fluid Simulation",
+ * Sec. 3.1: the D3Q27 lattice of Fig. 2 and Omega = -M^-1 D (m - m_eq) of Eq. 5, where M is
+ * a central-moment matrix; the adaptive rates of its refs. [1, 2] are not available, so the
+ * rates are fixed inputs).  Readings: M(u) has the rows prod_a (c_a - u_a)^e_a for
+ * e in {0,1,2}^3, except that the second-order normal rows are taken as xx - yy, xx - zz
+ * (relaxed with the shear rate 1/tau, like xy, xz, yz) and xx + yy + zz (bulk rate); the
+ * third- to sixth-order rows each take their order's rate; rows of order 0 and 1 are
+ * conserved.  The equilibrium is the product form rho prod_a phi(c_a, u_a) with
+ * phi(0, u) = 2/3 - u^2 and phi(+-1, u) = (1/3 + u^2 +- u)/2, whose central moments are those
+ * of a Maxwellian, rho prod_a (1, 0, 1/3)[e_a].  The force enters as Guo's does on the other
+ * lattices: the source is (F/rho) . d f_eq / du, mapped through M^-1 (I - D/2) M, with
+ * u = (j + F/2)/rho.  M(u) f = m is inverted by Gaussian elimination.
  */
 #include "lbm_oracle.h"
 
@@ -36,7 +49,7 @@
 #include <omp.h>
 #endif
 
-#define QMAX 19
+#define QMAX 27
 
 typedef struct {
     int Q;
@@ -61,6 +74,17 @@ static const int C_D3Q19[19][3] = {
 /* D2Q9: rest, +x, +y, -x, -y, (+,+), (-,+), (-,-), (+,-); with this order f2, f5, f6
  * cross the top face and f4, f7, f8 the bottom face, as the multi-GPU thermal page's
  * halo description (Sec. 3.1, Fig. 3(b)) requires. */
+/* D3Q27: the D3Q19 order, then the corners (+,+,+), (-,+,+), (+,-,+), (-,-,+), (+,+,-),
+ * (-,+,-), (+,-,-), (-,-,-). */
+static const int C_D3Q27[27][3] = {
+    {0, 0, 0},
+    {1, 0, 0}, {-1, 0, 0}, {0, 1, 0}, {0, -1, 0}, {0, 0, 1}, {0, 0, -1},
+    {1, 1, 0}, {-1, 1, 0}, {1, -1, 0}, {-1, -1, 0},
+    {1, 0, 1}, {-1, 0, 1}, {1, 0, -1}, {-1, 0, -1},
+    {0, 1, 1}, {0, -1, 1}, {0, 1, -1}, {0, -1, -1},
+    {1, 1, 1}, {-1, 1, 1}, {1, -1, 1}, {-1, -1, 1},
+    {1, 1, -1}, {-1, 1, -1}, {1, -1, -1}, {-1, -1, -1}};
+
 static const int C_D2Q9[9][3] = {
     {0, 0, 0}, {1, 0, 0}, {0, 1, 0}, {-1, 0, 0}, {0, -1, 0},
     {1, 1, 0}, {-1, 1, 0}, {-1, -1, 0}, {1, -1, 0}};
@@ -143,6 +167,7 @@ static int make_lattice(int kind, lattice_t *L)
     const int(*c)[3];
     switch (kind) {
     case 19: L->Q = 19; c = C_D3Q19; break;
+    case 27: L->Q = 27; c = C_D3Q27; break;
     case 9: L->Q = 9; c = C_D2Q9; break;
     case 7: L->Q = 7; c = C_D3Q7; break;
     case 5: L->Q = 5; c = C_D2Q5; break;
@@ -161,7 +186,12 @@ static int make_lattice(int kind, lattice_t *L)
         const int c2 = c[q][0] * c[q][0] + c[q][1] * c[q][1] + c[q][2] * c[q][2];
         if (kind == 19) L->w[q] = (c2 == 0) ? 1.0 / 3.0 : (c2 == 1) ? 1.0 / 18.0 : 1.0 / 36.0;
         if (kind == 9) L->w[q] = (c2 == 0) ? 4.0 / 9.0 : (c2 == 1) ? 1.0 / 9.0 : 1.0 / 36.0;
+        /* D3Q27: product of the D1Q3 weights 2/3 (rest) and 1/6 (moving) */
+        if (kind == 27)
+            L->w[q] = (c2 == 0) ? 8.0 / 27.0 : (c2 == 1) ? 2.0 / 27.0 : (c2 == 2) ? 1.0 / 54.0
+                                                                             : 1.0 / 216.0;
     }
+    if (kind == 27) return 0;   /* the central-moment matrix depends on u: built per cell */
     for (int k = 0; k < Q; ++k)
         for (int q = 0; q < Q; ++q) {
             if (kind == 19) L->M[k][q] = row_d3q19(k, c[q]);
@@ -194,8 +224,35 @@ typedef struct {
     long W;
 } ctx_t;
 
+/* Exponents (e_x, e_y, e_z) of the D3Q27 central-moment rows.  Rows 7, 8, 9 are the
+ * recombined second-order normal moments xx - yy, xx - zz, xx + yy + zz (see cm_row). */
+static const int CM_EXP[27][3] = {
+    {0, 0, 0},
+    {1, 0, 0}, {0, 1, 0}, {0, 0, 1},
+    {1, 1, 0}, {1, 0, 1}, {0, 1, 1},
+    {2, 0, 0}, {0, 2, 0}, {0, 0, 2},
+    {1, 2, 0}, {1, 0, 2}, {2, 1, 0}, {0, 1, 2}, {2, 0, 1}, {0, 2, 1}, {1, 1, 1},
+    {2, 2, 0}, {2, 0, 2}, {0, 2, 2}, {2, 1, 1}, {1, 2, 1}, {1, 1, 2},
+    {2, 2, 1}, {2, 1, 2}, {1, 2, 2},
+    {2, 2, 2}};
+
+/* Rate of D3Q27 central-moment row k: 0 for the conserved orders 0 and 1, the shear rate
+ * for xy, xz, yz, xx - yy, xx - zz, the bulk rate for xx + yy + zz, then one rate per
+ * order (rows 10-16: third, 17-22: fourth, 23-25: fifth, 26: sixth). */
+static double cm_rate(const oracle_problem *p, int k)
+{
+    if (k < 4) return 0.0;
+    if (k < 9) return 1.0 / p->tau;
+    if (k == 9) return p->cm_rates[0];
+    if (k < 17) return p->cm_rates[1];
+    if (k < 23) return p->cm_rates[2];
+    if (k < 26) return p->cm_rates[3];
+    return p->cm_rates[4];
+}
+
 static int is_conserved_row(int lattice, int k)
 {
+    if (lattice == 27) return k < 4;
     if (lattice == 19) return k == 0 || k == 3 || k == 5 || k == 7;
     return k == 0 || k == 3 || k == 5;
 }
@@ -203,11 +260,18 @@ static int is_conserved_row(int lattice, int k)
 int oracle_check(const oracle_problem *p)
 {
     if (!p) return -1;
-    if (p->lattice != 19 && p->lattice != 9) return -2;
+    if (p->lattice != 19 && p->lattice != 9 && p->lattice != 27) return -2;
     if (p->thermal != 0 && !((p->lattice == 19 && p->thermal == 7) ||
                              (p->lattice == 9 && p->thermal == 5)))
         return -3;
-    if (p->collision != ORC_BGK && p->collision != ORC_MRT) return -4;
+    if (p->lattice == 27 ? p->collision != ORC_CM
+                         : (p->collision != ORC_BGK && p->collision != ORC_MRT))
+        return -4;
+    if (p->lattice == 27) {
+        if (!(p->tau > 0.5)) return -9;
+        for (int k = 0; k < 5; ++k)
+            if (!(p->cm_rates[k] > 0.0 && p->cm_rates[k] < 2.0)) return -13;
+    }
     if (p->nx < 1 || p->ny < 1 || p->nz < 1) return -5;
     if (p->lattice == 9 && p->nz != 1) return -6;
     if (p->wx < 1 || p->wy < 1 || p->wz < 1) return -7;
@@ -232,7 +296,10 @@ static int make_ctx(const oracle_problem *p, ctx_t *C)
     C->p = p;
     if (make_lattice(p->lattice, &C->F)) return -20;
     if (p->thermal && make_lattice(p->thermal, &C->G)) return -21;
-    for (int k = 0; k < C->F.Q; ++k) C->s[k] = is_conserved_row(p->lattice, k) ? 0.0 : p->s[k];
+    for (int k = 0; k < C->F.Q; ++k)
+        C->s[k] = is_conserved_row(p->lattice, k) ? 0.0
+                  : (p->lattice == 27)           ? cm_rate(p, k)
+                                                 : p->s[k];
     for (int k = 0; k < C->G.Q; ++k) C->sT[k] = (k == 0) ? 0.0 : p->s_T[k];
     /* anti-bounce-back weight as the thermal page prints it */
     if (p->thermal == 5) C->omega = (4.0 + p->a_T) / 10.0;
@@ -253,9 +320,25 @@ static void body_force(const ctx_t *C, double rho, double T, double F[3])
     if (p->thermal) F[p->up_axis] += rho * p->gbeta * (T - p->T0);
 }
 
-/* Quadratic equilibrium f_eq_q = w_q rho (1 + 3 c.u + 9/2 (c.u)^2 - 3/2 u.u). */
+/* D1Q3 factor of the D3Q27 product equilibrium: its zeroth, first and second moments are
+ * 1, u and 1/3 + u^2, those of a Maxwellian with c_s^2 = 1/3. */
+static double phi(int c, double u)
+{
+    return c == 0 ? 2.0 / 3.0 - u * u : 0.5 * (1.0 / 3.0 + u * u + c * u);
+}
+
+/* d phi / du */
+static double dphi(int c, double u) { return c == 0 ? -2.0 * u : u + 0.5 * c; }
+
+/* Equilibrium.  D3Q27: the product form rho prod_a phi(c_a, u_a).  Otherwise the quadratic
+ * f_eq_q = w_q rho (1 + 3 c.u + 9/2 (c.u)^2 - 3/2 u.u). */
 static void f_equilibrium(const lattice_t *L, double rho, const double u[3], double *feq)
 {
+    if (L->Q == 27) {
+        for (int q = 0; q < 27; ++q)
+            feq[q] = rho * phi(L->c[q][0], u[0]) * phi(L->c[q][1], u[1]) * phi(L->c[q][2], u[2]);
+        return;
+    }
     const double uu = u[0] * u[0] + u[1] * u[1] + u[2] * u[2];
     for (int q = 0; q < L->Q; ++q) {
         const double cu = L->c[q][0] * u[0] + L->c[q][1] * u[1] + L->c[q][2] * u[2];
@@ -286,15 +369,79 @@ static void g_equilibrium(const ctx_t *C, double T, const double u[3], double *g
     }
 }
 
-/* Guo's source in velocity space: F~_q = w_q [3 (c_q - u) + 9 (c_q.u) c_q] . F */
+/* Guo's source in velocity space: F~_q = w_q [3 (c_q - u) + 9 (c_q.u) c_q] . F, which is
+ * (F/rho) . d f_eq / du of the quadratic equilibrium.  D3Q27: (F/rho) . d f_eq / du of the
+ * product form. */
 static void guo_source(const lattice_t *L, const double u[3], const double F[3], double *Ft)
 {
+    if (L->Q == 27) {
+        for (int q = 0; q < 27; ++q) {
+            const int *c = L->c[q];
+            const double px = phi(c[0], u[0]), py = phi(c[1], u[1]), pz = phi(c[2], u[2]);
+            Ft[q] = F[0] * dphi(c[0], u[0]) * py * pz + F[1] * px * dphi(c[1], u[1]) * pz +
+                    F[2] * px * py * dphi(c[2], u[2]);
+        }
+        return;
+    }
     for (int q = 0; q < L->Q; ++q) {
         const double cu = L->c[q][0] * u[0] + L->c[q][1] * u[1] + L->c[q][2] * u[2];
         double v = 0.0;
         for (int a = 0; a < 3; ++a) v += (3.0 * (L->c[q][a] - u[a]) + 9.0 * cu * L->c[q][a]) * F[a];
         Ft[q] = L->w[q] * v;
     }
+}
+
+/* Central moment of velocity c about u with exponents e: prod_a (c_a - u_a)^e_a. */
+static double cmono(const int *c, const double u[3], const int *e)
+{
+    double v = 1.0;
+    for (int a = 0; a < 3; ++a)
+        for (int n = 0; n < e[a]; ++n) v *= c[a] - u[a];
+    return v;
+}
+
+/* Entry (k, c) of the central-moment matrix M(u). */
+static double cm_row(int k, const int *c, const double u[3])
+{
+    static const int XX[3] = {2, 0, 0}, YY[3] = {0, 2, 0}, ZZ[3] = {0, 0, 2};
+    if (k == 7) return cmono(c, u, XX) - cmono(c, u, YY);
+    if (k == 8) return cmono(c, u, XX) - cmono(c, u, ZZ);
+    if (k == 9) return cmono(c, u, XX) + cmono(c, u, YY) + cmono(c, u, ZZ);
+    return cmono(c, u, CM_EXP[k]);
+}
+
+/* Solve A x = b for n <= QMAX by Gaussian elimination with partial pivoting (A and b are
+ * overwritten).  Returns -1 on a singular matrix. */
+static int solve_dense(int n, double A[][QMAX], double *b, double *x)
+{
+    for (int col = 0; col < n; ++col) {
+        int piv = col;
+        for (int r = col + 1; r < n; ++r)
+            if (fabs(A[r][col]) > fabs(A[piv][col])) piv = r;
+        if (A[piv][col] == 0.0) return -1;
+        if (piv != col) {
+            for (int k = 0; k < n; ++k) {
+                const double t = A[col][k];
+                A[col][k] = A[piv][k];
+                A[piv][k] = t;
+            }
+            const double t = b[col];
+            b[col] = b[piv];
+            b[piv] = t;
+        }
+        for (int r = col + 1; r < n; ++r) {
+            const double m = A[r][col] / A[col][col];
+            if (m == 0.0) continue;
+            for (int k = col; k < n; ++k) A[r][k] -= m * A[col][k];
+            b[r] -= m * b[col];
+        }
+    }
+    for (int r = n - 1; r >= 0; --r) {
+        double v = b[r];
+        for (int k = r + 1; k < n; ++k) v -= A[r][k] * x[k];
+        x[r] = v / A[r][r];
+    }
+    return 0;
 }
 
 /* Collide one fluid cell: fin/gin -> fout/gout (post-collision).  Fext: additional force
@@ -321,7 +468,27 @@ static void collide_cell(const ctx_t *C, const double *fin, const double *gin, d
     double feq[QMAX], Ft[QMAX];
     f_equilibrium(L, rho, u, feq);
     guo_source(L, u, F, Ft);
-    if (C->p->collision == ORC_BGK) {
+    if (C->p->collision == ORC_CM) {
+        /* m = M(u) f, relax each row toward m_eq = M(u) f_eq with its rate, add
+         * (I - D/2) M(u) F~, and solve M(u) f_out = m_post */
+        double A[QMAX][QMAX], m[QMAX], meq[QMAX], mF[QMAX], mpost[QMAX];
+        for (int k = 0; k < Q; ++k) {
+            double a = 0.0, b = 0.0, d = 0.0;
+            for (int q = 0; q < Q; ++q) {
+                A[k][q] = cm_row(k, L->c[q], u);
+                a += A[k][q] * fin[q];
+                b += A[k][q] * feq[q];
+                d += A[k][q] * Ft[q];
+            }
+            m[k] = a;
+            meq[k] = b;
+            mF[k] = d;
+        }
+        for (int k = 0; k < Q; ++k)
+            mpost[k] = m[k] - C->s[k] * (m[k] - meq[k]) + (1.0 - 0.5 * C->s[k]) * mF[k];
+        if (solve_dense(Q, A, mpost, fout))
+            for (int q = 0; q < Q; ++q) fout[q] = NAN;
+    } else if (C->p->collision == ORC_BGK) {
         const double tau = C->p->tau;
         for (int q = 0; q < Q; ++q)
             fout[q] = fin[q] - (fin[q] - feq[q]) / tau + (1.0 - 1.0 / (2.0 * tau)) * Ft[q];
@@ -431,7 +598,7 @@ static int ib_forces(const ctx_t *C, const double *f, const double *g, double *F
 {
     const oracle_problem *p = C->p;
     const long W = C->W;
-    const int dim = (p->lattice == 19) ? 3 : 2;
+    const int dim = (p->lattice != 9) ? 3 : 2;
     for (long n = 0; n < 3 * W; ++n) Fib[n] = 0.0;
     double total[3] = {0, 0, 0}, torque[3] = {0, 0, 0}, centre[3] = {0, 0, 0};
     for (int s = 0; s < p->ib_n; ++s)
@@ -520,7 +687,7 @@ int oracle_init_equilibrium(const oracle_problem *p, const double *rho, const do
             for (int q = 0; q < C.G.Q; ++q) g[q * W + n] = 0.0;
             continue;
         }
-        const double un[3] = {u[n], u[W + n], (p->lattice == 19) ? u[2 * W + n] : 0.0};
+        const double un[3] = {u[n], u[W + n], (p->lattice != 9) ? u[2 * W + n] : 0.0};
         f_equilibrium(&C.F, rho[n], un, feq);
         for (int q = 0; q < C.F.Q; ++q) f[q * W + n] = feq[q];
         if (p->thermal) {
@@ -672,7 +839,7 @@ int oracle_macroscopic(const oracle_problem *p, const double *f, const double *g
     int rc = make_ctx(p, &C);
     if (rc) return rc;
     const long W = C.W;
-    const int dim = (p->lattice == 19) ? 3 : 2;
+    const int dim = (p->lattice != 9) ? 3 : 2;
 #pragma omp parallel for schedule(static)
     for (long n = 0; n < W; ++n) {
         if (is_solid(&C, n)) {
@@ -718,7 +885,7 @@ int oracle_diagnostics(const oracle_problem *p, const double *f, const double *g
                 /* cells next to a Dirichlet face: wall gradient over the half cell */
                 const int gc[3] = {p->x0 + i, p->y0 + j, p->z0 + k};
                 const int ext[3] = {p->nx, p->ny, p->nz};
-                const int dim = (p->lattice == 19) ? 3 : 2;
+                const int dim = (p->lattice != 9) ? 3 : 2;
                 for (int a = 0; a < dim; ++a) {
                     const int lo = 2 * a, hi = 2 * a + 1;
                     if (gc[a] == 0 && p->face_flow[lo] == ORC_WALL && p->face_T[lo] == ORC_DIRICHLET)

@@ -15,6 +15,13 @@
  * "GPU lattice Boltzmann: streaming layout and performance" (two-buffer scheme: collide,
  * then pull into the other buffer).
  *
+ * D3Q27 central-moment MRT ("GPU Optimization for High-Quality Kinetic Fluid Simulation",
+ * Sec. 3.1 Eq. 5 with the D3Q27 lattice of Fig. 2, fixed rates): the moments are the 27
+ * central moments prod_a (c_a - u_a)^e_a, e in {0,1,2}^3, with the three second-order
+ * normal moments recombined as xx - yy, xx - zz (shear) and xx + yy + zz (bulk); the
+ * equilibrium is the product form f_eq = rho prod_a phi(c_a, u_a) whose central moments are
+ * rho prod_a (1, 0, 1/3)[e_a]; the force source is (F/rho) . d f_eq / du.
+ *
  * Layout: structure of arrays, x fastest: f[q*W + i + wx*(j + wy*k)] where W = wx*wy*wz is
  * the number of cells the run holds (a window of the whole nx*ny*nz domain; the window is
  * the whole domain in an ordinary run).  A population whose pull source lies inside the
@@ -28,19 +35,21 @@
 extern "C" {
 #endif
 
-enum { ORC_D2Q9 = 9, ORC_D3Q19 = 19 };
+enum { ORC_D2Q9 = 9, ORC_D3Q19 = 19, ORC_D3Q27 = 27 };
 enum { ORC_THERMAL_NONE = 0, ORC_D2Q5 = 5, ORC_D3Q7 = 7 };
-enum { ORC_BGK = 0, ORC_MRT = 1 };
+enum { ORC_BGK = 0, ORC_MRT = 1, ORC_CM = 2 };
 enum { ORC_PERIODIC = 0, ORC_WALL = 1 };
 enum { ORC_ADIABATIC = 0, ORC_DIRICHLET = 1 };
 
 typedef struct {
-    int lattice;          /* ORC_D2Q9 or ORC_D3Q19 */
+    int lattice;          /* ORC_D2Q9, ORC_D3Q19 or ORC_D3Q27 */
     int thermal;          /* ORC_THERMAL_NONE, ORC_D2Q5 (with D2Q9), ORC_D3Q7 (with D3Q19) */
-    int collision;        /* ORC_BGK or ORC_MRT (momentum lattice) */
-    double tau;           /* BGK relaxation time */
+    int collision;        /* ORC_BGK or ORC_MRT (D2Q9, D3Q19); ORC_CM (D3Q27) */
+    double tau;           /* BGK relaxation time; CM: 1/tau is the shear rate */
     double s[19];         /* MRT rate of each moment row; rows of conserved moments ignored */
     double s_T[7];        /* thermal MRT rate of each row; row 0 (T) ignored */
+    double cm_rates[5];   /* CM rates: trace of the second-order moments (bulk), then the
+                             third-, fourth-, fifth- and sixth-order central moments */
     double a_T;           /* thermal energy-moment constant: e_eq = a_T * T */
     double g_body[3];     /* body acceleration: F += rho * g_body */
     double gbeta;         /* buoyancy: F += rho * gbeta * (T - T0) along up_axis */
