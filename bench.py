@@ -39,7 +39,7 @@ METRIC = "MLUPS at 1 GB300 (D3Q19 MRT fp32, AA) and % of HBM bandwidth roofline"
 UNIT = "MLUPS"
 
 # Algorithmic bytes per cell update: populations read once and written once, fp32.
-BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112}
+BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112, (27, 0): 216}
 
 # DRAM bytes per cell update of the step kernel measured with ncu (dram__bytes_read.sum +
 # dram__bytes_write.sum per launch / cells), with a hash of the kernel sources they were
@@ -78,6 +78,9 @@ def make_workload(name: str):
         "cavity2d_4096": lambda: W.cavity2d(),
         "cavity2d_2048": lambda: W.cavity2d(n=2048),
         "cavity3d_512": lambda: W.cavity3d(),
+        "d3q27_cm_periodic_512": lambda: W.random_periodic(n=512, seed=2, lattice=27),
+        "d3q27_cm_periodic_256": lambda: W.random_periodic(n=256, seed=2, lattice=27),
+        "channel_sphere_d3q27_128": lambda: W.channel_sphere(lattice=27),
     }
     return table[name]()
 
@@ -436,7 +439,8 @@ def run_gpu(args, dctx):
     if not args.no_secondary:
         _WORKLOAD_CACHE[args.workload] = w
         runs = [("cavity3d_512", "aa"), ("cavity2d_4096", "aa"), ("taylor_green_32", "aa"),
-                ("channel_ib_sphere_128", "aa")]
+                ("channel_ib_sphere_128", "aa"), ("d3q27_cm_periodic_512", "aa"),
+                ("channel_sphere_d3q27_128", "aa")]
         # the streaming-layout page's comparison: in place vs two buffers
         for n in ("d3q19_mrt_periodic_128", "channel_sphere_128", args.workload):
             runs += [(n, "aa"), (n, "pull"), (n, "split")]

@@ -1,9 +1,9 @@
 /*
  * lbm.h -- C ABI of the GB300 (sm_103a) lattice-Boltzmann collide-and-stream library.
  *
- * One library call advances a lattice-Boltzmann flow (D3Q19 or D2Q9 populations, BGK or
- * MRT collision, Guo forcing with Boussinesq buoyancy, optional D3Q7 / D2Q5 thermal
- * populations) by n time steps, one fused kernel launch per step, populations streamed in
+ * One library call advances a lattice-Boltzmann flow (D3Q19 or D2Q9 populations with BGK
+ * or MRT collision, or D3Q27 populations with central-moment MRT; Guo forcing with
+ * Boussinesq buoyancy; optional D3Q7 / D2Q5 thermal populations) by n time steps, one fused kernel launch per step, populations streamed in
  * place with the AA pattern in a single fp32 structure-of-arrays buffer.
  *
  * Sources (the method each call implements):
@@ -21,7 +21,8 @@
  *          momentum exchange read back from the last step of a submission.
  *   [KFS]  "GPU Optimization for High-Quality Kinetic Fluid Simulation", Sec. 3.1,
  *          Eq. 1-5 (lattice Boltzmann equation, moments, pull streaming, MRT collision
- *          Omega = -M^-1 D (m - m_eq)); Sec. 4 (SoA layout, bounce-back at solid nodes).
+ *          Omega = -M^-1 D (m - m_eq)); Fig. 2 (the D3Q27 lattice, central moments);
+ *          Sec. 4 (SoA layout, bounce-back at solid nodes).
  *
  * Conventions shared by every call:
  *   - Memory.  The caller owns all device memory: it allocates one device workspace of
@@ -47,6 +48,8 @@
  *   D3Q19: 0 rest; 1 +x, 2 -x, 3 +y, 4 -y, 5 +z, 6 -z; 7 (+,+,0), 8 (-,+,0), 9 (+,-,0),
  *          10 (-,-,0); 11 (+,0,+), 12 (-,0,+), 13 (+,0,-), 14 (-,0,-); 15 (0,+,+),
  *          16 (0,-,+), 17 (0,+,-), 18 (0,-,-).
+ *   D3Q27: 0-18 as D3Q19; 19 (+,+,+), 20 (-,+,+), 21 (+,-,+), 22 (-,-,+), 23 (+,+,-),
+ *          24 (-,+,-), 25 (+,-,-), 26 (-,-,-).
  *   D2Q9:  0 rest; 1 +x, 2 +y, 3 -x, 4 -y, 5 (+,+), 6 (-,+), 7 (-,-), 8 (+,-).
  *   D3Q7:  0 rest; 1 +x, 2 -x, 3 +y, 4 -y, 5 +z, 6 -z.   D2Q5: 0 rest; 1 +x, 2 +y, 3 -x, 4 -y.
  * Moment rows (index of s[] / s_T[]):
@@ -57,6 +60,14 @@
  *   D2Q5: 0 T, 1 jx, 2 jy, 3 e (rest weight -4), 4 (0,1,-1,1,-1).
  *   Rates of conserved rows (rho, j; T) are ignored.  Viscosity nu = (1/s_nu - 1/2)/3 on
  *   the stress rows; thermal diffusivity kappa = omega (1/s_kappa - 1/2) on the j rows.
+ *   D3Q27 central moments (LBM_CM): the 27 moments prod_a (c_a - u_a)^e_a, e in {0,1,2}^3,
+ *          about u = (j + F/2)/rho, with the second-order normal ones taken as xx - yy,
+ *          xx - zz (shear rate 1/tau, like xy, xz, yz; nu = (tau - 1/2)/3) and xx + yy + zz
+ *          (rate cm_rates[0]); orders 3, 4, 5, 6 relax at cm_rates[1..4]; orders 0, 1 are
+ *          conserved.  Equilibrium central moments rho prod_a (1, 0, 1/3)[e_a] (discrete
+ *          form: the product rho prod_a phi(c_a, u_a), phi(0, u) = 2/3 - u^2,
+ *          phi(+-1, u) = (1/3 + u^2 +- u)/2, also the initial state); the force enters as
+ *          the central moments of (F/rho) . d f_eq / du, relaxed with (I - D/2).
  */
 #ifndef LBM_GB300_H
 #define LBM_GB300_H
@@ -80,9 +91,10 @@ typedef enum {
     LBM_ERR_STATE = 6        /* call out of order (e.g. stepping before any init)   */
 } lbm_status;
 
-enum { LBM_D2Q9 = 9, LBM_D3Q19 = 19 };
+enum { LBM_D2Q9 = 9, LBM_D3Q19 = 19, LBM_D3Q27 = 27 };
 enum { LBM_THERMAL_NONE = 0, LBM_D2Q5 = 5, LBM_D3Q7 = 7 };
-enum { LBM_BGK = 0, LBM_MRT = 1 };
+/* LBM_CM: central-moment MRT, D3Q27 only (and the only collision of D3Q27) */
+enum { LBM_BGK = 0, LBM_MRT = 1, LBM_CM = 2 };
 enum { LBM_FACE_PERIODIC = 0, LBM_FACE_WALL = 1 };        /* flow: half-way bounce-back */
 /* A slab face: the context is one slab of a larger domain, split along its outer axis (z
  * in 3-D, y in 2-D).  The grid then includes one ghost plane at each HALO face (the first /
@@ -104,12 +116,15 @@ enum { LBM_STREAM_AA = 0, LBM_STREAM_PULL = 1, LBM_STREAM_SPLIT = 2 };
  * (DIRICHLET face, wall temperature T_wall[face]). */
 typedef struct {
     int nx, ny, nz;       /* cells; nz == 1 for D2Q9; nx*ny*nz < 2^31                  */
-    int lattice;          /* LBM_D3Q19 or LBM_D2Q9                                     */
+    int lattice;          /* LBM_D3Q19, LBM_D2Q9 or LBM_D3Q27                          */
     int thermal;          /* LBM_THERMAL_NONE, LBM_D3Q7 (with D3Q19), LBM_D2Q5 (D2Q9)  */
-    int collision;        /* LBM_BGK or LBM_MRT (momentum populations)                 */
-    double tau;           /* BGK relaxation time, > 1/2                                */
+    int collision;        /* LBM_BGK or LBM_MRT (D3Q19, D2Q9); LBM_CM (D3Q27)           */
+    double tau;           /* BGK relaxation time, > 1/2; LBM_CM: 1/tau = shear rate    */
     double s[19];         /* MRT rate of each moment row, in [0, 2)                    */
     double s_T[7];        /* thermal MRT rate of each row, in [0, 2)                   */
+    double cm_rates[5];   /* LBM_CM: bulk rate, then orders 3, 4, 5, 6; each in (0, 2).
+                             D3Q27 takes no thermal lattice, no immersed-boundary
+                             samples and only LBM_STREAM_AA (LBM_ERR_UNSUPPORTED).     */
     double a_T;           /* thermal energy-moment constant (e_eq = a_T T), in (-Q_T+1, 1) */
     double g_body[3];     /* body acceleration: F += rho g_body                        */
     double gbeta, T0;     /* buoyancy: F += rho gbeta (T - T0) e_up (thermal only)      */

@@ -18,9 +18,9 @@ LBM_ERR_CUDA, LBM_ERR_NONFINITE, LBM_ERR_STATE = 4, 5, 6
 STATUS_NAMES = {0: "LBM_OK", 1: "LBM_ERR_ARG", 2: "LBM_ERR_UNSUPPORTED",
                 3: "LBM_ERR_WORKSPACE", 4: "LBM_ERR_CUDA", 5: "LBM_ERR_NONFINITE",
                 6: "LBM_ERR_STATE"}
-LBM_D2Q9, LBM_D3Q19 = 9, 19
+LBM_D2Q9, LBM_D3Q19, LBM_D3Q27 = 9, 19, 27
 LBM_THERMAL_NONE, LBM_D2Q5, LBM_D3Q7 = 0, 5, 7
-LBM_BGK, LBM_MRT = 0, 1
+LBM_BGK, LBM_MRT, LBM_CM = 0, 1, 2
 LBM_FACE_PERIODIC, LBM_FACE_WALL, LBM_FACE_HALO = 0, 1, 2
 LBM_HALO_FILL, LBM_HALO_DRAIN = 0, 1
 LBM_TFACE_ADIABATIC, LBM_TFACE_DIRICHLET = 0, 1
@@ -39,6 +39,7 @@ class lbm_config(ctypes.Structure):
         ("nx", ctypes.c_int), ("ny", ctypes.c_int), ("nz", ctypes.c_int),
         ("lattice", ctypes.c_int), ("thermal", ctypes.c_int), ("collision", ctypes.c_int),
         ("tau", ctypes.c_double), ("s", ctypes.c_double * 19), ("s_T", ctypes.c_double * 7),
+        ("cm_rates", ctypes.c_double * 5),
         ("a_T", ctypes.c_double), ("g_body", ctypes.c_double * 3),
         ("gbeta", ctypes.c_double), ("T0", ctypes.c_double), ("up_axis", ctypes.c_int),
         ("face_flow", ctypes.c_int * 6), ("face_T", ctypes.c_int * 6),

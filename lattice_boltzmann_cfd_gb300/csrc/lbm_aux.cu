@@ -7,15 +7,17 @@
 namespace lbm {
 namespace {
 
-template <class F3, class F2>
-cudaError_t by_lattice(int lattice, int thermal, F3 &&f3, F2 &&f2)
+// Call fn(L{}, TL{}) with the momentum and thermal lattice types of a context.
+template <class Fn>
+cudaError_t by_lattice(int lattice, int thermal, Fn &&fn)
 {
     if (lattice == 19) {
-        if (thermal == 7) return f3(D3Q7{});
-        return f3(NoThermal{});
+        if (thermal == 7) return fn(D3Q19{}, D3Q7{});
+        return fn(D3Q19{}, NoThermal{});
     }
-    if (thermal == 5) return f2(D2Q5{});
-    return f2(NoThermal{});
+    if (lattice == 27) return fn(D3Q27{}, NoThermal{});
+    if (thermal == 5) return fn(D2Q9{}, D2Q5{});
+    return fn(D2Q9{}, NoThermal{});
 }
 
 Shape shape_of(const Params &P) { return cell_shape(P.nx, P.ny, P.nz); }
@@ -37,31 +39,25 @@ cudaError_t init_go(int pat, const Params &P, const float *rho, const float *u, 
 cudaError_t launch_init(int lattice, int thermal, int pat, const Params &P, const float *rho,
                         const float *u, const float *T, cudaStream_t s)
 {
-    return by_lattice(
-        lattice, thermal,
-        [&](auto tl) { return init_go<D3Q19, decltype(tl)>(pat, P, rho, u, T, s); },
-        [&](auto tl) { return init_go<D2Q9, decltype(tl)>(pat, P, rho, u, T, s); });
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        return init_go<decltype(l), decltype(tl)>(pat, P, rho, u, T, s);
+    });
 }
 
 cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t *solid,
                         uint32_t *mask, cudaStream_t s)
 {
     const Shape sh = shape_of(P);
-    return by_lattice(
-        lattice, thermal,
-        [&](auto tl) {
-            mask_kernel<D3Q19, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, solid, mask);
-            return cudaGetLastError();
-        },
-        [&](auto tl) {
-            mask_kernel<D2Q9, decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, solid, mask);
-            return cudaGetLastError();
-        });
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        mask_kernel<decltype(l), decltype(tl)><<<sh.grid, sh.block, 0, s>>>(P, solid, mask);
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s)
 {
     if (P.ib_n <= 0) return cudaSuccess;
+    if (lattice == 27) return cudaErrorNotSupported;   // rejected at create
     const int corners = lattice == 19 ? 8 : 4;
     const long long threads = (long long)P.ib_n * corners;
     const dim3 b(128), g((unsigned)((threads + 127) / 128));
@@ -73,9 +69,8 @@ cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaSt
         else ib_kernel<L, TL, NATURAL><<<g, b, 0, s>>>(P);
         return cudaGetLastError();
     };
-    return by_lattice(
-        lattice, thermal, [&](auto tl) { return go(D3Q19{}, tl); },
-        [&](auto tl) { return go(D2Q9{}, tl); });
+    if (lattice == 19) return thermal == 7 ? go(D3Q19{}, D3Q7{}) : go(D3Q19{}, NoThermal{});
+    return thermal == 5 ? go(D2Q9{}, D2Q5{}) : go(D2Q9{}, NoThermal{});
 }
 
 cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
@@ -86,25 +81,19 @@ cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long lo
     if (e != cudaSuccess || P.ib_n <= 0) return e;
     const dim3 b(128), g((P.ib_n + 127) / 128);
     if (lattice == 19) ib_mark_kernel<D3Q19><<<g, b, 0, s>>>(P, mask);
-    else ib_mark_kernel<D2Q9><<<g, b, 0, s>>>(P, mask);
+    else if (lattice == 9) ib_mark_kernel<D2Q9><<<g, b, 0, s>>>(P, mask);
     return cudaGetLastError();
 }
 
 cudaError_t launch_halo(int lattice, int thermal, const Params &P, int side, int phase,
                         int unpack, float *buf, cudaStream_t s)
 {
-    const int plane_cells = lattice == 19 ? P.nx * P.ny : P.nx;
+    const int plane_cells = lattice == 9 ? P.nx : P.nx * P.ny;
     const dim3 b(256), g((plane_cells + 255) / 256);
-    return by_lattice(
-        lattice, thermal,
-        [&](auto tl) {
-            halo_kernel<D3Q19, decltype(tl)><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
-            return cudaGetLastError();
-        },
-        [&](auto tl) {
-            halo_kernel<D2Q9, decltype(tl)><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
-            return cudaGetLastError();
-        });
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        halo_kernel<decltype(l), decltype(tl)><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+        return cudaGetLastError();
+    });
 }
 
 namespace {
@@ -162,34 +151,28 @@ cudaError_t diag_go(bool masked, int pat, const Params &P, double *partial, doub
 cudaError_t launch_macro(int lattice, int thermal, bool masked, int pat, const Params &P,
                          float *rho, float *u, float *T, cudaStream_t s)
 {
-    return by_lattice(
-        lattice, thermal,
-        [&](auto tl) { return macro_go<D3Q19, decltype(tl)>(masked, pat, P, rho, u, T, s); },
-        [&](auto tl) { return macro_go<D2Q9, decltype(tl)>(masked, pat, P, rho, u, T, s); });
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        return macro_go<decltype(l), decltype(tl)>(masked, pat, P, rho, u, T, s);
+    });
 }
 
 cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
                        const Params &P, float *f, float *g, cudaStream_t s)
 {
-    return by_lattice(
-        lattice, thermal,
-        [&](auto tl) {
-            return set ? pop_go<D3Q19, decltype(tl), true>(masked, pat, P, f, g, s)
-                       : pop_go<D3Q19, decltype(tl), false>(masked, pat, P, f, g, s);
-        },
-        [&](auto tl) {
-            return set ? pop_go<D2Q9, decltype(tl), true>(masked, pat, P, f, g, s)
-                       : pop_go<D2Q9, decltype(tl), false>(masked, pat, P, f, g, s);
-        });
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        using L = decltype(l);
+        using TL = decltype(tl);
+        return set ? pop_go<L, TL, true>(masked, pat, P, f, g, s)
+                   : pop_go<L, TL, false>(masked, pat, P, f, g, s);
+    });
 }
 
 cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s)
 {
-    return by_lattice(
-        lattice, thermal,
-        [&](auto tl) { return diag_go<D3Q19, decltype(tl)>(masked, pat, P, partial, out, s); },
-        [&](auto tl) { return diag_go<D2Q9, decltype(tl)>(masked, pat, P, partial, out, s); });
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        return diag_go<decltype(l), decltype(tl)>(masked, pat, P, partial, out, s);
+    });
 }
 
 }  // namespace lbm

@@ -273,8 +273,11 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
                : lbm::launch_split_d2q9(th, coll, masked, narrow, P, sh, stream);
         break;
     default:
-        e = d3 ? lbm::launch_step_d3q19(th, coll, masked, parity != 0, narrow, P, sh, stream)
-               : lbm::launch_step_d2q9(th, coll, masked, parity != 0, narrow, P, sh, stream);
+        if (c->cfg.lattice == LBM_D3Q27)
+            e = lbm::launch_step_d3q27(masked, parity != 0, narrow, P, sh, stream);
+        else
+            e = d3 ? lbm::launch_step_d3q19(th, coll, masked, parity != 0, narrow, P, sh, stream)
+                   : lbm::launch_step_d2q9(th, coll, masked, parity != 0, narrow, P, sh, stream);
     }
     if (c->L.streaming != LBM_STREAM_AA) {
         std::swap(P.f, P.fo);
@@ -580,12 +583,14 @@ namespace {
 // Populations per plane cell that cross a slab face (momentum + thermal).
 int halo_directions(const lbm_ctx *c)
 {
-    return c->cfg.lattice == LBM_D3Q19 ? 5 + (c->L.QT ? 1 : 0) : 3 + (c->L.QT ? 1 : 0);
+    const int thermal = c->L.QT ? 1 : 0;
+    if (c->cfg.lattice == LBM_D3Q27) return 9;        // every c with c_outer = +-1
+    return c->cfg.lattice == LBM_D3Q19 ? 5 + thermal : 3 + thermal;
 }
 
 size_t halo_plane_cells(const lbm_ctx *c)
 {
-    return c->cfg.lattice == LBM_D3Q19 ? (size_t)c->cfg.nx * c->cfg.ny : (size_t)c->cfg.nx;
+    return c->cfg.lattice == LBM_D2Q9 ? (size_t)c->cfg.nx : (size_t)c->cfg.nx * c->cfg.ny;
 }
 
 lbm_status halo_call(lbm_ctx *c, int side, int phase, int unpack, const void *buf)

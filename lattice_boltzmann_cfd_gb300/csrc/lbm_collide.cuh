@@ -37,6 +37,7 @@ struct CollideParams {
     float gx, gy, gz;   // body acceleration
     float gbeta, T0;
     int up_axis;
+    float cm[5];    // D3Q27 central moments: bulk rate, then the rates of orders 3, 4, 5, 6
 };
 
 // Body force and force-shifted velocity ([TLBM] Sec. 2).  ext: an additional force on the
@@ -336,13 +337,161 @@ LBM_HD void collide_bgk(float (&f)[L::Q], float (&g)[TL::QA], const CollideParam
     }
 }
 
+// ------------------------------------------------- D3Q27 central-moment MRT ---------
+//
+// "GPU Optimization for High-Quality Kinetic Fluid Simulation", Sec. 3.1: D3Q27 (Fig. 2) and
+// Omega = -M^-1 D (m - m_eq) (Eq. 5) with central moments, at fixed rates:
+//   k_e = sum_q prod_a (c_qa - u_a)^e_a f_q,  e in {0,1,2}^3,  u = (j + F/2)/rho;
+//   k_eq = rho prod_a mu[e_a], mu = (1, 0, 1/3) (a Maxwellian's central moments);
+//   the source's central moments R_e = F_a prod_{b != a} mu[e_b] where e_a = 1;
+//   k+ = k - s (k - k_eq) + (1 - s/2) R, with s = 0 on orders 0 and 1, the shear rate on
+//   xy, xz, yz, xx - yy, xx - zz, the bulk rate on xx + yy + zz, one rate per order 3..6.
+// The lattice is the tensor product of three D1Q3 stencils, so M(u) factors into one
+// 3-point transform per axis: (f-, f0, f+) -> (sum f, sum (c-u) f, sum (c-u)^2 f), applied
+// along x, then y, then z to the 3x3x3 array of populations (27 x 8 flops each way instead
+// of a 27 x 27 product).  The transform runs on the shifted populations fbar = f - w; the
+// rest part's central moments, prod_a h[e_a] with h = (1, -u_a, 1/3 + u_a^2), enter the
+// deviation k - k_eq analytically, so every quantity carried in fp32 is deviation-sized.
+
+// (f-, f0, f+) -> (k0, k1, k2) about u, in place.
+LBM_HD void cm_forward3(float &a, float &b, float &c, float u)
+{
+    const float s = c + a, d = c - a;
+    const float k0 = b + s;
+    const float k1 = fmaf(-u, k0, d);
+    const float k2 = fmaf(u, fmaf(u, k0, -2.0f * d), s);
+    a = k0;
+    b = k1;
+    c = k2;
+}
+
+// (k0, k1, k2) about u -> (f-, f0, f+), in place: raw moments m1 = k1 + u k0,
+// m2 = k2 + u (k1 + m1), then f0 = k0 - m2, f+- = (m2 +- m1) / 2.
+LBM_HD void cm_backward3(float &a, float &b, float &c, float u)
+{
+    const float k0 = a, k1 = b, k2 = c;
+    const float m1 = fmaf(u, k0, k1);
+    const float m2 = fmaf(u, k1 + m1, k2);
+    a = 0.5f * (m2 - m1);
+    b = k0 - m2;
+    c = 0.5f * (m2 + m1);
+}
+
+LBM_HD void collide_d3q27_cm(float (&f)[27], const CollideParams &P, const float *ext)
+{
+    using L = D3Q27;
+    float drho = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 27; ++q) {
+        drho += f[q];
+        if (L::cx(q)) jx += L::cx(q) * f[q];
+        if (L::cy(q)) jy += L::cy(q) * f[q];
+        if (L::cz(q)) jz += L::cz(q) * f[q];
+    }
+    const float rho = 1.0f + drho;
+    float Fx, Fy, Fz, ux, uy, uz;
+    force_velocity<false>(P, rho, 0.0f, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz, ext);
+    // a[z][y][x]: slot c + 1 of each axis, then (after the transforms) the exponent e
+    float a[3][3][3];
+#pragma unroll
+    for (int q = 0; q < 27; ++q) a[L::cz(q) + 1][L::cy(q) + 1][L::cx(q) + 1] = f[q];
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_forward3(a[i][j][0], a[i][j][1], a[i][j][2], ux);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_forward3(a[i][0][j], a[i][1][j], a[i][2][j], uy);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_forward3(a[0][i][j], a[1][i][j], a[2][i][j], uz);
+    // relaxation; h: central moments of the rest weights, mu: of the equilibrium per unit rho
+    const float third = 1.0f / 3.0f;
+    const float h[3][3] = {{1.0f, -ux, fmaf(ux, ux, third)},
+                           {1.0f, -uy, fmaf(uy, uy, third)},
+                           {1.0f, -uz, fmaf(uz, uz, third)}};
+    constexpr float mu[3] = {1.0f, 0.0f, 1.0f / 3.0f};
+    const float om = P.omega;
+    // second-order normal moments: xx - yy, xx - zz at the shear rate, the trace at bulk
+    {
+        const float dxx = a[0][0][2] + (h[0][2] - rho * third);
+        const float dyy = a[0][2][0] + (h[1][2] - rho * third);
+        const float dzz = a[2][0][0] + (h[2][2] - rho * third);
+        const float tr = P.cm[0] * (dxx + dyy + dzz);
+        const float p = dxx - dyy, r = dxx - dzz;
+        a[0][0][2] -= third * (tr + om * (p + r));
+        a[0][2][0] -= third * (tr + om * (r - 2.0f * p));
+        a[2][0][0] -= third * (tr + om * (p - 2.0f * r));
+    }
+#pragma unroll
+    for (int ez = 0; ez < 3; ++ez)
+#pragma unroll
+        for (int ey = 0; ey < 3; ++ey)
+#pragma unroll
+            for (int ex = 0; ex < 3; ++ex) {
+                const int n = ex + ey + ez;
+                const int ones = (ex == 1) + (ey == 1) + (ez == 1);
+                if (n == 0) continue;                       // rho
+                if (n == 2 && ones == 0) continue;          // normal moments: done above
+                float R = 0.0f;
+                if (ex == 1) R += Fx * mu[ey] * mu[ez];
+                if (ey == 1) R += Fy * mu[ex] * mu[ez];
+                if (ez == 1) R += Fz * mu[ex] * mu[ey];
+                float &k = a[ez][ey][ex];
+                if (n == 1) {                               // momentum: conserved
+                    k += R;
+                    continue;
+                }
+                const float s = n == 2 ? om : P.cm[n - 2];
+                const float dev = k + (h[0][ex] * h[1][ey] * h[2][ez] -
+                                       rho * (mu[ex] * mu[ey] * mu[ez]));
+                k = fmaf(-s, dev, k);
+                if (ones == 1) k = fmaf(1.0f - 0.5f * s, R, k);
+            }
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_backward3(a[0][i][j], a[1][i][j], a[2][i][j], uz);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_backward3(a[i][0][j], a[i][1][j], a[i][2][j], uy);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_backward3(a[i][j][0], a[i][j][1], a[i][j][2], ux);
+#pragma unroll
+    for (int q = 0; q < 27; ++q) f[q] = a[L::cz(q) + 1][L::cy(q) + 1][L::cx(q) + 1];
+}
+
+// D3Q27 equilibrium rho prod_a phi(c_a, u_a), phi(0, u) = 2/3 - u^2, phi(+-1, u) =
+// (1/3 + u^2 +- u)/2, returned shifted by w = prod_a phi(c_a, 0) as
+// (prod phi - prod phi0) + drho prod phi, the first part telescoped so that no O(1) terms
+// cancel in fp32.
+LBM_HD float d3q27_feq_shifted(int cx, int cy, int cz, float drho, float ux, float uy, float uz)
+{
+    auto phi0 = [](int c) { return c == 0 ? 2.0f / 3.0f : 1.0f / 6.0f; };
+    auto dphi = [](int c, float u) { return c == 0 ? -u * u : 0.5f * (u * u + c * u); };
+    const float x0 = phi0(cx), y0 = phi0(cy), z0 = phi0(cz);
+    const float dx = dphi(cx, ux), dy = dphi(cy, uy), dz = dphi(cz, uz);
+    const float x = x0 + dx, y = y0 + dy;
+    const float prod = x * y * (z0 + dz);
+    const float tele = dx * y0 * z0 + x * dy * z0 + x * y * dz;
+    return fmaf(drho, prod, tele);
+}
+
 // Dispatch on the collision model.  ext: additional force on the cell, or null.
 template <class L, class TL, int COLL>
 LBM_HD void collide(float (&f)[L::Q], float (&g)[TL::QA], const CollideParams &P,
                     const float *ext = nullptr)
 {
     constexpr bool TH = TL::Q > 0;
-    if (COLL == 0) {
+    if constexpr (L::Q == 27) {
+        (void)g;
+        collide_d3q27_cm(f, P, ext);
+    } else if (COLL == 0) {
         collide_bgk<L, TH, TL>(f, g, P, ext);
     } else if constexpr (L::Q == 19) {
         collide_d3q19_mrt<TH, TL>(f, g, P, ext);

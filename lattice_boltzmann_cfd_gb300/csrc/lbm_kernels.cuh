@@ -571,7 +571,8 @@ static __global__ void ib_clear_kernel(uint32_t *mask, long long N)
 // ------------------------------------------------------------ auxiliary kernels -------
 
 // f = f_eq(rho, u) - w, g = g_eq(T, u) as the logical state of one cell, stored for read
-// pattern PAT (NATURAL for AA and SPLIT, PULL for the PULL mode).
+// pattern PAT (NATURAL for AA and SPLIT, PULL for the PULL mode).  f_eq is the quadratic
+// equilibrium on D3Q19 / D2Q9 and the product form on D3Q27.
 template <class L, class TL, int PAT = NATURAL>
 LBM_HD void init_cell(const Params &P, int idx, const float *rho, const float *u,
                       const float *T, int x = 0, int y = 0, int z = 0)
@@ -588,11 +589,17 @@ LBM_HD void init_cell(const Params &P, int idx, const float *rho, const float *u
         const float r = rho[idx];
         const float dr = r - 1.0f;
         const float ux = u[idx], uy = u[N + idx], uz = (L::DIM == 3) ? u[2 * N + idx] : 0.0f;
-        const float u15 = 1.5f * (ux * ux + uy * uy + uz * uz);
+        if constexpr (L::Q == 27) {
 #pragma unroll
-        for (int q = 0; q < L::Q; ++q) {
-            const float cu = L::cx(q) * ux + L::cy(q) * uy + L::cz(q) * uz;
-            f[q] = L::w(q) * (dr + r * (3.0f * cu + 4.5f * cu * cu - u15));
+            for (int q = 0; q < L::Q; ++q)
+                f[q] = d3q27_feq_shifted(L::cx(q), L::cy(q), L::cz(q), dr, ux, uy, uz);
+        } else {
+            const float u15 = 1.5f * (ux * ux + uy * uy + uz * uz);
+#pragma unroll
+            for (int q = 0; q < L::Q; ++q) {
+                const float cu = L::cx(q) * ux + L::cy(q) * uy + L::cz(q) * uz;
+                f[q] = L::w(q) * (dr + r * (3.0f * cu + 4.5f * cu * cu - u15));
+            }
         }
         if constexpr (TL::Q == 7) d3q7_equilibrium(g, P.c.a_T, T[idx], ux, uy, uz);
         if constexpr (TL::Q == 5) d2q5_equilibrium(g, P.c.a_T, T[idx], ux, uy);

@@ -54,6 +54,37 @@ struct D2Q9 {
     }
 };
 
+// D3Q27 (every c in {-1, 0, 1}^3): D3Q19's order, then the corners (+,+,+), (-,+,+),
+// (+,-,+), (-,-,+), (+,+,-), (-,+,-), (+,-,-), (-,-,-).  Weights are products of the D1Q3
+// weights 2/3 (rest) and 1/6 (moving).
+struct D3Q27 {
+    static constexpr int Q = 27, DIM = 3;
+    LBM_HD static constexpr int cx(int q) {
+        constexpr int t[27] = {0, 1, -1, 0, 0, 0, 0, 1, -1, 1, -1, 1, -1, 1, -1, 0, 0, 0, 0,
+                               1, -1, 1, -1, 1, -1, 1, -1};
+        return t[q];
+    }
+    LBM_HD static constexpr int cy(int q) {
+        constexpr int t[27] = {0, 0, 0, 1, -1, 0, 0, 1, 1, -1, -1, 0, 0, 0, 0, 1, -1, 1, -1,
+                               1, 1, -1, -1, 1, 1, -1, -1};
+        return t[q];
+    }
+    LBM_HD static constexpr int cz(int q) {
+        constexpr int t[27] = {0, 0, 0, 0, 0, 1, -1, 0, 0, 0, 0, 1, 1, -1, -1, 1, 1, -1, -1,
+                               1, 1, 1, 1, -1, -1, -1, -1};
+        return t[q];
+    }
+    LBM_HD static constexpr int opp(int q) {
+        constexpr int t[27] = {0, 2, 1, 4, 3, 6, 5, 10, 9, 8, 7, 14, 13, 12, 11, 18, 17, 16, 15,
+                               26, 25, 24, 23, 22, 21, 20, 19};
+        return t[q];
+    }
+    LBM_HD static constexpr float w(int q) {
+        return q == 0 ? 8.0f / 27.0f
+                      : (q <= 6 ? 2.0f / 27.0f : (q <= 18 ? 1.0f / 54.0f : 1.0f / 216.0f));
+    }
+};
+
 // Thermal lattices: Q = 0 means "no thermal populations"; QA is the array size to use.
 struct NoThermal {
     static constexpr int Q = 0, QA = 1;

@@ -139,8 +139,8 @@ extern "C" lbm_status lbm_reduce_populations_static(int lattice, int thermal, in
                                                     int nz, const float *f, const float *g,
                                                     double *out, void *cuda_stream)
 {
-    if (lattice != LBM_D3Q19 && lattice != LBM_D2Q9)
-        return reject(LBM_ERR_ARG, "lattice must be LBM_D3Q19 or LBM_D2Q9");
+    if (lattice != LBM_D3Q19 && lattice != LBM_D2Q9 && lattice != LBM_D3Q27)
+        return reject(LBM_ERR_ARG, "lattice must be LBM_D3Q19, LBM_D2Q9 or LBM_D3Q27");
     if (thermal != LBM_THERMAL_NONE && !((lattice == LBM_D3Q19 && thermal == LBM_D3Q7) ||
                                          (lattice == LBM_D2Q9 && thermal == LBM_D2Q5)))
         return reject(LBM_ERR_ARG, "thermal lattice must be none, D3Q7 (D3Q19) or D2Q5 (D2Q9)");
@@ -177,7 +177,9 @@ extern "C" lbm_status lbm_reduce_populations_static(int lattice, int thermal, in
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const float *pf = static_cast<const float *>(df), *pg = static_cast<const float *>(dg);
     double *po = static_cast<double *>(dout);
-    if (lattice == LBM_D3Q19)
+    if (lattice == LBM_D3Q27)
+        e = launch<lbm::D3Q27, lbm::NoThermal>(pf, pg, N, scratch, po, s);
+    else if (lattice == LBM_D3Q19)
         e = thermal ? launch<lbm::D3Q19, lbm::D3Q7>(pf, pg, N, scratch, po, s)
                     : launch<lbm::D3Q19, lbm::NoThermal>(pf, pg, N, scratch, po, s);
     else

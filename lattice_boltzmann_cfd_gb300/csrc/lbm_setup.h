@@ -46,15 +46,30 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
         return s;
     };
     if (!c) return bad(LBM_ERR_ARG, "config is NULL");
-    if (c->lattice != LBM_D3Q19 && c->lattice != LBM_D2Q9)
-        return bad(LBM_ERR_ARG, "lattice must be LBM_D3Q19 or LBM_D2Q9");
+    if (c->lattice != LBM_D3Q19 && c->lattice != LBM_D2Q9 && c->lattice != LBM_D3Q27)
+        return bad(LBM_ERR_ARG, "lattice must be LBM_D3Q19, LBM_D2Q9 or LBM_D3Q27");
     if (c->thermal != LBM_THERMAL_NONE && c->thermal != LBM_D3Q7 && c->thermal != LBM_D2Q5)
         return bad(LBM_ERR_ARG, "thermal must be NONE, LBM_D3Q7 or LBM_D2Q5");
     if ((c->thermal == LBM_D3Q7 && c->lattice != LBM_D3Q19) ||
         (c->thermal == LBM_D2Q5 && c->lattice != LBM_D2Q9))
         return bad(LBM_ERR_UNSUPPORTED, "thermal lattice must match: D3Q19+D3Q7 or D2Q9+D2Q5");
-    if (c->collision != LBM_BGK && c->collision != LBM_MRT)
-        return bad(LBM_ERR_ARG, "collision must be LBM_BGK or LBM_MRT");
+    if (c->collision != LBM_BGK && c->collision != LBM_MRT && c->collision != LBM_CM)
+        return bad(LBM_ERR_ARG, "collision must be LBM_BGK, LBM_MRT or LBM_CM");
+    if ((c->lattice == LBM_D3Q27) != (c->collision == LBM_CM))
+        return bad(LBM_ERR_UNSUPPORTED, "D3Q27 goes with LBM_CM, and LBM_CM with D3Q27 only");
+    if (c->lattice == LBM_D3Q27) {
+        if (!(std::isfinite(c->tau) && c->tau > 0.5))
+            return bad(LBM_ERR_ARG, "tau must be finite and > 1/2");
+        for (int k = 0; k < 5; ++k)
+            if (!(c->cm_rates[k] > 0.0 && c->cm_rates[k] < 2.0))
+                return bad(LBM_ERR_ARG, "central-moment rates must lie in (0, 2)");
+        if (c->thermal != LBM_THERMAL_NONE)
+            return bad(LBM_ERR_UNSUPPORTED, "D3Q27 takes no thermal lattice");
+        if (c->streaming != LBM_STREAM_AA)
+            return bad(LBM_ERR_UNSUPPORTED, "D3Q27 runs the AA layout only");
+        if (c->ib_max_samples > 0)
+            return bad(LBM_ERR_UNSUPPORTED, "D3Q27 takes no immersed-boundary samples");
+    }
     if (c->nx < 1 || c->ny < 1 || c->nz < 1) return bad(LBM_ERR_ARG, "grid sizes must be >= 1");
     if (c->lattice == LBM_D2Q9 && c->nz != 1) return bad(LBM_ERR_ARG, "D2Q9 needs nz == 1");
     const long long N = (long long)c->nx * c->ny * c->nz;
@@ -78,7 +93,7 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     } else if (c->gbeta != 0.0) {
         return bad(LBM_ERR_ARG, "buoyancy (gbeta != 0) needs a thermal lattice");
     }
-    const int dim = (Q == LBM_D3Q19) ? 3 : 2;
+    const int dim = (Q == LBM_D2Q9) ? 2 : 3;
     if (c->up_axis < 0 || c->up_axis >= dim) return bad(LBM_ERR_ARG, "up_axis out of range");
     if (dim == 2 && c->g_body[2] != 0.0) return bad(LBM_ERR_ARG, "g_body[2] must be 0 in 2-D");
     for (int a = 0; a < 3; ++a)
@@ -185,7 +200,8 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
         C.mA[k] = 0.0f;
         C.mB[k] = 0.0f;
     }
-    for (int k = 0; k < g.lattice; ++k) {
+    for (int k = 0; k < 5; ++k) C.cm[k] = g.lattice == LBM_D3Q27 ? (float)g.cm_rates[k] : 0.0f;
+    for (int k = 0; k < (g.lattice == LBM_D3Q27 ? 0 : g.lattice); ++k) {
         if (k == 0) continue;
         if (conserved_row(g.lattice, k)) {
             C.mB[k] = (float)(1.0 / norm[k]);

@@ -25,6 +25,9 @@ RATE_ROWS = {
     7: {"kappa": [1, 2, 3], "e": [4], "v": [5, 6]},
     5: {"kappa": [1, 2], "e": [3], "v": [4]},
 }
+# D3Q27 central moments: rates by name, in lbm_config.cm_rates order (the shear rate is
+# 1/tau).
+CM_RATES = ("bulk", "r3", "r4", "r5", "r6")
 _FLOW = {"periodic": capi.LBM_FACE_PERIODIC, "wall": capi.LBM_FACE_WALL,
          "halo": capi.LBM_FACE_HALO}
 _TFACE = {"adiabatic": capi.LBM_TFACE_ADIABATIC, "dirichlet": capi.LBM_TFACE_DIRICHLET}
@@ -42,14 +45,17 @@ def make_config(w, streaming: str = "aa"):
     cfg.nx, cfg.ny, cfg.nz = (int(v) for v in w.shape)
     cfg.lattice = int(w.lattice)
     cfg.thermal = int(w.thermal)
-    cfg.collision = {"bgk": capi.LBM_BGK, "mrt": capi.LBM_MRT}[w.collision]
+    cfg.collision = {"bgk": capi.LBM_BGK, "mrt": capi.LBM_MRT, "cm": capi.LBM_CM}[w.collision]
     cfg.tau = 3.0 * w.nu + 0.5
     rates = dict(w.rates)
     rates["nu"] = 1.0 / cfg.tau
     s = [0.0] * 19
-    for name, rows in RATE_ROWS[cfg.lattice].items():
-        for k in rows:
-            s[k] = float(rates[name])
+    if cfg.lattice == capi.LBM_D3Q27:
+        cfg.cm_rates = (ctypes.c_double * 5)(*[float(rates[n]) for n in CM_RATES])
+    else:
+        for name, rows in RATE_ROWS[cfg.lattice].items():
+            for k in rows:
+                s[k] = float(rates[name])
     cfg.s = (ctypes.c_double * 19)(*s)
     sT = [0.0] * 7
     if cfg.thermal:
@@ -98,7 +104,7 @@ class Simulation:
         self.shape = tuple(w.shape)
         self.grid = (self.cfg.nz, self.cfg.ny, self.cfg.nx)
         self.Q, self.QT = self.cfg.lattice, self.cfg.thermal
-        self.dim = 3 if self.Q == 19 else 2
+        self.dim = 2 if self.Q == 9 else 3
         self.cells = self.cfg.nx * self.cfg.ny * self.cfg.nz
         if getattr(w, "ib_x", None) is not None and len(w.ib_x):
             self.set_ib_samples(w.ib_x, w.ib_ub, w.ib_w)

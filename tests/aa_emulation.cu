@@ -257,6 +257,7 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
     using Dom = Domain<L, TL, C, NARROW>;
     const int dim = L::DIM, outer = dim - 1;
     const int n_outer = dim == 3 ? cfg.nz : cfg.ny;
+    const int halo_dirs = L::Q == 27 ? 9 : (L::Q == 19 ? 5 : 3) + (TL::Q ? 1 : 0);
     const size_t plane = dim == 3 ? (size_t)cfg.nx * cfg.ny : (size_t)cfg.nx;
     const size_t N = (size_t)cfg.nx * cfg.ny * cfg.nz;
     const bool periodic = cfg.face_flow[2 * outer] == LBM_FACE_PERIODIC;
@@ -295,9 +296,8 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
         if (lbm_setup::validate(&lc, &Lay, &why) != LBM_OK) return -10 - r;
         auto d = std::make_unique<Dom>(lc, Lay);
         d->init(lr.data(), lu.data(), T ? lT.data() : nullptr);
-        const int dirs = (L::Q == 19 ? 5 : 3) + (TL::Q ? 1 : 0);
-        std::array<std::vector<float>, 2> b{std::vector<float>(dirs * plane),
-                                            std::vector<float>(dirs * plane)};
+        std::array<std::vector<float>, 2> b{std::vector<float>(halo_dirs * plane),
+                                            std::vector<float>(halo_dirs * plane)};
         bufs.push_back(std::move(b));
         doms.push_back(std::move(d));
         plane_lists.push_back(planes);
@@ -347,6 +347,8 @@ int run_any(const lbm_config *cfg, const lbm_setup::Layout &Lay, const float *rh
             const float *ib_w)
 {
     const bool mrt = cfg->collision == LBM_MRT;
+    if (cfg->lattice == 27)
+        return run<D3Q27, NoThermal, 2, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w);
     if (cfg->lattice == 19) {
         if (cfg->thermal == 7)
             return mrt ? run<D3Q19, D3Q7, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w)
@@ -388,6 +390,8 @@ extern "C" int emu_run_slabs(const lbm_config *cfg, const float *rho, const floa
     if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
     if (cfg->streaming != LBM_STREAM_AA || nslabs < 1) return -2;
     const bool mrt = cfg->collision == LBM_MRT;
+    if (cfg->lattice == 27)
+        return run_slabs<D3Q27, NoThermal, 2, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
     if (cfg->lattice == 19) {
         if (cfg->thermal == 7)
             return mrt ? run_slabs<D3Q19, D3Q7, 1, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout)
@@ -420,9 +424,9 @@ extern "C" long long emu_count_bad_indices(int lattice, int nx, int ny, int nz)
                 const Offs o = make_offs(x, y, z, P);
                 const int Q = lattice;
                 for (int q = 0; q < Q; ++q) {
-                    const int cx = lattice == 19 ? D3Q19::cx(q) : D2Q9::cx(q);
-                    const int cy = lattice == 19 ? D3Q19::cy(q) : D2Q9::cy(q);
-                    const int cz = lattice == 19 ? D3Q19::cz(q) : D2Q9::cz(q);
+                    const int cx = lattice == 27 ? D3Q27::cx(q) : lattice == 19 ? D3Q19::cx(q) : D2Q9::cx(q);
+                    const int cy = lattice == 27 ? D3Q27::cy(q) : lattice == 19 ? D3Q19::cy(q) : D2Q9::cy(q);
+                    const int cz = lattice == 27 ? D3Q27::cz(q) : lattice == 19 ? D3Q19::cz(q) : D2Q9::cz(q);
                     for (int sgn = -1; sgn <= 1; sgn += 2) {
                         const long long j = idx + nb(o, sgn * cx, sgn * cy, sgn * cz);
                         if (j < 0 || j >= N) ++bad;

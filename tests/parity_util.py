@@ -42,7 +42,10 @@ def mask_brute_force(w) -> np.ndarray:
               (1, 1, 0), (-1, 1, 0), (1, -1, 0), (-1, -1, 0), (1, 0, 1), (-1, 0, 1), (1, 0, -1),
               (-1, 0, -1), (0, 1, 1), (0, -1, 1), (0, 1, -1), (0, -1, -1)],
          9: [(0, 0, 0), (1, 0, 0), (0, 1, 0), (-1, 0, 0), (0, -1, 0), (1, 1, 0), (-1, 1, 0),
-             (-1, -1, 0), (1, -1, 0)]}[w.lattice]
+             (-1, -1, 0), (1, -1, 0)]}
+    c[27] = c[19] + [(1, 1, 1), (-1, 1, 1), (1, -1, 1), (-1, -1, 1), (1, 1, -1), (-1, 1, -1),
+                     (1, -1, -1), (-1, -1, -1)]
+    c = c[w.lattice]
     nz, ny, nx = w.grid
     solid = np.zeros(w.grid, bool) if w.solid is None else w.solid.astype(bool)
     z, y, x = np.meshgrid(np.arange(nz), np.arange(ny), np.arange(nx), indexing="ij")
@@ -146,8 +149,15 @@ def slab_cases():
     c2p = dataclasses.replace(
         c2, name=c2.name + " periodic-y",
         face_flow=("wall", "wall", "periodic", "periodic", "periodic", "periodic"))
+    d27 = W.perturbed(W.channel_sphere(shape=(8, 7, 10), center=(3, 3, 0), radius=2.5,
+                                       lattice=27), seed=38)
+    d27 = dataclasses.replace(
+        d27, name="D3Q27 CM channel periodic-z 8x7x10 + sphere across the wrap",
+        face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"),
+        g_body=(1e-4, 0.0, 2e-5))
     return [W.random_periodic(shape=(7, 6, 11), seed=34),
             W.random_periodic(shape=(7, 6, 11), seed=35, collision="bgk"),
+            W.random_periodic(shape=(7, 6, 9), seed=39, lattice=27), d27,
             ring, rb, dataclasses.replace(c3, collision="bgk"), c2, c2p,
             W.random_periodic(shape=(9, 10, 1), seed=36, lattice=9)]
 
@@ -191,7 +201,23 @@ def small_cases():
         c2, face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"),
         face_T=("adiabatic", "adiabatic", "dirichlet", "dirichlet", "adiabatic", "adiabatic"),
         T_wall=(0.0, 0.0, 0.3, -0.2, 0.0, 0.0)))
+    cases += d3q27_cases()
     return cases
+
+
+def d3q27_cases():
+    """D3Q27 central moments: periodic, periodic with a distinct rate per moment group, and a
+    forced channel (walls in y, z) around a solid sphere."""
+    rp = W.random_periodic(shape=(6, 5, 4), seed=11, lattice=27, nu=0.05)
+    distinct = dataclasses.replace(
+        W.random_periodic(shape=(5, 6, 7), seed=12, lattice=27, nu=0.08),
+        name="D3Q27 CM periodic 5x6x7, distinct rates",
+        rates={"bulk": 1.1, "r3": 1.3, "r4": 1.5, "r5": 1.7, "r6": 0.9},
+        g_body=(2e-4, -1e-4, 5e-5))
+    ch = W.perturbed(W.channel_sphere(shape=(12, 10, 9), center=(5, 4, 4), radius=2.5,
+                                      lattice=27), seed=13)
+    ch = dataclasses.replace(ch, g_body=(1e-4, 2e-5, -1e-5))
+    return [rp, distinct, ch]
 
 
 def split_steps(n):

@@ -169,3 +169,36 @@ def test_product_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in src and "from oracle" not in src, fn
                 assert "lbm_oracle" not in src, fn
+
+
+@pytest.mark.parametrize("overrides,status,text", [
+    ({"collision": 1}, 2, "D3Q27 goes with LBM_CM"),        # D3Q27 with MRT
+    ({"cm_rates": [2.0]}, 1, "central-moment rates"),
+    ({"cm_rates": [1.0, 0.0]}, 1, "central-moment rates"),
+    ({"tau": 0.5}, 1, "tau"),
+    ({"thermal": 7}, 2, "thermal"),
+    ({"streaming": 1}, 2, "AA layout"),
+    ({"ib_max_samples": 8}, 2, "immersed"),
+])
+def test_d3q27_configs_validated(capi, overrides, status, text):
+    """D3Q27 takes the central-moment collision only, rates in (0, 2), no thermal lattice,
+    no immersed-boundary samples and the AA layout only."""
+    w = W.random_periodic(shape=(8, 6, 5), lattice=27)
+    assert _bytes(capi, w) > 0
+    with pytest.raises(capi.LbmError) as e:
+        _bytes(capi, w, **overrides)
+    assert e.value.status == status
+    assert text in str(e.value)
+
+
+def test_central_moments_only_on_d3q27(capi):
+    with pytest.raises(capi.LbmError, match="LBM_CM with D3Q27 only"):
+        _bytes(capi, W.random_periodic(shape=(8, 6, 5)), collision=2)
+
+
+def test_d3q27_workspace_holds_27_planes(capi):
+    w = W.random_periodic(shape=(40, 30, 20), lattice=27)
+    S = (40 * 30 * 20 + 63) // 64 * 64
+    assert _bytes(capi, w) >= 27 * S * 4
+    # slab halos of D3Q27 move the 9 populations with c_z = +-1
+    assert _bytes(capi, w, face_flow=[0, 0, 0, 0, 2, 2]) > 0
