@@ -346,23 +346,31 @@ LBM_HD void collide_bgk(float (&f)[L::Q], float (&g)[TL::QA], const CollideParam
 //   the source's central moments R_e = F_a prod_{b != a} mu[e_b] where e_a = 1;
 //   k+ = k - s (k - k_eq) + (1 - s/2) R, with s = 0 on orders 0 and 1, the shear rate on
 //   xy, xz, yz, xx - yy, xx - zz, the bulk rate on xx + yy + zz, one rate per order 3..6.
-// The lattice is the tensor product of three D1Q3 stencils, so M(u) factors into one
-// 3-point transform per axis: (f-, f0, f+) -> (sum f, sum (c-u) f, sum (c-u)^2 f), applied
-// along x, then y, then z to the 3x3x3 array of populations (27 x 8 flops each way instead
-// of a 27 x 27 product).  The transform runs on the shifted populations fbar = f - w; the
-// rest part's central moments, prod_a h[e_a] with h = (1, -u_a, 1/3 + u_a^2), enter the
-// deviation k - k_eq analytically, so every quantity carried in fp32 is deviation-sized.
+// The lattice is the tensor product of three D1Q3 stencils, so M(u) factors into 3-point
+// transforms per axis, applied to the 3x3x3 array of populations: first the raw moments
+// (f-, f0, f+) -> (sum f, sum c f, sum c^2 f) along x, y and z (u-independent: rho and j
+// come out of it), then the shift of each axis to central moments about u_a (about 160
+// flops in all instead of a 27 x 27 product).  The transform runs on the shifted
+// populations fbar = f - w; the rest part's central moments, prod_a h[e_a] with
+// h = (1, -u_a, 1/3 + u_a^2), enter the deviation k - k_eq analytically, so every quantity
+// carried in fp32 is deviation-sized.
 
-// (f-, f0, f+) -> (k0, k1, k2) about u, in place.
-LBM_HD void cm_forward3(float &a, float &b, float &c, float u)
+// (f-, f0, f+) -> raw moments (m0, m1, m2) = (sum f, sum c f, sum c^2 f), in place.
+LBM_HD void cm_raw3(float &a, float &b, float &c)
 {
     const float s = c + a, d = c - a;
-    const float k0 = b + s;
-    const float k1 = fmaf(-u, k0, d);
-    const float k2 = fmaf(u, fmaf(u, k0, -2.0f * d), s);
-    a = k0;
+    a = b + s;
+    b = d;
+    c = s;
+}
+
+// Raw moments (m0, m1, m2) -> central moments about u: k1 = m1 - u m0,
+// k2 = m2 - 2 u m1 + u^2 m0 = m2 - u (m1 + k1), in place.
+LBM_HD void cm_shift3(float &a, float &b, float &c, float u)
+{
+    const float k1 = fmaf(-u, a, b);
+    c = fmaf(-u, b + k1, c);
     b = k1;
-    c = k2;
 }
 
 // (k0, k1, k2) about u -> (f-, f0, f+), in place: raw moments m1 = k1 + u k0,
@@ -380,17 +388,6 @@ LBM_HD void cm_backward3(float &a, float &b, float &c, float u)
 LBM_HD void collide_d3q27_cm(float (&f)[27], const CollideParams &P, const float *ext)
 {
     using L = D3Q27;
-    float drho = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 27; ++q) {
-        drho += f[q];
-        if (L::cx(q)) jx += L::cx(q) * f[q];
-        if (L::cy(q)) jy += L::cy(q) * f[q];
-        if (L::cz(q)) jz += L::cz(q) * f[q];
-    }
-    const float rho = 1.0f + drho;
-    float Fx, Fy, Fz, ux, uy, uz;
-    force_velocity<false>(P, rho, 0.0f, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz, ext);
     // a[z][y][x]: slot c + 1 of each axis, then (after the transforms) the exponent e
     float a[3][3][3];
 #pragma unroll
@@ -398,15 +395,32 @@ LBM_HD void collide_d3q27_cm(float (&f)[27], const CollideParams &P, const float
 #pragma unroll
     for (int i = 0; i < 3; ++i)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) cm_forward3(a[i][j][0], a[i][j][1], a[i][j][2], ux);
+        for (int j = 0; j < 3; ++j) cm_raw3(a[i][j][0], a[i][j][1], a[i][j][2]);
 #pragma unroll
     for (int i = 0; i < 3; ++i)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) cm_forward3(a[i][0][j], a[i][1][j], a[i][2][j], uy);
+        for (int j = 0; j < 3; ++j) cm_raw3(a[i][0][j], a[i][1][j], a[i][2][j]);
 #pragma unroll
     for (int i = 0; i < 3; ++i)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) cm_forward3(a[0][i][j], a[1][i][j], a[2][i][j], uz);
+        for (int j = 0; j < 3; ++j) cm_raw3(a[0][i][j], a[1][i][j], a[2][i][j]);
+    // raw moments of fbar: sum fbar = rho - 1, sum c fbar = j
+    const float rho = 1.0f + a[0][0][0];
+    float Fx, Fy, Fz, ux, uy, uz;
+    force_velocity<false>(P, rho, 0.0f, a[0][0][1], a[0][1][0], a[1][0][0], Fx, Fy, Fz, ux, uy,
+                          uz, ext);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_shift3(a[i][j][0], a[i][j][1], a[i][j][2], ux);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_shift3(a[i][0][j], a[i][1][j], a[i][2][j], uy);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+#pragma unroll
+        for (int j = 0; j < 3; ++j) cm_shift3(a[0][i][j], a[1][i][j], a[2][i][j], uz);
     // relaxation; h: central moments of the rest weights, mu: of the equilibrium per unit rho
     const float third = 1.0f / 3.0f;
     const float h[3][3] = {{1.0f, -ux, fmaf(ux, ux, third)},
