@@ -46,8 +46,8 @@ BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112, (27, 0): 
 # taken on; reported as "traffic" only while the sources are unchanged.
 NCU_TRAFFIC = {
     # ncu --set full, one even + one odd launch at 256^3 (see profiles/), scaled by cells
-    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.56, "src_hash": "be2c4d067370035d"},
-    "cavity3d_512": {"bytes_per_cell": 208.61, "src_hash": "be2c4d067370035d"},
+    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.57, "src_hash": "32e8c8e6c164cdeb"},
+    "cavity3d_512": {"bytes_per_cell": 208.64, "src_hash": "32e8c8e6c164cdeb"},
 }
 
 
@@ -192,8 +192,66 @@ def timed_device_leg(sim, w, steps, warmup, lbm_steps, dist_ctx):
         torch.cuda.synchronize()
     dist_ctx.barrier()
     secs = t0.elapsed_time(t1) / 1e3
-    kernel_ms = sum(a.elapsed_time(b) for a, b in ev) / (steps * lbm_steps)
-    return secs, kernel_ms, clk.summary()
+    per_step = [a.elapsed_time(b) / lbm_steps for a, b in ev]   # ms per LBM step
+    kernel_ms = sum(per_step) / steps
+    return secs, kernel_ms, clk.summary(), per_step
+
+
+def live_copy_gbs(nbytes: int = 2 << 30, reps: int = 5) -> float:
+    """Device-to-device copy bandwidth measured now (read + write bytes / time): a second
+    roofline denominator taken in the same run as the kernel."""
+    import torch
+    n = nbytes // 4
+    a = torch.empty(n, dtype=torch.float32, device="cuda")
+    b = torch.empty_like(a)
+    a.fill_(1.0)
+    for _ in range(2):
+        b.copy_(a)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record()
+    for _ in range(reps):
+        b.copy_(a)
+    t1.record()
+    torch.cuda.synchronize()
+    gbs = 2 * nbytes * reps / (t0.elapsed_time(t1) / 1e3) / 1e9
+    del a, b
+    torch.cuda.empty_cache()
+    return gbs
+
+
+def nominal_hbm_gbs():
+    """2 x memory clock x bus width of the current device, or None if neither torch's device
+    properties nor (nvidia-smi's maximum memory clock, the CUDA runtime's bus-width
+    attribute) give them."""
+    import torch
+    dev = torch.cuda.current_device()
+    p = torch.cuda.get_device_properties(dev)
+    clk_khz = getattr(p, "memory_clock_rate", None)
+    bus = getattr(p, "memory_bus_width", None)
+    if not clk_khz or not bus:
+        try:
+            q = subprocess.run(["nvidia-smi", "-i", str(dev), "--query-gpu=clocks.max.memory",
+                                "--format=csv,noheader,nounits"], capture_output=True,
+                               text=True, timeout=20)
+            clk_khz = float(q.stdout.strip().splitlines()[0]) * 1e3
+            import ctypes
+            rt = None
+            for name in ("libcudart.so", "libcudart.so.13", "libcudart.so.12"):
+                try:
+                    rt = ctypes.CDLL(name)
+                    break
+                except OSError:
+                    continue
+            v = ctypes.c_int(0)
+            if rt is None or rt.cudaDeviceGetAttribute(ctypes.byref(v), 37, dev) != 0:
+                return None            # 37 = cudaDevAttrGlobalMemoryBusWidth
+            bus = v.value
+        except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+            return None
+    if not clk_khz or not bus:
+        return None
+    return 2.0 * clk_khz * 1e3 * bus / 8 / 1e9
 
 
 def timed_e2e_leg(sim, w, steps, warmup, lbm_steps, dist_ctx):
@@ -259,11 +317,20 @@ def time_oracle(name: str, steps: int):
     return mlups, dt, w.cells, label, oracle.max_threads()
 
 
-def cpu_baseline(name: str, steps: int = 16) -> dict:
+def cpu_baseline(name: str, steps: int = 16, steps_1thread: int = 1) -> dict:
+    import oracle
     mlups, dt, cells, label, cores = time_oracle(name, steps)
+    prev = oracle.set_threads(1)
+    try:
+        mlups1, dt1, _, _, _ = time_oracle(name, steps_1thread)
+    finally:
+        oracle.set_threads(prev)
     return {"value": round(mlups, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{label} of the same workload, {steps} fp64 two-buffer steps "
-                      f"({cells * steps / 1e6:.0f} M cell updates, {dt:.1f} s)"}
+                      f"({cells * steps / 1e6:.0f} M cell updates, {dt:.1f} s)",
+            "value_1thread": round(mlups1, 3),
+            "sample_1thread": f"the same sample, {steps_1thread} steps on 1 thread "
+                              f"({dt1:.1f} s)"}
 
 
 # ----------------------------------------------------------------- helpers --------
@@ -338,10 +405,13 @@ def run_secondary(name, lbm_steps, reps, streaming="aa"):
     sim.close()
     del sim
     torch.cuda.empty_cache()
-    return {"workload": workload_label(name, w), "layout": streaming,
-            "mlups": round(w.cells / kernel_s / 1e6, 1),
-            "bytes_per_cell": bpc, "achieved_gbs": round(achieved, 1),
-            "frac": round(achieved / peak, 4)}
+    out = {"workload": workload_label(name, w), "layout": streaming,
+           "mlups": round(w.cells / kernel_s / 1e6, 1),
+           "bytes_per_cell": bpc, "achieved_gbs": round(achieved, 1),
+           "frac": round(achieved / peak, 4)}
+    if w.solid is not None:   # fluid cells only (solid cells are skipped, not updated)
+        out["fluid_mlups"] = round(w.fluid_cells() / kernel_s / 1e6, 1)
+    return out
 
 
 def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None):
@@ -389,8 +459,8 @@ def run_gpu(args, dctx):
     w = make_workload(args.workload)
     sim = Simulation(w)
     sim.init_equilibrium(*upload(w, sim.device))
-    secs, kernel_ms, clocks = timed_device_leg(sim, w, args.steps, args.warmup,
-                                               args.lbm_steps, dctx)
+    secs, kernel_ms, clocks, per_step = timed_device_leg(sim, w, args.steps, args.warmup,
+                                                         args.lbm_steps, dctx)
     secs = dctx.max(secs)
     kernel_ms = dctx.max(kernel_ms)
     updates = w.cells * args.lbm_steps * args.steps * dctx.world
@@ -407,6 +477,11 @@ def run_gpu(args, dctx):
     bpc = BYTES_PER_CELL[(w.lattice, w.thermal)]
     peak, peak_kind = measured_peak()
     achieved = bpc * w.cells / (kernel_ms / 1e3) / 1e9
+    live = live_copy_gbs()
+    nominal = nominal_hbm_gbs()
+    per_step = sorted(per_step)
+    median_ms = per_step[len(per_step) // 2] if len(per_step) % 2 else \
+        0.5 * (per_step[len(per_step) // 2 - 1] + per_step[len(per_step) // 2])
     src = kernel_source_hash()
     tr = NCU_TRAFFIC.get(args.workload)
     traffic = (round(tr["bytes_per_cell"] * w.cells) if tr and tr["src_hash"] == src else None)
@@ -428,7 +503,16 @@ def run_gpu(args, dctx):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "step_kernel (even/odd AA forms)",
                      "kernel_ms": round(kernel_ms, 4), "bytes_per_cell": bpc,
-                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)"},
+                     "kernel_ms_median": round(median_ms, 4),
+                     "kernel_ms_mean": round(kernel_ms, 4),
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth (MEASURED_PEAKS.json)",
+                     "live_copy_gbs": round(live, 1),
+                     "frac_of_live_copy": round(achieved / live, 4),
+                     "nominal_gbs": None if nominal is None else round(nominal, 1),
+                     "frac_of_nominal": None if nominal is None else round(achieved / nominal, 4),
+                     "denominators": "peak: the measured copy; live_copy_gbs: a 2 GiB "
+                                     "device copy timed in this run; nominal: 2 x memory "
+                                     "clock x bus width from the device attributes"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "path": "page-locked host rho,u in -> lbm_init_equilibrium -> lbm_step -> "

@@ -155,6 +155,12 @@ typedef struct {
     int ib_samples;       /* immersed-boundary samples in use                              */
     double ib_force[3];   /* their reaction force -sum g_s in the last step               */
     double ib_torque[3];  /* -sum (x_s - centroid) x g_s about the samples' centroid      */
+    double uT[3];         /* sum over fluid cells of u_a T, u = (j + F/2)/rho (thermal)    */
+    double nu_volume;     /* volume-averaged Nusselt number along the axis of the hottest
+                             and coldest DIRICHLET faces (when they face each other):
+                             1 + <u_a T> H / (kappa dT), <.> over fluid cells, H = cells
+                             across, kappa = omega (1/s_T[1 + a] - 1/2), the flux counted
+                             from the hot face towards the cold one                      */
 } lbm_diag;
 
 /* Bytes of device workspace lbm_create() needs for this configuration (validates it). */

@@ -57,6 +57,7 @@ class lbm_diag(ctypes.Structure):
         ("fluid_cells", ctypes.c_longlong), ("steps", ctypes.c_longlong),
         ("finite", ctypes.c_int), ("ib_samples", ctypes.c_int),
         ("ib_force", ctypes.c_double * 3), ("ib_torque", ctypes.c_double * 3),
+        ("uT", ctypes.c_double * 3), ("nu_volume", ctypes.c_double),
     ]
 
 
@@ -189,7 +190,8 @@ def lbm_diagnostics(ctx, allow_nonfinite: bool = False) -> dict:
             "heat": list(d.heat), "nu_hot": d.nu_hot, "nu_cold": d.nu_cold,
             "fluid_cells": d.fluid_cells, "steps": d.steps, "finite": bool(d.finite),
             "ib_samples": d.ib_samples, "ib_force": list(d.ib_force),
-            "ib_torque": list(d.ib_torque), "status": st}
+            "ib_torque": list(d.ib_torque), "uT": list(d.uT), "nu_volume": d.nu_volume,
+            "status": st}
 
 
 def lbm_get_populations(ctx, f, g=None):

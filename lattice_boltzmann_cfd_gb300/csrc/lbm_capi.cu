@@ -374,7 +374,8 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
                                      c->P, c->partial, c->result, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "diagnostics kernel");
     double r[lbm::DIAG_N] = {0};
-    e = cudaMemcpyAsync(r, c->result, sizeof(double) * 15, cudaMemcpyDeviceToHost, c->stream);
+    e = cudaMemcpyAsync(r, c->result, sizeof(double) * lbm::DIAG_VALUES,
+                        cudaMemcpyDeviceToHost, c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "diagnostics read-back");
     std::memset(out, 0, sizeof(*out));
@@ -405,7 +406,19 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
         };
         out->nu_hot = nusselt(hot);
         out->nu_cold = nusselt(cold);
+        // volume average along the hot-cold axis: 1 + <u_a T> H / (kappa dT), with the
+        // flux counted from the hot face towards the cold one
+        const int a = hot / 2;
+        if (cold / 2 == a && c->cfg.thermal && out->fluid_cells > 0) {
+            const double omega = c->cfg.thermal == LBM_D2Q5 ? (4.0 + c->cfg.a_T) / 10.0
+                                                            : (6.0 + c->cfg.a_T) / 21.0;
+            const double kappa = omega * (1.0 / c->cfg.s_T[1 + a] - 0.5);
+            const double sign = (hot % 2 == 0) ? 1.0 : -1.0;
+            const double uT = r[15 + a] / (double)out->fluid_cells;
+            out->nu_volume = 1.0 + sign * uT * n[a] / (kappa * dT);
+        }
     }
+    for (int a = 0; a < 3; ++a) out->uT[a] = r[15 + a];
     out->ib_samples = c->P.ib_n;
     if (c->P.ib_n > 0) {
         // reaction force and torque of the last step's penalties (fp64 on the host)

@@ -322,7 +322,14 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     asm volatile("" : "+r"(xs), "+r"(ys), "+r"(zs), "+r"(is), "+r"(ms));
     Offs o{};
     if (ODD) o = make_offs(xs, ys, zs, Pw);
-    store_cell<L, TL, MASKED, ODD, NARROW>(Pw, is, o, ms, f, g);
+    if constexpr (MASKED && ODD) {
+        // only cells next to a wall or solid redirect stores; the rest (whole warps away
+        // from the walls) take the plain neighbour stores
+        if (ms & wall_bits<L>()) store_cell<L, TL, true, true, NARROW>(Pw, is, o, ms, f, g);
+        else store_cell<L, TL, false, true, NARROW>(Pw, is, o, 0u, f, g);
+    } else {
+        store_cell<L, TL, MASKED, ODD, NARROW>(Pw, is, o, ms, f, g);
+    }
 }
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
@@ -775,16 +782,18 @@ __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__rest
 
 // Diagnostics: per-block fp64 partial sums of
 //   [0] sum (rho - 1), [1..3] sum j, [4..6] momentum exchange with solid cells,
-//   [7..12] wall heat flux per Dirichlet face, [13] non-finite cells, [14] fluid cells.
-constexpr int DIAG_N = 16;
+//   [7..12] wall heat flux per Dirichlet face, [13] non-finite cells, [14] fluid cells,
+//   [15..17] sum u_a T with u = (j + F/2)/rho (thermal lattices).
+constexpr int DIAG_VALUES = 18;
+constexpr int DIAG_N = 20;   // row stride of the partial sums
 constexpr int DIAG_THREADS = 256;
 
 template <class L, class TL, bool MASKED, int PAT>
 __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, double *partial)
 {
-    double acc[15];
+    double acc[DIAG_VALUES];
 #pragma unroll
-    for (int i = 0; i < 15; ++i) acc[i] = 0.0;
+    for (int i = 0; i < DIAG_VALUES; ++i) acc[i] = 0.0;
     const long long N = (long long)P.nx * P.ny * P.nz;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < N;
          i += (long long)gridDim.x * blockDim.x) {
@@ -818,6 +827,14 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
         }
         if (!isfinite(dr) || !isfinite(t)) acc[13] += 1.0;
         acc[14] += 1.0;
+        if constexpr (TL::Q > 0) {
+            // convective transport, with the velocity of the macroscopic read-out
+            float Fx, Fy, Fz, ux, uy, uz;
+            force_velocity<true>(P.c, 1.0f + dr, t, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz);
+            acc[15] += ux * t;
+            acc[16] += uy * t;
+            acc[17] += uz * t;
+        }
         if (MASKED) {
             // links into solid cells: the bounced-back population of the last step is the
             // logical f_opp(q)(x) now; exchange 2 f+_q c_q
@@ -851,16 +868,16 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
         }
     }
     // block reduction in a fixed order: warp shuffles, then warps in order
-    __shared__ double sh[DIAG_THREADS / 32][15];
+    __shared__ double sh[DIAG_THREADS / 32][DIAG_VALUES];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int i = 0; i < 15; ++i) {
+    for (int i = 0; i < DIAG_VALUES; ++i) {
         double v = acc[i];
         for (int s = 16; s > 0; s >>= 1) v += __shfl_down_sync(0xffffffffu, v, s);
         if (lane == 0) sh[warp][i] = v;
     }
     __syncthreads();
-    if (threadIdx.x < 15) {
+    if (threadIdx.x < DIAG_VALUES) {
         double v = 0.0;
         for (int w = 0; w < DIAG_THREADS / 32; ++w) v += sh[w][threadIdx.x];
         partial[blockIdx.x * DIAG_N + threadIdx.x] = v;
@@ -871,19 +888,19 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
 static __global__ void __launch_bounds__(DIAG_THREADS) diag_finalize(const double *partial, int nblocks,
                                                                double *out)
 {
-    __shared__ double sh[DIAG_THREADS][15];
-    double acc[15];
-    for (int i = 0; i < 15; ++i) acc[i] = 0.0;
+    __shared__ double sh[DIAG_THREADS][DIAG_VALUES];
+    double acc[DIAG_VALUES];
+    for (int i = 0; i < DIAG_VALUES; ++i) acc[i] = 0.0;
     for (int b = threadIdx.x; b < nblocks; b += DIAG_THREADS)
-        for (int i = 0; i < 15; ++i) acc[i] += partial[b * DIAG_N + i];
-    for (int i = 0; i < 15; ++i) sh[threadIdx.x][i] = acc[i];
+        for (int i = 0; i < DIAG_VALUES; ++i) acc[i] += partial[b * DIAG_N + i];
+    for (int i = 0; i < DIAG_VALUES; ++i) sh[threadIdx.x][i] = acc[i];
     __syncthreads();
     for (int s = DIAG_THREADS / 2; s > 0; s >>= 1) {
         if (threadIdx.x < s)
-            for (int i = 0; i < 15; ++i) sh[threadIdx.x][i] += sh[threadIdx.x + s][i];
+            for (int i = 0; i < DIAG_VALUES; ++i) sh[threadIdx.x][i] += sh[threadIdx.x + s][i];
         __syncthreads();
     }
-    if (threadIdx.x < 15) out[threadIdx.x] = sh[0][threadIdx.x];
+    if (threadIdx.x < DIAG_VALUES) out[threadIdx.x] = sh[0][threadIdx.x];
 }
 
 // ------------------------------------------------------------------ slab halos -------

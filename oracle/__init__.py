@@ -83,9 +83,10 @@ def _load():
             lib.oracle_lattice.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                            ctypes.POINTER(ctypes.c_int), D, D]
             lib.oracle_max_threads.argtypes = []
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
             for fn in ("oracle_check", "oracle_init_equilibrium", "oracle_step", "oracle_run",
                        "oracle_macroscopic", "oracle_diagnostics", "oracle_lattice",
-                       "oracle_max_threads", "oracle_ib_forces"):
+                       "oracle_max_threads", "oracle_ib_forces", "oracle_set_threads"):
                 getattr(lib, fn).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -258,10 +259,11 @@ def macroscopic(prob: Problem, f, g):
 
 
 def diagnostics(prob: Problem, f, g):
-    out = np.zeros(10)
+    out = np.zeros(13)
     _check(_load().oracle_diagnostics(ctypes.byref(prob.p), _dptr(f), _dptr(g), _dptr(out)),
            "diagnostics")
-    return {"mass": out[0], "momentum": out[1:4].copy(), "heat": out[4:10].copy()}
+    return {"mass": out[0], "momentum": out[1:4].copy(), "heat": out[4:10].copy(),
+            "uT": out[10:13].copy()}
 
 
 def lattice(kind: int):
@@ -279,3 +281,8 @@ def lattice(kind: int):
 
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
+
+
+def set_threads(n: int) -> int:
+    """Threads of the following oracle calls; returns the previous count."""
+    return int(_load().oracle_set_threads(int(n)))

@@ -863,25 +863,33 @@ int oracle_macroscopic(const oracle_problem *p, const double *f, const double *g
 }
 
 int oracle_diagnostics(const oracle_problem *p, const double *f, const double *g,
-                       double out[10])
+                       double out[13])
 {
     ctx_t C;
     int rc = make_ctx(p, &C);
     if (rc) return rc;
     const long W = C.W;
-    for (int i = 0; i < 10; ++i) out[i] = 0.0;
+    for (int i = 0; i < 13; ++i) out[i] = 0.0;
     for (int k = 0; k < p->wz; ++k)
         for (int j = 0; j < p->wy; ++j)
             for (int i = 0; i < p->wx; ++i) {
                 const long n = i + (long)p->wx * (j + (long)p->wy * k);
                 if (is_solid(&C, n)) continue;
-                double t = 0.0;
+                double t = 0.0, r = 0.0, jm[3] = {0, 0, 0};
                 for (int q = 0; q < C.F.Q; ++q) {
                     out[0] += f[q * W + n];
-                    for (int a = 0; a < 3; ++a) out[1 + a] += C.F.c[q][a] * f[q * W + n];
+                    r += f[q * W + n];
+                    for (int a = 0; a < 3; ++a) {
+                        out[1 + a] += C.F.c[q][a] * f[q * W + n];
+                        jm[a] += C.F.c[q][a] * f[q * W + n];
+                    }
                 }
                 for (int q = 0; q < C.G.Q; ++q) t += g[q * W + n];
                 if (!p->thermal) continue;
+                /* convective transport u T, u = (j + F/2)/rho as in the macroscopic fields */
+                double F[3];
+                body_force(&C, r, t, F);
+                for (int a = 0; a < 3; ++a) out[10 + a] += (jm[a] + 0.5 * F[a]) / r * t;
                 /* cells next to a Dirichlet face: wall gradient over the half cell */
                 const int gc[3] = {p->x0 + i, p->y0 + j, p->z0 + k};
                 const int ext[3] = {p->nx, p->ny, p->nz};
@@ -926,6 +934,18 @@ int oracle_max_threads(void)
 #ifdef _OPENMP
     return omp_get_max_threads();
 #else
+    return 1;
+#endif
+}
+
+int oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    const int prev = omp_get_max_threads();
+    if (n >= 1) omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
     return 1;
 #endif
 }

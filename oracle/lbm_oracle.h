@@ -103,15 +103,19 @@ int oracle_macroscopic(const oracle_problem *p, const double *f, const double *g
                        double *u, double *T);
 
 /* out[0] mass = sum rho, out[1..3] momentum = sum c f over fluid cells,
- * out[4..9] per face: sum over fluid cells next to a DIRICHLET face of 2 (T_w - T_cell). */
+ * out[4..9] per face: sum over fluid cells next to a DIRICHLET face of 2 (T_w - T_cell),
+ * out[10..12]: sum over fluid cells of u_a T with u = (j + F/2)/rho (0 without thermal). */
 int oracle_diagnostics(const oracle_problem *p, const double *f, const double *g,
-                       double out[10]);
+                       double out[13]);
 
 /* The lattice tables the oracle uses, for inspection by tests.  kind = 9, 19 (momentum)
  * or 5, 7 (thermal).  c: Q*3 ints, w: Q (NULL for thermal), M: Q*Q row-major. */
 int oracle_lattice(int kind, int *Q, int *c, double *w, double *M);
 
 int oracle_max_threads(void);
+
+/* Threads the following calls use (OpenMP); returns the previous count.  n < 1 is ignored. */
+int oracle_set_threads(int n);
 
 #ifdef __cplusplus
 }

@@ -136,6 +136,17 @@ def test_configs_200_and_201_steps(oracle_mod, w):
         assert np.allclose(d["momentum"], dr["momentum"], rtol=1e-4, atol=1e-6 * dr["mass"])
         if w.thermal:
             assert np.allclose(d["heat"], dr["heat"], rtol=1e-4, atol=1e-3)
+            # convective transport and the volume-averaged Nusselt number built on it
+            scale = max(1e-12, float(np.abs(dr["uT"]).max()))
+            assert np.allclose(d["uT"], dr["uT"], rtol=1e-4, atol=1e-4 * scale)
+            hot = int(np.argmax(w.T_wall))
+            cold = int(np.argmin(w.T_wall))
+            a = hot // 2
+            sign = 1.0 if hot % 2 == 0 else -1.0
+            fluid = w.fluid_cells()
+            want = 1 + sign * dr["uT"][a] / fluid * w.shape[a] / (
+                w.kappa * (w.T_wall[hot] - w.T_wall[cold]))
+            assert abs(d["nu_volume"] - want) <= 1e-4 * max(1.0, abs(want))
 
 
 TWO_BUFFER = [REDUCED[i] for i in (0, 1, 3, 5, 7)]   # TG, periodic, and the perturbed ones

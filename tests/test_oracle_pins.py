@@ -581,3 +581,35 @@ def test_buoyancy_momentum_increment(oracle_mod):
             want = np.zeros(3)
             want[up] = (rho * w.gbeta * (T - w.T0)).sum()
             assert np.allclose(d1["momentum"] - d0["momentum"], want, rtol=1e-10, atol=1e-14)
+
+
+@pytest.mark.parametrize("lattice,thermal", [(19, 7), (9, 5)])
+def test_convective_transport_sum_closed_form(oracle_mod, lattice, thermal):
+    """A uniform state in a periodic box with buoyancy stays uniform, and its momentum grows
+    by F = rho gbeta (T - T0) e_up per step, so after n steps the diagnostics' sum of u_a T
+    with u = (j + F/2)/rho is N T (u0 + (n + 1/2) gbeta (T - T0) e_up) in closed form."""
+    dim = 3 if lattice == 19 else 2
+    shape = (5, 4, 3) if dim == 3 else (5, 4, 1)
+    up = dim - 1
+    rates = ({"e": 1.2, "eps": 1.2, "q": 1.2, "pi": 1.2, "m": 1.2} if lattice == 19
+             else {"e": 1.2, "eps": 1.2, "q": 1.2})
+    w = W.Workload(name="uT", lattice=lattice, thermal=thermal, collision="mrt", shape=shape,
+                   nu=0.05, rates=rates, kappa=0.05, thermal_rates={"e": 1.2, "v": 1.2},
+                   gbeta=2e-3, T0=0.1, up_axis=up)
+    N = int(np.prod(shape))
+    u0 = np.array([0.02, -0.01, 0.015])[:dim]
+    T, rho = 0.35, 1.0
+    w.rho0 = np.full(w.grid, rho)
+    w.u0 = np.broadcast_to(u0.reshape((dim,) + (1,) * 3), (dim,) + w.grid).copy()
+    w.T_init = np.full(w.grid, T)
+    p = oracle_mod.Problem(w)
+    f, g = oracle_mod.init_equilibrium(p, w.rho0, w.u0, w.T_init)
+    acc = w.gbeta * (T - w.T0)
+    for n in (0, 1, 4):
+        if n:
+            oracle_mod.run(p, f, g, n - (0 if n == 1 else 1))
+        want = np.zeros(3)
+        want[:dim] = N * T * u0
+        want[up] += N * T * (n + 0.5) * acc
+        d = oracle_mod.diagnostics(p, f, g)
+        assert np.allclose(d["uT"], want, rtol=1e-12, atol=1e-15), n
