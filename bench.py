@@ -81,6 +81,7 @@ def make_workload(name: str):
         "d3q27_cm_periodic_512": lambda: W.random_periodic(n=512, seed=2, lattice=27),
         "d3q27_cm_periodic_256": lambda: W.random_periodic(n=256, seed=2, lattice=27),
         "channel_sphere_d3q27_128": lambda: W.channel_sphere(lattice=27),
+        "channel_ib_sphere_d3q27_128": lambda: W.channel_ib_sphere(lattice=27),
     }
     return table[name]()
 
@@ -524,7 +525,7 @@ def run_gpu(args, dctx):
         _WORKLOAD_CACHE[args.workload] = w
         runs = [("cavity3d_512", "aa"), ("cavity2d_4096", "aa"), ("taylor_green_32", "aa"),
                 ("channel_ib_sphere_128", "aa"), ("d3q27_cm_periodic_512", "aa"),
-                ("channel_sphere_d3q27_128", "aa")]
+                ("channel_sphere_d3q27_128", "aa"), ("channel_ib_sphere_d3q27_128", "aa")]
         # the streaming-layout page's comparison: in place vs two buffers
         for n in ("d3q19_mrt_periodic_128", "channel_sphere_128", args.workload):
             runs += [(n, "aa"), (n, "pull"), (n, "split")]

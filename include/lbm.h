@@ -123,8 +123,8 @@ typedef struct {
     double s[19];         /* MRT rate of each moment row, in [0, 2)                    */
     double s_T[7];        /* thermal MRT rate of each row, in [0, 2)                   */
     double cm_rates[5];   /* LBM_CM: bulk rate, then orders 3, 4, 5, 6; each in (0, 2).
-                             D3Q27 takes no thermal lattice, no immersed-boundary
-                             samples and only LBM_STREAM_AA (LBM_ERR_UNSUPPORTED).     */
+                             D3Q27 takes no thermal lattice and only LBM_STREAM_AA
+                             (LBM_ERR_UNSUPPORTED).                                    */
     double a_T;           /* thermal energy-moment constant (e_eq = a_T T), in (-Q_T+1, 1) */
     double g_body[3];     /* body acceleration: F += rho g_body                        */
     double gbeta, T0;     /* buoyancy: F += rho gbeta (T - T0) e_up (thermal only)      */

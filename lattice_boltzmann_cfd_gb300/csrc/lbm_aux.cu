@@ -57,8 +57,7 @@ cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t
 cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s)
 {
     if (P.ib_n <= 0) return cudaSuccess;
-    if (lattice == 27) return cudaErrorNotSupported;   // rejected at create
-    const int corners = lattice == 19 ? 8 : 4;
+    const int corners = lattice == 9 ? 4 : 8;
     const long long threads = (long long)P.ib_n * corners;
     const dim3 b(128), g((unsigned)((threads + 127) / 128));
     auto go = [&](auto l, auto tl) {
@@ -69,8 +68,7 @@ cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaSt
         else ib_kernel<L, TL, NATURAL><<<g, b, 0, s>>>(P);
         return cudaGetLastError();
     };
-    if (lattice == 19) return thermal == 7 ? go(D3Q19{}, D3Q7{}) : go(D3Q19{}, NoThermal{});
-    return thermal == 5 ? go(D2Q9{}, D2Q5{}) : go(D2Q9{}, NoThermal{});
+    return by_lattice(lattice, thermal, go);
 }
 
 cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
@@ -81,7 +79,8 @@ cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long lo
     if (e != cudaSuccess || P.ib_n <= 0) return e;
     const dim3 b(128), g((P.ib_n + 127) / 128);
     if (lattice == 19) ib_mark_kernel<D3Q19><<<g, b, 0, s>>>(P, mask);
-    else if (lattice == 9) ib_mark_kernel<D2Q9><<<g, b, 0, s>>>(P, mask);
+    else if (lattice == 27) ib_mark_kernel<D3Q27><<<g, b, 0, s>>>(P, mask);
+    else ib_mark_kernel<D2Q9><<<g, b, 0, s>>>(P, mask);
     return cudaGetLastError();
 }
 

@@ -33,7 +33,7 @@ cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool 
                               const Params &P, const Shape &sh, cudaStream_t s);
 cudaError_t launch_step_d2q9(int thermal, int coll, int masked, bool odd, bool narrow,
                              const Params &P, const Shape &sh, cudaStream_t s);
-// D3Q27, central moments, AA only; masked 0 or 1.
+// D3Q27, central moments, AA only; masked as above.
 cudaError_t launch_step_d3q27(int masked, bool odd, bool narrow, const Params &P,
                               const Shape &sh, cudaStream_t s);
 // Two-buffer modes: one PULL step, or one SPLIT step (collide + stream), from P.f/P.g

@@ -67,8 +67,6 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
             return bad(LBM_ERR_UNSUPPORTED, "D3Q27 takes no thermal lattice");
         if (c->streaming != LBM_STREAM_AA)
             return bad(LBM_ERR_UNSUPPORTED, "D3Q27 runs the AA layout only");
-        if (c->ib_max_samples > 0)
-            return bad(LBM_ERR_UNSUPPORTED, "D3Q27 takes no immersed-boundary samples");
     }
     if (c->nx < 1 || c->ny < 1 || c->nz < 1) return bad(LBM_ERR_ARG, "grid sizes must be >= 1");
     if (c->lattice == LBM_D2Q9 && c->nz != 1) return bad(LBM_ERR_ARG, "D2Q9 needs nz == 1");

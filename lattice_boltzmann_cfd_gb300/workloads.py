@@ -183,11 +183,12 @@ def sphere_samples(center, radius: float, n: int, seed: int = 0) -> np.ndarray:
 
 def channel_ib_sphere(n: int = 128, radius: float = 16, center=(40, 64, 64),
                       gx: float = 1e-6, nu: float = 0.02, samples_per_area: float = 4.0,
-                      shape=None) -> Workload:
+                      shape=None, lattice: int = 19) -> Workload:
     """Config 3's channel with the sphere represented by immersed-boundary samples instead
     of bounce-back cells: samples_per_area samples per unit area, each weighted by the area
     it represents, at rest."""
-    w = channel_sphere(n=n, radius=radius, center=center, gx=gx, nu=nu, shape=shape)
+    w = channel_sphere(n=n, radius=radius, center=center, gx=gx, nu=nu, shape=shape,
+                       lattice=lattice)
     area = 4.0 * math.pi * radius * radius
     ns = max(4, int(round(samples_per_area * area)))
     x = sphere_samples(center, radius, ns)

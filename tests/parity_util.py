@@ -217,7 +217,10 @@ def d3q27_cases():
     ch = W.perturbed(W.channel_sphere(shape=(12, 10, 9), center=(5, 4, 4), radius=2.5,
                                       lattice=27), seed=13)
     ch = dataclasses.replace(ch, g_body=(1e-4, 2e-5, -1e-5))
-    return [rp, distinct, ch]
+    ib = W.channel_ib_sphere(shape=(14, 12, 11), center=(6.3, 5.7, 5.2), radius=2.6,
+                             gx=1e-4, samples_per_area=2.0, lattice=27)
+    ib = dataclasses.replace(W.perturbed(ib, seed=14), name=ib.name + " perturbed")
+    return [rp, distinct, ch, ib]
 
 
 def split_steps(n):

@@ -178,13 +178,13 @@ def test_product_package_does_not_import_oracle():
     ({"tau": 0.5}, 1, "tau"),
     ({"thermal": 7}, 2, "thermal"),
     ({"streaming": 1}, 2, "AA layout"),
-    ({"ib_max_samples": 8}, 2, "immersed"),
 ])
 def test_d3q27_configs_validated(capi, overrides, status, text):
-    """D3Q27 takes the central-moment collision only, rates in (0, 2), no thermal lattice,
-    no immersed-boundary samples and the AA layout only."""
+    """D3Q27 takes the central-moment collision only, rates in (0, 2), no thermal lattice
+    and the AA layout only (immersed-boundary samples are accepted)."""
     w = W.random_periodic(shape=(8, 6, 5), lattice=27)
     assert _bytes(capi, w) > 0
+    assert _bytes(capi, w, ib_max_samples=8) > _bytes(capi, w)
     with pytest.raises(capi.LbmError) as e:
         _bytes(capi, w, **overrides)
     assert e.value.status == status

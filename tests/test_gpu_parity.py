@@ -68,7 +68,11 @@ IB_CASES = [W.channel_ib_sphere(shape=(300, 24, 20), center=(40.3, 11.6, 9.8), r
             dataclasses.replace(
                 W.perturbed(W.channel_ib_sphere(shape=(300, 24, 20), center=(40.3, 11.6, 9.8),
                                                 radius=6, gx=1e-5), seed=24),
-                name="IB channel perturbed")]
+                name="IB channel perturbed"),
+            dataclasses.replace(
+                W.perturbed(W.channel_ib_sphere(shape=(300, 20, 18), center=(40.3, 9.6, 8.8),
+                                                radius=5, gx=1e-5, lattice=27), seed=27),
+                name="D3Q27 IB channel perturbed")]
 
 
 def _compare_ib(got, ref):
@@ -79,10 +83,13 @@ def _compare_ib(got, ref):
 
 
 @pytest.mark.parametrize("streaming", ["aa", "pull", "split"])
-@pytest.mark.parametrize("w", IB_CASES, ids=["IB sphere rest start", "IB sphere perturbed"])
+@pytest.mark.parametrize("w", IB_CASES, ids=["IB sphere rest start", "IB sphere perturbed",
+                                             "D3Q27 IB sphere perturbed"])
 def test_immersed_boundary_200_and_201_steps(oracle_mod, w, streaming):
     """Immersed-boundary sphere in the channel against the oracle: fields after 200 and 201
     steps, reaction force (1e-4 relative) and torque."""
+    if w.lattice == 27 and streaming != "aa":
+        pytest.skip("D3Q27 runs the AA layout only")
     ref = oracle_states(oracle_mod, w, [200, 201])
     got = gpu_states(w, [200, 201], streaming=streaming)
     for n in (200, 201):
@@ -257,17 +264,22 @@ def _windows(shape, size, steps, rng, extra=6):
                                           ("cavity2d", False), ("cavity2d", True),
                                           ("random_periodic_512", True),
                                           ("random_periodic_wide", True),
-                                          ("d3q27_periodic_512", True)])
+                                          ("d3q27_periodic_512", True),
+                                          ("d3q27_periodic_wide", True)])
 def test_full_size_sampled_windows(oracle_mod, name, perturb):
     """At the full 512^3 / 4096^2 sizes, in the launch configuration the benchmark uses:
     after 1, 2 and 3 steps every cell of sampled windows (corners, edges, faces, centre,
     random) matches the oracle run on that window (cells the window's cut faces can
-    reach are unknown to the oracle and skipped).  The 640x640x568 case has more than 2^32
-    population slots, so its steps take the 64-bit index form."""
+    reach are unknown to the oracle and skipped).  The 640x640x568 D3Q19 and 576x560x560
+    D3Q27 cases have more than 2^32 population slots, so their steps take the 64-bit index
+    form."""
     if name == "random_periodic_512":
         w = W.random_periodic(n=512, seed=2)
     elif name == "d3q27_periodic_512":
         w = W.random_periodic(n=512, seed=2, lattice=27)
+    elif name == "d3q27_periodic_wide":
+        w = W.random_periodic(shape=(576, 560, 560), seed=4, lattice=27)
+        assert 27 * ((w.cells + 63) // 64 * 64) > 2 ** 32
     elif name == "random_periodic_wide":
         w = W.random_periodic(shape=(640, 640, 568), seed=3)
         assert 19 * ((w.cells + 63) // 64 * 64) > 2 ** 32
