@@ -1,0 +1,67 @@
+"""JobPipeline (host-link copies overlapped with the neighbouring jobs' steps) against the
+same jobs run one after another: every job's outputs and diagnostics are bit-identical."""
+import numpy as np
+import pytest
+
+from lattice_boltzmann_cfd_gb300 import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+
+
+def _pinned(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+
+@pytest.mark.parametrize("make", [lambda s: W.perturbed(W.cavity3d(shape=(48, 20, 18)), seed=s),
+                                  lambda s: W.random_periodic(shape=(64, 24, 20), seed=s),
+                                  lambda s: W.perturbed(W.cavity2d(shape=(96, 80, 1)), seed=s)],
+                         ids=["cavity3d", "periodic", "cavity2d"])
+def test_pipeline_matches_serial_jobs(make):
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    from lattice_boltzmann_cfd_gb300.pipeline import JobPipeline
+    ws = [make(seed) for seed in (3, 4, 5, 6, 7)]
+    steps = 9
+    jobs = []
+    for w in ws:
+        ins = tuple(_pinned(a) for a in (w.rho0, w.u0, w.T_init if w.thermal else None))
+        outs = tuple(None if t is None else torch.empty_like(t).pin_memory() for t in ins)
+        jobs.append((ins, outs))
+    # one after another, on device buffers
+    sim = Simulation(ws[0])
+    serial = []
+    for (ins, _), w in zip(jobs, ws):
+        dev = [None if t is None else t.cuda() for t in ins]
+        sim.init_equilibrium(*dev)
+        sim.step(steps)
+        rho, u, T = sim.macroscopic()
+        serial.append(([t.cpu() for t in (rho, u) + ((T,) if T is not None else ())],
+                       sim.diagnostics()))
+    sim.close()
+    # pipelined
+    sim = Simulation(ws[0])
+    diags = JobPipeline(sim).run(jobs, steps)
+    sim.close()
+    for (fields, d), (_, outs), dp in zip(serial, jobs, diags):
+        for a, b in zip(fields, [t for t in outs if t is not None]):
+            assert torch.equal(a, b)
+        for key in ("mass", "momentum", "heat", "fluid_cells", "uT"):
+            assert d[key] == dp[key], key
+
+
+def test_pipeline_without_readout():
+    """Jobs whose outputs are None run and return diagnostics only."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    from lattice_boltzmann_cfd_gb300.pipeline import JobPipeline
+    w = W.random_periodic(shape=(32, 16, 16), seed=9)
+    ins = (_pinned(w.rho0), _pinned(w.u0), None)
+    sim = Simulation(w)
+    diags = JobPipeline(sim).run([(ins, None)] * 3, 4)
+    assert len(diags) == 3 and diags[0]["mass"] == diags[2]["mass"]
+    sim.close()
