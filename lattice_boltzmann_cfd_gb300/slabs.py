@@ -132,7 +132,6 @@ class SlabDomain:
         self.n_outer = w.shape[self.axis]
         self.periodic = w.face_flow[2 * self.axis] == "periodic"
         devices = list(devices) if devices else [torch.device("cuda")]
-        self.ranges = split_ranges(self.n_outer, nslabs) if 1 <= nslabs <= self.n_outer else []
         self.slabs, self.sides, self.plane_lists, self.buffers = [], [], [], []
         for r in range(nslabs):
             local, sides, planes = slab_part(w, nslabs, r)
