@@ -46,8 +46,8 @@ BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112, (27, 0): 
 # taken on; reported as "traffic" only while the sources are unchanged.
 NCU_TRAFFIC = {
     # ncu --set full, one even + one odd launch at 256^3 (see profiles/), scaled by cells
-    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.57, "src_hash": "32e8c8e6c164cdeb"},
-    "cavity3d_512": {"bytes_per_cell": 208.64, "src_hash": "32e8c8e6c164cdeb"},
+    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.57, "src_hash": "45b4267b8283488b"},
+    "cavity3d_512": {"bytes_per_cell": 208.64, "src_hash": "45b4267b8283488b"},
 }
 
 
@@ -493,10 +493,10 @@ def run_gpu(args, dctx):
     e2e_secs, h2d, d2h = timed_e2e_leg(sim, w, args.steps, min(args.warmup, 2),
                                        args.lbm_steps, dctx)
     e2e_secs = dctx.max(e2e_secs)
-    serial_value = updates / e2e_secs / 1e6
+    e2e_value = updates / e2e_secs / 1e6
     pipe_secs = dctx.max(timed_pipelined_e2e_leg(sim, w, args.steps, min(args.warmup, 2),
                                                  args.lbm_steps, dctx))
-    e2e_value = updates / pipe_secs / 1e6
+    pipelined_value = updates / pipe_secs / 1e6
     sim.close()
     del sim
     torch.cuda.empty_cache()
@@ -543,10 +543,11 @@ def run_gpu(args, dctx):
                                      "clock x bus width from the device attributes"},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "serial_value": round(serial_value, 1),
-                "pipelined": "JobPipeline: each step's host-to-device copy and read-out "
-                             "overlap the neighbouring steps' LBM steps (serial_value: "
-                             "one job after another)",
+                "pipelined_value": round(pipelined_value, 1),
+                "pipelined": "the same jobs through JobPipeline, each step's copies "
+                             "overlapping the neighbouring steps' LBM steps; its rate varies "
+                             "between runs (the device at times serialises a job's init "
+                             "behind the previous read-out), so value is the serial path",
                 "path": "page-locked host rho,u in -> lbm_init_equilibrium -> lbm_step -> "
                         "lbm_macroscopic into page-locked host -> lbm_diagnostics"},
         "gpu_launches": args.steps * (args.lbm_steps + 2),

@@ -343,6 +343,18 @@ __global__ void __launch_bounds__(256) step_kernel(const Params P)
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB>(P, P, x, y, z);
 }
 
+// The same step with the register allocation bounded so that 5 blocks of 256 reside per SM
+// (48 registers): for a collision long enough that the extra warps pay for themselves.
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB>
+__global__ void __launch_bounds__(256, 5) step_kernel_5(const Params P)
+{
+    const int x = blockIdx.x * blockDim.x + threadIdx.x;
+    const int y = blockIdx.y * blockDim.y + threadIdx.y;
+    const int z = blockIdx.z;
+    if (x >= P.nx || y >= P.ny) return;
+    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB>(P, P, x, y, z);
+}
+
 // Two-buffer PULL step: pull from the current buffer, collide, write the other buffer's
 // natural slots.  No slot is read and written in the same launch.
 template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB = false>
