@@ -173,6 +173,27 @@ def outer_walls_case(shape=(12, 7, 11), seed=37):
         T_wall=(0.0, 0.0, 0.0, 0.0, 0.4, -0.3))
 
 
+def degenerate_cases():
+    """Grids of extent 1 or 2 along some axes (every neighbour is the cell itself or its one
+    neighbour, through a wrap or a wall), on every lattice."""
+    out = []
+    for shape in ((1, 1, 1), (1, 2, 3), (3, 1, 2), (2, 3, 1)):
+        out.append(W.random_periodic(shape=shape, seed=50 + sum(shape)))
+        walled = W.perturbed(W.cavity3d(shape=shape), seed=60 + sum(shape))
+        out.append(dataclasses.replace(walled, name=walled.name + f" {shape}", gbeta=0.02))
+    for shape in ((1, 1, 1), (1, 5, 1), (4, 1, 1)):
+        out.append(W.random_periodic(shape=shape, seed=70 + sum(shape), lattice=9))
+        c2 = W.perturbed(W.cavity2d(shape=shape), seed=80 + sum(shape))
+        out.append(dataclasses.replace(c2, name=c2.name + f" {shape}", gbeta=0.02))
+    for shape in ((1, 1, 1), (2, 1, 3)):
+        out.append(W.random_periodic(shape=shape, seed=90 + sum(shape), lattice=27))
+        ch = W.perturbed(W.channel_sphere(shape=shape, center=(0, 0, 0), radius=0.0,
+                                          lattice=27), seed=95 + sum(shape))
+        out.append(dataclasses.replace(ch, name=ch.name + f" {shape}", solid=None,
+                                       g_body=(1e-3, 0.0, 0.0)))
+    return out
+
+
 def small_cases():
     """Small problems covering every lattice, collision, boundary kind and forcing."""
     cases = [W.random_periodic(shape=(6, 5, 4), seed=1),

@@ -10,8 +10,8 @@ parity-aware.  The link mask is compared bit for bit with a brute-force builder.
 import numpy as np
 import pytest
 
-from parity_util import (emulate, emulate_slabs, fluid_of, mask_brute_force, oracle_states,
-                         outer_walls_case, slab_cases, small_cases)
+from parity_util import (degenerate_cases, emulate, emulate_slabs, fluid_of, mask_brute_force,
+                         oracle_states, outer_walls_case, slab_cases, small_cases)
 
 CASES = small_cases()
 
@@ -83,3 +83,22 @@ def test_slabs_match_single_domain_bitwise(oracle_mod, emu_lib, w):
             if w.thermal:
                 assert not np.isnan(gs).any(), (n, k)
                 assert np.array_equal(gs, g1), (n, k)
+
+
+DEGENERATE = degenerate_cases()
+
+
+@pytest.mark.parametrize("mode", ["aa", "pull", "split"])
+@pytest.mark.parametrize("w", DEGENERATE, ids=[c.name for c in DEGENERATE])
+def test_degenerate_grids(oracle_mod, emu_lib, w, mode):
+    """Extents of 1 or 2: the wrapped or walled neighbour is the cell itself or its twin."""
+    if w.lattice == 27 and mode != "aa":
+        pytest.skip("D3Q27 runs the AA layout only")
+    ref = oracle_states(oracle_mod, w, [1, 2, 5, 6])
+    fluid = fluid_of(w)
+    for n, r in ref.items():
+        f, g, m = emulate(emu_lib, w, n, True, mode)
+        assert np.abs(f - r["f"])[:, fluid].max() < 1e-6, n
+        if w.thermal:
+            assert np.abs(g - r["g"])[:, fluid].max() < 1e-6, n
+    assert np.array_equal(emulate(emu_lib, w, 0)[2], mask_brute_force(w))

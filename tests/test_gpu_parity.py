@@ -12,8 +12,8 @@ import numpy as np
 import pytest
 
 from lattice_boltzmann_cfd_gb300 import workloads as W
-from parity_util import (TOL_FIELDS, TOL_FORCE_REL, compare_fields, fluid_of, gpu_states,
-                         mask_brute_force, oracle_states, small_cases)
+from parity_util import (TOL_FIELDS, TOL_FORCE_REL, compare_fields, degenerate_cases, fluid_of,
+                         gpu_states, mask_brute_force, oracle_states, small_cases)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -43,6 +43,22 @@ def test_small_grids_few_steps(oracle_mod, w, streaming):
     for n in ref:
         compare_fields(w, got[n], ref[n], tol=1e-6)
         assert got[n]["parity"] == n % 2
+
+
+DEGENERATE = degenerate_cases()
+
+
+@pytest.mark.parametrize("streaming", ["aa", "pull", "split"])
+@pytest.mark.parametrize("w", DEGENERATE, ids=[c.name for c in DEGENERATE])
+def test_degenerate_grids(oracle_mod, w, streaming):
+    """Extents of 1 or 2 along some axes (the neighbour through a wrap or a wall is the cell
+    itself or its twin), every lattice, 1, 2, 5 and 6 steps."""
+    if w.lattice == 27 and streaming != "aa":
+        pytest.skip("D3Q27 runs the AA layout only")
+    ref = oracle_states(oracle_mod, w, [1, 2, 5, 6])
+    got = gpu_states(w, [1, 2, 5, 6], streaming=streaming)
+    for n in ref:
+        compare_fields(w, got[n], ref[n], tol=1e-6)
 
 
 # --------------------------------------------------- 200 / 201 steps, all configs ---
