@@ -115,7 +115,8 @@ enum { LBM_STREAM_AA = 0, LBM_STREAM_PULL = 1, LBM_STREAM_SPLIT = 2 };
  * bounce back f, and bounce back g (adiabatic face or solid) or anti-bounce-back g
  * (DIRICHLET face, wall temperature T_wall[face]). */
 typedef struct {
-    int nx, ny, nz;       /* cells; nz == 1 for D2Q9; nx*ny*nz < 2^31                  */
+    int nx, ny, nz;       /* cells; nz == 1 for D2Q9; nx*ny*nz < 2^31; nz <= 65535;
+                             ny <= 65535 (131070 when nx <= 32): launch-grid extents     */
     int lattice;          /* LBM_D3Q19, LBM_D2Q9 or LBM_D3Q27                          */
     int thermal;          /* LBM_THERMAL_NONE, LBM_D3Q7 (with D3Q19), LBM_D2Q5 (D2Q9)  */
     int collision;        /* LBM_BGK or LBM_MRT (D3Q19, D2Q9); LBM_CM (D3Q27)           */

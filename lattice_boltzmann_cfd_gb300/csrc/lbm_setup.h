@@ -73,7 +73,9 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     const long long N = (long long)c->nx * c->ny * c->nz;
     if (N >= (1LL << 31)) return bad(LBM_ERR_ARG, "nx*ny*nz must be < 2^31");
     if (c->nz > 65535) return bad(LBM_ERR_UNSUPPORTED, "nz must be <= 65535");
-    if (c->ny > 65535 * 8) return bad(LBM_ERR_UNSUPPORTED, "ny too large");
+    if (lbm::cell_shape(c->nx, c->ny, c->nz).grid.y > 65535)
+        return bad(LBM_ERR_UNSUPPORTED,
+                   "ny too large: ny / (rows per block) must be <= 65535 (ny <= 65535 once nx > 32)");
     if (c->collision == LBM_BGK && !(std::isfinite(c->tau) && c->tau > 0.5))
         return bad(LBM_ERR_ARG, "BGK tau must be finite and > 1/2");
     const int Q = c->lattice;

@@ -202,3 +202,17 @@ def test_d3q27_workspace_holds_27_planes(capi):
     assert _bytes(capi, w) >= 27 * S * 4
     # slab halos of D3Q27 move the 9 populations with c_z = +-1
     assert _bytes(capi, w, face_flow=[0, 0, 0, 0, 2, 2]) > 0
+
+
+def test_launch_grid_limits(capi):
+    """The launch grid's y extent (ny over the rows per block) and z extent (nz) stay within
+    65535: rows of 64 cells take one y row per block, rows of 32 or fewer two."""
+    w = W.random_periodic(shape=(8, 8, 8))
+    assert _bytes(capi, w, nx=64, ny=65535, nz=1) > 0
+    with pytest.raises(capi.LbmError, match="ny too large"):
+        _bytes(capi, w, nx=64, ny=65536, nz=1)
+    assert _bytes(capi, w, nx=32, ny=131070, nz=1) > 0
+    with pytest.raises(capi.LbmError, match="ny too large"):
+        _bytes(capi, w, nx=32, ny=131071, nz=1)
+    with pytest.raises(capi.LbmError, match="nz must be"):
+        _bytes(capi, w, nx=4, ny=4, nz=65536)
