@@ -132,17 +132,33 @@ cudaError_t pop_go(bool masked, int pat, const Params &P, float *f, float *g, cu
     return cudaGetLastError();
 }
 
+// Blocks of a grid-stride kernel that make exactly one resident wave on this device (every
+// block then does the same share of the work, and none waits for a second wave).
+template <class K>
+int one_wave(K kernel, int threads, int cap)
+{
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess ||
+        sms * per_sm < 1)
+        return cap;
+    return sms * per_sm < cap ? sms * per_sm : cap;
+}
+
 template <class L, class TL>
 cudaError_t diag_go(bool masked, int pat, const Params &P, double *partial, double *out,
                     cudaStream_t s)
 {
-    const dim3 g(DIAG_BLOCKS), b(DIAG_THREADS);
+    int blocks = DIAG_BLOCKS;
     with_pattern(masked, pat, [&](auto m, auto p) {
-        diag_kernel<L, TL, decltype(m)::value, decltype(p)::value><<<g, b, 0, s>>>(P, partial);
+        auto kernel = diag_kernel<L, TL, decltype(m)::value, decltype(p)::value>;
+        blocks = one_wave(kernel, DIAG_THREADS, DIAG_BLOCKS);
+        kernel<<<blocks, DIAG_THREADS, 0, s>>>(P, partial);
     });
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    diag_finalize<<<1, DIAG_THREADS, 0, s>>>(partial, DIAG_BLOCKS, out);
+    diag_finalize<<<1, DIAG_THREADS, 0, s>>>(partial, blocks, out);
     return cudaGetLastError();
 }
 }  // namespace

@@ -28,7 +28,7 @@ inline Shape cell_shape(int nx, int ny, int nz, int threads = 64)
     return s;
 }
 
-constexpr int DIAG_BLOCKS = 1024;
+constexpr int DIAG_BLOCKS = 2048;   // capacity of the partial-sum rows (one resident wave at most)
 
 // Each returns the launch error (cudaGetLastError) of what it enqueued.
 // narrow: every population index fits in 32 bits (see slot()).  masked: 0 = no link

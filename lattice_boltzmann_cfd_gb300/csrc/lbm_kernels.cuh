@@ -800,12 +800,33 @@ constexpr int DIAG_VALUES = 18;
 constexpr int DIAG_N = 20;   // row stride of the partial sums
 constexpr int DIAG_THREADS = 256;
 
+constexpr int DIAG_CHUNK = 16;   // cells summed in fp32 before joining the fp64 totals
+
+// The sums every fluid cell contributes (rho - 1, j, u T) run in fp32 over chunks of
+// DIAG_CHUNK cells and join the fp64 totals once per chunk: GB300's fp64 rate is low enough
+// that one fp64 add and conversion per value and cell would cost as much as the reads.
+// The chunks' rounding (~1e-7 relative on sums of 16 deviation-sized values) stays far
+// below the diagnostics' use.  Counts are integers; the rare wall and solid terms stay fp64.
 template <class L, class TL, bool MASKED, int PAT>
 __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, double *partial)
 {
     double acc[DIAG_VALUES];
 #pragma unroll
     for (int i = 0; i < DIAG_VALUES; ++i) acc[i] = 0.0;
+    float part[7] = {0, 0, 0, 0, 0, 0, 0};   // rho - 1, j, u T of the current chunk
+    int in_chunk = 0, cells = 0, nonfinite = 0;
+    auto flush = [&]() {
+        acc[0] += part[0];
+        acc[1] += part[1];
+        acc[2] += part[2];
+        acc[3] += part[3];
+        acc[15] += part[4];
+        acc[16] += part[5];
+        acc[17] += part[6];
+#pragma unroll
+        for (int k = 0; k < 7; ++k) part[k] = 0.0f;
+        in_chunk = 0;
+    };
     const long long N = (long long)P.nx * P.ny * P.nz;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < N;
          i += (long long)gridDim.x * blockDim.x) {
@@ -829,23 +850,23 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
             if (L::cy(q)) jy += L::cy(q) * f[q];
             if (L::cz(q)) jz += L::cz(q) * f[q];
         }
-        acc[0] += dr;
-        acc[1] += jx;
-        acc[2] += jy;
-        acc[3] += jz;
+        part[0] += dr;
+        part[1] += jx;
+        part[2] += jy;
+        part[3] += jz;
         if constexpr (TL::Q > 0) {
 #pragma unroll
             for (int k = 0; k < TL::Q; ++k) t += g[k];
         }
-        if (!isfinite(dr) || !isfinite(t)) acc[13] += 1.0;
-        acc[14] += 1.0;
+        if (!isfinite(dr) || !isfinite(t)) ++nonfinite;
+        ++cells;
         if constexpr (TL::Q > 0) {
             // convective transport, with the velocity of the macroscopic read-out
             float Fx, Fy, Fz, ux, uy, uz;
             force_velocity<true>(P.c, 1.0f + dr, t, jx, jy, jz, Fx, Fy, Fz, ux, uy, uz);
-            acc[15] += ux * t;
-            acc[16] += uy * t;
-            acc[17] += uz * t;
+            part[4] += ux * t;
+            part[5] += uy * t;
+            part[6] += uz * t;
         }
         if (MASKED) {
             // links into solid cells: the bounced-back population of the last step is the
@@ -878,7 +899,11 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
                     acc[8 + 2 * a] += 2.0 * (P.T_wall[2 * a + 1] - t);
             }
         }
+        if (++in_chunk == DIAG_CHUNK) flush();
     }
+    flush();
+    acc[13] = nonfinite;
+    acc[14] = cells;
     // block reduction in a fixed order: warp shuffles, then warps in order
     __shared__ double sh[DIAG_THREADS / 32][DIAG_VALUES];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
