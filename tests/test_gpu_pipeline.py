@@ -65,3 +65,15 @@ def test_pipeline_without_readout():
     diags = JobPipeline(sim).run([(ins, None)] * 3, 4)
     assert len(diags) == 3 and diags[0]["mass"] == diags[2]["mass"]
     sim.close()
+
+
+def test_ib_block_search_returns_the_fastest_candidate():
+    """The measured search of the immersed-boundary block edge times every candidate and
+    returns the one with the lowest step time."""
+    from lattice_boltzmann_cfd_gb300.tuning import default_candidates, search_ib_block
+    w = W.channel_ib_sphere(shape=(64, 48, 48), center=(20.3, 23.7, 24.2), radius=8)
+    cands = default_candidates(w)
+    assert cands[0] == 2 and cands[-1] == 16
+    best, times = search_ib_block(w, candidates=[2, 4, 8], steps=8, warmup=2)
+    assert set(times) == {2, 4, 8} and all(t > 0 for t in times.values())
+    assert times[best] == min(times.values())
