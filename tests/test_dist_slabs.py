@@ -111,3 +111,37 @@ def test_slab_parts_tile_the_domain():
                 np_axis = 0 if w.dim == 3 else 1
                 assert np.array_equal(local.rho0, np.take(w.rho0, planes, axis=np_axis))
             assert owned == list(range(n))
+
+
+def _dying_worker(rank, world, port, out):
+    import datetime
+    import time
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import torch.distributed as dist
+    from lattice_boltzmann_cfd_gb300.slabs import ring_exchange
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=8))
+    dist.barrier()
+    if rank == 1:
+        os._exit(0)                  # leaves between steps: no exchange in flight
+    send = [torch.zeros(4), torch.zeros(4)]
+    recv = [torch.zeros(4), torch.zeros(4)]
+    t0 = time.time()
+    try:
+        ring_exchange(0, 2, True, 0, lambda s, p, b: b.fill_(1.0), lambda s, p, b: None,
+                      send, recv)
+        out[0] = ("completed", 0.0)
+    except Exception as e:           # the back-end reports the lost peer
+        out[0] = (type(e).__name__, time.time() - t0)
+
+
+def test_lost_rank_fails_the_next_exchange():
+    """A rank that leaves between steps makes its neighbour's next halo exchange raise (a
+    lost connection, or the process group's timeout) instead of waiting forever."""
+    import torch.multiprocessing as mp
+    port = _free_port()
+    out = mp.get_context("spawn").Manager().dict()
+    mp.spawn(_dying_worker, args=(2, port, out), nprocs=2, join=True)
+    kind, seconds = out[0]
+    assert kind != "completed"
+    assert seconds < 30
