@@ -476,16 +476,21 @@ LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float
     }
     const int idx = q[0] + P.nx * (q[1] + P.ny * q[2]);
     K = k;
+    // the populations load as if no link were a wall, together with the mask (one memory
+    // round trip instead of two); wall links are fixed once the mask is in
     const uint32_t m = P.mask ? P.mask[idx] : 0u;
+    Offs o{};
+    if (PAT != NATURAL) o = make_offs(q[0], q[1], q[2], P);
+    float f[L::Q], g[TL::QA];
+    load_cell<L, TL, false, PAT>(P, idx, o, 0u, f, g);
     if (m & SOLID_BIT) {
         Krho = k;
         Ku[0] = Ku[1] = Ku[2] = 0.0f;
         return idx;
     }
-    Offs o{};
-    if (PAT != NATURAL) o = make_offs(q[0], q[1], q[2], P);
-    float f[L::Q], g[TL::QA];
-    load_cell<L, TL, true, PAT>(P, idx, o, m, f, g);
+    if constexpr (PAT != NATURAL) {
+        if (m & wall_bits<L>()) fix_wall_loads<L, TL, PAT, false>(P, idx, m, f, g);
+    }
     float dr = 0.0f, jx = 0.0f, jy = 0.0f, jz = 0.0f, t = 0.0f;
     for (int i = 0; i < L::Q; ++i) {
         dr += f[i];
@@ -506,13 +511,21 @@ LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float
     return idx;
 }
 
-// Penalty of sample s from its interpolated rho and u: g = w rho (u_b - u).
+// Penalty from a sample's weight w, boundary velocity u_b and interpolated rho and u:
+// g = w rho (u_b - u).
+template <class L>
+LBM_HD void ib_penalty(float w, const float (&ub)[3], float rho, const float (&u)[3],
+                       float (&gs)[3])
+{
+    for (int a = 0; a < 3; ++a) gs[a] = (a < L::DIM) ? w * rho * (ub[a] - u[a]) : 0.0f;
+}
+
+// The same for sample s of the parameter block.
 template <class L>
 LBM_HD void ib_penalty(const Params &P, int s, float rho, const float (&u)[3], float (&gs)[3])
 {
-    const float w = P.ibw[s];
-    for (int a = 0; a < 3; ++a)
-        gs[a] = (a < L::DIM) ? w * rho * (P.ibub[a * P.ib_cap + s] - u[a]) : 0.0f;
+    const float ub[3] = {P.ibub[s], P.ibub[P.ib_cap + s], P.ibub[2 * P.ib_cap + s]};
+    ib_penalty<L>(P.ibw[s], ub, rho, u, gs);
 }
 
 // Whole sample s, corner by corner (the host emulation's form of the kernel below).
@@ -543,8 +556,14 @@ __global__ void __launch_bounds__(128) ib_kernel(const Params P)
     const int s = t / CORNERS, c = t % CORNERS;
     const bool active = s < P.ib_n;
     float K = 0.0f, kr = 0.0f, ku[3] = {0.0f, 0.0f, 0.0f};
+    float w = 0.0f, ub[3] = {0.0f, 0.0f, 0.0f};
     int idx = 0;
-    if (active) idx = ib_corner<L, TL, PAT>(P, s, c, K, kr, ku);
+    if (active) {
+        // the sample's own data first, so that its loads overlap the cell's
+        w = P.ibw[s];
+        for (int a = 0; a < 3; ++a) ub[a] = P.ibub[a * P.ib_cap + s];
+        idx = ib_corner<L, TL, PAT>(P, s, c, K, kr, ku);
+    }
 #pragma unroll
     for (int off = 1; off < CORNERS; off <<= 1) {
         kr += __shfl_xor_sync(0xffffffffu, kr, off, CORNERS);
@@ -552,7 +571,7 @@ __global__ void __launch_bounds__(128) ib_kernel(const Params P)
     }
     if (!active) return;
     float gs[3];
-    ib_penalty<L>(P, s, kr, ku, gs);
+    ib_penalty<L>(w, ub, kr, ku, gs);
     if (c == 0)
         for (int a = 0; a < 3; ++a) P.ibg[a * P.ib_cap + s] = gs[a];
     if (P.mask[idx] & SOLID_BIT) return;
