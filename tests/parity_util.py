@@ -10,7 +10,7 @@ import numpy as np
 from lattice_boltzmann_cfd_gb300 import workloads as W
 from lattice_boltzmann_cfd_gb300.solver import make_config
 
-# the benchmark spec tolerances: fp32 GPU vs fp64 oracle after 200 steps
+# parity tolerances: fp32 GPU against the fp64 oracle after 200 steps
 TOL_FIELDS = 2e-5      # max-abs on rho, u, T
 TOL_FORCE_REL = 1e-4   # relative on the solid force
 
