@@ -180,6 +180,127 @@ LBM_HD void fix_wall_loads(const Params &P, int idx, uint32_t m, float (&f)[L::Q
 template <class L>
 LBM_HD constexpr uint32_t wall_bits() { return (1u << L::Q) - 2u; }
 
+// Mask bits of the links with c_x = SIGN (the links that leave through the -x face when
+// SIGN = -1, through the +x face when SIGN = +1).
+template <class L, int SIGN>
+LBM_HD constexpr uint32_t x_links()
+{
+    uint32_t b = 0;
+    for (int q = 1; q < L::Q; ++q)
+        if (L::cx(q) == SIGN) b |= 1u << q;
+    return b;
+}
+
+// The wall links of cell x that the coordinates alone decide: those through an x face that
+// is a wall.  With walls on x every row of cells has one such cell at each end, so the
+// first and last warp of each row would otherwise wait for the mask before loading them.
+template <class L>
+LBM_HD uint32_t x_wall_links(const Params &P, int x)
+{
+    uint32_t b = 0;
+    if (x == 0 && P.face_wall[0]) b |= x_links<L, -1>();
+    if (x == P.nx - 1 && P.face_wall[1]) b |= x_links<L, +1>();
+    return b;
+}
+
+// Mask bits of the links with c_a = SIGN along axis a, and the Dirichlet bits of the
+// thermal links among them (thermal link k is flow link k, an axis link).
+template <class L, int A, int SIGN>
+LBM_HD constexpr uint32_t axis_links()
+{
+    uint32_t b = 0;
+    for (int q = 1; q < L::Q; ++q) {
+        const int c = A == 0 ? L::cx(q) : A == 1 ? L::cy(q) : L::cz(q);
+        if (c == SIGN) b |= 1u << q;
+    }
+    return b;
+}
+
+template <class L, class TL, int A, int SIGN>
+LBM_HD constexpr uint32_t axis_dirichlet()
+{
+    uint32_t b = 0;
+    for (int k = 1; k < TL::Q; ++k) {
+        const int c = A == 0 ? L::cx(k) : A == 1 ? L::cy(k) : L::cz(k);
+        if (c == SIGN) b |= 1u << (DIRICHLET_SHIFT + k);
+    }
+    return b;
+}
+
+// Faces of axis A that cell coordinate c touches, as mask bits (wall links, and the
+// Dirichlet bits of the thermal links through Dirichlet faces).
+template <class L, class TL, int A>
+LBM_HD uint32_t face_bits(const Params &P, int c, int n)
+{
+    uint32_t m = 0;
+    if (c == 0 && P.face_wall[2 * A])
+        m |= axis_links<L, A, -1>() | (P.face_dir[2 * A] ? axis_dirichlet<L, TL, A, -1>() : 0u);
+    if (c == n - 1 && P.face_wall[2 * A + 1])
+        m |= axis_links<L, A, +1>() | (P.face_dir[2 * A + 1] ? axis_dirichlet<L, TL, A, +1>() : 0u);
+    return m;
+}
+
+// The link mask of a cell of a domain whose walls are all domain faces (no solid cell):
+// cell_mask without the solid array, for every cell that is not on a slab's ghost plane.
+// A link is a wall link when it leaves through a wall face along any axis; a thermal link
+// crosses one face only.
+template <class L, class TL>
+LBM_HD uint32_t face_mask(const Params &P, int x, int y, int z)
+{
+    uint32_t m = face_bits<L, TL, 0>(P, x, P.nx) | face_bits<L, TL, 1>(P, y, P.ny);
+    if constexpr (L::DIM == 3) m |= face_bits<L, TL, 2>(P, z, P.nz);
+    return m;
+}
+
+// Odd-step load (read pattern AA_ODD) that redirects the links in xw, a subset of
+// x_wall_links, to the cell's own slots, as load_cell does for every wall link, and loads
+// all other links from the neighbours.  Thermal values are the raw stored ones: the
+// anti-bounce-back sign flip and omega T_w need the mask (abb_x_links).
+template <class L, class TL, bool NARROW>
+LBM_HD void load_odd_xwall(const Params &P, int idx, const Offs &o, uint32_t xw,
+                           float (&f)[L::Q], float (&g)[TL::QA])
+{
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q) {
+        if (q == 0) {
+            f[q] = P.f[slot<NARROW>(P, 0, idx)];
+            continue;
+        }
+        const int oq = L::opp(q);
+        const bool wall_in = L::cx(q) != 0 && bit(xw, oq);
+        f[q] = P.f[wall_in ? slot<NARROW>(P, q, idx)
+                           : slot<NARROW>(P, oq, idx + nb(o, -L::cx(q), -L::cy(q), -L::cz(q)))];
+    }
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 0; k < TL::Q; ++k) {
+            if (k == 0) {
+                g[k] = P.g[slot<NARROW>(P, 0, idx)];
+                continue;
+            }
+            const int ok = L::opp(k);
+            const bool wall_in = L::cx(k) != 0 && bit(xw, ok);
+            g[k] = P.g[wall_in ? slot<NARROW>(P, k, idx)
+                               : slot<NARROW>(P, ok, idx + nb(o, -L::cx(k), -L::cy(k), -L::cz(k)))];
+        }
+    }
+}
+
+// Anti-bounce-back on the thermal links loaded by load_odd_xwall from the own slot, once
+// the mask (with its Dirichlet bits) is in.
+template <class L, class TL>
+LBM_HD void abb_x_links(const Params &P, uint32_t m, uint32_t xw, float (&g)[TL::QA])
+{
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int k = 1; k < TL::Q; ++k) {
+            const int ok = L::opp(k);
+            if (L::cx(k) != 0 && bit(xw, ok) && bit(m, DIRICHLET_SHIFT + ok))
+                g[k] = P.abbT[ok] - g[k];
+        }
+    }
+}
+
 // Store populations into the natural slots (q, x) of the given arrays.
 template <class L, class TL, bool NARROW>
 LBM_HD void store_natural(const Params &P, float *F, float *G, int idx, const float (&f)[L::Q],
@@ -288,24 +409,38 @@ LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
 // the kernel; a separate one in the host emulation of the tests).
 // IB: the context has immersed-boundary samples (cells with IB_BIT take a per-cell force);
 // kernels without it carry no trace of that path.
-template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB = false>
+// FACES (with MASKED): the walls are domain faces only (no solid cell, no immersed
+// boundary), so the mask is computed from the coordinates (face_mask) instead of loaded.
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB = false,
+          bool FACES = false>
 LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
 {
-    if (!MASKED && ghost_plane<L>(Pr, y, z)) return;
+    static_assert(!FACES || (MASKED && !IB), "FACES is a masked form without IB");
+    if ((!MASKED || FACES) && ghost_plane<L>(Pr, y, z)) return;
     const int idx = x + Pr.nx * (y + Pr.ny * z);
     // The mask load and the population loads are issued together: the populations are
-    // loaded as if no link were a wall, and wall links are fixed once the mask is in.
-    const uint32_t m = MASKED ? Pr.mask[idx] : 0u;
+    // loaded as if no link were a wall (except the x-face wall links, known from x), and
+    // the remaining wall links are fixed once the mask is in.
+    const uint32_t m = FACES ? face_mask<L, TL>(Pr, x, y, z) : MASKED ? Pr.mask[idx] : 0u;
     float f[L::Q], g[TL::QA];
+    // wall links through an x face need no mask: they are redirected at once
+    const uint32_t xw = (MASKED && ODD) ? x_wall_links<L>(Pr, x) : 0u;
     {
         Offs o{};
         if (ODD) o = make_offs(x, y, z, Pr);
-        load_cell<L, TL, false, ODD ? AA_ODD : NATURAL, NARROW>(Pr, idx, o, 0u, f, g);
+        if (MASKED && ODD)
+            load_odd_xwall<L, TL, NARROW>(Pr, idx, o, xw, f, g);
+        else
+            load_cell<L, TL, false, ODD ? AA_ODD : NATURAL, NARROW>(Pr, idx, o, 0u, f, g);
     }
     float ext[3];
     if (MASKED) {
         if (m & SKIP_BITS) return;
-        if (ODD && (m & wall_bits<L>())) fix_wall_loads<L, TL, AA_ODD, NARROW>(Pr, idx, m, f, g);
+        if (ODD) {
+            const uint32_t rest = m & ~xw;   // Dirichlet bits stay; x-face links are done
+            if (rest & wall_bits<L>()) fix_wall_loads<L, TL, AA_ODD, NARROW>(Pr, idx, rest, f, g);
+            if (xw) abb_x_links<L, TL>(Pr, m, xw, g);
+        }
     }
     if constexpr (IB) {
         const bool forced = m & IB_BIT;
@@ -333,26 +468,28 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
 }
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
-template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB>
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB,
+          bool FACES = false>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
     if (x >= P.nx || y >= P.ny) return;
-    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB>(P, P, x, y, z);
+    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
 // The same step with the register allocation bounded so that 5 blocks of 256 reside per SM
 // (48 registers): for a collision long enough that the extra warps pay for themselves.
-template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB>
+template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB,
+          bool FACES = false>
 __global__ void __launch_bounds__(256, 5) step_kernel_5(const Params P)
 {
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
     if (x >= P.nx || y >= P.ny) return;
-    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB>(P, P, x, y, z);
+    aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
 // Two-buffer PULL step: pull from the current buffer, collide, write the other buffer's

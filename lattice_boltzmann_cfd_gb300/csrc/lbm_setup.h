@@ -31,6 +31,9 @@ struct Layout {
     long long N = 0;
     size_t S = 0;
     bool masked = false, has_solid = false;
+    // faces: masked only by walls on domain faces (no solid cells, no immersed boundary), so
+    // the AA step kernels compute the mask from the coordinates instead of loading it
+    bool faces = false;
     int streaming = LBM_STREAM_AA;
     bool halo = false;
     size_t off_f = 0, off_g = 0, off_f2 = 0, off_g2 = 0, off_mask = 0, off_solid = 0;
@@ -141,6 +144,7 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     L->ib_cap = c->ib_max_samples;
     // a slab's ghost planes are found by their coordinate: HALO faces need no mask
     L->masked = any_wall || L->has_solid || L->ib_cap > 0;
+    L->faces = any_wall && !L->has_solid && L->ib_cap == 0;
     L->halo = any_halo;
     size_t off = 0;
     L->off_f = off;

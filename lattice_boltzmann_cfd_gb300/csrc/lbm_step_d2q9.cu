@@ -4,27 +4,30 @@
 namespace lbm {
 namespace {
 
-template <class TL, int C, bool M, bool O, bool N, bool I>
+template <class TL, int C, bool M, bool O, bool N, bool I, bool F = false>
 cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s)
 {
-    step_kernel<D2Q9, TL, C, M, O, N, I><<<sh.grid, sh.block, 0, s>>>(P);
+    step_kernel<D2Q9, TL, C, M, O, N, I, F><<<sh.grid, sh.block, 0, s>>>(P);
     return cudaGetLastError();
 }
 
 using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
 
-// masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces
+// masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces, 3 = mask
+// computed from the coordinates (walls on domain faces only)
 template <class TL, bool N>
 cudaError_t dispatch_n(int coll, int masked, bool odd, const Params &P, const Shape &sh,
                        cudaStream_t s)
 {
-    static const Fn table[2][3][2] = {
+    static const Fn table[2][4][2] = {
         {{go<TL, 0, false, false, N, false>, go<TL, 0, false, true, N, false>},
          {go<TL, 0, true, false, N, false>, go<TL, 0, true, true, N, false>},
-         {go<TL, 0, true, false, N, true>, go<TL, 0, true, true, N, true>}},
+         {go<TL, 0, true, false, N, true>, go<TL, 0, true, true, N, true>},
+         {go<TL, 0, true, false, N, false, true>, go<TL, 0, true, true, N, false, true>}},
         {{go<TL, 1, false, false, N, false>, go<TL, 1, false, true, N, false>},
          {go<TL, 1, true, false, N, false>, go<TL, 1, true, true, N, false>},
-         {go<TL, 1, true, false, N, true>, go<TL, 1, true, true, N, true>}}};
+         {go<TL, 1, true, false, N, true>, go<TL, 1, true, true, N, true>},
+         {go<TL, 1, true, false, N, false, true>, go<TL, 1, true, true, N, false, true>}}};
     return table[coll ? 1 : 0][masked][odd ? 1 : 0](P, sh, s);
 }
 

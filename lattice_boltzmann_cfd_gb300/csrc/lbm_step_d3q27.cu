@@ -9,25 +9,27 @@ namespace {
 // memory latency in this issue-heavy kernel (periodic 512^3: 92.4 % -> 96.3 % of the copy
 // bandwidth).  The 64-bit and immersed-boundary forms would spill there (up to 224 bytes)
 // and keep the default bound.
-template <bool M, bool O, bool N, bool I>
+template <bool M, bool O, bool N, bool I, bool F = false>
 cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s)
 {
     if constexpr (N && !I)
-        step_kernel_5<D3Q27, NoThermal, 2, M, O, N, I><<<sh.grid, sh.block, 0, s>>>(P);
+        step_kernel_5<D3Q27, NoThermal, 2, M, O, N, I, F><<<sh.grid, sh.block, 0, s>>>(P);
     else
-        step_kernel<D3Q27, NoThermal, 2, M, O, N, I><<<sh.grid, sh.block, 0, s>>>(P);
+        step_kernel<D3Q27, NoThermal, 2, M, O, N, I, F><<<sh.grid, sh.block, 0, s>>>(P);
     return cudaGetLastError();
 }
 
 using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
 
-// masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces
+// masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces, 3 = mask
+// computed from the coordinates (walls on domain faces only)
 template <bool N>
 cudaError_t dispatch_n(int masked, bool odd, const Params &P, const Shape &sh, cudaStream_t s)
 {
-    static const Fn table[3][2] = {{go<false, false, N, false>, go<false, true, N, false>},
+    static const Fn table[4][2] = {{go<false, false, N, false>, go<false, true, N, false>},
                                    {go<true, false, N, false>, go<true, true, N, false>},
-                                   {go<true, false, N, true>, go<true, true, N, true>}};
+                                   {go<true, false, N, true>, go<true, true, N, true>},
+                                   {go<true, false, N, false, true>, go<true, true, N, false, true>}};
     return table[masked][odd ? 1 : 0](P, sh, s);
 }
 

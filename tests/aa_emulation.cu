@@ -20,12 +20,15 @@ using namespace lbm;
 
 namespace {
 
-template <class L, class TL, int C, bool M, bool O, bool NARROW>
+// F: the mask computed from the coordinates, as the kernels do for domains walled only on
+// their faces.
+template <class L, class TL, int C, bool M, bool O, bool NARROW, bool F = false>
 void step_all(const Params &Pr, const Params &Pw)
 {
     for (int z = 0; z < Pr.nz; ++z)
         for (int y = 0; y < Pr.ny; ++y)
-            for (int x = 0; x < Pr.nx; ++x) aa_step_cell<L, TL, C, M, O, NARROW, M>(Pr, Pw, x, y, z);
+            for (int x = 0; x < Pr.nx; ++x)
+                aa_step_cell<L, TL, C, M, O, NARROW, M && !F, F>(Pr, Pw, x, y, z);
 }
 
 // Two-buffer PULL step: pull from P.f, collide, natural store into W.
@@ -124,10 +127,16 @@ struct Domain {
         if (Lay.masked)
             for (int z = 0; z < cfg.nz; ++z)
                 for (int y = 0; y < cfg.ny; ++y)
-                    for (int x = 0; x < cfg.nx; ++x)
-                        mask[x + cfg.nx * (y + cfg.ny * z)] =
-                            cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
+                    for (int x = 0; x < cfg.nx; ++x) {
+                        const uint32_t m = cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
+                        mask[x + cfg.nx * (y + cfg.ny * z)] = m;
+                        // the coordinate-derived mask must equal the built one off the ghosts
+                        if (Lay.faces && !ghost_plane<L>(P, y, z) && face_mask<L, TL>(P, x, y, z) != m)
+                            ++face_mask_mismatches;
+                    }
     }
+
+    long long face_mask_mismatches = 0;
 
     void point()
     {
@@ -195,6 +204,9 @@ struct Domain {
         } else if (mode == LBM_STREAM_SPLIT) {
             if (Lay.masked) split_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
             else split_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
+        } else if (Lay.masked && Lay.faces) {
+            if (parity) step_all<L, TL, C, true, true, NARROW, true>(P, Pw);
+            else step_all<L, TL, C, true, false, NARROW, true>(P, Pw);
         } else if (Lay.masked) {
             if (parity) step_all<L, TL, C, true, true, NARROW>(P, Pw);
             else step_all<L, TL, C, true, false, NARROW>(P, Pw);
@@ -238,6 +250,7 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
         const float *ib_x, const float *ib_ub, const float *ib_w)
 {
     Domain<L, TL, C, NARROW> d(cfg, Lay);
+    if (d.face_mask_mismatches) return -30;
     if (ib_n > 0) d.set_ib(ib_n, ib_x, ib_ub, ib_w);
     d.init(rho, u, T);
     for (int s = 0; s < steps; ++s) d.step();
@@ -295,6 +308,7 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
         std::string why;
         if (lbm_setup::validate(&lc, &Lay, &why) != LBM_OK) return -10 - r;
         auto d = std::make_unique<Dom>(lc, Lay);
+        if (d->face_mask_mismatches) return -40 - r;
         d->init(lr.data(), lu.data(), T ? lT.data() : nullptr);
         std::array<std::vector<float>, 2> b{std::vector<float>(halo_dirs * plane),
                                             std::vector<float>(halo_dirs * plane)};
