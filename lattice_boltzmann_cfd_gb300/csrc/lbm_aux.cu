@@ -54,7 +54,8 @@ cudaError_t launch_mask(int lattice, int thermal, const Params &P, const uint8_t
     });
 }
 
-cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s)
+cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s,
+                      bool chained)
 {
     if (P.ib_n <= 0) return cudaSuccess;
     const int corners = lattice == 9 ? 4 : 8;
@@ -63,10 +64,9 @@ cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaSt
     auto go = [&](auto l, auto tl) {
         using L = decltype(l);
         using TL = decltype(tl);
-        if (pat == AA_ODD) ib_kernel<L, TL, AA_ODD><<<g, b, 0, s>>>(P);
-        else if (pat == PULL) ib_kernel<L, TL, PULL><<<g, b, 0, s>>>(P);
-        else ib_kernel<L, TL, NATURAL><<<g, b, 0, s>>>(P);
-        return cudaGetLastError();
+        if (pat == AA_ODD) return launch_step_kernel(ib_kernel<L, TL, AA_ODD>, g, b, s, chained, P);
+        if (pat == PULL) return launch_step_kernel(ib_kernel<L, TL, PULL>, g, b, s, chained, P);
+        return launch_step_kernel(ib_kernel<L, TL, NATURAL>, g, b, s, chained, P);
     };
     return by_lattice(lattice, thermal, go);
 }

@@ -46,6 +46,7 @@ struct lbm_ctx {
     double *partial = nullptr, *result = nullptr;
     cudaStream_t stream = nullptr;
     int device = 0;
+    bool chained = false;   // step kernels launched chained (lbm::chain_steps)
     int parity = 0;
     long long steps = 0;
     bool initialized = false;
@@ -176,6 +177,13 @@ lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace
     c->ws = static_cast<char *>(d_workspace);
     c->stream = static_cast<cudaStream_t>(cuda_stream);
     c->device = dev;
+    {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            cudaGetLastError();
+        const lbm::Shape sh = lbm::cell_shape(cfg->nx, cfg->ny, cfg->nz);
+        c->chained = sms > 0 && lbm::chain_steps((long long)sh.grid.x * sh.grid.y * sh.grid.z, sms);
+    }
     c->partial = reinterpret_cast<double *>(c->ws + L.off_partial);
     c->result = reinterpret_cast<double *>(c->ws + L.off_result);
     lbm_setup::fill_params(c->cfg, c->L, c->ws, c->P);
@@ -261,7 +269,7 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
                         : c->L.streaming == LBM_STREAM_SPLIT ? lbm::NATURAL
                         : parity                             ? lbm::AA_ODD
                                                              : lbm::NATURAL;
-        e = lbm::launch_ib(c->cfg.lattice, th, pat, P, stream);
+        e = lbm::launch_ib(c->cfg.lattice, th, pat, P, stream, c->chained);
         if (e != cudaSuccess) return e;
     }
     switch (c->L.streaming) {
@@ -275,10 +283,12 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
         break;
     default:
         if (c->cfg.lattice == LBM_D3Q27)
-            e = lbm::launch_step_d3q27(masked_aa, parity != 0, narrow, P, sh, stream);
+            e = lbm::launch_step_d3q27(masked_aa, parity != 0, narrow, P, sh, stream, c->chained);
         else
-            e = d3 ? lbm::launch_step_d3q19(th, coll, masked_aa, parity != 0, narrow, P, sh, stream)
-                   : lbm::launch_step_d2q9(th, coll, masked_aa, parity != 0, narrow, P, sh, stream);
+            e = d3 ? lbm::launch_step_d3q19(th, coll, masked_aa, parity != 0, narrow, P, sh, stream,
+                                            c->chained)
+                   : lbm::launch_step_d2q9(th, coll, masked_aa, parity != 0, narrow, P, sh, stream,
+                                           c->chained);
     }
     if (c->L.streaming != LBM_STREAM_AA) {
         std::swap(P.f, P.fo);

@@ -2,9 +2,38 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "lbm_kernels.cuh"
 
 namespace lbm {
+
+// Launch a kernel that starts with wait_prerequisites().  chained: with programmatic stream
+// serialization, so that it may be scheduled before the previous kernel in the stream
+// completes (its blocks fill the SMs that the previous kernel's last wave leaves idle);
+// otherwise an ordinary launch.
+template <class... K, class... A>
+cudaError_t launch_step_kernel(void (*kernel)(K...), dim3 grid, dim3 block, cudaStream_t s,
+                               bool chained, A &&...args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = chained ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
+
+// Whether the step kernels of a grid of `blocks` blocks are launched chained: only grids of
+// at least two waves (16 resident blocks of 64 threads per SM).  Chaining gained 2-4 % on
+// 128^3 grids (14 waves) and nothing at 512^3; on the 32^3 grid (512 blocks, part of one
+// wave) it cost 8 %, with several launched grids resident and waiting at once.
+inline bool chain_steps(long long blocks, int sms) { return blocks >= 2LL * 16 * sms; }
 
 struct Shape {
     dim3 grid, block;
@@ -34,13 +63,14 @@ constexpr int DIAG_BLOCKS = 2048;   // capacity of the partial-sum rows (one res
 // narrow: every population index fits in 32 bits (see slot()).  masked: 0 = no link
 // mask, 1 = link mask, 2 = link mask and immersed-boundary forces, 3 = link mask computed
 // from the coordinates (walls on domain faces only; AA steps only).
+// chained: see launch_step_kernel.
 cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
-                              const Params &P, const Shape &sh, cudaStream_t s);
+                              const Params &P, const Shape &sh, cudaStream_t s, bool chained);
 cudaError_t launch_step_d2q9(int thermal, int coll, int masked, bool odd, bool narrow,
-                             const Params &P, const Shape &sh, cudaStream_t s);
+                             const Params &P, const Shape &sh, cudaStream_t s, bool chained);
 // D3Q27, central moments, AA only; masked as above.
 cudaError_t launch_step_d3q27(int masked, bool odd, bool narrow, const Params &P,
-                              const Shape &sh, cudaStream_t s);
+                              const Shape &sh, cudaStream_t s, bool chained);
 // Two-buffer modes: one PULL step, or one SPLIT step (collide + stream), from P.f/P.g
 // into P.fo/P.go.
 cudaError_t launch_pull_d3q19(int thermal, int coll, int masked, bool narrow, const Params &P,
@@ -62,7 +92,8 @@ cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
                        const Params &P, float *f, float *g, cudaStream_t s);
 // Immersed boundary: penalty + spreading for every sample (read pattern pat), and the
 // IB_BIT marking of the samples' stencil cells.
-cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s);
+cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s,
+                      bool chained);
 cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
                            cudaStream_t s);
 // Slab halo pack (unpack = 0) or unpack (unpack = 1) of one side and phase.

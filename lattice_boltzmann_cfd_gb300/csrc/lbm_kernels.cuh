@@ -393,6 +393,27 @@ LBM_HD void store_logical(const Params &P, int idx, const Offs &o, uint32_t m,
 
 // ------------------------------------------------------------------ the step ----------
 
+// Programmatic dependent launch (sm_90 and later).  A kernel launched with programmatic
+// stream serialization (launch_chained) may be scheduled while the kernel before it in the
+// stream is still running; before it touches anything that kernel wrote it waits
+// (griddepcontrol.wait) until that kernel has completed and its writes are visible.
+// allow_dependents lets the next such kernel be scheduled once every block of this one has
+// started, so that its blocks fill the SMs freed during this kernel's last wave instead of
+// after it.  Both are no-ops in a kernel launched without the attribute, and on the host.
+LBM_HD void allow_dependents()
+{
+#if defined(__CUDA_ARCH__)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+LBM_HD void wait_prerequisites()
+{
+#if defined(__CUDA_ARCH__)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
 // Read the immersed-boundary force of a cell and zero it for the next step.
 LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
@@ -472,6 +493,8 @@ template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool 
           bool FACES = false>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
+    allow_dependents();
+    wait_prerequisites();   // every load reads the previous step's stores
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
@@ -485,6 +508,8 @@ template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool 
           bool FACES = false>
 __global__ void __launch_bounds__(256, 5) step_kernel_5(const Params P)
 {
+    allow_dependents();
+    wait_prerequisites();   // every load reads the previous step's stores
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
@@ -688,6 +713,8 @@ LBM_HD int ib_sample(const Params &P, int s, int (&node)[8], float (&K)[8], floa
 template <class L, class TL, int PAT>
 __global__ void __launch_bounds__(128) ib_kernel(const Params P)
 {
+    allow_dependents();
+    wait_prerequisites();   // the stencil cells hold the previous step's stores
     constexpr int CORNERS = 1 << L::DIM;
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const int s = t / CORNERS, c = t % CORNERS;

@@ -5,19 +5,19 @@ namespace lbm {
 namespace {
 
 template <class TL, int C, bool M, bool O, bool N, bool I, bool F = false>
-cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s)
+cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s, bool chained)
 {
-    step_kernel<D3Q19, TL, C, M, O, N, I, F><<<sh.grid, sh.block, 0, s>>>(P);
-    return cudaGetLastError();
+    return launch_step_kernel(step_kernel<D3Q19, TL, C, M, O, N, I, F>, sh.grid, sh.block, s, chained,
+                              P);
 }
 
-using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
+using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t, bool);
 
 // masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces, 3 = mask
 // computed from the coordinates (walls on domain faces only)
 template <class TL, bool N>
 cudaError_t dispatch_n(int coll, int masked, bool odd, const Params &P, const Shape &sh,
-                       cudaStream_t s)
+                       cudaStream_t s, bool chained)
 {
     static const Fn table[2][4][2] = {
         {{go<TL, 0, false, false, N, false>, go<TL, 0, false, true, N, false>},
@@ -28,25 +28,24 @@ cudaError_t dispatch_n(int coll, int masked, bool odd, const Params &P, const Sh
          {go<TL, 1, true, false, N, false>, go<TL, 1, true, true, N, false>},
          {go<TL, 1, true, false, N, true>, go<TL, 1, true, true, N, true>},
          {go<TL, 1, true, false, N, false, true>, go<TL, 1, true, true, N, false, true>}}};
-    return table[coll ? 1 : 0][masked][odd ? 1 : 0](P, sh, s);
+    return table[coll ? 1 : 0][masked][odd ? 1 : 0](P, sh, s, chained);
 }
 
 template <class TL>
 cudaError_t dispatch(int coll, int masked, bool odd, bool narrow, const Params &P,
-                     const Shape &sh, cudaStream_t s)
+                     const Shape &sh, cudaStream_t s, bool chained)
 {
-    return narrow ? dispatch_n<TL, true>(coll, masked, odd, P, sh, s)
-                  : dispatch_n<TL, false>(coll, masked, odd, P, sh, s);
+    return narrow ? dispatch_n<TL, true>(coll, masked, odd, P, sh, s, chained)
+                  : dispatch_n<TL, false>(coll, masked, odd, P, sh, s, chained);
 }
 
 }  // namespace
 
 cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
-                              const Params &P,
-                              const Shape &sh, cudaStream_t s)
+                              const Params &P, const Shape &sh, cudaStream_t s, bool chained)
 {
-    if (thermal == 7) return dispatch<D3Q7>(coll, masked, odd, narrow, P, sh, s);
-    return dispatch<NoThermal>(coll, masked, odd, narrow, P, sh, s);
+    if (thermal == 7) return dispatch<D3Q7>(coll, masked, odd, narrow, P, sh, s, chained);
+    return dispatch<NoThermal>(coll, masked, odd, narrow, P, sh, s, chained);
 }
 
 }  // namespace lbm

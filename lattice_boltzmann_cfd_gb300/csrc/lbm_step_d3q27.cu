@@ -10,36 +10,38 @@ namespace {
 // bandwidth).  The 64-bit and immersed-boundary forms would spill there (up to 224 bytes)
 // and keep the default bound.
 template <bool M, bool O, bool N, bool I, bool F = false>
-cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s)
+cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s, bool chained)
 {
     if constexpr (N && !I)
-        step_kernel_5<D3Q27, NoThermal, 2, M, O, N, I, F><<<sh.grid, sh.block, 0, s>>>(P);
+        return launch_step_kernel(step_kernel_5<D3Q27, NoThermal, 2, M, O, N, I, F>, sh.grid,
+                                  sh.block, s, chained, P);
     else
-        step_kernel<D3Q27, NoThermal, 2, M, O, N, I, F><<<sh.grid, sh.block, 0, s>>>(P);
-    return cudaGetLastError();
+        return launch_step_kernel(step_kernel<D3Q27, NoThermal, 2, M, O, N, I, F>, sh.grid,
+                                  sh.block, s, chained, P);
 }
 
-using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t);
+using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t, bool);
 
 // masked: 0 = no mask, 1 = mask, 2 = mask and immersed-boundary forces, 3 = mask
 // computed from the coordinates (walls on domain faces only)
 template <bool N>
-cudaError_t dispatch_n(int masked, bool odd, const Params &P, const Shape &sh, cudaStream_t s)
+cudaError_t dispatch_n(int masked, bool odd, const Params &P, const Shape &sh, cudaStream_t s,
+                       bool chained)
 {
     static const Fn table[4][2] = {{go<false, false, N, false>, go<false, true, N, false>},
                                    {go<true, false, N, false>, go<true, true, N, false>},
                                    {go<true, false, N, true>, go<true, true, N, true>},
                                    {go<true, false, N, false, true>, go<true, true, N, false, true>}};
-    return table[masked][odd ? 1 : 0](P, sh, s);
+    return table[masked][odd ? 1 : 0](P, sh, s, chained);
 }
 
 }  // namespace
 
 cudaError_t launch_step_d3q27(int masked, bool odd, bool narrow, const Params &P,
-                              const Shape &sh, cudaStream_t s)
+                              const Shape &sh, cudaStream_t s, bool chained)
 {
-    return narrow ? dispatch_n<true>(masked, odd, P, sh, s)
-                  : dispatch_n<false>(masked, odd, P, sh, s);
+    return narrow ? dispatch_n<true>(masked, odd, P, sh, s, chained)
+                  : dispatch_n<false>(masked, odd, P, sh, s, chained);
 }
 
 }  // namespace lbm
