@@ -274,12 +274,12 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
     }
     switch (c->L.streaming) {
     case LBM_STREAM_PULL:
-        e = d3 ? lbm::launch_pull_d3q19(th, coll, masked, narrow, P, sh, stream)
-               : lbm::launch_pull_d2q9(th, coll, masked, narrow, P, sh, stream);
+        e = d3 ? lbm::launch_pull_d3q19(th, coll, masked, narrow, P, sh, stream, c->chained)
+               : lbm::launch_pull_d2q9(th, coll, masked, narrow, P, sh, stream, c->chained);
         break;
     case LBM_STREAM_SPLIT:
-        e = d3 ? lbm::launch_split_d3q19(th, coll, masked, narrow, P, sh, stream)
-               : lbm::launch_split_d2q9(th, coll, masked, narrow, P, sh, stream);
+        e = d3 ? lbm::launch_split_d3q19(th, coll, masked, narrow, P, sh, stream, c->chained)
+               : lbm::launch_split_d2q9(th, coll, masked, narrow, P, sh, stream, c->chained);
         break;
     default:
         if (c->cfg.lattice == LBM_D3Q27)

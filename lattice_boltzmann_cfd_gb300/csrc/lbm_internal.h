@@ -74,13 +74,13 @@ cudaError_t launch_step_d3q27(int masked, bool odd, bool narrow, const Params &P
 // Two-buffer modes: one PULL step, or one SPLIT step (collide + stream), from P.f/P.g
 // into P.fo/P.go.
 cudaError_t launch_pull_d3q19(int thermal, int coll, int masked, bool narrow, const Params &P,
-                              const Shape &sh, cudaStream_t s);
+                              const Shape &sh, cudaStream_t s, bool chained);
 cudaError_t launch_pull_d2q9(int thermal, int coll, int masked, bool narrow, const Params &P,
-                             const Shape &sh, cudaStream_t s);
+                             const Shape &sh, cudaStream_t s, bool chained);
 cudaError_t launch_split_d3q19(int thermal, int coll, int masked, bool narrow, const Params &P,
-                               const Shape &sh, cudaStream_t s);
+                               const Shape &sh, cudaStream_t s, bool chained);
 cudaError_t launch_split_d2q9(int thermal, int coll, int masked, bool narrow, const Params &P,
-                              const Shape &sh, cudaStream_t s);
+                              const Shape &sh, cudaStream_t s, bool chained);
 // pat: read pattern of the logical state (NATURAL, AA_ODD or PULL).
 cudaError_t launch_init(int lattice, int thermal, int pat, const Params &P, const float *rho,
                         const float *u, const float *T, cudaStream_t s);

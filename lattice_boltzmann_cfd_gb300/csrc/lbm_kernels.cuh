@@ -550,6 +550,8 @@ LBM_HD void pull_step_cell(const Params &P, float *Wf, float *Wg, int x, int y, 
 template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB>
 __global__ void __launch_bounds__(256) pull_kernel(const Params P)
 {
+    allow_dependents();
+    wait_prerequisites();
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
@@ -580,6 +582,8 @@ LBM_HD void collide_in_place_cell(const Params &P, int idx)
 template <class L, class TL, int COLL, bool MASKED, bool NARROW, bool IB>
 __global__ void __launch_bounds__(256) collide_kernel(const Params P)
 {
+    allow_dependents();
+    wait_prerequisites();
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
@@ -606,6 +610,8 @@ LBM_HD void stream_cell(const Params &P, float *Wf, float *Wg, int x, int y, int
 template <class L, class TL, bool MASKED, bool NARROW>
 __global__ void __launch_bounds__(256) stream_kernel(const Params P)
 {
+    allow_dependents();
+    wait_prerequisites();
     const int x = blockIdx.x * blockDim.x + threadIdx.x;
     const int y = blockIdx.y * blockDim.y + threadIdx.y;
     const int z = blockIdx.z;
