@@ -173,6 +173,32 @@ def outer_walls_case(shape=(12, 7, 11), seed=37):
         T_wall=(0.0, 0.0, 0.0, 0.0, 0.4, -0.3))
 
 
+def faces_only_cases(large=False):
+    """Walled problems without solid cells or immersed-boundary samples: their AA step
+    kernels compute the link mask from the coordinates.  large: sizes that span several
+    thread blocks along x with ragged tails (for the GPU)."""
+    s3, s2, s27, sz = (((70, 40, 37), (300, 181, 1), (66, 20, 18), (64, 20, 24)) if large
+                       else ((9, 7, 6), (10, 8, 1), (8, 6, 7), (7, 6, 9)))
+    c3 = W.perturbed(W.cavity3d(shape=s3), seed=51)
+    c2 = dataclasses.replace(W.perturbed(W.cavity2d(shape=s2), seed=52), gbeta=0.01)
+    c2y = dataclasses.replace(
+        c2, name=c2.name + ", walls and Dirichlet faces on y only",
+        face_flow=("periodic", "periodic", "wall", "wall", "periodic", "periodic"),
+        face_T=("adiabatic", "adiabatic", "dirichlet", "dirichlet", "adiabatic", "adiabatic"),
+        T_wall=(0.0, 0.0, 0.3, -0.2, 0.0, 0.0))
+    q27 = W.random_periodic(shape=s27, seed=53, lattice=27, nu=0.05)
+    q27 = dataclasses.replace(q27, name=f"D3Q27 CM box {s27[0]}x{s27[1]}x{s27[2]}, walls",
+                              face_flow=("wall",) * 6, g_body=(1e-4, -2e-5, 3e-5))
+    return [c3, c2, c2y, q27, outer_walls_case(shape=sz, seed=54)]
+
+
+def with_loaded_mask(w):
+    """The same problem with an all-zero solid array: the step kernels then load the link
+    mask instead of computing it."""
+    return dataclasses.replace(w, solid=np.zeros(w.grid, np.uint8),
+                               name=w.name + " (zero solid array)")
+
+
 def degenerate_cases():
     """Grids of extent 1 or 2 along some axes (every neighbour is the cell itself or its one
     neighbour, through a wrap or a wall), on every lattice."""

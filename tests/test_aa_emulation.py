@@ -10,8 +10,9 @@ parity-aware.  The link mask is compared bit for bit with a brute-force builder.
 import numpy as np
 import pytest
 
-from parity_util import (degenerate_cases, emulate, emulate_slabs, fluid_of, mask_brute_force,
-                         oracle_states, outer_walls_case, slab_cases, small_cases)
+from parity_util import (degenerate_cases, emulate, emulate_slabs, faces_only_cases, fluid_of,
+                         mask_brute_force, oracle_states, outer_walls_case, slab_cases,
+                         small_cases, with_loaded_mask)
 
 CASES = small_cases()
 
@@ -102,3 +103,24 @@ def test_degenerate_grids(oracle_mod, emu_lib, w, mode):
         if w.thermal:
             assert np.abs(g - r["g"])[:, fluid].max() < 1e-6, n
     assert np.array_equal(emulate(emu_lib, w, 0)[2], mask_brute_force(w))
+
+
+FACES = faces_only_cases()
+
+
+@pytest.mark.parametrize("w", FACES, ids=[c.name for c in FACES])
+def test_mask_from_coordinates_equals_loaded_mask(oracle_mod, emu_lib, w):
+    """A walled problem without solids runs the step with the link mask computed from the
+    coordinates; the same problem given an all-zero solid array loads the mask instead.
+    Both are bit-identical at both parities, and match the oracle."""
+    fluid = fluid_of(w)
+    ref = oracle_states(oracle_mod, w, [5, 6])
+    for n in (5, 6):
+        f1, g1, m1 = emulate(emu_lib, w, n)
+        f2, g2, m2 = emulate(emu_lib, with_loaded_mask(w), n)
+        assert np.array_equal(m1, m2)
+        assert np.array_equal(f1, f2), n
+        assert np.array_equal(g1, g2), n
+        assert np.abs(f1 - ref[n]["f"])[:, fluid].max() < 1e-6, n
+        if w.thermal:
+            assert np.abs(g1 - ref[n]["g"])[:, fluid].max() < 1e-6, n
