@@ -541,15 +541,18 @@ def run_gpu(args, dctx):
                      "denominators": "peak: the measured copy; live_copy_gbs: a 2 GiB "
                                      "device copy timed in this run; nominal: 2 x memory "
                                      "clock x bus width from the device attributes"},
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(pipelined_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "pipelined_value": round(pipelined_value, 1),
-                "pipelined": "the same jobs through JobPipeline, each step's copies "
-                             "overlapping the neighbouring steps' LBM steps; its rate varies "
-                             "between runs (the device at times serialises a job's init "
-                             "behind the previous read-out), so value is the serial path",
-                "path": "page-locked host rho,u in -> lbm_init_equilibrium -> lbm_step -> "
-                        "lbm_macroscopic into page-locked host -> lbm_diagnostics"},
+                "path": "JobPipeline: each step's page-locked host rho,u copied in on a "
+                        "copy stream -> lbm_init_equilibrium -> lbm_step -> lbm_macroscopic "
+                        "-> copied out to page-locked host on a second copy stream, the "
+                        "copies overlapping the neighbouring steps' LBM steps; "
+                        "lbm_diagnostics read back every step",
+                "serial_value": round(e2e_value, 1),
+                "serial_path": "one step at a time through the C ABI: lbm_init_equilibrium "
+                               "reads the page-locked host fields, lbm_step, "
+                               "lbm_macroscopic writes page-locked host fields, "
+                               "lbm_diagnostics"},
         "gpu_launches": args.steps * (args.lbm_steps + 2),
         "clocks": clocks,
     }
