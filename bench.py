@@ -46,8 +46,8 @@ BYTES_PER_CELL = {(19, 0): 152, (19, 7): 208, (9, 0): 72, (9, 5): 112, (27, 0): 
 # taken on; reported as "traffic" only while the sources are unchanged.
 NCU_TRAFFIC = {
     # ncu --set full, one even + one odd launch at 256^3 (see profiles/), scaled by cells
-    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.63, "src_hash": "ffcd1e3e6aeeec58"},
-    "cavity3d_512": {"bytes_per_cell": 204.77, "src_hash": "ffcd1e3e6aeeec58"},
+    "d3q19_mrt_periodic_512": {"bytes_per_cell": 148.61, "src_hash": "bd94ee045e34b2d3"},
+    "cavity3d_512": {"bytes_per_cell": 204.77, "src_hash": "bd94ee045e34b2d3"},
 }
 
 
@@ -541,18 +541,17 @@ def run_gpu(args, dctx):
                      "denominators": "peak: the measured copy; live_copy_gbs: a 2 GiB "
                                      "device copy timed in this run; nominal: 2 x memory "
                                      "clock x bus width from the device attributes"},
-        "e2e": {"value": round(pipelined_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "path": "JobPipeline: each step's page-locked host rho,u copied in on a "
-                        "copy stream -> lbm_init_equilibrium -> lbm_step -> lbm_macroscopic "
-                        "-> copied out to page-locked host on a second copy stream, the "
-                        "copies overlapping the neighbouring steps' LBM steps; "
-                        "lbm_diagnostics read back every step",
-                "serial_value": round(e2e_value, 1),
-                "serial_path": "one step at a time through the C ABI: lbm_init_equilibrium "
-                               "reads the page-locked host fields, lbm_step, "
-                               "lbm_macroscopic writes page-locked host fields, "
-                               "lbm_diagnostics"},
+                "path": "one step at a time through the C ABI: lbm_init_equilibrium reads "
+                        "the page-locked host rho,u, lbm_step, lbm_macroscopic writes "
+                        "page-locked host fields, lbm_diagnostics",
+                "pipelined_value": round(pipelined_value, 1),
+                "pipelined": "the same steps through JobPipeline: copies on two copy streams "
+                             "overlapping the neighbouring steps' LBM steps, each read-out "
+                             "issued behind the next step's kernels; about 42k MLUPS in a "
+                             "fresh process, 35-42k here after the other legs, so value is "
+                             "the serial path"},
         "gpu_launches": args.steps * (args.lbm_steps + 2),
         "clocks": clocks,
     }

@@ -262,7 +262,6 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
     const bool d3 = c->cfg.lattice == LBM_D3Q19;
     const int th = c->cfg.thermal, coll = c->cfg.collision;
     const int masked = !c->L.masked ? 0 : (c->L.ib_cap > 0 ? 2 : 1);
-    const int masked_aa = masked == 1 && c->L.faces ? 3 : masked;   // mask from coordinates
     cudaError_t e;
     if (P.ib_n > 0) {
         const int pat = c->L.streaming == LBM_STREAM_PULL    ? lbm::PULL
@@ -283,11 +282,11 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
         break;
     default:
         if (c->cfg.lattice == LBM_D3Q27)
-            e = lbm::launch_step_d3q27(masked_aa, parity != 0, narrow, P, sh, stream, c->chained);
+            e = lbm::launch_step_d3q27(masked, parity != 0, narrow, P, sh, stream, c->chained);
         else
-            e = d3 ? lbm::launch_step_d3q19(th, coll, masked_aa, parity != 0, narrow, P, sh, stream,
+            e = d3 ? lbm::launch_step_d3q19(th, coll, masked, parity != 0, narrow, P, sh, stream,
                                             c->chained)
-                   : lbm::launch_step_d2q9(th, coll, masked_aa, parity != 0, narrow, P, sh, stream,
+                   : lbm::launch_step_d2q9(th, coll, masked, parity != 0, narrow, P, sh, stream,
                                            c->chained);
     }
     if (c->L.streaming != LBM_STREAM_AA) {

@@ -61,8 +61,9 @@ constexpr int DIAG_BLOCKS = 2048;   // capacity of the partial-sum rows (one res
 
 // Each returns the launch error (cudaGetLastError) of what it enqueued.
 // narrow: every population index fits in 32 bits (see slot()).  masked: 0 = no link
-// mask, 1 = link mask, 2 = link mask and immersed-boundary forces, 3 = link mask computed
-// from the coordinates (walls on domain faces only; AA steps only).
+// mask, 1 = link mask, 2 = link mask and immersed-boundary forces.  The AA step kernels of
+// form 1 compute the mask from the coordinates outside the solid cells' box (boxed_mask);
+// the two-buffer kernels load it.
 // chained: see launch_step_kernel.
 cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
                               const Params &P, const Shape &sh, cudaStream_t s, bool chained);

@@ -47,6 +47,7 @@ struct Params {
     int face_wall[6];      // per face: 1 = wall (flow)
     int face_halo[6];      // per face: 1 = halo face of a slab (ghost plane, no wrap)
     int ghost_lo, ghost_hi;  // outer-axis coordinate of a slab's ghost planes, -1 = none
+    int box_lo[3], box_hi[3];  // solid cells' box widened by one (inclusive; empty: lo > hi)
     int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
     float T_wall[6];
     // immersed boundary: per-cell force (3 planes of S, consumed and zeroed by the step),
@@ -240,8 +241,8 @@ LBM_HD uint32_t face_bits(const Params &P, int c, int n)
     return m;
 }
 
-// The link mask of a cell of a domain whose walls are all domain faces (no solid cell):
-// cell_mask without the solid array, for every cell that is not on a slab's ghost plane.
+// The link mask of a cell that neither is solid nor has a link into a solid cell: cell_mask
+// from the face kinds alone, for every cell that is not on a slab's ghost plane.
 // A link is a wall link when it leaves through a wall face along any axis; a thermal link
 // crosses one face only.
 template <class L, class TL>
@@ -250,6 +251,17 @@ LBM_HD uint32_t face_mask(const Params &P, int x, int y, int z)
     uint32_t m = face_bits<L, TL, 0>(P, x, P.nx) | face_bits<L, TL, 1>(P, y, P.ny);
     if constexpr (L::DIM == 3) m |= face_bits<L, TL, 2>(P, z, P.nz);
     return m;
+}
+
+// The link mask of a cell for the AA step kernels without an immersed boundary: loaded
+// inside the box around the solid cells, the face bits elsewhere (no cell outside the box is
+// solid or has a link into a solid cell).
+template <class L, class TL>
+LBM_HD uint32_t boxed_mask(const Params &P, int idx, int x, int y, int z)
+{
+    const bool inside = x >= P.box_lo[0] && x <= P.box_hi[0] && y >= P.box_lo[1] &&
+                        y <= P.box_hi[1] && z >= P.box_lo[2] && z <= P.box_hi[2];
+    return inside ? P.mask[idx] : face_mask<L, TL>(P, x, y, z);
 }
 
 // Odd-step load (read pattern AA_ODD) that redirects the links in xw, a subset of
@@ -430,8 +442,8 @@ LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
 // the kernel; a separate one in the host emulation of the tests).
 // IB: the context has immersed-boundary samples (cells with IB_BIT take a per-cell force);
 // kernels without it carry no trace of that path.
-// FACES (with MASKED): the walls are domain faces only (no solid cell, no immersed
-// boundary), so the mask is computed from the coordinates (face_mask) instead of loaded.
+// FACES (with MASKED, without IB): the mask comes from the coordinates (face_mask) outside
+// the solid cells' box and is loaded only inside it (boxed_mask).
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB = false,
           bool FACES = false>
 LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
@@ -442,7 +454,7 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     // The mask load and the population loads are issued together: the populations are
     // loaded as if no link were a wall (except the x-face wall links, known from x), and
     // the remaining wall links are fixed once the mask is in.
-    const uint32_t m = FACES ? face_mask<L, TL>(Pr, x, y, z) : MASKED ? Pr.mask[idx] : 0u;
+    const uint32_t m = FACES ? boxed_mask<L, TL>(Pr, idx, x, y, z) : MASKED ? Pr.mask[idx] : 0u;
     float f[L::Q], g[TL::QA];
     // wall links through an x face need no mask: they are redirected at once
     const uint32_t xw = (MASKED && ODD) ? x_wall_links<L>(Pr, x) : 0u;

@@ -31,9 +31,10 @@ struct Layout {
     long long N = 0;
     size_t S = 0;
     bool masked = false, has_solid = false;
-    // faces: masked only by walls on domain faces (no solid cells, no immersed boundary), so
-    // the AA step kernels compute the mask from the coordinates instead of loading it
-    bool faces = false;
+    // Without an immersed boundary, the masked AA step kernels compute a cell's link mask
+    // from its coordinates (its wall faces) and load it only inside box_lo..box_hi: the
+    // bounding box of the solid cells widened by one cell, empty without solid cells.
+    int box_lo[3] = {0, 0, 0}, box_hi[3] = {-1, -1, -1};
     int streaming = LBM_STREAM_AA;
     bool halo = false;
     size_t off_f = 0, off_g = 0, off_f2 = 0, off_g2 = 0, off_mask = 0, off_solid = 0;
@@ -41,6 +42,43 @@ struct Layout {
     int ib_cap = 0;
     size_t bytes = 0;
 };
+
+// Bounding box (inclusive) of the solid cells of c->solid_mask, widened by one cell on each
+// side: every cell with a link into a solid cell, and every solid cell, lies inside it.  An
+// axis on which the widened range leaves the grid through a periodic face is taken whole
+// (the neighbour across the face is at the other end); otherwise the range is clipped to
+// the grid.  Empty (lo > hi) when no cell is solid.
+inline void solid_box(const lbm_config *c, int lo[3], int hi[3])
+{
+    const int n[3] = {c->nx, c->ny, c->nz};
+    int l[3] = {n[0], n[1], n[2]}, h[3] = {-1, -1, -1};
+    const uint8_t *s = c->solid_mask;
+    size_t i = 0;
+    for (int z = 0; z < n[2]; ++z)
+        for (int y = 0; y < n[1]; ++y)
+            for (int x = 0; x < n[0]; ++x, ++i) {
+                if (!s[i]) continue;
+                const int p[3] = {x, y, z};
+                for (int a = 0; a < 3; ++a) {
+                    l[a] = p[a] < l[a] ? p[a] : l[a];
+                    h[a] = p[a] > h[a] ? p[a] : h[a];
+                }
+            }
+    for (int a = 0; a < 3; ++a) {
+        lo[a] = 0;
+        hi[a] = -1;
+    }
+    if (h[0] < 0) return;
+    for (int a = 0; a < 3; ++a) {
+        int wl = l[a] - 1, wh = h[a] + 1;
+        if ((wl < 0 || wh > n[a] - 1) && c->face_flow[2 * a] == LBM_FACE_PERIODIC) {
+            wl = 0;
+            wh = n[a] - 1;
+        }
+        lo[a] = wl < 0 ? 0 : wl;
+        hi[a] = wh > n[a] - 1 ? n[a] - 1 : wh;
+    }
+}
 
 inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
 {
@@ -144,7 +182,7 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     L->ib_cap = c->ib_max_samples;
     // a slab's ghost planes are found by their coordinate: HALO faces need no mask
     L->masked = any_wall || L->has_solid || L->ib_cap > 0;
-    L->faces = any_wall && !L->has_solid && L->ib_cap == 0;
+    if (L->has_solid) solid_box(c, L->box_lo, L->box_hi);
     L->halo = any_halo;
     size_t off = 0;
     L->off_f = off;
@@ -233,6 +271,10 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
         P.T_wall[i] = (float)g.T_wall[i];
     }
     const int outer = dim - 1, n_outer = dim == 3 ? g.nz : g.ny;
+    for (int a = 0; a < 3; ++a) {
+        P.box_lo[a] = L.box_lo[a];
+        P.box_hi[a] = L.box_hi[a];
+    }
     P.ghost_lo = P.face_halo[2 * outer] ? 0 : -1;
     P.ghost_hi = P.face_halo[2 * outer + 1] ? n_outer - 1 : -1;
     // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)

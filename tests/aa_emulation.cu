@@ -20,8 +20,13 @@ using namespace lbm;
 
 namespace {
 
-// F: the mask computed from the coordinates, as the kernels do for domains walled only on
-// their faces.
+// Run the masked AA steps without an immersed boundary with the mask loaded for every cell
+// (the per-cell function's plain masked form) instead of computed outside the solid cells'
+// box, as the kernels do; for tests that compare the two (emu_set_loaded_mask).
+bool g_loaded_mask = false;
+
+// F: the mask computed from the coordinates outside the solid cells' box (boxed_mask), as
+// the kernels do without an immersed boundary.
 template <class L, class TL, int C, bool M, bool O, bool NARROW, bool F = false>
 void step_all(const Params &Pr, const Params &Pw)
 {
@@ -129,9 +134,11 @@ struct Domain {
                 for (int y = 0; y < cfg.ny; ++y)
                     for (int x = 0; x < cfg.nx; ++x) {
                         const uint32_t m = cell_mask<L, TL>(P, cfg.solid_mask, x, y, z);
-                        mask[x + cfg.nx * (y + cfg.ny * z)] = m;
-                        // the coordinate-derived mask must equal the built one off the ghosts
-                        if (Lay.faces && !ghost_plane<L>(P, y, z) && face_mask<L, TL>(P, x, y, z) != m)
+                        const int idx = x + cfg.nx * (y + cfg.ny * z);
+                        mask[idx] = m;
+                        // the mask the kernels compute must equal the built one off the ghosts
+                        if (Lay.ib_cap == 0 && !ghost_plane<L>(P, y, z) &&
+                            boxed_mask<L, TL>(P, idx, x, y, z) != m)
                             ++face_mask_mismatches;
                     }
     }
@@ -204,7 +211,7 @@ struct Domain {
         } else if (mode == LBM_STREAM_SPLIT) {
             if (Lay.masked) split_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
             else split_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
-        } else if (Lay.masked && Lay.faces) {
+        } else if (Lay.masked && Lay.ib_cap == 0 && !g_loaded_mask) {
             if (parity) step_all<L, TL, C, true, true, NARROW, true>(P, Pw);
             else step_all<L, TL, C, true, false, NARROW, true>(P, Pw);
         } else if (Lay.masked) {
@@ -376,6 +383,8 @@ int run_any(const lbm_config *cfg, const lbm_setup::Layout &Lay, const float *rh
     return mrt ? run<D2Q9, NoThermal, 1, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w)
                : run<D2Q9, NoThermal, 0, NARROW>(*cfg, Lay, rho, u, T, steps, fout, gout, mask_out, ib_n, ib_x, ib_ub, ib_w);
 }
+
+extern "C" void emu_set_loaded_mask(int on) { g_loaded_mask = on != 0; }
 
 // narrow != 0: the step uses 32-bit population indices, as the library does whenever
 // every index fits in 32 bits; 0: the 64-bit form used for larger grids.

@@ -175,8 +175,8 @@ def outer_walls_case(shape=(12, 7, 11), seed=37):
 
 def faces_only_cases(large=False):
     """Walled problems without solid cells or immersed-boundary samples: their AA step
-    kernels compute the link mask from the coordinates.  large: sizes that span several
-    thread blocks along x with ragged tails (for the GPU)."""
+    kernels compute the link mask of every cell from the coordinates.  large: sizes that
+    span several thread blocks along x with ragged tails (for the GPU)."""
     s3, s2, s27, sz = (((70, 40, 37), (300, 181, 1), (66, 20, 18), (64, 20, 24)) if large
                        else ((9, 7, 6), (10, 8, 1), (8, 6, 7), (7, 6, 9)))
     c3 = W.perturbed(W.cavity3d(shape=s3), seed=51)
@@ -192,11 +192,20 @@ def faces_only_cases(large=False):
     return [c3, c2, c2y, q27, outer_walls_case(shape=sz, seed=54)]
 
 
-def with_loaded_mask(w):
-    """The same problem with an all-zero solid array: the step kernels then load the link
-    mask instead of computing it."""
+def with_zero_solid_array(w):
+    """The same problem with an all-zero solid array instead of none."""
     return dataclasses.replace(w, solid=np.zeros(w.grid, np.uint8),
                                name=w.name + " (zero solid array)")
+
+
+def emulate_loaded_mask(emu_lib, w, steps):
+    """emulate() with the link mask loaded for every cell in the AA steps, instead of
+    computed from the coordinates outside the solid cells' box as the kernels do."""
+    emu_lib.emu_set_loaded_mask(1)
+    try:
+        return emulate(emu_lib, w, steps)
+    finally:
+        emu_lib.emu_set_loaded_mask(0)
 
 
 def degenerate_cases():

@@ -10,9 +10,9 @@ parity-aware.  The link mask is compared bit for bit with a brute-force builder.
 import numpy as np
 import pytest
 
-from parity_util import (degenerate_cases, emulate, emulate_slabs, faces_only_cases, fluid_of,
-                         mask_brute_force, oracle_states, outer_walls_case, slab_cases,
-                         small_cases, with_loaded_mask)
+from parity_util import (degenerate_cases, emulate, emulate_loaded_mask, emulate_slabs,
+                         faces_only_cases, fluid_of, mask_brute_force, oracle_states,
+                         outer_walls_case, slab_cases, small_cases)
 
 CASES = small_cases()
 
@@ -105,19 +105,21 @@ def test_degenerate_grids(oracle_mod, emu_lib, w, mode):
     assert np.array_equal(emulate(emu_lib, w, 0)[2], mask_brute_force(w))
 
 
-FACES = faces_only_cases()
+WALLED = faces_only_cases() + [c for c in small_cases() + slab_cases()
+                               if c.solid is not None and getattr(c, "ib_x", None) is None]
 
 
-@pytest.mark.parametrize("w", FACES, ids=[c.name for c in FACES])
+@pytest.mark.parametrize("w", WALLED, ids=[c.name for c in WALLED])
 def test_mask_from_coordinates_equals_loaded_mask(oracle_mod, emu_lib, w):
-    """A walled problem without solids runs the step with the link mask computed from the
-    coordinates; the same problem given an all-zero solid array loads the mask instead.
-    Both are bit-identical at both parities, and match the oracle."""
+    """The AA step with the link mask computed from the coordinates outside the solid cells'
+    box (as the kernels run it) and with the mask loaded for every cell are bit-identical at
+    both parities, and match the oracle.  (The emulation also checks, at every cell off a
+    ghost plane, that the computed mask equals the built one.)"""
     fluid = fluid_of(w)
     ref = oracle_states(oracle_mod, w, [5, 6])
     for n in (5, 6):
         f1, g1, m1 = emulate(emu_lib, w, n)
-        f2, g2, m2 = emulate(emu_lib, with_loaded_mask(w), n)
+        f2, g2, m2 = emulate_loaded_mask(emu_lib, w, n)
         assert np.array_equal(m1, m2)
         assert np.array_equal(f1, f2), n
         assert np.array_equal(g1, g2), n

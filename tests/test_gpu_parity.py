@@ -14,7 +14,7 @@ import pytest
 from lattice_boltzmann_cfd_gb300 import workloads as W
 from parity_util import (TOL_FIELDS, TOL_FORCE_REL, compare_fields, degenerate_cases,
                          faces_only_cases, fluid_of, gpu_states, mask_brute_force, oracle_states,
-                         small_cases, with_loaded_mask)
+                         small_cases, with_zero_solid_array)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -345,16 +345,16 @@ FACES = faces_only_cases(large=True)
 
 
 @pytest.mark.parametrize("w", FACES, ids=[c.name for c in FACES])
-def test_mask_from_coordinates_equals_loaded_mask(w):
-    """The step kernels that compute the link mask from the coordinates (walls on the faces
-    only) and those that load it (the same problem with an all-zero solid array) give
-    bit-identical states at both parities."""
+def test_zero_solid_array_changes_nothing(w):
+    """A walled problem without a solid array and the same problem with an all-zero one give
+    bit-identical states at both parities (the solid cells' box is empty in both, so every
+    cell's link mask comes from its coordinates)."""
     def run(prob, steps):
         out = gpu_states(prob, [steps], window_fn=lambda r: {
             k: (None if r[k] is None else r[k].cpu().numpy()) for k in ("f", "g")})
         return out[steps]
     for n in (7, 8):
-        a, b = run(w, n), run(with_loaded_mask(w), n)
+        a, b = run(w, n), run(with_zero_solid_array(w), n)
         assert np.array_equal(a["f"], b["f"]), n
         if w.thermal:
             assert np.array_equal(a["g"], b["g"]), n
