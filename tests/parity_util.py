@@ -192,6 +192,27 @@ def faces_only_cases(large=False):
     return [c3, c2, c2y, q27, outer_walls_case(shape=sz, seed=54)]
 
 
+def box_edge_cases():
+    """Solid cells against the faces: a block across the periodic x faces (its widened box
+    wraps, so the whole x axis is inside), a block on a wall face (the box is clipped), one
+    solid cell in a corner of a periodic box, and a 2-D cavity with a solid strip along a
+    Dirichlet wall."""
+    ch = W.perturbed(W.channel_sphere(shape=(11, 9, 8), center=(5, 4, 4), radius=0.0), seed=61)
+    sol = np.zeros(ch.grid, np.uint8)
+    sol[3:5, 2:4, 0] = 1          # z, y, x = 0: across the periodic x faces
+    sol[0, 5:7, 6:8] = 1          # on the z = 0 wall
+    a = dataclasses.replace(ch, solid=sol, name="channel, solids on a periodic face and a wall")
+    rp = W.random_periodic(shape=(7, 6, 5), seed=62)
+    sol = np.zeros(rp.grid, np.uint8)
+    sol[0, 0, 0] = 1
+    b = dataclasses.replace(rp, solid=sol, name="periodic box, one solid corner cell")
+    c2 = W.perturbed(W.cavity2d(shape=(12, 9, 1)), seed=63)
+    sol = np.zeros(c2.grid, np.uint8)
+    sol[0, 3:6, 0] = 1            # along the hot x = 0 wall
+    c = dataclasses.replace(c2, solid=sol, gbeta=0.01, name="2-D cavity, solid strip on a wall")
+    return [a, b, c]
+
+
 def with_zero_solid_array(w):
     """The same problem with an all-zero solid array instead of none."""
     return dataclasses.replace(w, solid=np.zeros(w.grid, np.uint8),

@@ -10,9 +10,9 @@ parity-aware.  The link mask is compared bit for bit with a brute-force builder.
 import numpy as np
 import pytest
 
-from parity_util import (degenerate_cases, emulate, emulate_loaded_mask, emulate_slabs,
-                         faces_only_cases, fluid_of, mask_brute_force, oracle_states,
-                         outer_walls_case, slab_cases, small_cases)
+from parity_util import (box_edge_cases, degenerate_cases, emulate, emulate_loaded_mask,
+                         emulate_slabs, faces_only_cases, fluid_of, mask_brute_force,
+                         oracle_states, outer_walls_case, slab_cases, small_cases)
 
 CASES = small_cases()
 
@@ -128,30 +128,7 @@ def test_mask_from_coordinates_equals_loaded_mask(oracle_mod, emu_lib, w):
             assert np.abs(g1 - ref[n]["g"])[:, fluid].max() < 1e-6, n
 
 
-def _box_edge_cases():
-    """Solid cells against the faces: a block touching the periodic x faces (its widened box
-    wraps, so the whole x axis is inside), a block on a wall face (the box is clipped), one
-    solid cell in a corner of a periodic box, and a 2-D cavity with a solid strip along a
-    Dirichlet wall."""
-    import dataclasses
-    from lattice_boltzmann_cfd_gb300 import workloads as W
-    ch = W.perturbed(W.channel_sphere(shape=(11, 9, 8), center=(5, 4, 4), radius=0.0), seed=61)
-    sol = np.zeros(ch.grid, np.uint8)
-    sol[3:5, 2:4, 0] = 1          # z, y, x = 0: across the periodic x faces
-    sol[0, 5:7, 6:8] = 1          # on the z = 0 wall
-    a = dataclasses.replace(ch, solid=sol, name="channel, solids on a periodic face and a wall")
-    rp = W.random_periodic(shape=(7, 6, 5), seed=62)
-    sol = np.zeros(rp.grid, np.uint8)
-    sol[0, 0, 0] = 1
-    b = dataclasses.replace(rp, solid=sol, name="periodic box, one solid corner cell")
-    c2 = W.perturbed(W.cavity2d(shape=(12, 9, 1)), seed=63)
-    sol = np.zeros(c2.grid, np.uint8)
-    sol[0, 3:6, 0] = 1            # along the hot x = 0 wall
-    c = dataclasses.replace(c2, solid=sol, gbeta=0.01, name="2-D cavity, solid strip on a wall")
-    return [a, b, c]
-
-
-BOX_EDGES = _box_edge_cases()
+BOX_EDGES = box_edge_cases()
 
 
 @pytest.mark.parametrize("w", BOX_EDGES, ids=[c.name for c in BOX_EDGES])

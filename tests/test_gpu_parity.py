@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 
 from lattice_boltzmann_cfd_gb300 import workloads as W
-from parity_util import (TOL_FIELDS, TOL_FORCE_REL, compare_fields, degenerate_cases,
+from parity_util import (TOL_FIELDS, TOL_FORCE_REL, box_edge_cases, compare_fields,
+                         degenerate_cases,
                          faces_only_cases, fluid_of, gpu_states, mask_brute_force, oracle_states,
                          small_cases, with_zero_solid_array)
 
@@ -340,6 +341,20 @@ def test_full_size_sampled_windows(oracle_mod, name, perturb):
 
 
 # ------------------------------------------------------------------- link mask -----
+
+BOX_EDGES = box_edge_cases()
+
+
+@pytest.mark.parametrize("w", BOX_EDGES, ids=[c.name for c in BOX_EDGES])
+def test_solid_box_at_the_faces_200_and_201_steps(oracle_mod, w):
+    """Solids across a periodic face, on a wall, in a corner and along a Dirichlet wall: the
+    kernels' box around them (outside it the mask comes from the coordinates) gives the
+    oracle's state at both parities."""
+    got = gpu_states(w, [200, 201])
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    for n in (200, 201):
+        compare_fields(w, got[n], ref[n])
+
 
 FACES = faces_only_cases(large=True)
 
