@@ -134,7 +134,11 @@ typedef struct {
     int face_T[6];        /* LBM_TFACE_ADIABATIC or LBM_TFACE_DIRICHLET (WALL faces)    */
     double T_wall[6];     /* wall temperature of DIRICHLET faces                       */
     const uint8_t *solid_mask; /* HOST pointer, nx*ny*nz bytes, x fastest, nonzero =
-                                  solid; NULL = no solid cells.  Copied by lbm_create. */
+                                  solid; NULL = no solid cells.  Read once by
+                                  lbm_workspace_bytes and lbm_create (the bounding box
+                                  of the solid cells, outside which the step derives
+                                  the link mask from the coordinates) and copied by
+                                  lbm_create; not kept. */
     int streaming;        /* LBM_STREAM_AA (default 0), LBM_STREAM_PULL or LBM_STREAM_SPLIT */
     int ib_max_samples;   /* capacity for immersed-boundary samples (0 = none); see
                              lbm_set_ib_samples                                          */
