@@ -7,6 +7,7 @@
 // slot of a fluid cell were left unwritten, the stale or NaN value would reach the
 // results; tests compare them with the oracle.
 // The read-out uses the parity-aware logical load, as lbm_get_populations does.
+#include <algorithm>
 #include <array>
 #include <cmath>
 #include <cstring>
@@ -359,7 +360,118 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
     return 0;
 }
 
+// Read and write sets of one AA step, brute force on a tiny grid.  W(c): the slots cell c
+// writes, found by stepping c alone into a NaN-filled buffer.  R(c): the slots whose value
+// reaches c's outputs, found by poisoning each slot of the state with NaN in turn.  The step
+// is race-free in place when R(c) == W(c) for every cell and no slot lies in two cells' W.
+// The step runs in the form the kernels use (F: mask from the coordinates outside the solid
+// cells' box).  Returns the number of violations.
+template <class L, class TL, int C, bool M, bool F, bool O>
+long long race_violations(Domain<L, TL, C, true> &d)
+{
+    const float nan = std::numeric_limits<float>::quiet_NaN();
+    const Params Pr = d.P;
+    Params Pw = d.P;
+    std::vector<float> wf(d.f.size()), wg(d.g.size());
+    Pw.f = wf.data();
+    Pw.g = d.Lay.QT ? wg.data() : nullptr;
+    std::vector<int> owner_f(wf.size(), -1), owner_g(wg.size(), -1);
+    long long bad = 0;
+    std::vector<size_t> Wf, Wg;
+    auto step_cell = [&](int x, int y, int z) {
+        std::fill(wf.begin(), wf.end(), nan);
+        std::fill(wg.begin(), wg.end(), nan);
+        aa_step_cell<L, TL, C, M, O, true, M && !F, F>(Pr, Pw, x, y, z);
+    };
+    auto outputs_poisoned = [&]() {
+        for (size_t s : Wf)
+            if (std::isnan(wf[s])) return true;
+        for (size_t s : Wg)
+            if (std::isnan(wg[s])) return true;
+        return false;
+    };
+    auto read_set_check = [&](std::vector<float> &state, const std::vector<size_t> &W, int x,
+                              int y, int z) {
+        for (size_t s = 0; s < state.size(); ++s) {
+            const float keep = state[s];
+            state[s] = nan;
+            step_cell(x, y, z);
+            const bool read = outputs_poisoned();
+            state[s] = keep;
+            const bool written = std::binary_search(W.begin(), W.end(), s);
+            if (read != written) ++bad;
+        }
+    };
+    for (int z = 0; z < d.cfg.nz; ++z)
+        for (int y = 0; y < d.cfg.ny; ++y)
+            for (int x = 0; x < d.cfg.nx; ++x) {
+                const int c = x + d.cfg.nx * (y + d.cfg.ny * z);
+                step_cell(x, y, z);
+                Wf.clear();
+                Wg.clear();
+                for (size_t s = 0; s < wf.size(); ++s)
+                    if (!std::isnan(wf[s])) Wf.push_back(s);
+                if (d.Lay.QT)
+                    for (size_t s = 0; s < wg.size(); ++s)
+                        if (!std::isnan(wg[s])) Wg.push_back(s);
+                for (size_t s : Wf) {
+                    if (owner_f[s] >= 0) ++bad;
+                    owner_f[s] = c;
+                }
+                for (size_t s : Wg) {
+                    if (owner_g[s] >= 0) ++bad;
+                    owner_g[s] = c;
+                }
+                read_set_check(d.f, Wf, x, y, z);
+                if (d.Lay.QT) read_set_check(d.g, Wg, x, y, z);
+            }
+    return bad;
+}
+
+template <class L, class TL, int C>
+long long race_any(const lbm_config &cfg, const lbm_setup::Layout &Lay, bool odd)
+{
+    Domain<L, TL, C, true> d(cfg, Lay);
+    if (d.face_mask_mismatches) return -30;
+    const size_t N = (size_t)Lay.N;
+    std::vector<float> rho(N), u(3 * N), T(N);
+    for (size_t i = 0; i < N; ++i) {
+        rho[i] = 1.0f + 1e-3f * (float)(i % 7);
+        for (int a = 0; a < 3; ++a) u[a * N + i] = 0.01f * (float)((i + 3 * a) % 5) - 0.02f;
+        T[i] = 0.05f * (float)(i % 3);
+    }
+    d.init(rho.data(), u.data(), T.data());
+    const bool M = Lay.masked, F = Lay.masked && Lay.ib_cap == 0;
+    if (!M) return odd ? race_violations<L, TL, C, false, false, true>(d)
+                       : race_violations<L, TL, C, false, false, false>(d);
+    if (F) return odd ? race_violations<L, TL, C, true, true, true>(d)
+                      : race_violations<L, TL, C, true, true, false>(d);
+    return odd ? race_violations<L, TL, C, true, false, true>(d)
+               : race_violations<L, TL, C, true, false, false>(d);
+}
+
 }  // namespace
+
+// Violations of race-freedom of one AA step (even: odd = 0) on a tiny grid, see
+// race_violations; negative on a bad configuration.
+extern "C" long long emu_race_violations(const lbm_config *cfg, int odd)
+{
+    lbm_setup::Layout Lay;
+    std::string why;
+    if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
+    if (cfg->streaming != LBM_STREAM_AA) return -2;
+    const bool mrt = cfg->collision == LBM_MRT, o = odd != 0;
+    if (cfg->lattice == 27) return race_any<D3Q27, NoThermal, 2>(*cfg, Lay, o);
+    if (cfg->lattice == 19) {
+        if (cfg->thermal == 7)
+            return mrt ? race_any<D3Q19, D3Q7, 1>(*cfg, Lay, o) : race_any<D3Q19, D3Q7, 0>(*cfg, Lay, o);
+        return mrt ? race_any<D3Q19, NoThermal, 1>(*cfg, Lay, o)
+                   : race_any<D3Q19, NoThermal, 0>(*cfg, Lay, o);
+    }
+    if (cfg->thermal == 5)
+        return mrt ? race_any<D2Q9, D2Q5, 1>(*cfg, Lay, o) : race_any<D2Q9, D2Q5, 0>(*cfg, Lay, o);
+    return mrt ? race_any<D2Q9, NoThermal, 1>(*cfg, Lay, o) : race_any<D2Q9, NoThermal, 0>(*cfg, Lay, o);
+}
 
 template <bool NARROW>
 int run_any(const lbm_config *cfg, const lbm_setup::Layout &Lay, const float *rho,

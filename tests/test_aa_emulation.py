@@ -145,3 +145,43 @@ def test_solid_box_at_the_faces(oracle_mod, emu_lib, w):
         assert np.abs(f1 - ref[n]["f"])[:, fluid].max() < 1e-6, n
         if w.thermal:
             assert np.abs(g1 - ref[n]["g"])[:, fluid].max() < 1e-6, n
+
+
+def _race_cases():
+    """Tiny grids for the brute-force read/write-set check: every lattice and boundary
+    kind, solids, slab ghost planes and a degenerate extent."""
+    import dataclasses
+    from lattice_boltzmann_cfd_gb300 import workloads as W
+    rp = W.random_periodic(shape=(4, 4, 4), seed=71)
+    bgk2 = W.random_periodic(shape=(3, 4, 1), seed=72, collision="bgk", lattice=9)
+    c3 = W.perturbed(W.cavity3d(shape=(5, 4, 3)), seed=73)
+    sol = np.zeros(c3.grid, np.uint8)
+    sol[1, 2, 2] = 1
+    c3 = dataclasses.replace(c3, solid=sol, gbeta=0.01, name=c3.name + " + solid cell")
+    c2 = W.perturbed(W.cavity2d(shape=(5, 4, 1)), seed=74)
+    sol = np.zeros(c2.grid, np.uint8)
+    sol[0, 1, 3] = 1
+    c2 = dataclasses.replace(c2, solid=sol, gbeta=0.01, name=c2.name + " + solid cell")
+    q27 = W.perturbed(W.channel_sphere(shape=(4, 4, 4), center=(1, 2, 2), radius=0.0,
+                                       lattice=27), seed=75)
+    halo = dataclasses.replace(W.random_periodic(shape=(4, 3, 5), seed=76),
+                               face_flow=("periodic",) * 4 + ("halo", "halo"),
+                               name="D3Q19 slab 4x3x5 with ghost planes")
+    thin = dataclasses.replace(W.perturbed(W.cavity3d(shape=(1, 2, 3)), seed=77), gbeta=0.02,
+                               name="cavity 1x2x3")
+    return [rp, bgk2, c3, c2, q27, halo, outer_walls_case(shape=(4, 3, 5), seed=78), thin]
+
+
+RACE = _race_cases()
+
+
+@pytest.mark.parametrize("odd", [0, 1], ids=["even", "odd"])
+@pytest.mark.parametrize("w", RACE, ids=[c.name for c in RACE])
+def test_aa_step_reads_and_writes_the_same_slots(emu_lib, w, odd):
+    """Race-freedom of the in-place step, by brute force over every slot: each cell writes
+    exactly the slots whose values it uses, and no slot is written by two cells."""
+    import ctypes
+    from lattice_boltzmann_cfd_gb300.solver import make_config
+    cfg, keep = make_config(w, "aa")
+    emu_lib.emu_race_violations.restype = ctypes.c_longlong
+    assert emu_lib.emu_race_violations(ctypes.byref(cfg), odd) == 0
