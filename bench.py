@@ -549,9 +549,9 @@ def run_gpu(args, dctx):
                 "pipelined_value": round(pipelined_value, 1),
                 "pipelined": "the same steps through JobPipeline: copies on two copy streams "
                              "overlapping the neighbouring steps' LBM steps, each read-out "
-                             "issued behind the next step's kernels; about 42k MLUPS in a "
-                             "fresh process, 35-42k here after the other legs, so value is "
-                             "the serial path"},
+                             "issued behind the next step's kernels; 41-42k MLUPS in a "
+                             "fresh process, 35-42k between runs here, so value is the "
+                             "serial path"},
         "gpu_launches": args.steps * (args.lbm_steps + 2),
         "clocks": clocks,
     }
