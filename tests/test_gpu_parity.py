@@ -115,6 +115,41 @@ def test_immersed_boundary_200_and_201_steps(oracle_mod, w, streaming):
         _compare_ib(got[n], ref[n])
 
 
+def test_moving_samples_200_and_201_steps(oracle_mod):
+    """A sphere of samples translating through the channel, the samples replaced before
+    every step (lbm_set_ib_samples): after 200 and 201 steps the state matches the oracle
+    stepped with the same positions and boundary velocity."""
+    import torch
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = W.perturbed(W.channel_ib_sphere(shape=(24, 16, 14), center=(8.3, 7.7, 6.9), radius=3.0,
+                                        gx=1e-4, samples_per_area=2.0), seed=81)
+    v = np.array([0.02, 0.004, -0.003], np.float32)
+    ub = np.tile(v, (len(w.ib_x), 1))
+
+    def positions(k):
+        x = w.ib_x.astype(np.float64) + k * v.astype(np.float64)
+        x[:, 0] = np.mod(x[:, 0], w.shape[0])          # x is periodic
+        return x.astype(np.float32)
+
+    sim = Simulation(w)
+    sim.init_equilibrium(torch.from_numpy(w.rho0).cuda(), torch.from_numpy(w.u0).cuda())
+    p0 = oracle_mod.Problem(w)
+    f, g = oracle_mod.init_equilibrium(p0, w.rho0, w.u0)
+    for k in range(201):
+        xk = positions(k)
+        sim.set_ib_samples(xk, ub, w.ib_w)
+        sim.step(1)
+        oracle_mod.run(oracle_mod.Problem(dataclasses.replace(w, ib_x=xk, ib_ub=ub)), f, g, 1)
+        if k + 1 in (200, 201):
+            rho, u, _ = sim.macroscopic()
+            fg, _ = sim.populations()
+            r_rho, r_u, _ = oracle_mod.macroscopic(p0, f, g)
+            assert np.abs(rho.cpu().numpy() - r_rho).max() <= TOL_FIELDS, k + 1
+            assert np.abs(u.cpu().numpy() - r_u).max() <= TOL_FIELDS, k + 1
+            assert np.abs(fg.cpu().numpy() - f).max() <= TOL_FIELDS, k + 1
+    sim.close()
+
+
 def test_immersed_boundary_sample_order_does_not_matter():
     """The library sorts samples into l-blocks and Morton order; giving them in a shuffled
     order gives the same flow (up to the order of the atomic additions)."""

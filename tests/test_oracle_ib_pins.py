@@ -142,3 +142,34 @@ def test_steady_force_balance_with_body_force(oracle_mod):
     total_body = d["mass"] * w.g_body[0]
     assert abs(p.last_ib[0] / total_body - 1) < 1e-3
     assert abs(p.last_ib[1]) < 1e-3 * total_body and abs(p.last_ib[2]) < 1e-3 * total_body
+
+
+@pytest.mark.parametrize("lattice", [19, 9])
+def test_samples_moving_with_a_uniform_flow_exert_no_force(oracle_mod, lattice):
+    """A uniform flow u0 on a periodic box is a fixed point.  Samples that move with it
+    (displaced by u0 every step, boundary velocity u0) see u(x_s) = u0 wherever they sit
+    between the cells, since the kernel weights sum to 1, so their penalty
+    w rho (u_b - u) vanishes: every step's reaction force is zero and the state stays
+    uniform, while the samples sweep through new stencils."""
+    rng = np.random.default_rng(11)
+    shape = (10, 8, 6) if lattice == 19 else (10, 8, 1)
+    w = _box(shape, lattice)
+    dim = w.dim
+    u0 = np.array([0.03, -0.02, 0.01], np.float32)
+    w.u0 = np.broadcast_to(u0[:dim].reshape((dim,) + (1,) * 3), (dim,) + w.grid).astype(np.float32)
+    xs0 = _samples(rng, 7, 1.0, min(shape[:dim]) - 2.0, dim).astype(np.float64)
+    v = np.zeros(3)
+    v[:dim] = u0[:dim]
+    ub = np.tile(v.astype(np.float32), (len(xs0), 1))
+    ext = np.array(shape, np.float64)
+    f, g = oracle_mod.init_equilibrium(oracle_mod.Problem(w), w.rho0, w.u0)
+    for k in range(6):
+        xk = xs0 + k * v
+        xk[:, :dim] = np.mod(xk[:, :dim], ext[:dim])
+        p = oracle_mod.Problem(dataclasses.replace(w, ib_x=xk.astype(np.float32), ib_ub=ub))
+        oracle_mod.run(p, f, g, 1)
+        assert np.abs(p.last_ib[:3]).max() < 1e-13, k
+    rho, u, _ = oracle_mod.macroscopic(p, f, g)
+    assert np.abs(rho - 1.0).max() < 1e-13
+    for a in range(dim):
+        assert np.abs(u[a] - float(u0[a])).max() < 1e-13
