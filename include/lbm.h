@@ -185,7 +185,13 @@ lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace
 lbm_status lbm_init_equilibrium(lbm_ctx *ctx, const float *rho, const float *u, const float *T);
 
 /* Advance n >= 0 time steps ([TLBM] Eq. 5 and Eq. 7 fused with streaming, [AA]): one
- * kernel launch per step, alternating the even and odd AA forms. */
+ * kernel launch per step, alternating the even and odd AA forms (plus one immersed-boundary
+ * launch per step when samples are set).  On grids of two or more waves of thread blocks
+ * the step kernels are launched with programmatic stream serialization: a step's blocks may
+ * be scheduled while the kernel before it on the stream is finishing, but they wait for
+ * that kernel to complete, with its writes visible, before touching memory.  Work the
+ * caller puts on the stream before or after lbm_step is therefore ordered as usual.  Grids
+ * of at most 4 M cells replay captured graphs of 64 steps. */
 lbm_status lbm_step(lbm_ctx *ctx, int n);
 
 /* rho = sum f, u = (sum c f + F/2)/rho, T = sum g of the current state ([TLBM] Sec. 2).
