@@ -10,9 +10,13 @@ from lattice_boltzmann_cfd_gb300 import workloads as W
 
 
 def _box(shape=(12, 10, 8), lattice=19, **kw):
-    rates = ({"e": 1.2, "eps": 1.2, "q": 1.2, "pi": 1.2, "m": 1.2} if lattice == 19
-             else {"e": 1.2, "eps": 1.2, "q": 1.2})
-    w = W.Workload(name="ib", lattice=lattice, thermal=0, collision="mrt", shape=shape, nu=0.1,
+    if lattice == 27:
+        rates, coll = {"bulk": 1.2, "r3": 1.2, "r4": 1.2, "r5": 1.2, "r6": 1.2}, "cm"
+    elif lattice == 19:
+        rates, coll = {"e": 1.2, "eps": 1.2, "q": 1.2, "pi": 1.2, "m": 1.2}, "mrt"
+    else:
+        rates, coll = {"e": 1.2, "eps": 1.2, "q": 1.2}, "mrt"
+    w = W.Workload(name="ib", lattice=lattice, thermal=0, collision=coll, shape=shape, nu=0.1,
                    rates=rates, up_axis=1 if lattice == 9 else 2, **kw)
     dim = w.dim
     if w.rho0 is None:
@@ -29,14 +33,14 @@ def _samples(rng, n, lo, hi, dim):
     return x
 
 
-@pytest.mark.parametrize("lattice", [19, 9])
+@pytest.mark.parametrize("lattice", [19, 9, 27])
 def test_linear_field_interpolation_and_momentum_balance(oracle_mod, lattice):
     """With rho = 1 and a velocity field linear in x, y, z the trilinear kernel interpolates
     exactly, so the penalty of each sample is w (u_b - u(x_s)) in closed form; the spread
     conserves it (the kernel weights sum to 1), so the fluid momentum grows by exactly
     sum_s w (u_b - u(x_s)) in one step, and the reported reaction is minus that."""
     rng = np.random.default_rng(3)
-    shape = (12, 10, 8) if lattice == 19 else (12, 10, 1)
+    shape = (12, 10, 1) if lattice == 9 else (12, 10, 8)
     w = _box(shape, lattice)
     dim = w.dim
     nz, ny, nx = w.grid
@@ -144,7 +148,7 @@ def test_steady_force_balance_with_body_force(oracle_mod):
     assert abs(p.last_ib[1]) < 1e-3 * total_body and abs(p.last_ib[2]) < 1e-3 * total_body
 
 
-@pytest.mark.parametrize("lattice", [19, 9])
+@pytest.mark.parametrize("lattice", [19, 9, 27])
 def test_samples_moving_with_a_uniform_flow_exert_no_force(oracle_mod, lattice):
     """A uniform flow u0 on a periodic box is a fixed point.  Samples that move with it
     (displaced by u0 every step, boundary velocity u0) see u(x_s) = u0 wherever they sit
@@ -152,7 +156,7 @@ def test_samples_moving_with_a_uniform_flow_exert_no_force(oracle_mod, lattice):
     w rho (u_b - u) vanishes: every step's reaction force is zero and the state stays
     uniform, while the samples sweep through new stencils."""
     rng = np.random.default_rng(11)
-    shape = (10, 8, 6) if lattice == 19 else (10, 8, 1)
+    shape = (10, 8, 1) if lattice == 9 else (10, 8, 6)
     w = _box(shape, lattice)
     dim = w.dim
     u0 = np.array([0.03, -0.02, 0.01], np.float32)
