@@ -7,6 +7,7 @@ e in {0,1,2}^3, with the second-order normal ones recombined as xx - yy, xx - zz
 rate 1/tau) and xx + yy + zz (bulk rate); orders 3 to 6 relax at one fixed rate each; the
 equilibrium central moments are those of a Maxwellian, rho prod_a (1, 0, 1/3)[e_a]; the
 force source is (F/rho) . d f_eq / du, relaxed with (I - D/2), with u = (j + F/2)/rho."""
+import dataclasses
 import itertools
 import math
 
@@ -240,3 +241,95 @@ def test_poiseuille_between_walls(oracle_mod):
     exact = gx * z * (n - z) / (2 * nu)
     assert np.abs(u[0, :, 0, 0] - exact).max() < 5e-3 * exact.max()
     assert np.abs(u[1:]).max() < 1e-12
+
+
+# ------------------------------------- streaming, walls, conservation on D3Q27 -------
+
+_FROZEN = {"bulk": 1e-300, "r3": 1e-300, "r4": 1e-300, "r5": 1e-300, "r6": 1e-300}
+
+
+def _frozen(shape, **kw):
+    """No relaxation: every central-moment rate 1e-300 and the shear rate 1/tau ~ 3e-13
+    (nu = 1e12), so a step is streaming (with the wall rules) to ~1e-12."""
+    return _cube(shape, rates=dict(_FROZEN), nu=1e12, **kw)
+
+
+def _opp(c):
+    return [int(np.nonzero((c == -c[q]).all(axis=1))[0][0]) for q in range(27)]
+
+
+def test_d3q27_streaming_is_the_lattice_permutation(oracle_mod):
+    """Without relaxation a D3Q27 step is the pull permutation f_q(x) <- f_q(x - c_q) on
+    the periodic grid, for all 27 velocities (brute force with np.roll)."""
+    shape = (5, 4, 3)
+    w = _frozen(shape)
+    p = oracle_mod.Problem(w)
+    f = np.random.default_rng(21).random((27,) + w.grid)
+    g = np.zeros((1,) + w.grid)
+    c, _, _ = oracle_mod.lattice(27)
+    expect = np.stack([np.roll(f[q], shift=(c[q, 2], c[q, 1], c[q, 0]), axis=(0, 1, 2))
+                       for q in range(27)])
+    oracle_mod.run(p, f, g, 1)
+    assert np.allclose(f, expect, rtol=0, atol=1e-10)
+
+
+def test_d3q27_bounce_back_links_brute_force(oracle_mod):
+    """Without relaxation, with walls on y and z and a solid cell, each D3Q27 wall link
+    (corner links included) returns the cell's own opposite population."""
+    shape = (5, 4, 3)
+    solid = np.zeros(shape[::-1], np.uint8)
+    solid[1, 2, 2] = 1
+    w = _frozen(shape, face_flow=("periodic", "periodic", "wall", "wall", "wall", "wall"),
+                solid=solid)
+    p = oracle_mod.Problem(w)
+    f = np.random.default_rng(22).random((27,) + w.grid)
+    f[:, solid == 1] = 0.0
+    g = np.zeros((1,) + w.grid)
+    f_old = f.copy()
+    oracle_mod.run(p, f, g, 1)
+    c, _, _ = oracle_mod.lattice(27)
+    opp = _opp(c)
+    nx, ny, nz = shape
+    for z, y, x in itertools.product(range(nz), range(ny), range(nx)):
+        if solid[z, y, x]:
+            continue
+        for q in range(27):
+            sx, sy, sz = (x - c[q, 0]) % nx, y - c[q, 1], z - c[q, 2]
+            wall = not (0 <= sy < ny and 0 <= sz < nz) or solid[sz, sy, sx]
+            want = f_old[opp[q], z, y, x] if wall else f_old[q, sz, sy, sx]
+            assert abs(f[q, z, y, x] - want) < 1e-10
+
+
+def test_d3q27_mass_momentum_and_forcing(oracle_mod):
+    """Periodic D3Q27 with the fixed central-moment rates: mass is conserved to 1e-12 and
+    the total momentum grows by exactly sum(rho) g per step."""
+    w = W.random_periodic(shape=(6, 5, 4), seed=23, lattice=27, nu=0.05)
+    w = dataclasses.replace(w, g_body=(2e-4, -1e-4, 5e-5))
+    p = oracle_mod.Problem(w)
+    f, g = oracle_mod.init_equilibrium(p, w.rho0, w.u0)
+    for _ in range(4):
+        d0 = oracle_mod.diagnostics(p, f, g)
+        oracle_mod.run(p, f, g, 1)
+        d1 = oracle_mod.diagnostics(p, f, g)
+        assert abs(d1["mass"] - d0["mass"]) <= 1e-12 * d0["mass"]
+        expect = d0["mass"] * np.array(w.g_body)
+        assert np.allclose(d1["momentum"] - d0["momentum"], expect, rtol=1e-10, atol=1e-15)
+
+
+def test_d3q27_momentum_exchange_balances_momentum(oracle_mod):
+    """Periodic D3Q27 box with a solid obstacle and a body force: per step the fluid's
+    momentum change equals the body force minus the momentum exchanged with the solid."""
+    shape = (10, 8, 7)
+    solid = W.sphere_mask(shape, (4, 4, 3), 2.0)
+    base = W.perturbed(W.channel_sphere(shape=shape, lattice=27), seed=24)
+    w = dataclasses.replace(base, face_flow=("periodic",) * 6, solid=solid,
+                            g_body=(1e-4, 3e-5, -2e-5))
+    p = oracle_mod.Problem(w)
+    f, g = oracle_mod.init_equilibrium(p, w.rho0, w.u0)
+    for _ in range(3):
+        d0 = oracle_mod.diagnostics(p, f, g)
+        F = oracle_mod.run(p, f, g, 1)
+        d1 = oracle_mod.diagnostics(p, f, g)
+        body = d0["mass"] * np.array(w.g_body)
+        assert np.allclose(d1["momentum"] - d0["momentum"], body - F, rtol=0, atol=1e-13)
+        assert np.linalg.norm(F) > 1e-6
