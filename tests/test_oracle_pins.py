@@ -5,6 +5,7 @@ form, a conservation law, an exact fixed point, a brute-force permutation, or a 
 pages print.  CPU only.
 """
 import dataclasses
+import itertools
 import json
 import math
 import os
@@ -257,6 +258,61 @@ def test_bounce_back_links_brute_force(oracle_mod):
                     wall = not (0 <= sy < ny and 0 <= sz < nz) or solid[sz, sy, sx]
                     want = f_old[opp[q], z, y, x] if wall else f_old[q, sz, sy, sx]
                     assert abs(f[q, z, y, x] - want) < 1e-11
+
+
+@pytest.mark.parametrize("lattice,thermal", [(19, 7), (9, 5)])
+def test_thermal_wall_links_brute_force(oracle_mod, lattice, thermal):
+    """Without relaxation (flow and thermal rates ~0), one step on a cavity with Dirichlet
+    x faces, adiabatic walls elsewhere and a solid cell, checked link by link: a thermal
+    link through a Dirichlet face returns -g_opp(x) + omega T_w with the page's omega,
+    (4 + a_T)/10 on D2Q5 and (6 + a_T)/21 on D3Q7 ("Multi-GPU thermal lattice Boltzmann
+    simulations using OpenACC and MPI", Sec. 2); a link through an adiabatic wall or into
+    the solid returns g_opp(x); every other link streams, g_k(x) = g_k(x - c_k)."""
+    shape = (5, 4, 3) if lattice == 19 else (6, 5, 1)
+    base = W.cavity3d(shape=shape) if lattice == 19 else W.cavity2d(shape=shape)
+    solid = np.zeros(base.grid, np.uint8)
+    solid[(0, 2, 2) if lattice == 9 else (1, 2, 2)] = 1
+    frozen = ({k: 0.0 for k in ("e", "eps", "q", "pi", "m")} if lattice == 19
+              else {k: 0.0 for k in ("e", "eps", "q")})
+    a_T = 0.3
+    w = dataclasses.replace(base, solid=solid, nu=1e12, rates=frozen, kappa=1e12,
+                            thermal_rates={"e": 0.0, "v": 0.0}, a_T=a_T, gbeta=0.0,
+                            T_wall=(0.7, -0.4, 0.0, 0.0, 0.0, 0.0))
+    omega = (4.0 + a_T) / 10.0 if thermal == 5 else (6.0 + a_T) / 21.0
+    p = oracle_mod.Problem(w)
+    rng = np.random.default_rng(9)
+    f = 0.05 + 0.01 * rng.random((lattice,) + w.grid)
+    g = rng.uniform(-0.2, 0.2, size=(thermal,) + w.grid)
+    g_old = g.copy()
+    oracle_mod.run(p, f, g, 1)
+    c, _, _ = oracle_mod.lattice(thermal)
+    opp = [int(np.nonzero((c == -c[k]).all(axis=1))[0][0]) for k in range(thermal)]
+    nz, ny, nx = w.grid
+    n = (nx, ny, nz)
+    checked = 0
+    for z, y, x in itertools.product(range(nz), range(ny), range(nx)):
+        if solid[z, y, x]:
+            continue
+        for k in range(thermal):
+            src = [x - c[k, 0], y - c[k, 1], z - c[k, 2]]
+            face = None
+            for a in range(3):
+                if src[a] < 0:
+                    face = 2 * a
+                elif src[a] >= n[a]:
+                    face = 2 * a + 1
+            if face is not None:
+                if w.face_T[face] == "dirichlet":
+                    want = -g_old[opp[k], z, y, x] + omega * w.T_wall[face]
+                else:
+                    want = g_old[opp[k], z, y, x]
+            elif solid[src[2], src[1], src[0]]:
+                want = g_old[opp[k], z, y, x]
+            else:
+                want = g_old[k, src[2], src[1], src[0]]
+            assert abs(g[k, z, y, x] - want) < 1e-10, (x, y, z, k)
+            checked += 1
+    assert checked == thermal * (nx * ny * nz - 1)
 
 
 # -------------------------------------------------------------------- MRT --------
