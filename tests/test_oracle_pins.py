@@ -213,47 +213,56 @@ def test_guo_forcing_momentum_increment(oracle_mod):
 
 # ---------------------------------------------------------------- streaming ------
 
-@pytest.mark.parametrize("shape", [(4, 4, 4), (5, 4, 3)])
-def test_streaming_is_the_lattice_permutation(oracle_mod, shape):
+_FROZEN_RATES = {19: ("e", "eps", "q", "pi", "m"), 9: ("e", "eps", "q")}
+
+
+@pytest.mark.parametrize("lattice,shape", [(19, (4, 4, 4)), (19, (5, 4, 3)), (9, (5, 4, 1))])
+def test_streaming_is_the_lattice_permutation(oracle_mod, lattice, shape):
     """With no relaxation (every rate 0, no force) a step is pure streaming: the new
     f_q(x) is f_q(x - c_q) on the periodic grid (brute force with np.roll)."""
     # the viscous rate follows from nu: a huge nu makes it ~3e-13
-    w = _spec(shape=shape, nu=1e12, rates={k: 0.0 for k in ("e", "eps", "q", "pi", "m")})
+    w = _spec(lattice=lattice, shape=shape, nu=1e12,
+              rates={k: 0.0 for k in _FROZEN_RATES[lattice]})
     p = oracle_mod.Problem(w)
     rng = np.random.default_rng(1)
-    f = rng.random((19,) + w.grid)
+    Q = lattice
+    f = rng.random((Q,) + w.grid)
     g = np.zeros((1,) + w.grid)
-    c, _, _ = oracle_mod.lattice(19)
+    c, _, _ = oracle_mod.lattice(Q)
     expect = np.stack([np.roll(f[q], shift=(c[q, 2], c[q, 1], c[q, 0]), axis=(0, 1, 2))
-                       for q in range(19)])
+                       for q in range(Q)])
     oracle_mod.run(p, f, g, 1)
     assert np.allclose(f, expect, rtol=0, atol=1e-11)
 
 
-def test_bounce_back_links_brute_force(oracle_mod):
+@pytest.mark.parametrize("lattice", [19, 9])
+def test_bounce_back_links_brute_force(oracle_mod, lattice):
     """With no relaxation, on a grid with walls and a solid cell, each wall link returns
     the cell's own opposite population (brute force over every cell and direction)."""
-    shape = (5, 4, 3)
+    shape = (5, 4, 3) if lattice == 19 else (6, 5, 1)
     solid = np.zeros(shape[::-1], np.uint8)
-    solid[1, 2, 2] = 1
-    w = _spec(shape=shape, nu=1e12, rates={k: 0.0 for k in ("e", "eps", "q", "pi", "m")},
-              face_flow=("periodic", "periodic", "wall", "wall", "wall", "wall"), solid=solid)
+    solid[(1, 2, 2) if lattice == 19 else (0, 2, 2)] = 1
+    # x periodic, every other axis walled (z is unused in 2-D: c_z = 0)
+    faces = ("periodic", "periodic", "wall", "wall", "wall", "wall")
+    w = _spec(lattice=lattice, shape=shape, nu=1e12,
+              rates={k: 0.0 for k in _FROZEN_RATES[lattice]}, face_flow=faces, solid=solid)
     p = oracle_mod.Problem(w)
     rng = np.random.default_rng(2)
-    f = rng.random((19,) + w.grid)
+    Q = lattice
+    f = rng.random((Q,) + w.grid)
     f[:, solid == 1] = 0.0
     g = np.zeros((1,) + w.grid)
     f_old = f.copy()
     oracle_mod.run(p, f, g, 1)
-    c, _, _ = oracle_mod.lattice(19)
-    opp = [int(np.nonzero((c == -c[q]).all(axis=1))[0][0]) for q in range(19)]
+    c, _, _ = oracle_mod.lattice(Q)
+    opp = [int(np.nonzero((c == -c[q]).all(axis=1))[0][0]) for q in range(Q)]
     nx, ny, nz = shape
     for z in range(nz):
         for y in range(ny):
             for x in range(nx):
                 if solid[z, y, x]:
                     continue
-                for q in range(19):
+                for q in range(Q):
                     sx, sy, sz = (x - c[q, 0]) % nx, y - c[q, 1], z - c[q, 2]
                     wall = not (0 <= sy < ny and 0 <= sz < nz) or solid[sz, sy, sx]
                     want = f_old[opp[q], z, y, x] if wall else f_old[q, sz, sy, sx]
