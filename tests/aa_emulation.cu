@@ -26,6 +26,18 @@ namespace {
 // box, as the kernels do; for tests that compare the two (emu_set_loaded_mask).
 bool g_loaded_mask = false;
 
+// Every population buffer carries GUARD NaN floats before and after its Q * S slots.  A read
+// outside the slots yields NaN, which reaches the results; a write outside them is found by
+// guards_intact() after every step.
+constexpr size_t GUARD = 1024;
+
+bool guards_intact(const std::vector<float> &v)
+{
+    for (size_t i = 0; i < GUARD; ++i)
+        if (!std::isnan(v[i]) || !std::isnan(v[v.size() - 1 - i])) return false;
+    return true;
+}
+
 // F: the mask computed from the coordinates outside the solid cells' box (boxed_mask), as
 // the kernels do without an immersed boundary.
 template <class L, class TL, int C, bool M, bool O, bool NARROW, bool F = false>
@@ -121,10 +133,10 @@ struct Domain {
     {
         const float nan = std::numeric_limits<float>::quiet_NaN();
         const size_t S = Lay.S;
-        f.assign(Lay.Q * S, nan);
-        fn.assign(Lay.Q * S, nan);
-        g.assign((Lay.QT ? Lay.QT : 1) * S, nan);
-        gn.assign((Lay.QT ? Lay.QT : 1) * S, nan);
+        f.assign(Lay.Q * S + 2 * GUARD, nan);
+        fn.assign(Lay.Q * S + 2 * GUARD, nan);
+        g.assign((Lay.QT ? Lay.QT : 1) * S + 2 * GUARD, nan);
+        gn.assign((Lay.QT ? Lay.QT : 1) * S + 2 * GUARD, nan);
         mask.assign(S, 0u);
         ws.resize(Lay.bytes + 256);
         lbm_setup::fill_params(cfg, Lay, ws.data(), P);
@@ -148,9 +160,11 @@ struct Domain {
 
     void point()
     {
-        P.f = f.data();
-        P.g = Lay.QT ? g.data() : nullptr;
+        P.f = f.data() + GUARD;
+        P.g = Lay.QT ? g.data() + GUARD : nullptr;
     }
+
+    long long guard_violations = 0;
 
     // immersed-boundary samples (given inside the domain) and their stencils' IB_BIT
     void set_ib(int ib_n, const float *ib_x, const float *ib_ub, const float *ib_w)
@@ -199,19 +213,20 @@ struct Domain {
         std::fill(fn.begin(), fn.end(), nan);
         std::fill(gn.begin(), gn.end(), nan);
         Params Pw = P;
-        Pw.f = fn.data();
-        Pw.g = Lay.QT ? gn.data() : nullptr;
-        float *wg = Lay.QT ? gn.data() : nullptr;
+        Pw.f = fn.data() + GUARD;
+        Pw.g = Lay.QT ? gn.data() + GUARD : nullptr;
+        float *wf = fn.data() + GUARD;
+        float *wg = Lay.QT ? gn.data() + GUARD : nullptr;
         ib_pass<L, TL>(P, mode == LBM_STREAM_PULL    ? PULL
                           : mode == LBM_STREAM_SPLIT ? NATURAL
                           : parity                   ? AA_ODD
                                                      : NATURAL);
         if (mode == LBM_STREAM_PULL) {
-            if (Lay.masked) pull_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
-            else pull_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
+            if (Lay.masked) pull_all<L, TL, C, true, NARROW>(P, wf, wg);
+            else pull_all<L, TL, C, false, NARROW>(P, wf, wg);
         } else if (mode == LBM_STREAM_SPLIT) {
-            if (Lay.masked) split_all<L, TL, C, true, NARROW>(P, fn.data(), wg);
-            else split_all<L, TL, C, false, NARROW>(P, fn.data(), wg);
+            if (Lay.masked) split_all<L, TL, C, true, NARROW>(P, wf, wg);
+            else split_all<L, TL, C, false, NARROW>(P, wf, wg);
         } else if (Lay.masked && Lay.ib_cap == 0 && !g_loaded_mask) {
             if (parity) step_all<L, TL, C, true, true, NARROW, true>(P, Pw);
             else step_all<L, TL, C, true, false, NARROW, true>(P, Pw);
@@ -222,6 +237,8 @@ struct Domain {
             if (parity) step_all<L, TL, C, false, true, NARROW>(P, Pw);
             else step_all<L, TL, C, false, false, NARROW>(P, Pw);
         }
+        for (const auto *v : {&f, &fn, &g, &gn})
+            if (!guards_intact(*v)) ++guard_violations;
         f.swap(fn);
         g.swap(gn);
         point();
@@ -262,6 +279,7 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
     if (ib_n > 0) d.set_ib(ib_n, ib_x, ib_ub, ib_w);
     d.init(rho, u, T);
     for (int s = 0; s < steps; ++s) d.step();
+    if (d.guard_violations) return -31;
     d.read(fout, gout);
     if (mask_out) std::memcpy(mask_out, d.mask.data(), sizeof(uint32_t) * (size_t)Lay.N);
     return 0;
@@ -341,6 +359,8 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
             doms[b]->halo(0, phase, 1, bufs[a][1].data());
         }
     }
+    for (auto &d : doms)
+        if (d->guard_violations) return -32;
     const int QT = TL::Q;
     for (int r = 0; r < nslabs; ++r) {
         const Dom &d = *doms[r];
@@ -373,8 +393,8 @@ long long race_violations(Domain<L, TL, C, true> &d)
     const Params Pr = d.P;
     Params Pw = d.P;
     std::vector<float> wf(d.f.size()), wg(d.g.size());
-    Pw.f = wf.data();
-    Pw.g = d.Lay.QT ? wg.data() : nullptr;
+    Pw.f = wf.data() + GUARD;
+    Pw.g = d.Lay.QT ? wg.data() + GUARD : nullptr;
     std::vector<int> owner_f(wf.size(), -1), owner_g(wg.size(), -1);
     long long bad = 0;
     std::vector<size_t> Wf, Wg;
