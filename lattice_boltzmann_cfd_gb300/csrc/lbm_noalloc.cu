@@ -145,11 +145,15 @@ extern "C" lbm_status lbm_reduce_populations_static(int lattice, int thermal, in
                                          (lattice == LBM_D2Q9 && thermal == LBM_D2Q5)))
         return reject(LBM_ERR_ARG, "thermal lattice must be none, D3Q7 (D3Q19) or D2Q5 (D2Q9)");
     if (nx < 1 || ny < 1 || nz < 1) return reject(LBM_ERR_ARG, "grid sizes must be >= 1");
-    const long long N = (long long)nx * ny * nz;
-    if (N > RED_MAX_CELLS)
-        return reject(LBM_ERR_ARG, "lbm_reduce_populations_static: " + std::to_string(N) +
+    if (lattice == LBM_D2Q9 && nz != 1) return reject(LBM_ERR_ARG, "D2Q9 needs nz == 1");
+    // nx*ny < 2^62 cannot overflow; once it is within the limit, so is the product with nz
+    const long long nxy = (long long)nx * ny;
+    if (nxy > RED_MAX_CELLS || nxy * nz > RED_MAX_CELLS)
+        return reject(LBM_ERR_ARG, "lbm_reduce_populations_static: " + std::to_string(nx) +
+                                       "x" + std::to_string(ny) + "x" + std::to_string(nz) +
                                        " cells exceed the static scratch limit of " +
                                        std::to_string(RED_MAX_CELLS) + " cells");
+    const long long N = nxy * nz;
     if (!f || !out || (thermal && !g))
         return reject(LBM_ERR_ARG, "f, out (and g with a thermal lattice) are required");
     int dev = 0;
