@@ -439,14 +439,65 @@ def run_secondary(name, lbm_steps, reps, streaming="aa"):
     return out
 
 
-def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None):
+def run_moving_ib_secondary(name, lbm_steps, reps):
+    """The immersed-boundary channel with its samples replaced before every step from
+    device tensors (lbm_set_ib_samples_device: placement, radix sort by l-block and Morton
+    code, re-marking of the stencils, all on the device), against the same steps with the
+    samples left in place.  The positions of every step are prepared before the timed
+    region (a sphere translating by 0.01 cells per step)."""
+    import torch
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    w = cached_workload(name)
+    sim = Simulation(w)
+    sim.init_equilibrium(*upload(w, sim.device))
+    x0 = torch.from_numpy(w.ib_x).to(sim.device)
+    v = torch.tensor([0.01, 0.0, 0.0], device=sim.device)
+    X = torch.stack([x0 + k * v for k in range(lbm_steps)]).contiguous()
+    ub = torch.zeros_like(x0)
+    ub[:, 0] = 0.01
+    wt = torch.from_numpy(w.ib_w).to(sim.device)
+    sim.step(4)
+    torch.cuda.synchronize()
+
+    def timed(mode):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        sim.set_ib_samples_device(X[0], ub, wt, reorder=True)
+        a.record()
+        for _ in range(reps):
+            for k in range(lbm_steps):
+                if mode != "static":
+                    sim.set_ib_samples_device(X[k], ub, wt, reorder=(mode == "sort"))
+                sim.step(1)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * lbm_steps)
+
+    timed("sort")
+    static_ms, keep_ms, sort_ms = timed("static"), timed("keep"), timed("sort")
+    sim.close()
+    del sim
+    torch.cuda.empty_cache()
+    return {"workload": workload_label(name, w) + ", samples replaced every step",
+            "layout": "aa", "samples": int(len(w.ib_x)),
+            "ms_per_step_static": round(static_ms, 4),
+            "ms_per_step_moving": round(keep_ms, 4),
+            "ms_per_step_moving_resorted": round(sort_ms, 4),
+            "mlups": round(w.cells / (keep_ms / 1e3) / 1e6, 1),
+            "update_us": round((keep_ms - static_ms) * 1e3, 2),
+            "update_us_resorted": round((sort_ms - static_ms) * 1e3, 2),
+            "moving": "lbm_set_ib_samples_device before every step in the stored order of "
+                      "one sort (update_us), or sorted every step (update_us_resorted)"}
+
+
+def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None, overlap=False):
     """MLUPS of a workload run as ``nslabs`` slabs along its outer axis on this GPU, with
     the halo exchange after every step (a step = one step launch per slab + the exchange's
-    pack and unpack launches)."""
+    pack and unpack launches).  overlap: interior planes, boundary planes, and the exchange
+    on a second stream beside the next step's interior (two step launches per slab)."""
     import torch
     from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
     w = cached_workload(name)
-    dom = SlabDomain(w, nslabs)
+    dom = SlabDomain(w, nslabs, overlap=overlap)
     dom.init_equilibrium()
     dom.step(4)
     torch.cuda.synchronize()
@@ -466,6 +517,7 @@ def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None):
     out = {"workload": workload_label(name, w), "layout": "aa", "slabs": nslabs,
            "decomposition": "slabs along the outer axis, 1 ghost plane per inner face, "
                             "FILL after even / DRAIN after odd steps, all on this GPU",
+           "overlap": bool(overlap),
            "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
            "halo_launches_per_step": 4 * pairs}
     if single_mlups:
@@ -570,12 +622,15 @@ def run_gpu(args, dctx):
             # the 32^3 case fits in L2 and is launch-bound: long submissions replay graphs
             steps_n = 2048 if n == "taylor_green_32" else args.lbm_steps
             line["secondary"].append(run_secondary(n, steps_n, 4, mode))
+        line["secondary"].append(run_moving_ib_secondary("channel_ib_sphere_128",
+                                                         args.lbm_steps, 4))
         single = {r["workload"]: r["mlups"] for r in line["secondary"] if r["layout"] == "aa"}
         single[workload_label(args.workload, w)] = round(value, 1)
         for n in (args.workload, "cavity3d_512"):
             lbl = workload_label(n, cached_workload(n))
-            line["secondary"].append(run_slabs_secondary(n, 4, args.lbm_steps, 2,
-                                                         single.get(lbl)))
+            for overlap in (False, True):
+                line["secondary"].append(run_slabs_secondary(n, 4, args.lbm_steps, 2,
+                                                             single.get(lbl), overlap))
     line["cpu_baseline"] = cpu_baseline(args.workload)
     return line
 

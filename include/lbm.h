@@ -166,6 +166,8 @@ typedef struct {
                              1 + <u_a T> H / (kappa dT), <.> over fluid cells, H = cells
                              across, kappa = omega (1/s_T[1 + a] - 1/2), the flux counted
                              from the hot face towards the cold one                      */
+    int ib_dropped;       /* samples the last lbm_set_ib_samples_device dropped (invalid
+                             positions); 0 after lbm_set_ib_samples                         */
 } lbm_diag;
 
 /* Bytes of device workspace lbm_create() needs for this configuration (validates it). */
@@ -193,6 +195,23 @@ lbm_status lbm_init_equilibrium(lbm_ctx *ctx, const float *rho, const float *u, 
  * caller puts on the stream before or after lbm_step is therefore ordered as usual.  Grids
  * of at most 4 M cells replay captured graphs of 64 steps. */
 lbm_status lbm_step(lbm_ctx *ctx, int n);
+
+/* One time step split across calls by outer-axis planes (z in 3-D, y in 2-D): each call
+ * launches the current step (the same even or odd AA form lbm_step would launch) on the
+ * planes [lo, hi) only.  The step is complete, and the parity and step count advance, once
+ * the calls since the last complete step have covered every plane of [0, n_outer) exactly
+ * once, in any order and any grouping; a slab's ghost planes may be included, they are
+ * skipped.  The result is bit for bit that of lbm_step(1): even steps only touch their own
+ * cells, and in the odd step every slot is read and then written by one cell alone.
+ * This lets a slab driver overlap its halo exchange with the interior planes ([TLBM]
+ * Sec. 4, overlapping communication with computation; see the halo calls below).
+ * While a step is partly done, lbm_step, lbm_init_equilibrium, lbm_macroscopic,
+ * lbm_diagnostics, lbm_solid_force and the population calls return LBM_ERR_STATE; the halo
+ * calls are allowed.  Each call is one launch on the context's stream, not chained to
+ * the work before it.  Errors: LBM_ERR_ARG for an empty or out-of-range range or a plane
+ * already stepped in this step; LBM_ERR_UNSUPPORTED for the two-buffer layouts and for
+ * contexts with immersed-boundary capacity. */
+lbm_status lbm_step_planes(lbm_ctx *ctx, int lo, int hi);
 
 /* rho = sum f, u = (sum c f + F/2)/rho, T = sum g of the current state ([TLBM] Sec. 2).
  * Any of the three pointers may be NULL to skip that field. */
@@ -239,6 +258,26 @@ lbm_status lbm_get_link_mask(lbm_ctx *ctx, uint32_t *mask);
 lbm_status lbm_set_ib_samples(lbm_ctx *ctx, int n, const float *xyz, const float *ub,
                               const float *weight);
 
+/* The same replacement with the samples in device memory (or page-locked host memory),
+ * placed and ordered on the device: a body that moves every step updates its samples
+ * without a host round trip.  Nothing waits for the stream; the arrays must stay valid
+ * until the stream has run the call's kernels.
+ *   reorder != 0: sort the samples ([KFS] Sec. 4: l-blocks, Morton code inside a block; the
+ *     same order lbm_set_ib_samples gives) with a stable radix sort over (l-block, Morton)
+ *     keys -- one thread block for up to 16384 samples, a multi-block pass per 8-bit digit
+ *     beyond that -- and store the order;
+ *   reorder == 0: place caller sample perm[i] in slot i, perm being the stored order of the
+ *     last sort (of this call or of lbm_set_ib_samples), which must have had the same n
+ *     (LBM_ERR_STATE otherwise).  A rigid body whose samples keep their indices keeps the
+ *     locality of that sort while it moves, at the cost of one gather instead of a sort.
+ * Placement is checked on the device: periodic axes wrap, and a sample with a non-finite
+ * position or a stencil that would leave through a wall face is dropped -- it takes weight
+ * 0 and position 0, is left out of the torque's centroid, and is counted in
+ * lbm_diag.ib_dropped -- instead of failing the call.  Uses workspace that
+ * lbm_workspace_bytes reserves with ib_max_samples. */
+lbm_status lbm_set_ib_samples_device(lbm_ctx *ctx, int n, const float *xyz, const float *ub,
+                                     const float *weight, int reorder);
+
 /* Slab halos ([TLBM] Sec. 3: direction-selective exchange of contiguous buffers).  With
  * the AA pattern only odd steps read or write across a slab face, so a slab driver runs one
  * exchange after every lbm_step(1) of all its slabs:
@@ -258,6 +297,14 @@ lbm_status lbm_set_ib_samples(lbm_ctx *ctx, int n, const float *xyz, const float
  * FILL is allowed at parity 1, DRAIN at parity 0 after at least one step (LBM_ERR_STATE
  * otherwise).  HALO faces need the AA layout and no immersed-boundary capacity
  * (LBM_ERR_UNSUPPORTED at create).  Stream-ordered; nothing waits.
+ * Overlap with lbm_step_planes.  Call the planes next to a HALO face -- its ghost plane and
+ * the first owned plane -- the boundary planes, the others the interior.  A pack reads
+ * slots of the boundary planes (FILL: slots the even step wrote and the odd step leaves
+ * alone; DRAIN: ghost slots the odd step wrote), and an unpack writes slots that only the
+ * boundary planes' next step reads (FILL: ghost slots; DRAIN: slots the even step reads at
+ * the first owned plane).  So, with the halo calls on a second stream (lbm_set_stream),
+ * each step can run as: interior planes; wait for the previous exchange's unpack; boundary
+ * planes; then this step's exchange, which overlaps the next step's interior planes.
  * lbm_halo_bytes gives 0 for a context without HALO faces. */
 lbm_status lbm_halo_bytes(const lbm_ctx *ctx, size_t *bytes);
 lbm_status lbm_halo_pack(lbm_ctx *ctx, int side, int phase, void *buf);
@@ -276,7 +323,8 @@ lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);
  *      default stream): sum f, sum c_x f, sum c_y f, sum c_z f, sum g, and the number of
  *      cells whose sum f or sum g is not finite.  Nothing waits for the stream.
  *   f, g, out: device memory of the current device or page-locked host memory.
- * Limit: nx*ny*nz <= 2^28 (268435456) cells; larger grids are rejected with LBM_ERR_ARG.
+ * Limit: nx*ny*nz <= 2^28 (268435456) cells; larger grids are rejected with LBM_ERR_ARG,
+ * as are D2Q9 grids with nz != 1.
  * The reduction's scratch is one file-scope static device array of 2 MiB, which every
  * device that loads the library keeps until the process exits.  The first call on a
  * device looks up that array's device address (once per device, with the device

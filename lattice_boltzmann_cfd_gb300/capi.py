@@ -58,6 +58,7 @@ class lbm_diag(ctypes.Structure):
         ("finite", ctypes.c_int), ("ib_samples", ctypes.c_int),
         ("ib_force", ctypes.c_double * 3), ("ib_torque", ctypes.c_double * 3),
         ("uT", ctypes.c_double * 3), ("nu_volume", ctypes.c_double),
+        ("ib_dropped", ctypes.c_int),
     ]
 
 
@@ -70,6 +71,7 @@ SIGNATURES = [
                                   ctypes.POINTER(_VP)]),
     ("lbm_init_equilibrium", ctypes.c_int, [_VP, _VP, _VP, _VP]),
     ("lbm_step", ctypes.c_int, [_VP, ctypes.c_int]),
+    ("lbm_step_planes", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int]),
     ("lbm_macroscopic", ctypes.c_int, [_VP, _VP, _VP, _VP]),
     ("lbm_solid_force", ctypes.c_int, [_VP, _D]),
     ("lbm_diagnostics", ctypes.c_int, [_VP, ctypes.POINTER(lbm_diag)]),
@@ -77,6 +79,8 @@ SIGNATURES = [
     ("lbm_set_populations", ctypes.c_int, [_VP, _VP, _VP]),
     ("lbm_get_link_mask", ctypes.c_int, [_VP, _VP]),
     ("lbm_set_ib_samples", ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP, _VP]),
+    ("lbm_set_ib_samples_device", ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP, _VP,
+                                                  ctypes.c_int]),
     ("lbm_halo_bytes", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     ("lbm_halo_pack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_halo_unpack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP]),
@@ -171,6 +175,10 @@ def lbm_step(ctx, n: int):
     _check(load().lbm_step(ctx, int(n)), ctx)
 
 
+def lbm_step_planes(ctx, lo: int, hi: int):
+    _check(load().lbm_step_planes(ctx, int(lo), int(hi)), ctx)
+
+
 def lbm_macroscopic(ctx, rho=None, u=None, T=None):
     _check(load().lbm_macroscopic(ctx, _addr(rho), _addr(u), _addr(T)), ctx)
 
@@ -191,7 +199,7 @@ def lbm_diagnostics(ctx, allow_nonfinite: bool = False) -> dict:
             "fluid_cells": d.fluid_cells, "steps": d.steps, "finite": bool(d.finite),
             "ib_samples": d.ib_samples, "ib_force": list(d.ib_force),
             "ib_torque": list(d.ib_torque), "uT": list(d.uT), "nu_volume": d.nu_volume,
-            "status": st}
+            "ib_dropped": d.ib_dropped, "status": st}
 
 
 def lbm_get_populations(ctx, f, g=None):
@@ -215,6 +223,14 @@ def lbm_set_ib_samples(ctx, xyz, ub=None, weight=None):
     w = None if weight is None else np.ascontiguousarray(weight, dtype=np.float32).reshape(n)
     ptr = lambda a: None if a is None else a.ctypes.data
     _check(load().lbm_set_ib_samples(ctx, n, ptr(x), ptr(u), ptr(w)), ctx)
+
+
+def lbm_set_ib_samples_device(ctx, n: int, xyz, ub=None, weight=None, reorder=True):
+    """Immersed-boundary samples from device (or page-locked host) tensors: xyz (n, 3)
+    float32, ub (n, 3) or None, weight (n,) or None; sorted on the device (reorder) or
+    placed in the stored order of the last sort."""
+    _check(load().lbm_set_ib_samples_device(ctx, int(n), _addr(xyz), _addr(ub),
+                                            _addr(weight), int(bool(reorder))), ctx)
 
 
 def lbm_halo_bytes(ctx) -> int:

@@ -71,16 +71,24 @@ cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaSt
     return by_lattice(lattice, thermal, go);
 }
 
-cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
+cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, bool set,
                            cudaStream_t s)
 {
-    ib_clear_kernel<<<1024, 256, 0, s>>>(mask, cells);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || P.ib_n <= 0) return e;
+    int *box = const_cast<int *>(P.ib_box);
+    if (set) {   // an empty box: every entry very negative
+        cudaError_t e = cudaMemsetAsync(box, 0x80, 6 * sizeof(int), s);
+        if (e != cudaSuccess) return e;
+    }
+    if (P.ib_n <= 0) return cudaSuccess;
     const dim3 b(128), g((P.ib_n + 127) / 128);
-    if (lattice == 19) ib_mark_kernel<D3Q19><<<g, b, 0, s>>>(P, mask);
-    else if (lattice == 27) ib_mark_kernel<D3Q27><<<g, b, 0, s>>>(P, mask);
-    else ib_mark_kernel<D2Q9><<<g, b, 0, s>>>(P, mask);
+    auto go = [&](auto l) {
+        using L = decltype(l);
+        if (set) ib_mark_kernel<L, true><<<g, b, 0, s>>>(P, mask, box);
+        else ib_mark_kernel<L, false><<<g, b, 0, s>>>(P, mask, box);
+    };
+    if (lattice == 19) go(D3Q19{});
+    else if (lattice == 27) go(D3Q27{});
+    else go(D2Q9{});
     return cudaGetLastError();
 }
 

@@ -50,14 +50,16 @@ struct lbm_ctx {
     int parity = 0;
     long long steps = 0;
     bool initialized = false;
+    // lbm_step_planes: outer-axis planes already stepped in the current (unfinished) step
+    std::vector<uint8_t> planes_done;
+    int planes_left = 0;   // > 0 while a step is partly done
+    int ib_order_n = -1;   // sample count of the stored sample order, -1 = none
     std::string err;
     // CUDA graphs of GRAPH_STEPS steps, one per start parity, built on first use for
     // grids small enough that launch overhead matters; captured on a private stream.
     cudaGraphExec_t graph[2] = {nullptr, nullptr};
     cudaStream_t capture_stream = nullptr;
     bool graphs_disabled = false;
-    // immersed-boundary samples as stored on the device (sorted), for the torque
-    std::vector<float> ib_x;
     void drop_graphs()
     {
         for (auto &g : graph)
@@ -78,6 +80,14 @@ lbm_status fail(lbm_ctx *c, lbm_status s, const std::string &msg)
     if (c) c->err = msg;
     else g_error = msg;
     return s;
+}
+
+// Calls that need a whole time step behind them, made while lbm_step_planes has stepped
+// only some of the planes.
+lbm_status partly_stepped(lbm_ctx *c)
+{
+    return fail(c, LBM_ERR_STATE,
+                "a step is partly done: lbm_step_planes must cover the remaining planes first");
 }
 
 lbm_status cuda_fail(lbm_ctx *c, cudaError_t e, const char *where)
@@ -189,6 +199,7 @@ lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace
     lbm_setup::fill_params(c->cfg, c->L, c->ws, c->P);
     if (L.ib_cap > 0) {
         e = cudaMemsetAsync(c->P.fib, 0, 3 * L.S * sizeof(float), c->stream);
+
         if (e != cudaSuccess) {
             lbm_status r = cuda_fail(nullptr, e, "clearing the immersed-boundary force");
             delete c;
@@ -222,6 +233,7 @@ lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace
 lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, const float *T)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (c->planes_left) return partly_stepped(c);
     if (!rho || !u) return fail(c, LBM_ERR_ARG, "rho and u are required");
     if (c->L.QT && !T) return fail(c, LBM_ERR_ARG, "T is required with a thermal lattice");
     DeviceGuard guard(c->device);
@@ -297,6 +309,27 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
     return e;
 }
 
+// AA step kernel launch over the outer-axis planes [lo, hi) (lbm_step_planes).
+cudaError_t launch_planes(const lbm_ctx *c, const lbm::Params &P0, int parity, int lo, int hi,
+                          cudaStream_t stream, bool chained)
+{
+    const bool d2 = c->cfg.lattice == LBM_D2Q9;
+    lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
+    if (d2) sh.grid.y = (unsigned)((hi - lo + (int)sh.block.y - 1) / (int)sh.block.y);
+    else sh.grid.z = (unsigned)(hi - lo);
+    lbm::Params P = P0;
+    P.plane_lo = lo;
+    P.plane_hi = hi;
+    const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
+    const int th = c->cfg.thermal, coll = c->cfg.collision;
+    const int masked = !c->L.masked ? 0 : (c->L.ib_cap > 0 ? 2 : 1);
+    const bool odd = parity != 0;
+    if (c->cfg.lattice == LBM_D3Q27)
+        return lbm::launch_step_d3q27(masked, odd, narrow, P, sh, stream, chained);
+    return d2 ? lbm::launch_step_d2q9(th, coll, masked, odd, narrow, P, sh, stream, chained)
+              : lbm::launch_step_d3q19(th, coll, masked, odd, narrow, P, sh, stream, chained);
+}
+
 // The graph of GRAPH_STEPS steps starting at the context's parity (built on first use).
 // Returns nullptr (and stops trying) if capture is not possible.
 cudaGraphExec_t step_graph(lbm_ctx *c)
@@ -336,6 +369,7 @@ lbm_status lbm_step(lbm_ctx *c, int n)
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (n < 0) return fail(c, LBM_ERR_ARG, "n must be >= 0");
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    if (c->planes_left) return partly_stepped(c);
     DeviceGuard guard(c->device);
     // Small grids: replay a captured graph of GRAPH_STEPS steps (it leaves the parity and
     // the buffers as it found them), then launch the remainder one by one.
@@ -357,10 +391,46 @@ lbm_status lbm_step(lbm_ctx *c, int n)
     return LBM_OK;
 }
 
+lbm_status lbm_step_planes(lbm_ctx *c, int lo, int hi)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    if (c->L.streaming != LBM_STREAM_AA)
+        return fail(c, LBM_ERR_UNSUPPORTED, "lbm_step_planes needs the AA layout");
+    if (c->L.ib_cap > 0)
+        return fail(c, LBM_ERR_UNSUPPORTED,
+                    "lbm_step_planes takes no context with immersed-boundary capacity");
+    const bool d2 = c->cfg.lattice == LBM_D2Q9;
+    const int n_outer = d2 ? c->cfg.ny : c->cfg.nz;
+    if (lo < 0 || hi > n_outer || lo >= hi)
+        return fail(c, LBM_ERR_ARG, "planes [lo, hi) must be a non-empty range of [0, " +
+                                        std::to_string(n_outer) + ")");
+    if (!c->planes_left) {
+        c->planes_done.assign((size_t)n_outer, 0);
+        c->planes_left = n_outer;
+    }
+    for (int k = lo; k < hi; ++k)
+        if (c->planes_done[(size_t)k])
+            return fail(c, LBM_ERR_ARG, "plane " + std::to_string(k) +
+                                            " was already stepped in this step");
+    DeviceGuard guard(c->device);
+    // not chained: the launch may follow an event wait on another stream's halo work
+    cudaError_t e = launch_planes(c, c->P, c->parity, lo, hi, c->stream, false);
+    if (e != cudaSuccess) return cuda_fail(c, e, "step kernel (planes)");
+    for (int k = lo; k < hi; ++k) c->planes_done[(size_t)k] = 1;
+    c->planes_left -= hi - lo;
+    if (!c->planes_left) {
+        c->parity ^= 1;
+        ++c->steps;
+    }
+    return LBM_OK;
+}
+
 lbm_status lbm_macroscopic(lbm_ctx *c, float *rho, float *u, float *T)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
+    if (c->planes_left) return partly_stepped(c);
     DeviceGuard guard(c->device);
     void *dr = nullptr, *du = nullptr, *dT = nullptr;
     lbm_status s = LBM_OK;
@@ -378,6 +448,7 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (!out) return fail(c, LBM_ERR_ARG, "out is NULL");
+    if (c->planes_left) return partly_stepped(c);
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
     DeviceGuard guard(c->device);
     cudaError_t e = lbm::launch_diag(c->cfg.lattice, c->cfg.thermal, c->L.masked, pattern(c),
@@ -431,21 +502,36 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
     for (int a = 0; a < 3; ++a) out->uT[a] = r[15 + a];
     out->ib_samples = c->P.ib_n;
     if (c->P.ib_n > 0) {
-        // reaction force and torque of the last step's penalties (fp64 on the host)
-        const int n = c->P.ib_n;
+        // reaction force and torque of the last step's penalties (fp64 on the host), over
+        // the samples kept (dropped ones are ordered last)
         const size_t cap = c->L.ib_cap;
-        std::vector<float> gs(3 * cap);
-        e = cudaMemcpyAsync(gs.data(), c->P.ibg, sizeof(float) * gs.size(),
+        std::vector<float> xs(8 * cap), gs(3 * cap);   // x3 ub3 w kept; g3
+        unsigned dropped = 0;
+        e = cudaMemcpyAsync(xs.data(), c->P.ibx, sizeof(float) * xs.size(),
                             cudaMemcpyDeviceToHost, c->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(gs.data(), c->P.ibg, sizeof(float) * gs.size(),
+                                cudaMemcpyDeviceToHost, c->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(&dropped, lbm::ib_dropped_counter(c->P, c->ws + c->L.off_ibsort),
+                                sizeof(unsigned), cudaMemcpyDeviceToHost, c->stream);
         if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
         if (e != cudaSuccess) return cuda_fail(c, e, "immersed-boundary read-back");
-        double centre[3] = {0, 0, 0};
-        for (int s = 0; s < n; ++s)
-            for (int a = 0; a < 3; ++a) centre[a] += (double)c->ib_x[3 * s + a] / n;
+        out->ib_dropped = (int)dropped;
+        // centroid of the kept samples (plane 7 flags them); dropped ones exert no force
+        const int n = c->P.ib_n;
+        double centre[3] = {0, 0, 0}, kept = 0.0;
         for (int s = 0; s < n; ++s) {
+            if (xs[7 * cap + s] == 0.0f) continue;
+            kept += 1.0;
+            for (int a = 0; a < 3; ++a) centre[a] += (double)xs[a * cap + s];
+        }
+        for (int a = 0; a < 3; ++a) centre[a] = kept > 0 ? centre[a] / kept : 0.0;
+        for (int s = 0; s < n; ++s) {
+            if (xs[7 * cap + s] == 0.0f) continue;
             const double g[3] = {gs[s], gs[cap + s], gs[2 * cap + s]};
-            const double r[3] = {c->ib_x[3 * s] - centre[0], c->ib_x[3 * s + 1] - centre[1],
-                                 c->ib_x[3 * s + 2] - centre[2]};
+            const double r[3] = {xs[s] - centre[0], xs[cap + s] - centre[1],
+                                 xs[2 * cap + s] - centre[2]};
             for (int a = 0; a < 3; ++a) out->ib_force[a] -= g[a];
             out->ib_torque[0] -= r[1] * g[2] - r[2] * g[1];
             out->ib_torque[1] -= r[2] * g[0] - r[0] * g[2];
@@ -470,6 +556,7 @@ lbm_status lbm_solid_force(lbm_ctx *c, double F_out[3])
 static lbm_status populations(lbm_ctx *c, float *f, float *g, bool set)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (c->planes_left) return partly_stepped(c);
     if (!f) return fail(c, LBM_ERR_ARG, "f is NULL");
     if (c->L.QT && !g && set) return fail(c, LBM_ERR_ARG, "g is required with a thermal lattice");
     if (!set && !c->initialized) return fail(c, LBM_ERR_STATE, "no state to read");
@@ -516,21 +603,6 @@ lbm_status lbm_get_link_mask(lbm_ctx *c, uint32_t *mask)
     return LBM_OK;
 }
 
-namespace {
-
-// Spread the low 10 bits of v to every third bit (Morton interleave).
-uint32_t spread3(uint32_t v)
-{
-    v &= 0x3ffu;
-    v = (v | (v << 16)) & 0x030000ffu;
-    v = (v | (v << 8)) & 0x0300f00fu;
-    v = (v | (v << 4)) & 0x030c30c3u;
-    v = (v | (v << 2)) & 0x09249249u;
-    return v;
-}
-
-}  // namespace
-
 lbm_status lbm_set_ib_samples(lbm_ctx *c, int n, const float *xyz, const float *ub,
                               const float *weight)
 {
@@ -545,58 +617,100 @@ lbm_status lbm_set_ib_samples(lbm_ctx *c, int n, const float *xyz, const float *
     const int l = c->cfg.ib_block > 0 ? c->cfg.ib_block : 4;
     // positions: wrap periodic axes, check wall axes
     std::vector<float> x(3 * (size_t)n);
-    for (int s = 0; s < n; ++s)
-        for (int a = 0; a < 3; ++a) {
-            float v = (a < dim) ? xyz[3 * s + a] : 0.0f;
-            if (!std::isfinite(v)) return fail(c, LBM_ERR_ARG, "non-finite sample position");
-            if (a < dim && !c->P.face_wall[2 * a]) {
-                v = std::fmod(v, (float)ext[a]);
-                if (v < 0.0f) v += (float)ext[a];
-                if (v >= (float)ext[a]) v = 0.0f;
-            } else if (a < dim && !(v >= 0.0f && v < (float)(ext[a] - 1))) {
-                return fail(c, LBM_ERR_ARG,
-                            "sample " + std::to_string(s) +
-                                ": its stencil would leave the domain through a wall face");
-            }
-            x[3 * s + a] = v;
+    for (int s = 0; s < n; ++s) {
+        float v[3];
+        if (!lbm::ib_place(c->P, dim, xyz + 3 * s, v)) {
+            for (int a = 0; a < dim; ++a)
+                if (!std::isfinite(xyz[3 * s + a]))
+                    return fail(c, LBM_ERR_ARG, "non-finite sample position");
+            return fail(c, LBM_ERR_ARG,
+                        "sample " + std::to_string(s) +
+                            ": its stencil would leave the domain through a wall face");
         }
+        for (int a = 0; a < 3; ++a) x[3 * s + a] = v[a];
+    }
     // order: l x l x l blocks in x-y-z order, Morton code of the position inside a block
     const long long nbx = (ext[0] + l - 1) / l, nby = (ext[1] + l - 1) / l;
     std::vector<std::pair<unsigned long long, int>> key(n);
     for (int s = 0; s < n; ++s) {
-        long long b[3] = {0, 0, 0};
-        uint32_t m = 0;
-        for (int a = 0; a < dim; ++a) {
-            const float v = x[3 * s + a];
-            b[a] = (long long)(v / l);
-            const float in = v - (float)(b[a] * l);
-            m |= spread3((uint32_t)std::min(1023.0f, in * (1024.0f / l))) << a;
-        }
-        const unsigned long long block = b[0] + nbx * (b[1] + nby * b[2]);
-        key[s] = {(block << 30) | m, s};
+        const float v[3] = {x[3 * s], x[3 * s + 1], x[3 * s + 2]};
+        key[s] = {lbm::ib_sort_key(v, dim, l, nbx, nby), s};
     }
     std::stable_sort(key.begin(), key.end());
     const size_t cap = c->L.ib_cap;
-    std::vector<float> host(10 * cap, 0.0f);   // planes: x, y, z, ub x3, w, g x3
-    c->ib_x.assign(3 * (size_t)n, 0.0f);
+    std::vector<float> host(8 * cap, 0.0f);   // planes: x, y, z, ub x3, w, kept
+    std::vector<int> perm(std::max(n, 1));
     for (int i = 0; i < n; ++i) {
         const int s = key[i].second;
+        perm[i] = s;
         for (int a = 0; a < 3; ++a) {
             host[a * cap + i] = x[3 * s + a];
             host[(3 + a) * cap + i] = (ub && a < dim) ? ub[3 * s + a] : 0.0f;
-            c->ib_x[3 * i + a] = x[3 * s + a];
         }
         host[6 * cap + i] = weight ? weight[s] : 1.0f;
+        host[7 * cap + i] = 1.0f;
     }
-    cudaError_t e = cudaMemcpyAsync(const_cast<float *>(c->P.ibx), host.data(),
-                                    sizeof(float) * host.size(), cudaMemcpyHostToDevice,
-                                    c->stream);
+    uint32_t *mask = const_cast<uint32_t *>(c->P.mask);
+    void *scratch = c->ws + c->L.off_ibsort;
+    // clear the current samples' stencil marks before their positions are overwritten
+    cudaError_t e = lbm::launch_ib_mark(c->cfg.lattice, c->P, mask, false, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "clearing the samples' stencils");
+    e = cudaMemcpyAsync(const_cast<float *>(c->P.ibx), host.data(), sizeof(float) * host.size(),
+                        cudaMemcpyHostToDevice, c->stream);
+    // the order, for lbm_set_ib_samples_device calls that keep it
+    if (e == cudaSuccess && n > 0)
+        e = cudaMemcpyAsync(lbm::ib_order_perm(c->P, scratch), perm.data(), sizeof(int) * n,
+                            cudaMemcpyHostToDevice, c->stream);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(lbm::ib_dropped_counter(c->P, scratch), 0, sizeof(unsigned),
+                            c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);   // host buffer lifetime
     if (e != cudaSuccess) return cuda_fail(c, e, "copy of the samples");
+    c->ib_order_n = n;
     c->P.ib_n = n;
     c->drop_graphs();   // captured steps hold the sample count
-    e = lbm::launch_ib_mark(c->cfg.lattice, c->P, const_cast<uint32_t *>(c->P.mask), c->L.N,
+    e = lbm::launch_ib_mark(c->cfg.lattice, c->P, mask, true, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "marking the samples' stencils");
+    return LBM_OK;
+}
+
+lbm_status lbm_set_ib_samples_device(lbm_ctx *c, int n, const float *xyz, const float *ub,
+                                     const float *weight, int reorder)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (c->L.ib_cap <= 0) return fail(c, LBM_ERR_STATE, "created with ib_max_samples = 0");
+    if (n < 0 || n > c->L.ib_cap)
+        return fail(c, LBM_ERR_ARG, "n must lie in [0, ib_max_samples]");
+    if (n > 0 && !xyz) return fail(c, LBM_ERR_ARG, "xyz is required");
+    if (!reorder && n != c->ib_order_n)
+        return fail(c, LBM_ERR_STATE,
+                    "no stored sample order for " + std::to_string(n) +
+                        " samples: order them first (reorder != 0 or lbm_set_ib_samples)");
+    DeviceGuard guard(c->device);
+    void *dx = nullptr, *du = nullptr, *dw = nullptr;
+    lbm_status st = LBM_OK;
+    if (n > 0) st = device_address(c, xyz, "xyz", &dx);
+    if (st == LBM_OK && n > 0 && ub) st = device_address(c, ub, "ub", &du);
+    if (st == LBM_OK && n > 0 && weight) st = device_address(c, weight, "weight", &dw);
+    if (st != LBM_OK) return st;
+    const int l = c->cfg.ib_block > 0 ? c->cfg.ib_block : 4;
+    uint32_t *mask = const_cast<uint32_t *>(c->P.mask);
+    void *scratch = c->ws + c->L.off_ibsort;
+    cudaError_t e = lbm::launch_ib_mark(c->cfg.lattice, c->P, mask, false, c->stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "clearing the samples' stencils");
+    if (n > 0) {
+        e = lbm::launch_ib_order(c->cfg.lattice, c->P, n, l, static_cast<const float *>(dx),
+                                 static_cast<const float *>(du), static_cast<const float *>(dw),
+                                 scratch, reorder != 0, c->stream);
+    } else {
+        e = cudaMemsetAsync(lbm::ib_dropped_counter(c->P, scratch), 0, sizeof(unsigned),
                             c->stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "ordering the samples");
+    c->ib_order_n = n;
+    if (c->P.ib_n != n) c->drop_graphs();   // captured steps hold the sample count
+    c->P.ib_n = n;
+    e = lbm::launch_ib_mark(c->cfg.lattice, c->P, mask, true, c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "marking the samples' stencils");
     return LBM_OK;
 }

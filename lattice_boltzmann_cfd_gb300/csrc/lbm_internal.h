@@ -62,8 +62,9 @@ constexpr int DIAG_BLOCKS = 2048;   // capacity of the partial-sum rows (one res
 // Each returns the launch error (cudaGetLastError) of what it enqueued.
 // narrow: every population index fits in 32 bits (see slot()).  masked: 0 = no link
 // mask, 1 = link mask, 2 = link mask and immersed-boundary forces.  The AA step kernels of
-// form 1 compute the mask from the coordinates outside the solid cells' box (boxed_mask);
-// the two-buffer kernels load it.
+// forms 1 and 2 compute the mask from the coordinates outside the box of the solid cells
+// (form 2: and of the samples' stencil cells) and load it inside (boxed_mask); the
+// two-buffer kernels load it.
 // chained: see launch_step_kernel.
 cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
                               const Params &P, const Shape &sh, cudaStream_t s, bool chained);
@@ -95,8 +96,36 @@ cudaError_t launch_pop(int lattice, int thermal, bool masked, int pat, bool set,
 // IB_BIT marking of the samples' stencil cells.
 cudaError_t launch_ib(int lattice, int thermal, int pat, const Params &P, cudaStream_t s,
                       bool chained);
-cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, long long cells,
+// set: IB_BIT on the stencil cells of P's samples; otherwise cleared there.
+cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, bool set,
                            cudaStream_t s);
+// Device ordering of n caller samples (device addresses; ub, w may be null) into P's sample
+// planes by l-block and Morton code (lbm_ib_order.cu); scratch: ib_order_scratch_bytes(cap)
+// bytes, 256-byte aligned.  The number of dropped samples lands in ib_dropped_counter.
+// Scratch of the device ordering: keys[2][cap] (64-bit), indices[2][cap], digit counts
+// [256][tiles], the order of the last sort (perm[cap]: slot i holds caller sample perm[i]),
+// and the dropped-sample count.
+constexpr int IB_SORT_TILE = 2048;   // keys per block of the multi-block sort
+inline size_t ib_sort_tiles(int cap) { return ((size_t)cap + IB_SORT_TILE - 1) / IB_SORT_TILE; }
+inline size_t ib_order_scratch_bytes(int cap)
+{
+    return 2 * (size_t)cap * 8 + 3 * (size_t)cap * 4 + 256 * ib_sort_tiles(cap) * 4 + 256;
+}
+inline int *ib_order_perm(const Params &P, void *scratch)
+{
+    const size_t cap = (size_t)P.ib_cap;
+    return reinterpret_cast<int *>(static_cast<char *>(scratch) + 2 * cap * 8 + 2 * cap * 4 +
+                                   256 * ib_sort_tiles(P.ib_cap) * 4);
+}
+inline unsigned *ib_dropped_counter(const Params &P, void *scratch)
+{
+    return reinterpret_cast<unsigned *>(ib_order_perm(P, scratch) + P.ib_cap);
+}
+// reorder: sort the samples (and keep the order in perm); otherwise place them in the order
+// of the last sort (perm), which must have had the same n.
+cudaError_t launch_ib_order(int lattice, const Params &P, int n, int l, const float *xyz,
+                            const float *ub, const float *w, void *scratch, bool reorder,
+                            cudaStream_t s);
 // Slab halo pack (unpack = 0) or unpack (unpack = 1) of one side and phase.
 cudaError_t launch_halo(int lattice, int thermal, const Params &P, int side, int phase,
                         int unpack, float *buf, cudaStream_t s);

@@ -28,6 +28,7 @@
 // slots), then a second kernel pulls into the other buffer, so the stored state is the
 // natural pre-collision one (304 B per D3Q19 update instead of 152).
 #pragma once
+#include <climits>
 #include <cstddef>
 #include <cstdint>
 
@@ -47,6 +48,9 @@ struct Params {
     int face_wall[6];      // per face: 1 = wall (flow)
     int face_halo[6];      // per face: 1 = halo face of a slab (ghost plane, no wrap)
     int ghost_lo, ghost_hi;  // outer-axis coordinate of a slab's ghost planes, -1 = none
+    // outer-axis planes (z in 3-D, y in 2-D) the AA step kernels cover: [plane_lo,
+    // plane_hi); the whole axis except in launches of lbm_step_planes
+    int plane_lo, plane_hi;
     int box_lo[3], box_hi[3];  // solid cells' box widened by one (inclusive; empty: lo > hi)
     int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
     float T_wall[6];
@@ -56,6 +60,9 @@ struct Params {
     const float *ibx, *ibub, *ibw;
     float *ibg;
     int ib_n, ib_cap;
+    // bounding box of the samples' stencil cells, kept on the device by the marking kernel:
+    // {-lo_x, -lo_y, -lo_z, hi_x, hi_y, hi_z} (all very negative when there is no sample)
+    const int *ib_box;
 };
 
 // Neighbour offsets with periodic wrap by compare and add.
@@ -253,14 +260,20 @@ LBM_HD uint32_t face_mask(const Params &P, int x, int y, int z)
     return m;
 }
 
-// The link mask of a cell for the AA step kernels without an immersed boundary: loaded
-// inside the box around the solid cells, the face bits elsewhere (no cell outside the box is
-// solid or has a link into a solid cell).
-template <class L, class TL>
+// The link mask of a cell for the AA step kernels: loaded inside the box around the solid
+// cells, the face bits elsewhere (no cell outside the box is solid or has a link into a
+// solid cell).  IB: also loaded inside the box around the immersed-boundary samples'
+// stencil cells (the only cells with IB_BIT).
+template <class L, class TL, bool IB = false>
 LBM_HD uint32_t boxed_mask(const Params &P, int idx, int x, int y, int z)
 {
-    const bool inside = x >= P.box_lo[0] && x <= P.box_hi[0] && y >= P.box_lo[1] &&
-                        y <= P.box_hi[1] && z >= P.box_lo[2] && z <= P.box_hi[2];
+    bool inside = x >= P.box_lo[0] && x <= P.box_hi[0] && y >= P.box_lo[1] &&
+                  y <= P.box_hi[1] && z >= P.box_lo[2] && z <= P.box_hi[2];
+    if constexpr (IB) {
+        const int *b = P.ib_box;
+        inside = inside || (x >= -b[0] && y >= -b[1] && z >= -b[2] && x <= b[3] && y <= b[4] &&
+                            z <= b[5]);
+    }
     return inside ? P.mask[idx] : face_mask<L, TL>(P, x, y, z);
 }
 
@@ -442,19 +455,20 @@ LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
 // the kernel; a separate one in the host emulation of the tests).
 // IB: the context has immersed-boundary samples (cells with IB_BIT take a per-cell force);
 // kernels without it carry no trace of that path.
-// FACES (with MASKED, without IB): the mask comes from the coordinates (face_mask) outside
-// the solid cells' box and is loaded only inside it (boxed_mask).
+// FACES (with MASKED): the mask comes from the coordinates (face_mask) outside the box of
+// the solid cells (and, with IB, of the samples' stencil cells) and is loaded only inside
+// it (boxed_mask).
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB = false,
           bool FACES = false>
 LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
 {
-    static_assert(!FACES || (MASKED && !IB), "FACES is a masked form without IB");
+    static_assert(!FACES || MASKED, "FACES is a masked form");
     if ((!MASKED || FACES) && ghost_plane<L>(Pr, y, z)) return;
     const int idx = x + Pr.nx * (y + Pr.ny * z);
     // The mask load and the population loads are issued together: the populations are
     // loaded as if no link were a wall (except the x-face wall links, known from x), and
     // the remaining wall links are fixed once the mask is in.
-    const uint32_t m = FACES ? boxed_mask<L, TL>(Pr, idx, x, y, z) : MASKED ? Pr.mask[idx] : 0u;
+    const uint32_t m = FACES ? boxed_mask<L, TL, IB>(Pr, idx, x, y, z) : MASKED ? Pr.mask[idx] : 0u;
     float f[L::Q], g[TL::QA];
     // wall links through an x face need no mask: they are redirected at once
     const uint32_t xw = (MASKED && ODD) ? x_wall_links<L>(Pr, x) : 0u;
@@ -500,6 +514,26 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     }
 }
 
+// Cell of the calling thread in an AA step launch over the outer-axis planes
+// [P.plane_lo, P.plane_hi): the launch grid covers those planes only, offset by plane_lo.
+// Returns false for threads past the grid's edge.
+template <class L>
+LBM_HD bool step_cell_coords(const Params &P, int &x, int &y, int &z)
+{
+#if defined(__CUDA_ARCH__)
+    x = blockIdx.x * blockDim.x + threadIdx.x;
+    y = blockIdx.y * blockDim.y + threadIdx.y;
+    z = blockIdx.z;
+#endif
+    if constexpr (L::DIM == 3) {
+        z += P.plane_lo;
+        return x < P.nx && y < P.ny;
+    } else {
+        y += P.plane_lo;
+        return x < P.nx && y < P.plane_hi;
+    }
+}
+
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB,
           bool FACES = false>
@@ -507,10 +541,8 @@ __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
     allow_dependents();
     wait_prerequisites();   // every load reads the previous step's stores
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
-    if (x >= P.nx || y >= P.ny) return;
+    int x = 0, y = 0, z = 0;
+    if (!step_cell_coords<L>(P, x, y, z)) return;
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
@@ -522,10 +554,8 @@ __global__ void __launch_bounds__(256, 5) step_kernel_5(const Params P)
 {
     allow_dependents();
     wait_prerequisites();   // every load reads the previous step's stores
-    const int x = blockIdx.x * blockDim.x + threadIdx.x;
-    const int y = blockIdx.y * blockDim.y + threadIdx.y;
-    const int z = blockIdx.z;
-    if (x >= P.nx || y >= P.ny) return;
+    int x = 0, y = 0, z = 0;
+    if (!step_cell_coords<L>(P, x, y, z)) return;
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
@@ -638,12 +668,14 @@ __global__ void __launch_bounds__(256) stream_kernel(const Params P)
 // K, and K rho, K u with rho and u = (j + F_body/2)/rho of the logical state (read with
 // pattern PAT).  A solid stencil cell counts as rho = 1, u = 0.  Sample positions were
 // checked on the host: stencils never leave through a wall face.
-template <class L, class TL, int PAT>
-LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float (&Ku)[3])
+// The cell (returned) of corner c of sample s's stencil and its weight K; q receives its
+// coordinates.
+template <class L>
+LBM_HD int ib_corner_cell(const Params &P, int s, int c, float &K, int (&q)[3])
 {
     const int dim = L::DIM;
     const int n[3] = {P.nx, P.ny, P.nz};
-    int q[3] = {0, 0, 0};
+    q[0] = q[1] = q[2] = 0;
     float k = 1.0f;
     for (int a = 0; a < dim; ++a) {
         const float xa = P.ibx[a * P.ib_cap + s];
@@ -654,11 +686,16 @@ LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float
         if (q[a] >= n[a]) q[a] -= n[a];
         k *= d ? fr : 1.0f - fr;
     }
-    const int idx = q[0] + P.nx * (q[1] + P.ny * q[2]);
     K = k;
-    // the populations load as if no link were a wall, together with the mask (one memory
-    // round trip instead of two); wall links are fixed once the mask is in
-    const uint32_t m = P.mask ? P.mask[idx] : 0u;
+    return q[0] + P.nx * (q[1] + P.ny * q[2]);
+}
+
+// K rho and K u of the corner cell idx (coordinates q, link mask m) of weight k.
+template <class L, class TL, int PAT>
+LBM_HD void ib_corner_moments(const Params &P, int idx, const int (&q)[3], float k, uint32_t m,
+                              float &Krho, float (&Ku)[3])
+{
+    // the populations load as if no link were a wall; wall links are fixed after
     Offs o{};
     if (PAT != NATURAL) o = make_offs(q[0], q[1], q[2], P);
     float f[L::Q], g[TL::QA];
@@ -666,7 +703,7 @@ LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float
     if (m & SOLID_BIT) {
         Krho = k;
         Ku[0] = Ku[1] = Ku[2] = 0.0f;
-        return idx;
+        return;
     }
     if constexpr (PAT != NATURAL) {
         if (m & wall_bits<L>()) fix_wall_loads<L, TL, PAT, false>(P, idx, m, f, g);
@@ -688,7 +725,75 @@ LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float
     Ku[0] = k * ux;
     Ku[1] = k * uy;
     Ku[2] = k * uz;
+}
+
+template <class L, class TL, int PAT>
+LBM_HD int ib_corner(const Params &P, int s, int c, float &K, float &Krho, float (&Ku)[3])
+{
+    int q[3];
+    const int idx = ib_corner_cell<L>(P, s, c, K, q);
+    ib_corner_moments<L, TL, PAT>(P, idx, q, K, P.mask ? P.mask[idx] : 0u, Krho, Ku);
     return idx;
+}
+
+// Sample order ("GPU Optimization for High-Quality Kinetic Fluid Simulation", Sec. 4,
+// Fig. 7): samples sorted by the l x l x l block of the grid they lie in (blocks in x-y-z
+// order), then by the Morton code of their position inside the block (8 bits per axis),
+// so that the samples one warp handles touch nearby cells.
+constexpr int IB_MORTON_BITS = 24;
+
+// Spread the low 8 bits of v to every third bit (Morton interleave).
+LBM_HD uint32_t spread3(uint32_t v)
+{
+    v &= 0xffu;
+    v = (v | (v << 8)) & 0x0000f00fu;
+    v = (v | (v << 4)) & 0x000c30c3u;
+    v = (v | (v << 2)) & 0x00249249u;
+    return v;
+}
+
+// Sort key of a sample at (wrapped, checked) position x: (block index << 24) | Morton code.
+// nbx, nby: blocks along x and y.  The host and the device compute it with the same fp32
+// operations, so both order samples identically.
+LBM_HD unsigned long long ib_sort_key(const float (&x)[3], int dim, int l, long long nbx,
+                                      long long nby)
+{
+    long long b[3] = {0, 0, 0};
+    uint32_t m = 0;
+    for (int a = 0; a < dim; ++a) {
+        const float v = x[a];
+        b[a] = (long long)(v / (float)l);
+        const float in = v - (float)(b[a] * l);
+        float t = in * (256.0f / (float)l);
+        t = t < 255.0f ? t : 255.0f;
+        m |= spread3(t > 0.0f ? (uint32_t)t : 0u) << a;
+    }
+    const unsigned long long block = (unsigned long long)(b[0] + nbx * (b[1] + nby * b[2]));
+    return (block << IB_MORTON_BITS) | m;
+}
+
+// Position of a sample given in cells: periodic axes wrap into [0, n); on a wall axis the
+// stencil (base and base + 1) must stay inside, i.e. 0 <= x < n - 1.  Returns false for a
+// non-finite position or a stencil that would leave through a wall face.
+LBM_HD bool ib_place(const Params &P, int dim, const float *in, float (&x)[3])
+{
+    const int ext[3] = {P.nx, P.ny, P.nz};
+    bool ok = true;
+    for (int a = 0; a < 3; ++a) {
+        float v = a < dim ? in[a] : 0.0f;
+        if (!(fabsf(v) <= 3.402823466e38f)) {   // NaN or infinite
+            ok = false;
+            v = 0.0f;
+        } else if (a < dim && !P.face_wall[2 * a]) {
+            v = fmodf(v, (float)ext[a]);
+            if (v < 0.0f) v += (float)ext[a];
+            if (v >= (float)ext[a]) v = 0.0f;
+        } else if (a < dim && !(v >= 0.0f && v < (float)(ext[a] - 1))) {
+            ok = false;
+        }
+        x[a] = v;
+    }
+    return ok;
 }
 
 // Penalty from a sample's weight w, boundary velocity u_b and interpolated rho and u:
@@ -727,25 +832,31 @@ LBM_HD int ib_sample(const Params &P, int s, int (&node)[8], float (&K)[8], floa
 // One thread per stencil corner (2^dim threads per sample, adjacent lanes): each loads its
 // cell, the group sums K rho and K u with shuffles, every thread forms the penalty and
 // spreads its share K g into its cell with atomic additions (cells are shared between
-// samples); corner 0 keeps the penalty for the diagnostics.
+// samples); corner 0 keeps the penalty for the diagnostics.  t: the corner's thread index
+// over all samples; whole warps call this (the shuffles span 2^dim lanes).  Waits for the
+// prerequisite grid (wait_prerequisites) before it reads any population.
 template <class L, class TL, int PAT>
-__global__ void __launch_bounds__(128) ib_kernel(const Params P)
+LBM_HD void ib_corner_thread(const Params &P, int t)
 {
-    allow_dependents();
-    wait_prerequisites();   // the stencil cells hold the previous step's stores
     constexpr int CORNERS = 1 << L::DIM;
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
     const int s = t / CORNERS, c = t % CORNERS;
     const bool active = s < P.ib_n;
     float K = 0.0f, kr = 0.0f, ku[3] = {0.0f, 0.0f, 0.0f};
     float w = 0.0f, ub[3] = {0.0f, 0.0f, 0.0f};
-    int idx = 0;
+    int idx = 0, q[3] = {0, 0, 0};
+    uint32_t m = 0;
+    // The samples and the link mask are written only by the context's set-up and
+    // sample-setting calls, which finish before the step before this kernel: read them,
+    // and place the stencil, while that step is still running.
     if (active) {
-        // the sample's own data first, so that its loads overlap the cell's
         w = P.ibw[s];
         for (int a = 0; a < 3; ++a) ub[a] = P.ibub[a * P.ib_cap + s];
-        idx = ib_corner<L, TL, PAT>(P, s, c, K, kr, ku);
+        idx = ib_corner_cell<L>(P, s, c, K, q);
+        m = P.mask[idx];
     }
+    wait_prerequisites();   // the stencil cells hold the previous step's stores
+    if (active) ib_corner_moments<L, TL, PAT>(P, idx, q, K, m, kr, ku);
+#if defined(__CUDA_ARCH__)
 #pragma unroll
     for (int off = 1; off < CORNERS; off <<= 1) {
         kr += __shfl_xor_sync(0xffffffffu, kr, off, CORNERS);
@@ -756,36 +867,55 @@ __global__ void __launch_bounds__(128) ib_kernel(const Params P)
     ib_penalty<L>(w, ub, kr, ku, gs);
     if (c == 0)
         for (int a = 0; a < 3; ++a) P.ibg[a * P.ib_cap + s] = gs[a];
-    if (P.mask[idx] & SOLID_BIT) return;
+    if (m & SOLID_BIT) return;
     for (int a = 0; a < L::DIM; ++a)
         atomicAdd(P.fib + ((size_t)a * P.S + (unsigned)idx), K * gs[a]);
+#endif
 }
 
-// Mark the stencil cells of every sample with IB_BIT (after ib_clear_kernel).
-template <class L>
-__global__ void ib_mark_kernel(const Params P, uint32_t *mask)
+template <class L, class TL, int PAT>
+__global__ void __launch_bounds__(128) ib_kernel(const Params P)
+{
+    allow_dependents();
+    ib_corner_thread<L, TL, PAT>(P, blockIdx.x * blockDim.x + threadIdx.x);
+}
+
+// Set (SET) or clear IB_BIT on the stencil cells of every sample of P: clearing the
+// current samples' stencils before new samples replace them, then setting the new ones',
+// keeps IB_BIT on exactly the stencil cells of the current samples.
+// SET also grows box (the layout of Params::ib_box, reset beforehand) to cover the
+// stencil cells: the step kernels load the mask inside it.
+template <class L, bool SET>
+__global__ void ib_mark_kernel(const Params P, uint32_t *mask, int *box)
 {
     const int s = blockIdx.x * blockDim.x + threadIdx.x;
-    if (s >= P.ib_n) return;
     const int dim = L::DIM;
     const int n[3] = {P.nx, P.ny, P.nz};
-    int base[3] = {0, 0, 0};
-    for (int a = 0; a < dim; ++a) base[a] = (int)floorf(P.ibx[a * P.ib_cap + s]);
-    for (int c = 0; c < (1 << dim); ++c) {
-        int q[3] = {base[0], base[1], base[2]};
-        for (int a = 0; a < dim; ++a) {
-            q[a] += (c >> a) & 1;
-            if (q[a] >= n[a]) q[a] -= n[a];
+    int ext[6] = {INT_MIN, INT_MIN, INT_MIN, INT_MIN, INT_MIN, INT_MIN};   // -lo, hi
+    if (s < P.ib_n) {
+        int base[3] = {0, 0, 0};
+        for (int a = 0; a < dim; ++a) base[a] = (int)floorf(P.ibx[a * P.ib_cap + s]);
+        for (int c = 0; c < (1 << dim); ++c) {
+            int q[3] = {base[0], base[1], base[2]};
+            for (int a = 0; a < dim; ++a) {
+                q[a] += (c >> a) & 1;
+                if (q[a] >= n[a]) q[a] -= n[a];
+            }
+            for (int a = 0; a < 3; ++a) {
+                ext[a] = max(ext[a], -q[a]);
+                ext[3 + a] = max(ext[3 + a], q[a]);
+            }
+            uint32_t *m = mask + (q[0] + P.nx * (q[1] + P.ny * q[2]));
+            if (SET) atomicOr(m, IB_BIT);
+            else atomicAnd(m, ~IB_BIT);
         }
-        atomicOr(mask + (q[0] + P.nx * (q[1] + P.ny * q[2])), IB_BIT);
     }
-}
-
-static __global__ void ib_clear_kernel(uint32_t *mask, long long N)
-{
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < N;
-         i += (long long)gridDim.x * blockDim.x)
-        mask[i] &= ~IB_BIT;
+    if (!SET) return;
+    for (int k = 0; k < 6; ++k) {
+        int v = ext[k];
+        for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
+        if ((threadIdx.x & 31) == 0 && v != INT_MIN) atomicMax(box + k, v);
+    }
 }
 
 // ------------------------------------------------------------ auxiliary kernels -------

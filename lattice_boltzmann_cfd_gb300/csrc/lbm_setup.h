@@ -38,7 +38,8 @@ struct Layout {
     int streaming = LBM_STREAM_AA;
     bool halo = false;
     size_t off_f = 0, off_g = 0, off_f2 = 0, off_g2 = 0, off_mask = 0, off_solid = 0;
-    size_t off_partial = 0, off_result = 0, off_fib = 0, off_ib = 0;
+    size_t off_partial = 0, off_result = 0, off_fib = 0, off_ib = 0, off_ibsort = 0;
+    size_t off_ibbox = 0;
     int ib_cap = 0;
     size_t bytes = 0;
 };
@@ -204,7 +205,11 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     if (L->ib_cap > 0) {
         off = align_up(off + 3 * L->S * sizeof(float));   // per-cell force
         L->off_ib = off;
-        off = align_up(off + (size_t)10 * L->ib_cap * sizeof(float));   // x3 ub3 w g3
+        off = align_up(off + (size_t)11 * L->ib_cap * sizeof(float));   // x3 ub3 w kept g3
+        L->off_ibsort = off;   // device ordering of samples (lbm_set_ib_samples_device)
+        off = align_up(off + lbm::ib_order_scratch_bytes(L->ib_cap));
+        L->off_ibbox = off;    // box of the samples' stencil cells (6 ints)
+        off = align_up(off + 6 * sizeof(int));
     }
     L->off_partial = off;
     off = align_up(off + (size_t)lbm::DIAG_BLOCKS * lbm::DIAG_N * sizeof(double));
@@ -225,7 +230,8 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
     P.ibx = ib;
     P.ibub = ib ? ib + 3 * (size_t)L.ib_cap : nullptr;
     P.ibw = ib ? ib + 6 * (size_t)L.ib_cap : nullptr;
-    P.ibg = ib ? ib + 7 * (size_t)L.ib_cap : nullptr;
+    P.ibg = ib ? ib + 8 * (size_t)L.ib_cap : nullptr;   // plane 7: 1 = kept, 0 = dropped
+    P.ib_box = L.ib_cap ? reinterpret_cast<const int *>(ws + L.off_ibbox) : nullptr;
     const bool two = L.streaming != LBM_STREAM_AA;
     P.fo = two ? reinterpret_cast<float *>(ws + L.off_f2) : nullptr;
     P.go = (two && L.QT) ? reinterpret_cast<float *>(ws + L.off_g2) : nullptr;
@@ -277,6 +283,8 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
     }
     P.ghost_lo = P.face_halo[2 * outer] ? 0 : -1;
     P.ghost_hi = P.face_halo[2 * outer + 1] ? n_outer - 1 : -1;
+    P.plane_lo = 0;
+    P.plane_hi = n_outer;
     // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)
     const double omega = (g.thermal == LBM_D2Q5) ? (4.0 + g.a_T) / 10.0 : (6.0 + g.a_T) / 21.0;
     for (int k = 0; k < 7; ++k) P.abbT[k] = 0.0f;

@@ -14,7 +14,8 @@ cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s, bool chained)
 using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t, bool);
 
 // masked: 0 = no mask; 1 = mask, computed from the coordinates outside the solid cells'
-// box and loaded inside it; 2 = mask (loaded) and immersed-boundary forces
+// box and loaded inside it; 2 = the same with the box of the immersed-boundary samples'
+// stencil cells included, and immersed-boundary forces
 template <class TL, bool N>
 cudaError_t dispatch_n(int coll, int masked, bool odd, const Params &P, const Shape &sh,
                        cudaStream_t s, bool chained)
@@ -22,10 +23,10 @@ cudaError_t dispatch_n(int coll, int masked, bool odd, const Params &P, const Sh
     static const Fn table[2][3][2] = {
         {{go<TL, 0, false, false, N, false>, go<TL, 0, false, true, N, false>},
          {go<TL, 0, true, false, N, false, true>, go<TL, 0, true, true, N, false, true>},
-         {go<TL, 0, true, false, N, true>, go<TL, 0, true, true, N, true>}},
+         {go<TL, 0, true, false, N, true, true>, go<TL, 0, true, true, N, true, true>}},
         {{go<TL, 1, false, false, N, false>, go<TL, 1, false, true, N, false>},
          {go<TL, 1, true, false, N, false, true>, go<TL, 1, true, true, N, false, true>},
-         {go<TL, 1, true, false, N, true>, go<TL, 1, true, true, N, true>}}};
+         {go<TL, 1, true, false, N, true, true>, go<TL, 1, true, true, N, true, true>}}};
     return table[coll ? 1 : 0][masked][odd ? 1 : 0](P, sh, s, chained);
 }
 

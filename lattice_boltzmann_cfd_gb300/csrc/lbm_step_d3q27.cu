@@ -23,14 +23,15 @@ cudaError_t go(const Params &P, const Shape &sh, cudaStream_t s, bool chained)
 using Fn = cudaError_t (*)(const Params &, const Shape &, cudaStream_t, bool);
 
 // masked: 0 = no mask; 1 = mask, computed from the coordinates outside the solid cells'
-// box and loaded inside it; 2 = mask (loaded) and immersed-boundary forces
+// box and loaded inside it; 2 = the same with the box of the immersed-boundary samples'
+// stencil cells included, and immersed-boundary forces
 template <bool N>
 cudaError_t dispatch_n(int masked, bool odd, const Params &P, const Shape &sh, cudaStream_t s,
                        bool chained)
 {
     static const Fn table[3][2] = {{go<false, false, N, false>, go<false, true, N, false>},
                                    {go<true, false, N, false, true>, go<true, true, N, false, true>},
-                                   {go<true, false, N, true>, go<true, true, N, true>}};
+                                   {go<true, false, N, true, true>, go<true, true, N, true, true>}};
     return table[masked][odd ? 1 : 0](P, sh, s, chained);
 }
 

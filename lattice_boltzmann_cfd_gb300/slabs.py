@@ -19,6 +19,18 @@ bit.
 Two drivers share the slicing: SlabDomain holds every slab in one process (on one device or
 several); DistSlabDomain is one slab per torch.distributed rank, its buffers moved by
 point-to-point messages (ring_exchange).
+
+Overlap ("Multi-GPU thermal lattice Boltzmann simulations using OpenACC and MPI", Sec. 4:
+the boundary layers first, then the exchange beside the interior update).  With
+``overlap=True`` each step runs through lbm_step_planes as: the interior planes; a wait for
+the previous step's exchange; the boundary planes (the ghost plane and the first owned
+plane at each HALO face); then this step's exchange on a second stream, where it runs beside
+the next step's interior planes.  A pack reads only slots the interior update leaves alone,
+and an unpack writes only slots that the boundary planes' next step reads first, so the
+result is bit for bit that of the plain order.  The host never waits for the device, except
+where the messages themselves go through the host (page-locked buffers over a CPU back-end
+such as gloo): there the host waits for the pack alone, after the next interior launch is
+queued.
 """
 from __future__ import annotations
 
@@ -75,31 +87,38 @@ def slab_part(w, nslabs: int, r: int):
     return local, (low, high), planes
 
 
-def ring_exchange(rank: int, world: int, periodic: bool, phase: int, pack, unpack, send,
-                  recv, group=None, sync=None):
-    """One halo exchange of slab ``rank`` with its neighbours over torch.distributed.
+def plane_groups(n: int, low: bool, high: bool):
+    """(interior, boundary) lists of [lo, hi) outer-axis plane ranges of a slab with ``n``
+    local planes and ghost planes at the low / high end when ``low`` / ``high``.  The
+    boundary ranges are the ghost plane and the first owned plane of each HALO face; the
+    interior is what lies between.  A slab too thin for an interior is all boundary."""
+    lo_b = 2 if low else 0
+    hi_b = n - 2 if high else n
+    if hi_b <= lo_b:
+        return [], [(0, n)]
+    boundary = ([(0, lo_b)] if low else []) + ([(hi_b, n)] if high else [])
+    return [(lo_b, hi_b)], boundary
 
-    pack(side, phase, buf) fills send[side]; unpack(side, phase, buf) consumes a buffer;
-    sync(), if given, runs after the packs and again after the receives (to order device
-    work around the messages).
+
+def ring_neighbours(rank: int, world: int, periodic: bool):
+    """(low, high) neighbour ranks of slab ``rank`` (None at the end of a walled axis)."""
+    lo_nb = rank - 1 if rank > 0 else (world - 1 if periodic else None)
+    hi_nb = rank + 1 if rank < world - 1 else (0 if periodic else None)
+    return lo_nb, hi_nb
+
+
+def ring_messages(rank: int, world: int, periodic: bool, send, recv, group=None):
+    """Move packed buffers between neighbours; returns [(side, buffer to unpack there)].
+
     My side-s buffer goes to the neighbour's opposite side.  Messages carry as tag the side
     they land on, and are posted in one fixed order (sends of sides 0, 1; receives of the
     neighbours' side 0, then side 1), so that back-ends which match point-to-point messages
-    by order (NCCL) pair them right even when both neighbours are the same rank."""
-    import torch.distributed as dist
-    lo_nb = rank - 1 if rank > 0 else (world - 1 if periodic else None)
-    hi_nb = rank + 1 if rank < world - 1 else (0 if periodic else None)
-    nbs = (lo_nb, hi_nb)
-    for side in (0, 1):
-        if nbs[side] is not None:
-            pack(side, phase, send[side])
-    if sync is not None:
-        sync()
+    by order (NCCL) pair them right even when both neighbours are the same rank.  A ring of
+    one slab unpacks its own buffers, crossed."""
+    nbs = ring_neighbours(rank, world, periodic)
     if world == 1:
-        if periodic:     # a ring of one slab: its own buffers, crossed
-            unpack(0, phase, send[1])
-            unpack(1, phase, send[0])
-        return
+        return [(0, send[1]), (1, send[0])] if periodic else []
+    import torch.distributed as dist
     ops = []
     for side in (0, 1):
         if nbs[side] is not None:
@@ -112,19 +131,42 @@ def ring_exchange(rank: int, world: int, periodic: bool, phase: int, pack, unpac
     if ops:
         for req in dist.batch_isend_irecv(ops):
             req.wait()
-    if sync is not None:
-        sync()
+    return [(side, recv[side]) for side in (0, 1) if nbs[side] is not None]
+
+
+def ring_exchange(rank: int, world: int, periodic: bool, phase: int, pack, unpack, send,
+                  recv, group=None, sync=None):
+    """One halo exchange of slab ``rank`` with its neighbours over torch.distributed.
+
+    pack(side, phase, buf) fills send[side]; unpack(side, phase, buf) consumes a buffer;
+    sync(), if given, runs after the packs and again after the receives (to order device
+    work around the messages).
+    My side-s buffer goes to the neighbour's opposite side.  Messages carry as tag the side
+    they land on, and are posted in one fixed order (sends of sides 0, 1; receives of the
+    neighbours' side 0, then side 1), so that back-ends which match point-to-point messages
+    by order (NCCL) pair them right even when both neighbours are the same rank."""
+    nbs = ring_neighbours(rank, world, periodic)
     for side in (0, 1):
         if nbs[side] is not None:
-            unpack(side, phase, recv[side])
+            pack(side, phase, send[side])
+    if sync is not None:
+        sync()
+    arrived = ring_messages(rank, world, periodic, send, recv, group)
+    if sync is not None and world > 1:
+        sync()
+    for side, buf in arrived:
+        unpack(side, phase, buf)
 
 
 class SlabDomain:
     """The workload ``w`` split into ``nslabs`` slabs along its outer axis, slab r on
     ``devices[r % len(devices)]``.  The outer axis must be periodic (the slabs form a ring)
-    or have WALL faces (the end slabs keep them)."""
+    or have WALL faces (the end slabs keep them).
 
-    def __init__(self, w, nslabs: int, devices=None):
+    ``overlap``: run each step as interior planes, then boundary planes, with the exchange
+    on a second stream beside the next step's interior (one device only)."""
+
+    def __init__(self, w, nslabs: int, devices=None, overlap: bool = False):
         import torch
         self.w = w
         self.dim = w.dim
@@ -133,6 +175,7 @@ class SlabDomain:
         self.periodic = w.face_flow[2 * self.axis] == "periodic"
         devices = list(devices) if devices else [torch.device("cuda")]
         self.slabs, self.sides, self.plane_lists, self.buffers = [], [], [], []
+        self.groups = []
         for r in range(nslabs):
             local, sides, planes = slab_part(w, nslabs, r)
             sim = Simulation(local, device=devices[r % len(devices)])
@@ -140,9 +183,18 @@ class SlabDomain:
             self.slabs.append(sim)
             self.sides.append(sides)
             self.plane_lists.append(planes)
+            self.groups.append(plane_groups(len(planes), *sides))
             self.buffers.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
                                  for _ in range(2)])   # [low side, high side]
         self.multi_device = len({s.device for s in self.slabs}) > 1
+        self.overlap = bool(overlap)
+        if self.overlap and self.multi_device:
+            raise ValueError("overlap needs every slab on one device")
+        dev = self.slabs[0].device
+        # the contexts' stream (torch's current stream at creation) and the exchange stream
+        self.main = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(dev) if self.overlap else None
+        self._pending = None    # event: the last exchange's unpacks are queued before it
 
     def _take(self, a, planes, lead=0):
         if a is None:
@@ -176,6 +228,24 @@ class SlabDomain:
             capi.lbm_halo_unpack(self.slabs[b].ctx, 0, phase, to_b)
         self._sync()
 
+    def _exchange_on_side(self, phase: int):
+        """This step's exchange on the side stream, after the boundary planes on the main
+        stream; leaves an event the next boundary planes wait for."""
+        self.side.wait_stream(self.main)
+        for sim in self.slabs:
+            sim.set_stream(self.side)
+        try:
+            self._exchange(phase)
+        finally:
+            for sim in self.slabs:
+                sim.set_stream(self.main)
+        self._pending = self.side.record_event()
+
+    def _wait_pending(self):
+        if self._pending is not None:
+            self.main.wait_event(self._pending)
+            self._pending = None
+
     @property
     def parity(self) -> int:
         return self.slabs[0].parity
@@ -190,11 +260,24 @@ class SlabDomain:
             sim.init_equilibrium(dev(self.w.rho0), dev(self.w.u0, 1), dev(self.w.T_init))
 
     def step(self, n: int = 1):
-        """n time steps, each followed by its exchange (FILL after even, DRAIN after odd)."""
+        """n time steps, each followed by its exchange (FILL after even, DRAIN after odd).
+        Returns with every exchange ordered before later work on the main stream."""
         for _ in range(n):
-            for sim in self.slabs:
-                sim.step(1)
-            self._exchange(capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN)
+            if not self.overlap:
+                for sim in self.slabs:
+                    sim.step(1)
+                self._exchange(capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN)
+                continue
+            for sim, (interior, _) in zip(self.slabs, self.groups):
+                for lo, hi in interior:
+                    sim.step_planes(lo, hi)
+            self._wait_pending()
+            for sim, (_, boundary) in zip(self.slabs, self.groups):
+                for lo, hi in boundary:
+                    sim.step_planes(lo, hi)
+            self._exchange_on_side(capi.LBM_HALO_FILL if self.parity == 1
+                                   else capi.LBM_HALO_DRAIN)
+        self._wait_pending()
 
     def _owned(self, t, r, lead=0):
         low, high = self.sides[r]
@@ -246,23 +329,44 @@ class SlabDomain:
 
 class DistSlabDomain:
     """Slab ``rank`` of ``w`` split into ``world`` slabs, one per torch.distributed rank
-    (one process per GPU).  Every step is followed by ring_exchange of its halos (FILL after
-    even, DRAIN after odd steps), so between steps the owned planes hold what one undivided
-    domain would hold."""
+    (one process per GPU).  Every step is followed by the exchange of its halos with the
+    neighbouring ranks (FILL after even, DRAIN after odd steps), so between steps the owned
+    planes hold what one undivided domain would hold.
 
-    def __init__(self, w, rank: int, world: int, device=None, group=None):
+    ``transport``: "device" keeps the halo buffers in device memory and hands them to the
+    process group on the exchange stream (a GPU back-end such as NCCL: the exchange is
+    ordered by streams and the host does not wait); "host" keeps them in page-locked host
+    memory, which the halo kernels write and read directly, for a CPU back-end such as gloo
+    (the host waits for the pack before sending).
+    ``overlap``: interior planes, boundary planes, then the exchange beside the next step's
+    interior (see the module notes); otherwise each step is followed by its exchange."""
+
+    def __init__(self, w, rank: int, world: int, device=None, group=None,
+                 transport: str = "device", overlap: bool = False):
         import torch
+        if transport not in ("device", "host"):
+            raise ValueError("transport must be 'device' or 'host'")
         self.w, self.rank, self.world, self.group = w, rank, world, group
+        self.transport, self.overlap = transport, bool(overlap)
         self.axis, self.np_axis = outer_axis(w)
         self.periodic = w.face_flow[2 * self.axis] == "periodic"
         self.range = split_ranges(w.shape[self.axis], world)[rank]
         local, self.sides, self.planes = slab_part(w, world, rank)
         self.local = local
-        self.sim = Simulation(local, device=device)
+        dev = torch.device(device if device is not None else "cuda")
+        self.main = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(dev)
+        self.sim = Simulation(local, device=dev, stream=self.main)
+        self.interior, self.boundary = plane_groups(len(self.planes), *self.sides)
         nfloat = capi.lbm_halo_bytes(self.sim.ctx) // 4
-        new = lambda: torch.empty(nfloat, dtype=torch.float32, device=self.sim.device)
+        if transport == "host":
+            new = lambda: torch.empty(nfloat, dtype=torch.float32).pin_memory()
+        else:
+            new = lambda: torch.empty(nfloat, dtype=torch.float32, device=dev)
         self.send = [new(), new()]
         self.recv = [new(), new()]
+        self._packed = None     # (event after the packs, phase) awaiting its messages
+        self._pending = None    # event: the unpacks of the last exchange are queued before it
 
     @property
     def parity(self) -> int:
@@ -274,26 +378,71 @@ class DistSlabDomain:
         self.sim.init_equilibrium(dev(self.local.rho0), dev(self.local.u0),
                                   dev(self.local.T_init))
 
-    # The halo kernels run on the context's stream, which need not be torch's current
-    # stream (the one communication back-ends order against): the device is synchronised
-    # after the packs and before the unpacks.
     def _pack(self, side, phase, buf):
         capi.lbm_halo_pack(self.sim.ctx, side, phase, buf)
 
     def _unpack(self, side, phase, buf):
         capi.lbm_halo_unpack(self.sim.ctx, side, phase, buf)
 
-    def _sync(self):
+    def _start_exchange(self):
+        """Queue this step's packs on the exchange stream behind the step's last planes;
+        with device buffers, the messages and the unpacks too."""
         import torch
-        if self.sim.device.type == "cuda":
-            torch.cuda.synchronize(self.sim.device)
+        phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
+        nbs = ring_neighbours(self.rank, self.world, self.periodic)
+        self.side.wait_stream(self.main)
+        self.sim.set_stream(self.side)
+        try:
+            for side in (0, 1):
+                if nbs[side] is not None:
+                    self._pack(side, phase, self.send[side])
+            if self.transport == "host":
+                self._packed = (self.side.record_event(), phase)
+                return
+            with torch.cuda.stream(self.side):
+                arrived = ring_messages(self.rank, self.world, self.periodic, self.send,
+                                        self.recv, self.group)
+            for side, buf in arrived:
+                self._unpack(side, phase, buf)
+        finally:
+            self.sim.set_stream(self.main)
+        self._pending = self.side.record_event()
+
+    def _finish_exchange(self):
+        """Complete the exchange in flight (host transport: wait for the packs, move the
+        messages, queue the unpacks) and order it before later work on the main stream."""
+        if self._packed is not None:
+            event, phase = self._packed
+            self._packed = None
+            event.synchronize()
+            arrived = ring_messages(self.rank, self.world, self.periodic, self.send,
+                                    self.recv, self.group)
+            self.sim.set_stream(self.side)
+            try:
+                for side, buf in arrived:
+                    self._unpack(side, phase, buf)
+            finally:
+                self.sim.set_stream(self.main)
+            self._pending = self.side.record_event()
+        if self._pending is not None:
+            self.main.wait_event(self._pending)
+            self._pending = None
 
     def step(self, n: int = 1):
+        """n time steps with their exchanges; returns with the last exchange done (its
+        unpacks ordered before later work on the main stream)."""
         for _ in range(n):
-            self.sim.step(1)
-            phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
-            ring_exchange(self.rank, self.world, self.periodic, phase, self._pack,
-                          self._unpack, self.send, self.recv, self.group, sync=self._sync)
+            if self.overlap:
+                for lo, hi in self.interior:
+                    self.sim.step_planes(lo, hi)
+                self._finish_exchange()
+                for lo, hi in self.boundary:
+                    self.sim.step_planes(lo, hi)
+            else:
+                self._finish_exchange()
+                self.sim.step(1)
+            self._start_exchange()
+        self._finish_exchange()
 
     def owned(self, t, lead=0):
         """The owned planes of a local field (ghost planes dropped)."""

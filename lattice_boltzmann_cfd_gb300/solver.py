@@ -116,6 +116,10 @@ class Simulation:
     def step(self, n: int = 1):
         capi.lbm_step(self.ctx, n)
 
+    def step_planes(self, lo: int, hi: int):
+        """The current step on outer-axis planes [lo, hi) only (see lbm_step_planes)."""
+        capi.lbm_step_planes(self.ctx, lo, hi)
+
     def macroscopic(self, rho=None, u=None, T=None):
         import torch
         rho = rho if rho is not None else torch.empty(self.grid, device=self.device)
@@ -143,6 +147,12 @@ class Simulation:
 
     def set_ib_samples(self, xyz, ub=None, weight=None):
         capi.lbm_set_ib_samples(self.ctx, xyz, ub, weight)
+
+    def set_ib_samples_device(self, xyz, ub=None, weight=None, reorder=True):
+        """Samples as device tensors (float32, xyz and ub (n, 3), weight (n,)), sorted on
+        the device (reorder) or placed in the order of the last sort; nothing waits for the
+        stream."""
+        capi.lbm_set_ib_samples_device(self.ctx, int(xyz.shape[0]), xyz, ub, weight, reorder)
 
     def diagnostics(self, allow_nonfinite: bool = False) -> dict:
         return capi.lbm_diagnostics(self.ctx, allow_nonfinite)

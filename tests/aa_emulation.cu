@@ -40,13 +40,14 @@ bool guards_intact(const std::vector<float> &v)
 
 // F: the mask computed from the coordinates outside the solid cells' box (boxed_mask), as
 // the kernels do without an immersed boundary.
-template <class L, class TL, int C, bool M, bool O, bool NARROW, bool F = false>
+// I: the immersed-boundary form (cells with IB_BIT take the per-cell force).
+template <class L, class TL, int C, bool M, bool O, bool NARROW, bool F, bool I>
 void step_all(const Params &Pr, const Params &Pw)
 {
     for (int z = 0; z < Pr.nz; ++z)
         for (int y = 0; y < Pr.ny; ++y)
             for (int x = 0; x < Pr.nx; ++x)
-                aa_step_cell<L, TL, C, M, O, NARROW, M && !F, F>(Pr, Pw, x, y, z);
+                aa_step_cell<L, TL, C, M, O, NARROW, I, F>(Pr, Pw, x, y, z);
 }
 
 // Two-buffer PULL step: pull from P.f, collide, natural store into W.
@@ -177,9 +178,13 @@ struct Domain {
                 planes[(3 + a) * cap + s] = ib_ub ? ib_ub[3 * s + a] : 0.0f;
             }
             planes[6 * cap + s] = ib_w ? ib_w[s] : 1.0f;
+            planes[7 * cap + s] = 1.0f;   // kept
         }
         P.ib_n = ib_n;
         const int n[3] = {cfg.nx, cfg.ny, cfg.nz};
+        // the box of the stencil cells, as the marking kernel keeps it: {-lo, hi}
+        int *box = const_cast<int *>(P.ib_box);
+        for (int k = 0; k < 6; ++k) box[k] = std::numeric_limits<int>::min();
         for (int s = 0; s < ib_n; ++s) {
             int base[3] = {0, 0, 0};
             for (int a = 0; a < L::DIM; ++a) base[a] = (int)floorf(P.ibx[a * cap + s]);
@@ -190,8 +195,20 @@ struct Domain {
                     if (q[a] >= n[a]) q[a] -= n[a];
                 }
                 mask[q[0] + cfg.nx * (q[1] + cfg.ny * q[2])] |= IB_BIT;
+                for (int a = 0; a < 3; ++a) {
+                    box[a] = std::max(box[a], -q[a]);
+                    box[3 + a] = std::max(box[3 + a], q[a]);
+                }
             }
         }
+        // the mask the kernels compute must equal the built one at every cell
+        for (int z = 0; z < cfg.nz; ++z)
+            for (int y = 0; y < cfg.ny; ++y)
+                for (int x = 0; x < cfg.nx; ++x) {
+                    const int idx = x + cfg.nx * (y + cfg.ny * z);
+                    if (boxed_mask<L, TL, true>(P, idx, x, y, z) != mask[idx])
+                        ++face_mask_mismatches;
+                }
     }
 
     void init(const float *rho, const float *u, const float *T)
@@ -227,15 +244,22 @@ struct Domain {
         } else if (mode == LBM_STREAM_SPLIT) {
             if (Lay.masked) split_all<L, TL, C, true, NARROW>(P, wf, wg);
             else split_all<L, TL, C, false, NARROW>(P, wf, wg);
-        } else if (Lay.masked && Lay.ib_cap == 0 && !g_loaded_mask) {
-            if (parity) step_all<L, TL, C, true, true, NARROW, true>(P, Pw);
-            else step_all<L, TL, C, true, false, NARROW, true>(P, Pw);
+        } else if (Lay.masked && !g_loaded_mask) {
+            // the kernels' form: the mask from the coordinates outside the box of the solid
+            // cells and of the samples' stencil cells
+            if (Lay.ib_cap > 0) {
+                if (parity) step_all<L, TL, C, true, true, NARROW, true, true>(P, Pw);
+                else step_all<L, TL, C, true, false, NARROW, true, true>(P, Pw);
+            } else {
+                if (parity) step_all<L, TL, C, true, true, NARROW, true, false>(P, Pw);
+                else step_all<L, TL, C, true, false, NARROW, true, false>(P, Pw);
+            }
         } else if (Lay.masked) {
-            if (parity) step_all<L, TL, C, true, true, NARROW>(P, Pw);
-            else step_all<L, TL, C, true, false, NARROW>(P, Pw);
+            if (parity) step_all<L, TL, C, true, true, NARROW, false, true>(P, Pw);
+            else step_all<L, TL, C, true, false, NARROW, false, true>(P, Pw);
         } else {
-            if (parity) step_all<L, TL, C, false, true, NARROW>(P, Pw);
-            else step_all<L, TL, C, false, false, NARROW>(P, Pw);
+            if (parity) step_all<L, TL, C, false, true, NARROW, false, false>(P, Pw);
+            else step_all<L, TL, C, false, false, NARROW, false, false>(P, Pw);
         }
         for (const auto *v : {&f, &fn, &g, &gn})
             if (!guards_intact(*v)) ++guard_violations;
@@ -276,7 +300,8 @@ int run(const lbm_config &cfg, const lbm_setup::Layout &Lay, const float *rho, c
 {
     Domain<L, TL, C, NARROW> d(cfg, Lay);
     if (d.face_mask_mismatches) return -30;
-    if (ib_n > 0) d.set_ib(ib_n, ib_x, ib_ub, ib_w);
+    if (Lay.ib_cap > 0) d.set_ib(ib_n, ib_x, ib_ub, ib_w);
+    if (d.face_mask_mismatches) return -32;
     d.init(rho, u, T);
     for (int s = 0; s < steps; ++s) d.step();
     if (d.guard_violations) return -31;
@@ -470,6 +495,119 @@ long long race_any(const lbm_config &cfg, const lbm_setup::Layout &Lay, bool odd
                : race_violations<L, TL, C, true, false, false>(d);
 }
 
+// Overlap of a slab's halo exchange with the next step's interior planes (the slab driver's
+// overlapped order): the exchange after a step -- FILL before an odd step, DRAIN before an
+// even one -- runs beside the next step's launch over the outer-axis planes [ilo, ihi).
+// Brute force on a tiny grid: the pack's read set (each slot holds its own index; the
+// buffer shows which were read), the unpack's write set (a sentinel buffer), and, for every
+// interior cell of the next step, its write set (stepped alone into a NaN-filled buffer) and
+// which of the pack's and unpack's slots it reads (each such slot poisoned in turn).  The
+// overlap is race-free when no interior cell reads or writes a slot the pack reads or the
+// unpack writes.  Returns the number of such (cell, slot) pairs.
+template <class L, class TL, int C, bool M, bool F, bool O>
+long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
+{
+    const float nan = std::numeric_limits<float>::quiet_NaN();
+    const int phase = O ? LBM_HALO_FILL : LBM_HALO_DRAIN;
+    const int outer = L::DIM - 1;
+    const int plane_cells = L::DIM == 3 ? d.cfg.nx * d.cfg.ny : d.cfg.nx;
+    const int ndir = L::Q == 27 ? 9 : (L::Q == 19 ? 5 : 3) + (TL::Q ? 1 : 0);
+    std::vector<float> buf((size_t)ndir * plane_cells);
+    // slots: f slot s as s, g slot s as -1 - s (indices into the vectors, guards included)
+    std::vector<long long> touched;
+    const std::vector<float> f0 = d.f, g0 = d.g;
+    for (int side = 0; side < 2; ++side) {
+        if (d.cfg.face_flow[2 * outer + side] != LBM_FACE_HALO) continue;
+        for (size_t i = 0; i < d.f.size(); ++i) d.f[i] = (float)i;
+        for (size_t i = 0; i < d.g.size(); ++i) d.g[i] = -1.0f - (float)i;
+        std::fill(buf.begin(), buf.end(), nan);
+        d.halo(side, phase, 0, buf.data());
+        for (float v : buf)
+            if (!std::isnan(v)) touched.push_back((long long)v);
+        d.f = f0;
+        d.g = g0;
+        d.point();
+        const float mark = 1.0e30f;
+        std::fill(buf.begin(), buf.end(), mark);
+        for (auto *v : {&d.f, &d.g}) std::fill(v->begin(), v->end(), 0.0f);
+        d.halo(side, phase, 1, buf.data());
+        for (size_t i = 0; i < d.f.size(); ++i)
+            if (d.f[i] == mark) touched.push_back((long long)i);
+        for (size_t i = 0; i < d.g.size(); ++i)
+            if (d.g[i] == mark) touched.push_back(-1 - (long long)i);
+        d.f = f0;
+        d.g = g0;
+        d.point();
+    }
+    std::sort(touched.begin(), touched.end());
+    touched.erase(std::unique(touched.begin(), touched.end()), touched.end());
+    if (touched.empty()) return -50;   // nothing exchanged: the check would be vacuous
+    std::vector<float> wf(d.f.size()), wg(d.g.size());
+    Params Pw = d.P;
+    Pw.f = wf.data() + GUARD;
+    Pw.g = d.Lay.QT ? wg.data() + GUARD : nullptr;
+    auto step_cell = [&](int x, int y, int z) {
+        std::fill(wf.begin(), wf.end(), nan);
+        std::fill(wg.begin(), wg.end(), nan);
+        aa_step_cell<L, TL, C, M, O, true, M && !F, F>(d.P, Pw, x, y, z);
+    };
+    auto slot_ref = [&](std::vector<float> &fv, std::vector<float> &gv, long long t) -> float & {
+        return t >= 0 ? fv[(size_t)t] : gv[(size_t)(-1 - t)];
+    };
+    long long bad = 0;
+    for (int z = 0; z < d.cfg.nz; ++z)
+        for (int y = 0; y < d.cfg.ny; ++y)
+            for (int x = 0; x < d.cfg.nx; ++x) {
+                const int c = L::DIM == 3 ? z : y;
+                if (c < ilo || c >= ihi) continue;
+                step_cell(x, y, z);
+                std::vector<size_t> Wf, Wg;
+                for (size_t i = 0; i < wf.size(); ++i)
+                    if (!std::isnan(wf[i])) Wf.push_back(i);
+                for (size_t i = 0; i < wg.size(); ++i)
+                    if (!std::isnan(wg[i]) && d.Lay.QT) Wg.push_back(i);
+                for (long long t : touched) {
+                    if (!std::isnan(slot_ref(wf, wg, t))) {   // written by the cell
+                        ++bad;
+                        continue;
+                    }
+                    float &st = slot_ref(d.f, d.g, t);
+                    const float keep = st;
+                    st = nan;
+                    step_cell(x, y, z);
+                    st = keep;
+                    bool read = false;
+                    for (size_t i : Wf) read = read || std::isnan(wf[i]);
+                    for (size_t i : Wg) read = read || std::isnan(wg[i]);
+                    if (read) ++bad;
+                }
+            }
+    return bad;
+}
+
+template <class L, class TL, int C>
+long long overlap_any(const lbm_config &cfg, const lbm_setup::Layout &Lay, bool next_odd,
+                      int ilo, int ihi)
+{
+    Domain<L, TL, C, true> d(cfg, Lay);
+    if (d.face_mask_mismatches) return -30;
+    const size_t N = (size_t)Lay.N;
+    std::vector<float> rho(N), u(3 * N), T(N);
+    for (size_t i = 0; i < N; ++i) {
+        rho[i] = 1.0f + 1e-3f * (float)(i % 7);
+        for (int a = 0; a < 3; ++a) u[a * N + i] = 0.01f * (float)((i + 3 * a) % 5) - 0.02f;
+        T[i] = 0.05f * (float)(i % 3);
+    }
+    d.init(rho.data(), u.data(), T.data());
+    const bool M = Lay.masked, F = Lay.masked && Lay.ib_cap == 0;
+    if (!M) return next_odd ? overlap_pairs<L, TL, C, false, false, true>(d, ilo, ihi)
+                            : overlap_pairs<L, TL, C, false, false, false>(d, ilo, ihi);
+    if (F) return next_odd ? overlap_pairs<L, TL, C, true, true, true>(d, ilo, ihi)
+                           : overlap_pairs<L, TL, C, true, true, false>(d, ilo, ihi);
+    return next_odd ? overlap_pairs<L, TL, C, true, false, true>(d, ilo, ihi)
+                    : overlap_pairs<L, TL, C, true, false, false>(d, ilo, ihi);
+}
+
 }  // namespace
 
 // Violations of race-freedom of one AA step (even: odd = 0) on a tiny grid, see
@@ -589,4 +727,30 @@ extern "C" long long emu_count_bad_indices(int lattice, int nx, int ny, int nz)
                 }
             }
     return bad;
+}
+
+// (cell, slot) pairs by which the next step's launch over outer-axis planes [ilo, ihi) would
+// race with the exchange before it (see overlap_pairs); next_odd: the next step is odd (the
+// exchange is a FILL), else even (a DRAIN).  Negative on a bad configuration.
+extern "C" long long emu_overlap_violations(const lbm_config *cfg, int next_odd, int ilo,
+                                            int ihi)
+{
+    lbm_setup::Layout Lay;
+    std::string why;
+    if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
+    if (cfg->streaming != LBM_STREAM_AA || !Lay.halo) return -2;
+    const bool mrt = cfg->collision == LBM_MRT, o = next_odd != 0;
+    if (cfg->lattice == 27) return overlap_any<D3Q27, NoThermal, 2>(*cfg, Lay, o, ilo, ihi);
+    if (cfg->lattice == 19) {
+        if (cfg->thermal == 7)
+            return mrt ? overlap_any<D3Q19, D3Q7, 1>(*cfg, Lay, o, ilo, ihi)
+                       : overlap_any<D3Q19, D3Q7, 0>(*cfg, Lay, o, ilo, ihi);
+        return mrt ? overlap_any<D3Q19, NoThermal, 1>(*cfg, Lay, o, ilo, ihi)
+                   : overlap_any<D3Q19, NoThermal, 0>(*cfg, Lay, o, ilo, ihi);
+    }
+    if (cfg->thermal == 5)
+        return mrt ? overlap_any<D2Q9, D2Q5, 1>(*cfg, Lay, o, ilo, ihi)
+                   : overlap_any<D2Q9, D2Q5, 0>(*cfg, Lay, o, ilo, ihi);
+    return mrt ? overlap_any<D2Q9, NoThermal, 1>(*cfg, Lay, o, ilo, ihi)
+               : overlap_any<D2Q9, NoThermal, 0>(*cfg, Lay, o, ilo, ihi);
 }

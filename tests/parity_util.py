@@ -329,9 +329,9 @@ def gpu_states(w, checkpoints, window_fn=None, edit=None, streaming="aa"):
         r = dict(rho=rho, u=u, T=Tt, f=f, g=g)
         if window_fn is None:
             r = {k: (None if v is None else v.cpu().numpy()) for k, v in r.items()}
-            r["diag"] = sim.diagnostics(allow_nonfinite=True)
         else:
             r = window_fn(r)
+        r["diag"] = sim.diagnostics(allow_nonfinite=True)
         r["parity"] = sim.parity
         out[n] = r
     torch.cuda.synchronize()

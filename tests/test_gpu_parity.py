@@ -7,6 +7,7 @@ counts) with lbm_step called in uneven chunks.
 """
 import dataclasses
 import math
+import os
 
 import numpy as np
 import pytest
@@ -115,10 +116,13 @@ def test_immersed_boundary_200_and_201_steps(oracle_mod, w, streaming):
         _compare_ib(got[n], ref[n])
 
 
-def test_moving_samples_200_and_201_steps(oracle_mod):
+@pytest.mark.parametrize("path", ["host", "device", "device_keep_order"])
+def test_moving_samples_200_and_201_steps(oracle_mod, path):
     """A sphere of samples translating through the channel, the samples replaced before
-    every step (lbm_set_ib_samples): after 200 and 201 steps the state matches the oracle
-    stepped with the same positions and boundary velocity."""
+    every step (lbm_set_ib_samples from host arrays; lbm_set_ib_samples_device from device
+    tensors, sorted on the device every step, or sorted once and then placed in that
+    stored order): after 200 and 201 steps the state matches the oracle stepped with the
+    same positions and boundary velocity."""
     import torch
     from lattice_boltzmann_cfd_gb300 import Simulation
     w = W.perturbed(W.channel_ib_sphere(shape=(24, 16, 14), center=(8.3, 7.7, 6.9), radius=3.0,
@@ -135,9 +139,14 @@ def test_moving_samples_200_and_201_steps(oracle_mod):
     sim.init_equilibrium(torch.from_numpy(w.rho0).cuda(), torch.from_numpy(w.u0).cuda())
     p0 = oracle_mod.Problem(w)
     f, g = oracle_mod.init_equilibrium(p0, w.rho0, w.u0)
+    ub_d, w_d = torch.from_numpy(ub).cuda(), torch.from_numpy(w.ib_w).cuda()
     for k in range(201):
         xk = positions(k)
-        sim.set_ib_samples(xk, ub, w.ib_w)
+        if path == "host":
+            sim.set_ib_samples(xk, ub, w.ib_w)
+        else:
+            sim.set_ib_samples_device(torch.from_numpy(xk).cuda(), ub_d, w_d,
+                                      reorder=(path == "device" or k == 0))
         sim.step(1)
         oracle_mod.run(oracle_mod.Problem(dataclasses.replace(w, ib_x=xk, ib_ub=ub)), f, g, 1)
         if k + 1 in (200, 201):
@@ -148,6 +157,77 @@ def test_moving_samples_200_and_201_steps(oracle_mod):
             assert np.abs(u.cpu().numpy() - r_u).max() <= TOL_FIELDS, k + 1
             assert np.abs(fg.cpu().numpy() - f).max() <= TOL_FIELDS, k + 1
     sim.close()
+
+
+def _ib_states(w, steps, device_path):
+    """(populations, diagnostics, link mask) after ``steps`` steps with the samples set
+    through the host or the device path."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    x = w.ib_x
+    sim = Simulation(dataclasses.replace(w, ib_x=None),
+                     edit=lambda cfg: setattr(cfg, "ib_max_samples", len(x)))
+    if device_path:
+        sim.set_ib_samples_device(torch.from_numpy(np.ascontiguousarray(x)).cuda(),
+                                  torch.from_numpy(w.ib_ub).cuda(),
+                                  torch.from_numpy(w.ib_w).cuda())
+    else:
+        sim.set_ib_samples(x, w.ib_ub, w.ib_w)
+    sim.init_equilibrium(torch.from_numpy(w.rho0).cuda(), torch.from_numpy(w.u0).cuda())
+    sim.step(steps)
+    f = sim.populations()[0]
+    out = (f, sim.diagnostics(), sim.link_mask().cpu().numpy())
+    sim.close()
+    return out
+
+
+@pytest.mark.parametrize("samples", [3000, 40000], ids=["one block", "multi-block sort"])
+def test_device_ordered_samples_match_host_ordered(samples):
+    """Samples ordered on the device mark the same stencil cells bit for bit, and give the
+    same flow as the host-ordered ones (to the order of the atomic additions), with the
+    same reaction force and torque.  40,000 samples take the multi-block radix sort."""
+    n = 64
+    w = W.perturbed(W.channel_ib_sphere(shape=(n, 48, 48), center=(20.3, 23.6, 24.1),
+                                        radius=9, gx=1e-5), seed=7)
+    rng = np.random.default_rng(samples)
+    x = (np.array([20.3, 23.6, 24.1]) + rng.normal(size=(samples, 3)) * 5.0)
+    x[:, 1:] = np.clip(x[:, 1:], 1.0, 45.0)   # walls in y and z: stencils stay inside
+    x[:, 0] = x[:, 0] - 3 * n       # exercises the periodic wrap along x
+    x = x.astype(np.float32)
+    ub = rng.uniform(-0.01, 0.01, size=(samples, 3)).astype(np.float32)
+    # weights shrink with the sample count, so that the total penalty stays bounded
+    wt = (rng.uniform(0.1, 1.0, size=samples) * 2000.0 / samples).astype(np.float32)
+    w = dataclasses.replace(w, ib_x=x, ib_ub=ub, ib_w=wt)
+    fa, da, ma = _ib_states(w, 20, False)
+    fb, db, mb = _ib_states(w, 20, True)
+    assert np.array_equal(ma, mb)
+    assert (fa - fb).abs().max().item() < 1e-6
+    assert db["ib_dropped"] == 0
+    assert np.allclose(da["ib_force"], db["ib_force"], rtol=1e-5, atol=1e-9)
+    assert np.allclose(da["ib_torque"], db["ib_torque"], rtol=1e-4,
+                       atol=1e-6 * np.abs(da["ib_torque"]).max())
+
+
+def test_device_samples_drop_invalid_positions():
+    """On the device path a sample with a non-finite position, or whose stencil would leave
+    through a wall face, is dropped and counted; the rest act as if given alone."""
+    w = W.perturbed(W.channel_ib_sphere(shape=(40, 24, 22), center=(12.3, 11.7, 10.9),
+                                        radius=4, gx=1e-5), seed=8)
+    good = w.ib_x
+    bad = np.array([[5.0, np.nan, 4.0], [7.0, 23.5, 4.0], [3.0, 5.0, -0.5],
+                    [np.inf, 5.0, 5.0]], np.float32)
+    n_bad = len(bad)
+    mixed = np.concatenate([bad[:2], good, bad[2:]])
+    extra = lambda a, fill: np.concatenate([np.full((2,) + a.shape[1:], fill, a.dtype), a,
+                                            np.full((2,) + a.shape[1:], fill, a.dtype)])
+    wm = dataclasses.replace(w, ib_x=mixed, ib_ub=extra(w.ib_ub, 0.01),
+                             ib_w=extra(w.ib_w, 1.0))
+    fa, da, _ = _ib_states(w, 12, False)
+    fb, db, _ = _ib_states(wm, 12, True)
+    assert db["ib_dropped"] == n_bad
+    assert (fa - fb).abs().max().item() < 1e-6
+    assert np.allclose(da["ib_force"], db["ib_force"], rtol=1e-5, atol=1e-9)
+    assert np.allclose(da["ib_torque"], db["ib_torque"], rtol=1e-4,
+                       atol=1e-6 * np.abs(da["ib_torque"]).max())
 
 
 def test_immersed_boundary_sample_order_does_not_matter():
@@ -293,6 +373,85 @@ def test_full_size_128_cubed_200_201(oracle_mod, name):
             assert np.linalg.norm(F - Fr) <= TOL_FORCE_REL * np.linalg.norm(Fr), (F, Fr)
         if w.ib_x is not None:
             _compare_ib(got[n], ref[n])
+
+
+def test_full_size_cavity2d_4096_200_201(oracle_mod):
+    """Config 4 (D2Q9 MRT + D2Q5 MRT side-heated cavity, 4096^2) at full size, whole domain,
+    after 200 and 201 steps: fields, populations and the wall heat sums against the
+    oracle run on the whole domain."""
+    w = W.by_name("cavity2d")
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    got = gpu_states(w, [200, 201])
+    for n in (200, 201):
+        compare_fields(w, got[n], ref[n])
+        d, dr = got[n]["diag"], ref[n]["diag"]
+        assert math.isclose(d["mass"], dr["mass"], rel_tol=1e-6)
+        assert np.allclose(d["momentum"], dr["momentum"], rtol=1e-4, atol=1e-6 * dr["mass"])
+        assert np.allclose(d["heat"], dr["heat"], rtol=1e-4, atol=1e-3)
+        assert got[n]["parity"] == n % 2
+
+
+GOLDEN_512 = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                          "cavity3d_512_walls.npz")
+
+
+def test_full_size_cavity3d_512_200_201():
+    """Config 5 (D3Q19 MRT + D3Q7 MRT side-heated cube, 512^3) at full size after 200 and
+    201 steps, in the benchmark's launch configuration.
+
+    The oracle's values come from tests/golden/cavity3d_512_walls.npz, written by
+    tests/golden/make_cavity3d_512_walls.py (oracle only): the 8 planes next to the hot and
+    the cold wall in 13 blocks of 4 x 4 cells (corners, edge centres, face centre, random),
+    fields and the populations of the 2 planes nearest each wall, and each wall's heat sum
+    over its whole face.  Away from those walls the state is the initial rest state: the
+    Dirichlet walls are the only source of change, and a disturbance moves at most one cell
+    per step, so after n steps every cell with n + 1 <= x <= 510 - n still holds
+    rho = 1, u = 0, T = 0 (a rest state is a fixed point of every boundary kind)."""
+    gold = np.load(GOLDEN_512)
+    blk = gold["blocks"]
+    w = W.by_name("cavity3d")
+    nx = w.shape[0]
+
+    def take(r):
+        res = {}
+        for wall in ("hot", "cold"):
+            xs = torch.as_tensor(gold[f"x_{wall}"], device=r["rho"].device)
+            for i, (y0, z0) in enumerate(blk):
+                sl = (slice(int(z0), int(z0) + 4), slice(int(y0), int(y0) + 4))
+                res[wall, i] = dict(
+                    rho=r["rho"][sl].index_select(-1, xs).cpu().numpy(),
+                    u=r["u"][(slice(None),) + sl].index_select(-1, xs).cpu().numpy(),
+                    T=r["T"][sl].index_select(-1, xs).cpu().numpy(),
+                    f=r["f"][(slice(None),) + sl].index_select(-1, xs[:2]).cpu().numpy(),
+                    g=r["g"][(slice(None),) + sl].index_select(-1, xs[:2]).cpu().numpy())
+        res["fields"] = (r["rho"], r["u"], r["T"])
+        return res
+
+    mid = slice(202, nx - 202)   # untouched after 200 and after 201 steps
+
+    def take_and_check_rest(r):
+        res = take(r)
+        rho, u, T = res.pop("fields")
+        res["rest"] = max(float((rho[..., mid] - 1).abs().max()),
+                          float(u[..., mid].abs().max()), float(T[..., mid].abs().max()))
+        return res
+
+    got = gpu_states(w, [200, 201], window_fn=take_and_check_rest)
+    for n in (200, 201):
+        assert got[n]["rest"] <= TOL_FIELDS, (n, got[n]["rest"])
+        for wall in ("hot", "cold"):
+            for i in range(len(blk)):
+                g_, k = got[n][wall, i], f"{wall}_{n}_"
+                assert np.abs(g_["rho"] - gold[k + "rho"][i]).max() <= TOL_FIELDS, (n, wall, i)
+                assert np.abs(g_["u"] - gold[k + "u"][i]).max() <= TOL_FIELDS, (n, wall, i)
+                assert np.abs(g_["T"] - gold[k + "T"][i]).max() <= TOL_FIELDS, (n, wall, i)
+                assert np.abs(g_["f"] - gold[k + "f"][i]).max() <= TOL_FIELDS, (n, wall, i)
+                assert np.abs(g_["g"] - gold[k + "g"][i]).max() <= TOL_FIELDS, (n, wall, i)
+        heat = got[n]["diag"]["heat"]
+        for face, wall in ((0, "hot"), (1, "cold")):
+            want = float(gold[f"{wall}_{n}_heat"])
+            assert abs(heat[face] - want) <= 1e-4 * abs(want) + 1e-3, (n, wall, heat[face], want)
+        assert got[n]["parity"] == n % 2
 
 
 # --------------------------------------------------- full sizes: sampled windows ----

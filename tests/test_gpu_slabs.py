@@ -5,9 +5,10 @@ the same kernels, at both AA parities, and their summed diagnostics agree with i
 In these cases every slab runs the same kernel family as the undivided domain (masked where
 the domain has walls or solids on its other axes, unmasked where it is periodic and
 all-fluid), so the comparison is between identical per-cell arithmetic and any difference
-is an exchange error.  The undivided domain is in turn held to the oracle by the parity
-tests.  A domain whose only walls close the outer axis mixes the two families (the end
-slabs are masked, the inner ones are not); it is compared within fp32 rounding."""
+is an exchange error.  Every slab run is also compared element by element with the fp64
+oracle run on the undivided domain.  A domain whose only walls close the outer axis mixes
+the two families (the end slabs are masked, the inner ones are not); it is compared with
+the undivided domain within fp32 rounding."""
 import dataclasses
 
 import numpy as np
@@ -15,7 +16,8 @@ import pytest
 
 from lattice_boltzmann_cfd_gb300 import capi
 from lattice_boltzmann_cfd_gb300 import workloads as W
-from parity_util import outer_walls_case, slab_cases
+from parity_util import (TOL_FIELDS, compare_fields, oracle_states, outer_walls_case,
+                         slab_cases)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -40,7 +42,8 @@ def _single(w, steps):
     return out
 
 
-def _slabs(w, steps, nslabs, chunks=None):
+def _slabs(w, steps, nslabs, chunks=None, fields=False):
+    """(f, g, diagnostics) of the slab run, plus its (rho, u, T) when ``fields``."""
     from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
     dom = SlabDomain(w, nslabs)
     dom.init_equilibrium()
@@ -48,6 +51,10 @@ def _slabs(w, steps, nslabs, chunks=None):
         dom.step(c)
     f, g = dom.populations()
     out = (f.cpu().numpy(), None if g is None else g.cpu().numpy(), dom.diagnostics())
+    if fields:
+        rho, u, T = dom.macroscopic()
+        out += ({"rho": rho.cpu().numpy(), "u": u.cpu().numpy(),
+                 "T": None if T is None else T.cpu().numpy(), "f": out[0], "g": out[1]},)
     dom.close()
     return out
 
@@ -67,12 +74,16 @@ CASES = slab_cases() + _large_cases()
 
 
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
-def test_slabs_bitwise_equal_single_domain(w):
+def test_slabs_bitwise_equal_single_domain(oracle_mod, w):
+    """Every slab split matches the undivided domain bit for bit, and the fp64 oracle
+    (run on the undivided domain) within 1e-6 on the populations and 2e-5 on rho, u, T."""
     n_outer = w.shape[w.dim - 1]
+    ref = oracle_states(oracle_mod, w, [7, 8])
     for steps in (7, 8):
         f1, g1, d1 = _single(w, steps)
         for k in sorted({2, 3, n_outer if n_outer <= 13 else 5}):
-            fs, gs, ds = _slabs(w, steps, k, chunks=[3, steps - 3])
+            fs, gs, ds, got = _slabs(w, steps, k, chunks=[3, steps - 3], fields=True)
+            compare_fields(w, got, ref[steps], tol=TOL_FIELDS, pop_tol=1e-6)
             assert np.array_equal(fs, f1), (steps, k)
             if w.thermal:
                 assert np.array_equal(gs, g1), (steps, k)
@@ -90,13 +101,15 @@ def test_slabs_bitwise_equal_single_domain(w):
                 assert np.allclose(ds["heat"], d1["heat"], rtol=0, atol=1e-6 * hscale)
 
 
-def test_walls_only_on_the_outer_axis():
+def test_walls_only_on_the_outer_axis(oracle_mod):
     """Walls (and Dirichlet faces) only at the ends of the outer axis: the end slabs run
     the masked kernels, the inner ones the unmasked kernels."""
     w = outer_walls_case(shape=(64, 20, 24), seed=47)
+    ref = oracle_states(oracle_mod, w, [8, 9])
     for steps in (8, 9):
         f1, g1, d1 = _single(w, steps)
-        fs, gs, ds = _slabs(w, steps, 4)
+        fs, gs, ds, got = _slabs(w, steps, 4, fields=True)
+        compare_fields(w, got, ref[steps], tol=TOL_FIELDS, pop_tol=1e-6)
         assert np.abs(fs - f1).max() < 1e-6
         assert np.abs(gs - g1).max() < 1e-6
         assert ds["fluid_cells"] == d1["fluid_cells"]
@@ -148,3 +161,104 @@ def test_per_rank_driver_alone(w):
         if w.thermal:
             assert np.array_equal(g.cpu().numpy(), g1)
         d.close()
+
+
+OVERLAP_CASES = [CASES[i] for i in (0, 3, 5, 7, 8)] + _large_cases()
+
+
+@pytest.mark.parametrize("w", OVERLAP_CASES, ids=[c.name for c in OVERLAP_CASES])
+def test_overlapped_slabs_equal_plain_order(w):
+    """The overlapped order (interior planes, boundary planes, exchange on a second stream
+    beside the next step's interior) gives the plain order's state bit for bit."""
+    n_outer = w.shape[w.dim - 1]
+    for steps in (7, 8):
+        f1, g1, d1 = _single(w, steps)
+        for k in sorted({2, 3, min(n_outer, 5)}):
+            from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
+            dom = SlabDomain(w, k, overlap=True)
+            dom.init_equilibrium()
+            for c in (3, steps - 3):
+                dom.step(c)
+            f, g = dom.populations()
+            assert np.array_equal(f.cpu().numpy(), f1), (steps, k)
+            if w.thermal:
+                assert np.array_equal(g.cpu().numpy(), g1), (steps, k)
+            dom.close()
+
+
+@pytest.mark.parametrize("overlap", [False, True], ids=["plain", "overlap"])
+@pytest.mark.parametrize("w", [W.perturbed(W.cavity3d(shape=(70, 40, 37)), seed=43),
+                               W.perturbed(W.cavity2d(shape=(300, 181, 1)), seed=44)],
+                         ids=["cavity3d 70x40x37", "cavity2d 300x181"])
+def test_slabs_200_and_201_steps_against_the_oracle(oracle_mod, w, overlap):
+    """Three slabs, 200 and 201 steps, against the oracle on the undivided domain (2e-5 on
+    the fields and populations, heat sums 1e-4 relative)."""
+    from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    dom = SlabDomain(w, 3, overlap=overlap)
+    dom.init_equilibrium()
+    done = 0
+    for n in (200, 201):
+        dom.step(n - done)
+        done = n
+        f, g = dom.populations()
+        rho, u, T = dom.macroscopic()
+        got = {"rho": rho.cpu().numpy(), "u": u.cpu().numpy(), "T": T.cpu().numpy(),
+               "f": f.cpu().numpy(), "g": g.cpu().numpy()}
+        compare_fields(w, got, ref[n])
+        assert np.allclose(dom.diagnostics()["heat"], ref[n]["diag"]["heat"], rtol=1e-4,
+                           atol=1e-3)
+    dom.close()
+
+
+def test_step_planes_equals_step():
+    """lbm_step_planes over any partition of the planes, in any order, is lbm_step(1), at both
+    parities; calls that need a whole step are refused while one is partly done."""
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    cases = [W.perturbed(W.cavity3d(shape=(70, 20, 13)), seed=61),
+             W.perturbed(W.cavity2d(shape=(100, 23, 1)), seed=62),
+             W.random_periodic(shape=(40, 12, 11), seed=63, lattice=27)]
+    rng = np.random.default_rng(9)
+    for w in cases:
+        n_outer = w.shape[w.dim - 1]
+        ref = Simulation(w)
+        sim = Simulation(w)
+        dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        for s in (ref, sim):
+            s.init_equilibrium(dev(w.rho0), dev(w.u0), dev(w.T_init))
+        for step in range(5):
+            ref.step(1)
+            cuts = sorted(rng.choice(np.arange(1, n_outer), size=3, replace=False))
+            parts = list(zip([0] + cuts, cuts + [n_outer]))
+            rng.shuffle(parts)
+            for i, (lo, hi) in enumerate(parts):
+                sim.step_planes(int(lo), int(hi))
+                if i < len(parts) - 1:
+                    assert sim.parity == step % 2
+                    with pytest.raises(capi.LbmError) as e:
+                        sim.step(1)
+                    assert e.value.status == capi.LBM_ERR_STATE
+                    with pytest.raises(capi.LbmError):
+                        sim.populations()
+                    with pytest.raises(capi.LbmError) as e:
+                        sim.step_planes(int(lo), int(hi))        # already stepped
+                    assert e.value.status == capi.LBM_ERR_ARG
+            assert sim.parity == (step + 1) % 2
+            fa, ga = ref.populations()
+            fb, gb = sim.populations()
+            assert torch.equal(fa, fb), (w.name, step)
+            if w.thermal:
+                assert torch.equal(ga, gb), (w.name, step)
+        with pytest.raises(capi.LbmError):
+            sim.step_planes(0, n_outer + 1)
+        with pytest.raises(capi.LbmError):
+            sim.step_planes(3, 3)
+        ref.close()
+        sim.close()
+    two = Simulation(W.random_periodic(shape=(16, 8, 6), seed=64), streaming="pull")
+    w2 = W.random_periodic(shape=(16, 8, 6), seed=64)
+    two.init_equilibrium(*(torch.from_numpy(a).cuda() for a in (w2.rho0, w2.u0)))
+    with pytest.raises(capi.LbmError) as e:
+        two.step_planes(0, 6)
+    assert e.value.status == capi.LBM_ERR_UNSUPPORTED
+    two.close()
