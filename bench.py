@@ -525,6 +525,41 @@ def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None, overla
     return out
 
 
+def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None):
+    """MLUPS of a workload cut into nb = (bx, by, bz) blocks on this GPU, with the per-axis
+    halo exchange after every step (z, then y, then x; a step = one step launch per block +
+    one pack and one unpack launch per block face and direction)."""
+    import torch
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain, exchange_axes
+    w = cached_workload(name)
+    dom = BlockDomain(w, nb)
+    dom.init_equilibrium()
+    dom.step(4)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        dom.step(lbm_steps)
+    b.record()
+    torch.cuda.synchronize()
+    step_s = a.elapsed_time(b) / 1e3 / (reps * lbm_steps)
+    halo = dom.halo_bytes_per_step()
+    faces = sum(len(dom.pairs(ax)) for ax in exchange_axes(w.dim, dom.nb))
+    dom.close()
+    del dom
+    torch.cuda.empty_cache()
+    mlups = w.cells / step_s / 1e6
+    out = {"workload": workload_label(name, w), "layout": "aa", "blocks": list(nb),
+           "decomposition": "blocks, 1 ghost plane per inner face of each split axis, "
+                            "exchanged axis by axis with the ghost rows of the other axes "
+                            "(edges and corners in two or three hops), all on this GPU",
+           "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
+           "halo_launches_per_step": 4 * faces}
+    if single_mlups:
+        out["vs_single_domain"] = round(mlups / single_mlups, 4)
+    return out
+
+
 # --------------------------------------------------------------------- main --------
 
 def run_gpu(args, dctx):
@@ -631,6 +666,12 @@ def run_gpu(args, dctx):
             for overlap in (False, True):
                 line["secondary"].append(run_slabs_secondary(n, 4, args.lbm_steps, 2,
                                                              single.get(lbl), overlap))
+            for nb in ((1, 2, 2), (1, 2, 4)):
+                line["secondary"].append(run_blocks_secondary(n, nb, args.lbm_steps, 2,
+                                                              single.get(lbl)))
+        lbl = workload_label("cavity2d_4096", cached_workload("cavity2d_4096"))
+        line["secondary"].append(run_blocks_secondary("cavity2d_4096", (2, 2, 1),
+                                                      args.lbm_steps, 2, single.get(lbl)))
     line["cpu_baseline"] = cpu_baseline(args.workload)
     return line
 

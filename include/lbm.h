@@ -97,9 +97,10 @@ enum { LBM_THERMAL_NONE = 0, LBM_D2Q5 = 5, LBM_D3Q7 = 7 };
 enum { LBM_BGK = 0, LBM_MRT = 1, LBM_CM = 2 };
 enum { LBM_FACE_PERIODIC = 0, LBM_FACE_WALL = 1 };        /* flow: half-way bounce-back */
 /* A slab face: the context is one slab of a larger domain, split along its outer axis (z
- * in 3-D, y in 2-D).  The grid then includes one ghost plane at each HALO face (the first /
- * last plane of that axis); ghost cells are never updated and hold the neighbouring slab's
- * populations, moved by lbm_halo_pack / lbm_halo_unpack ([TLBM] Sec. 3). */
+ * in 3-D, y in 2-D), or one block of a domain split along several axes.  The grid then
+ * includes one ghost plane at each HALO face (the first / last plane of that axis); ghost
+ * cells are never updated and hold the neighbouring slab's or block's populations, moved by
+ * lbm_halo_pack / lbm_halo_unpack and their per-axis forms ([TLBM] Sec. 3). */
 enum { LBM_FACE_HALO = 2 };
 enum { LBM_HALO_FILL = 0, LBM_HALO_DRAIN = 1 };
 enum { LBM_TFACE_ADIABATIC = 0, LBM_TFACE_DIRICHLET = 1 }; /* thermal, on WALL faces   */
@@ -309,6 +310,29 @@ lbm_status lbm_set_ib_samples_device(lbm_ctx *ctx, int n, const float *xyz, cons
 lbm_status lbm_halo_bytes(const lbm_ctx *ctx, size_t *bytes);
 lbm_status lbm_halo_pack(lbm_ctx *ctx, int side, int phase, void *buf);
 lbm_status lbm_halo_unpack(lbm_ctx *ctx, int side, int phase, const void *buf);
+
+/* Block halos: the same exchange along any axis, for a domain split along several axes
+ * (the multi-dimensional partitioning that [TLBM] Sec. 3 compares with slabs).  A context
+ * may have HALO faces on every axis (x, y and z in 3-D; x and y in 2-D); its ghost planes
+ * are then the first / last plane of each such axis, and the cells where ghost planes of
+ * two or three axes meet are ghost cells too.  lbm_halo_axis_pack / _unpack move the plane
+ * of one axis, exactly as lbm_halo_pack / _unpack do for the outer axis:
+ *   axis: 0 = x, 1 = y, 2 = z (3-D only); side 0 / 1 = the low / high face of that axis,
+ *         which must be a HALO face (LBM_ERR_ARG otherwise);
+ *   buf: lbm_halo_axis_bytes(axis) bytes, packed as [direction][plane cell] fp32, momentum
+ *        then thermal, directions with c_axis = +-1 in index order, plane cells with the
+ *        lower remaining axis fastest (y then z for axis x; x then z for y; x then y for z).
+ * The whole plane moves, the ghost rows of the other axes included.  Run the axes one after
+ * another -- every pack and unpack of one axis before the next axis's packs, in the same
+ * axis order at FILL and at DRAIN -- and a link across an edge or a corner reaches the
+ * diagonal block in two or three hops through those rows: the FILL of the later axis
+ * carries what the earlier one put in its ghost rows, and a DRAIN unpack writes a ghost row
+ * of the other axis whenever the cell it lands in is one, from where the next axis's DRAIN
+ * takes it on.  Between steps every owned cell then holds what one undivided domain would.
+ * lbm_step_planes and the overlap above stay with the outer axis. */
+lbm_status lbm_halo_axis_bytes(const lbm_ctx *ctx, int axis, size_t *bytes);
+lbm_status lbm_halo_axis_pack(lbm_ctx *ctx, int axis, int side, int phase, void *buf);
+lbm_status lbm_halo_axis_unpack(lbm_ctx *ctx, int axis, int side, int phase, const void *buf);
 
 /* Enqueue later work on another stream (a cudaStream_t). */
 lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);

@@ -84,6 +84,9 @@ SIGNATURES = [
     ("lbm_halo_bytes", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_size_t)]),
     ("lbm_halo_pack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_halo_unpack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP]),
+    ("lbm_halo_axis_bytes", ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    ("lbm_halo_axis_pack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP]),
+    ("lbm_halo_axis_unpack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_set_stream", ctypes.c_int, [_VP, _VP]),
     ("lbm_reduce_populations_static", ctypes.c_int,
      [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP,
@@ -245,6 +248,20 @@ def lbm_halo_pack(ctx, side: int, phase: int, buf):
 
 def lbm_halo_unpack(ctx, side: int, phase: int, buf):
     _check(load().lbm_halo_unpack(ctx, int(side), int(phase), _addr(buf)), ctx)
+
+
+def lbm_halo_axis_bytes(ctx, axis: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().lbm_halo_axis_bytes(ctx, int(axis), ctypes.byref(n)), ctx)
+    return n.value
+
+
+def lbm_halo_axis_pack(ctx, axis: int, side: int, phase: int, buf):
+    _check(load().lbm_halo_axis_pack(ctx, int(axis), int(side), int(phase), _addr(buf)), ctx)
+
+
+def lbm_halo_axis_unpack(ctx, axis: int, side: int, phase: int, buf):
+    _check(load().lbm_halo_axis_unpack(ctx, int(axis), int(side), int(phase), _addr(buf)), ctx)
 
 
 def lbm_set_stream(ctx, stream):

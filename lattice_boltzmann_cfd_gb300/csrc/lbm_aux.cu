@@ -92,13 +92,15 @@ cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, bool se
     return cudaGetLastError();
 }
 
-cudaError_t launch_halo(int lattice, int thermal, const Params &P, int side, int phase,
-                        int unpack, float *buf, cudaStream_t s)
+cudaError_t launch_halo(int lattice, int thermal, const Params &P, int axis, int side,
+                        int phase, int unpack, float *buf, cudaStream_t s)
 {
-    const int plane_cells = lattice == 9 ? P.nx : P.nx * P.ny;
+    const int n[3] = {P.nx, P.ny, P.nz};
+    const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
     const dim3 b(256), g((plane_cells + 255) / 256);
     return by_lattice(lattice, thermal, [&](auto l, auto tl) {
-        halo_kernel<decltype(l), decltype(tl)><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+        halo_kernel<decltype(l), decltype(tl)><<<g, b, 0, s>>>(P, axis, side, phase, unpack,
+                                                                buf);
         return cudaGetLastError();
     });
 }

@@ -717,25 +717,27 @@ lbm_status lbm_set_ib_samples_device(lbm_ctx *c, int n, const float *xyz, const 
 
 namespace {
 
-// Populations per plane cell that cross a slab face (momentum + thermal).
+// Populations per plane cell that cross a face (momentum + thermal), on any axis.
 int halo_directions(const lbm_ctx *c)
 {
     const int thermal = c->L.QT ? 1 : 0;
-    if (c->cfg.lattice == LBM_D3Q27) return 9;        // every c with c_outer = +-1
+    if (c->cfg.lattice == LBM_D3Q27) return 9;        // every c with c_axis = +-1
     return c->cfg.lattice == LBM_D3Q19 ? 5 + thermal : 3 + thermal;
 }
 
-size_t halo_plane_cells(const lbm_ctx *c)
+size_t halo_plane_cells(const lbm_ctx *c, int axis)
 {
-    return c->cfg.lattice == LBM_D2Q9 ? (size_t)c->cfg.nx : (size_t)c->cfg.nx * c->cfg.ny;
+    const size_t n[3] = {(size_t)c->cfg.nx, (size_t)c->cfg.ny, (size_t)c->cfg.nz};
+    return n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
 }
 
-lbm_status halo_call(lbm_ctx *c, int side, int phase, int unpack, const void *buf)
+lbm_status halo_call(lbm_ctx *c, int axis, int side, int phase, int unpack, const void *buf)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (!c->L.halo) return fail(c, LBM_ERR_STATE, "no HALO face in this context");
+    if (axis < 0 || axis >= c->L.dim) return fail(c, LBM_ERR_ARG, "axis out of range");
     if (side != 0 && side != 1) return fail(c, LBM_ERR_ARG, "side must be 0 (low) or 1 (high)");
-    const int face = 2 * (c->L.dim - 1) + side;
+    const int face = 2 * axis + side;
     if (c->cfg.face_flow[face] != LBM_FACE_HALO)
         return fail(c, LBM_ERR_ARG, "that side is not a HALO face");
     if (phase != LBM_HALO_FILL && phase != LBM_HALO_DRAIN)
@@ -750,8 +752,8 @@ lbm_status halo_call(lbm_ctx *c, int side, int phase, int unpack, const void *bu
     void *db;
     lbm_status st = device_address(c, buf, "buf", &db);
     if (st != LBM_OK) return st;
-    cudaError_t e = lbm::launch_halo(c->cfg.lattice, c->cfg.thermal, c->P, side, phase, unpack,
-                                     static_cast<float *>(db), c->stream);
+    cudaError_t e = lbm::launch_halo(c->cfg.lattice, c->cfg.thermal, c->P, axis, side, phase,
+                                     unpack, static_cast<float *>(db), c->stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "halo kernel");
     return LBM_OK;
 }
@@ -761,18 +763,38 @@ lbm_status halo_call(lbm_ctx *c, int side, int phase, int unpack, const void *bu
 lbm_status lbm_halo_bytes(const lbm_ctx *c, size_t *bytes)
 {
     if (!c || !bytes) return fail(nullptr, LBM_ERR_ARG, "ctx and bytes are required");
-    *bytes = c->L.halo ? sizeof(float) * halo_directions(c) * halo_plane_cells(c) : 0;
+    *bytes = c->L.halo ? sizeof(float) * halo_directions(c) * halo_plane_cells(c, c->L.dim - 1)
+                       : 0;
     return LBM_OK;
 }
 
 lbm_status lbm_halo_pack(lbm_ctx *c, int side, int phase, void *buf)
 {
-    return halo_call(c, side, phase, 0, buf);
+    return halo_call(c, c ? c->L.dim - 1 : 0, side, phase, 0, buf);
 }
 
 lbm_status lbm_halo_unpack(lbm_ctx *c, int side, int phase, const void *buf)
 {
-    return halo_call(c, side, phase, 1, buf);
+    return halo_call(c, c ? c->L.dim - 1 : 0, side, phase, 1, buf);
+}
+
+lbm_status lbm_halo_axis_bytes(const lbm_ctx *c, int axis, size_t *bytes)
+{
+    if (!c || !bytes) return fail(nullptr, LBM_ERR_ARG, "ctx and bytes are required");
+    if (axis < 0 || axis >= c->L.dim)
+        return fail(const_cast<lbm_ctx *>(c), LBM_ERR_ARG, "axis out of range");
+    *bytes = c->L.halo ? sizeof(float) * halo_directions(c) * halo_plane_cells(c, axis) : 0;
+    return LBM_OK;
+}
+
+lbm_status lbm_halo_axis_pack(lbm_ctx *c, int axis, int side, int phase, void *buf)
+{
+    return halo_call(c, axis, side, phase, 0, buf);
+}
+
+lbm_status lbm_halo_axis_unpack(lbm_ctx *c, int axis, int side, int phase, const void *buf)
+{
+    return halo_call(c, axis, side, phase, 1, buf);
 }
 
 lbm_status lbm_set_stream(lbm_ctx *c, void *cuda_stream)

@@ -126,9 +126,9 @@ inline unsigned *ib_dropped_counter(const Params &P, void *scratch)
 cudaError_t launch_ib_order(int lattice, const Params &P, int n, int l, const float *xyz,
                             const float *ub, const float *w, void *scratch, bool reorder,
                             cudaStream_t s);
-// Slab halo pack (unpack = 0) or unpack (unpack = 1) of one side and phase.
-cudaError_t launch_halo(int lattice, int thermal, const Params &P, int side, int phase,
-                        int unpack, float *buf, cudaStream_t s);
+// Halo pack (unpack = 0) or unpack (unpack = 1) of one side of one axis, one phase.
+cudaError_t launch_halo(int lattice, int thermal, const Params &P, int axis, int side,
+                        int phase, int unpack, float *buf, cudaStream_t s);
 cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s);
 

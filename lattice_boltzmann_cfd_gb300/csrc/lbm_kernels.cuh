@@ -48,6 +48,8 @@ struct Params {
     int face_wall[6];      // per face: 1 = wall (flow)
     int face_halo[6];      // per face: 1 = halo face of a slab (ghost plane, no wrap)
     int ghost_lo, ghost_hi;  // outer-axis coordinate of a slab's ghost planes, -1 = none
+    // blocks: ghost planes on the other axes too (ghost_inner = 1); per axis, -1 = none
+    int ghost_inner, ghost3_lo[3], ghost3_hi[3];
     // outer-axis planes (z in 3-D, y in 2-D) the AA step kernels cover: [plane_lo,
     // plane_hi); the whole axis except in launches of lbm_step_planes
     int plane_lo, plane_hi;
@@ -92,13 +94,17 @@ LBM_HD int nb(const Offs &o, int cx, int cy, int cz)
 
 LBM_HD bool bit(uint32_t m, int b) { return (m >> b) & 1u; }
 
-// A ghost plane of a slab (outer axis: z in 3-D, y in 2-D).  Masked kernels see GHOST_BIT;
-// unmasked ones (a slab with neither walls nor solids) test the coordinate.
+// A cell on a ghost plane of a slab (outer axis: z in 3-D, y in 2-D) or of a block (any
+// axis).  Masked kernels see GHOST_BIT; unmasked ones (neither walls nor solids) test the
+// coordinates: the outer axis always, the others only in blocks (a uniform flag).
 template <class L>
-LBM_HD bool ghost_plane(const Params &P, int y, int z)
+LBM_HD bool ghost_plane(const Params &P, int x, int y, int z)
 {
     const int c = L::DIM == 3 ? z : y;
-    return c == P.ghost_lo || c == P.ghost_hi;
+    if (c == P.ghost_lo || c == P.ghost_hi) return true;
+    if (!P.ghost_inner) return false;
+    return x == P.ghost3_lo[0] || x == P.ghost3_hi[0] || y == P.ghost3_lo[1] ||
+           y == P.ghost3_hi[1] || (L::DIM == 3 && (z == P.ghost3_lo[2] || z == P.ghost3_hi[2]));
 }
 
 // ---------------------------------------------------------------- cell access ---------
@@ -463,7 +469,7 @@ template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool 
 LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z)
 {
     static_assert(!FACES || MASKED, "FACES is a masked form");
-    if ((!MASKED || FACES) && ghost_plane<L>(Pr, y, z)) return;
+    if ((!MASKED || FACES) && ghost_plane<L>(Pr, x, y, z)) return;
     const int idx = x + Pr.nx * (y + Pr.ny * z);
     // The mask load and the population loads are issued together: the populations are
     // loaded as if no link were a wall (except the x-face wall links, known from x), and
@@ -1043,7 +1049,7 @@ __global__ void macro_kernel(const Params P, float *__restrict__ rho, float *__r
     const size_t N = (size_t)P.nx * P.ny * P.nz;
     uint32_t m = 0;
     if (MASKED) m = P.mask[idx];
-    if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, y, z))) {
+    if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, x, y, z))) {
         if (rho) rho[idx] = 0.0f;
         if (u) {
             for (int a = 0; a < L::DIM; ++a) u[a * N + idx] = 0.0f;
@@ -1091,7 +1097,7 @@ __global__ void pop_kernel(const Params P, float *__restrict__ fo, float *__rest
     const size_t N = (size_t)P.nx * P.ny * P.nz;
     uint32_t m = 0;
     if (MASKED) m = P.mask[idx];
-    if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, y, z))) {
+    if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, x, y, z))) {
         if (!SET) {
             for (int q = 0; q < L::Q; ++q) fo[q * N + idx] = 0.0f;
             if (TL::Q > 0 && go)
@@ -1167,7 +1173,7 @@ __global__ void __launch_bounds__(DIAG_THREADS) diag_kernel(const Params P, doub
         const int z = idx / (P.nx * P.ny);
         uint32_t m = 0;
         if (MASKED) m = P.mask[idx];
-        if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, y, z))) continue;
+        if ((m & SKIP_BITS) || (!MASKED && ghost_plane<L>(P, x, y, z))) continue;
         Offs o{};
         if (PAT != NATURAL) o = make_offs(x, y, z, P);
         float f[L::Q], g[TL::QA];
@@ -1273,43 +1279,53 @@ static __global__ void __launch_bounds__(DIAG_THREADS) diag_finalize(const doubl
 
 // ------------------------------------------------------------------ slab halos -------
 
-// Halo exchange of a slab whose outer axis (z in 3-D, y in 2-D) has HALO faces with ghost
-// planes ("Multi-GPU thermal lattice Boltzmann simulations using OpenACC and MPI", Sec. 3:
-// only the populations that cross a face are sent, as contiguous buffers).  Under the AA
-// pattern only the odd step reads and writes across a slab face:
+// Halo exchange of a slab (HALO faces on the outer axis: z in 3-D, y in 2-D) or a block
+// (HALO faces on any axes), with a ghost plane at each HALO face ("Multi-GPU thermal
+// lattice Boltzmann simulations using OpenACC and MPI", Sec. 3: only the populations that
+// cross a face are sent, as contiguous buffers).  Under the AA pattern only the odd step
+// reads and writes across a face:
 //   FILL  (before an odd step): the neighbour's boundary plane -> my ghost plane, the
 //         populations pointing out through my face (they are what my boundary cells pull);
 //   DRAIN (after it): my ghost plane -> the neighbour's boundary plane, the same populations
 //         (what my boundary cells pushed into the ghost).
 // A pack of side s / phase FILL reads my boundary plane at s with the populations pointing
 // into my slab; unpack of side s / FILL writes my ghost plane at s with those pointing out;
-// DRAIN swaps the planes' roles.  A DRAIN leaves slot (q, x) alone where the link of x
-// towards the ghost (opposite q) is a wall link: x bounced that population back into the
-// slot itself, and the ghost's copy was never written.  buf: [direction][plane cell],
-// momentum then thermal.
+// DRAIN swaps the planes' roles.  A plane spans the whole extent of the other axes, their
+// ghost rows included: a block driver exchanges the axes one after another (FILL in one
+// order, DRAIN in the reverse one), so that what crosses an edge or a corner travels through
+// the ghost rows of the intermediate neighbours.  A DRAIN leaves slot (q, x) alone where
+// the link of x towards the ghost (opposite q) is a wall link: x bounced that population
+// back into the slot itself, and the ghost's copy was never written; and it leaves solid
+// cells alone.  buf: [direction][plane cell], momentum then thermal; plane cells with the
+// lower remaining axis fastest.
 template <class L, class TL>
-LBM_HD void halo_cell(const Params &P, int side, int phase, int unpack, float *buf, int i)
+LBM_HD void halo_cell(const Params &P, int axis, int side, int phase, int unpack, float *buf,
+                      int i)
 {
-    constexpr int outer = L::DIM == 3 ? 2 : 1;
-    const int n_outer = outer == 2 ? P.nz : P.ny;
-    const int plane_cells = outer == 2 ? P.nx * P.ny : P.nx;
+    const int n[3] = {P.nx, P.ny, P.nz};
+    const int u = axis == 0 ? 1 : 0, v = axis == 2 ? 1 : 2;   // the other two axes
+    const int plane_cells = n[u] * n[v];
     // ghost plane of the side, or the owned plane next to it
     const bool ghost_plane = (phase == 0) == (unpack != 0);
-    int plane = side ? n_outer - 1 : 0;
+    int plane = side ? n[axis] - 1 : 0;
     if (!ghost_plane) plane += side ? -1 : 1;
-    const int idx = i + plane * plane_cells;
+    int c3[3];
+    c3[axis] = plane;
+    c3[u] = i % n[u];
+    c3[v] = i / n[u];
+    const int idx = c3[0] + P.nx * (c3[1] + P.ny * c3[2]);
     // directions pointing out through the side (ghost plane) or into the slab (owned plane)
     const int out_sign = side ? 1 : -1;
     const int sign = ghost_plane ? out_sign : -out_sign;
-    // DRAIN into my boundary plane: links that are bounced (or a cell never updated) keep
-    // their own value
+    // DRAIN into my boundary plane: links that are bounced (or a solid cell) keep their own
+    // value; a ghost cell on it (a block's edge) holds values in transit
     const bool drain_in = unpack && !ghost_plane;
     const uint32_t keep = drain_in && P.mask ? P.mask[idx] : 0u;
-    const bool skip_cell = keep & SKIP_BITS;
+    const bool skip_cell = keep & SOLID_BIT;
     int k = 0;
 #pragma unroll
     for (int q = 0; q < L::Q; ++q) {
-        const int c = outer == 2 ? L::cz(q) : L::cy(q);
+        const int c = axis == 0 ? L::cx(q) : axis == 1 ? L::cy(q) : L::cz(q);
         if (c != sign) continue;
         float *slot = P.f + ((size_t)q * P.S + (unsigned)idx);
         float *b = buf + ((size_t)k * plane_cells + i);
@@ -1320,7 +1336,7 @@ LBM_HD void halo_cell(const Params &P, int side, int phase, int unpack, float *b
     if constexpr (TL::Q > 0) {
 #pragma unroll
         for (int q = 0; q < TL::Q; ++q) {
-            const int c = outer == 2 ? L::cz(q) : L::cy(q);
+            const int c = axis == 0 ? L::cx(q) : axis == 1 ? L::cy(q) : L::cz(q);
             if (c != sign) continue;
             float *slot = P.g + ((size_t)q * P.S + (unsigned)idx);
             float *b = buf + ((size_t)k * plane_cells + i);
@@ -1332,11 +1348,12 @@ LBM_HD void halo_cell(const Params &P, int side, int phase, int unpack, float *b
 }
 
 template <class L, class TL>
-__global__ void halo_kernel(const Params P, int side, int phase, int unpack, float *buf)
+__global__ void halo_kernel(const Params P, int axis, int side, int phase, int unpack, float *buf)
 {
-    const int plane_cells = L::DIM == 3 ? P.nx * P.ny : P.nx;
+    const int n[3] = {P.nx, P.ny, P.nz};
+    const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < plane_cells) halo_cell<L, TL>(P, side, phase, unpack, buf, i);
+    if (i < plane_cells) halo_cell<L, TL>(P, axis, side, phase, unpack, buf, i);
 }
 
 }  // namespace lbm

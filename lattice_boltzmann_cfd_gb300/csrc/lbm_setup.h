@@ -143,13 +143,10 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
     if (!std::isfinite(c->gbeta) || !std::isfinite(c->T0))
         return bad(LBM_ERR_ARG, "gbeta and T0 must be finite");
     bool any_wall = false, any_halo = false;
-    const int outer = dim - 1;   // z in 3-D, y in 2-D
     for (int i = 0; i < 2 * dim; ++i) {
         const int k = c->face_flow[i];
         if (k != LBM_FACE_PERIODIC && k != LBM_FACE_WALL && k != LBM_FACE_HALO)
             return bad(LBM_ERR_ARG, "face_flow entries must be PERIODIC, WALL or HALO");
-        if (k == LBM_FACE_HALO && i / 2 != outer)
-            return bad(LBM_ERR_UNSUPPORTED, "HALO faces only on the outer axis (z in 3-D, y in 2-D)");
         if (c->face_T[i] != LBM_TFACE_ADIABATIC && c->face_T[i] != LBM_TFACE_DIRICHLET)
             return bad(LBM_ERR_ARG, "face_T entries must be ADIABATIC or DIRICHLET");
         if (!std::isfinite(c->T_wall[i])) return bad(LBM_ERR_ARG, "T_wall must be finite");
@@ -164,11 +161,14 @@ inline lbm_status validate(const lbm_config *c, Layout *L, std::string *why)
                        "both faces of an axis must have the same flow kind (AA addressing)");
     }
     if (any_halo) {
-        const int n_outer = dim == 3 ? c->nz : c->ny;
-        const int ghosts = (c->face_flow[2 * outer] == LBM_FACE_HALO) +
-                           (c->face_flow[2 * outer + 1] == LBM_FACE_HALO);
-        if (n_outer < ghosts + 1)
-            return bad(LBM_ERR_ARG, "a slab needs at least one owned plane besides its ghosts");
+        const int n[3] = {c->nx, c->ny, c->nz};
+        for (int a = 0; a < dim; ++a) {
+            const int ghosts = (c->face_flow[2 * a] == LBM_FACE_HALO) +
+                               (c->face_flow[2 * a + 1] == LBM_FACE_HALO);
+            if (n[a] < ghosts + 1)
+                return bad(LBM_ERR_ARG,
+                           "a slab or block needs at least one owned plane besides its ghosts");
+        }
         if (c->streaming != LBM_STREAM_AA)
             return bad(LBM_ERR_UNSUPPORTED, "HALO faces need the AA layout");
         if (c->ib_max_samples > 0)
@@ -283,6 +283,13 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
     }
     P.ghost_lo = P.face_halo[2 * outer] ? 0 : -1;
     P.ghost_hi = P.face_halo[2 * outer + 1] ? n_outer - 1 : -1;
+    const int ext[3] = {g.nx, g.ny, g.nz};
+    P.ghost_inner = 0;
+    for (int a = 0; a < 3; ++a) {
+        P.ghost3_lo[a] = P.face_halo[2 * a] ? 0 : -1;
+        P.ghost3_hi[a] = P.face_halo[2 * a + 1] ? ext[a] - 1 : -1;
+        if (a != outer && (P.face_halo[2 * a] || P.face_halo[2 * a + 1])) P.ghost_inner = 1;
+    }
     P.plane_lo = 0;
     P.plane_hi = n_outer;
     // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)

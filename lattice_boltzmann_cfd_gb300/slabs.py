@@ -118,6 +118,13 @@ def ring_messages(rank: int, world: int, periodic: bool, send, recv, group=None)
     nbs = ring_neighbours(rank, world, periodic)
     if world == 1:
         return [(0, send[1]), (1, send[0])] if periodic else []
+    return halo_messages(nbs, send, recv, group)
+
+
+def halo_messages(nbs, send, recv, group=None):
+    """Send send[s] to rank nbs[s] and receive recv[s] from it, for each side s whose
+    neighbour is not None; returns [(side, buffer to unpack there)].  The messages are
+    tagged and posted as ring_messages describes."""
     import torch.distributed as dist
     ops = []
     for side in (0, 1):
@@ -451,6 +458,371 @@ class DistSlabDomain:
         ax = self.np_axis + lead
         idx[ax] = slice(1 if low else 0, t.shape[ax] - (1 if high else 0))
         return t[tuple(idx)]
+
+    def populations(self):
+        f, g = self.sim.populations()
+        return self.owned(f, 1), (None if g is None else self.owned(g, 1))
+
+    def macroscopic(self):
+        rho, u, T = self.sim.macroscopic()
+        return self.owned(rho), self.owned(u, 1), (None if T is None else self.owned(T))
+
+    def diagnostics(self) -> dict:
+        return self.sim.diagnostics(allow_nonfinite=True)
+
+    def close(self):
+        self.sim.close()
+
+
+# ------------------------------------------------------------------ block partitioning ---
+#
+# Block partitioning ("Multi-GPU thermal lattice Boltzmann simulations using OpenACC and
+# MPI", Sec. 4, Fig. 5): the domain is cut along several axes, each block with a ghost plane
+# at every face it shares with another block.  The exchange runs axis by axis (z, y, x), with
+# the whole plane of an axis moved, the ghost rows of the other axes included, so that the
+# populations of diagonal links reach the block across an edge or a corner through the
+# block beside it (lbm_halo_axis_pack / _unpack).
+
+def block_counts(shape, dim: int, parts: int):
+    """(bx, by, bz) with bx * by * bz = parts, following the pages' two rules: keep the rows
+    along x (the contiguous axis) whole where possible, and make the block extents as even
+    as possible.  In 3-D, x is split only when y and z cannot take every piece; among the
+    remaining splits the one whose blocks are closest to cubes (the smallest largest-to-
+    smallest extent ratio) wins, the outer axis taking the larger count on a tie.  A 2-D
+    domain cut into blocks is cut along x and y."""
+    best = None
+    for bz in (range(1, parts + 1) if dim == 3 else (1,)):
+        if parts % bz:
+            continue
+        for by in range(1, parts // bz + 1):
+            if (parts // bz) % by:
+                continue
+            bx = parts // (bz * by)
+            nb = (bx, by, bz)
+            if any(nb[a] > shape[a] for a in range(3)):
+                continue
+            ext = [shape[a] / nb[a] for a in range(dim)]
+            key = (dim == 3 and bx > 1, max(ext) / min(ext), -nb[dim - 1],
+                   -nb[1 if dim == 3 else 0])
+            if best is None or key < best[0]:
+                best = (key, nb)
+    if best is None:
+        raise ValueError(f"{parts} blocks do not fit the grid {tuple(shape)}")
+    return best[1]
+
+
+def block_index(bi, nb) -> int:
+    """Rank (or list position) of block bi = (i, j, k): x fastest."""
+    return bi[0] + nb[0] * (bi[1] + nb[1] * bi[2])
+
+
+def block_coords(b: int, nb):
+    return (b % nb[0], (b // nb[0]) % nb[1], b // (nb[0] * nb[1]))
+
+
+def block_part(w, nb, b: int):
+    """Block b of ``w`` cut into nb = (bx, by, bz) pieces: (local workload, per-axis (low,
+    high) ghost flags, per-axis list of the domain coordinate of each local plane).  An axis
+    split into two or more pieces gets ghost planes at its inner faces, and at both ends
+    when it is periodic (the pieces form a ring); its end blocks keep a wall face."""
+    if getattr(w, "ib_x", None) is not None and len(w.ib_x):
+        raise ValueError("blocks do not take immersed-boundary samples")
+    bi = block_coords(b, nb)
+    faces = list(w.face_flow)
+    shape = list(w.shape)
+    sides, coords = [], []
+    for a in range(3):
+        n = w.shape[a]
+        split = a < w.dim and nb[a] > 1
+        if a >= w.dim and nb[a] != 1:
+            raise ValueError("a 2-D domain has one block along z")
+        if split and nb[a] > n:
+            raise ValueError("more blocks than planes along an axis")
+        periodic = w.face_flow[2 * a] == "periodic"
+        lo, hi = split_ranges(n, nb[a])[bi[a]] if split else (0, n)
+        low = split and (periodic or bi[a] > 0)
+        high = split and (periodic or bi[a] < nb[a] - 1)
+        planes = ([(lo - 1) % n] if low else []) + list(range(lo, hi)) + \
+                 ([hi % n] if high else [])
+        if low:
+            faces[2 * a] = "halo"
+        if high:
+            faces[2 * a + 1] = "halo"
+        shape[a] = len(planes)
+        sides.append((low, high))
+        coords.append(planes)
+    sel = np.ix_(coords[2], coords[1], coords[0])     # fields are (nz, ny, nx)
+
+    def take(a, lead=0):
+        if a is None:
+            return None
+        return np.ascontiguousarray(a[(slice(None),) * lead + sel])
+
+    local = dataclasses.replace(
+        w, shape=tuple(shape), face_flow=tuple(faces), solid=take(w.solid),
+        rho0=take(w.rho0), u0=take(w.u0, 1), T_init=take(w.T_init))
+    return local, sides, coords
+
+
+def block_neighbours(b: int, nb, periodic):
+    """Per axis, the (low, high) neighbour block indices of block b (None at the end of a
+    walled axis or along an axis that is not split).  periodic: per axis."""
+    bi = block_coords(b, nb)
+    out = []
+    for a in range(3):
+        if nb[a] < 2:
+            out.append((None, None))
+            continue
+        nbs = []
+        for d in (-1, 1):
+            j = list(bi)
+            j[a] += d
+            if 0 <= j[a] < nb[a]:
+                nbs.append(block_index(j, nb))
+            elif periodic[a]:
+                j[a] %= nb[a]
+                nbs.append(block_index(j, nb))
+            else:
+                nbs.append(None)
+        out.append(tuple(nbs))
+    return out
+
+
+def exchange_axes(dim: int, nb):
+    """The axes a block exchange runs through, in order: z, y, x, those split only."""
+    return [a for a in range(dim - 1, -1, -1) if nb[a] > 1]
+
+
+def block_exchange(b: int, nb, periodic, dim: int, phase: int, pack, unpack, send, recv,
+                   group=None, sync=None):
+    """One halo exchange of block ``b`` (its torch.distributed rank) with its neighbours:
+    per axis in exchange_axes order, the packs, the messages (halo_messages), then the
+    unpacks, before the next axis starts.  pack(axis, side, phase, buf) fills
+    send[axis][side]; unpack(axis, side, phase, buf) consumes a buffer; sync(), if given,
+    runs after each axis's packs and after its receives."""
+    nbs = block_neighbours(b, nb, periodic)
+    for a in exchange_axes(dim, nb):
+        for side in (0, 1):
+            if nbs[a][side] is not None:
+                pack(a, side, phase, send[a][side])
+        if sync is not None:
+            sync()
+        arrived = halo_messages(nbs[a], send[a], recv[a], group)
+        if sync is not None:
+            sync()
+        for side, buf in arrived:
+            unpack(a, side, phase, buf)
+
+
+def owned_slices(sides, coords, lead=0):
+    """Index of a block's owned cells in a local field with ``lead`` leading axes."""
+    idx = [slice(None)] * lead
+    for a in (2, 1, 0):
+        low, high = sides[a]
+        idx.append(slice(1 if low else 0, len(coords[a]) - (1 if high else 0)))
+    return tuple(idx)
+
+
+class BlockDomain:
+    """The workload ``w`` cut into nb = (bx, by, bz) blocks (block_counts picks nb for a
+    number of pieces), block b on ``devices[b % len(devices)]``, all driven from this
+    process.  Each step is followed by the exchange of every split axis, z then y then x;
+    between steps every owned cell holds what one undivided domain would hold."""
+
+    def __init__(self, w, nb, devices=None):
+        import torch
+        nb = tuple(int(v) for v in nb)
+        if len(nb) != 3 or min(nb) < 1:
+            raise ValueError("nb must be three positive block counts")
+        self.w, self.nb, self.dim = w, nb, w.dim
+        self.periodic = [w.face_flow[2 * a] == "periodic" for a in range(3)]
+        devices = list(devices) if devices else [torch.device("cuda")]
+        self.blocks, self.sides, self.coords, self.buffers = [], [], [], []
+        for b in range(nb[0] * nb[1] * nb[2]):
+            local, sides, coords = block_part(w, nb, b)
+            sim = Simulation(local, device=devices[b % len(devices)])
+            bufs = []
+            for a in range(3):
+                if a < w.dim and nb[a] > 1:
+                    nfloat = capi.lbm_halo_axis_bytes(sim.ctx, a) // 4
+                    bufs.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
+                                 for _ in range(2)])
+                else:
+                    bufs.append(None)
+            self.blocks.append(sim)
+            self.sides.append(sides)
+            self.coords.append(coords)
+            self.buffers.append(bufs)
+        self.multi_device = len({s.device for s in self.blocks}) > 1
+
+    @property
+    def parity(self) -> int:
+        return self.blocks[0].parity
+
+    def pairs(self, a: int):
+        """(block, its high neighbour along axis a) for every face between blocks."""
+        out = []
+        for b in range(len(self.blocks)):
+            hi = block_neighbours(b, self.nb, self.periodic)[a][1]
+            if hi is not None:
+                out.append((b, hi))
+        return out
+
+    def _sync(self):
+        import torch
+        if self.multi_device:
+            for d in {s.device for s in self.blocks}:
+                torch.cuda.synchronize(d)
+
+    def _exchange(self, phase: int):
+        for a in exchange_axes(self.dim, self.nb):
+            pairs = self.pairs(a)
+            for lo, hi in pairs:
+                capi.lbm_halo_axis_pack(self.blocks[lo].ctx, a, 1, phase, self.buffers[lo][a][1])
+                capi.lbm_halo_axis_pack(self.blocks[hi].ctx, a, 0, phase, self.buffers[hi][a][0])
+            self._sync()
+            for lo, hi in pairs:
+                to_lo = self.buffers[hi][a][0].to(self.blocks[lo].device)
+                to_hi = self.buffers[lo][a][1].to(self.blocks[hi].device)
+                capi.lbm_halo_axis_unpack(self.blocks[lo].ctx, a, 1, phase, to_lo)
+                capi.lbm_halo_axis_unpack(self.blocks[hi].ctx, a, 0, phase, to_hi)
+            self._sync()
+
+    def init_equilibrium(self):
+        """Every block from the workload's initial fields (its ghost planes included)."""
+        import torch
+        for sim, coords in zip(self.blocks, self.coords):
+            sel = np.ix_(coords[2], coords[1], coords[0])
+
+            def dev(a, lead=0):
+                if a is None:
+                    return None
+                t = np.ascontiguousarray(a[(slice(None),) * lead + sel])
+                return torch.from_numpy(t).to(sim.device)
+            sim.init_equilibrium(dev(self.w.rho0), dev(self.w.u0, 1), dev(self.w.T_init))
+
+    def step(self, n: int = 1):
+        """n time steps, each followed by its exchange (FILL after even, DRAIN after odd)."""
+        for _ in range(n):
+            for sim in self.blocks:
+                sim.step(1)
+            self._exchange(capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN)
+
+    def _gather(self, parts, lead=0):
+        import torch
+        dev = self.blocks[0].device
+        out = None
+        for t, sides, coords in zip(parts, self.sides, self.coords):
+            own = t[owned_slices(sides, coords, lead)].to(dev)
+            if out is None:
+                out = torch.empty(tuple(t.shape[:lead]) + self.w.grid, dtype=t.dtype,
+                                  device=dev)
+            lo = []
+            for a in (2, 1, 0):
+                first = coords[a][1 if sides[a][0] else 0]
+                lo.append(slice(first, first + own.shape[lead + 2 - a]))
+            out[(slice(None),) * lead + tuple(lo)] = own
+        return out
+
+    def populations(self):
+        """Logical populations of the whole domain, (Q, nz, ny, nx), ghost planes dropped."""
+        pops = [sim.populations() for sim in self.blocks]
+        f = self._gather([p[0] for p in pops], 1)
+        g = self._gather([p[1] for p in pops], 1) if pops[0][1] is not None else None
+        return f, g
+
+    def macroscopic(self):
+        """rho, u, T of the whole domain (T is None without a thermal lattice)."""
+        fields = [sim.macroscopic() for sim in self.blocks]
+        rho = self._gather([m[0] for m in fields])
+        u = self._gather([m[1] for m in fields], 1)
+        T = self._gather([m[2] for m in fields]) if fields[0][2] is not None else None
+        return rho, u, T
+
+    def diagnostics(self) -> dict:
+        """Sums over the blocks (each block leaves its ghost cells out)."""
+        ds = [sim.diagnostics(allow_nonfinite=True) for sim in self.blocks]
+        total = lambda key: [float(v) for v in np.sum([d[key] for d in ds], axis=0)]
+        return {"mass": sum(d["mass"] for d in ds), "momentum": total("momentum"),
+                "force": total("force"), "heat": total("heat"),
+                "fluid_cells": sum(d["fluid_cells"] for d in ds),
+                "finite": all(d["finite"] for d in ds)}
+
+    def halo_bytes_per_step(self) -> float:
+        """Bytes the exchanges move between blocks per time step (both ways, every face)."""
+        return float(sum(2 * self.buffers[lo][a][1].numel() * 4
+                         for a in exchange_axes(self.dim, self.nb) for lo, _ in self.pairs(a)))
+
+    def close(self):
+        for sim in self.blocks:
+            sim.close()
+
+
+class DistBlockDomain:
+    """Block ``rank`` of ``w`` cut into nb = (bx, by, bz) blocks, one per torch.distributed
+    rank (world = bx * by * bz).  Each step is followed by block_exchange: per split axis,
+    z then y then x, the packs, the messages to the two neighbours along that axis, and the
+    unpacks.  ``transport`` as for DistSlabDomain: "device" buffers handed to the process
+    group on the compute stream (NCCL), or "host" page-locked buffers (gloo), where the host
+    waits for each axis's packs before sending."""
+
+    def __init__(self, w, nb, rank: int, world: int, device=None, group=None,
+                 transport: str = "device"):
+        import torch
+        nb = tuple(int(v) for v in nb)
+        if nb[0] * nb[1] * nb[2] != world:
+            raise ValueError("the block counts must multiply to the world size")
+        if transport not in ("device", "host"):
+            raise ValueError("transport must be 'device' or 'host'")
+        self.w, self.nb, self.rank, self.world, self.group = w, nb, rank, world, group
+        self.transport = transport
+        self.periodic = [w.face_flow[2 * a] == "periodic" for a in range(3)]
+        self.local, self.sides, self.coords = block_part(w, nb, rank)
+        dev = torch.device(device if device is not None else "cuda")
+        self.sim = Simulation(self.local, device=dev)
+        self.send, self.recv = [], []
+        for a in range(3):
+            if a < w.dim and nb[a] > 1:
+                nfloat = capi.lbm_halo_axis_bytes(self.sim.ctx, a) // 4
+                if transport == "host":
+                    new = lambda: torch.empty(nfloat, dtype=torch.float32).pin_memory()
+                else:
+                    new = lambda: torch.empty(nfloat, dtype=torch.float32, device=dev)
+                self.send.append([new(), new()])
+                self.recv.append([new(), new()])
+            else:
+                self.send.append(None)
+                self.recv.append(None)
+
+    @property
+    def parity(self) -> int:
+        return self.sim.parity
+
+    def init_equilibrium(self):
+        import torch
+        dev = lambda a: None if a is None else torch.from_numpy(a).to(self.sim.device)
+        self.sim.init_equilibrium(dev(self.local.rho0), dev(self.local.u0),
+                                  dev(self.local.T_init))
+
+    def step(self, n: int = 1):
+        import torch
+        stream = torch.cuda.current_stream(self.sim.device)
+        # host buffers: the host waits for the packs before sending, and the unpacks may
+        # not overwrite a receive buffer that the next axis reuses before it is read
+        sync = (lambda: stream.synchronize()) if self.transport == "host" else None
+        for _ in range(n):
+            self.sim.step(1)
+            phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
+            block_exchange(self.rank, self.nb, self.periodic, self.w.dim, phase,
+                           lambda a, s, p, buf: capi.lbm_halo_axis_pack(self.sim.ctx, a, s, p, buf),
+                           lambda a, s, p, buf: capi.lbm_halo_axis_unpack(self.sim.ctx, a, s, p, buf),
+                           self.send, self.recv, self.group, sync)
+        if sync is not None:
+            sync()
+
+    def owned(self, t, lead=0):
+        """The owned cells of a local field (ghost planes dropped)."""
+        return t[owned_slices(self.sides, self.coords, lead)]
 
     def populations(self):
         f, g = self.sim.populations()

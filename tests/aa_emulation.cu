@@ -151,7 +151,7 @@ struct Domain {
                         const int idx = x + cfg.nx * (y + cfg.ny * z);
                         mask[idx] = m;
                         // the mask the kernels compute must equal the built one off the ghosts
-                        if (Lay.ib_cap == 0 && !ghost_plane<L>(P, y, z) &&
+                        if (Lay.ib_cap == 0 && !ghost_plane<L>(P, x, y, z) &&
                             boxed_mask<L, TL>(P, idx, x, y, z) != m)
                             ++face_mask_mismatches;
                     }
@@ -285,11 +285,13 @@ struct Domain {
         }
     }
 
-    // The library's per-cell halo function over one side's plane.
-    void halo(int side, int phase, int unpack, float *buf)
+    // The library's per-cell halo function over one side's plane of an axis.
+    void halo(int axis, int side, int phase, int unpack, float *buf)
     {
-        const int plane_cells = L::DIM == 3 ? cfg.nx * cfg.ny : cfg.nx;
-        for (int i = 0; i < plane_cells; ++i) halo_cell<L, TL>(P, side, phase, unpack, buf, i);
+        const int n[3] = {cfg.nx, cfg.ny, cfg.nz};
+        const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
+        for (int i = 0; i < plane_cells; ++i)
+            halo_cell<L, TL>(P, axis, side, phase, unpack, buf, i);
     }
 };
 
@@ -376,12 +378,12 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
         for (auto &d : doms) d->step();
         const int phase = doms[0]->parity == 1 ? LBM_HALO_FILL : LBM_HALO_DRAIN;
         for (auto [a, b] : pairs) {
-            doms[a]->halo(1, phase, 0, bufs[a][1].data());
-            doms[b]->halo(0, phase, 0, bufs[b][0].data());
+            doms[a]->halo(outer, 1, phase, 0, bufs[a][1].data());
+            doms[b]->halo(outer, 0, phase, 0, bufs[b][0].data());
         }
         for (auto [a, b] : pairs) {
-            doms[a]->halo(1, phase, 1, bufs[b][0].data());
-            doms[b]->halo(0, phase, 1, bufs[a][1].data());
+            doms[a]->halo(outer, 1, phase, 1, bufs[b][0].data());
+            doms[b]->halo(outer, 0, phase, 1, bufs[a][1].data());
         }
     }
     for (auto &d : doms)
@@ -401,6 +403,142 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
                 for (int q = 0; q < QT; ++q) gout[q * N + gi] = lg[q * Nl + li];
             }
         }
+    }
+    return 0;
+}
+
+// The domain split into blocks: nb[a] pieces along axis a at planes edges[a][0..nb[a]].
+// A block has a ghost plane at each face along a split axis that meets another block
+// (every face of a split periodic axis).  After every step the blocks exchange axis by
+// axis, z, then y, then x, each axis's unpacks done before the next axis's packs: a plane
+// of a later axis includes the ghost rows that the earlier axes just filled or drained, so
+// the populations of diagonal links reach the block across an edge or a corner in two or
+// three hops.  The owned cells' logical populations are gathered into fout, gout.
+template <class L, class TL, int C, bool NARROW>
+int run_blocks(const lbm_config &cfg, const float *rho, const float *u, const float *T,
+               int steps, const int *nb, const int *const *edges, int ordered, float *fout,
+               float *gout)
+{
+    using Dom = Domain<L, TL, C, NARROW>;
+    const int dim = L::DIM;
+    const int n[3] = {cfg.nx, cfg.ny, cfg.nz};
+    const size_t N = (size_t)n[0] * n[1] * n[2];
+    const int halo_dirs = L::Q == 27 ? 9 : (L::Q == 19 ? 5 : 3) + (TL::Q ? 1 : 0);
+    const int nblocks = nb[0] * nb[1] * nb[2];
+    struct Block {
+        std::unique_ptr<Dom> d;
+        std::vector<int> coords[3];   // global coordinate of each local index, per axis
+        int bi[3], owned_lo[3], owned_hi[3], ext[3];
+        bool low[3], high[3];
+        std::vector<uint8_t> sol;
+    };
+    std::vector<Block> blocks(nblocks);
+    auto block_at = [&](int i, int j, int k) { return i + nb[0] * (j + nb[1] * k); };
+    for (int b = 0; b < nblocks; ++b) {
+        Block &B = blocks[b];
+        B.bi[0] = b % nb[0];
+        B.bi[1] = (b / nb[0]) % nb[1];
+        B.bi[2] = b / (nb[0] * nb[1]);
+        lbm_config lc = cfg;
+        for (int a = 0; a < 3; ++a) {
+            const bool split = a < dim && nb[a] > 1;
+            const bool periodic = cfg.face_flow[2 * a] == LBM_FACE_PERIODIC;
+            const int lo = split ? edges[a][B.bi[a]] : 0;
+            const int hi = split ? edges[a][B.bi[a] + 1] : n[a];
+            B.low[a] = split && (periodic || B.bi[a] > 0);
+            B.high[a] = split && (periodic || B.bi[a] < nb[a] - 1);
+            if (B.low[a]) B.coords[a].push_back((lo - 1 + n[a]) % n[a]);
+            for (int p = lo; p < hi; ++p) B.coords[a].push_back(p);
+            if (B.high[a]) B.coords[a].push_back(hi % n[a]);
+            B.ext[a] = (int)B.coords[a].size();
+            B.owned_lo[a] = B.low[a] ? 1 : 0;
+            B.owned_hi[a] = B.owned_lo[a] + (hi - lo);
+            if (B.low[a]) lc.face_flow[2 * a] = LBM_FACE_HALO;
+            if (B.high[a]) lc.face_flow[2 * a + 1] = LBM_FACE_HALO;
+        }
+        lc.nx = B.ext[0];
+        lc.ny = B.ext[1];
+        lc.nz = B.ext[2];
+        const size_t Nl = (size_t)B.ext[0] * B.ext[1] * B.ext[2];
+        std::vector<float> lr(Nl), lu((size_t)dim * Nl), lT(Nl);
+        if (cfg.solid_mask) B.sol.resize(Nl);
+        for (int k = 0; k < B.ext[2]; ++k)
+            for (int j = 0; j < B.ext[1]; ++j)
+                for (int i = 0; i < B.ext[0]; ++i) {
+                    const size_t li = i + (size_t)B.ext[0] * (j + (size_t)B.ext[1] * k);
+                    const size_t gi = B.coords[0][i] +
+                                      (size_t)n[0] * (B.coords[1][j] + (size_t)n[1] * B.coords[2][k]);
+                    if (cfg.solid_mask) B.sol[li] = cfg.solid_mask[gi];
+                    lr[li] = rho[gi];
+                    for (int a = 0; a < dim; ++a) lu[a * Nl + li] = u[a * N + gi];
+                    if (T) lT[li] = T[gi];
+                }
+        lc.solid_mask = cfg.solid_mask ? B.sol.data() : nullptr;
+        lbm_setup::Layout Lay;
+        std::string why;
+        if (lbm_setup::validate(&lc, &Lay, &why) != LBM_OK) return -10 - b;
+        B.d = std::make_unique<Dom>(lc, Lay);
+        if (B.d->face_mask_mismatches) return -40 - b;
+        B.d->init(lr.data(), lu.data(), T ? lT.data() : nullptr);
+    }
+    // one axis's packed buffers: (lower block, upper block, [lower's high side, upper's low])
+    struct Exchange {
+        int axis, lo, hi;
+        std::array<std::vector<float>, 2> buf;
+    };
+    for (int s = 0; s < steps; ++s) {
+        for (auto &B : blocks) B.d->step();
+        const int phase = blocks[0].d->parity == 1 ? LBM_HALO_FILL : LBM_HALO_DRAIN;
+        std::vector<Exchange> held;   // ordered == 0: every axis packs before any unpacks
+        auto unpack = [&](std::vector<Exchange> &xs) {
+            for (auto &x : xs) {
+                blocks[x.lo].d->halo(x.axis, 1, phase, 1, x.buf[1].data());
+                blocks[x.hi].d->halo(x.axis, 0, phase, 1, x.buf[0].data());
+            }
+        };
+        for (int a = dim - 1; a >= 0; --a) {
+            if (nb[a] < 2) continue;
+            // pairs (block, its high neighbour along a), with the wrap on a periodic axis
+            std::vector<std::pair<int, int>> pairs;
+            for (int b = 0; b < nblocks; ++b) {
+                const Block &B = blocks[b];
+                if (!B.high[a]) continue;
+                int j[3] = {B.bi[0], B.bi[1], B.bi[2]};
+                j[a] = (j[a] + 1) % nb[a];
+                pairs.push_back({b, block_at(j[0], j[1], j[2])});
+            }
+            const int u0 = a == 0 ? 1 : 0, v0 = a == 2 ? 1 : 2;
+            std::vector<Exchange> xs;
+            for (const auto [lo, hi] : pairs) {
+                const Block &B = blocks[lo];
+                const size_t cells = (size_t)B.ext[u0] * B.ext[v0];
+                Exchange x{a, lo, hi, {}};
+                x.buf[0].assign(halo_dirs * cells, 0.0f);
+                x.buf[1].assign(halo_dirs * cells, 0.0f);
+                blocks[lo].d->halo(a, 1, phase, 0, x.buf[0].data());
+                blocks[hi].d->halo(a, 0, phase, 0, x.buf[1].data());
+                xs.push_back(std::move(x));
+            }
+            if (ordered) unpack(xs);
+            else for (auto &x : xs) held.push_back(std::move(x));
+        }
+        unpack(held);
+    }
+    const int QT = TL::Q;
+    for (const Block &B : blocks) {
+        if (B.d->guard_violations) return -32;
+        const size_t Nl = B.d->Lay.N;
+        std::vector<float> lf((size_t)L::Q * Nl), lg((size_t)(QT ? QT : 1) * Nl);
+        B.d->read(lf.data(), lg.data());
+        for (int k = B.owned_lo[2]; k < B.owned_hi[2]; ++k)
+            for (int j = B.owned_lo[1]; j < B.owned_hi[1]; ++j)
+                for (int i = B.owned_lo[0]; i < B.owned_hi[0]; ++i) {
+                    const size_t li = i + (size_t)B.ext[0] * (j + (size_t)B.ext[1] * k);
+                    const size_t gi = B.coords[0][i] +
+                                      (size_t)n[0] * (B.coords[1][j] + (size_t)n[1] * B.coords[2][k]);
+                    for (int q = 0; q < L::Q; ++q) fout[q * N + gi] = lf[q * Nl + li];
+                    for (int q = 0; q < QT; ++q) gout[q * N + gi] = lg[q * Nl + li];
+                }
     }
     return 0;
 }
@@ -521,7 +659,7 @@ long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
         for (size_t i = 0; i < d.f.size(); ++i) d.f[i] = (float)i;
         for (size_t i = 0; i < d.g.size(); ++i) d.g[i] = -1.0f - (float)i;
         std::fill(buf.begin(), buf.end(), nan);
-        d.halo(side, phase, 0, buf.data());
+        d.halo(outer, side, phase, 0, buf.data());
         for (float v : buf)
             if (!std::isnan(v)) touched.push_back((long long)v);
         d.f = f0;
@@ -530,7 +668,7 @@ long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
         const float mark = 1.0e30f;
         std::fill(buf.begin(), buf.end(), mark);
         for (auto *v : {&d.f, &d.g}) std::fill(v->begin(), v->end(), 0.0f);
-        d.halo(side, phase, 1, buf.data());
+        d.halo(outer, side, phase, 1, buf.data());
         for (size_t i = 0; i < d.f.size(); ++i)
             if (d.f[i] == mark) touched.push_back((long long)i);
         for (size_t i = 0; i < d.g.size(); ++i)
@@ -697,6 +835,35 @@ extern "C" int emu_run_slabs(const lbm_config *cfg, const float *rho, const floa
                    : run_slabs<D2Q9, D2Q5, 0, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
     return mrt ? run_slabs<D2Q9, NoThermal, 1, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout)
                : run_slabs<D2Q9, NoThermal, 0, true>(*cfg, rho, u, T, steps, nslabs, edges, fout, gout);
+}
+
+// Block decomposition of the whole domain cfg (AA layout), see run_blocks: nb[3] pieces per
+// axis, edges the concatenated plane lists (nb[0] + 1 entries for x, then y, then z).
+// ordered = 0 packs every axis before any unpack (the diagonal hops then have nothing to
+// carry): a negative control for the tests.
+extern "C" int emu_run_blocks(const lbm_config *cfg, const float *rho, const float *u,
+                              const float *T, int steps, const int *nb, const int *edges,
+                              int ordered, float *fout, float *gout)
+{
+    lbm_setup::Layout Lay;
+    std::string why;
+    if (lbm_setup::validate(cfg, &Lay, &why) != LBM_OK) return -1;
+    if (cfg->streaming != LBM_STREAM_AA) return -2;
+    for (int a = 0; a < 3; ++a)
+        if (nb[a] < 1) return -3;
+    const int *e[3] = {edges, edges + nb[0] + 1, edges + nb[0] + nb[1] + 2};
+    const bool mrt = cfg->collision == LBM_MRT;
+#define LBM_EMU_BLOCKS(Lt, Tt, Ct) run_blocks<Lt, Tt, Ct, true>(*cfg, rho, u, T, steps, nb, e, ordered, fout, gout)
+    if (cfg->lattice == 27) return LBM_EMU_BLOCKS(D3Q27, NoThermal, 2);
+    if (cfg->lattice == 19) {
+        if (cfg->thermal == 7)
+            return mrt ? LBM_EMU_BLOCKS(D3Q19, D3Q7, 1) : LBM_EMU_BLOCKS(D3Q19, D3Q7, 0);
+        return mrt ? LBM_EMU_BLOCKS(D3Q19, NoThermal, 1) : LBM_EMU_BLOCKS(D3Q19, NoThermal, 0);
+    }
+    if (cfg->thermal == 5)
+        return mrt ? LBM_EMU_BLOCKS(D2Q9, D2Q5, 1) : LBM_EMU_BLOCKS(D2Q9, D2Q5, 0);
+    return mrt ? LBM_EMU_BLOCKS(D2Q9, NoThermal, 1) : LBM_EMU_BLOCKS(D2Q9, NoThermal, 0);
+#undef LBM_EMU_BLOCKS
 }
 
 // Every neighbour index the odd-step access pattern forms (idx + offset of +-c_q for each

@@ -130,6 +130,33 @@ def emulate_slabs(emu_lib, w, steps, nslabs):
     return fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid)
 
 
+def emulate_blocks(emu_lib, w, steps, nb, edges=None, ordered=True):
+    """(f, g) of the whole domain after ``steps`` steps of the host emulation run as
+    nb = (bx, by, bz) blocks with the library's per-axis halo exchange.  edges: per axis the
+    block boundaries (default: as even as possible).  ordered=False packs every axis before
+    any unpack (a negative control)."""
+    from lattice_boltzmann_cfd_gb300.slabs import split_ranges
+    cfg, keep = make_config(w, "aa")
+    N = w.cells
+    fo = np.full((w.lattice, N), np.nan, np.float32)
+    go = np.full((max(w.thermal, 1), N), np.nan, np.float32)
+    rho = np.ascontiguousarray(w.rho0, np.float32)
+    u = np.ascontiguousarray(w.u0, np.float32)
+    T = np.ascontiguousarray(w.T_init, np.float32) if w.thermal else None
+    if edges is None:
+        edges = []
+        for a in range(3):
+            r = split_ranges(w.shape[a], nb[a])
+            edges.append([x[0] for x in r] + [r[-1][1]])
+    flat = np.array([e for a in range(3) for e in edges[a]], np.int32)
+    nbs = np.array(nb, np.int32)
+    vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = emu_lib.emu_run_blocks(ctypes.byref(cfg), vp(rho), vp(u), vp(T), int(steps), vp(nbs),
+                                vp(flat), int(bool(ordered)), vp(fo), vp(go))
+    assert rc == 0, rc
+    return fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid)
+
+
 def slab_cases():
     """Problems whose outer axis is periodic (the slabs form a ring) or walled, with solid
     cells and thermal Dirichlet faces on both kinds of axis."""

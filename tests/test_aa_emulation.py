@@ -10,8 +10,8 @@ parity-aware.  The link mask is compared bit for bit with a brute-force builder.
 import numpy as np
 import pytest
 
-from parity_util import (box_edge_cases, degenerate_cases, emulate, emulate_loaded_mask,
-                         emulate_slabs, faces_only_cases, fluid_of, mask_brute_force,
+from parity_util import (box_edge_cases, degenerate_cases, emulate, emulate_blocks,
+                         emulate_loaded_mask, emulate_slabs, faces_only_cases, fluid_of, mask_brute_force,
                          oracle_states, outer_walls_case, slab_cases, small_cases)
 
 CASES = small_cases()
@@ -84,6 +84,71 @@ def test_slabs_match_single_domain_bitwise(oracle_mod, emu_lib, w):
             if w.thermal:
                 assert not np.isnan(gs).any(), (n, k)
                 assert np.array_equal(gs, g1), (n, k)
+
+
+# ------------------------------------------------------------ block decomposition ---
+
+def _block_layouts(w):
+    """Splits along two and three axes, with one-plane blocks and ragged ends."""
+    if w.dim == 2:
+        return [(2, 2, 1), (3, 2, 1), (w.shape[0], 1, 1), (2, w.shape[1], 1)]
+    return [(2, 2, 1), (1, 2, 2), (2, 1, 3), (2, 2, 2), (3, 3, 2)]
+
+
+@pytest.mark.parametrize("w", SLAB_CASES, ids=[c.name for c in SLAB_CASES])
+def test_blocks_match_single_domain_bitwise(emu_lib, w):
+    """The domain run as blocks split along several axes, exchanging axis by axis (z, y, x)
+    after every step, holds bit for bit the single domain's state at both parities.  The
+    links that cross a block's edge or corner go to the diagonal neighbour through the ghost
+    rows of the axis exchanged before, so a missing hop would leave a NaN or a stale value
+    at the cells along the edges."""
+    for n in (1, 2, 5, 6):
+        f1, g1, _ = emulate(emu_lib, w, n)
+        for nb in _block_layouts(w):
+            fb, gb = emulate_blocks(emu_lib, w, n, nb)
+            assert not np.isnan(fb).any(), (n, nb)
+            assert np.array_equal(fb, f1), (n, nb)
+            if w.thermal:
+                assert not np.isnan(gb).any(), (n, nb)
+                assert np.array_equal(gb, g1), (n, nb)
+
+
+def test_blocks_along_the_slab_axis_equal_slabs(emu_lib):
+    """Blocks split along the outer axis only are slabs: both runners agree bit for bit."""
+    w = SLAB_CASES[0]
+    for n in (3, 4):
+        fs, _ = emulate_slabs(emu_lib, w, n, 3)
+        fb, _ = emulate_blocks(emu_lib, w, n, (1, 1, 3))
+        assert np.array_equal(fs, fb)
+
+
+@pytest.mark.parametrize("w", [SLAB_CASES[0], SLAB_CASES[5], SLAB_CASES[7]],
+                         ids=["periodic", "cavity3d-solid", "cavity2d"])
+def test_blocks_catch_a_missing_diagonal_hop(emu_lib, w):
+    """Negative control: packing every axis before any unpack drops the second hop of the
+    diagonal links, and the state differs from the single domain, but only next to the
+    block edges (the cells off them still agree)."""
+    nb = (2, 2, 1) if w.dim == 2 else (1, 2, 2)
+    f1, _, _ = emulate(emu_lib, w, 2)
+    fb, _ = emulate_blocks(emu_lib, w, 2, nb, ordered=False)
+    bad = ~(fb == f1).all(axis=0)          # per cell (z, y, x)
+    assert bad.any()
+    # the split axes' block boundaries, as (array axis, planes next to a boundary)
+    from lattice_boltzmann_cfd_gb300.slabs import split_ranges
+    near = np.zeros(w.grid, bool)
+    for a in range(3):
+        if nb[a] < 2:
+            continue
+        ax = 2 - a
+        r = split_ranges(w.shape[a], nb[a])
+        cuts = [x[0] for x in r] + [r[-1][1]]
+        planes = {(c + d) % w.shape[a] for c in cuts for d in (-2, -1, 0, 1)}
+        idx = [slice(None)] * near.ndim
+        idx[ax] = sorted(planes)
+        m = np.zeros(w.grid, bool)
+        m[tuple(idx)] = True
+        near |= m
+    assert not (bad & ~near).any()
 
 
 DEGENERATE = degenerate_cases()

@@ -100,15 +100,19 @@ def test_bad_3d_configs_rejected(capi, overrides, status, text):
 
 
 @pytest.mark.parametrize("lattice,faces,extra,text", [
-    (19, [2, 2, 0, 0, 0, 0], {}, "outer axis"),               # HALO on x
     (19, [0, 0, 0, 0, 0, 2], {}, "same flow kind"),           # periodic paired with HALO
+    (19, [0, 2, 0, 0, 0, 0], {}, "same flow kind"),           # the same on x
     (19, [0, 0, 0, 0, 2, 2], {"streaming": 1}, "AA layout"),  # PULL layout
+    (19, [2, 2, 0, 0, 0, 0], {"streaming": 2}, "AA layout"),
     (19, [0, 0, 0, 0, 2, 2], {"ib_max_samples": 4}, "immersed"),
     (19, [0, 0, 0, 0, 2, 2], {"nz": 2}, "owned plane"),      # ghosts only
+    (19, [2, 2, 0, 0, 0, 0], {"nx": 2}, "owned plane"),
+    (19, [1, 2, 2, 2, 0, 0], {"ny": 2}, "owned plane"),
     (9, [1, 1, 2, 1, 0, 0], {"ny": 1}, "owned plane"),
+    (9, [2, 2, 1, 1, 0, 0], {"nx": 2}, "owned plane"),
 ])
 def test_halo_faces_validated(capi, lattice, faces, extra, text):
-    """HALO faces: outer axis only, never paired with a wrap, AA layout only, no immersed
+    """HALO faces (on any axis): never paired with a wrap, AA layout only, no immersed
     samples, and at least one owned plane besides the ghosts."""
     w = (W.random_periodic(shape=(8, 6, 5)) if lattice == 19
          else W.random_periodic(shape=(8, 6, 1), lattice=9))
@@ -124,6 +128,10 @@ def test_halo_faces_accepted(capi):
     assert _bytes(capi, w2, face_flow=[1, 1, 2, 1, 0, 0]) > 0
     # the z faces of a 2-D problem are not read, whatever they hold
     assert _bytes(capi, w2, face_flow=[1, 1, 1, 1, 2, 2]) > 0
+    # blocks: HALO faces on several axes, mixed with walls
+    assert _bytes(capi, w, face_flow=[2, 2, 2, 1, 2, 2]) > 0
+    assert _bytes(capi, w, face_flow=[1, 2, 0, 0, 2, 1], nx=2) > 0
+    assert _bytes(capi, w2, face_flow=[2, 2, 2, 2, 0, 0]) > 0
 
 
 def test_buoyancy_needs_thermal(capi):

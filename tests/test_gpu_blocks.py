@@ -1,0 +1,254 @@
+"""Block partitioning (the domain cut along several axes) with the per-axis halo exchange,
+on the GPU through the C ABI.
+
+The blocks together must hold bit for bit the state of one domain run with the same kernels,
+at both AA parities, and match the fp64 oracle run on the undivided domain.  A block whose
+faces are all HALO or periodic and which holds no solid cell runs the unmasked kernels even
+when the undivided domain (which has walls) runs the masked ones; where that mixes the two
+kernel families the comparison with the undivided domain is within fp32 rounding instead
+of bitwise (the oracle comparison is the same either way).
+"""
+import dataclasses
+import datetime
+import os
+import socket
+
+import numpy as np
+import pytest
+
+from lattice_boltzmann_cfd_gb300 import capi
+from lattice_boltzmann_cfd_gb300 import workloads as W
+from parity_util import TOL_FIELDS, compare_fields, oracle_states, outer_walls_case, slab_cases
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    capi.load()
+
+
+def _dev(a):
+    return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _single(w, steps):
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    sim = Simulation(w)
+    sim.init_equilibrium(_dev(w.rho0), _dev(w.u0), _dev(w.T_init))
+    sim.step(steps)
+    f, g = sim.populations()
+    out = (f.cpu().numpy(), None if g is None else g.cpu().numpy(), sim.diagnostics())
+    sim.close()
+    return out
+
+
+def _masked(w):
+    return any(k == "wall" for k in w.face_flow[:2 * w.dim]) or (
+        w.solid is not None and bool(w.solid.any()))
+
+
+def _same_family(w, nb):
+    """Every block runs the kernel family of the undivided domain."""
+    from lattice_boltzmann_cfd_gb300.slabs import block_part
+    want = _masked(w)
+    return all(_masked(block_part(w, nb, b)[0]) == want for b in range(nb[0] * nb[1] * nb[2]))
+
+
+def _blocks(w, nb, chunks):
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    dom = BlockDomain(w, nb)
+    dom.init_equilibrium()
+    for c in chunks:
+        dom.step(c)
+    f, g = dom.populations()
+    rho, u, T = dom.macroscopic()
+    got = {"rho": rho.cpu().numpy(), "u": u.cpu().numpy(),
+           "T": None if T is None else T.cpu().numpy(), "f": f.cpu().numpy(),
+           "g": None if g is None else g.cpu().numpy()}
+    d = dom.diagnostics()
+    dom.close()
+    return got, d
+
+
+def _large_cases():
+    """Grids spanning several thread blocks along x with ragged tails."""
+    rp = W.random_periodic(shape=(300, 20, 23), seed=81)
+    cs = W.perturbed(W.channel_sphere(shape=(150, 24, 22), center=(40, 12, 11), radius=6,
+                                      gx=1e-5), seed=82)
+    cs = dataclasses.replace(cs, name=cs.name + " perturbed")
+    c3 = W.perturbed(W.cavity3d(shape=(70, 40, 37)), seed=83)
+    c2 = W.perturbed(W.cavity2d(shape=(300, 181, 1)), seed=84)
+    return [rp, cs, c3, c2]
+
+
+CASES = slab_cases() + [outer_walls_case()] + _large_cases()
+
+
+def _layouts(w):
+    if w.dim == 2:
+        return [(2, 2, 1), (3, 2, 1), (2, 3, 1)]
+    return [(2, 2, 1), (1, 2, 2), (2, 2, 2), (3, 2, 2)]
+
+
+@pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
+def test_blocks_equal_single_domain(oracle_mod, w):
+    """Each block layout against the undivided domain (bitwise where the kernel families
+    agree) and the fp64 oracle (1e-6 on the populations, 2e-5 on rho, u, T), at 7 and 8
+    steps; the summed diagnostics agree with the undivided domain's."""
+    ref = oracle_states(oracle_mod, w, [7, 8])
+    for steps in (7, 8):
+        f1, g1, d1 = _single(w, steps)
+        for nb in _layouts(w):
+            got, ds = _blocks(w, nb, [3, steps - 3])
+            compare_fields(w, got, ref[steps], tol=TOL_FIELDS, pop_tol=1e-6)
+            if _same_family(w, nb):
+                assert np.array_equal(got["f"], f1), (steps, nb)
+                if w.thermal:
+                    assert np.array_equal(got["g"], g1), (steps, nb)
+            else:
+                assert np.abs(got["f"] - f1).max() < 1e-6, (steps, nb)
+                if w.thermal:
+                    assert np.abs(got["g"] - g1).max() < 1e-6, (steps, nb)
+            assert ds["fluid_cells"] == d1["fluid_cells"]
+            assert ds["finite"]
+            assert abs(ds["mass"] - d1["mass"]) <= 1e-9 * abs(d1["mass"])
+            cells = d1["fluid_cells"]
+            assert np.allclose(ds["momentum"], d1["momentum"], rtol=0, atol=1e-7 * cells)
+            fscale = max(1e-30, float(np.abs(d1["force"]).max()))
+            assert np.allclose(ds["force"], d1["force"], rtol=0, atol=1e-5 * fscale)
+            if w.thermal:
+                hscale = max(1e-30, float(np.abs(d1["heat"]).max()))
+                assert np.allclose(ds["heat"], d1["heat"], rtol=0, atol=1e-6 * hscale)
+
+
+@pytest.mark.parametrize("w,nb", [
+    (W.perturbed(W.cavity3d(shape=(70, 40, 37)), seed=83), (2, 2, 2)),
+    (W.perturbed(W.cavity2d(shape=(300, 181, 1)), seed=84), (2, 2, 1))],
+    ids=["cavity3d 70x40x37 2x2x2", "cavity2d 300x181 2x2"])
+def test_blocks_200_and_201_steps_against_the_oracle(oracle_mod, w, nb):
+    """Blocks over 200 and 201 steps against the oracle on the undivided domain (2e-5 on the
+    fields and populations, heat sums 1e-4 relative)."""
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    ref = oracle_states(oracle_mod, w, [200, 201])
+    dom = BlockDomain(w, nb)
+    dom.init_equilibrium()
+    done = 0
+    for n in (200, 201):
+        dom.step(n - done)
+        done = n
+        f, g = dom.populations()
+        rho, u, T = dom.macroscopic()
+        got = {"rho": rho.cpu().numpy(), "u": u.cpu().numpy(), "T": T.cpu().numpy(),
+               "f": f.cpu().numpy(), "g": g.cpu().numpy()}
+        compare_fields(w, got, ref[n])
+        assert np.allclose(dom.diagnostics()["heat"], ref[n]["diag"]["heat"], rtol=1e-4,
+                           atol=1e-3)
+    dom.close()
+
+
+def test_axis_halo_calls_are_checked():
+    """Per-axis halo calls: the plane size of each axis, only HALO sides, axes in range,
+    the same parity rules as the outer-axis calls."""
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    w = W.random_periodic(shape=(16, 8, 10), seed=86)
+    w = dataclasses.replace(w, face_flow=("halo", "halo", "wall", "halo", "periodic",
+                                          "periodic"))
+    sim = Simulation(w)
+    assert capi.lbm_halo_axis_bytes(sim.ctx, 0) == 4 * 5 * 8 * 10
+    assert capi.lbm_halo_axis_bytes(sim.ctx, 1) == 4 * 5 * 16 * 10
+    assert capi.lbm_halo_axis_bytes(sim.ctx, 2) == 4 * 5 * 16 * 8
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_axis_bytes(sim.ctx, 3)
+    buf = torch.empty(5 * 16 * 10, device="cuda")
+    sim.init_equilibrium(_dev(w.rho0), _dev(w.u0))
+    sim.step(1)
+    capi.lbm_halo_axis_pack(sim.ctx, 0, 1, capi.LBM_HALO_FILL, buf)
+    capi.lbm_halo_axis_pack(sim.ctx, 1, 1, capi.LBM_HALO_FILL, buf)
+    for axis, side in ((1, 0), (2, 0), (2, 1), (3, 0), (-1, 0)):
+        with pytest.raises(capi.LbmError):
+            capi.lbm_halo_axis_pack(sim.ctx, axis, side, capi.LBM_HALO_FILL, buf)
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_axis_unpack(sim.ctx, 0, 0, capi.LBM_HALO_DRAIN, buf)   # parity 1
+    sim.step(1)
+    capi.lbm_halo_axis_unpack(sim.ctx, 0, 0, capi.LBM_HALO_DRAIN, buf)
+    torch.cuda.synchronize()
+    sim.close()
+
+
+# ------------------------------------------------------------- one block per rank ---
+
+STEPS = (7, 8)
+
+
+def _case(name):
+    if name == "periodic 2x2":
+        return W.random_periodic(shape=(40, 12, 20), seed=87), (2, 1, 2)
+    if name == "cavity3d 2x2":
+        return W.perturbed(W.cavity3d(shape=(36, 20, 22)), seed=88), (1, 2, 2)
+    return W.perturbed(W.cavity2d(shape=(70, 30, 1)), seed=89), (2, 2, 1)
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, name, out):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import torch.distributed as dist
+    from lattice_boltzmann_cfd_gb300.slabs import DistBlockDomain
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=120))
+    w, nb = _case(name)
+    d = DistBlockDomain(w, nb, rank, world, device="cuda:0", transport="host")
+    d.init_equilibrium()
+    res, done = {}, 0
+    for n in STEPS:
+        d.step(n - done)
+        done = n
+        f, g = d.populations()
+        res[n] = (f.cpu().numpy(), None if g is None else g.cpu().numpy())
+    out[rank] = res
+    d.close()
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("name", ["periodic 2x2", "cavity3d 2x2", "cavity2d 2x2"])
+def test_four_ranks_share_the_gpu(oracle_mod, name):
+    """Four gloo ranks, one block each, on the one GPU of the test box: the halo kernels
+    write and read page-locked host buffers and the waiting is on the host, in the gloo
+    messages.  The gathered owned cells equal the undivided domain bit for bit and match
+    the fp64 oracle."""
+    import torch.multiprocessing as mp
+    from lattice_boltzmann_cfd_gb300.slabs import block_part, owned_slices
+    w, nb = _case(name)
+    world = nb[0] * nb[1] * nb[2]
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.spawn(_rank, args=(world, _free_port(), name, out), nprocs=world, join=True)
+    ref = oracle_states(oracle_mod, w, list(STEPS))
+    for n in STEPS:
+        f1, g1, _ = _single(w, n)
+        f = np.full_like(f1, np.nan)
+        g = None if g1 is None else np.full_like(g1, np.nan)
+        for r in range(world):
+            _, sides, coords = block_part(w, nb, r)
+            own = owned_slices(sides, coords)
+            sel = np.ix_(*(np.array(coords[a])[own[2 - a]] for a in (2, 1, 0)))
+            f[(slice(None),) + sel] = out[r][n][0]
+            if g is not None:
+                g[(slice(None),) + sel] = out[r][n][1]
+        assert np.array_equal(f, f1), n
+        if w.thermal:
+            assert np.array_equal(g, g1), n
+        assert np.abs(f - ref[n]["f"]).max() <= 1e-6
+        if w.thermal:
+            assert np.abs(g - ref[n]["g"]).max() <= 1e-6
