@@ -509,17 +509,18 @@ def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None, overla
     torch.cuda.synchronize()
     step_s = a.elapsed_time(b) / 1e3 / (reps * lbm_steps)
     halo = dom.halo_bytes_per_step()
-    pairs = len(dom.pairs())
+    launches = len(dom.pairs()) * (1 if dom.swap else 4)
     dom.close()
     del dom
     torch.cuda.empty_cache()
     mlups = w.cells / step_s / 1e6
     out = {"workload": workload_label(name, w), "layout": "aa", "slabs": nslabs,
            "decomposition": "slabs along the outer axis, 1 ghost plane per inner face, "
-                            "FILL after even / DRAIN after odd steps, all on this GPU",
+                            "FILL after even / DRAIN after odd steps, all on this GPU, each "
+                            "face moved by one buffer-free swap kernel",
            "overlap": bool(overlap),
            "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
-           "halo_launches_per_step": 4 * pairs}
+           "halo_launches_per_step": launches}
     if single_mlups:
         out["vs_single_domain"] = round(mlups / single_mlups, 4)
     return out
@@ -530,7 +531,7 @@ def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None):
     halo exchange after every step (z, then y, then x; a step = one step launch per block +
     one pack and one unpack launch per block face and direction)."""
     import torch
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain, exchange_axes
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
     w = cached_workload(name)
     dom = BlockDomain(w, nb)
     dom.init_equilibrium()
@@ -544,7 +545,7 @@ def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None):
     torch.cuda.synchronize()
     step_s = a.elapsed_time(b) / 1e3 / (reps * lbm_steps)
     halo = dom.halo_bytes_per_step()
-    faces = sum(len(dom.pairs(ax)) for ax in exchange_axes(w.dim, dom.nb))
+    launches = dom.halo_launches_per_step()
     dom.close()
     del dom
     torch.cuda.empty_cache()
@@ -552,9 +553,10 @@ def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None):
     out = {"workload": workload_label(name, w), "layout": "aa", "blocks": list(nb),
            "decomposition": "blocks, 1 ghost plane per inner face of each split axis, "
                             "exchanged axis by axis with the ghost rows of the other axes "
-                            "(edges and corners in two or three hops), all on this GPU",
+                            "(edges and corners in two or three hops), all on this GPU, each "
+                            "face moved by one buffer-free swap kernel",
            "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
-           "halo_launches_per_step": 4 * faces}
+           "halo_launches_per_step": launches}
     if single_mlups:
         out["vs_single_domain"] = round(mlups / single_mlups, 4)
     return out

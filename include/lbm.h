@@ -334,6 +334,21 @@ lbm_status lbm_halo_axis_bytes(const lbm_ctx *ctx, int axis, size_t *bytes);
 lbm_status lbm_halo_axis_pack(lbm_ctx *ctx, int axis, int side, int phase, void *buf);
 lbm_status lbm_halo_axis_unpack(lbm_ctx *ctx, int axis, int side, int phase, const void *buf);
 
+/* The exchange across one face of two blocks on the same device, without a buffer: lo's high
+ * face of `axis` meets hi's low face.  One kernel moves both ways what lbm_halo_axis_pack on
+ * one side and lbm_halo_axis_unpack on the other would move:
+ *   FILL:  hi's first owned plane -> lo's ghost plane (directions with c_axis = +1), and lo's
+ *          first owned plane -> hi's ghost plane (c_axis = -1);
+ *   DRAIN: lo's ghost plane -> hi's first owned plane (c_axis = +1, wall links and solid cells
+ *          of hi keep their slots), and hi's ghost plane -> lo's first owned plane (c_axis = -1).
+ * lo and hi may be the same context (a ring of one block along that axis).  Both must be
+ * initialised, at the same step, with the same lattices and equal extents on the other two
+ * axes (LBM_ERR_ARG / LBM_ERR_STATE), and on one device (LBM_ERR_UNSUPPORTED otherwise).  The
+ * kernel runs on lo's stream: work on hi issued on another stream must be ordered before the
+ * call by the caller (an event), and later work on hi after it.  The parity rules are those of
+ * the pack and unpack calls; the axis order rule for blocks holds as well. */
+lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase);
+
 /* Enqueue later work on another stream (a cudaStream_t). */
 lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);
 

@@ -87,6 +87,7 @@ SIGNATURES = [
     ("lbm_halo_axis_bytes", ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
     ("lbm_halo_axis_pack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_halo_axis_unpack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP]),
+    ("lbm_halo_axis_swap", ctypes.c_int, [_VP, _VP, ctypes.c_int, ctypes.c_int]),
     ("lbm_set_stream", ctypes.c_int, [_VP, _VP]),
     ("lbm_reduce_populations_static", ctypes.c_int,
      [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP,
@@ -262,6 +263,10 @@ def lbm_halo_axis_pack(ctx, axis: int, side: int, phase: int, buf):
 
 def lbm_halo_axis_unpack(ctx, axis: int, side: int, phase: int, buf):
     _check(load().lbm_halo_axis_unpack(ctx, int(axis), int(side), int(phase), _addr(buf)), ctx)
+
+
+def lbm_halo_axis_swap(lo, hi, axis: int, phase: int):
+    _check(load().lbm_halo_axis_swap(lo, hi, int(axis), int(phase)), lo)
 
 
 def lbm_set_stream(ctx, stream):

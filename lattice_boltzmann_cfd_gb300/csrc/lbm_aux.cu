@@ -92,15 +92,38 @@ cudaError_t launch_ib_mark(int lattice, const Params &P, uint32_t *mask, bool se
     return cudaGetLastError();
 }
 
+// Halo kernels move a plane of cells with a few slots each: small blocks spread a plane over
+// more SMs, which keeps more loads in flight.
+constexpr int HALO_THREADS = 128;
+
 cudaError_t launch_halo(int lattice, int thermal, const Params &P, int axis, int side,
                         int phase, int unpack, float *buf, cudaStream_t s)
 {
     const int n[3] = {P.nx, P.ny, P.nz};
     const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
-    const dim3 b(256), g((plane_cells + 255) / 256);
+    const dim3 b(HALO_THREADS), g((plane_cells + HALO_THREADS - 1) / HALO_THREADS);
     return by_lattice(lattice, thermal, [&](auto l, auto tl) {
-        halo_kernel<decltype(l), decltype(tl)><<<g, b, 0, s>>>(P, axis, side, phase, unpack,
-                                                                buf);
+        using Lt = decltype(l);
+        using Tt = decltype(tl);
+        if (axis == 0) halo_kernel<Lt, Tt, 0><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+        else if (axis == 1) halo_kernel<Lt, Tt, 1><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+        else halo_kernel<Lt, Tt, 2><<<g, b, 0, s>>>(P, side, phase, unpack, buf);
+        return cudaGetLastError();
+    });
+}
+
+cudaError_t launch_halo_swap(int lattice, int thermal, const Params &lo, const Params &hi,
+                             int axis, int phase, cudaStream_t s)
+{
+    const int n[3] = {lo.nx, lo.ny, lo.nz};
+    const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
+    const dim3 b(HALO_THREADS), g((plane_cells + HALO_THREADS - 1) / HALO_THREADS);
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        using Lt = decltype(l);
+        using Tt = decltype(tl);
+        if (axis == 0) halo_swap_kernel<Lt, Tt, 0><<<g, b, 0, s>>>(lo, hi, phase);
+        else if (axis == 1) halo_swap_kernel<Lt, Tt, 1><<<g, b, 0, s>>>(lo, hi, phase);
+        else halo_swap_kernel<Lt, Tt, 2><<<g, b, 0, s>>>(lo, hi, phase);
         return cudaGetLastError();
     });
 }

@@ -269,6 +269,8 @@ constexpr long long GRAPH_MAX_CELLS = 1LL << 22;   // launch-bound below ~4 M ce
 cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStream_t stream)
 {
     const lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
+    const lbm::Shape sh_aa = lbm::step_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz, c->L.dim, 0,
+                                             c->L.dim == 3 ? c->cfg.nz : c->cfg.ny, P.linear);
     // 32-bit population indices when the largest index (Q * S - 1) fits
     const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
     const bool d3 = c->cfg.lattice == LBM_D3Q19;
@@ -294,12 +296,12 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
         break;
     default:
         if (c->cfg.lattice == LBM_D3Q27)
-            e = lbm::launch_step_d3q27(masked, parity != 0, narrow, P, sh, stream, c->chained);
+            e = lbm::launch_step_d3q27(masked, parity != 0, narrow, P, sh_aa, stream, c->chained);
         else
-            e = d3 ? lbm::launch_step_d3q19(th, coll, masked, parity != 0, narrow, P, sh, stream,
-                                            c->chained)
-                   : lbm::launch_step_d2q9(th, coll, masked, parity != 0, narrow, P, sh, stream,
-                                           c->chained);
+            e = d3 ? lbm::launch_step_d3q19(th, coll, masked, parity != 0, narrow, P, sh_aa,
+                                            stream, c->chained)
+                   : lbm::launch_step_d2q9(th, coll, masked, parity != 0, narrow, P, sh_aa,
+                                           stream, c->chained);
     }
     if (c->L.streaming != LBM_STREAM_AA) {
         std::swap(P.f, P.fo);
@@ -314,9 +316,8 @@ cudaError_t launch_planes(const lbm_ctx *c, const lbm::Params &P0, int parity, i
                           cudaStream_t stream, bool chained)
 {
     const bool d2 = c->cfg.lattice == LBM_D2Q9;
-    lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
-    if (d2) sh.grid.y = (unsigned)((hi - lo + (int)sh.block.y - 1) / (int)sh.block.y);
-    else sh.grid.z = (unsigned)(hi - lo);
+    const lbm::Shape sh =
+        lbm::step_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz, c->L.dim, lo, hi, P0.linear);
     lbm::Params P = P0;
     P.plane_lo = lo;
     P.plane_hi = hi;
@@ -795,6 +796,39 @@ lbm_status lbm_halo_axis_pack(lbm_ctx *c, int axis, int side, int phase, void *b
 lbm_status lbm_halo_axis_unpack(lbm_ctx *c, int axis, int side, int phase, const void *buf)
 {
     return halo_call(c, axis, side, phase, 1, buf);
+}
+
+lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase)
+{
+    if (!lo || !hi) return fail(nullptr, LBM_ERR_ARG, "both contexts are required");
+    if (!lo->L.halo || !hi->L.halo) return fail(lo, LBM_ERR_STATE, "no HALO face in a context");
+    if (axis < 0 || axis >= lo->L.dim) return fail(lo, LBM_ERR_ARG, "axis out of range");
+    if (lo->cfg.face_flow[2 * axis + 1] != LBM_FACE_HALO ||
+        hi->cfg.face_flow[2 * axis] != LBM_FACE_HALO)
+        return fail(lo, LBM_ERR_ARG, "lo's high face and hi's low face must be HALO faces");
+    if (phase != LBM_HALO_FILL && phase != LBM_HALO_DRAIN)
+        return fail(lo, LBM_ERR_ARG, "phase must be LBM_HALO_FILL or LBM_HALO_DRAIN");
+    if (lo->cfg.lattice != hi->cfg.lattice || lo->cfg.thermal != hi->cfg.thermal)
+        return fail(lo, LBM_ERR_ARG, "the two contexts must have the same lattices");
+    const int nlo[3] = {lo->cfg.nx, lo->cfg.ny, lo->cfg.nz};
+    const int nhi[3] = {hi->cfg.nx, hi->cfg.ny, hi->cfg.nz};
+    for (int a = 0; a < 3; ++a)
+        if (a != axis && nlo[a] != nhi[a])
+            return fail(lo, LBM_ERR_ARG, "the two faces must have the same extents");
+    if (lo->device != hi->device)
+        return fail(lo, LBM_ERR_UNSUPPORTED, "the two contexts must be on one device");
+    if (!lo->initialized || !hi->initialized) return fail(lo, LBM_ERR_STATE, "no state");
+    if (lo->parity != hi->parity || lo->steps != hi->steps)
+        return fail(lo, LBM_ERR_STATE, "the two contexts must be at the same step");
+    if (phase == LBM_HALO_FILL && lo->parity != 1)
+        return fail(lo, LBM_ERR_STATE, "FILL belongs before an odd step (parity 1)");
+    if (phase == LBM_HALO_DRAIN && (lo->parity != 0 || lo->steps == 0))
+        return fail(lo, LBM_ERR_STATE, "DRAIN belongs after an odd step (parity 0)");
+    DeviceGuard guard(lo->device);
+    cudaError_t e = lbm::launch_halo_swap(lo->cfg.lattice, lo->cfg.thermal, lo->P, hi->P, axis,
+                                          phase, lo->stream);
+    if (e != cudaSuccess) return cuda_fail(lo, e, "halo swap kernel");
+    return LBM_OK;
 }
 
 lbm_status lbm_set_stream(lbm_ctx *c, void *cuda_stream)

@@ -57,6 +57,24 @@ inline Shape cell_shape(int nx, int ny, int nz, int threads = 64)
     return s;
 }
 
+// The AA step kernels' launch over the outer-axis planes [lo, hi): cell_shape's grid cut to
+// those planes when rows are a multiple of 32 cells; otherwise (linear) a 1-D grid of
+// 64-thread blocks over the planes' cells in storage order (Params::linear).
+inline Shape step_shape(int nx, int ny, int nz, int dim, int lo, int hi, bool linear)
+{
+    Shape s;
+    if (linear) {
+        const long long cells = (long long)(dim == 3 ? (long long)nx * ny : nx) * (hi - lo);
+        s.block = dim3(64, 1, 1);
+        s.grid = dim3((unsigned)((cells + 63) / 64), 1, 1);
+        return s;
+    }
+    s = cell_shape(nx, ny, nz);
+    if (dim == 2) s.grid.y = (unsigned)((hi - lo + (int)s.block.y - 1) / (int)s.block.y);
+    else s.grid.z = (unsigned)(hi - lo);
+    return s;
+}
+
 constexpr int DIAG_BLOCKS = 2048;   // capacity of the partial-sum rows (one resident wave at most)
 
 // Each returns the launch error (cudaGetLastError) of what it enqueued.
@@ -129,6 +147,9 @@ cudaError_t launch_ib_order(int lattice, const Params &P, int n, int l, const fl
 // Halo pack (unpack = 0) or unpack (unpack = 1) of one side of one axis, one phase.
 cudaError_t launch_halo(int lattice, int thermal, const Params &P, int axis, int side,
                         int phase, int unpack, float *buf, cudaStream_t s);
+// The buffer-free exchange of lo's high face with hi's low face on `axis` (halo_swap_kernel).
+cudaError_t launch_halo_swap(int lattice, int thermal, const Params &lo, const Params &hi,
+                             int axis, int phase, cudaStream_t s);
 cudaError_t launch_diag(int lattice, int thermal, bool masked, int pat, const Params &P,
                         double *partial, double *out, cudaStream_t s);
 

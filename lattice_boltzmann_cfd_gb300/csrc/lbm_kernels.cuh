@@ -31,10 +31,26 @@
 #include <climits>
 #include <cstddef>
 #include <cstdint>
+#include <type_traits>
 
 #include "lbm_collide.cuh"
 
 namespace lbm {
+
+// Division of 0 <= n < 2^31 by an invariant d >= 1 with one multiply and one shift
+// (Granlund and Montgomery, "Division by invariant integers using multiplication", 1994):
+// m = ceil(2^s / d) with s = 31 + ceil(log2 d).  floor(n m / 2^s) = floor(n / d) because the
+// excess n (m d - 2^s) / (d 2^s) stays below 1/d: m d - 2^s < d <= 2^(s-31) and n < 2^31.
+// m <= 2^32, so n m fits in 64 bits.
+struct Divisor {
+    unsigned long long m;
+    int s;
+};
+
+LBM_HD unsigned div_by(unsigned n, const Divisor &d)
+{
+    return (unsigned)(((unsigned long long)n * d.m) >> d.s);
+}
 
 struct Params {
     float *f;              // Q planes of S floats (shifted populations), current buffer
@@ -53,6 +69,11 @@ struct Params {
     // outer-axis planes (z in 3-D, y in 2-D) the AA step kernels cover: [plane_lo,
     // plane_hi); the whole axis except in launches of lbm_step_planes
     int plane_lo, plane_hi;
+    // AA step launches over rows that are not a multiple of 32 cells (linear = 1): one thread
+    // per cell in storage order, so that no thread idles past the end of a row and every warp
+    // covers 32 consecutive cells; the coordinates come from dividing by nx and ny
+    int linear;
+    Divisor div_nx, div_ny;
     int box_lo[3], box_hi[3];  // solid cells' box widened by one (inclusive; empty: lo > hi)
     int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
     float T_wall[6];
@@ -520,13 +541,35 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     }
 }
 
+// Cell t (counted from the first cell of plane P.plane_lo, in storage order) of a linear AA
+// step launch; false past the last cell of plane P.plane_hi - 1.
+template <class L>
+LBM_HD bool linear_cell_coords(const Params &P, int t, int &x, int &y, int &z)
+{
+    const int plane = L::DIM == 3 ? P.nx * P.ny : P.nx;
+    const int i = P.plane_lo * plane + t;
+    if (i >= P.plane_hi * plane) return false;
+    const int q = (int)div_by((unsigned)i, P.div_nx);   // row index: y + ny z
+    x = i - q * P.nx;
+    if constexpr (L::DIM == 3) {
+        z = (int)div_by((unsigned)q, P.div_ny);
+        y = q - z * P.ny;
+    } else {
+        y = q;
+        z = 0;
+    }
+    return true;
+}
+
 // Cell of the calling thread in an AA step launch over the outer-axis planes
-// [P.plane_lo, P.plane_hi): the launch grid covers those planes only, offset by plane_lo.
-// Returns false for threads past the grid's edge.
+// [P.plane_lo, P.plane_hi): the launch grid covers those planes only, offset by plane_lo
+// (blocks along x, rows stacked in y, planes in z; or, with P.linear, a 1-D grid over the
+// cells in storage order).  Returns false for threads past the grid's edge.
 template <class L>
 LBM_HD bool step_cell_coords(const Params &P, int &x, int &y, int &z)
 {
 #if defined(__CUDA_ARCH__)
+    if (P.linear) return linear_cell_coords<L>(P, blockIdx.x * blockDim.x + threadIdx.x, x, y, z);
     x = blockIdx.x * blockDim.x + threadIdx.x;
     y = blockIdx.y * blockDim.y + threadIdx.y;
     z = blockIdx.z;
@@ -1291,69 +1334,203 @@ static __global__ void __launch_bounds__(DIAG_THREADS) diag_finalize(const doubl
 // A pack of side s / phase FILL reads my boundary plane at s with the populations pointing
 // into my slab; unpack of side s / FILL writes my ghost plane at s with those pointing out;
 // DRAIN swaps the planes' roles.  A plane spans the whole extent of the other axes, their
-// ghost rows included: a block driver exchanges the axes one after another (FILL in one
-// order, DRAIN in the reverse one), so that what crosses an edge or a corner travels through
-// the ghost rows of the intermediate neighbours.  A DRAIN leaves slot (q, x) alone where
+// ghost rows included: a block driver exchanges the axes one after another (the same order
+// at FILL and at DRAIN), so that what crosses an edge or a corner travels through the ghost
+// rows of the intermediate neighbours.  A DRAIN leaves slot (q, x) alone where
 // the link of x towards the ghost (opposite q) is a wall link: x bounced that population
 // back into the slot itself, and the ghost's copy was never written; and it leaves solid
 // cells alone.  buf: [direction][plane cell], momentum then thermal; plane cells with the
 // lower remaining axis fastest.
+// Cell index of plane cell i (the lower remaining axis fastest) of the plane next to face
+// `side` of AXIS: the ghost plane (ghost) or the first owned plane.
+template <int AXIS>
+LBM_HD int halo_plane_cell(const Params &P, int side, bool ghost, int i)
+{
+    const int n[3] = {P.nx, P.ny, P.nz};
+    constexpr int u = AXIS == 0 ? 1 : 0, v = AXIS == 2 ? 1 : 2;
+    int c3[3];
+    c3[AXIS] = side ? n[AXIS] - 1 : 0;
+    if (!ghost) c3[AXIS] += side ? -1 : 1;
+    c3[u] = i % n[u];
+    c3[v] = i / n[u];
+    return c3[0] + P.nx * (c3[1] + P.ny * c3[2]);
+}
+
+template <class L, int AXIS>
+LBM_HD constexpr int axis_c(int q)
+{
+    return AXIS == 0 ? L::cx(q) : AXIS == 1 ? L::cy(q) : L::cz(q);
+}
+
+// The slots of one cell that cross a face of AXIS in direction SIGN (c_AXIS = SIGN), held
+// in registers: every load of a move is issued before its first store, since the source
+// and the destination may be the same buffer and the compiler would otherwise keep each
+// store behind the load before it.
+template <class L, class TL>
+struct HaloSlots {
+    float f[L::Q], g[TL::QA];
+};
+
+template <class L, class TL, int AXIS, int SIGN>
+LBM_HD void halo_load(const Params &S, int cell, HaloSlots<L, TL> &v)
+{
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q)
+        if (axis_c<L, AXIS>(q) == SIGN) v.f[q] = S.f[(size_t)q * S.S + (unsigned)cell];
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int q = 0; q < TL::Q; ++q)   // thermal direction q is flow direction q
+            if (axis_c<L, AXIS>(q) == SIGN) v.g[q] = S.g[(size_t)q * S.S + (unsigned)cell];
+    }
+}
+
+// keep: the destination cell's mask on a DRAIN into an owned plane (else 0): a slot whose
+// opposite link is a wall link keeps its value, and so does every slot of a solid cell.
+template <class L, class TL, int AXIS, int SIGN>
+LBM_HD void halo_store(const Params &D, int cell, uint32_t keep, const HaloSlots<L, TL> &v)
+{
+    if (keep & SOLID_BIT) return;
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q)
+        if (axis_c<L, AXIS>(q) == SIGN && !bit(keep, L::opp(q)))
+            D.f[(size_t)q * D.S + (unsigned)cell] = v.f[q];
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int q = 0; q < TL::Q; ++q)
+            if (axis_c<L, AXIS>(q) == SIGN && !bit(keep, L::opp(q)))
+                D.g[(size_t)q * D.S + (unsigned)cell] = v.g[q];
+    }
+}
+
+// The same slots to or from a contiguous buffer: [direction][plane cell], momentum then
+// thermal, directions in index order.
+template <class L, class TL, int AXIS, int SIGN>
+LBM_HD void halo_to_buf(const HaloSlots<L, TL> &v, float *buf, int plane_cells, int i)
+{
+    int k = 0;
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q)
+        if (axis_c<L, AXIS>(q) == SIGN) buf[(size_t)(k++) * plane_cells + i] = v.f[q];
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int q = 0; q < TL::Q; ++q)
+            if (axis_c<L, AXIS>(q) == SIGN) buf[(size_t)(k++) * plane_cells + i] = v.g[q];
+    }
+}
+
+template <class L, class TL, int AXIS, int SIGN>
+LBM_HD void halo_from_buf(const float *buf, int plane_cells, int i, HaloSlots<L, TL> &v)
+{
+    int k = 0;
+#pragma unroll
+    for (int q = 0; q < L::Q; ++q)
+        if (axis_c<L, AXIS>(q) == SIGN) v.f[q] = buf[(size_t)(k++) * plane_cells + i];
+    if constexpr (TL::Q > 0) {
+#pragma unroll
+        for (int q = 0; q < TL::Q; ++q)
+            if (axis_c<L, AXIS>(q) == SIGN) v.g[q] = buf[(size_t)(k++) * plane_cells + i];
+    }
+}
+
+template <int AXIS>
+LBM_HD int halo_plane_cells(const Params &P)
+{
+    const int n[3] = {P.nx, P.ny, P.nz};
+    return n[AXIS == 0 ? 1 : 0] * n[AXIS == 2 ? 1 : 2];
+}
+
+// Pack (unpack = 0) or unpack plane cell i of side `side` of AXIS in phase `phase`.
+template <class L, class TL, int AXIS>
+LBM_HD void halo_cell_axis(const Params &P, int side, int phase, int unpack, float *buf, int i)
+{
+    const int plane_cells = halo_plane_cells<AXIS>(P);
+    // ghost plane of the side, or the owned plane next to it
+    const bool ghost = (phase == 0) == (unpack != 0);
+    const int idx = halo_plane_cell<AXIS>(P, side, ghost, i);
+    // directions pointing out through the side (ghost plane) or into the block (owned plane)
+    const int out_sign = side ? 1 : -1;
+    const int sign = ghost ? out_sign : -out_sign;
+    // DRAIN into my boundary plane: links that are bounced (or a solid cell) keep their own
+    // value; a ghost cell on it (a block's edge) holds values in transit and takes them all
+    const uint32_t keep = unpack && !ghost && P.mask ? P.mask[idx] : 0u;
+    HaloSlots<L, TL> v;
+    auto run = [&](auto sg) {
+        constexpr int SG = decltype(sg)::value;
+        if (!unpack) {
+            halo_load<L, TL, AXIS, SG>(P, idx, v);
+            halo_to_buf<L, TL, AXIS, SG>(v, buf, plane_cells, i);
+        } else {
+            halo_from_buf<L, TL, AXIS, SG>(buf, plane_cells, i, v);
+            halo_store<L, TL, AXIS, SG>(P, idx, keep, v);
+        }
+    };
+    if (sign > 0) run(std::integral_constant<int, 1>{});
+    else run(std::integral_constant<int, -1>{});
+}
+
 template <class L, class TL>
 LBM_HD void halo_cell(const Params &P, int axis, int side, int phase, int unpack, float *buf,
                       int i)
 {
-    const int n[3] = {P.nx, P.ny, P.nz};
-    const int u = axis == 0 ? 1 : 0, v = axis == 2 ? 1 : 2;   // the other two axes
-    const int plane_cells = n[u] * n[v];
-    // ghost plane of the side, or the owned plane next to it
-    const bool ghost_plane = (phase == 0) == (unpack != 0);
-    int plane = side ? n[axis] - 1 : 0;
-    if (!ghost_plane) plane += side ? -1 : 1;
-    int c3[3];
-    c3[axis] = plane;
-    c3[u] = i % n[u];
-    c3[v] = i / n[u];
-    const int idx = c3[0] + P.nx * (c3[1] + P.ny * c3[2]);
-    // directions pointing out through the side (ghost plane) or into the slab (owned plane)
-    const int out_sign = side ? 1 : -1;
-    const int sign = ghost_plane ? out_sign : -out_sign;
-    // DRAIN into my boundary plane: links that are bounced (or a solid cell) keep their own
-    // value; a ghost cell on it (a block's edge) holds values in transit
-    const bool drain_in = unpack && !ghost_plane;
-    const uint32_t keep = drain_in && P.mask ? P.mask[idx] : 0u;
-    const bool skip_cell = keep & SOLID_BIT;
-    int k = 0;
-#pragma unroll
-    for (int q = 0; q < L::Q; ++q) {
-        const int c = axis == 0 ? L::cx(q) : axis == 1 ? L::cy(q) : L::cz(q);
-        if (c != sign) continue;
-        float *slot = P.f + ((size_t)q * P.S + (unsigned)idx);
-        float *b = buf + ((size_t)k * plane_cells + i);
-        if (!unpack) *b = *slot;
-        else if (!skip_cell && !bit(keep, L::opp(q))) *slot = *b;
-        ++k;
-    }
-    if constexpr (TL::Q > 0) {
-#pragma unroll
-        for (int q = 0; q < TL::Q; ++q) {
-            const int c = axis == 0 ? L::cx(q) : axis == 1 ? L::cy(q) : L::cz(q);
-            if (c != sign) continue;
-            float *slot = P.g + ((size_t)q * P.S + (unsigned)idx);
-            float *b = buf + ((size_t)k * plane_cells + i);
-            if (!unpack) *b = *slot;
-            else if (!skip_cell && !bit(keep, L::opp(q))) *slot = *b;
-            ++k;
-        }
-    }
+    if (axis == 0) halo_cell_axis<L, TL, 0>(P, side, phase, unpack, buf, i);
+    else if (axis == 1) halo_cell_axis<L, TL, 1>(P, side, phase, unpack, buf, i);
+    else halo_cell_axis<L, TL, 2>(P, side, phase, unpack, buf, i);
+}
+
+template <class L, class TL, int AXIS>
+__global__ void halo_kernel(const Params P, int side, int phase, int unpack, float *buf)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < halo_plane_cells<AXIS>(P)) halo_cell_axis<L, TL, AXIS>(P, side, phase, unpack, buf, i);
+}
+
+// The exchange across one face without a buffer: block `lo`'s high face of AXIS meets block
+// `hi`'s low face, both in memory this device can address.  Plane cell i, both ways:
+// FILL: hi's first owned plane -> lo's ghost plane (slots with c_AXIS = +1), lo's first
+//   owned plane -> hi's ghost plane (c_AXIS = -1);
+// DRAIN: lo's ghost plane -> hi's first owned plane (c_AXIS = +1), hi's ghost plane -> lo's
+//   first owned plane (c_AXIS = -1).
+// It moves exactly what a pack on one side and an unpack on the other move.  Each move
+// reads one plane of a block and writes another, so no thread reads a slot that another
+// writes (lo may be hi: the two faces of a ring of one block, at least three planes thick).
+template <class L, class TL, int AXIS>
+LBM_HD void halo_swap_cell_axis(const Params &lo, const Params &hi, int phase, int i)
+{
+    const bool fill = phase == 0;
+    // +1 direction: from hi (FILL: its owned plane) or lo (DRAIN: its ghost plane)
+    const Params &s_up = fill ? hi : lo, &d_up = fill ? lo : hi;
+    const int from_up = fill ? halo_plane_cell<AXIS>(hi, 0, false, i)
+                             : halo_plane_cell<AXIS>(lo, 1, true, i);
+    const int to_up = fill ? halo_plane_cell<AXIS>(lo, 1, true, i)
+                           : halo_plane_cell<AXIS>(hi, 0, false, i);
+    // -1 direction: from lo (FILL: its owned plane) or hi (DRAIN: its ghost plane)
+    const Params &s_dn = fill ? lo : hi, &d_dn = fill ? hi : lo;
+    const int from_dn = fill ? halo_plane_cell<AXIS>(lo, 1, false, i)
+                             : halo_plane_cell<AXIS>(hi, 0, true, i);
+    const int to_dn = fill ? halo_plane_cell<AXIS>(hi, 0, true, i)
+                           : halo_plane_cell<AXIS>(lo, 1, false, i);
+    const uint32_t keep_up = !fill && d_up.mask ? d_up.mask[to_up] : 0u;
+    const uint32_t keep_dn = !fill && d_dn.mask ? d_dn.mask[to_dn] : 0u;
+    HaloSlots<L, TL> up, dn;
+    halo_load<L, TL, AXIS, 1>(s_up, from_up, up);
+    halo_load<L, TL, AXIS, -1>(s_dn, from_dn, dn);
+    halo_store<L, TL, AXIS, 1>(d_up, to_up, keep_up, up);
+    halo_store<L, TL, AXIS, -1>(d_dn, to_dn, keep_dn, dn);
 }
 
 template <class L, class TL>
-__global__ void halo_kernel(const Params P, int axis, int side, int phase, int unpack, float *buf)
+LBM_HD void halo_swap_cell(const Params &lo, const Params &hi, int axis, int phase, int i)
 {
-    const int n[3] = {P.nx, P.ny, P.nz};
-    const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
+    if (axis == 0) halo_swap_cell_axis<L, TL, 0>(lo, hi, phase, i);
+    else if (axis == 1) halo_swap_cell_axis<L, TL, 1>(lo, hi, phase, i);
+    else halo_swap_cell_axis<L, TL, 2>(lo, hi, phase, i);
+}
+
+template <class L, class TL, int AXIS>
+__global__ void halo_swap_kernel(const Params lo, const Params hi, int phase)
+{
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < plane_cells) halo_cell<L, TL>(P, axis, side, phase, unpack, buf, i);
+    if (i < halo_plane_cells<AXIS>(lo)) halo_swap_cell_axis<L, TL, AXIS>(lo, hi, phase, i);
 }
 
 }  // namespace lbm

@@ -171,10 +171,14 @@ class SlabDomain:
     or have WALL faces (the end slabs keep them).
 
     ``overlap``: run each step as interior planes, then boundary planes, with the exchange
-    on a second stream beside the next step's interior (one device only)."""
+    on a second stream beside the next step's interior (one device only).
+    ``exchange``: as for BlockDomain ("auto": the buffer-free swap on one device)."""
 
-    def __init__(self, w, nslabs: int, devices=None, overlap: bool = False):
+    def __init__(self, w, nslabs: int, devices=None, overlap: bool = False,
+                 exchange: str = "auto"):
         import torch
+        if exchange not in ("auto", "swap", "buffers"):
+            raise ValueError("exchange must be 'auto', 'swap' or 'buffers'")
         self.w = w
         self.dim = w.dim
         self.axis, self.np_axis = outer_axis(w)
@@ -194,6 +198,9 @@ class SlabDomain:
             self.buffers.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
                                  for _ in range(2)])   # [low side, high side]
         self.multi_device = len({s.device for s in self.slabs}) > 1
+        if exchange == "swap" and self.multi_device:
+            raise ValueError("the buffer-free swap needs every slab on one device")
+        self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
         self.overlap = bool(overlap)
         if self.overlap and self.multi_device:
             raise ValueError("overlap needs every slab on one device")
@@ -224,6 +231,10 @@ class SlabDomain:
 
     def _exchange(self, phase: int):
         pairs = self.pairs()
+        if self.swap:
+            for a, b in pairs:
+                capi.lbm_halo_axis_swap(self.slabs[a].ctx, self.slabs[b].ctx, self.axis, phase)
+            return
         for a, b in pairs:
             capi.lbm_halo_pack(self.slabs[a].ctx, 1, phase, self.buffers[a][1])
             capi.lbm_halo_pack(self.slabs[b].ctx, 0, phase, self.buffers[b][0])
@@ -627,10 +638,16 @@ class BlockDomain:
     """The workload ``w`` cut into nb = (bx, by, bz) blocks (block_counts picks nb for a
     number of pieces), block b on ``devices[b % len(devices)]``, all driven from this
     process.  Each step is followed by the exchange of every split axis, z then y then x;
-    between steps every owned cell holds what one undivided domain would hold."""
+    between steps every owned cell holds what one undivided domain would hold.
 
-    def __init__(self, w, nb, devices=None):
+    ``exchange``: "swap" moves each face with one buffer-free kernel (lbm_halo_axis_swap,
+    blocks on one device), "buffers" packs, copies and unpacks; "auto" takes the swap on one
+    device."""
+
+    def __init__(self, w, nb, devices=None, exchange: str = "auto"):
         import torch
+        if exchange not in ("auto", "swap", "buffers"):
+            raise ValueError("exchange must be 'auto', 'swap' or 'buffers'")
         nb = tuple(int(v) for v in nb)
         if len(nb) != 3 or min(nb) < 1:
             raise ValueError("nb must be three positive block counts")
@@ -654,6 +671,9 @@ class BlockDomain:
             self.coords.append(coords)
             self.buffers.append(bufs)
         self.multi_device = len({s.device for s in self.blocks}) > 1
+        if exchange == "swap" and self.multi_device:
+            raise ValueError("the buffer-free swap needs every block on one device")
+        self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
 
     @property
     def parity(self) -> int:
@@ -677,6 +697,10 @@ class BlockDomain:
     def _exchange(self, phase: int):
         for a in exchange_axes(self.dim, self.nb):
             pairs = self.pairs(a)
+            if self.swap:
+                for lo, hi in pairs:
+                    capi.lbm_halo_axis_swap(self.blocks[lo].ctx, self.blocks[hi].ctx, a, phase)
+                continue
             for lo, hi in pairs:
                 capi.lbm_halo_axis_pack(self.blocks[lo].ctx, a, 1, phase, self.buffers[lo][a][1])
                 capi.lbm_halo_axis_pack(self.blocks[hi].ctx, a, 0, phase, self.buffers[hi][a][0])
@@ -747,6 +771,10 @@ class BlockDomain:
                 "force": total("force"), "heat": total("heat"),
                 "fluid_cells": sum(d["fluid_cells"] for d in ds),
                 "finite": all(d["finite"] for d in ds)}
+
+    def halo_launches_per_step(self) -> int:
+        faces = sum(len(self.pairs(a)) for a in exchange_axes(self.dim, self.nb))
+        return faces if self.swap else 4 * faces
 
     def halo_bytes_per_step(self) -> float:
         """Bytes the exchanges move between blocks per time step (both ways, every face)."""

@@ -416,8 +416,8 @@ int run_slabs(const lbm_config &cfg, const float *rho, const float *u, const flo
 // three hops.  The owned cells' logical populations are gathered into fout, gout.
 template <class L, class TL, int C, bool NARROW>
 int run_blocks(const lbm_config &cfg, const float *rho, const float *u, const float *T,
-               int steps, const int *nb, const int *const *edges, int ordered, float *fout,
-               float *gout)
+               int steps, const int *nb, const int *const *edges, int ordered, int swap,
+               float *fout, float *gout)
 {
     using Dom = Domain<L, TL, C, NARROW>;
     const int dim = L::DIM;
@@ -498,6 +498,20 @@ int run_blocks(const lbm_config &cfg, const float *rho, const float *u, const fl
         };
         for (int a = dim - 1; a >= 0; --a) {
             if (nb[a] < 2) continue;
+            if (swap) {   // the buffer-free form, one face after another
+                for (int b = 0; b < nblocks; ++b) {
+                    const Block &B = blocks[b];
+                    if (!B.high[a]) continue;
+                    int j[3] = {B.bi[0], B.bi[1], B.bi[2]};
+                    j[a] = (j[a] + 1) % nb[a];
+                    const Block &H = blocks[block_at(j[0], j[1], j[2])];
+                    const int u0 = a == 0 ? 1 : 0, v0 = a == 2 ? 1 : 2;
+                    const int cells = B.ext[u0] * B.ext[v0];
+                    for (int i = 0; i < cells; ++i)
+                        halo_swap_cell<L, TL>(B.d->P, H.d->P, a, phase, i);
+                }
+                continue;
+            }
             // pairs (block, its high neighbour along a), with the wrap on a periodic axis
             std::vector<std::pair<int, int>> pairs;
             for (int b = 0; b < nblocks; ++b) {
@@ -840,10 +854,11 @@ extern "C" int emu_run_slabs(const lbm_config *cfg, const float *rho, const floa
 // Block decomposition of the whole domain cfg (AA layout), see run_blocks: nb[3] pieces per
 // axis, edges the concatenated plane lists (nb[0] + 1 entries for x, then y, then z).
 // ordered = 0 packs every axis before any unpack (the diagonal hops then have nothing to
-// carry): a negative control for the tests.
+// carry): a negative control for the tests.  swap = 1 moves each face with halo_swap_cell
+// (no buffer) instead of a pack and an unpack.
 extern "C" int emu_run_blocks(const lbm_config *cfg, const float *rho, const float *u,
                               const float *T, int steps, const int *nb, const int *edges,
-                              int ordered, float *fout, float *gout)
+                              int ordered, int swap, float *fout, float *gout)
 {
     lbm_setup::Layout Lay;
     std::string why;
@@ -853,7 +868,7 @@ extern "C" int emu_run_blocks(const lbm_config *cfg, const float *rho, const flo
         if (nb[a] < 1) return -3;
     const int *e[3] = {edges, edges + nb[0] + 1, edges + nb[0] + nb[1] + 2};
     const bool mrt = cfg->collision == LBM_MRT;
-#define LBM_EMU_BLOCKS(Lt, Tt, Ct) run_blocks<Lt, Tt, Ct, true>(*cfg, rho, u, T, steps, nb, e, ordered, fout, gout)
+#define LBM_EMU_BLOCKS(Lt, Tt, Ct) run_blocks<Lt, Tt, Ct, true>(*cfg, rho, u, T, steps, nb, e, ordered, swap, fout, gout)
     if (cfg->lattice == 27) return LBM_EMU_BLOCKS(D3Q27, NoThermal, 2);
     if (cfg->lattice == 19) {
         if (cfg->thermal == 7)
@@ -864,6 +879,58 @@ extern "C" int emu_run_blocks(const lbm_config *cfg, const float *rho, const flo
         return mrt ? LBM_EMU_BLOCKS(D2Q9, D2Q5, 1) : LBM_EMU_BLOCKS(D2Q9, D2Q5, 0);
     return mrt ? LBM_EMU_BLOCKS(D2Q9, NoThermal, 1) : LBM_EMU_BLOCKS(D2Q9, NoThermal, 0);
 #undef LBM_EMU_BLOCKS
+}
+
+// div_by against the quotient for divisor d at the numerators n_lo .. n_hi (inclusive) and at
+// every multiple of d, and one below it, up to 2^31 - 1 (at most `multiples` of them):
+// returns the number of wrong quotients.
+extern "C" long long emu_divisor_errors(unsigned d, unsigned n_lo, unsigned n_hi,
+                                        long long multiples)
+{
+    const Divisor dv = lbm_setup::divisor(d);
+    long long bad = 0;
+    for (unsigned long long n = n_lo; n <= n_hi; ++n)
+        bad += div_by((unsigned)n, dv) != (unsigned)(n / d);
+    const unsigned long long top = (1ull << 31) - 1;
+    const unsigned long long step = std::max<unsigned long long>(
+        d, (top / d / (unsigned long long)std::max<long long>(multiples, 1)) * d);
+    for (unsigned long long k = d; k <= top; k += step)
+        for (unsigned long long n : {k - 1, k, std::min(k + d - 1, top)})
+            bad += div_by((unsigned)n, dv) != (unsigned)(n / d);
+    bad += div_by((unsigned)top, dv) != (unsigned)(top / d);
+    return bad;
+}
+
+// The linear AA launch's cell mapping over the planes [lo, hi) of a grid: every thread index
+// below the range's cell count names a distinct cell of those planes, in storage order, and
+// the next index none.  Returns the number of violations.
+extern "C" long long emu_linear_mapping_errors(int dim, int nx, int ny, int nz, int lo, int hi)
+{
+    Params P{};
+    P.nx = nx;
+    P.ny = ny;
+    P.nz = nz;
+    P.plane_lo = lo;
+    P.plane_hi = hi;
+    P.linear = 1;
+    P.div_nx = lbm_setup::divisor((unsigned)nx);
+    P.div_ny = lbm_setup::divisor((unsigned)ny);
+    const long long plane = dim == 3 ? (long long)nx * ny : nx;
+    const long long cells = plane * (hi - lo);
+    long long bad = 0;
+    for (long long t = 0; t <= cells; ++t) {
+        int x = -1, y = -1, z = -1;
+        const bool in = dim == 3 ? linear_cell_coords<D3Q19>(P, (int)t, x, y, z)
+                                 : linear_cell_coords<D2Q9>(P, (int)t, x, y, z);
+        if (t == cells) {
+            bad += in;
+            break;
+        }
+        const long long idx = x + (long long)nx * (y + (long long)ny * z);
+        bad += !in || x < 0 || x >= nx || y < 0 || y >= ny || z < 0 || z >= nz ||
+               idx != lo * plane + t;
+    }
+    return bad;
 }
 
 // Every neighbour index the odd-step access pattern forms (idx + offset of +-c_q for each

@@ -130,11 +130,11 @@ def emulate_slabs(emu_lib, w, steps, nslabs):
     return fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid)
 
 
-def emulate_blocks(emu_lib, w, steps, nb, edges=None, ordered=True):
+def emulate_blocks(emu_lib, w, steps, nb, edges=None, ordered=True, swap=False):
     """(f, g) of the whole domain after ``steps`` steps of the host emulation run as
     nb = (bx, by, bz) blocks with the library's per-axis halo exchange.  edges: per axis the
     block boundaries (default: as even as possible).  ordered=False packs every axis before
-    any unpack (a negative control)."""
+    any unpack (a negative control); swap=True moves each face with the buffer-free swap."""
     from lattice_boltzmann_cfd_gb300.slabs import split_ranges
     cfg, keep = make_config(w, "aa")
     N = w.cells
@@ -152,7 +152,7 @@ def emulate_blocks(emu_lib, w, steps, nb, edges=None, ordered=True):
     nbs = np.array(nb, np.int32)
     vp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     rc = emu_lib.emu_run_blocks(ctypes.byref(cfg), vp(rho), vp(u), vp(T), int(steps), vp(nbs),
-                                vp(flat), int(bool(ordered)), vp(fo), vp(go))
+                                vp(flat), int(bool(ordered)), int(bool(swap)), vp(fo), vp(go))
     assert rc == 0, rc
     return fo.reshape((w.lattice,) + w.grid), go.reshape((max(w.thermal, 1),) + w.grid)
 

@@ -54,6 +54,34 @@ def test_neighbour_indices_stay_in_grid(emu_lib, lattice, shape):
     assert emu_lib.emu_count_bad_indices(lattice, *shape) == 0
 
 
+@pytest.mark.parametrize("d", [1, 2, 3, 7, 9, 31, 33, 63, 65, 70, 255, 257, 258, 300, 1000,
+                               4095, 4097, 65535, 65537, 1 << 20, (1 << 20) + 1,
+                               (1 << 30) + 3, (1 << 31) - 1, 1 << 31])
+def test_division_by_multiply_and_shift(emu_lib, d):
+    """The step kernels' division by an invariant divisor (multiply, shift) equals the
+    quotient for the numerators 0 .. 70000, and around every sampled multiple of d up to
+    2^31 - 1."""
+    import ctypes
+    emu_lib.emu_divisor_errors.restype = ctypes.c_longlong
+    emu_lib.emu_divisor_errors.argtypes = [ctypes.c_uint, ctypes.c_uint, ctypes.c_uint,
+                                           ctypes.c_longlong]
+    assert emu_lib.emu_divisor_errors(d, 0, 70000, 200000) == 0
+    assert emu_lib.emu_divisor_errors(d, (1 << 31) - 70000, (1 << 31) - 1, 10) == 0
+
+
+@pytest.mark.parametrize("dim,shape,lo,hi", [
+    (3, (258, 7, 5), 0, 5), (3, (258, 7, 5), 2, 4), (3, (33, 1, 3), 0, 3), (3, (1, 1, 1), 0, 1),
+    (3, (70, 40, 37), 1, 36), (2, (300, 181, 1), 0, 181), (2, (300, 181, 1), 179, 181),
+    (2, (65, 3, 1), 1, 2)])
+def test_linear_step_launch_covers_each_cell_once(emu_lib, dim, shape, lo, hi):
+    """The 1-D step launch used when rows are not a multiple of 32 cells: thread t of the
+    planes [lo, hi) is cell lo * plane + t in storage order, and the thread after the last
+    cell is outside."""
+    import ctypes
+    emu_lib.emu_linear_mapping_errors.restype = ctypes.c_longlong
+    assert emu_lib.emu_linear_mapping_errors(dim, *shape, lo, hi) == 0
+
+
 # ------------------------------------------------------------- slab decomposition ---
 
 SLAB_CASES = slab_cases() + [outer_walls_case()]
@@ -98,19 +126,21 @@ def _block_layouts(w):
 @pytest.mark.parametrize("w", SLAB_CASES, ids=[c.name for c in SLAB_CASES])
 def test_blocks_match_single_domain_bitwise(emu_lib, w):
     """The domain run as blocks split along several axes, exchanging axis by axis (z, y, x)
-    after every step, holds bit for bit the single domain's state at both parities.  The
+    after every step, through buffers or with the buffer-free swap, holds bit for bit the
+    single domain's state at both parities.  The
     links that cross a block's edge or corner go to the diagonal neighbour through the ghost
     rows of the axis exchanged before, so a missing hop would leave a NaN or a stale value
     at the cells along the edges."""
     for n in (1, 2, 5, 6):
         f1, g1, _ = emulate(emu_lib, w, n)
         for nb in _block_layouts(w):
-            fb, gb = emulate_blocks(emu_lib, w, n, nb)
-            assert not np.isnan(fb).any(), (n, nb)
-            assert np.array_equal(fb, f1), (n, nb)
-            if w.thermal:
-                assert not np.isnan(gb).any(), (n, nb)
-                assert np.array_equal(gb, g1), (n, nb)
+            for swap in (False, True):
+                fb, gb = emulate_blocks(emu_lib, w, n, nb, swap=swap)
+                assert not np.isnan(fb).any(), (n, nb, swap)
+                assert np.array_equal(fb, f1), (n, nb, swap)
+                if w.thermal:
+                    assert not np.isnan(gb).any(), (n, nb, swap)
+                    assert np.array_equal(gb, g1), (n, nb, swap)
 
 
 def test_blocks_along_the_slab_axis_equal_slabs(emu_lib):

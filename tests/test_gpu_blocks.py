@@ -58,9 +58,9 @@ def _same_family(w, nb):
     return all(_masked(block_part(w, nb, b)[0]) == want for b in range(nb[0] * nb[1] * nb[2]))
 
 
-def _blocks(w, nb, chunks):
+def _blocks(w, nb, chunks, exchange="auto"):
     from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
-    dom = BlockDomain(w, nb)
+    dom = BlockDomain(w, nb, exchange=exchange)
     dom.init_equilibrium()
     for c in chunks:
         dom.step(c)
@@ -96,14 +96,16 @@ def _layouts(w):
 
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
 def test_blocks_equal_single_domain(oracle_mod, w):
-    """Each block layout against the undivided domain (bitwise where the kernel families
-    agree) and the fp64 oracle (1e-6 on the populations, 2e-5 on rho, u, T), at 7 and 8
-    steps; the summed diagnostics agree with the undivided domain's."""
+    """Each block layout, exchanged with the buffer-free swap (and one layout through
+    buffers), against the undivided domain (bitwise where the kernel families agree) and the
+    fp64 oracle (1e-6 on the populations, 2e-5 on rho, u, T), at 7 and 8 steps; the summed
+    diagnostics agree with the undivided domain's."""
     ref = oracle_states(oracle_mod, w, [7, 8])
     for steps in (7, 8):
         f1, g1, d1 = _single(w, steps)
-        for nb in _layouts(w):
-            got, ds = _blocks(w, nb, [3, steps - 3])
+        runs = [(nb, "swap") for nb in _layouts(w)] + [(_layouts(w)[-1], "buffers")]
+        for nb, exchange in runs:
+            got, ds = _blocks(w, nb, [3, steps - 3], exchange)
             compare_fields(w, got, ref[steps], tol=TOL_FIELDS, pop_tol=1e-6)
             if _same_family(w, nb):
                 assert np.array_equal(got["f"], f1), (steps, nb)
@@ -177,6 +179,43 @@ def test_axis_halo_calls_are_checked():
     capi.lbm_halo_axis_unpack(sim.ctx, 0, 0, capi.LBM_HALO_DRAIN, buf)
     torch.cuda.synchronize()
     sim.close()
+
+
+def test_swap_calls_are_checked():
+    """lbm_halo_axis_swap: both faces HALO, the same step, lattices and face extents."""
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    base = W.random_periodic(shape=(16, 8, 10), seed=90)
+    w = dataclasses.replace(base, face_flow=("periodic",) * 4 + ("halo", "halo"))
+    a, b = Simulation(w), Simulation(w)
+    wz = dataclasses.replace(w, shape=(16, 8, 7), rho0=w.rho0[:7], u0=w.u0[:, :7])
+    c = Simulation(wz)                                   # another z extent: still one face
+    wy = dataclasses.replace(w, shape=(16, 9, 10), rho0=np.ones((10, 9, 16), np.float32),
+                             u0=np.zeros((3, 10, 9, 16), np.float32))
+    d = Simulation(wy)                                   # another y extent: not the same face
+    for sim, ww in ((a, w), (b, w), (c, wz), (d, wy)):
+        sim.init_equilibrium(_dev(ww.rho0), _dev(ww.u0))
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_axis_swap(a.ctx, b.ctx, 2, capi.LBM_HALO_FILL)     # parity 0
+    for sim in (a, b, c, d):
+        sim.step(1)
+    capi.lbm_halo_axis_swap(a.ctx, b.ctx, 2, capi.LBM_HALO_FILL)
+    capi.lbm_halo_axis_swap(a.ctx, c.ctx, 2, capi.LBM_HALO_FILL)
+    capi.lbm_halo_axis_swap(a.ctx, a.ctx, 2, capi.LBM_HALO_FILL)         # a ring of one
+    for args in ((a.ctx, d.ctx, 2, capi.LBM_HALO_FILL),                  # faces differ
+                 (a.ctx, b.ctx, 0, capi.LBM_HALO_FILL),                  # x is periodic
+                 (a.ctx, b.ctx, 3, capi.LBM_HALO_FILL),
+                 (a.ctx, b.ctx, 2, capi.LBM_HALO_DRAIN),                 # parity 1
+                 (a.ctx, b.ctx, 2, 7)):
+        with pytest.raises(capi.LbmError):
+            capi.lbm_halo_axis_swap(*args)
+    b.step(1)
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_axis_swap(a.ctx, b.ctx, 2, capi.LBM_HALO_FILL)     # not the same step
+    a.step(1)
+    capi.lbm_halo_axis_swap(a.ctx, b.ctx, 2, capi.LBM_HALO_DRAIN)
+    torch.cuda.synchronize()
+    for sim in (a, b, c, d):
+        sim.close()
 
 
 # ------------------------------------------------------------- one block per rank ---

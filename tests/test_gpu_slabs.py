@@ -42,10 +42,10 @@ def _single(w, steps):
     return out
 
 
-def _slabs(w, steps, nslabs, chunks=None, fields=False):
+def _slabs(w, steps, nslabs, chunks=None, fields=False, exchange="auto"):
     """(f, g, diagnostics) of the slab run, plus its (rho, u, T) when ``fields``."""
     from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
-    dom = SlabDomain(w, nslabs)
+    dom = SlabDomain(w, nslabs, exchange=exchange)
     dom.init_equilibrium()
     for c in chunks or [steps]:
         dom.step(c)
@@ -76,13 +76,16 @@ CASES = slab_cases() + _large_cases()
 @pytest.mark.parametrize("w", CASES, ids=[c.name for c in CASES])
 def test_slabs_bitwise_equal_single_domain(oracle_mod, w):
     """Every slab split matches the undivided domain bit for bit, and the fp64 oracle
-    (run on the undivided domain) within 1e-6 on the populations and 2e-5 on rho, u, T."""
+    (run on the undivided domain) within 1e-6 on the populations and 2e-5 on rho, u, T,
+    with the buffer-free swap and (3 slabs) through buffers."""
     n_outer = w.shape[w.dim - 1]
     ref = oracle_states(oracle_mod, w, [7, 8])
     for steps in (7, 8):
         f1, g1, d1 = _single(w, steps)
-        for k in sorted({2, 3, n_outer if n_outer <= 13 else 5}):
-            fs, gs, ds, got = _slabs(w, steps, k, chunks=[3, steps - 3], fields=True)
+        counts = sorted({2, 3, n_outer if n_outer <= 13 else 5})
+        for k, exchange in [(k, "swap") for k in counts] + [(3, "buffers")]:
+            fs, gs, ds, got = _slabs(w, steps, k, chunks=[3, steps - 3], fields=True,
+                                     exchange=exchange)
             compare_fields(w, got, ref[steps], tol=TOL_FIELDS, pop_tol=1e-6)
             assert np.array_equal(fs, f1), (steps, k)
             if w.thermal:
