@@ -71,6 +71,9 @@ def make_workload(name: str):
         "d3q19_mrt_periodic_512": lambda: W.random_periodic(n=512, seed=2),
         "d3q19_mrt_periodic_256": lambda: W.random_periodic(n=256, seed=2),
         "d3q19_mrt_periodic_128": lambda: W.random_periodic(n=128, seed=2),
+        # rows of 258 cells: the step kernels' 1-D launch over the cells
+        "d3q19_mrt_periodic_258x256x256": lambda: W.random_periodic(shape=(258, 256, 256),
+                                                                    seed=2),
         "cavity3d_256": lambda: W.cavity3d(n=256),
         "taylor_green_32": lambda: W.taylor_green(),
         "channel_sphere_128": lambda: W.channel_sphere(),

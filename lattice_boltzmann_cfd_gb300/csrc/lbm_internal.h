@@ -58,15 +58,16 @@ inline Shape cell_shape(int nx, int ny, int nz, int threads = 64)
 }
 
 // The AA step kernels' launch over the outer-axis planes [lo, hi): cell_shape's grid cut to
-// those planes when rows are a multiple of 32 cells; otherwise (linear) a 1-D grid of
-// 64-thread blocks over the planes' cells in storage order (Params::linear).
+// those planes when rows are a multiple of 32 cells; otherwise (linear) 64-thread blocks over
+// the cells in storage order (Params::linear): in 3-D, blocks along each z plane (grid.x)
+// and one grid row per plane (grid.y); in 2-D, along the rows [lo, hi) as one run.
 inline Shape step_shape(int nx, int ny, int nz, int dim, int lo, int hi, bool linear)
 {
     Shape s;
     if (linear) {
-        const long long cells = (long long)(dim == 3 ? (long long)nx * ny : nx) * (hi - lo);
         s.block = dim3(64, 1, 1);
-        s.grid = dim3((unsigned)((cells + 63) / 64), 1, 1);
+        if (dim == 3) s.grid = dim3((unsigned)(((long long)nx * ny + 63) / 64), (unsigned)(hi - lo), 1);
+        else s.grid = dim3((unsigned)(((long long)nx * (hi - lo) + 63) / 64), 1, 1);
         return s;
     }
     s = cell_shape(nx, ny, nz);

@@ -71,9 +71,9 @@ struct Params {
     int plane_lo, plane_hi;
     // AA step launches over rows that are not a multiple of 32 cells (linear = 1): one thread
     // per cell in storage order, so that no thread idles past the end of a row and every warp
-    // covers 32 consecutive cells; the coordinates come from dividing by nx and ny
+    // covers 32 consecutive cells; the coordinates come from dividing by nx
     int linear;
-    Divisor div_nx, div_ny;
+    Divisor div_nx;
     int box_lo[3], box_hi[3];  // solid cells' box widened by one (inclusive; empty: lo > hi)
     int face_dir[6];       // per face: 1 = Dirichlet wall (thermal)
     float T_wall[6];
@@ -541,21 +541,22 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     }
 }
 
-// Cell t (counted from the first cell of plane P.plane_lo, in storage order) of a linear AA
-// step launch; false past the last cell of plane P.plane_hi - 1.
+// Cell t of a linear AA step launch: in 3-D, cell t of outer-axis plane P.plane_lo + plane
+// in storage order; in 2-D, cell t counted from the first cell of row P.plane_lo.  false past
+// the plane (3-D) or past the last cell of row P.plane_hi - 1 (2-D).
 template <class L>
-LBM_HD bool linear_cell_coords(const Params &P, int t, int &x, int &y, int &z)
+LBM_HD bool linear_cell_coords(const Params &P, int t, int plane, int &x, int &y, int &z)
 {
-    const int plane = L::DIM == 3 ? P.nx * P.ny : P.nx;
-    const int i = P.plane_lo * plane + t;
-    if (i >= P.plane_hi * plane) return false;
-    const int q = (int)div_by((unsigned)i, P.div_nx);   // row index: y + ny z
-    x = i - q * P.nx;
     if constexpr (L::DIM == 3) {
-        z = (int)div_by((unsigned)q, P.div_ny);
-        y = q - z * P.ny;
+        if (t >= P.nx * P.ny) return false;
+        z = P.plane_lo + plane;
+        y = (int)div_by((unsigned)t, P.div_nx);
+        x = t - y * P.nx;
     } else {
-        y = q;
+        const int i = P.plane_lo * P.nx + t;
+        if (i >= P.plane_hi * P.nx) return false;
+        y = (int)div_by((unsigned)i, P.div_nx);
+        x = i - y * P.nx;
         z = 0;
     }
     return true;
@@ -569,7 +570,8 @@ template <class L>
 LBM_HD bool step_cell_coords(const Params &P, int &x, int &y, int &z)
 {
 #if defined(__CUDA_ARCH__)
-    if (P.linear) return linear_cell_coords<L>(P, blockIdx.x * blockDim.x + threadIdx.x, x, y, z);
+    if (P.linear)
+        return linear_cell_coords<L>(P, blockIdx.x * blockDim.x + threadIdx.x, blockIdx.y, x, y, z);
     x = blockIdx.x * blockDim.x + threadIdx.x;
     y = blockIdx.y * blockDim.y + threadIdx.y;
     z = blockIdx.z;

@@ -305,7 +305,6 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
     P.plane_hi = n_outer;
     P.linear = g.nx % 32 != 0;
     P.div_nx = divisor((unsigned)g.nx);
-    P.div_ny = divisor((unsigned)g.ny);
     // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)
     const double omega = (g.thermal == LBM_D2Q5) ? (4.0 + g.a_T) / 10.0 : (6.0 + g.a_T) / 21.0;
     for (int k = 0; k < 7; ++k) P.abbT[k] = 0.0f;

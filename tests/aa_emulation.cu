@@ -901,9 +901,10 @@ extern "C" long long emu_divisor_errors(unsigned d, unsigned n_lo, unsigned n_hi
     return bad;
 }
 
-// The linear AA launch's cell mapping over the planes [lo, hi) of a grid: every thread index
-// below the range's cell count names a distinct cell of those planes, in storage order, and
-// the next index none.  Returns the number of violations.
+// The linear AA launch's cell mapping over the planes [lo, hi) of a grid (3-D: one grid row
+// per plane, threads along the plane; 2-D: threads along the rows [lo, hi)): every thread
+// index below the range's cell count names a distinct cell of those planes, in storage order,
+// and the next index none.  Returns the number of violations.
 extern "C" long long emu_linear_mapping_errors(int dim, int nx, int ny, int nz, int lo, int hi)
 {
     Params P{};
@@ -914,21 +915,29 @@ extern "C" long long emu_linear_mapping_errors(int dim, int nx, int ny, int nz, 
     P.plane_hi = hi;
     P.linear = 1;
     P.div_nx = lbm_setup::divisor((unsigned)nx);
-    P.div_ny = lbm_setup::divisor((unsigned)ny);
-    const long long plane = dim == 3 ? (long long)nx * ny : nx;
-    const long long cells = plane * (hi - lo);
     long long bad = 0;
-    for (long long t = 0; t <= cells; ++t) {
-        int x = -1, y = -1, z = -1;
-        const bool in = dim == 3 ? linear_cell_coords<D3Q19>(P, (int)t, x, y, z)
-                                 : linear_cell_coords<D2Q9>(P, (int)t, x, y, z);
-        if (t == cells) {
-            bad += in;
-            break;
-        }
+    auto check = [&](bool in, int x, int y, int z, long long want) {
         const long long idx = x + (long long)nx * (y + (long long)ny * z);
-        bad += !in || x < 0 || x >= nx || y < 0 || y >= ny || z < 0 || z >= nz ||
-               idx != lo * plane + t;
+        bad += !in || x < 0 || x >= nx || y < 0 || y >= ny || z < 0 || z >= nz || idx != want;
+    };
+    if (dim == 3) {
+        const long long plane = (long long)nx * ny;
+        for (int p = 0; p < hi - lo; ++p) {
+            for (long long t = 0; t <= plane; ++t) {
+                int x = -1, y = -1, z = -1;
+                const bool in = linear_cell_coords<D3Q19>(P, (int)t, p, x, y, z);
+                if (t == plane) bad += in;
+                else check(in, x, y, z, (lo + p) * plane + t);
+            }
+        }
+    } else {
+        const long long cells = (long long)nx * (hi - lo);
+        for (long long t = 0; t <= cells; ++t) {
+            int x = -1, y = -1, z = -1;
+            const bool in = linear_cell_coords<D2Q9>(P, (int)t, 0, x, y, z);
+            if (t == cells) bad += in;
+            else check(in, x, y, z, (long long)lo * nx + t);
+        }
     }
     return bad;
 }
