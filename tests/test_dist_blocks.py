@@ -141,3 +141,46 @@ def test_block_parts_tile_the_domain(nb):
     local, sides, _ = block_part(wp, (2, 1, 3), 0)
     assert sides[0] == (True, True) and sides[1] == (False, False) and sides[2] == (True, True)
     assert local.face_flow == ("halo", "halo", "periodic", "periodic", "halo", "halo")
+
+
+def _dying_block(rank, world, port, out):
+    import datetime
+    import time
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import torch.distributed as dist
+    from lattice_boltzmann_cfd_gb300.slabs import block_exchange
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=8))
+    dist.barrier()
+    if rank == 3:
+        os._exit(0)                  # leaves between steps: no exchange in flight
+    send = [[torch.zeros(4), torch.zeros(4)] for _ in range(3)]
+    recv = [[torch.zeros(4), torch.zeros(4)] for _ in range(3)]
+    t0 = time.time()
+    try:
+        block_exchange(rank, (2, 2, 1), (True, True, True), 3, 0,
+                       lambda a, s, p, b: b.fill_(1.0), lambda a, s, p, b: None, send, recv)
+        out[rank] = ("completed", 0.0)
+    except Exception as e:           # the back-end reports the lost peer
+        out[rank] = (type(e).__name__, time.time() - t0)
+
+
+def test_lost_block_fails_its_neighbours_next_exchange():
+    """In a 2 x 2 split, a rank that leaves between steps makes the exchange of each block
+    that faces it (along y, then along x) raise instead of waiting forever."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_dying_block, args=(r, 4, port, out)) for r in range(4)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        # blocks 1 (x-neighbour of 3) and 2 (y-neighbour of 3) face the lost rank
+        for r in (1, 2):
+            kind, seconds = out[r]
+            assert kind != "completed", r
+            assert seconds < 30
