@@ -53,6 +53,70 @@ def outer_axis(w):
     return w.dim - 1, (0 if w.dim == 3 else 1)
 
 
+# ------------------------------------------------------------- whole-domain diagnostics ---
+
+# The extensive sums of lbm_diagnostics, in the order diag_vector packs them.
+_DIAG_SUMS = (("mass", 1), ("momentum", 3), ("force", 3), ("heat", 6), ("uT", 3),
+              ("fluid_cells", 1))
+
+
+def diag_vector(d: dict):
+    """The extensive sums of one part's diagnostics as a flat list, then 0 / 1 for finite /
+    not finite (so that a sum over parts counts the parts that are not)."""
+    v = []
+    for key, n in _DIAG_SUMS:
+        v += [float(x) for x in (d[key] if n > 1 else [d[key]])]
+    return v + [0.0 if d["finite"] else 1.0]
+
+
+def combine_diagnostics(w, v) -> dict:
+    """Whole-domain diagnostics of workload ``w`` from the summed diag_vector of its parts
+    (slabs or blocks, each of which leaves its ghost cells out): the sums, and the Nusselt
+    numbers recomputed from them with the whole domain's extents, as lbm_diagnostics does for
+    one domain (wall heat |heat| H / (dT A) of the hottest and coldest DIRICHLET faces, and
+    the volume average 1 + <u_a T> H / (kappa dT) along their axis)."""
+    from .solver import make_config
+    out, i = {}, 0
+    for key, n in _DIAG_SUMS:
+        out[key] = list(v[i:i + n]) if n > 1 else v[i]
+        i += n
+    out["fluid_cells"] = int(round(out["fluid_cells"]))
+    out["finite"] = v[i] == 0.0
+    out["nu_hot"] = out["nu_cold"] = out["nu_volume"] = 0.0
+    cfg, _ = make_config(w)
+    dirichlet = [f for f in range(2 * w.dim)
+                 if cfg.thermal and cfg.face_flow[f] == capi.LBM_FACE_WALL
+                 and cfg.face_T[f] == capi.LBM_TFACE_DIRICHLET]
+    if not dirichlet:
+        return out
+    hot = max(dirichlet, key=lambda f: (cfg.T_wall[f], -f))    # the first of equal faces
+    cold = min(dirichlet, key=lambda f: (cfg.T_wall[f], f))
+    dT = cfg.T_wall[hot] - cfg.T_wall[cold]
+    if dT <= 0:
+        return out
+    n = list(w.shape)
+    cells = n[0] * n[1] * n[2]
+    nusselt = lambda f: abs(out["heat"][f]) * n[f // 2] / (dT * cells / n[f // 2])
+    out["nu_hot"], out["nu_cold"] = nusselt(hot), nusselt(cold)
+    a = hot // 2
+    if cold // 2 == a and out["fluid_cells"] > 0:
+        omega = (4.0 + cfg.a_T) / 10.0 if cfg.thermal == 5 else (6.0 + cfg.a_T) / 21.0
+        kappa = omega * (1.0 / cfg.s_T[1 + a] - 0.5)
+        sign = 1.0 if hot % 2 == 0 else -1.0
+        out["nu_volume"] = 1.0 + sign * out["uT"][a] / out["fluid_cells"] * n[a] / (kappa * dT)
+    return out
+
+
+def allreduce_diagnostics(w, d: dict, group=None, device=None) -> dict:
+    """combine_diagnostics over every rank of a process group: one all-reduce (sum) of the
+    ranks' diag_vector, in fp64, on ``device`` (None: the CPU, for gloo)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(diag_vector(d), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM, group=group)
+    return combine_diagnostics(w, t.cpu().tolist())
+
+
 def slab_part(w, nslabs: int, r: int):
     """Slab r of ``w`` split into ``nslabs`` along its outer axis: (local workload, (low,
     high) ghost flags, the domain plane of each local plane).  A periodic outer axis wraps
@@ -326,13 +390,10 @@ class SlabDomain:
         return rho, u, T
 
     def diagnostics(self) -> dict:
-        """Sums over the slabs (each slab leaves its ghost planes out)."""
-        ds = [sim.diagnostics(allow_nonfinite=True) for sim in self.slabs]
-        total = lambda key: [float(v) for v in np.sum([d[key] for d in ds], axis=0)]
-        return {"mass": sum(d["mass"] for d in ds), "momentum": total("momentum"),
-                "force": total("force"), "heat": total("heat"),
-                "fluid_cells": sum(d["fluid_cells"] for d in ds),
-                "finite": all(d["finite"] for d in ds)}
+        """Whole-domain diagnostics: the slabs' sums (each slab leaves its ghost planes out)
+        and the Nusselt numbers from them (combine_diagnostics)."""
+        vs = [diag_vector(sim.diagnostics(allow_nonfinite=True)) for sim in self.slabs]
+        return combine_diagnostics(self.w, [float(x) for x in np.sum(vs, axis=0)])
 
     def halo_bytes_per_step(self) -> float:
         """Bytes the exchanges move between slabs per time step, averaged over a step pair
@@ -479,7 +540,14 @@ class DistSlabDomain:
         return self.owned(rho), self.owned(u, 1), (None if T is None else self.owned(T))
 
     def diagnostics(self) -> dict:
+        """This rank's own diagnostics (its owned cells)."""
         return self.sim.diagnostics(allow_nonfinite=True)
+
+    def global_diagnostics(self) -> dict:
+        """The whole domain's diagnostics: an all-reduce over the ranks (a collective: every
+        rank calls it), on the device for the device transport, on the CPU for the host one."""
+        dev = self.sim.device if self.transport == "device" else None
+        return allreduce_diagnostics(self.w, self.diagnostics(), self.group, dev)
 
     def close(self):
         self.sim.close()
@@ -764,13 +832,10 @@ class BlockDomain:
         return rho, u, T
 
     def diagnostics(self) -> dict:
-        """Sums over the blocks (each block leaves its ghost cells out)."""
-        ds = [sim.diagnostics(allow_nonfinite=True) for sim in self.blocks]
-        total = lambda key: [float(v) for v in np.sum([d[key] for d in ds], axis=0)]
-        return {"mass": sum(d["mass"] for d in ds), "momentum": total("momentum"),
-                "force": total("force"), "heat": total("heat"),
-                "fluid_cells": sum(d["fluid_cells"] for d in ds),
-                "finite": all(d["finite"] for d in ds)}
+        """Whole-domain diagnostics: the blocks' sums (each block leaves its ghost cells out)
+        and the Nusselt numbers from them (combine_diagnostics)."""
+        vs = [diag_vector(sim.diagnostics(allow_nonfinite=True)) for sim in self.blocks]
+        return combine_diagnostics(self.w, [float(x) for x in np.sum(vs, axis=0)])
 
     def halo_launches_per_step(self) -> int:
         faces = sum(len(self.pairs(a)) for a in exchange_axes(self.dim, self.nb))
@@ -861,7 +926,14 @@ class DistBlockDomain:
         return self.owned(rho), self.owned(u, 1), (None if T is None else self.owned(T))
 
     def diagnostics(self) -> dict:
+        """This rank's own diagnostics (its owned cells)."""
         return self.sim.diagnostics(allow_nonfinite=True)
+
+    def global_diagnostics(self) -> dict:
+        """The whole domain's diagnostics: an all-reduce over the ranks (a collective: every
+        rank calls it), on the device for the device transport, on the CPU for the host one."""
+        dev = self.sim.device if self.transport == "device" else None
+        return allreduce_diagnostics(self.w, self.diagnostics(), self.group, dev)
 
     def close(self):
         self.sim.close()

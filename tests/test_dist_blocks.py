@@ -184,3 +184,60 @@ def test_lost_block_fails_its_neighbours_next_exchange():
             kind, seconds = out[r]
             assert kind != "completed", r
             assert seconds < 30
+
+
+def _diag_worker(rank, world, port, out):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    import torch.distributed as dist
+    from lattice_boltzmann_cfd_gb300.slabs import allreduce_diagnostics
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    out[rank] = allreduce_diagnostics(_diag_case(), _fake_diag(rank))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def _diag_case():
+    return W.cavity3d(shape=(12, 10, 8))
+
+
+def _fake_diag(rank):
+    rng = np.random.default_rng(100 + rank)
+    return {"mass": float(rng.uniform(10, 20)), "momentum": list(rng.normal(size=3)),
+            "force": list(rng.normal(size=3)), "heat": list(rng.normal(size=6)),
+            "uT": list(rng.normal(size=3)), "fluid_cells": int(rng.integers(100, 200)),
+            "finite": rank != 2}
+
+
+def test_allreduce_diagnostics_sums_every_rank():
+    """The all-reduce of the ranks' sums (gloo, 3 ranks) equals combine_diagnostics of the
+    summed parts; one rank with a non-finite state makes the whole not finite; the Nusselt
+    numbers follow the whole domain's extents (the cavity's hot x = 0 and cold x = L faces)."""
+    import multiprocessing as mp
+    from lattice_boltzmann_cfd_gb300.slabs import combine_diagnostics, diag_vector
+    world = 3
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_diag_worker, args=(r, world, port, out))
+                 for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        want = combine_diagnostics(
+            _diag_case(), list(np.sum([diag_vector(_fake_diag(r)) for r in range(world)],
+                                      axis=0)))
+        for r in range(world):
+            got = out[r]
+            assert got["fluid_cells"] == want["fluid_cells"]
+            assert got["finite"] is False
+            for key in ("mass", "nu_hot", "nu_cold", "nu_volume"):
+                assert got[key] == pytest.approx(want[key], rel=1e-12, abs=1e-12), key
+            for key in ("momentum", "force", "heat", "uT"):
+                assert np.allclose(got[key], want[key], rtol=1e-12, atol=1e-12), key
+    # the wall heat of the hot face (x = 0, face 0) over the whole face: |heat| H / (dT A)
+    w = _diag_case()
+    heat0 = sum(_fake_diag(r)["heat"][0] for r in range(world))
+    assert want["nu_hot"] == pytest.approx(abs(heat0) * 12 / (1.0 * 10 * 8), rel=1e-12)

@@ -125,6 +125,12 @@ def test_blocks_equal_single_domain(oracle_mod, w):
             if w.thermal:
                 hscale = max(1e-30, float(np.abs(d1["heat"]).max()))
                 assert np.allclose(ds["heat"], d1["heat"], rtol=0, atol=1e-6 * hscale)
+                # the Nusselt numbers, recomputed from the parts' sums with the whole
+                # domain's extents, against the library's own on the undivided domain
+                assert np.allclose(ds["uT"], d1["uT"], rtol=0, atol=1e-7 * cells)
+                for key in ("nu_hot", "nu_cold"):
+                    assert abs(ds[key] - d1[key]) <= 1e-5 * max(1.0, abs(d1[key])), key
+                assert abs(ds["nu_volume"] - d1["nu_volume"]) <= 1e-3
 
 
 @pytest.mark.parametrize("w,nb", [
@@ -254,6 +260,7 @@ def _rank(rank, world, port, name, out):
         done = n
         f, g = d.populations()
         res[n] = (f.cpu().numpy(), None if g is None else g.cpu().numpy())
+    res["diag"] = d.global_diagnostics()      # a collective: every rank calls it
     out[rank] = res
     d.close()
     dist.barrier()
@@ -291,3 +298,14 @@ def test_four_ranks_share_the_gpu(oracle_mod, name):
         assert np.abs(f - ref[n]["f"]).max() <= 1e-6
         if w.thermal:
             assert np.abs(g - ref[n]["g"]).max() <= 1e-6
+    # the all-reduced diagnostics after the last step, against the undivided domain's
+    d1 = _single(w, STEPS[-1])[2]
+    for r in range(world):
+        dg = out[r]["diag"]
+        assert dg["fluid_cells"] == d1["fluid_cells"] and dg["finite"]
+        assert abs(dg["mass"] - d1["mass"]) <= 1e-9 * abs(d1["mass"])
+        assert np.allclose(dg["momentum"], d1["momentum"], rtol=0, atol=1e-7 * d1["fluid_cells"])
+        if w.thermal:
+            for key in ("nu_hot", "nu_cold"):
+                assert abs(dg[key] - d1[key]) <= 1e-5 * max(1.0, abs(d1[key])), key
+            assert abs(dg["nu_volume"] - d1["nu_volume"]) <= 1e-3

@@ -55,6 +55,7 @@ def _rank(rank, world, port, name, overlap, out):
         done = n
         f, g = d.populations()
         res[n] = (f.cpu().numpy(), None if g is None else g.cpu().numpy())
+    res["diag"] = d.global_diagnostics()      # a collective: every rank calls it
     out[rank] = res
     d.close()
     dist.barrier()
@@ -95,3 +96,19 @@ def test_two_ranks_share_the_gpu(oracle_mod, name, overlap):
         assert np.abs(f - ref[n]["f"])[:, fluid].max() <= 1e-6
         if w.thermal:
             assert np.abs(g - ref[n]["g"])[:, fluid].max() <= 1e-6
+    # the all-reduced diagnostics after the last step, against the undivided domain's
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    sim = Simulation(w)
+    dev = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    sim.init_equilibrium(dev(w.rho0), dev(w.u0), dev(w.T_init))
+    sim.step(STEPS[-1])
+    d1 = sim.diagnostics()
+    sim.close()
+    for r in range(2):
+        dg = out[r]["diag"]
+        assert dg["fluid_cells"] == d1["fluid_cells"] and dg["finite"]
+        assert abs(dg["mass"] - d1["mass"]) <= 1e-9 * abs(d1["mass"])
+        if w.thermal:
+            for key in ("nu_hot", "nu_cold"):
+                assert abs(dg[key] - d1[key]) <= 1e-5 * max(1.0, abs(d1[key])), key
+            assert abs(dg["nu_volume"] - d1["nu_volume"]) <= 1e-3

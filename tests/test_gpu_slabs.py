@@ -82,7 +82,7 @@ def test_slabs_bitwise_equal_single_domain(oracle_mod, w):
     ref = oracle_states(oracle_mod, w, [7, 8])
     for steps in (7, 8):
         f1, g1, d1 = _single(w, steps)
-        counts = sorted({2, 3, n_outer if n_outer <= 13 else 5})
+        counts = sorted({1, 2, 3, n_outer if n_outer <= 13 else 5})   # 1: a ring of one slab
         for k, exchange in [(k, "swap") for k in counts] + [(3, "buffers")]:
             fs, gs, ds, got = _slabs(w, steps, k, chunks=[3, steps - 3], fields=True,
                                      exchange=exchange)
@@ -102,6 +102,12 @@ def test_slabs_bitwise_equal_single_domain(oracle_mod, w):
             if w.thermal:
                 hscale = max(1e-30, float(np.abs(d1["heat"]).max()))
                 assert np.allclose(ds["heat"], d1["heat"], rtol=0, atol=1e-6 * hscale)
+                # the Nusselt numbers, recomputed from the parts' sums with the whole
+                # domain's extents, against the library's own on the undivided domain
+                assert np.allclose(ds["uT"], d1["uT"], rtol=0, atol=1e-7 * cells)
+                for key in ("nu_hot", "nu_cold"):
+                    assert abs(ds[key] - d1[key]) <= 1e-5 * max(1.0, abs(d1[key])), key
+                assert abs(ds["nu_volume"] - d1["nu_volume"]) <= 1e-3
 
 
 def test_walls_only_on_the_outer_axis(oracle_mod):
