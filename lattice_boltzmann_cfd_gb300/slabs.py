@@ -53,6 +53,24 @@ def outer_axis(w):
     return w.dim - 1, (0 if w.dim == 3 else 1)
 
 
+# ------------------------------------------------------------------ checkpoint / resume ---
+
+def part_of(t, coords, lead=1):
+    """The part of a whole-domain field t (``lead`` leading axes, then z, y, x) at the domain
+    coordinates coords = (x list, y list, z list) of a part's local planes (ghost planes
+    included), as a contiguous tensor on t's device."""
+    import torch
+    for a, dim in ((2, lead), (1, lead + 1), (0, lead + 2)):
+        idx = torch.as_tensor(coords[a], dtype=torch.long, device=t.device)
+        t = torch.index_select(t, dim, idx)
+    return t.contiguous()
+
+
+def _as_tensor(a):
+    import torch
+    return a if a is None or isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))
+
+
 # ------------------------------------------------------------- whole-domain diagnostics ---
 
 # The extensive sums of lbm_diagnostics, in the order diag_vector packs them.
@@ -361,6 +379,23 @@ class SlabDomain:
                                    else capi.LBM_HALO_DRAIN)
         self._wait_pending()
 
+    def _coords(self, r):
+        """(x, y, z) domain coordinates of slab r's local planes."""
+        c = [list(range(n)) for n in self.w.shape]
+        c[self.axis] = list(self.plane_lists[r])
+        return c
+
+    def set_populations(self, f, g=None):
+        """Resume from whole-domain logical populations (Q, nz, ny, nx) as populations()
+        returns them, from any decomposition or none: each slab takes its planes, its ghost
+        planes included, so the exchange state is the one the step after needs at either
+        parity."""
+        f, g = _as_tensor(f), _as_tensor(g)
+        for r, sim in enumerate(self.slabs):
+            c = self._coords(r)
+            sim.set_populations(part_of(f, c).to(sim.device),
+                                None if g is None else part_of(g, c).to(sim.device))
+
     def _owned(self, t, r, lead=0):
         low, high = self.sides[r]
         idx = [slice(None)] * t.dim()
@@ -522,6 +557,14 @@ class DistSlabDomain:
                 self.sim.step(1)
             self._start_exchange()
         self._finish_exchange()
+
+    def set_populations(self, f, g=None):
+        """Resume this rank's slab from whole-domain logical populations (Q, nz, ny, nx)."""
+        c = [list(range(n)) for n in self.w.shape]
+        c[self.axis] = list(self.planes)
+        f, g = _as_tensor(f), _as_tensor(g)
+        self.sim.set_populations(part_of(f, c).to(self.sim.device),
+                                 None if g is None else part_of(g, c).to(self.sim.device))
 
     def owned(self, t, lead=0):
         """The owned planes of a local field (ghost planes dropped)."""
@@ -800,6 +843,15 @@ class BlockDomain:
                 sim.step(1)
             self._exchange(capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN)
 
+    def set_populations(self, f, g=None):
+        """Resume from whole-domain logical populations (Q, nz, ny, nx) as populations()
+        returns them, from any decomposition or none: each block takes its cells, its ghost
+        cells included."""
+        f, g = _as_tensor(f), _as_tensor(g)
+        for sim, c in zip(self.blocks, self.coords):
+            sim.set_populations(part_of(f, c).to(sim.device),
+                                None if g is None else part_of(g, c).to(sim.device))
+
     def _gather(self, parts, lead=0):
         import torch
         dev = self.blocks[0].device
@@ -912,6 +964,12 @@ class DistBlockDomain:
                            self.send, self.recv, self.group, sync)
         if sync is not None:
             sync()
+
+    def set_populations(self, f, g=None):
+        """Resume this rank's block from whole-domain logical populations (Q, nz, ny, nx)."""
+        f, g = _as_tensor(f), _as_tensor(g)
+        self.sim.set_populations(part_of(f, self.coords).to(self.sim.device),
+                                 None if g is None else part_of(g, self.coords).to(self.sim.device))
 
     def owned(self, t, lead=0):
         """The owned cells of a local field (ghost planes dropped)."""

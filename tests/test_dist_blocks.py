@@ -241,3 +241,16 @@ def test_allreduce_diagnostics_sums_every_rank():
     w = _diag_case()
     heat0 = sum(_fake_diag(r)["heat"][0] for r in range(world))
     assert want["nu_hot"] == pytest.approx(abs(heat0) * 12 / (1.0 * 10 * 8), rel=1e-12)
+
+
+@pytest.mark.parametrize("nb", [(2, 2, 1), (1, 3, 2), (3, 2, 2)])
+def test_part_of_takes_a_parts_cells(nb):
+    """part_of cuts a whole-domain field at a part's coordinates, ghost planes included, as
+    block_part cuts the initial fields."""
+    from lattice_boltzmann_cfd_gb300.slabs import part_of
+    w = W.perturbed(W.cavity3d(shape=(7, 6, 5)), seed=5)
+    for b in range(nb[0] * nb[1] * nb[2]):
+        local, _, coords = block_part(w, nb, b)
+        assert np.array_equal(part_of(torch.from_numpy(w.rho0), coords, lead=0).numpy(),
+                              local.rho0)
+        assert np.array_equal(part_of(torch.from_numpy(w.u0), coords).numpy(), local.u0)
