@@ -529,14 +529,14 @@ def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None, overla
     return out
 
 
-def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None):
+def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None, overlap=False):
     """MLUPS of a workload cut into nb = (bx, by, bz) blocks on this GPU, with the per-axis
     halo exchange after every step (z, then y, then x; a step = one step launch per block +
     one pack and one unpack launch per block face and direction)."""
     import torch
     from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
     w = cached_workload(name)
-    dom = BlockDomain(w, nb)
+    dom = BlockDomain(w, nb, overlap=overlap)
     dom.init_equilibrium()
     dom.step(4)
     torch.cuda.synchronize()
@@ -558,6 +558,7 @@ def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None):
                             "exchanged axis by axis with the ghost rows of the other axes "
                             "(edges and corners in two or three hops), all on this GPU, each "
                             "face moved by one buffer-free swap kernel",
+           "overlap": bool(overlap),
            "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
            "halo_launches_per_step": launches}
     if single_mlups:
@@ -671,9 +672,9 @@ def run_gpu(args, dctx):
             for overlap in (False, True):
                 line["secondary"].append(run_slabs_secondary(n, 4, args.lbm_steps, 2,
                                                              single.get(lbl), overlap))
-            for nb in ((1, 2, 2), (1, 2, 4)):
+            for nb, overlap in (((1, 2, 2), False), ((1, 2, 2), True), ((1, 2, 4), False)):
                 line["secondary"].append(run_blocks_secondary(n, nb, args.lbm_steps, 2,
-                                                              single.get(lbl)))
+                                                              single.get(lbl), overlap))
         lbl = workload_label("cavity2d_4096", cached_workload("cavity2d_4096"))
         line["secondary"].append(run_blocks_secondary("cavity2d_4096", (2, 2, 1),
                                                       args.lbm_steps, 2, single.get(lbl)))

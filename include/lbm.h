@@ -197,21 +197,25 @@ lbm_status lbm_init_equilibrium(lbm_ctx *ctx, const float *rho, const float *u, 
  * of at most 4 M cells replay captured graphs of 64 steps. */
 lbm_status lbm_step(lbm_ctx *ctx, int n);
 
-/* One time step split across calls by outer-axis planes (z in 3-D, y in 2-D): each call
- * launches the current step (the same even or odd AA form lbm_step would launch) on the
- * planes [lo, hi) only.  The step is complete, and the parity and step count advance, once
- * the calls since the last complete step have covered every plane of [0, n_outer) exactly
- * once, in any order and any grouping; a slab's ghost planes may be included, they are
- * skipped.  The result is bit for bit that of lbm_step(1): even steps only touch their own
- * cells, and in the odd step every slot is read and then written by one cell alone.
- * This lets a slab driver overlap its halo exchange with the interior planes ([TLBM]
- * Sec. 4, overlapping communication with computation; see the halo calls below).
- * While a step is partly done, lbm_step, lbm_init_equilibrium, lbm_macroscopic,
- * lbm_diagnostics, lbm_solid_force and the population calls return LBM_ERR_STATE; the halo
- * calls are allowed.  Each call is one launch on the context's stream, not chained to
- * the work before it.  Errors: LBM_ERR_ARG for an empty or out-of-range range or a plane
- * already stepped in this step; LBM_ERR_UNSUPPORTED for the two-buffer layouts and for
- * contexts with immersed-boundary capacity. */
+/* One time step split across calls by boxes of cells: each call launches the current step
+ * (the same even or odd AA form lbm_step would launch) on the cells [lo, hi) only, lo and
+ * hi host arrays of 3 ints (x, y, z; in 2-D lo[2] = 0, hi[2] = 1).  The step is complete,
+ * and the parity and step count advance, once the calls since the last complete step have
+ * covered every cell exactly once, in any order and any grouping; ghost cells of a slab or
+ * block may be included, they are skipped.  The result is bit for bit that of lbm_step(1):
+ * even steps only touch their own cells, and in the odd step every slot is read and then
+ * written by one cell alone.  This lets a slab or block driver overlap its halo exchange
+ * with the interior cells ([TLBM] Sec. 4, overlapping communication with computation; see
+ * the halo calls below).  While a step is partly done, lbm_step, lbm_init_equilibrium,
+ * lbm_macroscopic, lbm_diagnostics, lbm_solid_force and the population calls return
+ * LBM_ERR_STATE; the halo calls are allowed.  Each call is one launch on the context's
+ * stream, not chained to the work before it.  Errors: LBM_ERR_ARG for an empty box, a box
+ * outside the grid, or one that overlaps a box already stepped in this step;
+ * LBM_ERR_UNSUPPORTED for the two-buffer layouts and for contexts with immersed-boundary
+ * capacity. */
+lbm_status lbm_step_box(lbm_ctx *ctx, const int *lo, const int *hi);
+
+/* lbm_step_box over the whole outer-axis planes [lo, hi) (z in 3-D, y in 2-D). */
 lbm_status lbm_step_planes(lbm_ctx *ctx, int lo, int hi);
 
 /* rho = sum f, u = (sum c f + F/2)/rho, T = sum g of the current state ([TLBM] Sec. 2).

@@ -72,6 +72,7 @@ SIGNATURES = [
     ("lbm_init_equilibrium", ctypes.c_int, [_VP, _VP, _VP, _VP]),
     ("lbm_step", ctypes.c_int, [_VP, ctypes.c_int]),
     ("lbm_step_planes", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int]),
+    ("lbm_step_box", ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     ("lbm_macroscopic", ctypes.c_int, [_VP, _VP, _VP, _VP]),
     ("lbm_solid_force", ctypes.c_int, [_VP, _D]),
     ("lbm_diagnostics", ctypes.c_int, [_VP, ctypes.POINTER(lbm_diag)]),
@@ -181,6 +182,13 @@ def lbm_step(ctx, n: int):
 
 def lbm_step_planes(ctx, lo: int, hi: int):
     _check(load().lbm_step_planes(ctx, int(lo), int(hi)), ctx)
+
+
+def lbm_step_box(ctx, lo, hi):
+    """The current step on the cells [lo, hi) (3 ints each: x, y, z)."""
+    a = (ctypes.c_int * 3)(*[int(v) for v in lo])
+    b = (ctypes.c_int * 3)(*[int(v) for v in hi])
+    _check(load().lbm_step_box(ctx, a, b), ctx)
 
 
 def lbm_macroscopic(ctx, rho=None, u=None, T=None):

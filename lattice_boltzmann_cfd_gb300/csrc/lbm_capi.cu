@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstring>
 #include <new>
+#include <array>
 #include <string>
 #include <utility>
 #include <algorithm>
@@ -51,8 +52,10 @@ struct lbm_ctx {
     long long steps = 0;
     bool initialized = false;
     // lbm_step_planes: outer-axis planes already stepped in the current (unfinished) step
-    std::vector<uint8_t> planes_done;
-    int planes_left = 0;   // > 0 while a step is partly done
+    // boxes of cells stepped so far in a step split across lbm_step_box calls, and the
+    // cells still to step (> 0 while a step is partly done)
+    std::vector<std::array<int, 6>> boxes_done;
+    long long cells_left = 0;
     int ib_order_n = -1;   // sample count of the stored sample order, -1 = none
     std::string err;
     // CUDA graphs of GRAPH_STEPS steps, one per start parity, built on first use for
@@ -233,7 +236,7 @@ lbm_status lbm_create(const lbm_config *cfg, void *d_workspace, size_t workspace
 lbm_status lbm_init_equilibrium(lbm_ctx *c, const float *rho, const float *u, const float *T)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
-    if (c->planes_left) return partly_stepped(c);
+    if (c->cells_left) return partly_stepped(c);
     if (!rho || !u) return fail(c, LBM_ERR_ARG, "rho and u are required");
     if (c->L.QT && !T) return fail(c, LBM_ERR_ARG, "T is required with a thermal lattice");
     DeviceGuard guard(c->device);
@@ -269,8 +272,9 @@ constexpr long long GRAPH_MAX_CELLS = 1LL << 22;   // launch-bound below ~4 M ce
 cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStream_t stream)
 {
     const lbm::Shape sh = lbm::cell_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz);
-    const lbm::Shape sh_aa = lbm::step_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz, c->L.dim, 0,
-                                             c->L.dim == 3 ? c->cfg.nz : c->cfg.ny, P.linear);
+    const int whole_lo[3] = {0, 0, 0}, whole_hi[3] = {c->cfg.nx, c->cfg.ny, c->cfg.nz};
+    const lbm::Shape sh_aa =
+        lbm::step_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz, c->L.dim, whole_lo, whole_hi, P.linear);
     // 32-bit population indices when the largest index (Q * S - 1) fits
     const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
     const bool d3 = c->cfg.lattice == LBM_D3Q19;
@@ -311,24 +315,29 @@ cudaError_t enqueue_step(const lbm_ctx *c, lbm::Params &P, int &parity, cudaStre
     return e;
 }
 
-// AA step kernel launch over the outer-axis planes [lo, hi) (lbm_step_planes).
-cudaError_t launch_planes(const lbm_ctx *c, const lbm::Params &P0, int parity, int lo, int hi,
-                          cudaStream_t stream, bool chained)
+// AA step kernel launch over the box of cells [lo, hi) (lbm_step_box).
+cudaError_t launch_box(const lbm_ctx *c, const lbm::Params &P0, int parity, const int lo[3],
+                       const int hi[3], cudaStream_t stream, bool chained)
 {
     const bool d2 = c->cfg.lattice == LBM_D2Q9;
-    const lbm::Shape sh =
-        lbm::step_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz, c->L.dim, lo, hi, P0.linear);
     lbm::Params P = P0;
-    P.plane_lo = lo;
-    P.plane_hi = hi;
+    bool linear = false;
+    const lbm::Shape sh =
+        lbm::step_shape(c->cfg.nx, c->cfg.ny, c->cfg.nz, c->L.dim, lo, hi, P0.linear, &linear);
+    P.linear = linear;
+    for (int a = 0; a < 3; ++a) {
+        P.run_lo[a] = lo[a];
+        P.run_hi[a] = hi[a];
+    }
     const bool narrow = (unsigned long long)c->L.Q * c->L.S <= 0xffffffffull;
     const int th = c->cfg.thermal, coll = c->cfg.collision;
     const int masked = !c->L.masked ? 0 : (c->L.ib_cap > 0 ? 2 : 1);
     const bool odd = parity != 0;
     if (c->cfg.lattice == LBM_D3Q27)
-        return lbm::launch_step_d3q27(masked, odd, narrow, P, sh, stream, chained);
-    return d2 ? lbm::launch_step_d2q9(th, coll, masked, odd, narrow, P, sh, stream, chained)
-              : lbm::launch_step_d3q19(th, coll, masked, odd, narrow, P, sh, stream, chained);
+        return lbm::launch_step_d3q27(masked, odd, narrow, P, sh, stream, chained, true);
+    return d2 ? lbm::launch_step_d2q9(th, coll, masked, odd, narrow, P, sh, stream, chained, true)
+              : lbm::launch_step_d3q19(th, coll, masked, odd, narrow, P, sh, stream, chained,
+                                       true);
 }
 
 // The graph of GRAPH_STEPS steps starting at the context's parity (built on first use).
@@ -370,7 +379,7 @@ lbm_status lbm_step(lbm_ctx *c, int n)
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (n < 0) return fail(c, LBM_ERR_ARG, "n must be >= 0");
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
-    if (c->planes_left) return partly_stepped(c);
+    if (c->cells_left) return partly_stepped(c);
     DeviceGuard guard(c->device);
     // Small grids: replay a captured graph of GRAPH_STEPS steps (it leaves the parity and
     // the buffers as it found them), then launch the remainder one by one.
@@ -392,46 +401,60 @@ lbm_status lbm_step(lbm_ctx *c, int n)
     return LBM_OK;
 }
 
-lbm_status lbm_step_planes(lbm_ctx *c, int lo, int hi)
+lbm_status lbm_step_box(lbm_ctx *c, const int *lo, const int *hi)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    if (!lo || !hi) return fail(c, LBM_ERR_ARG, "lo and hi are required");
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
     if (c->L.streaming != LBM_STREAM_AA)
-        return fail(c, LBM_ERR_UNSUPPORTED, "lbm_step_planes needs the AA layout");
+        return fail(c, LBM_ERR_UNSUPPORTED, "stepping part of the grid needs the AA layout");
     if (c->L.ib_cap > 0)
         return fail(c, LBM_ERR_UNSUPPORTED,
-                    "lbm_step_planes takes no context with immersed-boundary capacity");
-    const bool d2 = c->cfg.lattice == LBM_D2Q9;
-    const int n_outer = d2 ? c->cfg.ny : c->cfg.nz;
-    if (lo < 0 || hi > n_outer || lo >= hi)
-        return fail(c, LBM_ERR_ARG, "planes [lo, hi) must be a non-empty range of [0, " +
-                                        std::to_string(n_outer) + ")");
-    if (!c->planes_left) {
-        c->planes_done.assign((size_t)n_outer, 0);
-        c->planes_left = n_outer;
+                    "stepping part of the grid takes no context with immersed-boundary capacity");
+    const int n[3] = {c->cfg.nx, c->cfg.ny, c->cfg.nz};
+    for (int a = 0; a < 3; ++a)
+        if (lo[a] < 0 || hi[a] > n[a] || lo[a] >= hi[a])
+            return fail(c, LBM_ERR_ARG, "the box [lo, hi) must be non-empty and inside the grid "
+                                        "on every axis");
+    // boxes of one step may not overlap: each cell is stepped once
+    for (const auto &b : c->boxes_done) {
+        bool meet = true;
+        for (int a = 0; a < 3; ++a) meet = meet && lo[a] < b[3 + a] && b[a] < hi[a];
+        if (meet) return fail(c, LBM_ERR_ARG, "the box overlaps one already stepped in this step");
     }
-    for (int k = lo; k < hi; ++k)
-        if (c->planes_done[(size_t)k])
-            return fail(c, LBM_ERR_ARG, "plane " + std::to_string(k) +
-                                            " was already stepped in this step");
+    if (!c->cells_left) {
+        c->boxes_done.clear();
+        c->cells_left = (long long)n[0] * n[1] * n[2];
+    }
     DeviceGuard guard(c->device);
     // not chained: the launch may follow an event wait on another stream's halo work
-    cudaError_t e = launch_planes(c, c->P, c->parity, lo, hi, c->stream, false);
-    if (e != cudaSuccess) return cuda_fail(c, e, "step kernel (planes)");
-    for (int k = lo; k < hi; ++k) c->planes_done[(size_t)k] = 1;
-    c->planes_left -= hi - lo;
-    if (!c->planes_left) {
+    cudaError_t e = launch_box(c, c->P, c->parity, lo, hi, c->stream, false);
+    if (e != cudaSuccess) return cuda_fail(c, e, "step kernel (box)");
+    c->boxes_done.push_back({lo[0], lo[1], lo[2], hi[0], hi[1], hi[2]});
+    c->cells_left -= (long long)(hi[0] - lo[0]) * (hi[1] - lo[1]) * (hi[2] - lo[2]);
+    if (!c->cells_left) {
+        c->boxes_done.clear();
         c->parity ^= 1;
         ++c->steps;
     }
     return LBM_OK;
 }
 
+lbm_status lbm_step_planes(lbm_ctx *c, int lo, int hi)
+{
+    if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
+    const int outer = c->L.dim - 1;
+    int blo[3] = {0, 0, 0}, bhi[3] = {c->cfg.nx, c->cfg.ny, c->cfg.nz};
+    blo[outer] = lo;
+    bhi[outer] = hi;
+    return lbm_step_box(c, blo, bhi);
+}
+
 lbm_status lbm_macroscopic(lbm_ctx *c, float *rho, float *u, float *T)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
-    if (c->planes_left) return partly_stepped(c);
+    if (c->cells_left) return partly_stepped(c);
     DeviceGuard guard(c->device);
     void *dr = nullptr, *du = nullptr, *dT = nullptr;
     lbm_status s = LBM_OK;
@@ -449,7 +472,7 @@ lbm_status lbm_diagnostics(lbm_ctx *c, lbm_diag *out)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
     if (!out) return fail(c, LBM_ERR_ARG, "out is NULL");
-    if (c->planes_left) return partly_stepped(c);
+    if (c->cells_left) return partly_stepped(c);
     if (!c->initialized) return fail(c, LBM_ERR_STATE, "no state: call lbm_init_equilibrium");
     DeviceGuard guard(c->device);
     cudaError_t e = lbm::launch_diag(c->cfg.lattice, c->cfg.thermal, c->L.masked, pattern(c),
@@ -557,7 +580,7 @@ lbm_status lbm_solid_force(lbm_ctx *c, double F_out[3])
 static lbm_status populations(lbm_ctx *c, float *f, float *g, bool set)
 {
     if (!c) return fail(nullptr, LBM_ERR_ARG, "ctx is NULL");
-    if (c->planes_left) return partly_stepped(c);
+    if (c->cells_left) return partly_stepped(c);
     if (!f) return fail(c, LBM_ERR_ARG, "f is NULL");
     if (c->L.QT && !g && set) return fail(c, LBM_ERR_ARG, "g is required with a thermal lattice");
     if (!set && !c->initialized) return fail(c, LBM_ERR_STATE, "no state to read");

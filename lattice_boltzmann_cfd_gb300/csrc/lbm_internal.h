@@ -57,22 +57,29 @@ inline Shape cell_shape(int nx, int ny, int nz, int threads = 64)
     return s;
 }
 
-// The AA step kernels' launch over the outer-axis planes [lo, hi): cell_shape's grid cut to
-// those planes when rows are a multiple of 32 cells; otherwise (linear) 64-thread blocks over
-// the cells in storage order (Params::linear): in 3-D, blocks along each z plane (grid.x)
-// and one grid row per plane (grid.y); in 2-D, along the rows [lo, hi) as one run.
-inline Shape step_shape(int nx, int ny, int nz, int dim, int lo, int hi, bool linear)
+// The AA step kernels' launch over the box of cells [lo, hi) (per axis x, y, z; in 2-D
+// lo[2] = 0, hi[2] = 1).  linear (Params::linear): rows that are not a multiple of 32
+// cells; it applies to boxes of whole outer-axis planes only (whole x, and whole y in 3-D):
+// 64-thread blocks over the cells in storage order, along each z plane with one grid row
+// per plane in 3-D, along the rows as one run in 2-D.  Otherwise cell_shape's blocks over
+// the box.  *linear_out: whether the launch is linear.
+inline Shape step_shape(int nx, int ny, int nz, int dim, const int lo[3], const int hi[3],
+                        bool linear, bool *linear_out = nullptr)
 {
     Shape s;
+    const bool whole = lo[0] == 0 && hi[0] == nx && (dim == 2 || (lo[1] == 0 && hi[1] == ny));
+    linear = linear && whole;
+    if (linear_out) *linear_out = linear;
     if (linear) {
         s.block = dim3(64, 1, 1);
-        if (dim == 3) s.grid = dim3((unsigned)(((long long)nx * ny + 63) / 64), (unsigned)(hi - lo), 1);
-        else s.grid = dim3((unsigned)(((long long)nx * (hi - lo) + 63) / 64), 1, 1);
+        if (dim == 3)
+            s.grid = dim3((unsigned)(((long long)nx * ny + 63) / 64), (unsigned)(hi[2] - lo[2]), 1);
+        else
+            s.grid = dim3((unsigned)(((long long)nx * (hi[1] - lo[1]) + 63) / 64), 1, 1);
         return s;
     }
-    s = cell_shape(nx, ny, nz);
-    if (dim == 2) s.grid.y = (unsigned)((hi - lo + (int)s.block.y - 1) / (int)s.block.y);
-    else s.grid.z = (unsigned)(hi - lo);
+    s = cell_shape(hi[0] - lo[0], hi[1] - lo[1], dim == 3 ? hi[2] - lo[2] : 1);
+    (void)nz;
     return s;
 }
 
@@ -85,13 +92,17 @@ constexpr int DIAG_BLOCKS = 2048;   // capacity of the partial-sum rows (one res
 // (form 2: and of the samples' stencil cells) and load it inside (boxed_mask); the
 // two-buffer kernels load it.
 // chained: see launch_step_kernel.
+// box: the launch covers the box [P.run_lo, P.run_hi) (lbm_step_box; masked 0 or 1 only),
+// otherwise the whole grid.
 cudaError_t launch_step_d3q19(int thermal, int coll, int masked, bool odd, bool narrow,
-                              const Params &P, const Shape &sh, cudaStream_t s, bool chained);
+                              const Params &P, const Shape &sh, cudaStream_t s, bool chained,
+                              bool box = false);
 cudaError_t launch_step_d2q9(int thermal, int coll, int masked, bool odd, bool narrow,
-                             const Params &P, const Shape &sh, cudaStream_t s, bool chained);
+                             const Params &P, const Shape &sh, cudaStream_t s, bool chained,
+                             bool box = false);
 // D3Q27, central moments, AA only; masked as above.
 cudaError_t launch_step_d3q27(int masked, bool odd, bool narrow, const Params &P,
-                              const Shape &sh, cudaStream_t s, bool chained);
+                              const Shape &sh, cudaStream_t s, bool chained, bool box = false);
 // Two-buffer modes: one PULL step, or one SPLIT step (collide + stream), from P.f/P.g
 // into P.fo/P.go.
 cudaError_t launch_pull_d3q19(int thermal, int coll, int masked, bool narrow, const Params &P,

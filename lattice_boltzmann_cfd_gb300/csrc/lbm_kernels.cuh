@@ -66,9 +66,9 @@ struct Params {
     int ghost_lo, ghost_hi;  // outer-axis coordinate of a slab's ghost planes, -1 = none
     // blocks: ghost planes on the other axes too (ghost_inner = 1); per axis, -1 = none
     int ghost_inner, ghost3_lo[3], ghost3_hi[3];
-    // outer-axis planes (z in 3-D, y in 2-D) the AA step kernels cover: [plane_lo,
-    // plane_hi); the whole axis except in launches of lbm_step_planes
-    int plane_lo, plane_hi;
+    // the box of cells [run_lo, run_hi) (per axis x, y, z) an AA step launch of
+    // lbm_step_box / lbm_step_planes covers (read by the BOX kernels only)
+    int run_lo[3], run_hi[3];
     // AA step launches over rows that are not a multiple of 32 cells (linear = 1): one thread
     // per cell in storage order, so that no thread idles past the end of a row and every warp
     // covers 32 consecutive cells; the coordinates come from dividing by nx
@@ -541,20 +541,22 @@ LBM_HD void aa_step_cell(const Params &Pr, const Params &Pw, int x, int y, int z
     }
 }
 
-// Cell t of a linear AA step launch: in 3-D, cell t of outer-axis plane P.plane_lo + plane
-// in storage order; in 2-D, cell t counted from the first cell of row P.plane_lo.  false past
-// the plane (3-D) or past the last cell of row P.plane_hi - 1 (2-D).
-template <class L>
+// Cell t of a linear AA step launch over whole planes of the outer axis: in 3-D, cell t of
+// plane `plane` of the launch in storage order; in 2-D, cell t of the launch's rows.  BOX:
+// the launch starts at plane P.run_lo[2] (3-D) or row P.run_lo[1] (2-D) and, in 2-D, ends
+// at row P.run_hi[1]; otherwise it covers the whole grid.  false past the plane (3-D) or
+// past the launch's last row (2-D).
+template <class L, bool BOX>
 LBM_HD bool linear_cell_coords(const Params &P, int t, int plane, int &x, int &y, int &z)
 {
     if constexpr (L::DIM == 3) {
         if (t >= P.nx * P.ny) return false;
-        z = P.plane_lo + plane;
+        z = BOX ? P.run_lo[2] + plane : plane;
         y = (int)div_by((unsigned)t, P.div_nx);
         x = t - y * P.nx;
     } else {
-        const int i = P.plane_lo * P.nx + t;
-        if (i >= P.plane_hi * P.nx) return false;
+        const int i = BOX ? P.run_lo[1] * P.nx + t : t;
+        if (i >= (BOX ? P.run_hi[1] : P.ny) * P.nx) return false;
         y = (int)div_by((unsigned)i, P.div_nx);
         x = i - y * P.nx;
         z = 0;
@@ -562,51 +564,54 @@ LBM_HD bool linear_cell_coords(const Params &P, int t, int plane, int &x, int &y
     return true;
 }
 
-// Cell of the calling thread in an AA step launch over the outer-axis planes
-// [P.plane_lo, P.plane_hi): the launch grid covers those planes only, offset by plane_lo
-// (blocks along x, rows stacked in y, planes in z; or, with P.linear, a 1-D grid over the
-// cells in storage order).  Returns false for threads past the grid's edge.
-template <class L>
+// Cell of the calling thread in an AA step launch: blocks along x, rows stacked in y,
+// planes in z (3-D); or, with P.linear, a grid over the cells of whole planes in storage
+// order.  BOX (lbm_step_box): the launch covers the box [P.run_lo, P.run_hi) and is offset
+// by run_lo; otherwise the whole grid, with no offset at all (the plain steps keep the
+// simplest index arithmetic).  Returns false for threads past the launch's edge.
+template <class L, bool BOX>
 LBM_HD bool step_cell_coords(const Params &P, int &x, int &y, int &z)
 {
 #if defined(__CUDA_ARCH__)
     if (P.linear)
-        return linear_cell_coords<L>(P, blockIdx.x * blockDim.x + threadIdx.x, blockIdx.y, x, y, z);
+        return linear_cell_coords<L, BOX>(P, blockIdx.x * blockDim.x + threadIdx.x, blockIdx.y,
+                                          x, y, z);
     x = blockIdx.x * blockDim.x + threadIdx.x;
     y = blockIdx.y * blockDim.y + threadIdx.y;
     z = blockIdx.z;
 #endif
-    if constexpr (L::DIM == 3) {
-        z += P.plane_lo;
-        return x < P.nx && y < P.ny;
+    if constexpr (BOX) {
+        x += P.run_lo[0];
+        y += P.run_lo[1];
+        z += P.run_lo[2];
+        return x < P.run_hi[0] && y < P.run_hi[1];
     } else {
-        y += P.plane_lo;
-        return x < P.nx && y < P.plane_hi;
+        return x < P.nx && y < P.ny;
     }
 }
 
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB,
-          bool FACES = false>
+          bool FACES = false, bool BOX = false>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
     allow_dependents();
     wait_prerequisites();   // every load reads the previous step's stores
     int x = 0, y = 0, z = 0;
-    if (!step_cell_coords<L>(P, x, y, z)) return;
+    if (!step_cell_coords<L, BOX>(P, x, y, z)) return;
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
 // The same step with the register allocation bounded so that 5 blocks of 256 reside per SM
 // (48 registers): for a collision long enough that the extra warps pay for themselves.
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB,
-          bool FACES = false>
+          bool FACES = false, bool BOX = false>
 __global__ void __launch_bounds__(256, 5) step_kernel_5(const Params P)
 {
     allow_dependents();
     wait_prerequisites();   // every load reads the previous step's stores
     int x = 0, y = 0, z = 0;
-    if (!step_cell_coords<L>(P, x, y, z)) return;
+    if (!step_cell_coords<L, BOX>(P, x, y, z)) return;
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 

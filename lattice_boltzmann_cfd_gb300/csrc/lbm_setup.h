@@ -301,8 +301,10 @@ inline void fill_params(const lbm_config &g, const Layout &L, char *ws, lbm::Par
         P.ghost3_hi[a] = P.face_halo[2 * a + 1] ? ext[a] - 1 : -1;
         if (a != outer && (P.face_halo[2 * a] || P.face_halo[2 * a + 1])) P.ghost_inner = 1;
     }
-    P.plane_lo = 0;
-    P.plane_hi = n_outer;
+    for (int a = 0; a < 3; ++a) {
+        P.run_lo[a] = 0;
+        P.run_hi[a] = ext[a];
+    }
     P.linear = g.nx % 32 != 0;
     P.div_nx = divisor((unsigned)g.nx);
     // anti-bounce-back weight omega = (4 + a_T)/10 (D2Q5) or (6 + a_T)/21 (D3Q7)

@@ -715,6 +715,33 @@ def exchange_axes(dim: int, nb):
     return [a for a in range(dim - 1, -1, -1) if nb[a] > 1]
 
 
+def block_groups(ext, sides, dim: int):
+    """(interior box or None, [boundary boxes]) of a block with local extents ext (x, y, z)
+    and per-axis (low, high) ghost flags: the boundary is every cell within two planes of a
+    HALO face (its ghost plane and the first owned plane), cut into disjoint boxes axis by
+    axis (z, then y, then x); the interior is the rest.  Boxes are (lo, hi) triples of cell
+    coordinates.  A block too thin for an interior is one boundary box."""
+    lo = [0, 0, 0]
+    hi = [int(ext[0]), int(ext[1]), int(ext[2]) if dim == 3 else 1]
+    inner_lo = [2 if sides[a][0] else 0 for a in range(3)]
+    inner_hi = [hi[a] - 2 if sides[a][1] else hi[a] for a in range(3)]
+    if any(inner_hi[a] <= inner_lo[a] for a in range(3)):
+        return None, [(tuple(lo), tuple(hi))]
+    boundary = []
+    for a in range(dim - 1, -1, -1):
+        if inner_lo[a] > lo[a]:
+            b_hi = list(hi)
+            b_hi[a] = inner_lo[a]
+            boundary.append((tuple(lo), tuple(b_hi)))
+            lo[a] = inner_lo[a]
+        if inner_hi[a] < hi[a]:
+            b_lo = list(lo)
+            b_lo[a] = inner_hi[a]
+            boundary.append((tuple(b_lo), tuple(hi)))
+            hi[a] = inner_hi[a]
+    return (tuple(lo), tuple(hi)), boundary
+
+
 def block_exchange(b: int, nb, periodic, dim: int, phase: int, pack, unpack, send, recv,
                    group=None, sync=None):
     """One halo exchange of block ``b`` (its torch.distributed rank) with its neighbours:
@@ -753,9 +780,9 @@ class BlockDomain:
 
     ``exchange``: "swap" moves each face with one buffer-free kernel (lbm_halo_axis_swap,
     blocks on one device), "buffers" packs, copies and unpacks; "auto" takes the swap on one
-    device."""
+    device.  ``overlap``: see step (one device only)."""
 
-    def __init__(self, w, nb, devices=None, exchange: str = "auto"):
+    def __init__(self, w, nb, devices=None, exchange: str = "auto", overlap: bool = False):
         import torch
         if exchange not in ("auto", "swap", "buffers"):
             raise ValueError("exchange must be 'auto', 'swap' or 'buffers'")
@@ -785,6 +812,15 @@ class BlockDomain:
         if exchange == "swap" and self.multi_device:
             raise ValueError("the buffer-free swap needs every block on one device")
         self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
+        self.overlap = bool(overlap)
+        if self.overlap and self.multi_device:
+            raise ValueError("overlap needs every block on one device")
+        self.groups = [block_groups([len(c) for c in coords], sides, w.dim)
+                       for coords, sides in zip(self.coords, self.sides)]
+        dev = self.blocks[0].device
+        self.main = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(dev) if self.overlap else None
+        self._pending = None    # event: the last exchange's unpacks are queued before it
 
     @property
     def parity(self) -> int:
@@ -837,11 +873,39 @@ class BlockDomain:
             sim.init_equilibrium(dev(self.w.rho0), dev(self.w.u0, 1), dev(self.w.T_init))
 
     def step(self, n: int = 1):
-        """n time steps, each followed by its exchange (FILL after even, DRAIN after odd)."""
+        """n time steps, each followed by its exchange (FILL after even, DRAIN after odd).
+        With ``overlap``: each block's interior box, a wait for the previous exchange, its
+        boundary boxes, then the exchange on a second stream beside the next step's interior
+        (block_groups; the interior is two planes away from every HALO face, so it touches
+        no slot an exchange reads or writes)."""
         for _ in range(n):
+            if not self.overlap:
+                for sim in self.blocks:
+                    sim.step(1)
+                self._exchange(capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN)
+                continue
+            for sim, (interior, _) in zip(self.blocks, self.groups):
+                if interior is not None:
+                    sim.step_box(*interior)
+            if self._pending is not None:
+                self.main.wait_event(self._pending)
+                self._pending = None
+            for sim, (_, boundary) in zip(self.blocks, self.groups):
+                for lo, hi in boundary:
+                    sim.step_box(lo, hi)
+            phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
+            self.side.wait_stream(self.main)
             for sim in self.blocks:
-                sim.step(1)
-            self._exchange(capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN)
+                sim.set_stream(self.side)
+            try:
+                self._exchange(phase)
+            finally:
+                for sim in self.blocks:
+                    sim.set_stream(self.main)
+            self._pending = self.side.record_event()
+        if self._pending is not None:
+            self.main.wait_event(self._pending)
+            self._pending = None
 
     def set_populations(self, f, g=None):
         """Resume from whole-domain logical populations (Q, nz, ny, nx) as populations()
@@ -905,14 +969,17 @@ class BlockDomain:
 
 class DistBlockDomain:
     """Block ``rank`` of ``w`` cut into nb = (bx, by, bz) blocks, one per torch.distributed
-    rank (world = bx * by * bz).  Each step is followed by block_exchange: per split axis,
-    z then y then x, the packs, the messages to the two neighbours along that axis, and the
-    unpacks.  ``transport`` as for DistSlabDomain: "device" buffers handed to the process
-    group on the compute stream (NCCL), or "host" page-locked buffers (gloo), where the host
-    waits for each axis's packs before sending."""
+    rank (world = bx * by * bz).  Each step is followed by the exchange of every split axis,
+    z then y then x: per axis the packs, the messages to the two neighbours along that axis
+    (halo_messages), and the unpacks, before the next axis packs.  ``transport`` as for
+    DistSlabDomain: "device" buffers handed to the process group on the exchange stream
+    (NCCL; the host never waits), or "host" page-locked buffers (gloo), where the host waits
+    for each axis's packs before sending.  ``overlap``: each step runs as the interior box,
+    the wait for the previous exchange, the boundary boxes (block_groups), then the exchange
+    on the exchange stream beside the next step's interior."""
 
     def __init__(self, w, nb, rank: int, world: int, device=None, group=None,
-                 transport: str = "device"):
+                 transport: str = "device", overlap: bool = False):
         import torch
         nb = tuple(int(v) for v in nb)
         if nb[0] * nb[1] * nb[2] != world:
@@ -920,14 +987,20 @@ class DistBlockDomain:
         if transport not in ("device", "host"):
             raise ValueError("transport must be 'device' or 'host'")
         self.w, self.nb, self.rank, self.world, self.group = w, nb, rank, world, group
-        self.transport = transport
+        self.transport, self.overlap = transport, bool(overlap)
         self.periodic = [w.face_flow[2 * a] == "periodic" for a in range(3)]
         self.local, self.sides, self.coords = block_part(w, nb, rank)
         dev = torch.device(device if device is not None else "cuda")
-        self.sim = Simulation(self.local, device=dev)
+        self.main = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(dev)
+        self.sim = Simulation(self.local, device=dev, stream=self.main)
+        self.interior, self.boundary = block_groups([len(c) for c in self.coords], self.sides,
+                                                    w.dim)
+        self.axes = exchange_axes(w.dim, nb)
+        self.nbs = block_neighbours(rank, nb, self.periodic)
         self.send, self.recv = [], []
         for a in range(3):
-            if a < w.dim and nb[a] > 1:
+            if a in self.axes:
                 nfloat = capi.lbm_halo_axis_bytes(self.sim.ctx, a) // 4
                 if transport == "host":
                     new = lambda: torch.empty(nfloat, dtype=torch.float32).pin_memory()
@@ -938,6 +1011,8 @@ class DistBlockDomain:
             else:
                 self.send.append(None)
                 self.recv.append(None)
+        self._packed = None     # host transport: (event after axis k's packs, k, phase)
+        self._pending = None    # event: the last exchange's unpacks are queued before it
 
     @property
     def parity(self) -> int:
@@ -949,21 +1024,80 @@ class DistBlockDomain:
         self.sim.init_equilibrium(dev(self.local.rho0), dev(self.local.u0),
                                   dev(self.local.T_init))
 
-    def step(self, n: int = 1):
+    def _pack_axis(self, k: int, phase: int):
+        a = self.axes[k]
+        for side in (0, 1):
+            if self.nbs[a][side] is not None:
+                capi.lbm_halo_axis_pack(self.sim.ctx, a, side, phase, self.send[a][side])
+
+    def _unpack_axis(self, k: int, phase: int, arrived):
+        for side, buf in arrived:
+            capi.lbm_halo_axis_unpack(self.sim.ctx, self.axes[k], side, phase, buf)
+
+    def _start_exchange(self):
+        """Queue this step's exchange on the exchange stream behind the step's last launch:
+        with device buffers all of it; with host buffers the first axis's packs."""
         import torch
-        stream = torch.cuda.current_stream(self.sim.device)
-        # host buffers: the host waits for the packs before sending, and the unpacks may
-        # not overwrite a receive buffer that the next axis reuses before it is read
-        sync = (lambda: stream.synchronize()) if self.transport == "host" else None
+        if not self.axes:
+            return
+        phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
+        self.side.wait_stream(self.main)
+        self.sim.set_stream(self.side)
+        try:
+            if self.transport == "host":
+                self._pack_axis(0, phase)
+                self._packed = (self.side.record_event(), 0, phase)
+                return
+            with torch.cuda.stream(self.side):
+                for k, a in enumerate(self.axes):
+                    self._pack_axis(k, phase)
+                    arrived = halo_messages(self.nbs[a], self.send[a], self.recv[a], self.group)
+                    self._unpack_axis(k, phase, arrived)
+        finally:
+            self.sim.set_stream(self.main)
+        self._pending = self.side.record_event()
+
+    def _finish_exchange(self):
+        """Complete the exchange in flight (host transport: per axis, wait for its packs, move
+        the messages, queue the unpacks and the next axis's packs) and order it before later
+        work on the main stream."""
+        if self._packed is not None:
+            event, k, phase = self._packed
+            self._packed = None
+            self.sim.set_stream(self.side)
+            try:
+                while True:
+                    event.synchronize()
+                    a = self.axes[k]
+                    arrived = halo_messages(self.nbs[a], self.send[a], self.recv[a], self.group)
+                    self._unpack_axis(k, phase, arrived)
+                    k += 1
+                    if k == len(self.axes):
+                        break
+                    self._pack_axis(k, phase)
+                    event = self.side.record_event()
+            finally:
+                self.sim.set_stream(self.main)
+            self._pending = self.side.record_event()
+        if self._pending is not None:
+            self.main.wait_event(self._pending)
+            self._pending = None
+
+    def step(self, n: int = 1):
+        """n time steps with their exchanges; returns with the last exchange done (its
+        unpacks ordered before later work on the main stream)."""
         for _ in range(n):
-            self.sim.step(1)
-            phase = capi.LBM_HALO_FILL if self.parity == 1 else capi.LBM_HALO_DRAIN
-            block_exchange(self.rank, self.nb, self.periodic, self.w.dim, phase,
-                           lambda a, s, p, buf: capi.lbm_halo_axis_pack(self.sim.ctx, a, s, p, buf),
-                           lambda a, s, p, buf: capi.lbm_halo_axis_unpack(self.sim.ctx, a, s, p, buf),
-                           self.send, self.recv, self.group, sync)
-        if sync is not None:
-            sync()
+            if self.overlap:
+                if self.interior is not None:
+                    self.sim.step_box(*self.interior)
+                self._finish_exchange()
+                for lo, hi in self.boundary:
+                    self.sim.step_box(lo, hi)
+            else:
+                self._finish_exchange()
+                self.sim.step(1)
+            self._start_exchange()
+        self._finish_exchange()
 
     def set_populations(self, f, g=None):
         """Resume this rank's block from whole-domain logical populations (Q, nz, ny, nx)."""

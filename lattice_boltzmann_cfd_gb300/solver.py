@@ -120,6 +120,10 @@ class Simulation:
         """The current step on outer-axis planes [lo, hi) only (see lbm_step_planes)."""
         capi.lbm_step_planes(self.ctx, lo, hi)
 
+    def step_box(self, lo, hi):
+        """The current step on the cells [lo, hi) only, (x, y, z) each (see lbm_step_box)."""
+        capi.lbm_step_box(self.ctx, lo, hi)
+
     def macroscopic(self, rho=None, u=None, T=None):
         import torch
         rho = rho if rho is not None else torch.empty(self.grid, device=self.device)

@@ -647,33 +647,34 @@ long long race_any(const lbm_config &cfg, const lbm_setup::Layout &Lay, bool odd
                : race_violations<L, TL, C, true, false, false>(d);
 }
 
-// Overlap of a slab's halo exchange with the next step's interior planes (the slab driver's
+// Overlap of a slab's or block's halo exchange with the next step's interior (the drivers'
 // overlapped order): the exchange after a step -- FILL before an odd step, DRAIN before an
-// even one -- runs beside the next step's launch over the outer-axis planes [ilo, ihi).
-// Brute force on a tiny grid: the pack's read set (each slot holds its own index; the
+// even one, over every HALO face of every axis -- runs beside the next step's launch over
+// the box of cells [ilo, ihi).  Brute force on a tiny grid: the packs' read set (each slot holds its own index; the
 // buffer shows which were read), the unpack's write set (a sentinel buffer), and, for every
 // interior cell of the next step, its write set (stepped alone into a NaN-filled buffer) and
-// which of the pack's and unpack's slots it reads (each such slot poisoned in turn).  The
-// overlap is race-free when no interior cell reads or writes a slot the pack reads or the
+// which of the packs' and unpacks' slots it reads (each such slot poisoned in turn).  The
+// overlap is race-free when no interior cell reads or writes a slot a pack reads or an
 // unpack writes.  Returns the number of such (cell, slot) pairs.
 template <class L, class TL, int C, bool M, bool F, bool O>
-long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
+long long overlap_pairs(Domain<L, TL, C, true> &d, const int *ilo, const int *ihi)
 {
     const float nan = std::numeric_limits<float>::quiet_NaN();
     const int phase = O ? LBM_HALO_FILL : LBM_HALO_DRAIN;
-    const int outer = L::DIM - 1;
-    const int plane_cells = L::DIM == 3 ? d.cfg.nx * d.cfg.ny : d.cfg.nx;
+    const int n[3] = {d.cfg.nx, d.cfg.ny, d.cfg.nz};
     const int ndir = L::Q == 27 ? 9 : (L::Q == 19 ? 5 : 3) + (TL::Q ? 1 : 0);
-    std::vector<float> buf((size_t)ndir * plane_cells);
     // slots: f slot s as s, g slot s as -1 - s (indices into the vectors, guards included)
     std::vector<long long> touched;
     const std::vector<float> f0 = d.f, g0 = d.g;
-    for (int side = 0; side < 2; ++side) {
-        if (d.cfg.face_flow[2 * outer + side] != LBM_FACE_HALO) continue;
+    for (int face = 0; face < 2 * L::DIM; ++face) {
+        const int axis = face / 2, side = face % 2;
+        if (d.cfg.face_flow[face] != LBM_FACE_HALO) continue;
+        const int plane_cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
+        std::vector<float> buf((size_t)ndir * plane_cells);
         for (size_t i = 0; i < d.f.size(); ++i) d.f[i] = (float)i;
         for (size_t i = 0; i < d.g.size(); ++i) d.g[i] = -1.0f - (float)i;
         std::fill(buf.begin(), buf.end(), nan);
-        d.halo(outer, side, phase, 0, buf.data());
+        d.halo(axis, side, phase, 0, buf.data());
         for (float v : buf)
             if (!std::isnan(v)) touched.push_back((long long)v);
         d.f = f0;
@@ -682,7 +683,7 @@ long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
         const float mark = 1.0e30f;
         std::fill(buf.begin(), buf.end(), mark);
         for (auto *v : {&d.f, &d.g}) std::fill(v->begin(), v->end(), 0.0f);
-        d.halo(outer, side, phase, 1, buf.data());
+        d.halo(axis, side, phase, 1, buf.data());
         for (size_t i = 0; i < d.f.size(); ++i)
             if (d.f[i] == mark) touched.push_back((long long)i);
         for (size_t i = 0; i < d.g.size(); ++i)
@@ -710,8 +711,10 @@ long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
     for (int z = 0; z < d.cfg.nz; ++z)
         for (int y = 0; y < d.cfg.ny; ++y)
             for (int x = 0; x < d.cfg.nx; ++x) {
-                const int c = L::DIM == 3 ? z : y;
-                if (c < ilo || c >= ihi) continue;
+                const int c3[3] = {x, y, z};
+                bool inside = true;
+                for (int a = 0; a < 3; ++a) inside = inside && c3[a] >= ilo[a] && c3[a] < ihi[a];
+                if (!inside) continue;
                 step_cell(x, y, z);
                 std::vector<size_t> Wf, Wg;
                 for (size_t i = 0; i < wf.size(); ++i)
@@ -739,7 +742,7 @@ long long overlap_pairs(Domain<L, TL, C, true> &d, int ilo, int ihi)
 
 template <class L, class TL, int C>
 long long overlap_any(const lbm_config &cfg, const lbm_setup::Layout &Lay, bool next_odd,
-                      int ilo, int ihi)
+                      const int *ilo, const int *ihi)
 {
     Domain<L, TL, C, true> d(cfg, Lay);
     if (d.face_mask_mismatches) return -30;
@@ -907,12 +910,18 @@ extern "C" long long emu_divisor_errors(unsigned d, unsigned n_lo, unsigned n_hi
 // and the next index none.  Returns the number of violations.
 extern "C" long long emu_linear_mapping_errors(int dim, int nx, int ny, int nz, int lo, int hi)
 {
+    // the whole grid takes the plain form (no box), a range of planes the box form
+    const bool box = !(lo == 0 && hi == (dim == 3 ? nz : ny));
     Params P{};
     P.nx = nx;
     P.ny = ny;
     P.nz = nz;
-    P.plane_lo = lo;
-    P.plane_hi = hi;
+    P.run_lo[0] = P.run_lo[1] = P.run_lo[2] = 0;
+    P.run_hi[0] = nx;
+    P.run_hi[1] = ny;
+    P.run_hi[2] = nz;
+    P.run_lo[dim - 1] = lo;
+    P.run_hi[dim - 1] = hi;
     P.linear = 1;
     P.div_nx = lbm_setup::divisor((unsigned)nx);
     long long bad = 0;
@@ -925,7 +934,8 @@ extern "C" long long emu_linear_mapping_errors(int dim, int nx, int ny, int nz, 
         for (int p = 0; p < hi - lo; ++p) {
             for (long long t = 0; t <= plane; ++t) {
                 int x = -1, y = -1, z = -1;
-                const bool in = linear_cell_coords<D3Q19>(P, (int)t, p, x, y, z);
+                const bool in = (box ? linear_cell_coords<D3Q19, true>(P, (int)t, p, x, y, z)
+                                       : linear_cell_coords<D3Q19, false>(P, (int)t, p, x, y, z));
                 if (t == plane) bad += in;
                 else check(in, x, y, z, (lo + p) * plane + t);
             }
@@ -934,7 +944,8 @@ extern "C" long long emu_linear_mapping_errors(int dim, int nx, int ny, int nz, 
         const long long cells = (long long)nx * (hi - lo);
         for (long long t = 0; t <= cells; ++t) {
             int x = -1, y = -1, z = -1;
-            const bool in = linear_cell_coords<D2Q9>(P, (int)t, 0, x, y, z);
+            const bool in = (box ? linear_cell_coords<D2Q9, true>(P, (int)t, 0, x, y, z)
+                                       : linear_cell_coords<D2Q9, false>(P, (int)t, 0, x, y, z));
             if (t == cells) bad += in;
             else check(in, x, y, z, (long long)lo * nx + t);
         }
@@ -972,11 +983,12 @@ extern "C" long long emu_count_bad_indices(int lattice, int nx, int ny, int nz)
     return bad;
 }
 
-// (cell, slot) pairs by which the next step's launch over outer-axis planes [ilo, ihi) would
-// race with the exchange before it (see overlap_pairs); next_odd: the next step is odd (the
-// exchange is a FILL), else even (a DRAIN).  Negative on a bad configuration.
-extern "C" long long emu_overlap_violations(const lbm_config *cfg, int next_odd, int ilo,
-                                            int ihi)
+// (cell, slot) pairs by which the next step's launch over the box of cells [ilo, ihi) would
+// race with the exchange before it, every HALO face of every axis (see overlap_pairs);
+// next_odd: the next step is odd (the exchange is a FILL), else even (a DRAIN).  Negative on
+// a bad configuration.
+extern "C" long long emu_box_overlap_violations(const lbm_config *cfg, int next_odd,
+                                                const int *ilo, const int *ihi)
 {
     lbm_setup::Layout Lay;
     std::string why;
@@ -996,4 +1008,15 @@ extern "C" long long emu_overlap_violations(const lbm_config *cfg, int next_odd,
                    : overlap_any<D2Q9, D2Q5, 0>(*cfg, Lay, o, ilo, ihi);
     return mrt ? overlap_any<D2Q9, NoThermal, 1>(*cfg, Lay, o, ilo, ihi)
                : overlap_any<D2Q9, NoThermal, 0>(*cfg, Lay, o, ilo, ihi);
+}
+
+// The same for a launch over the whole outer-axis planes [ilo, ihi) (the slab overlap).
+extern "C" long long emu_overlap_violations(const lbm_config *cfg, int next_odd, int ilo,
+                                            int ihi)
+{
+    const int dim = cfg->lattice == 9 ? 2 : 3;
+    int lo[3] = {0, 0, 0}, hi[3] = {cfg->nx, cfg->ny, cfg->nz};
+    lo[dim - 1] = ilo;
+    hi[dim - 1] = ihi;
+    return emu_box_overlap_violations(cfg, next_odd, lo, hi);
 }

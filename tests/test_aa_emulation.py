@@ -342,3 +342,79 @@ def test_plane_groups_cover_each_plane_once():
                 for lo, hi in interior:
                     assert lo >= (2 if low else 0) and hi <= (n - 2 if high else n)
 
+
+
+def _block_overlap_cases():
+    """Blocks with HALO faces on two or three axes (ghost rows meeting at edges and corners),
+    on every lattice, with walls, solids next to the block faces and Dirichlet faces."""
+    import dataclasses
+    from lattice_boltzmann_cfd_gb300 import workloads as W
+    from lattice_boltzmann_cfd_gb300.slabs import block_part
+    rp = W.random_periodic(shape=(10, 10, 10), seed=91)
+    c3 = W.perturbed(W.cavity3d(shape=(10, 10, 10)), seed=92)
+    sol = np.zeros(c3.grid, np.uint8)
+    sol[4, 5, 4] = 1     # next to the blocks' faces at z = 5 and y = 5
+    sol[6, 4, 6] = 1
+    c3 = dataclasses.replace(c3, solid=sol, gbeta=0.01, name=c3.name + " + solids")
+    c2 = W.perturbed(W.cavity2d(shape=(10, 11, 1)), seed=93)
+    q27 = W.random_periodic(shape=(9, 9, 9), seed=94, lattice=27)
+    out = []
+    for w, nb, blocks in ((rp, (1, 2, 2), (0, 3)), (rp, (2, 2, 2), (0, 7)), (c3, (2, 2, 2), (0, 5)),
+                          (c2, (2, 2, 1), (0, 3)), (q27, (2, 2, 2), (0, 6))):
+        for b in blocks:
+            local, sides, coords = block_part(w, nb, b)
+            out.append((f"{w.name} block {b} of {nb}", local, sides))
+    return out
+
+
+BLOCK_OVERLAP = _block_overlap_cases()
+
+
+@pytest.mark.parametrize("next_odd", [1, 0], ids=["FILL then odd", "DRAIN then even"])
+@pytest.mark.parametrize("case", BLOCK_OVERLAP, ids=[c[0] for c in BLOCK_OVERLAP])
+def test_block_exchange_overlaps_the_interior_without_races(emu_lib, case, next_odd):
+    """The overlapped block order runs a step's exchange (every HALO face of every axis)
+    beside the next step's launch over the interior box.  By brute force over slots: no
+    interior cell reads or writes a slot a pack reads or an unpack writes.  Widening the box
+    by one plane towards any HALO face produces such pairs."""
+    import ctypes
+    from lattice_boltzmann_cfd_gb300.slabs import block_groups
+    from lattice_boltzmann_cfd_gb300.solver import make_config
+    name, local, sides = case
+    cfg, keep = make_config(local, "aa")
+    (lo, hi), boundary = block_groups(local.shape, sides, local.dim)
+    f = emu_lib.emu_box_overlap_violations
+    f.restype = ctypes.c_longlong
+    box = lambda v: (ctypes.c_int * 3)(*v)
+    assert f(ctypes.byref(cfg), next_odd, box(lo), box(hi)) == 0
+    for a in range(local.dim):
+        for s in (0, 1):
+            if not sides[a][s]:
+                continue
+            wlo, whi = list(lo), list(hi)
+            if s == 0:
+                wlo[a] -= 1
+            else:
+                whi[a] += 1
+            assert f(ctypes.byref(cfg), next_odd, box(wlo), box(whi)) > 0, (a, s)
+
+
+def test_block_groups_cover_each_cell_once():
+    import itertools
+    from lattice_boltzmann_cfd_gb300.slabs import block_groups
+    for dim in (2, 3):
+        for ext in ((7, 6, 5), (4, 9, 6), (3, 3, 3), (8, 5, 1)):
+            ext = ext if dim == 3 else (ext[0], ext[1], 1)
+            for flags in itertools.product((False, True), repeat=2 * dim):
+                sides = [(flags[2 * a], flags[2 * a + 1]) if a < dim else (False, False)
+                         for a in range(3)]
+                interior, boundary = block_groups(ext, sides, dim)
+                seen = np.zeros(ext[::-1], int)
+                for lo, hi in ([interior] if interior else []) + boundary:
+                    seen[lo[2]:hi[2], lo[1]:hi[1], lo[0]:hi[0]] += 1
+                assert (seen == 1).all(), (ext, sides)
+                if interior:
+                    lo, hi = interior
+                    for a in range(dim):
+                        assert lo[a] >= (2 if sides[a][0] else 0)
+                        assert hi[a] <= ext[a] - (2 if sides[a][1] else 0)

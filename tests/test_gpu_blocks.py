@@ -158,6 +158,80 @@ def test_blocks_200_and_201_steps_against_the_oracle(oracle_mod, w, nb):
     dom.close()
 
 
+OVERLAP_CASES = [CASES[i] for i in (0, 3, 5, 7, 8)] + _large_cases()
+
+
+@pytest.mark.parametrize("w", OVERLAP_CASES, ids=[c.name for c in OVERLAP_CASES])
+def test_overlapped_blocks_equal_plain_order(w):
+    """The overlapped block order (interior box, boundary boxes, the exchange of every axis on
+    a second stream beside the next step's interior) gives the plain order's state bit for
+    bit, through the swap and through buffers."""
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    for steps in (7, 8):
+        for nb, exchange in [(nb, "swap") for nb in _layouts(w)] + [(_layouts(w)[0], "buffers")]:
+            got = {}
+            for overlap in (False, True):
+                dom = BlockDomain(w, nb, exchange=exchange, overlap=overlap)
+                dom.init_equilibrium()
+                for c in (3, steps - 3):
+                    dom.step(c)
+                f, g = dom.populations()
+                got[overlap] = (f.cpu().numpy(), None if g is None else g.cpu().numpy())
+                dom.close()
+            assert np.array_equal(got[True][0], got[False][0]), (steps, nb, exchange)
+            if w.thermal:
+                assert np.array_equal(got[True][1], got[False][1]), (steps, nb, exchange)
+
+
+def test_step_box_equals_step():
+    """lbm_step_box over any partition of the grid into boxes, in any order, is lbm_step(1)
+    at both parities; a box that overlaps one already stepped is refused."""
+    from lattice_boltzmann_cfd_gb300.solver import Simulation
+    cases = [W.perturbed(W.cavity3d(shape=(70, 20, 13)), seed=95),
+             W.perturbed(W.cavity2d(shape=(100, 23, 1)), seed=96),
+             W.random_periodic(shape=(40, 12, 11), seed=97, lattice=27),
+             W.random_periodic(shape=(66, 10, 9), seed=98)]      # rows of 66: linear launch
+    rng = np.random.default_rng(11)
+    for w in cases:
+        ext = list(w.shape)
+        ref, sim = Simulation(w), Simulation(w)
+        for s_ in (ref, sim):
+            s_.init_equilibrium(_dev(w.rho0), _dev(w.u0), _dev(w.T_init))
+        for step in range(4):
+            ref.step(1)
+            # cut every axis at random points: the product of the pieces tiles the grid
+            cuts = []
+            for a in range(3):
+                k = min(2, ext[a] - 1)
+                c = sorted(rng.choice(np.arange(1, ext[a]), size=k, replace=False)) if k else []
+                edges = [0] + [int(v) for v in c] + [ext[a]]
+                cuts.append(list(zip(edges[:-1], edges[1:])))
+            boxes = [((x[0], y[0], z[0]), (x[1], y[1], z[1]))
+                     for x in cuts[0] for y in cuts[1] for z in cuts[2]]
+            rng.shuffle(boxes)
+            for i, (lo, hi) in enumerate(boxes):
+                sim.step_box(lo, hi)
+                if i == 0 and len(boxes) > 1:
+                    with pytest.raises(capi.LbmError) as e:
+                        sim.step_box(lo, hi)                         # already stepped
+                    assert e.value.status == capi.LBM_ERR_ARG
+                    with pytest.raises(capi.LbmError) as e:
+                        sim.step(1)
+                    assert e.value.status == capi.LBM_ERR_STATE
+            assert sim.parity == (step + 1) % 2
+            fa, ga = ref.populations()
+            fb, gb = sim.populations()
+            assert torch.equal(fa, fb), (w.name, step)
+            if w.thermal:
+                assert torch.equal(ga, gb), (w.name, step)
+        for lo, hi in (((0, 0, 0), (ext[0] + 1, ext[1], ext[2])), ((1, 0, 0), (1, ext[1], ext[2])),
+                       ((-1, 0, 0), (2, 2, 1))):
+            with pytest.raises(capi.LbmError):
+                sim.step_box(lo, hi)
+        ref.close()
+        sim.close()
+
+
 def test_axis_halo_calls_are_checked():
     """Per-axis halo calls: the plane size of each axis, only HALO sides, axes in range,
     the same parity rules as the outer-axis calls."""
@@ -245,14 +319,14 @@ def _free_port():
     return port
 
 
-def _rank(rank, world, port, name, out):
+def _rank(rank, world, port, name, overlap, out):
     os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
     import torch.distributed as dist
     from lattice_boltzmann_cfd_gb300.slabs import DistBlockDomain
     dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=120))
     w, nb = _case(name)
-    d = DistBlockDomain(w, nb, rank, world, device="cuda:0", transport="host")
+    d = DistBlockDomain(w, nb, rank, world, device="cuda:0", transport="host", overlap=overlap)
     d.init_equilibrium()
     res, done = {}, 0
     for n in STEPS:
@@ -267,11 +341,12 @@ def _rank(rank, world, port, name, out):
     dist.destroy_process_group()
 
 
+@pytest.mark.parametrize("overlap", [False, True], ids=["plain", "overlap"])
 @pytest.mark.parametrize("name", ["periodic 2x2", "cavity3d 2x2", "cavity2d 2x2"])
-def test_four_ranks_share_the_gpu(oracle_mod, name):
-    """Four gloo ranks, one block each, on the one GPU of the test box: the halo kernels
-    write and read page-locked host buffers and the waiting is on the host, in the gloo
-    messages.  The gathered owned cells equal the undivided domain bit for bit and match
+def test_four_ranks_share_the_gpu(oracle_mod, name, overlap):
+    """Four gloo ranks, one block each, on the one GPU of the test box, in the plain and the
+    overlapped order: the halo kernels write and read page-locked host buffers and the
+    waiting is on the host, in the gloo messages.  The gathered owned cells equal the undivided domain bit for bit and match
     the fp64 oracle."""
     import torch.multiprocessing as mp
     from lattice_boltzmann_cfd_gb300.slabs import block_part, owned_slices
@@ -279,7 +354,7 @@ def test_four_ranks_share_the_gpu(oracle_mod, name):
     world = nb[0] * nb[1] * nb[2]
     ctx = mp.get_context("spawn")
     out = ctx.Manager().dict()
-    mp.spawn(_rank, args=(world, _free_port(), name, out), nprocs=world, join=True)
+    mp.spawn(_rank, args=(world, _free_port(), name, overlap, out), nprocs=world, join=True)
     ref = oracle_states(oracle_mod, w, list(STEPS))
     for n in STEPS:
         f1, g1, _ = _single(w, n)
