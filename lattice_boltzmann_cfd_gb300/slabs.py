@@ -66,6 +66,13 @@ def part_of(t, coords, lead=1):
     return t.contiguous()
 
 
+def _device_index(d) -> int:
+    """The CUDA device index of a device or device name ("cuda" = the current device)."""
+    import torch
+    d = torch.device(d)
+    return d.index if d.index is not None else torch.cuda.current_device()
+
+
 def _as_tensor(a):
     import torch
     return a if a is None or isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))
@@ -267,8 +274,12 @@ class SlabDomain:
         self.n_outer = w.shape[self.axis]
         self.periodic = w.face_flow[2 * self.axis] == "periodic"
         devices = list(devices) if devices else [torch.device("cuda")]
+        self.multi_device = len({_device_index(d) for d in devices[:nslabs]}) > 1
+        if exchange == "swap" and self.multi_device:
+            raise ValueError("the buffer-free swap needs every slab on one device")
+        self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
         self.slabs, self.sides, self.plane_lists, self.buffers = [], [], [], []
-        self.groups = []
+        self.groups, self.face_floats = [], []
         for r in range(nslabs):
             local, sides, planes = slab_part(w, nslabs, r)
             sim = Simulation(local, device=devices[r % len(devices)])
@@ -277,12 +288,11 @@ class SlabDomain:
             self.sides.append(sides)
             self.plane_lists.append(planes)
             self.groups.append(plane_groups(len(planes), *sides))
-            self.buffers.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
-                                 for _ in range(2)])   # [low side, high side]
-        self.multi_device = len({s.device for s in self.slabs}) > 1
-        if exchange == "swap" and self.multi_device:
-            raise ValueError("the buffer-free swap needs every slab on one device")
-        self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
+            self.face_floats.append(nfloat)
+            # [low side, high side]; the swap needs none
+            self.buffers.append(None if self.swap else
+                                [torch.empty(nfloat, dtype=torch.float32, device=sim.device)
+                                 for _ in range(2)])
         self.overlap = bool(overlap)
         if self.overlap and self.multi_device:
             raise ValueError("overlap needs every slab on one device")
@@ -433,7 +443,7 @@ class SlabDomain:
     def halo_bytes_per_step(self) -> float:
         """Bytes the exchanges move between slabs per time step, averaged over a step pair
         (one FILL and one DRAIN per pair; two buffers per slab face, one each way)."""
-        per_face = sum(self.buffers[a][1].numel() * 4 for a, _ in self.pairs())
+        per_face = sum(self.face_floats[a] * 4 for a, _ in self.pairs())
         return 2 * per_face
 
     def close(self):
@@ -792,26 +802,28 @@ class BlockDomain:
         self.w, self.nb, self.dim = w, nb, w.dim
         self.periodic = [w.face_flow[2 * a] == "periodic" for a in range(3)]
         devices = list(devices) if devices else [torch.device("cuda")]
+        nblocks = nb[0] * nb[1] * nb[2]
+        self.multi_device = len({_device_index(d) for d in devices[:nblocks]}) > 1
+        if exchange == "swap" and self.multi_device:
+            raise ValueError("the buffer-free swap needs every block on one device")
+        self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
         self.blocks, self.sides, self.coords, self.buffers = [], [], [], []
-        for b in range(nb[0] * nb[1] * nb[2]):
+        self.face_floats = []     # per block and axis: floats of one face's buffer
+        for b in range(nblocks):
             local, sides, coords = block_part(w, nb, b)
             sim = Simulation(local, device=devices[b % len(devices)])
-            bufs = []
+            bufs, floats = [], []
             for a in range(3):
-                if a < w.dim and nb[a] > 1:
-                    nfloat = capi.lbm_halo_axis_bytes(sim.ctx, a) // 4
-                    bufs.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
-                                 for _ in range(2)])
-                else:
-                    bufs.append(None)
+                nfloat = capi.lbm_halo_axis_bytes(sim.ctx, a) // 4 if (
+                    a < w.dim and nb[a] > 1) else 0
+                floats.append(nfloat)
+                bufs.append([torch.empty(nfloat, dtype=torch.float32, device=sim.device)
+                             for _ in range(2)] if nfloat and not self.swap else None)
             self.blocks.append(sim)
             self.sides.append(sides)
             self.coords.append(coords)
             self.buffers.append(bufs)
-        self.multi_device = len({s.device for s in self.blocks}) > 1
-        if exchange == "swap" and self.multi_device:
-            raise ValueError("the buffer-free swap needs every block on one device")
-        self.swap = exchange == "swap" or (exchange == "auto" and not self.multi_device)
+            self.face_floats.append(floats)
         self.overlap = bool(overlap)
         if self.overlap and self.multi_device:
             raise ValueError("overlap needs every block on one device")
@@ -959,7 +971,7 @@ class BlockDomain:
 
     def halo_bytes_per_step(self) -> float:
         """Bytes the exchanges move between blocks per time step (both ways, every face)."""
-        return float(sum(2 * self.buffers[lo][a][1].numel() * 4
+        return float(sum(2 * self.face_floats[lo][a] * 4
                          for a in exchange_axes(self.dim, self.nb) for lo, _ in self.pairs(a)))
 
     def close(self):

@@ -454,6 +454,39 @@ def test_full_size_cavity3d_512_200_201():
         assert got[n]["parity"] == n % 2
 
 
+GOLDEN_P512 = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                           "periodic_512_window.npz")
+
+
+def test_full_size_periodic_512_200_201():
+    """The benchmark's own workload (D3Q19 MRT, periodic 512^3, seeded rho and u) at full
+    size after 200 and 201 steps, in the benchmark's launch configuration, against the fp64
+    oracle in an 8^3 block of cells (fields within 2e-5, populations within 2e-5).
+
+    The oracle's values come from tests/golden/periodic_512_window.npz, written by
+    tests/golden/make_periodic_512_window.py (oracle only), which runs the oracle on the
+    block plus the 201 cells around it that can reach it in 201 steps."""
+    gold = np.load(GOLDEN_P512)
+    x0, y0, z0 = (int(v) for v in gold["origin"])
+    w = W.random_periodic(n=512, seed=2)
+
+    def take(r):
+        sl = (slice(z0, z0 + 8), slice(y0, y0 + 8), slice(x0, x0 + 8))
+        return dict(rho=r["rho"][sl].cpu().numpy(),
+                    u=r["u"][(slice(None),) + sl].cpu().numpy(),
+                    f=r["f"][(slice(None),) + sl].cpu().numpy())
+
+    got = gpu_states(w, [200, 201], window_fn=take)
+    for n in (200, 201):
+        g_ = got[n]
+        assert np.abs(g_["rho"] - gold[f"rho_{n}"]).max() <= TOL_FIELDS, n
+        assert np.abs(g_["u"] - gold[f"u_{n}"]).max() <= TOL_FIELDS, n
+        assert np.abs(g_["f"] - gold[f"f_{n}"]).max() <= TOL_FIELDS, n
+        assert g_["parity"] == n % 2
+        # the state moved: the check is not against the initial fields
+        assert np.abs(gold[f"u_{n}"] - w.u0[:, z0:z0 + 8, y0:y0 + 8, x0:x0 + 8]).max() > 1e-4
+
+
 # --------------------------------------------------- full sizes: sampled windows ----
 
 def _windows(shape, size, steps, rng, extra=6):
