@@ -15,7 +15,7 @@ Stored for n in (200, 201):
   populations of the block, indexed [(component,) z, y, x],
 plus ``origin`` = the (x, y, z) of the block's first cell.
 
-Run:  python tests/golden/make_periodic_512_window.py   (about 30 minutes on 8 cores)
+Run:  python tests/golden/make_periodic_512_window.py   (about 40 minutes on 8 cores)
 """
 from __future__ import annotations
 

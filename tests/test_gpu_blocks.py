@@ -230,6 +230,15 @@ def test_step_box_equals_step():
                 sim.step_box(lo, hi)
         ref.close()
         sim.close()
+    # the box launches take neither the two-buffer layouts nor immersed-boundary capacity
+    wp = W.random_periodic(shape=(16, 8, 6), seed=99)
+    for kw in ({"streaming": "pull"}, {"edit": lambda cfg: setattr(cfg, "ib_max_samples", 4)}):
+        s_ = Simulation(wp, **kw)
+        s_.init_equilibrium(_dev(wp.rho0), _dev(wp.u0))
+        with pytest.raises(capi.LbmError) as e:
+            s_.step_box((0, 0, 0), (16, 8, 6))
+        assert e.value.status == capi.LBM_ERR_UNSUPPORTED
+        s_.close()
 
 
 def test_axis_halo_calls_are_checked():
