@@ -512,15 +512,15 @@ def run_slabs_secondary(name, nslabs, lbm_steps, reps, single_mlups=None, overla
     torch.cuda.synchronize()
     step_s = a.elapsed_time(b) / 1e3 / (reps * lbm_steps)
     halo = dom.halo_bytes_per_step()
-    launches = len(dom.pairs()) * (1 if dom.swap else 4)
+    launches = (len(dom.pairs()) + 31) // 32 if dom.swap else 4 * len(dom.pairs())
     dom.close()
     del dom
     torch.cuda.empty_cache()
     mlups = w.cells / step_s / 1e6
     out = {"workload": workload_label(name, w), "layout": "aa", "slabs": nslabs,
            "decomposition": "slabs along the outer axis, 1 ghost plane per inner face, "
-                            "FILL after even / DRAIN after odd steps, all on this GPU, each "
-                            "face moved by one buffer-free swap kernel",
+                            "FILL after even / DRAIN after odd steps, all on this GPU, every "
+                            "face moved by one buffer-free swap launch",
            "overlap": bool(overlap),
            "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
            "halo_launches_per_step": launches}
@@ -556,8 +556,8 @@ def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None, overlap=F
     out = {"workload": workload_label(name, w), "layout": "aa", "blocks": list(nb),
            "decomposition": "blocks, 1 ghost plane per inner face of each split axis, "
                             "exchanged axis by axis with the ghost rows of the other axes "
-                            "(edges and corners in two or three hops), all on this GPU, each "
-                            "face moved by one buffer-free swap kernel",
+                            "(edges and corners in two or three hops), all on this GPU, the "
+                            "faces of each axis moved by one buffer-free swap launch",
            "overlap": bool(overlap),
            "mlups": round(mlups, 1), "halo_bytes_per_step": int(halo),
            "halo_launches_per_step": launches}

@@ -353,6 +353,16 @@ lbm_status lbm_halo_axis_unpack(lbm_ctx *ctx, int axis, int side, int phase, con
  * the pack and unpack calls; the axis order rule for blocks holds as well. */
 lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase);
 
+/* n (1..32) face swaps of one axis in one launch: pair p swaps lo[p]'s high face with
+ * hi[p]'s low face, as lbm_halo_axis_swap would, with its checks on every pair.  Every
+ * context must be on one device, with the same lattices, at one step, and each face may
+ * appear once (no context twice among lo[], nor twice among hi[]; LBM_ERR_ARG otherwise).
+ * The swaps of one axis touch disjoint slots, so one launch equals the n calls in any
+ * order.  Runs on lo[0]'s stream; work on the other contexts issued on other streams must
+ * be ordered before the call by the caller.  lo and hi are host arrays of n pointers. */
+lbm_status lbm_halo_axis_swap_many(lbm_ctx *const *lo, lbm_ctx *const *hi, int n, int axis,
+                                   int phase);
+
 /* Enqueue later work on another stream (a cudaStream_t). */
 lbm_status lbm_set_stream(lbm_ctx *ctx, void *cuda_stream);
 

@@ -89,6 +89,8 @@ SIGNATURES = [
     ("lbm_halo_axis_pack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_halo_axis_unpack", ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP]),
     ("lbm_halo_axis_swap", ctypes.c_int, [_VP, _VP, ctypes.c_int, ctypes.c_int]),
+    ("lbm_halo_axis_swap_many", ctypes.c_int,
+     [ctypes.POINTER(_VP), ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     ("lbm_set_stream", ctypes.c_int, [_VP, _VP]),
     ("lbm_reduce_populations_static", ctypes.c_int,
      [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP,
@@ -275,6 +277,14 @@ def lbm_halo_axis_unpack(ctx, axis: int, side: int, phase: int, buf):
 
 def lbm_halo_axis_swap(lo, hi, axis: int, phase: int):
     _check(load().lbm_halo_axis_swap(lo, hi, int(axis), int(phase)), lo)
+
+
+def lbm_halo_axis_swap_many(lo, hi, axis: int, phase: int):
+    """Face swaps of pairs (lo[p], hi[p]) of one axis in one launch."""
+    n = len(lo)
+    a = (_VP * n)(*lo)
+    b = (_VP * n)(*hi)
+    _check(load().lbm_halo_axis_swap_many(a, b, n, int(axis), int(phase)), lo[0] if n else None)
 
 
 def lbm_set_stream(ctx, stream):

@@ -129,6 +129,46 @@ cudaError_t launch_halo_swap(int lattice, int thermal, const Params &lo, const P
 }
 
 namespace {
+
+// Several face swaps of one axis in one launch: grid row p moves pair p.  The pairs of one
+// axis touch disjoint slots (a block that is `hi` of one pair and `lo` of the next reads its
+// first owned planes on both sides but writes other planes, or other slots of them), so the
+// order of the swaps within an axis does not matter.
+template <class L, class TL, int AXIS>
+__global__ void halo_swap_many_kernel(const HaloPairs pairs, int phase)
+{
+    const int p = blockIdx.y;
+    if (p >= pairs.n) return;
+    Params lo{}, hi{};
+    pairs.lo[p].to_params(lo);
+    pairs.hi[p].to_params(hi);
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < halo_plane_cells<AXIS>(lo)) halo_swap_cell_axis<L, TL, AXIS>(lo, hi, phase, i);
+}
+
+}  // namespace
+
+cudaError_t launch_halo_swap_many(int lattice, int thermal, const HaloPairs &pairs, int axis,
+                                  int phase, cudaStream_t s)
+{
+    int most = 0;
+    for (int p = 0; p < pairs.n; ++p) {
+        const int n[3] = {pairs.lo[p].nx, pairs.lo[p].ny, pairs.lo[p].nz};
+        const int cells = n[axis == 0 ? 1 : 0] * n[axis == 2 ? 1 : 2];
+        most = cells > most ? cells : most;
+    }
+    const dim3 b(HALO_THREADS), g((most + HALO_THREADS - 1) / HALO_THREADS, pairs.n);
+    return by_lattice(lattice, thermal, [&](auto l, auto tl) {
+        using Lt = decltype(l);
+        using Tt = decltype(tl);
+        if (axis == 0) halo_swap_many_kernel<Lt, Tt, 0><<<g, b, 0, s>>>(pairs, phase);
+        else if (axis == 1) halo_swap_many_kernel<Lt, Tt, 1><<<g, b, 0, s>>>(pairs, phase);
+        else halo_swap_many_kernel<Lt, Tt, 2><<<g, b, 0, s>>>(pairs, phase);
+        return cudaGetLastError();
+    });
+}
+
+namespace {
 // Call fn with compile-time (MASKED, PAT).
 template <class Fn>
 void with_pattern(bool masked, int pat, Fn &&fn)

@@ -821,7 +821,10 @@ lbm_status lbm_halo_axis_unpack(lbm_ctx *c, int axis, int side, int phase, const
     return halo_call(c, axis, side, phase, 1, buf);
 }
 
-lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase)
+namespace {
+
+// The checks of one face swap (lbm_halo_axis_swap); errors are recorded on lo.
+lbm_status check_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase)
 {
     if (!lo || !hi) return fail(nullptr, LBM_ERR_ARG, "both contexts are required");
     if (!lo->L.halo || !hi->L.halo) return fail(lo, LBM_ERR_STATE, "no HALO face in a context");
@@ -847,10 +850,50 @@ lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase)
         return fail(lo, LBM_ERR_STATE, "FILL belongs before an odd step (parity 1)");
     if (phase == LBM_HALO_DRAIN && (lo->parity != 0 || lo->steps == 0))
         return fail(lo, LBM_ERR_STATE, "DRAIN belongs after an odd step (parity 0)");
+    return LBM_OK;
+}
+
+}  // namespace
+
+lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase)
+{
+    lbm_status st = check_swap(lo, hi, axis, phase);
+    if (st != LBM_OK) return st;
     DeviceGuard guard(lo->device);
     cudaError_t e = lbm::launch_halo_swap(lo->cfg.lattice, lo->cfg.thermal, lo->P, hi->P, axis,
                                           phase, lo->stream);
     if (e != cudaSuccess) return cuda_fail(lo, e, "halo swap kernel");
+    return LBM_OK;
+}
+
+lbm_status lbm_halo_axis_swap_many(lbm_ctx *const *lo, lbm_ctx *const *hi, int n, int axis,
+                                   int phase)
+{
+    if (!lo || !hi) return fail(nullptr, LBM_ERR_ARG, "lo and hi are required");
+    if (n < 1 || n > lbm::HALO_MAX_PAIRS)
+        return fail(nullptr, LBM_ERR_ARG,
+                    "n must lie in [1, " + std::to_string(lbm::HALO_MAX_PAIRS) + "]");
+    lbm::HaloPairs pairs{};
+    pairs.n = n;
+    for (int p = 0; p < n; ++p) {
+        lbm_status st = check_swap(lo[p], hi[p], axis, phase);
+        if (st != LBM_OK) return st;
+        if (lo[p]->device != lo[0]->device || lo[p]->cfg.lattice != lo[0]->cfg.lattice ||
+            lo[p]->cfg.thermal != lo[0]->cfg.thermal || lo[p]->parity != lo[0]->parity ||
+            lo[p]->steps != lo[0]->steps)
+            return fail(lo[p], LBM_ERR_ARG,
+                        "every pair must be on one device, with the same lattices, at one step");
+        // each face once: no context may be `lo` (or `hi`) of two pairs
+        for (int q = 0; q < p; ++q)
+            if (lo[q] == lo[p] || hi[q] == hi[p])
+                return fail(lo[p], LBM_ERR_ARG, "a face appears in two pairs");
+        pairs.lo[p].from_params(lo[p]->P);
+        pairs.hi[p].from_params(hi[p]->P);
+    }
+    DeviceGuard guard(lo[0]->device);
+    cudaError_t e = lbm::launch_halo_swap_many(lo[0]->cfg.lattice, lo[0]->cfg.thermal, pairs,
+                                               axis, phase, lo[0]->stream);
+    if (e != cudaSuccess) return cuda_fail(lo[0], e, "halo swap kernel (pairs)");
     return LBM_OK;
 }
 

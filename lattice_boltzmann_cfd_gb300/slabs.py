@@ -323,9 +323,12 @@ class SlabDomain:
 
     def _exchange(self, phase: int):
         pairs = self.pairs()
-        if self.swap:
-            for a, b in pairs:
-                capi.lbm_halo_axis_swap(self.slabs[a].ctx, self.slabs[b].ctx, self.axis, phase)
+        if self.swap:         # every face in one launch (32 per launch at most)
+            for k in range(0, len(pairs), 32):
+                chunk = pairs[k:k + 32]
+                capi.lbm_halo_axis_swap_many([self.slabs[a].ctx for a, _ in chunk],
+                                             [self.slabs[b].ctx for _, b in chunk],
+                                             self.axis, phase)
             return
         for a, b in pairs:
             capi.lbm_halo_pack(self.slabs[a].ctx, 1, phase, self.buffers[a][1])
@@ -856,9 +859,12 @@ class BlockDomain:
     def _exchange(self, phase: int):
         for a in exchange_axes(self.dim, self.nb):
             pairs = self.pairs(a)
-            if self.swap:
-                for lo, hi in pairs:
-                    capi.lbm_halo_axis_swap(self.blocks[lo].ctx, self.blocks[hi].ctx, a, phase)
+            if self.swap:     # every face of the axis in one launch (32 per launch at most)
+                for k in range(0, len(pairs), 32):
+                    chunk = pairs[k:k + 32]
+                    capi.lbm_halo_axis_swap_many([self.blocks[lo].ctx for lo, _ in chunk],
+                                                 [self.blocks[hi].ctx for _, hi in chunk],
+                                                 a, phase)
                 continue
             for lo, hi in pairs:
                 capi.lbm_halo_axis_pack(self.blocks[lo].ctx, a, 1, phase, self.buffers[lo][a][1])
@@ -966,8 +972,9 @@ class BlockDomain:
         return combine_diagnostics(self.w, [float(x) for x in np.sum(vs, axis=0)])
 
     def halo_launches_per_step(self) -> int:
-        faces = sum(len(self.pairs(a)) for a in exchange_axes(self.dim, self.nb))
-        return faces if self.swap else 4 * faces
+        if self.swap:
+            return sum((len(self.pairs(a)) + 31) // 32 for a in exchange_axes(self.dim, self.nb))
+        return 4 * sum(len(self.pairs(a)) for a in exchange_axes(self.dim, self.nb))
 
     def halo_bytes_per_step(self) -> float:
         """Bytes the exchanges move between blocks per time step (both ways, every face)."""

@@ -307,6 +307,60 @@ def test_swap_calls_are_checked():
         sim.close()
 
 
+def test_batched_swaps_equal_one_swap_per_face(monkeypatch):
+    """lbm_halo_axis_swap_many (every face of an axis in one launch) gives bit for bit the
+    state of one lbm_halo_axis_swap per face, in 3-D (faces on two and three axes, a
+    periodic ring of two blocks) and 2-D."""
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+
+    def one_by_one(lo, hi, axis, phase):
+        for a, b in zip(lo, hi):
+            capi.lbm_halo_axis_swap(a, b, axis, phase)
+
+    for w, nb in ((W.perturbed(W.cavity3d(shape=(40, 22, 18)), seed=101), (2, 2, 2)),
+                  (W.random_periodic(shape=(30, 20, 16), seed=102), (1, 2, 4)),
+                  (W.perturbed(W.cavity2d(shape=(70, 41, 1)), seed=103), (3, 2, 1))):
+        got = []
+        for batched in (True, False):
+            with monkeypatch.context() as m:
+                if not batched:
+                    m.setattr(capi, "lbm_halo_axis_swap_many", one_by_one)
+                dom = BlockDomain(w, nb)
+                dom.init_equilibrium()
+                dom.step(7)
+                f, g = dom.populations()
+                got.append((f.cpu().numpy(), None if g is None else g.cpu().numpy()))
+                dom.close()
+        assert np.array_equal(got[0][0], got[1][0]), w.name
+        if w.thermal:
+            assert np.array_equal(got[0][1], got[1][1]), w.name
+
+
+def test_batched_swap_calls_are_checked():
+    """lbm_halo_axis_swap_many: 1 to 32 pairs, each face once, the checks of a single swap
+    on every pair."""
+    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    w = W.random_periodic(shape=(16, 12, 10), seed=104)
+    dom = BlockDomain(w, (1, 2, 2))
+    dom.init_equilibrium()
+    dom.step(1)                                     # parity 1: FILL is due
+    ctx = [b.ctx for b in dom.blocks]
+    pairs = dom.pairs(2)
+    lo, hi = [ctx[a] for a, _ in pairs], [ctx[b] for _, b in pairs]
+    capi.lbm_halo_axis_swap_many(lo, hi, 2, capi.LBM_HALO_FILL)
+    for args in (([lo[0], lo[0]], [hi[0], hi[1]]),            # a face twice
+                 ([], []),                                     # no pair
+                 (lo * 17, hi * 17)):                          # 34 pairs
+        with pytest.raises(capi.LbmError):
+            capi.lbm_halo_axis_swap_many(args[0], args[1], 2, capi.LBM_HALO_FILL)
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_axis_swap_many(lo, hi, 2, capi.LBM_HALO_DRAIN)   # parity 1
+    with pytest.raises(capi.LbmError):
+        capi.lbm_halo_axis_swap_many(lo, hi, 0, capi.LBM_HALO_FILL)    # x is not split
+    torch.cuda.synchronize()
+    dom.close()
+
+
 # ------------------------------------------------------------- one block per rank ---
 
 STEPS = (7, 8)
