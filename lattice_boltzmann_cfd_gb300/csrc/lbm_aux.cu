@@ -3,6 +3,7 @@
 #include <type_traits>
 
 #include "lbm_internal.h"
+#include "lbm_halo.h"
 
 namespace lbm {
 namespace {

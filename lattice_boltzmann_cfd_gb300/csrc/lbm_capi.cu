@@ -12,6 +12,7 @@
 
 #include "../../include/lbm.h"
 #include "lbm_internal.h"
+#include "lbm_halo.h"
 #include "lbm_setup.h"
 
 using lbm_setup::Layout;
