@@ -590,15 +590,52 @@ LBM_HD bool step_cell_coords(const Params &P, int &x, int &y, int &z)
     }
 }
 
+// Whether cell (x, y, z) lies within two cells of the box of the immersed-boundary samples'
+// stencil cells (P.ib_box), along periodic wraps too.  The step on a cell farther away
+// touches no slot the immersed-boundary kernel reads and needs none of its forces.
+template <class L>
+LBM_HD bool near_ib_box(const Params &P, int x, int y, int z)
+{
+    const int c[3] = {x, y, z}, n[3] = {P.nx, P.ny, P.nz};
+    for (int a = 0; a < L::DIM; ++a) {
+        const int lo = -P.ib_box[a] - 2, hi = P.ib_box[3 + a] + 2;
+        if (hi < lo) return false;                  // no sample
+        if (hi - lo + 1 >= n[a]) continue;          // the whole axis
+        int d = c[a] - lo;                          // distance above lo, modulo n
+        if (d < 0) d += n[a];
+        else if (d >= n[a]) d -= n[a];
+        if (d > hi - lo) return false;
+    }
+    return true;
+}
+
+// The start of a step launch: the cell of the calling thread, and the wait for the kernel
+// before it (every load reads the previous step's stores).  With immersed-boundary samples
+// (IB and P.ib_n > 0) the kernel before is the immersed-boundary kernel, which releases
+// this launch only once the previous step has completed (it triggers its dependents after
+// its own wait): then only cells near the samples wait for its forces, and the others start
+// at once, beside it.
+template <class L, bool IB, bool BOX>
+LBM_HD bool step_start(const Params &P, int &x, int &y, int &z)
+{
+    if constexpr (!IB) {
+        wait_prerequisites();
+        return step_cell_coords<L, BOX>(P, x, y, z);
+    } else {
+        const bool in = step_cell_coords<L, BOX>(P, x, y, z);
+        if (P.ib_n == 0 || !in || near_ib_box<L>(P, x, y, z)) wait_prerequisites();
+        return in;
+    }
+}
+
 // One time step: one thread per cell, blocks along x (x fastest for coalescing).
 template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool IB,
           bool FACES = false, bool BOX = false>
 __global__ void __launch_bounds__(256) step_kernel(const Params P)
 {
     allow_dependents();
-    wait_prerequisites();   // every load reads the previous step's stores
     int x = 0, y = 0, z = 0;
-    if (!step_cell_coords<L, BOX>(P, x, y, z)) return;
+    if (!step_start<L, IB, BOX>(P, x, y, z)) return;
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
@@ -609,9 +646,8 @@ template <class L, class TL, int COLL, bool MASKED, bool ODD, bool NARROW, bool 
 __global__ void __launch_bounds__(256, 5) step_kernel_5(const Params P)
 {
     allow_dependents();
-    wait_prerequisites();   // every load reads the previous step's stores
     int x = 0, y = 0, z = 0;
-    if (!step_cell_coords<L, BOX>(P, x, y, z)) return;
+    if (!step_start<L, IB, BOX>(P, x, y, z)) return;
     aa_step_cell<L, TL, COLL, MASKED, ODD, NARROW, IB, FACES>(P, P, x, y, z);
 }
 
@@ -911,6 +947,9 @@ LBM_HD void ib_corner_thread(const Params &P, int t)
         m = P.mask[idx];
     }
     wait_prerequisites();   // the stencil cells hold the previous step's stores
+    // only now may the step after this kernel start: its cells away from the samples skip
+    // their wait, and must find the previous step complete
+    allow_dependents();
     if (active) ib_corner_moments<L, TL, PAT>(P, idx, q, K, m, kr, ku);
 #if defined(__CUDA_ARCH__)
 #pragma unroll
@@ -932,7 +971,6 @@ LBM_HD void ib_corner_thread(const Params &P, int t)
 template <class L, class TL, int PAT>
 __global__ void __launch_bounds__(128) ib_kernel(const Params P)
 {
-    allow_dependents();
     ib_corner_thread<L, TL, PAT>(P, blockIdx.x * blockDim.x + threadIdx.x);
 }
 
