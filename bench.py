@@ -534,7 +534,7 @@ def run_blocks_secondary(name, nb, lbm_steps, reps, single_mlups=None, overlap=F
     halo exchange after every step (z, then y, then x; a step = one step launch per block +
     one pack and one unpack launch per block face and direction)."""
     import torch
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     w = cached_workload(name)
     dom = BlockDomain(w, nb, overlap=overlap)
     dom.init_equilibrium()

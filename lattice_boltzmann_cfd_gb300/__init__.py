@@ -10,7 +10,8 @@ pattern in one fp32 structure-of-arrays buffer (two-buffer layouts for compariso
 * ``capi``      -- one Python function per C entry point (same names).
 * ``solver``    -- ``make_config`` and the ``Simulation`` handle.
 * ``slabs``     -- a domain split into slabs with the halo exchange (one process, or one
-  slab per torch.distributed rank).
+  slab per torch.distributed rank), whole-domain diagnostics and checkpoints.
+* ``blocks``    -- a domain cut into blocks along several axes, the same way.
 * ``pipeline``  -- independent jobs with host-link copies overlapped with the steps.
 * ``workloads`` -- seeded synthetic problems.
 """

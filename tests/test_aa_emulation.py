@@ -349,7 +349,7 @@ def _block_overlap_cases():
     on every lattice, with walls, solids next to the block faces and Dirichlet faces."""
     import dataclasses
     from lattice_boltzmann_cfd_gb300 import workloads as W
-    from lattice_boltzmann_cfd_gb300.slabs import block_part
+    from lattice_boltzmann_cfd_gb300.blocks import block_part
     rp = W.random_periodic(shape=(10, 10, 10), seed=91)
     c3 = W.perturbed(W.cavity3d(shape=(10, 10, 10)), seed=92)
     sol = np.zeros(c3.grid, np.uint8)
@@ -378,7 +378,7 @@ def test_block_exchange_overlaps_the_interior_without_races(emu_lib, case, next_
     interior cell reads or writes a slot a pack reads or an unpack writes.  Widening the box
     by one plane towards any HALO face produces such pairs."""
     import ctypes
-    from lattice_boltzmann_cfd_gb300.slabs import block_groups
+    from lattice_boltzmann_cfd_gb300.blocks import block_groups
     from lattice_boltzmann_cfd_gb300.solver import make_config
     name, local, sides = case
     cfg, keep = make_config(local, "aa")
@@ -401,7 +401,7 @@ def test_block_exchange_overlaps_the_interior_without_races(emu_lib, case, next_
 
 def test_block_groups_cover_each_cell_once():
     import itertools
-    from lattice_boltzmann_cfd_gb300.slabs import block_groups
+    from lattice_boltzmann_cfd_gb300.blocks import block_groups
     for dim in (2, 3):
         for ext in ((7, 6, 5), (4, 9, 6), (3, 3, 3), (8, 5, 1)):
             ext = ext if dim == 3 else (ext[0], ext[1], 1)

@@ -14,8 +14,8 @@ import pytest
 torch = pytest.importorskip("torch")
 
 from lattice_boltzmann_cfd_gb300 import workloads as W  # noqa: E402
-from lattice_boltzmann_cfd_gb300.slabs import (block_counts, block_index,  # noqa: E402
-                                               block_neighbours, block_part, owned_slices)
+from lattice_boltzmann_cfd_gb300.blocks import (block_counts, block_index,  # noqa: E402
+                                                block_neighbours, block_part, owned_slices)
 
 
 def _free_port():
@@ -33,7 +33,7 @@ def _stamp(rank, axis, side, phase):
 def _worker(rank, world, port, nb, periodic, dim, out):
     os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
     import torch.distributed as dist
-    from lattice_boltzmann_cfd_gb300.slabs import block_exchange
+    from lattice_boltzmann_cfd_gb300.blocks import block_exchange
     dist.init_process_group("gloo", rank=rank, world_size=world)
     got = []
     send = [[torch.zeros(5), torch.zeros(5)] for _ in range(3)]
@@ -148,7 +148,7 @@ def _dying_block(rank, world, port, out):
     import time
     os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
     import torch.distributed as dist
-    from lattice_boltzmann_cfd_gb300.slabs import block_exchange
+    from lattice_boltzmann_cfd_gb300.blocks import block_exchange
     dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=8))
     dist.barrier()

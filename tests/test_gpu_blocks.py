@@ -53,13 +53,13 @@ def _masked(w):
 
 def _same_family(w, nb):
     """Every block runs the kernel family of the undivided domain."""
-    from lattice_boltzmann_cfd_gb300.slabs import block_part
+    from lattice_boltzmann_cfd_gb300.blocks import block_part
     want = _masked(w)
     return all(_masked(block_part(w, nb, b)[0]) == want for b in range(nb[0] * nb[1] * nb[2]))
 
 
 def _blocks(w, nb, chunks, exchange="auto"):
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     dom = BlockDomain(w, nb, exchange=exchange)
     dom.init_equilibrium()
     for c in chunks:
@@ -140,7 +140,7 @@ def test_blocks_equal_single_domain(oracle_mod, w):
 def test_blocks_200_and_201_steps_against_the_oracle(oracle_mod, w, nb):
     """Blocks over 200 and 201 steps against the oracle on the undivided domain (2e-5 on the
     fields and populations, heat sums 1e-4 relative)."""
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     ref = oracle_states(oracle_mod, w, [200, 201])
     dom = BlockDomain(w, nb)
     dom.init_equilibrium()
@@ -166,7 +166,7 @@ def test_overlapped_blocks_equal_plain_order(w):
     """The overlapped block order (interior box, boundary boxes, the exchange of every axis on
     a second stream beside the next step's interior) gives the plain order's state bit for
     bit, through the swap and through buffers."""
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     for steps in (7, 8):
         for nb, exchange in [(nb, "swap") for nb in _layouts(w)] + [(_layouts(w)[0], "buffers")]:
             got = {}
@@ -311,7 +311,7 @@ def test_batched_swaps_equal_one_swap_per_face(monkeypatch):
     """lbm_halo_axis_swap_many (every face of an axis in one launch) gives bit for bit the
     state of one lbm_halo_axis_swap per face, in 3-D (faces on two and three axes, a
     periodic ring of two blocks) and 2-D."""
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
 
     def one_by_one(lo, hi, axis, phase):
         for a, b in zip(lo, hi):
@@ -339,7 +339,7 @@ def test_batched_swaps_equal_one_swap_per_face(monkeypatch):
 def test_batched_swap_calls_are_checked():
     """lbm_halo_axis_swap_many: 1 to 32 pairs, each face once, the checks of a single swap
     on every pair."""
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     w = W.random_periodic(shape=(16, 12, 10), seed=104)
     dom = BlockDomain(w, (1, 2, 2))
     dom.init_equilibrium()
@@ -385,7 +385,7 @@ def _free_port():
 def _rank(rank, world, port, name, overlap, out):
     os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
     import torch.distributed as dist
-    from lattice_boltzmann_cfd_gb300.slabs import DistBlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import DistBlockDomain
     dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=datetime.timedelta(seconds=120))
     w, nb = _case(name)
@@ -412,7 +412,7 @@ def test_four_ranks_share_the_gpu(oracle_mod, name, overlap):
     waiting is on the host, in the gloo messages.  The gathered owned cells equal the undivided domain bit for bit and match
     the fp64 oracle."""
     import torch.multiprocessing as mp
-    from lattice_boltzmann_cfd_gb300.slabs import block_part, owned_slices
+    from lattice_boltzmann_cfd_gb300.blocks import block_part, owned_slices
     w, nb = _case(name)
     world = nb[0] * nb[1] * nb[2]
     ctx = mp.get_context("spawn")
@@ -454,7 +454,8 @@ def test_checkpoint_resume_across_decompositions():
     another (slabs -> blocks, blocks -> slabs, blocks -> one domain and back): the remaining
     steps give the state of 201 straight steps within fp32 rounding (the read-out adds the
     rest weights back in fp32)."""
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain, SlabDomain
+    from lattice_boltzmann_cfd_gb300.slabs import SlabDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     from lattice_boltzmann_cfd_gb300.solver import Simulation
     w = W.perturbed(W.cavity3d(shape=(40, 20, 18)), seed=91)
     f_ref, g_ref, _ = _single(w, 201)

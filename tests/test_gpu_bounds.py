@@ -157,7 +157,7 @@ def test_immersed_boundary_stays_inside_the_cells(monkeypatch):
 def test_halo_exchanges_stay_inside_the_cells(monkeypatch, nb):
     """Packs, unpacks and swaps of every axis (slabs and blocks, FILL and DRAIN) write
     nothing outside the cells of either context."""
-    from lattice_boltzmann_cfd_gb300.slabs import BlockDomain
+    from lattice_boltzmann_cfd_gb300.blocks import BlockDomain
     from lattice_boltzmann_cfd_gb300.solver import Simulation
     w = W.perturbed(W.cavity3d(shape=(37, 29, 23)), seed=117)
     guards = {}
