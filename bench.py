@@ -650,35 +650,48 @@ def run_gpu(args, dctx):
     }
     if not args.no_secondary:
         _WORKLOAD_CACHE[args.workload] = w
+        line["secondary"] = []
+
+        def secondary(fn, *a):
+            """One secondary measurement; an error there is recorded in its entry instead of
+            ending the run (the headline line above does not depend on it)."""
+            try:
+                line["secondary"].append(fn(*a))
+            except Exception as e:   # noqa: BLE001 -- report any failure, keep the headline
+                line["secondary"].append({"run": f"{fn.__name__}{a[:2]}",
+                                          "error": f"{type(e).__name__}: {e}"[:300]})
+                import torch
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
+
         runs = [("cavity3d_512", "aa"), ("cavity2d_4096", "aa"), ("taylor_green_32", "aa"),
                 ("channel_ib_sphere_128", "aa"), ("d3q27_cm_periodic_512", "aa"),
                 ("channel_sphere_d3q27_128", "aa"), ("channel_ib_sphere_d3q27_128", "aa")]
         # the streaming-layout page's comparison: in place vs two buffers
         for n in ("d3q19_mrt_periodic_128", "channel_sphere_128", args.workload):
             runs += [(n, "aa"), (n, "pull"), (n, "split")]
-        line["secondary"] = []
         for n, mode in runs:
             if n == args.workload and mode == "aa":
                 continue
             # the 32^3 case fits in L2 and is launch-bound: long submissions replay graphs
             steps_n = 2048 if n == "taylor_green_32" else args.lbm_steps
-            line["secondary"].append(run_secondary(n, steps_n, 4, mode))
-        line["secondary"].append(run_moving_ib_secondary("channel_ib_sphere_128",
-                                                         args.lbm_steps, 4))
-        single = {r["workload"]: r["mlups"] for r in line["secondary"] if r["layout"] == "aa"}
+            secondary(run_secondary, n, steps_n, 4, mode)
+        secondary(run_moving_ib_secondary, "channel_ib_sphere_128", args.lbm_steps, 4)
+        single = {r["workload"]: r["mlups"] for r in line["secondary"]
+                  if r.get("layout") == "aa" and "mlups" in r}
         # the steps alone, as the secondaries time them (value adds the diagnostics)
         single[workload_label(args.workload, w)] = round(w.cells / (kernel_ms / 1e3) / 1e6, 1)
         for n in (args.workload, "cavity3d_512"):
             lbl = workload_label(n, cached_workload(n))
             for overlap in (False, True):
-                line["secondary"].append(run_slabs_secondary(n, 4, args.lbm_steps, 2,
-                                                             single.get(lbl), overlap))
+                secondary(run_slabs_secondary, n, 4, args.lbm_steps, 2, single.get(lbl),
+                          overlap)
             for nb, overlap in (((1, 2, 2), False), ((1, 2, 2), True), ((1, 2, 4), False)):
-                line["secondary"].append(run_blocks_secondary(n, nb, args.lbm_steps, 2,
-                                                              single.get(lbl), overlap))
+                secondary(run_blocks_secondary, n, nb, args.lbm_steps, 2, single.get(lbl),
+                          overlap)
         lbl = workload_label("cavity2d_4096", cached_workload("cavity2d_4096"))
-        line["secondary"].append(run_blocks_secondary("cavity2d_4096", (2, 2, 1),
-                                                      args.lbm_steps, 2, single.get(lbl)))
+        secondary(run_blocks_secondary, "cavity2d_4096", (2, 2, 1), args.lbm_steps, 2,
+                  single.get(lbl))
     line["cpu_baseline"] = cpu_baseline(args.workload)
     return line
 
