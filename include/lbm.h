@@ -359,7 +359,9 @@ lbm_status lbm_halo_axis_swap(lbm_ctx *lo, lbm_ctx *hi, int axis, int phase);
  * appear once (no context twice among lo[], nor twice among hi[]; LBM_ERR_ARG otherwise).
  * The swaps of one axis touch disjoint slots, so one launch equals the n calls in any
  * order.  Runs on lo[0]'s stream; work on the other contexts issued on other streams must
- * be ordered before the call by the caller.  lo and hi are host arrays of n pointers. */
+ * be ordered before the call by the caller.  lo and hi are host arrays of n pointers.
+ * The error text of a failed call is lo[0]'s (lbm_last_error(lo[0])), or the thread's for
+ * an n out of range. */
 lbm_status lbm_halo_axis_swap_many(lbm_ctx *const *lo, lbm_ctx *const *hi, int n, int axis,
                                    int phase);
 

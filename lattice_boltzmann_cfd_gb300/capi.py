@@ -284,7 +284,8 @@ def lbm_halo_axis_swap_many(lo, hi, axis: int, phase: int):
     n = len(lo)
     a = (_VP * n)(*lo)
     b = (_VP * n)(*hi)
-    _check(load().lbm_halo_axis_swap_many(a, b, n, int(axis), int(phase)), lo[0] if n else None)
+    _check(load().lbm_halo_axis_swap_many(a, b, n, int(axis), int(phase)),
+           lo[0] if 1 <= n <= 32 else None)
 
 
 def lbm_set_stream(ctx, stream):

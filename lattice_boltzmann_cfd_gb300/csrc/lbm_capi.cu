@@ -91,7 +91,8 @@ lbm_status fail(lbm_ctx *c, lbm_status s, const std::string &msg)
 lbm_status partly_stepped(lbm_ctx *c)
 {
     return fail(c, LBM_ERR_STATE,
-                "a step is partly done: lbm_step_planes must cover the remaining planes first");
+                "a step is partly done: lbm_step_box (or lbm_step_planes) must cover the "
+                "remaining cells first");
 }
 
 lbm_status cuda_fail(lbm_ctx *c, cudaError_t e, const char *where)
@@ -878,16 +879,19 @@ lbm_status lbm_halo_axis_swap_many(lbm_ctx *const *lo, lbm_ctx *const *hi, int n
     pairs.n = n;
     for (int p = 0; p < n; ++p) {
         lbm_status st = check_swap(lo[p], hi[p], axis, phase);
-        if (st != LBM_OK) return st;
+        if (st != LBM_OK) {
+            if (p > 0 && lo[p] && lo[0]) lo[0]->err = lo[p]->err;   // the call's error on lo[0]
+            return st;
+        }
         if (lo[p]->device != lo[0]->device || lo[p]->cfg.lattice != lo[0]->cfg.lattice ||
             lo[p]->cfg.thermal != lo[0]->cfg.thermal || lo[p]->parity != lo[0]->parity ||
             lo[p]->steps != lo[0]->steps)
-            return fail(lo[p], LBM_ERR_ARG,
+            return fail(lo[0], LBM_ERR_ARG,
                         "every pair must be on one device, with the same lattices, at one step");
         // each face once: no context may be `lo` (or `hi`) of two pairs
         for (int q = 0; q < p; ++q)
             if (lo[q] == lo[p] || hi[q] == hi[p])
-                return fail(lo[p], LBM_ERR_ARG, "a face appears in two pairs");
+                return fail(lo[0], LBM_ERR_ARG, "a face appears in two pairs");
         pairs.lo[p].from_params(lo[p]->P);
         pairs.hi[p].from_params(hi[p]->P);
     }

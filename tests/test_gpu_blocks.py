@@ -348,10 +348,10 @@ def test_batched_swap_calls_are_checked():
     pairs = dom.pairs(2)
     lo, hi = [ctx[a] for a, _ in pairs], [ctx[b] for _, b in pairs]
     capi.lbm_halo_axis_swap_many(lo, hi, 2, capi.LBM_HALO_FILL)
-    for args in (([lo[0], lo[0]], [hi[0], hi[1]]),            # a face twice
-                 ([], []),                                     # no pair
-                 (lo * 17, hi * 17)):                          # 34 pairs
-        with pytest.raises(capi.LbmError):
+    for args, text in ((([lo[0], lo[0]], [hi[0], hi[1]]), "two pairs"),   # a face twice
+                       (([], []), "n must lie"),                           # no pair
+                       ((lo * 17, hi * 17), "n must lie")):                # 34 pairs
+        with pytest.raises(capi.LbmError, match=text):
             capi.lbm_halo_axis_swap_many(args[0], args[1], 2, capi.LBM_HALO_FILL)
     with pytest.raises(capi.LbmError):
         capi.lbm_halo_axis_swap_many(lo, hi, 2, capi.LBM_HALO_DRAIN)   # parity 1
