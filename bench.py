@@ -292,7 +292,7 @@ def timed_e2e_leg(sim, w, steps, warmup, lbm_steps, dist_ctx):
 
 def timed_pipelined_e2e_leg(sim, w, steps, warmup, lbm_steps, dist_ctx):
     """The same jobs through JobPipeline: each job's host-to-device copy and read-out still
-    happen inside the timed region, overlapped with the neighbouring jobs' steps."""
+    happen inside the timed region; the next job's upload travels beside the steps."""
     import torch
     from lattice_boltzmann_cfd_gb300.pipeline import JobPipeline
     rho_h, u_h, T_h = upload(w, None, pinned=True)
@@ -640,11 +640,10 @@ def run_gpu(args, dctx):
                         "the page-locked host rho,u, lbm_step, lbm_macroscopic writes "
                         "page-locked host fields, lbm_diagnostics",
                 "pipelined_value": round(pipelined_value, 1),
-                "pipelined": "the same steps through JobPipeline: copies on two copy streams "
-                             "overlapping the neighbouring steps' LBM steps, each read-out "
-                             "issued behind the next step's kernels; 41-42k MLUPS in a "
-                             "fresh process, 35-42k between runs here, so value is the "
-                             "serial path"},
+                "pipelined": "the same steps through JobPipeline: the next step's upload "
+                             "in ~32 MB pieces on a copy stream beside the LBM steps, the "
+                             "read-out written to host by lbm_macroscopic; 31-39k MLUPS "
+                             "between runs, so value is the serial path"},
         "gpu_launches": args.steps * (args.lbm_steps + 2),
         "clocks": clocks,
     }

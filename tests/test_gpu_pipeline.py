@@ -1,5 +1,6 @@
 """JobPipeline (host-link copies overlapped with the neighbouring jobs' steps) against the
-same jobs run one after another: every job's outputs and diagnostics are bit-identical."""
+same jobs run one after another: every job's outputs and diagnostics are bit-identical,
+with the copies in one piece and cut into one piece per step."""
 import numpy as np
 import pytest
 
@@ -23,11 +24,13 @@ def _pinned(a):
                                   lambda s: W.random_periodic(shape=(64, 24, 20), seed=s),
                                   lambda s: W.perturbed(W.cavity2d(shape=(96, 80, 1)), seed=s)],
                          ids=["cavity3d", "periodic", "cavity2d"])
-def test_pipeline_matches_serial_jobs(make):
+@pytest.mark.parametrize("piece_bytes", [32 << 20, 4096], ids=["whole", "pieces"])
+@pytest.mark.parametrize("steps", [9, 1, 0])
+@pytest.mark.parametrize("overlap_readout", [False, True], ids=["readout_alone", "readout_overlap"])
+def test_pipeline_matches_serial_jobs(make, piece_bytes, steps, overlap_readout):
     from lattice_boltzmann_cfd_gb300 import Simulation
     from lattice_boltzmann_cfd_gb300.pipeline import JobPipeline
     ws = [make(seed) for seed in (3, 4, 5, 6, 7)]
-    steps = 9
     jobs = []
     for w in ws:
         ins = tuple(_pinned(a) for a in (w.rho0, w.u0, w.T_init if w.thermal else None))
@@ -46,7 +49,8 @@ def test_pipeline_matches_serial_jobs(make):
     sim.close()
     # pipelined
     sim = Simulation(ws[0])
-    diags = JobPipeline(sim).run(jobs, steps)
+    diags = JobPipeline(sim, piece_bytes=piece_bytes,
+                        overlap_readout=overlap_readout).run(jobs, steps)
     sim.close()
     for (fields, d), (_, outs), dp in zip(serial, jobs, diags):
         for a, b in zip(fields, [t for t in outs if t is not None]):
@@ -62,8 +66,9 @@ def test_pipeline_without_readout():
     w = W.random_periodic(shape=(32, 16, 16), seed=9)
     ins = (_pinned(w.rho0), _pinned(w.u0), None)
     sim = Simulation(w)
-    diags = JobPipeline(sim).run([(ins, None)] * 3, 4)
-    assert len(diags) == 3 and diags[0]["mass"] == diags[2]["mass"]
+    for piece_bytes in (32 << 20, 1000):
+        diags = JobPipeline(sim, piece_bytes=piece_bytes).run([(ins, None)] * 3, 4)
+        assert len(diags) == 3 and diags[0]["mass"] == diags[2]["mass"]
     sim.close()
 
 
@@ -77,3 +82,33 @@ def test_ib_block_search_returns_the_fastest_candidate():
     best, times = search_ib_block(w, candidates=[2, 4, 8], steps=8, warmup=2)
     assert set(times) == {2, 4, 8} and all(t > 0 for t in times.values())
     assert times[best] == min(times.values())
+
+
+def test_two_pipelines_on_one_simulation():
+    """A pipeline built later on the same simulation moves it to its own stream; each run()
+    takes the simulation back, so runs of either pipeline, in any order, stay correct."""
+    from lattice_boltzmann_cfd_gb300 import Simulation
+    from lattice_boltzmann_cfd_gb300.pipeline import JobPipeline
+    ws = [W.random_periodic(shape=(64, 24, 20), seed=s) for s in (11, 12)]
+    jobs = []
+    for w in ws:
+        ins = (_pinned(w.rho0), _pinned(w.u0), None)
+        jobs.append((ins, tuple(None if t is None else torch.empty_like(t).pin_memory()
+                                for t in ins)))
+    sim = Simulation(ws[0])
+    want = []
+    for (ins, _) in jobs:
+        sim.init_equilibrium(*[None if t is None else t.cuda() for t in ins])
+        sim.step(7)
+        rho, u, _ = sim.macroscopic()
+        torch.cuda.synchronize()
+        want.append((rho.cpu(), u.cpu()))
+    a = JobPipeline(sim, piece_bytes=4096)
+    b = JobPipeline(sim, overlap_readout=True)
+    for pipe in (a, b, a):
+        for t in (o for _, outs in jobs for o in outs if o is not None):
+            t.fill_(float("nan"))
+        pipe.run(jobs, 7)
+        for (rho, u), (_, outs) in zip(want, jobs):
+            assert torch.equal(rho, outs[0]) and torch.equal(u, outs[1])
+    sim.close()
