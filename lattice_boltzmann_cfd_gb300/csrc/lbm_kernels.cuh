@@ -466,15 +466,22 @@ LBM_HD void wait_prerequisites()
 #endif
 }
 
-// One time step: one thread per cell, blocks along x (x fastest for coalescing).
-// Read the immersed-boundary force of a cell and zero it for the next step.
+// Read the immersed-boundary force of a cell and zero it for the next step: one atomic
+// exchange per component on the device.  Measured on GB300 (128^3 channel, 12,868 samples),
+// a plain load followed by a store to the same address slowed every block on the GPU while
+// the planes holding stencil cells were stepped, about 7 us of a 66 us step; the exchange
+// costs about 0.3 us.  The host emulation runs one thread: there a load and a store do.
 LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
 {
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
         float *p = P.fib + ((size_t)a * P.S + (unsigned)idx);
+#if defined(__CUDA_ARCH__)
+        ext[a] = atomicExch(p, 0.0f);
+#else
         ext[a] = *p;
         *p = 0.0f;
+#endif
     }
 }
 
