@@ -30,6 +30,40 @@ every run.  The next job's upload still travels beside the steps.
 from __future__ import annotations
 
 
+def check_jobs(jobs, grid, dim: int, thermal: bool):
+    """Raise ValueError unless every job is ((rho, u, T), outputs) with rho and T of shape
+    ``grid``, u of shape (dim,) + grid, T present exactly when the lattice is thermal, and
+    outputs None or a triple of the same shapes (None entries skip that field)."""
+    grid = tuple(grid)
+    shapes = (grid, (dim,) + grid, grid)
+    names = ("rho", "u", "T")
+    for k, job in enumerate(jobs):
+        if not isinstance(job, (tuple, list)) or len(job) != 2:
+            raise ValueError(f"job {k}: expected (inputs, outputs)")
+        ins, outs = job
+        if not isinstance(ins, (tuple, list)) or len(ins) != 3:
+            raise ValueError(f"job {k}: inputs must be (rho, u, T or None)")
+        for i, (t, shape, name) in enumerate(zip(ins, shapes, names)):
+            needed = i < 2 or thermal
+            if t is None:
+                if needed:
+                    raise ValueError(f"job {k}: input {name} is required")
+                continue
+            if not needed:
+                raise ValueError(f"job {k}: input {name} given for a lattice without it")
+            if tuple(t.shape) != shape:
+                raise ValueError(f"job {k}: input {name} has shape {tuple(t.shape)}, "
+                                 f"expected {shape}")
+        if outs is None:
+            continue
+        if not isinstance(outs, (tuple, list)) or len(outs) != 3:
+            raise ValueError(f"job {k}: outputs must be None or (rho, u, T or None)")
+        for t, shape, name in zip(outs, shapes, names):
+            if t is not None and tuple(t.shape) != shape:
+                raise ValueError(f"job {k}: output {name} has shape {tuple(t.shape)}, "
+                                 f"expected {shape}")
+
+
 def _pieces(n: int, parts: int):
     """[lo, hi) ranges cutting range(n) into ``parts`` nearly equal pieces."""
     return [(n * i // parts, n * (i + 1) // parts) for i in range(parts)]
@@ -76,6 +110,7 @@ class JobPipeline:
         Returns each job's diagnostics (dict, as Simulation.diagnostics)."""
         import torch
         jobs = list(jobs)
+        check_jobs(jobs, self.sim.grid, self.sim.dim, bool(self.sim.QT))
         ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
         staged, staging_free, written, drained = ev(), ev(), ev(), ev()
         # another pipeline built on the same simulation since may have moved it

@@ -13,3 +13,41 @@ def test_pipeline_pieces_cover_every_element():
             assert all(p[i][1] == p[i + 1][0] for i in range(parts - 1))
             sizes = [b - a for a, b in p]
             assert max(sizes) - min(sizes) <= 1
+
+
+def test_check_jobs_accepts_the_workloads_fields():
+    """Inputs and outputs shaped as the workloads build them pass, thermal or not, 2-D or
+    3-D, with outputs None or with None entries."""
+    import numpy as np
+    from lattice_boltzmann_cfd_gb300 import workloads as W
+    from lattice_boltzmann_cfd_gb300.pipeline import check_jobs
+    for w in (W.cavity2d(shape=(96, 80, 1)), W.cavity3d(shape=(48, 20, 18)),
+              W.random_periodic(shape=(64, 24, 20), seed=3)):
+        grid, dim = w.rho0.shape, w.u0.shape[0]
+        ins = (w.rho0, w.u0, w.T_init if w.thermal else None)
+        outs = tuple(None if a is None else np.empty_like(a) for a in ins)
+        check_jobs([(ins, outs), (ins, None), (ins, (outs[0], None, None))], grid, dim,
+                   bool(w.thermal))
+
+
+def test_check_jobs_rejects_malformed_jobs():
+    """A missing or surplus temperature, a wrong shape or a malformed job raises before
+    anything is launched."""
+    import numpy as np
+    import pytest
+    from lattice_boltzmann_cfd_gb300.pipeline import check_jobs
+    grid = (4, 5, 6)
+    rho, u, T = np.zeros(grid), np.zeros((3,) + grid), np.zeros(grid)
+    bad = [
+        ([((rho, u, None), None)], True, "T is required"),
+        ([((rho, u, T), None)], False, "given for a lattice without it"),
+        ([((None, u, None), None)], False, "rho is required"),
+        ([((rho, np.zeros((2,) + grid), None), None)], False, "input u has shape"),
+        ([((rho, u, None), (np.zeros((4, 5, 7)), None, None))], False, "output rho has shape"),
+        ([((rho, u, None),)], False, "expected (inputs, outputs)"),
+        ([((rho, u), None)], False, "inputs must be"),
+        ([((rho, u, None), (rho, u))], False, "outputs must be"),
+    ]
+    for jobs, thermal, msg in bad:
+        with pytest.raises(ValueError, match=msg.replace("(", r"\(").replace(")", r"\)")):
+            check_jobs(jobs, grid, 3, thermal)
