@@ -56,6 +56,15 @@ KERNEL_FILES = ("lbm_lattice.cuh", "lbm_collide.cuh", "lbm_kernels.cuh", "lbm_st
                 "lbm_step_d2q9.cu", "lbm_internal.h")   # the last holds the launch shape
 
 
+def ncu_traffic(workload: str, cells: int, src: str):
+    """DRAM bytes per step launch for ``workload`` from NCU_TRAFFIC, or None when there is
+    no figure or it was taken on kernel sources other than ``src`` (their hash)."""
+    tr = NCU_TRAFFIC.get(workload)
+    if not tr or tr["src_hash"] != src:
+        return None
+    return round(tr["bytes_per_cell"] * cells)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lattice_boltzmann_cfd_gb300", "csrc")
@@ -605,7 +614,7 @@ def run_gpu(args, dctx):
         0.5 * (per_step[len(per_step) // 2 - 1] + per_step[len(per_step) // 2])
     src = kernel_source_hash()
     tr = NCU_TRAFFIC.get(args.workload)
-    traffic = (round(tr["bytes_per_cell"] * w.cells) if tr and tr["src_hash"] == src else None)
+    traffic = ncu_traffic(args.workload, w.cells, src)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dctx.world,
         "steps": args.steps, "warmup": args.warmup,
@@ -622,6 +631,8 @@ def run_gpu(args, dctx):
                    "parallelism": f"replicas x{dctx.world}" if dctx.world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel_src_hash": src,
+                     "traffic_src_hash": tr["src_hash"] if tr else None,
                      "kernel": "step_kernel (even/odd AA forms)",
                      "kernel_ms": round(kernel_ms, 4), "bytes_per_cell": bpc,
                      "kernel_ms_median": round(median_ms, 4),

@@ -1,4 +1,5 @@
-"""Host logic of JobPipeline that needs no GPU."""
+"""Host logic that needs no GPU: JobPipeline's job checks and pieces, and the bench's
+provenance rule for ncu traffic."""
 from lattice_boltzmann_cfd_gb300.pipeline import _pieces
 
 
@@ -51,3 +52,23 @@ def test_check_jobs_rejects_malformed_jobs():
     for jobs, thermal, msg in bad:
         with pytest.raises(ValueError, match=msg.replace("(", r"\(").replace(")", r"\)")):
             check_jobs(jobs, grid, 3, thermal)
+
+
+def test_bench_reports_ncu_traffic_only_for_the_sources_it_was_taken_on():
+    """The bench's roofline traffic comes from ncu counters tied to a hash of the kernel
+    sources: the stored figure (bytes per cell x cells) while the hash matches, None once
+    the sources differ or for a workload without a figure."""
+    import bench
+    w = "d3q19_mrt_periodic_512"
+    tr = bench.NCU_TRAFFIC[w]
+    cells = 512 ** 3
+    assert bench.ncu_traffic(w, cells, tr["src_hash"]) == round(tr["bytes_per_cell"] * cells)
+    assert bench.ncu_traffic(w, cells, "0" * 16) is None
+    assert bench.ncu_traffic("no_such_workload", cells, tr["src_hash"]) is None
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+    # every stored figure is positive and at most the algorithmic bytes (nothing re-read)
+    lattices = {"d3q19_mrt_periodic_512": (19, 0), "cavity3d_512": (19, 7)}
+    assert set(bench.NCU_TRAFFIC) == set(lattices)
+    for name, t in bench.NCU_TRAFFIC.items():
+        assert 0 < t["bytes_per_cell"] <= bench.BYTES_PER_CELL[lattices[name]]
