@@ -468,9 +468,12 @@ LBM_HD void wait_prerequisites()
 
 // Read the immersed-boundary force of a cell and zero it for the next step: one atomic
 // exchange per component on the device.  Measured on GB300 (128^3 channel, 12,868 samples),
-// a plain load followed by a store to the same address slowed every block on the GPU while
-// the planes holding stencil cells were stepped, about 7 us of a 66 us step; the exchange
-// costs about 0.3 us.  The host emulation runs one thread: there a load and a store do.
+// a plain load followed by a store of these values (accumulated by the immersed-boundary
+// kernel's atomic additions just before, a few lanes per warp) slowed every block on the
+// GPU while the planes holding stencil cells were stepped, about 7 us of a 66 us step; the
+// exchange costs about 0.3 us.  (The step's own loads and stores of the populations, at the
+// same addresses in every cell, show no such cost.)  The host emulation runs one thread:
+// there a load and a store do.
 LBM_HD void take_ib_force(const Params &P, int idx, float (&ext)[3])
 {
 #pragma unroll
