@@ -633,6 +633,9 @@ def run_gpu(args, dctx):
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel_src_hash": src,
                      "traffic_src_hash": tr["src_hash"] if tr else None,
+                     # the counters' figure, for sources other than these when traffic is null
+                     "traffic_last_measured": (round(tr["bytes_per_cell"] * w.cells)
+                                               if tr else None),
                      "kernel": "step_kernel (even/odd AA forms)",
                      "kernel_ms": round(kernel_ms, 4), "bytes_per_cell": bpc,
                      "kernel_ms_median": round(median_ms, 4),
